@@ -1,0 +1,514 @@
+#!/usr/bin/env python3
+"""Benchmark: one GLM-5.2-shaped MoE layer (Route -> Union -> int4 SwiGLU expert
+FFN -> combine -> Learn) on GB300, tokens/s and int4 expert-weight GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode] [--impl ours|reference]
+
+A step is one pass of the whole layer over one batch (T tokens) of synthetic
+input.  The default workload is the T = 1 decode layer (E = 256 routed + 1
+shared expert, k = 8, d = 6144, f = 2048, int4 group-32 weights with fp32
+scales).  Every step reads its weights from one of R device-resident copies of
+the layer, rotated, so the bytes of consecutive steps never share L2 (each
+copy is 6.06 GB; the L2 is 129 MB).  Steps are captured into CUDA graphs with
+CUDA events between the stages; the events of the last replay give the stage
+durations used for the roofline line.
+
+Multi-GPU: one process per GPU (torchrun); every rank runs the same layer on
+its own tokens with no collective in the data path (tokens are independent:
+weak scaling); the barrier and a MAX reduction of the elapsed time are the only
+communication.  Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (decode & prefill); int4 expert weight GB/s vs HBM peak"
+UNIT = "tokens/s"
+
+
+# ------------------------------------------------------------------ helpers --
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode", choices=["decode", "batched_decode"])
+    ap.add_argument("--replicas", type=int, default=4, help="device copies of the layer rotated across steps")
+    ap.add_argument("--graph-steps", type=int, default=100, help="steps captured per CUDA graph")
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU-baseline sample")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            j = json.load(fh)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running (read-only)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": float(max(power))}
+
+
+def gpu_uuid(torch, dev: int) -> str | None:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------- workloads --
+
+def layer_bytes(sh, n_uniq: int) -> dict:
+    """Algorithmic bytes of one layer step (each byte the definition must touch once)."""
+    import workloads
+    blk = workloads.expert_q_bytes(sh.d, sh.f) + 4 * workloads.expert_s_count(sh.d, sh.f, sh.G)
+    ffn = (n_uniq + 1) * blk
+    nib = (n_uniq + 1) * workloads.expert_q_bytes(sh.d, sh.f)
+    router = sh.E * sh.d * 4 + sh.E * 4
+    act = 2 * sh.T * sh.d * 4
+    return {"ffn": ffn, "nibbles": nib, "layer": ffn + router + act, "expert_block": blk}
+
+
+# ------------------------------------------------------------------ our arm --
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import int4_routed_expert_sigmoid_gb300 as moe
+    import workloads
+    from int4_routed_expert_sigmoid_gb300 import build as libbuild
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        try:
+            dist.init_process_group("nccl", device_id=dev)
+        except TypeError:
+            dist.init_process_group("nccl")
+    libbuild.build()
+    sh = workloads.WORKLOADS[args.workload]
+    T, E, k, d, f = sh.T, sh.E, sh.k, sh.d, sh.f
+    R = max(1, args.replicas)
+    S = max(1, min(args.graph_steps, args.steps))
+
+    # ---- inputs: one seeded layer, R device copies (weights, router, bias)
+    L = workloads.layer_inputs(sh, seed=0, threads=os.cpu_count() or 8)
+    qb, sc = workloads.expert_q_bytes(d, f), workloads.expert_s_count(d, f, sh.G)
+    q_all = torch.empty((R, E * qb + qb), dtype=torch.uint8, device=dev)     # routed experts + shared
+    s_all = torch.empty((R, E * sc + sc), dtype=torch.float32, device=dev)
+    q_all[0, :E * qb].copy_(torch.from_numpy(L.q_base.reshape(-1)))
+    q_all[0, E * qb:].copy_(torch.from_numpy(L.shared_q))
+    s_all[0, :E * sc].copy_(torch.from_numpy(L.s_base.reshape(-1)))
+    s_all[0, E * sc:].copy_(torch.from_numpy(L.shared_s))
+    wg0 = torch.from_numpy(L.wg).to(dev)
+    bias0 = None if L.bias is None else torch.from_numpy(L.bias).to(dev)
+    for r in range(1, R):
+        q_all[r].copy_(q_all[0])
+        s_all[r].copy_(s_all[0])
+    wgs = [wg0] + [wg0.clone() for _ in range(R - 1)]
+    biases = [bias0] + [None if bias0 is None else bias0.clone() for _ in range(R - 1)]
+    layers = [moe.LayerWeights(q_all[r, :E * qb], s_all[r, :E * sc], q_all[r, E * qb:], s_all[r, E * sc:],
+                               E=E, d=d, f=f, G=sh.G) for r in range(R)]
+    del L
+    # distinct tokens per captured step position, seeded per rank
+    xs = torch.from_numpy(workloads.activations(S * T, d, seed=1000 + rank)).to(dev).view(S, T, d)
+
+    # ---- step buffers (serial on one stream: one set suffices)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    un = dict(counts=torch.empty(E, dtype=torch.int32, device=dev),
+              offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+              perm=torch.empty(T * k, dtype=torch.int32, device=dev),
+              sorted_pair=torch.empty(T * k, dtype=torch.int32, device=dev),
+              uniq=torch.empty(E, dtype=torch.int32, device=dev),
+              n_uniq=torch.empty(1, dtype=torch.int32, device=dev))
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    hits = torch.zeros((R, E), dtype=torch.int64, device=dev)
+    y_pair = torch.empty((T * k, d), dtype=torch.float32, device=dev)
+    y_shared = torch.empty((T, d), dtype=torch.float32, device=dev)
+    outs = torch.empty((S, T, d), dtype=torch.float32, device=dev)
+    ws = moe.workspace(moe.ffn_workspace_bytes(T, k, d, f, moe.MOE_MODE_DECODE), dev)
+
+    def step(i, ev=None):
+        r = i % R
+        x = xs[i % S]
+        if ev:
+            ev[0].record()
+        moe.moe_route(x, wgs[r], biases[r], k, 1, 1.0, topk_idx=idx, topk_w=wts, logits=logits)
+        if ev:
+            ev[1].record()
+        moe.moe_union(idx, E, hits=hits[r], err=err, out=un)
+        if ev:
+            ev[2].record()
+        moe.moe_expert_ffn_int4(x, layers[r], un, k, moe.MOE_MODE_DECODE, y_pair=y_pair, y_shared=y_shared,
+                                ws=ws, err=err)
+        if ev:
+            ev[3].record()
+        moe.moe_combine(y_pair, y_shared, wts, un["perm"], out=outs[i % S])
+        if ev:
+            ev[4].record()
+
+    launches_per_step = 7   # logits, top-k, union, act fragments, gate/up, down, combine
+
+    # warm the code paths once outside capture, then capture
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(min(S, 2 * R)):
+            step(i)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+
+    def capture(n, with_events):
+        g = torch.cuda.CUDAGraph()
+        # external events become event-record nodes of the graph (timestamps of each replay)
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)] for _ in range(n)] \
+            if with_events else None
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            for i in range(n):
+                step(i, evs[i] if evs else None)
+        return g, evs
+
+    g_main, evs = capture(S, True)
+    tail = args.steps % S
+    g_tail = capture(tail, False)[0] if tail else None
+    n_main = args.steps // S
+
+    # ---- warm-up (untimed)
+    for _ in range(max(1, -(-args.warmup // S))):
+        g_main.replay()
+    torch.cuda.synchronize()
+    err.zero_()
+
+    sampler = ClockSampler(gpu_uuid(torch, local))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(n_main):
+        g_main.replay()
+    if g_tail is not None:
+        g_tail.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    dev_err = int(err.item())
+
+    # stage durations of the last replay of the main graph (S steps, inside the timed region)
+    st = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)] for i in range(S)])
+    stage_ms = st.mean(axis=0)
+    n_uniq = int(un["n_uniq"].item())
+
+    # ---- end to end through the public API with host buffers (not graph-captured)
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    x_host = torch.from_numpy(workloads.activations(e2e_steps * T, d, seed=5000 + rank)).view(e2e_steps, T, d)
+    x_host = x_host.pin_memory()
+    out_host = torch.empty((e2e_steps, T, d), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty((T, d), dtype=torch.float32, device=dev)
+    out_dev = torch.empty((T, d), dtype=torch.float32, device=dev)
+    lws = moe.workspace(moe.layer_workspace_bytes(T, k, E, d, f, moe.MOE_MODE_DECODE), dev)
+    for i in range(min(50, e2e_steps)):   # warm-up of the host path
+        r = i % R
+        moe.moe_layer_forward(x_dev, wgs[r], biases[r], layers[r], k, mode=moe.MOE_MODE_DECODE, out=out_dev,
+                              ws=lws, err=err)
+    torch.cuda.synchronize()
+    barrier(world)
+    w0 = time.perf_counter()
+    for i in range(e2e_steps):
+        r = i % R
+        x_dev.copy_(x_host[i], non_blocking=True)
+        moe.moe_layer_forward(x_dev, wgs[r], biases[r], layers[r], k, mode=moe.MOE_MODE_DECODE, out=out_dev,
+                              hits=hits[r], ws=lws, err=err)
+        out_host[i].copy_(out_dev, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - w0
+    barrier(world)
+    dev_err |= int(err.item())
+
+    elapsed_max, e2e_max = reduce_max(world, [elapsed_ms, e2e_s], dev)
+    peaks = load_peaks()
+    byts = layer_bytes(sh, n_uniq)
+    ffn_ms = float(stage_ms[2])
+    achieved = byts["ffn"] / (ffn_ms * 1e-3) / 1e9
+    value = T * args.steps * world / (elapsed_max * 1e-3)
+    ms_per_step = elapsed_max / args.steps
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: 1 MoE layer, E={E} routed + 1 shared, k={k}, d={d}, f={f}, "
+                               f"int4 group-{sh.G} fp32 scales, T={T} token(s) per step",
+                   "T": T, "E": E, "k": k, "d": d, "f": f, "G": sh.G, "weights": "int4",
+                   "l2": f"inputs larger than L2: {R} device copies of the layer "
+                         f"({R * E * byts['expert_block'] / 1e9:.1f} GB) rotated across steps",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "cuda_graph_steps": S},
+        "roofline": {"kernel": "expert FFN stage (act fragments + gate/up + down kernels)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(ROOT, "ffn"),
+                     "peak_source": peaks["source"], "bytes_per_launch": byts["ffn"], "ms_per_launch": round(ffn_ms, 5)},
+        "stages_ms": {"route": round(float(stage_ms[0]), 5), "union": round(float(stage_ms[1]), 5),
+                      "ffn": round(ffn_ms, 5), "combine": round(float(stage_ms[3]), 5)},
+        "layer_gbs": round(byts["layer"] / (ms_per_step * 1e-3) / 1e9, 1),
+        "nibble_gbs": round(byts["nibbles"] / (ms_per_step * 1e-3) / 1e9, 1),
+        "n_uniq": n_uniq,
+        "e2e": {"value": round(T * e2e_steps * world / e2e_max, 2), "unit": UNIT,
+                "h2d_bytes_per_step": T * d * 4, "d2h_bytes_per_step": T * d * 4, "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "device_error": dev_err,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sh, args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(world, vals, dev):
+    if world == 1:
+        return vals
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(vals, dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def ncu_traffic(root, key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernels."""
+    p = os.path.join(root, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as fh:
+            j = json.load(fh)
+        ent = j.get(key)
+        if not ent or ent.get("source_hash") != kernel_source_hash(root):
+            return None
+        return ent.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        return None
+
+
+def kernel_source_hash(root):
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(root, "int4_routed_expert_sigmoid_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        if n.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, n), "rb") as fh:
+                h.update(n.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+# -------------------------------------------------------------- CPU oracle --
+
+def _oracle_layer(sh, f_used, seed=0):
+    """The workload's layer for the oracle; f_used < f keeps the first f_used
+    intermediate rows of every expert (a bounded sample of the same work)."""
+    import oracle
+    import workloads
+    L = workloads.layer_inputs(sh, seed=seed, threads=os.cpu_count() or 8)
+    d, f, G = sh.d, sh.f, sh.G
+    if f_used != f:
+        def cut(q, s):
+            q = q.reshape(-1)
+            s = s.reshape(-1)
+            qg = q[: f * d // 2].reshape(f, d // 2)[:f_used]
+            qu = q[f * d // 2: f * d].reshape(f, d // 2)[:f_used]
+            qd = q[f * d:].reshape(d, f // 2)[:, : f_used // 2]
+            sg = s[: f * d // G].reshape(f, d // G)[:f_used]
+            su = s[f * d // G: 2 * f * d // G].reshape(f, d // G)[:f_used]
+            sd = s[2 * f * d // G:].reshape(d, f // G)[:, : f_used // G]
+            return (np.concatenate([qg.ravel(), qu.ravel(), qd.ravel()]),
+                    np.concatenate([sg.ravel(), su.ravel(), sd.ravel()]))
+        qs, ss = zip(*[cut(L.q_base[e], L.s_base[e]) for e in range(sh.E)])
+        q_base, s_base = np.stack(qs), np.stack(ss)
+        shq, shs = cut(L.shared_q, L.shared_s)
+    else:
+        q_base, s_base, shq, shs = L.q_base, L.s_base, L.shared_q, L.shared_s
+    return oracle, L, q_base, s_base, shq, shs
+
+
+def cpu_baseline(sh, seconds: float) -> dict:
+    """The oracle, as it stands, on a bounded sample: full layers for a few tokens."""
+    import workloads
+    oracle, L, q_base, s_base, shq, shs = _oracle_layer(sh, sh.f)
+    threads = oracle.threads()
+    x = workloads.activations(4 * threads, sh.d, seed=9000)
+    lay = oracle.Layer(x[:1], L.wg, L.bias, q_base, s_base, shq, shs, d=sh.d, f=sh.f, E=sh.E, k=sh.k, G=sh.G)
+    t = time.perf_counter()
+    lay.tokens(np.array([0], np.int32))
+    t1 = time.perf_counter() - t
+    n = int(min(4 * threads, max(threads, round(seconds * threads / max(t1, 1e-3)))))
+    lay = oracle.Layer(x[:n], L.wg, L.bias, q_base, s_base, shq, shs, d=sh.d, f=sh.f, E=sh.E, k=sh.k, G=sh.G)
+    t = time.perf_counter()
+    lay.tokens(np.arange(n, dtype=np.int32))
+    el = time.perf_counter() - t
+    return {"value": round(n / el, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} tokens of the {sh.name} layer (route + shared + {sh.k} routed int4 experts, full "
+                      f"d={sh.d}, f={sh.f}), fp64 C oracle, OpenMP over tokens, {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one token through the layer,
+    with the experts cut to their first f' intermediate rows so that the whole
+    run stays within about two minutes; the rate is scaled by f / f'."""
+    if rank != 0:
+        return
+    import workloads
+    sh = workloads.WORKLOADS[args.workload]
+    total = max(1, args.steps + args.warmup)
+    budget = 90.0
+    # measure one full token to size the sample
+    oracle, L, q_base, s_base, shq, shs = _oracle_layer(sh, sh.f)
+    x = workloads.activations(1, sh.d, seed=9100)
+    lay = oracle.Layer(x, L.wg, L.bias, q_base, s_base, shq, shs, d=sh.d, f=sh.f, E=sh.E, k=sh.k, G=sh.G)
+    t = time.perf_counter()
+    lay.tokens(np.array([0], np.int32))
+    t_full = time.perf_counter() - t
+    frac = min(1.0, budget / total / max(t_full, 1e-6))
+    f_used = max(sh.G, int(sh.f * frac) // sh.G * sh.G)
+    del L, q_base, s_base
+    oracle, L, q_base, s_base, shq, shs = _oracle_layer(sh, f_used)
+    xs = workloads.activations(total, sh.d, seed=9200)
+    laid = [None]
+
+    def one(i):
+        lay = oracle.Layer(xs[i:i + 1], L.wg, L.bias, q_base, s_base, shq, shs, d=sh.d, f=f_used, E=sh.E,
+                           k=sh.k, G=sh.G)
+        lay.tokens(np.array([0], np.int32))
+        laid[0] = lay
+
+    for i in range(args.warmup):
+        one(i)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        one(args.warmup + i)
+    el = time.perf_counter() - t
+    value = args.steps * sh.T * (f_used / sh.f) / el
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{sh.name}: 1 MoE layer, E={sh.E} routed + 1 shared, k={sh.k}, d={sh.d}, "
+                                   f"f={sh.f}, int4 group-{sh.G}, T={sh.T}"},
+            "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                             "sample": f"each step: one token through the layer with every expert cut to its first "
+                                       f"{f_used} of {sh.f} intermediate rows; rate scaled by {sh.f}/{f_used}"},
+            "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

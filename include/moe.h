@@ -1,0 +1,218 @@
+/*
+ * moe.h -- C ABI of libmoe: one MoE layer of the Colibri GLM-5.2 engine on one
+ * GB300 GPU (sm_103a): Route -> Union -> expert FFN (int4 SwiGLU, routed +
+ * shared) -> score-weighted combine -> Learn (hit counters).
+ *
+ * The five per-layer stages come from "Public Colibri Observation and Revision
+ * Ledger", section "Exact Architecture and Data-Flow Reconstruction" (Route,
+ * Union, Place, Overlap, Learn).  All experts are resident in device memory,
+ * so Place and Overlap have no work here; the remaining stages are the calls
+ * below.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers are CUDA device pointers owned by the caller, unless a comment
+ *    says "host".  Arrays are dense, row-major, with no padding; every pointer
+ *    must be 16-byte aligned.  The library allocates no memory: scratch comes
+ *    from a caller workspace whose size the *_workspace_bytes queries return.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Every call only enqueues work on that stream and returns; nothing is
+ *    synchronised and nothing is read back to the host.  The calls keep no
+ *    global state and are safe to issue from several host threads.
+ *  - Return value: MOE_OK, or a negative MOE_ERR_* code when an argument is
+ *    invalid or unsupported (nothing is enqueued then) or a launch failed.
+ *    The library never exits, traps or prints.
+ *  - Errors found by the kernels themselves (an expert id out of range, a
+ *    pipeline wait that ran out of time) are OR-ed into a caller-owned device
+ *    word `err` (int32, the caller zeroes it); the offending item is skipped.
+ *    Copy it to the host after the stream has finished and decode it with
+ *    moe_device_error().
+ *
+ * Data formats
+ *  - int4 weights: symmetric two's complement in [-8, 7], no zero point; in a
+ *    row of `cols` elements, element 2i is the low nibble of byte i and element
+ *    2i+1 its high nibble; a matrix is [rows][cols/2] bytes.
+ *  - scales: fp32, one per G = 32 consecutive elements of a row along the
+ *    input (reduction) axis: [rows][cols/G].  deq(W)[r][i] = q[r][i] * s[r][i/G].
+ *  - expert block: gate [f][d], up [f][d], down [d][f]: first the packed bytes
+ *    of the three matrices in that order (moe_expert_q_bytes bytes), then their
+ *    scales in the same order (moe_expert_s_count floats).  Expert e of a layer
+ *    starts at q_base + e * moe_expert_q_bytes(d, f) and
+ *    s_base + e * moe_expert_s_count(d, f, G).  ("each activated expert is a
+ *    three-matrix MLP (size ~19 MB at int4) stored contiguously": same page and
+ *    section as above.)
+ *  - FFN_e(x) = down_e( silu(gate_e x) * (up_e x) ), silu(g) = g * sigmoid(g).
+ *
+ * Supported shapes: G = 32; d a multiple of 256; f a multiple of 128;
+ * 1 <= k <= min(E, 32); 1 <= E <= 1024; 1 <= T.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status ---- */
+enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,   /* NULL pointer, misaligned pointer, size out of range */
+    MOE_ERR_UNSUPPORTED = -2,   /* a shape or mode this build does not implement */
+    MOE_ERR_WORKSPACE = -3,     /* workspace smaller than the matching *_workspace_bytes */
+    MOE_ERR_CUDA = -4           /* a CUDA runtime call or kernel launch failed */
+};
+
+/* Bits of the device error word `err`. */
+#define MOE_DEVERR_BAD_EXPERT 0x1   /* an expert id in topk_idx was outside [0, E) */
+#define MOE_DEVERR_TIMEOUT 0x2      /* a bounded pipeline wait gave up; outputs are incomplete */
+
+/* FFN execution modes. */
+enum {
+    MOE_MODE_AUTO = 0,     /* decode path when T < 1024, else prefill */
+    MOE_MODE_DECODE = 1,   /* fp32-accurate path (exact int4 x split-bf16 activations) */
+    MOE_MODE_PREFILL = 2   /* bf16 tensor-core grouped GEMM (tcgen05), fp32 accumulate */
+};
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char *moe_status_str(int status);
+
+/* Decode a device error word copied to the host: MOE_OK when zero, else
+ * MOE_ERR_INVALID_ARG for a bad expert id or MOE_ERR_CUDA for a timeout. */
+MOE_API int moe_device_error(int32_t err_word_host);
+
+/* Packed bytes / fp32 scale count of one expert block (layout above). */
+MOE_API size_t moe_expert_q_bytes(int d, int f);
+MOE_API size_t moe_expert_s_count(int d, int f, int G);
+
+/* One MoE layer's int4 experts (device pointers).  The shared expert has the
+ * same block layout as a routed one. */
+typedef struct {
+    const uint8_t *q_base;    /* [E][moe_expert_q_bytes(d, f)] */
+    const float *s_base;      /* [E][moe_expert_s_count(d, f, G)] */
+    const uint8_t *shared_q;  /* [moe_expert_q_bytes(d, f)] */
+    const float *shared_s;    /* [moe_expert_s_count(d, f, G)] */
+    int E, d, f, G;
+} moe_layer_int4;
+
+/*
+ * Route: sigmoid gate and top-k selection.
+ * Source: "Public Colibri Observation and Revision Ledger", "Exact Architecture
+ * and Data-Flow Reconstruction": the trained sigmoid router (n_group = 1)
+ * scores all experts of the layer with fp32 gate parameters; colibri README,
+ * "The idea": ~11 GB of routed experts per token, i.e. k = 8 for GLM-5.2.
+ *
+ *   l[t][e]  = sum_i x[t][i] * w_gate[e][i]               (fp32)
+ *   s[t][e]  = 1 / (1 + exp(-l[t][e]))
+ *   key      = s[t][e] + bias[e]       (bias selects only; NULL means 0)
+ *   topk_idx[t][j], j < k: experts by key descending, equal keys -> lower id
+ *   topk_w[t][j] = s of that expert            if normalize == 0
+ *                = route_scale * s / sum_j s   if normalize != 0
+ *
+ * x [T][d] fp32; w_gate [E][d] fp32; bias [E] fp32 or NULL.
+ * Outputs: topk_idx [T][k] int32, topk_w [T][k] fp32, logits [T][E] fp32
+ * (the raw l, written as a by-product; caller-owned).
+ * Errors: MOE_ERR_INVALID_ARG for NULL/misaligned pointers or T < 1, d < 1,
+ * E > 1024, k < 1, k > min(E, 32).
+ */
+MOE_API int moe_route(const float *x, const float *w_gate, const float *bias, int T, int d,
+              int E, int k, int normalize, float route_scale, int32_t *topk_idx,
+              float *topk_w, float *logits, void *stream);
+
+/*
+ * Union: merge the routed (token, slot) pairs of the batch so each unique
+ * expert is read once, and group the pairs by expert.
+ * Source: same page and section ("Union -- merge requests across the batch");
+ * same page, "Cache/Prefetch Design Comparison" figure caption ("each unique
+ * expert is read only once" under batch-union).
+ *
+ * Pair p = t*k + j.  Outputs (all int32, caller-owned):
+ *   counts [E]        number of pairs routed to each expert
+ *   offsets [E+1]     exclusive scan of counts over ascending expert id
+ *   sorted_pair [T*k] pairs ordered by (expert, p): expert e's pairs occupy
+ *                     positions offsets[e] .. offsets[e+1]-1, tokens ascending
+ *   perm [T*k]        perm[p] = position of pair p in sorted_pair
+ *   uniq [E]          experts with counts > 0, ascending; entries >= n_uniq unspecified
+ *   n_uniq [1]        number of such experts
+ * hits [E] uint64 or NULL: when given, hits[e] += counts[e] (the Learn stage,
+ * fused; see moe_hits).  A pair whose id is outside [0, E) sets
+ * MOE_DEVERR_BAD_EXPERT in *err, gets perm[p] = -1 and is left out.
+ * Runs in one thread block; T*k <= 1<<22.
+ */
+MOE_API int moe_union(const int32_t *topk_idx, int T, int k, int E, int32_t *counts,
+              int32_t *offsets, int32_t *perm, int32_t *sorted_pair, int32_t *uniq,
+              int32_t *n_uniq, uint64_t *hits, int32_t *err, void *stream);
+
+/*
+ * Learn: per-expert hit counters, hits[e] += counts[e] (uint64, cumulative
+ * across calls; one count per routed (token, slot) pair).
+ * Source: "Public Colibri Observation and Revision Ledger", "Exact
+ * Architecture and Data-Flow Reconstruction" ("after each token the engine
+ * updates per-expert hit counters (the Learn step)").
+ */
+MOE_API int moe_hits(const int32_t *counts, int E, uint64_t *hits, void *stream);
+
+/*
+ * Expert FFN over the batch union: each expert in uniq (and the shared expert)
+ * is streamed once and applied to all of its grouped tokens.
+ * Source: same section ("Each activated expert is a three-matrix MLP ...
+ * stored contiguously"; "a small shared expert branch ... is always used");
+ * the SwiGLU form is a reading (see the design notes).
+ *
+ * x [T][d] fp32; w: the layer's experts; offsets/sorted_pair/uniq/n_uniq from
+ * moe_union (device).  Outputs:
+ *   y_pair [T*k][d] fp32: row q = FFN_e(x_t) for the pair sorted_pair[q]
+ *                         (t = sorted_pair[q] / k, e its expert)
+ *   y_shared [T][d] fp32: FFN_shared(x_t)
+ * mode: MOE_MODE_*.  workspace: at least moe_ffn_workspace_bytes(T, k, d, f,
+ * mode) bytes of device memory, 256-byte aligned; its contents on entry do not
+ * matter.  Calls that share a workspace must not overlap in time.
+ */
+MOE_API int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *offsets,
+                        const int32_t *sorted_pair, const int32_t *uniq,
+                        const int32_t *n_uniq, int T, int k, int mode, float *y_pair,
+                        float *y_shared, void *workspace, size_t ws_bytes, int32_t *err,
+                        void *stream);
+
+MOE_API size_t moe_ffn_workspace_bytes(int T, int k, int d, int f, int mode);
+
+/*
+ * Score-weighted combine (+ residual):
+ *   out[t][c] = residual[t][c] + y_shared[t][c] + sum_{j<k} topk_w[t][j] * y_pair[perm[t*k+j]][c]
+ * summed left to right in slot order j.  residual may be NULL (taken as 0) and
+ * may alias out.  A pair with perm < 0 is skipped.
+ * Source: the weighted sum of the selected experts' outputs with the router's
+ * scores and the always-on shared branch ("Public Colibri Observation and
+ * Revision Ledger", "Exact Architecture and Data-Flow Reconstruction").
+ */
+MOE_API int moe_combine(const float *y_pair, const float *y_shared, const float *topk_w,
+                const int32_t *perm, const float *residual, int T, int k, int d,
+                float *out, void *stream);
+
+/*
+ * The whole layer in one call: route -> union (+ hits) -> FFN -> combine, all
+ * enqueued on `stream` with no host synchronisation.  Scratch (logits, union
+ * arrays, activation fragments, y_pair, y_shared) is carved from `workspace`
+ * (at least moe_layer_workspace_bytes(T, k, E, d, f, mode) bytes).
+ * topk_idx [T][k] and topk_w [T][k] may be NULL (then kept in the workspace);
+ * hits may be NULL (no Learn update).  residual may be NULL or alias out.
+ */
+MOE_API int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
+                      const moe_layer_int4 *w, const float *residual, int T, int k,
+                      int normalize, float route_scale, int mode, float *out,
+                      int32_t *topk_idx, float *topk_w, uint64_t *hits, void *workspace,
+                      size_t ws_bytes, int32_t *err, void *stream);
+
+MOE_API size_t moe_layer_workspace_bytes(int T, int k, int E, int d, int f, int mode);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

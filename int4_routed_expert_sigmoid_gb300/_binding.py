@@ -1,0 +1,247 @@
+"""ctypes binding of libmoe (include/moe.h): argument marshalling only.
+
+Every function here takes torch CUDA tensors, checks dtypes/shapes enough to
+build the C call, and calls the entry point of the same name.  All arithmetic
+runs in the CUDA kernels behind the C ABI.  There is no CPU fallback: if the
+library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libmoe.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = 0, -1, -2, -3, -4
+MOE_DEVERR_BAD_EXPERT, MOE_DEVERR_TIMEOUT = 0x1, 0x2
+MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL = 0, 1, 2
+
+_HITS_DTYPES = tuple(getattr(torch, n) for n in ("int64", "uint64") if hasattr(torch, n))
+_lock = threading.Lock()
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)} ({status})")
+
+
+class moe_layer_int4(ctypes.Structure):
+    _fields_ = [("q_base", ctypes.c_void_p), ("s_base", ctypes.c_void_p),
+                ("shared_q", ctypes.c_void_p), ("shared_s", ctypes.c_void_p),
+                ("E", ctypes.c_int), ("d", ctypes.c_int), ("f", ctypes.c_int), ("G", ctypes.c_int)]
+
+
+_P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_SIGNATURES = {
+    "moe_status_str": ([_I], ctypes.c_char_p),
+    "moe_device_error": ([ctypes.c_int32], _I),
+    "moe_expert_q_bytes": ([_I, _I], _SZ),
+    "moe_expert_s_count": ([_I, _I, _I], _SZ),
+    "moe_route": ([_P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P], _I),
+    "moe_union": ([_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_hits": ([_P, _I, _P, _P], _I),
+    "moe_expert_ffn_int4": ([_P, ctypes.POINTER(moe_layer_int4), _P, _P, _P, _P, _I, _I, _I, _P, _P,
+                             _P, _SZ, _P, _P], _I),
+    "moe_ffn_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
+    "moe_combine": ([_P, _P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "moe_layer_forward": ([_P, _P, _P, ctypes.POINTER(moe_layer_int4), _P, _I, _I, _I, _F, _I, _P, _P,
+                           _P, _P, _P, _SZ, _P, _P], _I),
+    "moe_layer_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe.so (built by ``int4_routed_expert_sigmoid_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libmoe.so is not built ({LIB_PATH}); run "
+                    "`python -m int4_routed_expert_sigmoid_gb300.build` -- there is no fallback path")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+        return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().moe_status_str(int(status)).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != MOE_OK:
+        raise MoeError(rc, what)
+
+
+def _p(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t: torch.Tensor, dtype, what: str) -> torch.Tensor:
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError(f"{what} must be a contiguous CUDA tensor of {dtype}")
+    return t
+
+
+def expert_q_bytes(d: int, f: int) -> int:
+    return int(lib().moe_expert_q_bytes(d, f))
+
+
+def expert_s_count(d: int, f: int, G: int = 32) -> int:
+    return int(lib().moe_expert_s_count(d, f, G))
+
+
+def device_error(err_word: int) -> int:
+    return int(lib().moe_device_error(int(err_word)))
+
+
+class LayerWeights:
+    """Device-resident int4 experts of one layer plus the moe_layer_int4 view."""
+
+    def __init__(self, q_base: torch.Tensor, s_base: torch.Tensor, shared_q: torch.Tensor,
+                 shared_s: torch.Tensor, E: int, d: int, f: int, G: int = 32):
+        self.q_base = _need(q_base, torch.uint8, "q_base")
+        self.s_base = _need(s_base, torch.float32, "s_base")
+        self.shared_q = _need(shared_q, torch.uint8, "shared_q")
+        self.shared_s = _need(shared_s, torch.float32, "shared_s")
+        if self.q_base.numel() < E * expert_q_bytes(d, f) or self.s_base.numel() < E * expert_s_count(d, f, G):
+            raise ValueError("expert arrays smaller than E expert blocks")
+        self.E, self.d, self.f, self.G = E, d, f, G
+        self.c = moe_layer_int4(q_base.data_ptr(), s_base.data_ptr(), shared_q.data_ptr(),
+                                shared_s.data_ptr(), E, d, f, G)
+
+
+def moe_route(x, w_gate, bias, k: int, normalize: int = 1, route_scale: float = 1.0,
+              topk_idx=None, topk_w=None, logits=None, stream=None):
+    _need(x, torch.float32, "x")
+    _need(w_gate, torch.float32, "w_gate")
+    T, d = x.shape
+    E = w_gate.shape[0]
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    dev = x.device
+    topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
+    topk_w = torch.empty((T, k), dtype=torch.float32, device=dev) if topk_w is None else topk_w
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev) if logits is None else logits
+    _check(lib().moe_route(_p(x), _p(w_gate), _p(bias), T, d, E, k, int(normalize), float(route_scale),
+                           _p(topk_idx), _p(topk_w), _p(logits), _stream(stream)), "moe_route")
+    return topk_idx, topk_w, logits
+
+
+def moe_union(topk_idx, E: int, hits=None, err=None, out=None, stream=None):
+    """Returns dict(counts, offsets, perm, sorted_pair, uniq, n_uniq, err) of device tensors."""
+    _need(topk_idx, torch.int32, "topk_idx")
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    if out is None:
+        out = dict(counts=torch.empty(E, dtype=torch.int32, device=dev),
+                   offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   perm=torch.empty(T * k, dtype=torch.int32, device=dev),
+                   sorted_pair=torch.empty(T * k, dtype=torch.int32, device=dev),
+                   uniq=torch.empty(E, dtype=torch.int32, device=dev),
+                   n_uniq=torch.empty(1, dtype=torch.int32, device=dev))
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out["err"] = err
+    if hits is not None and not (hits.is_cuda and hits.dtype in _HITS_DTYPES and hits.numel() >= E):
+        raise ValueError("hits must be a CUDA int64/uint64 tensor of E counters")
+    _check(lib().moe_union(_p(topk_idx), T, k, E, _p(out["counts"]), _p(out["offsets"]), _p(out["perm"]),
+                           _p(out["sorted_pair"]), _p(out["uniq"]), _p(out["n_uniq"]), _p(hits), _p(err),
+                           _stream(stream)), "moe_union")
+    return out
+
+
+def moe_hits(counts, hits, stream=None):
+    _need(counts, torch.int32, "counts")
+    if not (hits.is_cuda and hits.dtype in _HITS_DTYPES and hits.numel() >= counts.numel()):
+        raise ValueError("hits must be a CUDA int64/uint64 tensor of E counters")
+    _check(lib().moe_hits(_p(counts), counts.numel(), _p(hits), _stream(stream)), "moe_hits")
+
+
+def ffn_workspace_bytes(T: int, k: int, d: int, f: int, mode: int = MOE_MODE_AUTO) -> int:
+    return int(lib().moe_ffn_workspace_bytes(T, k, d, f, mode))
+
+
+def layer_workspace_bytes(T: int, k: int, E: int, d: int, f: int, mode: int = MOE_MODE_AUTO) -> int:
+    return int(lib().moe_layer_workspace_bytes(T, k, E, d, f, mode))
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A 256-byte aligned device scratch buffer of at least nbytes."""
+    return torch.empty(max(int(nbytes), 1) + 256, dtype=torch.uint8, device=device)
+
+
+def _ws_ptr(ws: torch.Tensor) -> tuple[ctypes.c_void_p, int]:
+    base = ws.data_ptr()
+    aligned = (base + 255) & ~255
+    return ctypes.c_void_p(aligned), ws.numel() - (aligned - base)
+
+
+def moe_expert_ffn_int4(x, layer: LayerWeights, un: dict, k: int, mode: int = MOE_MODE_AUTO,
+                        y_pair=None, y_shared=None, ws=None, err=None, stream=None):
+    _need(x, torch.float32, "x")
+    T, d = x.shape
+    dev = x.device
+    y_pair = torch.empty((T * k, d), dtype=torch.float32, device=dev) if y_pair is None else y_pair
+    y_shared = torch.empty((T, d), dtype=torch.float32, device=dev) if y_shared is None else y_shared
+    if ws is None:
+        ws = workspace(ffn_workspace_bytes(T, k, d, layer.f, mode), dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    wp, wn = _ws_ptr(ws)
+    _check(lib().moe_expert_ffn_int4(_p(x), ctypes.byref(layer.c), _p(un["offsets"]), _p(un["sorted_pair"]),
+                                     _p(un["uniq"]), _p(un["n_uniq"]), T, k, mode, _p(y_pair), _p(y_shared),
+                                     wp, wn, _p(err), _stream(stream)), "moe_expert_ffn_int4")
+    return y_pair, y_shared, err
+
+
+def moe_combine(y_pair, y_shared, topk_w, perm, residual=None, out=None, stream=None):
+    T, k = topk_w.shape
+    d = y_shared.shape[1]
+    out = torch.empty((T, d), dtype=torch.float32, device=y_shared.device) if out is None else out
+    _check(lib().moe_combine(_p(y_pair), _p(y_shared), _p(topk_w), _p(perm), _p(residual), T, k, d, _p(out),
+                             _stream(stream)), "moe_combine")
+    return out
+
+
+def moe_layer_forward(x, w_gate, bias, layer: LayerWeights, k: int, normalize: int = 1,
+                      route_scale: float = 1.0, mode: int = MOE_MODE_AUTO, residual=None, out=None,
+                      topk_idx=None, topk_w=None, hits=None, ws=None, err=None, stream=None):
+    _need(x, torch.float32, "x")
+    T, d = x.shape
+    dev = x.device
+    out = torch.empty((T, d), dtype=torch.float32, device=dev) if out is None else out
+    if ws is None:
+        ws = workspace(layer_workspace_bytes(T, k, layer.E, d, layer.f, mode), dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    wp, wn = _ws_ptr(ws)
+    _check(lib().moe_layer_forward(_p(x), _p(w_gate), _p(bias), ctypes.byref(layer.c), _p(residual), T, k,
+                                   int(normalize), float(route_scale), mode, _p(out), _p(topk_idx), _p(topk_w),
+                                   _p(hits), wp, wn, _p(err), _stream(stream)), "moe_layer_forward")
+    return out, err
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/moe.h declares (for export checks)."""
+    import re
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*MOE_API\s+(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M)))

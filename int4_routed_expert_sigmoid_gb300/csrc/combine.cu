@@ -1,0 +1,52 @@
+// combine.cu -- score-weighted combine of the routed experts' outputs with the
+// always-on shared expert and the residual stream:
+//   out[t][c] = res[t][c] + y_shared[t][c] + sum_{j<k} w[t][j] * y_pair[perm[t*k+j]][c]
+// in slot order j (deterministic).  Source: "Public Colibri Observation and
+// Revision Ledger", "Exact Architecture and Data-Flow Reconstruction" (selected
+// experts weighted by the router; the shared branch is always used).
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+// One thread per 4 consecutive columns of one token.
+__global__ void __launch_bounds__(256)
+combine_kernel(const float4 *__restrict__ y_pair, const float4 *__restrict__ y_shared,
+               const float *__restrict__ w, const int32_t *__restrict__ perm,
+               const float4 *res, int T, int k, int d4, float4 *out)
+{
+    const long long id = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (id >= (long long)T * d4)
+        return;
+    const int t = (int)(id / d4), c = (int)(id % d4);
+    float4 acc = res ? res[id] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 ys = y_shared[id];
+    acc.x += ys.x; acc.y += ys.y; acc.z += ys.z; acc.w += ys.w;
+    for (int j = 0; j < k; j++) {
+        const int q = perm[(size_t)t * k + j];
+        if (q < 0)
+            continue;
+        const float wj = w[(size_t)t * k + j];
+        const float4 y = y_pair[(size_t)q * d4 + c];
+        acc.x = fmaf(wj, y.x, acc.x);
+        acc.y = fmaf(wj, y.y, acc.y);
+        acc.z = fmaf(wj, y.z, acc.z);
+        acc.w = fmaf(wj, y.w, acc.w);
+    }
+    out[id] = acc;
+}
+
+}  // namespace
+
+int launch_combine(const float *y_pair, const float *y_shared, const float *w, const int32_t *perm,
+                   const float *res, int T, int k, int d, float *out, cudaStream_t s)
+{
+    const int d4 = d / 4;
+    const long long n = (long long)T * d4;
+    combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
+        reinterpret_cast<const float4 *>(y_pair), reinterpret_cast<const float4 *>(y_shared), w,
+        perm, reinterpret_cast<const float4 *>(res), T, k, d4, reinterpret_cast<float4 *>(out));
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace moe

@@ -1,0 +1,285 @@
+// moe_api.cu -- the extern "C" entry points of libmoe: argument validation,
+// workspace carving and launch sequencing.  See include/moe.h for the contract
+// of each call.
+#include <cstdint>
+
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool ok_ptr(const void *p) { return p != nullptr && aligned16(p); }
+inline bool ok_opt(const void *p) { return p == nullptr || aligned16(p); }
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+bool ok_route_shape(int T, int d, int E, int k)
+{
+    return T >= 1 && d >= 4 && d % 4 == 0 && E >= 1 && E <= 1024 && k >= 1 && k <= 32 && k <= E;
+}
+
+int check_layer(const moe_layer_int4 *w)
+{
+    if (w == nullptr || !ok_ptr(w->q_base) || !ok_ptr(w->s_base) || !ok_ptr(w->shared_q) ||
+        !ok_ptr(w->shared_s))
+        return MOE_ERR_INVALID_ARG;
+    if (w->E < 1 || w->E > 1024 || w->d < 1 || w->f < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (w->G != 32 || w->d % 256 != 0 || w->f % 128 != 0)
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int resolve_mode(int mode, int T)
+{
+    if (mode == MOE_MODE_AUTO)
+        return MOE_MODE_DECODE;
+    (void)T;
+    return mode;
+}
+
+// Scratch of the decode FFN: activation fragments of x and of h.
+struct FfnScratch {
+    uint16_t *x_frag, *h_frag;
+};
+
+size_t ffn_scratch_layout(int T, int k, int d, int f, uint8_t *base, FfnScratch *out)
+{
+    size_t off = 0;
+    const size_t x_bytes = (size_t)T * 2 * d * sizeof(uint16_t);
+    const size_t h_bytes = ((size_t)T * k + T) * 2 * f * sizeof(uint16_t);
+    if (out) out->x_frag = reinterpret_cast<uint16_t *>(base + off);
+    off = align_up(off + x_bytes);
+    if (out) out->h_frag = reinterpret_cast<uint16_t *>(base + off);
+    off = align_up(off + h_bytes);
+    return off;
+}
+
+struct LayerScratch {
+    float *logits;
+    int32_t *idx;
+    float *w;
+    int32_t *counts, *offsets, *perm, *sorted_pair, *uniq, *n_uniq;
+    float *y_pair, *y_shared;
+    uint8_t *ffn;
+};
+
+size_t layer_scratch_layout(int T, int k, int E, int d, int f, uint8_t *base, LayerScratch *o)
+{
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t *p = base ? base + off : nullptr;
+        off = align_up(off + bytes);
+        return p;
+    };
+    const size_t P = (size_t)T * k;
+    LayerScratch s{};
+    s.logits = reinterpret_cast<float *>(take((size_t)T * E * 4));
+    s.idx = reinterpret_cast<int32_t *>(take(P * 4));
+    s.w = reinterpret_cast<float *>(take(P * 4));
+    s.counts = reinterpret_cast<int32_t *>(take((size_t)E * 4));
+    s.offsets = reinterpret_cast<int32_t *>(take((size_t)(E + 1) * 4));
+    s.perm = reinterpret_cast<int32_t *>(take(P * 4));
+    s.sorted_pair = reinterpret_cast<int32_t *>(take(P * 4));
+    s.uniq = reinterpret_cast<int32_t *>(take((size_t)E * 4));
+    s.n_uniq = reinterpret_cast<int32_t *>(take(4));
+    s.y_pair = reinterpret_cast<float *>(take(P * d * 4));
+    s.y_shared = reinterpret_cast<float *>(take((size_t)T * d * 4));
+    s.ffn = take(ffn_scratch_layout(T, k, d, f, nullptr, nullptr));
+    if (o)
+        *o = s;
+    return off;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_str(int status)
+{
+    switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or mode";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+    }
+}
+
+int moe_device_error(int32_t err)
+{
+    if (err == 0)
+        return MOE_OK;
+    if (err & MOE_DEVERR_TIMEOUT)
+        return MOE_ERR_CUDA;
+    return MOE_ERR_INVALID_ARG;
+}
+
+size_t moe_expert_q_bytes(int d, int f) { return (size_t)3 * d * f / 2; }
+
+size_t moe_expert_s_count(int d, int f, int G) { return G > 0 ? (size_t)3 * d * f / G : 0; }
+
+int moe_route(const float *x, const float *w_gate, const float *bias, int T, int d, int E, int k,
+              int normalize, float route_scale, int32_t *topk_idx, float *topk_w, float *logits,
+              void *stream)
+{
+    if (!ok_ptr(x) || !ok_ptr(w_gate) || !ok_opt(bias) || !ok_ptr(topk_idx) || !ok_ptr(topk_w) ||
+        !ok_ptr(logits) || !ok_route_shape(T, d, E, k))
+        return MOE_ERR_INVALID_ARG;
+    const cudaStream_t s = as_stream(stream);
+    int rc = launch_router_logits(x, w_gate, T, d, E, logits, s);
+    if (rc == MOE_OK)
+        rc = launch_router_topk(logits, bias, T, E, k, normalize, route_scale, topk_idx, topk_w, s);
+    return rc;
+}
+
+int moe_union(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
+              int32_t *perm, int32_t *sorted_pair, int32_t *uniq, int32_t *n_uniq, uint64_t *hits,
+              int32_t *err, void *stream)
+{
+    if (!ok_ptr(topk_idx) || !ok_ptr(counts) || !ok_ptr(offsets) || !ok_ptr(perm) ||
+        !ok_ptr(sorted_pair) || !ok_ptr(uniq) || !ok_ptr(n_uniq) || !ok_opt(hits) || !ok_ptr(err))
+        return MOE_ERR_INVALID_ARG;
+    if (T < 1 || k < 1 || k > 32 || E < 1 || E > 1024 || (long long)T * k > (1LL << 22))
+        return MOE_ERR_INVALID_ARG;
+    return launch_union(topk_idx, T, k, E, counts, offsets, perm, sorted_pair, uniq, n_uniq, hits,
+                        err, as_stream(stream));
+}
+
+int moe_hits(const int32_t *counts, int E, uint64_t *hits, void *stream)
+{
+    if (!ok_ptr(counts) || !ok_ptr(hits) || E < 1 || E > (1 << 20))
+        return MOE_ERR_INVALID_ARG;
+    return launch_hits(counts, E, hits, as_stream(stream));
+}
+
+size_t moe_ffn_workspace_bytes(int T, int k, int d, int f, int mode)
+{
+    (void)mode;
+    if (T < 1 || k < 1 || d < 1 || f < 1)
+        return 0;
+    return ffn_scratch_layout(T, k, d, f, nullptr, nullptr);
+}
+
+int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *offsets,
+                        const int32_t *sorted_pair, const int32_t *uniq, const int32_t *n_uniq,
+                        int T, int k, int mode, float *y_pair, float *y_shared, void *workspace,
+                        size_t ws_bytes, int32_t *err, void *stream)
+{
+    int rc = check_layer(w);
+    if (rc != MOE_OK)
+        return rc;
+    if (!ok_ptr(x) || !ok_ptr(offsets) || !ok_ptr(sorted_pair) || !ok_ptr(uniq) ||
+        !ok_ptr(n_uniq) || !ok_ptr(y_pair) || !ok_ptr(y_shared) || !ok_ptr(err) ||
+        workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (T < 1 || k < 1 || k > 32 || k > w->E || (long long)T * (k + 1) > (1LL << 24))
+        return MOE_ERR_INVALID_ARG;
+    mode = resolve_mode(mode, T);
+    if (mode != MOE_MODE_DECODE)
+        return MOE_ERR_UNSUPPORTED;
+    if (ws_bytes < moe_ffn_workspace_bytes(T, k, w->d, w->f, mode))
+        return MOE_ERR_WORKSPACE;
+    FfnScratch sc{};
+    ffn_scratch_layout(T, k, w->d, w->f, static_cast<uint8_t *>(workspace), &sc);
+    const cudaStream_t s = as_stream(stream);
+    rc = launch_act_frag(x, T, w->d, sc.x_frag, s);
+    if (rc != MOE_OK)
+        return rc;
+    DecodeFfnArgs a{};
+    a.w = w;
+    a.offsets = offsets;
+    a.sorted_pair = sorted_pair;
+    a.uniq = uniq;
+    a.n_uniq = n_uniq;
+    a.T = T;
+    a.k = k;
+    a.x_frag = sc.x_frag;
+    a.h_frag = sc.h_frag;
+    a.y_pair = y_pair;
+    a.y_shared = y_shared;
+    a.err = err;
+    return launch_ffn_decode(a, s);
+}
+
+int moe_combine(const float *y_pair, const float *y_shared, const float *topk_w,
+                const int32_t *perm, const float *residual, int T, int k, int d, float *out,
+                void *stream)
+{
+    if (!ok_ptr(y_pair) || !ok_ptr(y_shared) || !ok_ptr(topk_w) || !ok_ptr(perm) ||
+        !ok_opt(residual) || !ok_ptr(out) || T < 1 || k < 1 || k > 32 || d < 4 || d % 4 != 0)
+        return MOE_ERR_INVALID_ARG;
+    return launch_combine(y_pair, y_shared, topk_w, perm, residual, T, k, d, out, as_stream(stream));
+}
+
+size_t moe_layer_workspace_bytes(int T, int k, int E, int d, int f, int mode)
+{
+    (void)mode;
+    if (T < 1 || k < 1 || E < 1 || d < 1 || f < 1)
+        return 0;
+    return layer_scratch_layout(T, k, E, d, f, nullptr, nullptr);
+}
+
+int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
+                      const moe_layer_int4 *w, const float *residual, int T, int k, int normalize,
+                      float route_scale, int mode, float *out, int32_t *topk_idx, float *topk_w,
+                      uint64_t *hits, void *workspace, size_t ws_bytes, int32_t *err, void *stream)
+{
+    int rc = check_layer(w);
+    if (rc != MOE_OK)
+        return rc;
+    const int E = w->E, d = w->d, f = w->f;
+    if (!ok_ptr(x) || !ok_ptr(w_gate) || !ok_opt(bias) || !ok_opt(residual) || !ok_ptr(out) ||
+        !ok_opt(topk_idx) || !ok_opt(topk_w) || !ok_opt(hits) || !ok_ptr(err) ||
+        workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!ok_route_shape(T, d, E, k) || (long long)T * (k + 1) > (1LL << 22))
+        return MOE_ERR_INVALID_ARG;
+    mode = resolve_mode(mode, T);
+    if (mode != MOE_MODE_DECODE)
+        return MOE_ERR_UNSUPPORTED;
+    if (ws_bytes < moe_layer_workspace_bytes(T, k, E, d, f, mode))
+        return MOE_ERR_WORKSPACE;
+    LayerScratch sc{};
+    layer_scratch_layout(T, k, E, d, f, static_cast<uint8_t *>(workspace), &sc);
+    int32_t *idx = topk_idx ? topk_idx : sc.idx;
+    float *wt = topk_w ? topk_w : sc.w;
+    const cudaStream_t s = as_stream(stream);
+    rc = launch_router_logits(x, w_gate, T, d, E, sc.logits, s);
+    if (rc == MOE_OK)
+        rc = launch_router_topk(sc.logits, bias, T, E, k, normalize, route_scale, idx, wt, s);
+    if (rc == MOE_OK)
+        rc = launch_union(idx, T, k, E, sc.counts, sc.offsets, sc.perm, sc.sorted_pair, sc.uniq,
+                          sc.n_uniq, hits, err, s);
+    if (rc != MOE_OK)
+        return rc;
+    FfnScratch fs{};
+    ffn_scratch_layout(T, k, d, f, sc.ffn, &fs);
+    rc = launch_act_frag(x, T, d, fs.x_frag, s);
+    if (rc != MOE_OK)
+        return rc;
+    DecodeFfnArgs a{};
+    a.w = w;
+    a.offsets = sc.offsets;
+    a.sorted_pair = sc.sorted_pair;
+    a.uniq = sc.uniq;
+    a.n_uniq = sc.n_uniq;
+    a.T = T;
+    a.k = k;
+    a.x_frag = fs.x_frag;
+    a.h_frag = fs.h_frag;
+    a.y_pair = sc.y_pair;
+    a.y_shared = sc.y_shared;
+    a.err = err;
+    rc = launch_ffn_decode(a, s);
+    if (rc != MOE_OK)
+        return rc;
+    return launch_combine(sc.y_pair, sc.y_shared, wt, sc.perm, residual, T, k, d, out, s);
+}
+
+}  // extern "C"

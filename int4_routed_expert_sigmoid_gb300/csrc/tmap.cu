@@ -1,0 +1,60 @@
+// tmap.cu -- host helpers: TMA tensor-map encoding through the driver entry
+// point (no link-time dependency on libcuda) and cached device properties.
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode()
+{
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+}  // namespace
+
+int make_tmap_3d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                 uint64_t inner, uint64_t rows, uint64_t outer, uint64_t row_stride_bytes,
+                 uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+                 CUtensorMapSwizzle swizzle)
+{
+    std::call_once(g_encode_once, load_encode);
+    if (!g_encode)
+        return MOE_ERR_CUDA;
+    const cuuint64_t dims[3] = {inner, rows, outer};
+    const cuuint64_t strides[2] = {row_stride_bytes, outer_stride_bytes};
+    const cuuint32_t box[3] = {box_inner, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    (void)elem_bytes;
+    const CUresult r = g_encode(m, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
+int sm_count(int device)
+{
+    static int cache[64] = {0};
+    if (device < 0 || device >= 64)
+        return 0;
+    if (cache[device] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+            return 0;
+        cache[device] = n;
+    }
+    return cache[device];
+}
+
+}  // namespace moe

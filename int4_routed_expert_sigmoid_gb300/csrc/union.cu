@@ -1,0 +1,199 @@
+// union.cu -- Union and Learn stages: group the batch's (token, slot) pairs by
+// expert so that every unique expert is read once, and bump the per-expert hit
+// counters.
+//
+// Sources: "Public Colibri Observation and Revision Ledger", "Exact
+// Architecture and Data-Flow Reconstruction" (Union merges requests across the
+// batch; Learn records which experts were used, per-expert hit counters), and
+// the figure caption of "Cache/Prefetch Design Comparison" (with batch-union
+// each unique expert is read only once).
+//
+// One thread block: a shared-memory histogram (atomics only count), a block
+// scan for the offsets, then a stable placement pass over the pairs in chunks
+// of the block size, where a pair's rank among equal experts is its rank in
+// its warp (match_any) plus the counts of earlier warps and earlier chunks.
+// The result is deterministic and independent of scheduling.
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxE = 1024;
+
+// Exclusive block scan of one int per thread (kThreads threads); returns the
+// exclusive prefix and writes the total to *total.
+__device__ int block_exclusive_scan(int v, int *warp_sums, int *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off)
+            inc += n;
+    }
+    if (lane == 31)
+        warp_sums[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int ws = warp_sums[lane];
+        int wi = ws;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off)
+                wi += n;
+        }
+        warp_sums[lane] = wi - ws;   // exclusive prefix of warp totals
+        if (lane == 31)
+            *total = wi;
+    }
+    __syncthreads();
+    const int r = warp_sums[warp] + inc - v;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads)
+union_kernel(const int32_t *__restrict__ idx, int P, int E, int32_t *__restrict__ counts,
+             int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
+             int32_t *__restrict__ sorted_pair, int32_t *__restrict__ uniq,
+             int32_t *__restrict__ n_uniq, uint64_t *__restrict__ hits, int32_t *__restrict__ err)
+{
+    extern __shared__ int dyn[];
+    int *cnt = dyn;                 // [E] pairs per expert
+    int *base = dyn + E;            // [E] next free position per expert
+    unsigned short *wcnt = reinterpret_cast<unsigned short *>(dyn + 2 * E);   // [kWarps][E]
+    __shared__ int warp_sums[32];
+    __shared__ int total;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    for (int e = tid; e < E; e += kThreads)
+        cnt[e] = 0;
+    __syncthreads();
+    int bad = 0;
+    for (int p = tid; p < P; p += kThreads) {
+        const int e = idx[p];
+        if (e < 0 || e >= E)
+            bad = 1;
+        else
+            atomicAdd(&cnt[e], 1);
+    }
+    if (__syncthreads_or(bad) && tid == 0)
+        atomicOr(err, MOE_DEVERR_BAD_EXPERT);
+
+    // offsets (exclusive scan over ascending expert id) and uniq list
+    for (int e0 = 0; e0 < E; e0 += kThreads) {
+        const int e = e0 + tid;
+        const int c = e < E ? cnt[e] : 0;
+        const int carry = e0 == 0 ? 0 : base[e0 - 1] + cnt[e0 - 1];
+        const int ex = block_exclusive_scan(c, warp_sums, &total) + carry;
+        if (e < E) {
+            base[e] = ex;
+            offsets[e] = ex;
+            counts[e] = c;
+            if (hits)
+                hits[e] += (uint64_t)c;
+        }
+        __syncthreads();
+    }
+    if (tid == 0)
+        offsets[E] = E > 0 ? base[E - 1] + cnt[E - 1] : 0;
+    {
+        int carry = 0;
+        for (int e0 = 0; e0 < E; e0 += kThreads) {
+            const int e = e0 + tid;
+            const int flag = (e < E && cnt[e] > 0) ? 1 : 0;
+            const int ex = block_exclusive_scan(flag, warp_sums, &total) + carry;
+            if (flag)
+                uniq[ex] = e;
+            carry += total;
+            __syncthreads();
+        }
+        if (tid == 0)
+            *n_uniq = carry;
+    }
+
+    // stable placement, one chunk of kThreads pairs at a time
+    for (int c0 = 0; c0 < P; c0 += kThreads) {
+        for (int i = tid; i < kWarps * E; i += kThreads)
+            wcnt[i] = 0;
+        __syncthreads();
+        const int p = c0 + tid;
+        int e = -1;
+        if (p < P) {
+            e = idx[p];
+            if (e < 0 || e >= E)
+                e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+        if (e >= 0 && rank_in_warp == 0)
+            wcnt[warp * E + e] = (unsigned short)__popc(peers);
+        __syncthreads();
+        int pos = -1;
+        if (e >= 0) {
+            int before = 0;
+            for (int w = 0; w < warp; w++)
+                before += wcnt[w * E + e];
+            pos = base[e] + before + rank_in_warp;
+        }
+        if (p < P) {
+            perm[p] = pos;
+            if (pos >= 0)
+                sorted_pair[pos] = p;
+        }
+        __syncthreads();
+        // advance the per-expert bases by this chunk's counts
+        for (int x = tid; x < E; x += kThreads) {
+            int s = 0;
+            for (int w = 0; w < kWarps; w++)
+                s += wcnt[w * E + x];
+            base[x] += s;
+        }
+        __syncthreads();
+    }
+}
+
+size_t union_smem_bytes(int E)
+{
+    return (size_t)E * 2 * sizeof(int) + (size_t)kWarps * E * sizeof(unsigned short);
+}
+
+__global__ void hits_kernel(const int32_t *__restrict__ counts, int E, uint64_t *__restrict__ hits)
+{
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e < E)
+        hits[e] += (uint64_t)counts[e];
+}
+
+}  // namespace
+
+int launch_union(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                 int32_t *perm, int32_t *sorted_pair, int32_t *uniq, int32_t *n_uniq,
+                 uint64_t *hits, int32_t *err, cudaStream_t s)
+{
+    const size_t smem = union_smem_bytes(E);
+    static thread_local int configured_for = -1;   // per host thread, per device attribute set once
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_for != dev) {
+        if (cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)union_smem_bytes(kMaxE)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        configured_for = dev;
+    }
+    union_kernel<<<1, kThreads, smem, s>>>(idx, T * k, E, counts, offsets, perm, sorted_pair, uniq,
+                                        n_uniq, hits, err);
+    return cuda_status(cudaGetLastError());
+}
+
+int launch_hits(const int32_t *counts, int E, uint64_t *hits, cudaStream_t s)
+{
+    hits_kernel<<<(E + 255) / 256, 256, 0, s>>>(counts, E, hits);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace moe

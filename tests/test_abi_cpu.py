@@ -1,0 +1,65 @@
+"""The C-ABI library builds, loads without a GPU, exports every symbol that
+include/moe.h declares, and rejects bad arguments on the host before any CUDA
+call.  No compute call is made here."""
+import ctypes
+
+import pytest
+
+import oracle
+import workloads
+
+
+@pytest.fixture(scope="module")
+def m():
+    from int4_routed_expert_sigmoid_gb300 import build
+    build.build()
+    import int4_routed_expert_sigmoid_gb300 as pkg
+    return pkg
+
+
+def test_exports_every_header_symbol(m):
+    names = m.header_functions()
+    assert len(names) >= 12
+    L = m.lib()
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_device_error_decoding(m):
+    assert m.status_str(m.MOE_OK) == "ok"
+    assert "workspace" in m.status_str(m.MOE_ERR_WORKSPACE)
+    assert m.device_error(0) == m.MOE_OK
+    assert m.device_error(m.MOE_DEVERR_BAD_EXPERT) == m.MOE_ERR_INVALID_ARG
+    assert m.device_error(m.MOE_DEVERR_TIMEOUT) == m.MOE_ERR_CUDA
+
+
+@pytest.mark.parametrize("d,f", [(256, 128), (6144, 2048), (1024, 384)])
+def test_expert_sizes_agree_with_oracle_layout(m, d, f):
+    assert m.expert_q_bytes(d, f) == oracle.expert_q_bytes(d, f) == workloads.expert_q_bytes(d, f)
+    assert m.expert_s_count(d, f, 32) == oracle.expert_s_count(d, f, 32) == workloads.expert_s_count(d, f, 32)
+
+
+def test_workspace_queries(m):
+    assert m.ffn_workspace_bytes(0, 8, 6144, 2048) == 0
+    a = m.layer_workspace_bytes(1, 8, 256, 6144, 2048)
+    b = m.layer_workspace_bytes(64, 8, 256, 6144, 2048)
+    assert 0 < a < b and a % 256 == 0
+    # y_pair alone is T*k*d floats
+    assert b >= 64 * 8 * 6144 * 4
+
+
+def test_host_validation_rejects_without_launching(m):
+    L = m.lib()
+    P = None
+    assert L.moe_route(P, P, P, 1, 256, 8, 2, 1, 1.0, P, P, P, P) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_union(P, 1, 2, 8, P, P, P, P, P, P, P, P, P) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_hits(P, 8, P, P) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(P, P, P, P, P, 1, 2, 256, P, P) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_layer_forward(P, P, P, None, P, 1, 2, 1, 1.0, 0, P, P, P, P, P, 0, P, P) == m.MOE_ERR_INVALID_ARG
+    # a layer with an unsupported group size is refused before its pointers are used
+    fake = m._binding.moe_layer_int4(16, 16, 16, 16, 8, 256, 128, 64)
+    assert L.moe_expert_ffn_int4(P, ctypes.byref(fake), P, P, P, P, 1, 2, 0, P, P, P, 0, P, P) == \
+        m.MOE_ERR_UNSUPPORTED
+    # misaligned pointers are refused
+    bad = ctypes.c_void_p(0x1004)
+    assert L.moe_hits(bad, 8, bad, P) == m.MOE_ERR_INVALID_ARG

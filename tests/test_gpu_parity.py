@@ -1,0 +1,146 @@
+"""GPU parity: the CUDA path through the C ABI vs the fp64 oracle on the same
+seeded inputs (small shapes that span several tiles, k-chunks and ragged tails).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from moe_testlib import (TOL_DECODE, check_union_equal, compare_routing, device_layer, host, moe,
+                         oracle_layer, rel_max_err, run_steps)
+
+pytestmark = pytest.mark.gpu
+
+Shape = workloads.Shape
+SMALL = [
+    workloads.WORKLOADS["tiny"],                                            # 4 gate/up tiles, 1 k-chunk
+    Shape("ragged_kc128", E=16, k=4, d=1024, f=384, T=37, bias="normal"),   # 4 k-chunks, 128-wide down chunks
+    Shape("zipf_small", E=64, k=8, d=512, f=512, T=5, bias="zipf"),
+    Shape("single_token", E=33, k=3, d=256, f=256, T=1, bias="normal"),
+    Shape("multi_pass", E=8, k=2, d=256, f=128, T=300),                     # > 16 tokens per expert
+    Shape("k1", E=4, k=1, d=256, f=128, T=9, bias="normal"),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from int4_routed_expert_sigmoid_gb300 import build
+    build.build()
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
+@pytest.mark.parametrize("normalize,route_scale,with_res", [(1, 1.0, False), (0, 1.0, True), (1, 2.5, True)])
+def test_layer_parity_small(shape, normalize, route_scale, with_res):
+    m = moe()
+    L = workloads.layer_inputs(shape, seed=1, threads=4)
+    res = workloads.activations(shape.T, shape.d, seed=77) if with_res else None
+    dev = device_layer(L)
+    res_d = torch.from_numpy(res).cuda() if res is not None else None
+    k = shape.k
+
+    o_idx, o_w, o_logits, keys = oracle.route(L.x, L.wg, L.bias, k, normalize, route_scale)
+    o_union = oracle.union(o_idx, shape.E)
+    _, _, o_out = oracle_layer(L, normalize=normalize, route_scale=route_scale, res=res).dense()
+
+    # 1) the layer as the GPU routes it
+    hits = torch.zeros(shape.E, dtype=torch.int64, device="cuda")
+    r = run_steps(dev, k, normalize=normalize, route_scale=route_scale, res=res_d, hits=hits)
+    assert r["err"] == 0
+    assert np.max(np.abs(r["logits"] - o_logits)) <= 1e-5 * max(1.0, float(np.abs(o_logits).max()))
+    same, flagged = compare_routing(r["idx"], r["w"], o_idx, o_w, keys, k)
+    if same.all():
+        check_union_equal(r, o_union, shape.E)
+        assert np.array_equal(host(hits), o_union["counts"].astype(np.int64))
+    assert int(host(hits).sum()) == shape.T * k
+    assert rel_max_err(r["out"][same], o_out[same]) <= TOL_DECODE
+
+    # 2) teacher-forced: downstream stages on the oracle's routing, all tokens
+    t = run_steps(dev, k, res=res_d, teacher_idx=o_idx, teacher_w=o_w)
+    assert t["err"] == 0
+    check_union_equal(t, o_union, shape.E)
+    assert rel_max_err(t["out"], o_out) <= TOL_DECODE
+    y_sh = oracle.expert_ffn_tokens(L.x, np.arange(shape.T), L.shared_q, L.shared_s, shape.d, shape.f, shape.G)
+    assert rel_max_err(t["y_shared"], y_sh) <= TOL_DECODE
+    for e in o_union["uniq"][:o_union["n_uniq"]]:
+        lo, hi = o_union["offsets"][e], o_union["offsets"][e + 1]
+        toks = o_union["sorted_pair"][lo:hi] // k
+        y = oracle.expert_ffn_tokens(L.x, toks, L.q_base[e], L.s_base[e], shape.d, shape.f, shape.G)
+        assert rel_max_err(t["y_pair"][lo:hi], y) <= TOL_DECODE, f"expert {e}"
+
+    # 3) the fused entry point gives the same bits as the separate calls
+    out_f, err_f = m.moe_layer_forward(dev["x"], dev["wg"], dev["bias"], dev["layer"], k, normalize, route_scale,
+                                       residual=res_d)
+    torch.cuda.synchronize()
+    assert int(host(err_f)[0]) == 0
+    assert np.array_equal(host(out_f), r["out"])
+
+
+def test_fused_layer_is_deterministic():
+    m = moe()
+    L = workloads.layer_inputs(SMALL[1], seed=3, threads=4)
+    dev = device_layer(L)
+    outs = []
+    for _ in range(3):
+        o, e = m.moe_layer_forward(dev["x"], dev["wg"], dev["bias"], dev["layer"], SMALL[1].k)
+        torch.cuda.synchronize()
+        assert int(host(e)[0]) == 0
+        outs.append(host(o))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+
+
+def test_union_flags_bad_expert_ids():
+    m = moe()
+    E, k = 8, 2
+    idx = torch.tensor([[0, 3], [8, 3], [3, -1], [7, 0]], dtype=torch.int32, device="cuda")
+    un = m.moe_union(idx, E)
+    torch.cuda.synchronize()
+    assert int(host(un["err"])[0]) & m.MOE_DEVERR_BAD_EXPERT
+    perm = host(un["perm"])
+    assert perm[2] == -1 and perm[5] == -1
+    valid = [0, 1, 3, 4, 6, 7]
+    sp = host(un["sorted_pair"])
+    assert sorted(perm[valid].tolist()) == list(range(6))
+    assert np.array_equal(sp[perm[valid]], np.array(valid))
+    assert host(un["counts"]).tolist() == [2, 0, 0, 3, 0, 0, 0, 1]
+
+
+def test_hits_accumulate_across_calls():
+    m = moe()
+    rng = np.random.default_rng(0)
+    E, T, k = 256, 64, 8
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    hits = torch.zeros(E, dtype=torch.int64, device="cuda")
+    d_idx = torch.from_numpy(idx).cuda()
+    for _ in range(3):
+        un = m.moe_union(d_idx, E, hits=hits)
+    m.moe_hits(un["counts"], hits)
+    torch.cuda.synchronize()
+    expect = 4 * np.bincount(idx.ravel(), minlength=E)
+    assert np.array_equal(host(hits), expect) and int(host(hits).sum()) == 4 * T * k
+
+
+def test_abi_rejects_bad_arguments_on_device():
+    m = moe()
+    L = workloads.layer_inputs(workloads.WORKLOADS["tiny"], seed=0, threads=2)
+    dev = device_layer(L)
+    lw = dev["layer"]
+    x = dev["x"]
+    T, d = x.shape
+    small_ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_layer_forward(x, dev["wg"], None, lw, 2, ws=small_ws)
+    assert ei.value.status == m.MOE_ERR_WORKSPACE
+    bad = m.LayerWeights(lw.q_base, lw.s_base, lw.shared_q, lw.shared_s, E=lw.E, d=lw.d, f=lw.f, G=32)
+    bad.c.G = 64
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_layer_forward(x, dev["wg"], None, bad, 2)
+    assert ei.value.status == m.MOE_ERR_UNSUPPORTED
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_route(x, dev["wg"], None, k=9)                # k > E
+    assert ei.value.status == m.MOE_ERR_INVALID_ARG
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_route(x[:, :255].contiguous(), dev["wg"], None, k=2)   # d not a multiple of 4
+    assert ei.value.status == m.MOE_ERR_INVALID_ARG
