@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode", choices=["decode", "batched_decode"])
     ap.add_argument("--replicas", type=int, default=4, help="device copies of the layer rotated across steps")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the routed expert count (small-footprint profiling runs); 0 = workload's")
     ap.add_argument("--graph-steps", type=int, default=100, help="steps captured per CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -173,6 +175,9 @@ def run_ours(args, rank, world, local):
             dist.init_process_group("nccl")
     libbuild.build()
     sh = workloads.WORKLOADS[args.workload]
+    if args.experts:
+        import dataclasses
+        sh = dataclasses.replace(sh, E=args.experts)
     T, E, k, d, f = sh.T, sh.E, sh.k, sh.d, sh.f
     R = max(1, args.replicas)
     S = max(1, min(args.graph_steps, args.steps))

@@ -184,6 +184,32 @@ MOE_API int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const i
 MOE_API size_t moe_ffn_workspace_bytes(int T, int k, int d, int f, int mode);
 
 /*
+ * moe_expert_ffn_int4_noalloc: moe_expert_ffn_int4 without a caller workspace.
+ * The pages have no counterpart of this call; it exists for callers that
+ * cannot allocate device memory: code inside a host framework that owns all
+ * device memory and forbids other allocations, or code on a latency-critical
+ * path that cannot afford cudaMalloc/cudaFree (both may synchronise the
+ * device).  Inputs and outputs are as for moe_expert_ffn_int4 and are still
+ * passed by the caller.
+ *
+ * Scratch: a static device array of MOE_NOALLOC_SCRATCH_BYTES (8 MiB) that
+ * every GPU which loads the library holds until the process exits.  The first
+ * call made on a device looks up that array's device address (once per
+ * device, with the device current); make that first call before any stream
+ * capture.  No call allocates memory.  A batch whose scratch need
+ * (moe_ffn_workspace_bytes) exceeds the array returns MOE_ERR_WORKSPACE and
+ * enqueues nothing.  All calls on a device share the array, which keeps the
+ * last call's contents: calls that overlap on the GPU race, so order them on
+ * one stream.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+MOE_API int moe_expert_ffn_int4_noalloc(const float *x, const moe_layer_int4 *w,
+                                        const int32_t *offsets, const int32_t *sorted_pair,
+                                        const int32_t *uniq, const int32_t *n_uniq, int T, int k,
+                                        int mode, float *y_pair, float *y_shared, int32_t *err,
+                                        void *stream);
+
+/*
  * Score-weighted combine (+ residual):
  *   out[t][c] = residual[t][c] + y_shared[t][c] + sum_{j<k} topk_w[t][j] * y_pair[perm[t*k+j]][c]
  * summed left to right in slot order j.  residual may be NULL (taken as 0) and

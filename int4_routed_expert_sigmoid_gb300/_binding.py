@@ -50,6 +50,8 @@ _SIGNATURES = {
     "moe_expert_ffn_int4": ([_P, ctypes.POINTER(moe_layer_int4), _P, _P, _P, _P, _I, _I, _I, _P, _P,
                              _P, _SZ, _P, _P], _I),
     "moe_ffn_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
+    "moe_expert_ffn_int4_noalloc": ([_P, ctypes.POINTER(moe_layer_int4), _P, _P, _P, _P, _I, _I, _I, _P, _P,
+                                     _P, _P], _I),
     "moe_combine": ([_P, _P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
     "moe_layer_forward": ([_P, _P, _P, ctypes.POINTER(moe_layer_int4), _P, _I, _I, _I, _F, _I, _P, _P,
                            _P, _P, _P, _SZ, _P, _P], _I),
@@ -209,6 +211,29 @@ def moe_expert_ffn_int4(x, layer: LayerWeights, un: dict, k: int, mode: int = MO
     _check(lib().moe_expert_ffn_int4(_p(x), ctypes.byref(layer.c), _p(un["offsets"]), _p(un["sorted_pair"]),
                                      _p(un["uniq"]), _p(un["n_uniq"]), T, k, mode, _p(y_pair), _p(y_shared),
                                      wp, wn, _p(err), _stream(stream)), "moe_expert_ffn_int4")
+    return y_pair, y_shared, err
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def moe_expert_ffn_int4_noalloc(x, layer: LayerWeights, un: dict, k: int, mode: int = MOE_MODE_AUTO,
+                                y_pair=None, y_shared=None, err=None, stream=None):
+    """moe_expert_ffn_int4 with its scratch in the library's static device array
+    (for callers that cannot allocate device memory); outputs as for
+    moe_expert_ffn_int4.  Calls on one device share that array: keep them on one
+    stream."""
+    _need(x, torch.float32, "x")
+    T, d = x.shape
+    dev = x.device
+    y_pair = torch.empty((T * k, d), dtype=torch.float32, device=dev) if y_pair is None else y_pair
+    y_shared = torch.empty((T, d), dtype=torch.float32, device=dev) if y_shared is None else y_shared
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(lib().moe_expert_ffn_int4_noalloc(_p(x), ctypes.byref(layer.c), _p(un["offsets"]),
+                                             _p(un["sorted_pair"]), _p(un["uniq"]), _p(un["n_uniq"]), T, k,
+                                             mode, _p(y_pair), _p(y_shared), _p(err), _stream(stream)),
+           "moe_expert_ffn_int4_noalloc")
     return y_pair, y_shared, err
 
 
