@@ -11,25 +11,31 @@
 //
 // Design (GB300, sm_103a)
 //  * Work item = (expert of the union or the shared expert, tile of output
-//    rows).  A persistent grid walks the items; warp 8 of every CTA is a TMA
-//    producer that streams the item's weight rows (packed nibbles + scales)
-//    through an 8-stage mbarrier ring, k-chunks of 256 elements, 128B-swizzled.
-//  * Eight consumer warps turn nibbles into bf16 *exactly* (magic-exponent
-//    trick: 0x4300|(n^8) is 136+q as bf16, minus 136) and run m16n8k16 MMAs
-//    whose B operand is the activation split into bf16 hi + lo columns, so each
-//    product is exact and the fp32 accumulation gives fp32-grade results.  The
-//    per-group scale multiplies each group's MMA result in fp32.
-//    A plain fp32 CUDA-core GEMV would need ~2 integer ops per weight for the
-//    unpacking (integer pipe at half rate) plus the FMA, which caps it below
-//    the HBM roofline; here the unpacking costs ~1 op per weight and the
-//    multiply-add runs on the tensor pipe.
+//    rows).  A persistent grid walks the items.  Warp 8 of every CTA is the
+//    producer: per k-chunk of 256 (or 128) elements it TMA-loads the item's
+//    weight rows (packed nibbles, 128B/64B-swizzled, and fp32 scales) and, with
+//    1-D bulk copies issued by one lane per token, the matching activation
+//    fragments and their corrections, all into one stage of an mbarrier ring.
+//    Consumers read every operand from shared memory.
+//  * Eight consumer warps run m16n8k16 fp16 MMAs.  A packed nibble becomes
+//    an fp16 *subnormal* with one logic op: (n ^ 8) in the mantissa is
+//    (q + 8) * 2^-24 exactly (a nibble four bits higher gives 16 (q + 8) * 2^-24,
+//    the 16 being undone in the activation operand).  The activation is split
+//    into fp16 hi + lo columns, scaled by a power of two for range.  Products
+//    are exact and accumulate in fp32; per group, 2^24 * D minus the
+//    precomputed 8 * sum(activation) correction is the exact-integer dot
+//    product, multiplied in fp32 by the group scale.  Unpacking costs 10
+//    integer ops per 512 weights and no float op (the integer pipe, which runs
+//    at half rate, is what bounds this loop).
 //  * Gate/up pass: rows of gate and up for a 32-row tile; the epilogue forms
-//    h = silu(g) * u in fp32 and stores it as hi/lo bf16 fragments (the B
-//    operand of the down pass).  Down pass: 64-row tiles of the down matrix,
-//    output y in fp32.
+//    h = silu(g) * u in fp32 and stores it as fragments (one power-of-two
+//    factor and one correction pair per 32 rows) for the down pass.  Down
+//    pass: 64-row tiles of the down matrix, output y in fp32.
 //  * Every mbarrier wait is bounded; a timeout sets MOE_DEVERR_TIMEOUT and the
 //    CTA finishes without further waits.
-#include <cuda_bf16.h>
+//  * The kernels wait on their predecessor grid (griddepcontrol) only after
+//    their prologue, so a programmatic-dependent launch overlaps the two.
+#include <cuda_fp16.h>
 
 #include "moe_internal.h"
 #include "ptx.cuh"
@@ -43,18 +49,30 @@ constexpr int kProducerWarp = kConsumerWarps;
 
 enum { kGateUp = 0, kDown = 1 };
 
-template <int MODE, int KC>
+template <int MODE, int NT, int KC>
 struct Cfg {
     static constexpr int kRowsPerMat = MODE == kGateUp ? 32 : 64;   // output rows per item
     static constexpr int kMats = MODE == kGateUp ? 2 : 1;
     static constexpr int kRowBytes = KC / 2;                        // packed bytes per row per stage
     static constexpr int kGps = KC / 32;                            // scale groups per stage
     static constexpr int kGph = kGps / 2;                           // groups per k-half
+    static constexpr int kTok = 4 * NT;                             // tokens per pass
     static constexpr int kQBytes = kRowsPerMat * kRowBytes;         // per matrix
     static constexpr int kSBytes = kRowsPerMat * kGps * 4;          // per matrix
-    static constexpr int kStageBytes = kMats * (kQBytes + kSBytes);
-    static constexpr int kStages = KC == 256 ? 8 : 16;
-    static_assert(kStageBytes % 1024 == 0, "stage must keep 1 KiB alignment");
+    static constexpr int kPlaneBytes = kGps * 64;                   // one token's hi (or lo) chunk
+    static constexpr int kCBytes = kGps * 8;                        // one token's corrections (hi, lo)
+    static constexpr int kFBytes = MODE == kDown ? kGps * 4 : 0;    // one token's group factors
+    static constexpr int kQOff = 0;
+    static constexpr int kSOff = kMats * kQBytes;
+    static constexpr int kBOff = kSOff + kMats * kSBytes;
+    static constexpr int kCOff = kBOff + kTok * 2 * kPlaneBytes;
+    static constexpr int kFOff = kCOff + kTok * kCBytes;
+    static constexpr int kUsed = kFOff + kTok * kFBytes;
+    static constexpr int kStageBytes = (kUsed + 1023) / 1024 * 1024;   // keeps the swizzle atoms aligned
+    static constexpr int kStages = (100 * 1024) / kStageBytes < 16 ? (100 * 1024) / kStageBytes : 16;
+    static constexpr int kWeightBytes = kMats * (kQBytes + kSBytes);
+    static constexpr int kTokBytes = 2 * kPlaneBytes + kCBytes + kFBytes;
+    static_assert(kStages >= 3, "ring too shallow");
 };
 
 struct Maps {
@@ -64,21 +82,34 @@ struct Maps {
 
 struct Params {
     const int32_t *offsets, *sorted_pair, *uniq, *n_uniq;
-    const uint16_t *act;   // activation fragments, row stride 2*K bf16
-    uint16_t *h_out;       // gate/up output fragments, row stride 2*f bf16
+    const uint16_t *act;        // activation fragments (fp16), row stride 2*K
+    const float *act_scale;     // gate/up: per-row factor of x; down: per-(row, group) factor of h
+    const float *act_corr;      // [rows][K/32][2] corrections
+    uint16_t *h_out;            // gate/up output fragments, row stride 2*f
+    float *h_scale;             // gate/up output factors [rows][f/32]
+    float *h_corr;              // gate/up output corrections [rows][f/32][2]
     float *y_pair, *y_shared;
     int32_t *err;
     int T, k, K, tiles, out_rows;   // K: reduction length; out_rows: rows of the output matrix
 };
 
-// Packed nibble pair (bits 0-3 and 16-19 of w) -> two exact bf16 values.
-__device__ __forceinline__ uint32_t nib2_to_bf16x2(uint32_t w)
+// Packed nibbles -> fp16 subnormal pairs: lo takes the nibbles at bits 0-3 and
+// 16-19 -> (q + 8) * 2^-24 each; hi those at bits 4-7 and 20-23 -> 16 (q + 8) * 2^-24.
+// (w & m) ^ x as one three-input logic op: both constants are passed in
+// registers (an instruction can carry only one immediate), LUT 0x6A.
+struct NibConst {
+    uint32_t m_lo, x_lo, m_hi, x_hi;
+};
+
+__device__ __forceinline__ uint32_t and_xor(uint32_t w, uint32_t m, uint32_t x)
 {
-    const uint32_t v = (w & 0x000F000Fu) ^ 0x43084308u;   // bf16 136 + q in each half
     uint32_t r;
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x43084308u));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(w), "r"(m), "r"(x));
     return r;
 }
+
+__device__ __forceinline__ uint32_t nib_lo(uint32_t w, const NibConst &k) { return and_xor(w, k.m_lo, k.x_lo); }
+__device__ __forceinline__ uint32_t nib_hi(uint32_t w, const NibConst &k) { return and_xor(w, k.m_hi, k.x_hi); }
 
 template <int KC>
 __device__ __forceinline__ int swz(int r)
@@ -111,12 +142,20 @@ __device__ __forceinline__ Item decode_item(const Params &p, int i)
     return it;
 }
 
+// Activation row of token tt (< m) of an item: x row (gate/up) or h row (down).
+template <int MODE>
+__device__ __forceinline__ int act_row(const Params &p, const Item &it, int tt)
+{
+    if (MODE == kGateUp)
+        return it.expert < 0 ? tt : p.sorted_pair[it.pos0 + tt] / p.k;
+    return it.expert < 0 ? p.T * p.k + tt : it.pos0 + tt;
+}
+
 template <int MODE, int NT, int KC>
-__global__ void __launch_bounds__(kThreads, NT <= 4 ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, 2)
 ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
 {
-    using C = Cfg<MODE, KC>;
-    constexpr int kTokPerPass = 4 * NT;
+    using C = Cfg<MODE, NT, KC>;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t full_bar[C::kStages];
     __shared__ __align__(8) uint64_t empty_bar[C::kStages];
@@ -126,6 +165,7 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
     const uint32_t stage0 = (raw + 1023u) & ~1023u;
     const uint8_t *stage_ptr = dyn_smem + (stage0 - raw);
     float *red = reinterpret_cast<float *>(dyn_smem + (stage0 - raw) + C::kStages * C::kStageBytes);
+    float *hbuf = red + kConsumerWarps * NT * 32 * 4;   // [kTok][32] h values of one item
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -136,103 +176,137 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
         abort_flag = 0;
         fence_mbar_init();
     }
+    if (warp == kProducerWarp && lane == 0)
+        for (int i = 0; i < 8; i++)
+            prefetch_tmap(&maps.m[i]);
     __syncthreads();
+    griddep_launch_dependents();
+    griddep_wait();   // routing, union and activation fragments come from the previous kernels
 
     const int n_items = (*p.n_uniq + 1) * p.tiles;
     const int nchunks = p.K / KC;
 
     if (warp == kProducerWarp) {
-        if (lane != 0)
-            return;
-        for (int i = 0; i < 8; i++)
-            prefetch_tmap(&maps.m[i]);
+        // ------------------------------------------------------- producer
         int stage = 0;
         uint32_t phase = 0;
-        int issued[C::kStages];
-        for (int s = 0; s < C::kStages; s++)
-            issued[s] = 0;
+        uint32_t issued = 0;   // bit s: stage s was filled at least once
         for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
             const Item it = decode_item(p, i);
-            const int npass = (it.m + kTokPerPass - 1) / kTokPerPass;
-            const int mbase = it.expert < 0 ? 4 : 0;   // shared expert's maps follow
+            const int npass = (it.m + C::kTok - 1) / C::kTok;
             const int z = it.expert < 0 ? 0 : it.expert;
             const int row0 = it.tile * C::kRowsPerMat;
-            for (int pass = 0; pass < npass; pass++)
+            for (int pass = 0; pass < npass; pass++) {
+                const int ntok = min(C::kTok, it.m - pass * C::kTok);
+                // lane j < ntok copies the activation data of token j of this pass
+                const int my_row = lane < ntok ? act_row<MODE>(p, it, pass * C::kTok + lane) : 0;
+                const uint16_t *my_act = p.act + (size_t)my_row * 2 * p.K;
+                const float *my_corr = p.act_corr + (size_t)my_row * (p.K / 32) * 2;
+                const float *my_fac = p.act_scale + (size_t)my_row * (p.K / 32);
+                const uint32_t tx = C::kWeightBytes + ntok * C::kTokBytes;
                 for (int c = 0; c < nchunks; c++) {
-                    if (!abort_flag) {
+                    if (!abort_flag && lane == 0) {
                         if (!mbar_wait(smem_addr(&empty_bar[stage]), phase ^ 1u)) {
                             atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                             abort_flag = 1;
                         }
                     }
+                    __syncwarp();
                     if (!abort_flag) {
                         const uint32_t sb = stage0 + stage * C::kStageBytes;
                         const uint32_t fb = smem_addr(&full_bar[stage]);
-                        mbar_arrive_expect_tx(fb, C::kStageBytes);
-                        if (MODE == kGateUp) {
-                            tma_load_3d(sb, &maps.m[mbase + 0], c * C::kRowBytes, row0, z, fb);
-                            tma_load_3d(sb + C::kQBytes, &maps.m[mbase + 1], c * C::kRowBytes, row0, z, fb);
-                            tma_load_3d(sb + 2 * C::kQBytes, &maps.m[mbase + 2], c * C::kGps, row0, z, fb);
-                            tma_load_3d(sb + 2 * C::kQBytes + C::kSBytes, &maps.m[mbase + 3], c * C::kGps,
-                                        row0, z, fb);
-                        } else {
-                            const int mb = it.expert < 0 ? 2 : 0;
-                            tma_load_3d(sb, &maps.m[mb + 0], c * C::kRowBytes, row0, z, fb);
-                            tma_load_3d(sb + C::kQBytes, &maps.m[mb + 1], c * C::kGps, row0, z, fb);
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(fb, tx);
+                            if (MODE == kGateUp) {
+                                const int mb = it.expert < 0 ? 4 : 0;   // shared expert's maps follow
+                                tma_load_3d(sb + C::kQOff, &maps.m[mb + 0], c * C::kRowBytes, row0, z, fb);
+                                tma_load_3d(sb + C::kQOff + C::kQBytes, &maps.m[mb + 1], c * C::kRowBytes,
+                                            row0, z, fb);
+                                tma_load_3d(sb + C::kSOff, &maps.m[mb + 2], c * C::kGps, row0, z, fb);
+                                tma_load_3d(sb + C::kSOff + C::kSBytes, &maps.m[mb + 3], c * C::kGps, row0,
+                                            z, fb);
+                            } else {
+                                const int mb = it.expert < 0 ? 2 : 0;
+                                tma_load_3d(sb + C::kQOff, &maps.m[mb + 0], c * C::kRowBytes, row0, z, fb);
+                                tma_load_3d(sb + C::kSOff, &maps.m[mb + 1], c * C::kGps, row0, z, fb);
+                            }
+                            issued |= 1u << stage;
                         }
-                        issued[stage] = 1;
+                        __syncwarp();   // expect_tx is posted before any copy below can complete
+                        if (lane < ntok) {
+                            const uint16_t *src = my_act + (size_t)c * KC;
+                            const uint32_t dst = sb + C::kBOff + lane * 2 * C::kPlaneBytes;
+                            bulk_load(dst, src, C::kPlaneBytes, fb);                          // hi plane
+                            bulk_load(dst + C::kPlaneBytes, src + p.K, C::kPlaneBytes, fb);     // lo plane
+                            bulk_load(sb + C::kCOff + lane * C::kCBytes, my_corr + c * C::kGps * 2,
+                                      C::kCBytes, fb);
+                            if (MODE == kDown)
+                                bulk_load(sb + C::kFOff + lane * C::kFBytes, my_fac + c * C::kGps,
+                                          C::kFBytes, fb);
+                        }
                     }
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
+            }
         }
-        // Let every copy this thread issued land before the CTA may exit.
-        // Stage s last used phase (phase of its last issue); walk back one round.
-        for (int s = 0; s < C::kStages; s++) {
-            if (!issued[s])
-                continue;
-            const uint32_t last_phase = s < stage ? phase : phase ^ 1u;
-            if (!mbar_wait(smem_addr(&full_bar[s]), last_phase))
-                atomicOr(p.err, MOE_DEVERR_TIMEOUT);
+        // Let every copy issued here land before the CTA may exit: stages below
+        // `stage` were last filled in the current round, the rest in the
+        // previous one.
+        if (lane == 0) {
+            for (int s = 0; s < C::kStages; s++) {
+                if (!((issued >> s) & 1u))
+                    continue;
+                const uint32_t last_phase = s < stage ? phase : phase ^ 1u;
+                if (!mbar_wait(smem_addr(&full_bar[s]), last_phase))
+                    atomicOr(p.err, MOE_DEVERR_TIMEOUT);
+            }
         }
         return;
     }
 
     // ------------------------------------------------------------ consumers
+    // warp -> (matrix, 16-row m-tile, k-half of every stage)
     const int mt = warp & 3, khalf = warp >> 2;
     const int mat = MODE == kGateUp ? (mt >> 1) : 0;
     const int mtile = MODE == kGateUp ? (mt & 1) : mt;
     const int g = lane >> 2, t4 = lane & 3;
-    const int ra = mtile * 16 + g, rb = ra + 8;
-    const uint32_t q_off_a = mat * C::kQBytes + ra * C::kRowBytes + 4 * t4;
-    const uint32_t q_off_b = mat * C::kQBytes + rb * C::kRowBytes + 4 * t4;
-    const uint32_t s_off = C::kMats * C::kQBytes + mat * C::kSBytes;
-    const int swa = swz<KC>(ra), swb = swz<KC>(rb);
+    const int ra = mtile * 16 + g;   // and ra + 8: same swizzle phase
+    uint32_t qoff[C::kGph];          // byte offset of this lane's word of row ra, per group of the k-half
+#pragma unroll
+    for (int gi = 0; gi < C::kGph; gi++) {
+        const int gl = khalf * C::kGph + gi;
+        qoff[gi] = C::kQOff + mat * C::kQBytes + ra * C::kRowBytes + ((gl ^ swz<KC>(ra)) << 4) + 4 * t4;
+    }
+    constexpr uint32_t kRowB = 8 * C::kRowBytes;
+    const uint32_t soff_a = C::kSOff + mat * C::kSBytes + (ra * C::kGps + khalf * C::kGph) * 4;
+    const uint32_t soff_b = soff_a + 8 * C::kGps * 4;
     int stage = 0;
     uint32_t phase = 0;
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    constexpr float kTwo24 = 16777216.0f;
+    const NibConst nk = {0x000F000Fu, 0x00080008u, 0x00F000F0u, 0x00800080u};
 
     for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
         const Item it = decode_item(p, i);
-        const int npass = (it.m + kTokPerPass - 1) / kTokPerPass;
+        const int npass = (it.m + C::kTok - 1) / C::kTok;
         for (int pass = 0; pass < npass; pass++) {
-            // activation rows feeding this lane's B column in each n-tile
-            const uint4 *brow[NT];
+            const int ntok = min(C::kTok, it.m - pass * C::kTok);
+            // stage offsets of this lane's B chunk (token g/2 of each n-tile, plane g&1) and of the
+            // corrections / factors of the token whose D columns it holds (token t4); tokens past
+            // ntok read token 0's data (finite, discarded)
+            uint32_t boff[NT], coff[NT], foff[NT];
 #pragma unroll
             for (int n = 0; n < NT; n++) {
-                const int tt = pass * kTokPerPass + n * 4 + (g >> 1);
-                brow[n] = nullptr;
-                if (tt < it.m) {
-                    int row;
-                    if (MODE == kGateUp)
-                        row = it.expert < 0 ? tt : p.sorted_pair[it.pos0 + tt] / p.k;
-                    else
-                        row = it.expert < 0 ? p.T * p.k + tt : it.pos0 + tt;
-                    brow[n] = reinterpret_cast<const uint4 *>(p.act + (size_t)row * 2 * p.K +
-                                                              (size_t)(g & 1) * p.K) + t4;
-                }
+                int jb = n * 4 + (g >> 1);
+                jb = jb < ntok ? jb : 0;
+                boff[n] = C::kBOff + (jb * 2 + (g & 1)) * C::kPlaneBytes + (khalf * C::kGph * 4 + t4) * 16;
+                int jd = n * 4 + t4;
+                jd = jd < ntok ? jd : 0;
+                coff[n] = C::kCOff + jd * C::kCBytes + khalf * C::kGph * 8;
+                foff[n] = C::kFOff + jd * C::kFBytes + khalf * C::kGph * 4;
             }
             float acc[NT][4];
 #pragma unroll
@@ -252,36 +326,32 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
                 __syncwarp();
                 if (!abort_flag) {
                     const uint8_t *sb = stage_ptr + stage * C::kStageBytes;
-                    const float *sc = reinterpret_cast<const float *>(sb + s_off);
 #pragma unroll
                     for (int gi = 0; gi < C::kGph; gi++) {
-                        const int gl = khalf * C::kGph + gi;
-                        const uint32_t wa = *reinterpret_cast<const uint32_t *>(sb + q_off_a + ((gl ^ swa) << 4));
-                        const uint32_t wb = *reinterpret_cast<const uint32_t *>(sb + q_off_b + ((gl ^ swb) << 4));
-                        const float sa = sc[ra * C::kGps + gl];
-                        const float sbv = sc[rb * C::kGps + gl];
-                        uint32_t a0[4], a1[4];
-                        a0[0] = nib2_to_bf16x2(wa);
-                        a0[1] = nib2_to_bf16x2(wb);
-                        a0[2] = nib2_to_bf16x2(wa >> 4);
-                        a0[3] = nib2_to_bf16x2(wb >> 4);
-                        a1[0] = nib2_to_bf16x2(wa >> 8);
-                        a1[1] = nib2_to_bf16x2(wb >> 8);
-                        a1[2] = nib2_to_bf16x2(wa >> 12);
-                        a1[3] = nib2_to_bf16x2(wb >> 12);
-                        const int gg = c * C::kGps + gl;
+                        const uint32_t wa = *reinterpret_cast<const uint32_t *>(sb + qoff[gi]);
+                        const uint32_t wb = *reinterpret_cast<const uint32_t *>(sb + qoff[gi] + kRowB);
+                        const float sa = reinterpret_cast<const float *>(sb + soff_a)[gi];
+                        const float sbv = reinterpret_cast<const float *>(sb + soff_b)[gi];
+                        const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+                        const uint32_t a0[4] = {nib_lo(wa, nk), nib_lo(wb, nk), nib_hi(wa, nk), nib_hi(wb, nk)};
+                        const uint32_t a1[4] = {nib_lo(wa8, nk), nib_lo(wb8, nk), nib_hi(wa8, nk), nib_hi(wb8, nk)};
 #pragma unroll
                         for (int n = 0; n < NT; n++) {
-                            uint4 bv = make_uint4(0u, 0u, 0u, 0u);
-                            if (brow[n])
-                                bv = __ldg(brow[n] + gg * 4);
+                            const uint4 bv = *reinterpret_cast<const uint4 *>(sb + boff[n] + gi * 64);
+                            const float2 cc = *reinterpret_cast<const float2 *>(sb + coff[n] + gi * 8);
                             float d[4];
-                            mma_bf16_16816(d, a0, bv.x, bv.y, zero4);
-                            mma_bf16_16816(d, a1, bv.z, bv.w, d);
-                            acc[n][0] = fmaf(sa, d[0], acc[n][0]);
-                            acc[n][1] = fmaf(sa, d[1], acc[n][1]);
-                            acc[n][2] = fmaf(sbv, d[2], acc[n][2]);
-                            acc[n][3] = fmaf(sbv, d[3], acc[n][3]);
+                            mma_f16_16816(d, a0, bv.x, bv.y, zero4);
+                            mma_f16_16816(d, a1, bv.z, bv.w, d);
+                            float fa = sa, fb = sbv;
+                            if (MODE == kDown) {
+                                const float hf = reinterpret_cast<const float *>(sb + foff[n])[gi];
+                                fa *= hf;
+                                fb *= hf;
+                            }
+                            acc[n][0] = fmaf(fa, fmaf(d[0], kTwo24, -cc.x), acc[n][0]);
+                            acc[n][1] = fmaf(fa, fmaf(d[1], kTwo24, -cc.y), acc[n][1]);
+                            acc[n][2] = fmaf(fb, fmaf(d[2], kTwo24, -cc.x), acc[n][2]);
+                            acc[n][3] = fmaf(fb, fmaf(d[3], kTwo24, -cc.y), acc[n][3]);
                         }
                     }
                 }
@@ -294,7 +364,7 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
                 }
             }
 
-            // ---- epilogue: reduce the two k-halves, then SwiGLU or store y
+            // ---- epilogue: reduce the two k-halves, then SwiGLU (+ fragments) or store y
             float4 *my_red = reinterpret_cast<float4 *>(red) + (warp * NT) * 32 + lane;
 #pragma unroll
             for (int n = 0; n < NT; n++)
@@ -302,49 +372,78 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
             named_bar_sync(1, kConsumerWarps * 32);
             const float4 *R = reinterpret_cast<const float4 *>(red);
             auto part = [&](int w, int n) { return R[(w * NT + n) * 32 + lane]; };
-            if (!abort_flag) {
-                if (MODE == kGateUp && (warp == 2 || warp == 3)) {
-                    // up warps of k-half 0 finish rows 16*mtile + g (+8)
-                    const int f = p.out_rows;
+            if (MODE == kGateUp) {
+                if (!abort_flag && (warp == 2 || warp == 3)) {
+                    // up warps of k-half 0: h for rows 16*mtile + g (+8), token t4 of each n-tile
 #pragma unroll
                     for (int n = 0; n < NT; n++) {
-                        const int tt = pass * kTokPerPass + n * 4 + t4;
-                        if (tt >= it.m)
+                        const int tl = n * 4 + t4;
+                        if (tl >= ntok)
                             continue;
+                        const float xf = p.act_scale[act_row<MODE>(p, it, pass * C::kTok + tl)];
                         const float4 g0 = part(warp - 2, n), g1 = part(warp + 2, n);
                         const float4 u0 = part(warp, n), u1 = part(warp + 4, n);
-                        const float gva = (g0.x + g1.x) + (g0.y + g1.y);
-                        const float gvb = (g0.z + g1.z) + (g0.w + g1.w);
-                        const float uva = (u0.x + u1.x) + (u0.y + u1.y);
-                        const float uvb = (u0.z + u1.z) + (u0.w + u1.w);
-                        const float ha = gva / (1.0f + expf(-gva)) * uva;
-                        const float hb = gvb / (1.0f + expf(-gvb)) * uvb;
+                        const float gva = ((g0.x + g1.x) + (g0.y + g1.y)) * xf;
+                        const float gvb = ((g0.z + g1.z) + (g0.w + g1.w)) * xf;
+                        const float uva = ((u0.x + u1.x) + (u0.y + u1.y)) * xf;
+                        const float uvb = ((u0.z + u1.z) + (u0.w + u1.w)) * xf;
+                        hbuf[tl * 32 + mtile * 16 + g] = gva / (1.0f + expf(-gva)) * uva;
+                        hbuf[tl * 32 + mtile * 16 + g + 8] = gvb / (1.0f + expf(-gvb)) * uvb;
+                    }
+                }
+                named_bar_sync(1, kConsumerWarps * 32);
+                // one warp per token: the item's 32 rows form one group of the down input
+                if (!abort_flag) {
+                    const int f = p.out_rows;
+                    for (int tl = warp; tl < ntok; tl += kConsumerWarps) {
+                        const int tt = pass * C::kTok + tl;
+                        float v = hbuf[tl * 32 + lane];
+                        float mx = fabsf(v);
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                        int e = 0;
+                        frexpf(mx, &e);
+                        const float up = mx > 0.f ? ldexpf(1.0f, 14 - e) : 1.0f;
+                        v *= up;
+                        if (lane & 1)
+                            v *= 0.0625f;
+                        const __half hi = __float2half_rn(v);
+                        const __half lo = __float2half_rn(v - __half2float(hi));
+                        const float wgt = (lane & 1) ? 128.0f : 8.0f;
+                        float chi = wgt * __half2float(hi), clo = wgt * __half2float(lo);
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1) {
+                            chi += __shfl_xor_sync(0xffffffffu, chi, off);
+                            clo += __shfl_xor_sync(0xffffffffu, clo, off);
+                        }
                         const int pos = it.expert < 0 ? p.T * p.k + tt : it.pos0 + tt;
                         uint16_t *hrow = p.h_out + (size_t)pos * 2 * f;
-                        const int grp = it.tile;                 // 32 rows = one group of the down input
-                        const int ia = (grp * 4 + 2 * mtile) * 8 + frag_pos(g);
-                        const int ib = ia + 8;                   // row + 8 -> next quad
-                        const __nv_bfloat16 ha_hi = __float2bfloat16_rn(ha);
-                        const __nv_bfloat16 hb_hi = __float2bfloat16_rn(hb);
-                        hrow[ia] = __bfloat16_as_ushort(ha_hi);
-                        hrow[ib] = __bfloat16_as_ushort(hb_hi);
-                        hrow[f + ia] = __bfloat16_as_ushort(__float2bfloat16_rn(ha - __bfloat162float(ha_hi)));
-                        hrow[f + ib] = __bfloat16_as_ushort(__float2bfloat16_rn(hb - __bfloat162float(hb_hi)));
+                        const int idx = (it.tile * 4 + (lane >> 3)) * 8 + frag_pos(lane & 7);
+                        hrow[idx] = __half_as_ushort(hi);
+                        hrow[f + idx] = __half_as_ushort(lo);
+                        if (lane == 0) {
+                            const size_t gidx = (size_t)pos * (f / 32) + it.tile;
+                            p.h_scale[gidx] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
+                            p.h_corr[gidx * 2 + 0] = chi;
+                            p.h_corr[gidx * 2 + 1] = clo;
+                        }
                     }
-                } else if (MODE == kDown && warp < 4) {
-                    const int d = p.out_rows;
-                    const int row_a = it.tile * 64 + mtile * 16 + g;
+                }
+            } else if (!abort_flag && warp < 4) {
+                const int d = p.out_rows;
+                const int row_a = it.tile * 64 + mtile * 16 + g;
 #pragma unroll
-                    for (int n = 0; n < NT; n++) {
-                        const int tt = pass * kTokPerPass + n * 4 + t4;
-                        if (tt >= it.m)
-                            continue;
-                        const float4 y0 = part(warp, n), y1 = part(warp + 4, n);
-                        float *yrow = it.expert < 0 ? p.y_shared + (size_t)tt * d
-                                                    : p.y_pair + (size_t)(it.pos0 + tt) * d;
-                        yrow[row_a] = (y0.x + y1.x) + (y0.y + y1.y);
-                        yrow[row_a + 8] = (y0.z + y1.z) + (y0.w + y1.w);
-                    }
+                for (int n = 0; n < NT; n++) {
+                    const int tl = n * 4 + t4;
+                    if (tl >= ntok)
+                        continue;
+                    const int tt = pass * C::kTok + tl;
+                    const float4 y0 = part(warp, n), y1 = part(warp + 4, n);
+                    float *yrow = it.expert < 0 ? p.y_shared + (size_t)tt * d
+                                                : p.y_pair + (size_t)(it.pos0 + tt) * d;
+                    yrow[row_a] = (y0.x + y1.x) + (y0.y + y1.y);
+                    yrow[row_a + 8] = (y0.z + y1.z) + (y0.w + y1.w);
                 }
             }
             named_bar_sync(1, kConsumerWarps * 32);
@@ -355,8 +454,9 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
 template <int MODE, int NT, int KC>
 int launch_one(const Maps &maps, const Params &prm, int max_items, cudaStream_t s)
 {
-    using C = Cfg<MODE, KC>;
-    const size_t smem = 1024 + (size_t)C::kStages * C::kStageBytes + (size_t)kConsumerWarps * NT * 32 * 16;
+    using C = Cfg<MODE, NT, KC>;
+    const size_t smem = 1024 + (size_t)C::kStages * C::kStageBytes + (size_t)kConsumerWarps * NT * 32 * 16 +
+                        (size_t)C::kTok * 32 * 4;
     auto kern = ffn_decode_kernel<MODE, NT, KC>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
@@ -377,8 +477,7 @@ int launch_one(const Maps &maps, const Params &prm, int max_items, cudaStream_t 
         grid = max_items;
     if (grid < 1)
         grid = 1;
-    kern<<<grid, kThreads, smem, s>>>(maps, prm);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(kern, grid, kThreads, smem, s, maps, prm);
 }
 
 template <int MODE, int KC>
@@ -433,7 +532,11 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
     pg.uniq = a.uniq;
     pg.n_uniq = a.n_uniq;
     pg.act = a.x_frag;
+    pg.act_scale = a.x_scale;
+    pg.act_corr = a.x_corr;
     pg.h_out = a.h_frag;
+    pg.h_scale = a.h_scale;
+    pg.h_corr = a.h_corr;
     pg.err = a.err;
     pg.T = a.T;
     pg.k = a.k;
@@ -457,7 +560,11 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
         return MOE_ERR_INVALID_ARG;
     Params pd = pg;
     pd.act = a.h_frag;
+    pd.act_scale = a.h_scale;
+    pd.act_corr = a.h_corr;
     pd.h_out = nullptr;
+    pd.h_scale = nullptr;
+    pd.h_corr = nullptr;
     pd.y_pair = a.y_pair;
     pd.y_shared = a.y_shared;
     pd.K = f;

@@ -42,20 +42,31 @@ int resolve_mode(int mode, int T)
     return mode;
 }
 
-// Scratch of the decode FFN: activation fragments of x and of h.
+// Scratch of the decode FFN: activation fragments of x and of h, their
+// factors and bias corrections.
 struct FfnScratch {
     uint16_t *x_frag, *h_frag;
+    float *x_scale, *h_scale, *x_corr, *h_corr;
 };
 
 size_t ffn_scratch_layout(int T, int k, int d, int f, uint8_t *base, FfnScratch *out)
 {
     size_t off = 0;
-    const size_t x_bytes = (size_t)T * 2 * d * sizeof(uint16_t);
-    const size_t h_bytes = ((size_t)T * k + T) * 2 * f * sizeof(uint16_t);
-    if (out) out->x_frag = reinterpret_cast<uint16_t *>(base + off);
-    off = align_up(off + x_bytes);
-    if (out) out->h_frag = reinterpret_cast<uint16_t *>(base + off);
-    off = align_up(off + h_bytes);
+    const size_t rows_h = (size_t)T * k + T;
+    auto take = [&](size_t bytes) {
+        uint8_t *p = base ? base + off : nullptr;
+        off = align_up(off + bytes);
+        return p;
+    };
+    FfnScratch s{};
+    s.x_frag = reinterpret_cast<uint16_t *>(take((size_t)T * 2 * d * sizeof(uint16_t)));
+    s.x_scale = reinterpret_cast<float *>(take((size_t)T * sizeof(float)));
+    s.x_corr = reinterpret_cast<float *>(take((size_t)T * (d / 32) * 2 * sizeof(float)));
+    s.h_frag = reinterpret_cast<uint16_t *>(take(rows_h * 2 * f * sizeof(uint16_t)));
+    s.h_scale = reinterpret_cast<float *>(take(rows_h * (f / 32) * sizeof(float)));
+    s.h_corr = reinterpret_cast<float *>(take(rows_h * (f / 32) * 2 * sizeof(float)));
+    if (out)
+        *out = s;
     return off;
 }
 
@@ -188,7 +199,7 @@ int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *
     FfnScratch sc{};
     ffn_scratch_layout(T, k, w->d, w->f, static_cast<uint8_t *>(workspace), &sc);
     const cudaStream_t s = as_stream(stream);
-    rc = launch_act_frag(x, T, w->d, sc.x_frag, s);
+    rc = launch_act_frag(x, T, w->d, sc.x_frag, sc.x_scale, sc.x_corr, s);
     if (rc != MOE_OK)
         return rc;
     DecodeFfnArgs a{};
@@ -200,7 +211,11 @@ int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *
     a.T = T;
     a.k = k;
     a.x_frag = sc.x_frag;
+    a.x_scale = sc.x_scale;
+    a.x_corr = sc.x_corr;
     a.h_frag = sc.h_frag;
+    a.h_scale = sc.h_scale;
+    a.h_corr = sc.h_corr;
     a.y_pair = y_pair;
     a.y_shared = y_shared;
     a.err = err;
@@ -260,7 +275,7 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
         return rc;
     FfnScratch fs{};
     ffn_scratch_layout(T, k, d, f, sc.ffn, &fs);
-    rc = launch_act_frag(x, T, d, fs.x_frag, s);
+    rc = launch_act_frag(x, T, d, fs.x_frag, fs.x_scale, fs.x_corr, s);
     if (rc != MOE_OK)
         return rc;
     DecodeFfnArgs a{};
@@ -272,7 +287,11 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
     a.T = T;
     a.k = k;
     a.x_frag = fs.x_frag;
+    a.x_scale = fs.x_scale;
+    a.x_corr = fs.x_corr;
     a.h_frag = fs.h_frag;
+    a.h_scale = fs.h_scale;
+    a.h_corr = fs.h_corr;
     a.y_pair = sc.y_pair;
     a.y_shared = sc.y_shared;
     a.err = err;

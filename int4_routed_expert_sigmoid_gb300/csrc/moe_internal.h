@@ -12,25 +12,53 @@ namespace moe {
 
 // ---------------------------------------------------------------------------
 // Activation fragment layout ("frag"): the B operand of the decode FFN's
-// m16n8k16 MMAs, precomputed once per activation row.
+// m16n8k16 fp16 MMAs, precomputed once per activation row.
 //
-// A row of K fp32 values v becomes two planes (hl = 0: hi = bf16(v),
-// hl = 1: lo = bf16(v - hi)), each [K/32 groups][4 quads][8 bf16].  Quad t of
-// group g holds elements 32g + 8t + kFragPerm[i], i = 0..7, kFragPerm =
-// {0,4,1,5,2,6,3,7}: the order in which the MMA's k index meets the nibbles of
-// a packed 32-bit weight word (see ffn_decode.cu).  Row stride = 2*K bf16.
+// A row of K fp32 values, scaled by a power of two (per row for x, per
+// 32-element group for h; the inverse is kept in a factor array) so that
+// |v| < 2^14, becomes two planes (hi = fp16(v), lo = fp16(v - hi)), each
+// [K/32 groups][4 quads][8 fp16]; row stride 2*K.  Quad t of group g holds
+// elements 32g + 8t + o at position frag_pos(o), o = 0..7, i.e. in the order
+// {0,4,1,5,2,6,3,7}: the order in which the MMA's k index meets the nibbles
+// of a packed 32-bit weight word.  Elements with odd o are stored divided by
+// 16, because their weights enter the MMA multiplied by 16.
+//
+// The weights enter the MMA as fp16 subnormals (q + 8) * 2^-24 (times 16 at
+// odd o), so a group's MMA sum is 2^-24 * (sum q v + corr / 1), where
+// corr = 8 * sum_k w_k B_k (w_k = 16 at odd o, else 1; B the stored fp16
+// values) is kept per (row, group, plane) in fp32 and subtracted exactly.
 // ---------------------------------------------------------------------------
 __host__ __device__ constexpr int frag_pos(int o) { return 2 * (o & 3) + (o >> 2); }
 
 // Error propagation helper for launchers.
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream finishes; it must execute
+// griddepcontrol.wait before it reads that kernel's results.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStream_t s, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...));
+}
+
 // router.cu
 int launch_router_logits(const float *x, const float *wg, int T, int d, int E, float *logits,
                          cudaStream_t s);
 int launch_router_topk(const float *logits, const float *bias, int T, int E, int k, int normalize,
                        float route_scale, int32_t *idx, float *w, cudaStream_t s);
-int launch_act_frag(const float *x, int rows, int K, uint16_t *frag, cudaStream_t s);
+int launch_act_frag(const float *x, int rows, int K, uint16_t *frag, float *row_scale, float *corr,
+                    cudaStream_t s);
 
 // union.cu
 int launch_union(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
@@ -43,8 +71,12 @@ struct DecodeFfnArgs {
     const moe_layer_int4 *w;
     const int32_t *offsets, *sorted_pair, *uniq, *n_uniq;
     int T, k;
-    const uint16_t *x_frag;   // [T][2*d] bf16 frag layout
-    uint16_t *h_frag;         // [T*k + T][2*f] bf16 frag layout (scratch)
+    const uint16_t *x_frag;   // [T][2*d] fp16 frag layout
+    const float *x_scale;     // [T] per-row factor of x_frag
+    const float *x_corr;      // [T][d/32][2] bias corrections of x_frag
+    uint16_t *h_frag;         // [T*k + T][2*f] fp16 frag layout (scratch)
+    float *h_scale;           // [T*k + T][f/32] per-group factor of h_frag (scratch)
+    float *h_corr;            // [T*k + T][f/32][2] bias corrections of h_frag (scratch)
     float *y_pair, *y_shared;
     int32_t *err;
 };

@@ -5,7 +5,7 @@
 // and Data-Flow Reconstruction": a trained sigmoid gate (n_group = 1, fp32
 // parameters) scores every expert of the layer for each token and the top
 // experts are selected.
-#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cfloat>
 #include <climits>
 
@@ -205,31 +205,77 @@ topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, in
 }
 
 // --------------------------------------------------------- act fragments ---
-// One thread per (row, group, quad): 8 fp32 -> hi/lo bf16 in fragment order.
-__global__ void act_frag_kernel(const float *__restrict__ x, int rows, int K,
-                                uint16_t *__restrict__ frag)
+// One CTA per row: the row's max |x| picks a power of two 2^(14-e) that brings
+// every element below 2^14 (exact scaling); elements at odd offsets within
+// each 8 are further divided by 16.  Each value becomes hi = fp16(v),
+// lo = fp16(v - hi); row_scale[r] = 2^(e-14) undoes the scaling and
+// corr[r][g][plane] = 8 * sum (16 at odd offsets, else 1) * stored value.
+constexpr int kFragThreads = 256;
+
+__global__ void __launch_bounds__(kFragThreads)
+act_frag_kernel(const float *__restrict__ x, int K, uint16_t *__restrict__ frag,
+                float *__restrict__ row_scale, float *__restrict__ corr)
 {
-    const int groups = K / 32;
-    const long long id = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (id >= (long long)rows * groups * 4)
-        return;
-    const int q = (int)(id & 3);
-    const int g = (int)((id >> 2) % groups);
-    const int r = (int)(id / (4LL * groups));
-    const float4 *src = reinterpret_cast<const float4 *>(x + (size_t)r * K + 32 * g + 8 * q);
-    const float4 v0 = src[0], v1 = src[1];
-    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    __align__(16) uint16_t hi[8], lo[8];
-#pragma unroll
-    for (int o = 0; o < 8; o++) {
-        const __nv_bfloat16 h = __float2bfloat16_rn(v[o]);
-        const __nv_bfloat16 l = __float2bfloat16_rn(v[o] - __bfloat162float(h));
-        hi[frag_pos(o)] = __bfloat16_as_ushort(h);
-        lo[frag_pos(o)] = __bfloat16_as_ushort(l);
+    __shared__ float wmax[kFragThreads / 32];
+    const int r = blockIdx.x;
+    const float *xr = x + (size_t)r * K;
+    float mx = 0.f;
+    for (int i = threadIdx.x; i < K / 4; i += kFragThreads) {
+        const float4 v = reinterpret_cast<const float4 *>(xr)[i];
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if ((threadIdx.x & 31) == 0)
+        wmax[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < kFragThreads / 32; w++)
+        mx = fmaxf(mx, wmax[w]);
+    int e = 0;
+    frexpf(mx, &e);
+    const float up = mx > 0.f ? ldexpf(1.0f, 14 - e) : 1.0f;
+    if (threadIdx.x == 0)
+        row_scale[r] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
     uint16_t *row = frag + (size_t)r * 2 * K;
-    *reinterpret_cast<uint4 *>(row + (size_t)(g * 4 + q) * 8) = *reinterpret_cast<const uint4 *>(hi);
-    *reinterpret_cast<uint4 *>(row + K + (size_t)(g * 4 + q) * 8) = *reinterpret_cast<const uint4 *>(lo);
+    const int n = (K / 32) * 4;                       // (group, quad) pairs; quads of a group are adjacent ids
+    const int n_pad = (n + 31) / 32 * 32;             // whole warps take part in the shuffles
+    for (int id = threadIdx.x; id < n_pad; id += kFragThreads) {
+        const bool act = id < n;
+        const int g = id >> 2, q = id & 3;
+        float chi = 0.f, clo = 0.f;
+        if (act) {
+            const float4 *src = reinterpret_cast<const float4 *>(xr + 32 * g + 8 * q);
+            const float4 v0 = src[0], v1 = src[1];
+            const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            __align__(16) uint16_t hi[8], lo[8];
+#pragma unroll
+            for (int o = 0; o < 8; o++) {
+                float sv = v[o] * up;
+                if (o & 1)
+                    sv *= 0.0625f;
+                const __half h = __float2half_rn(sv);
+                const __half l = __float2half_rn(sv - __half2float(h));
+                hi[frag_pos(o)] = __half_as_ushort(h);
+                lo[frag_pos(o)] = __half_as_ushort(l);
+                const float wgt = (o & 1) ? 128.0f : 8.0f;
+                chi += wgt * __half2float(h);
+                clo += wgt * __half2float(l);
+            }
+            *reinterpret_cast<uint4 *>(row + (size_t)id * 8) = *reinterpret_cast<const uint4 *>(hi);
+            *reinterpret_cast<uint4 *>(row + K + (size_t)id * 8) = *reinterpret_cast<const uint4 *>(lo);
+        }
+        chi += __shfl_xor_sync(0xffffffffu, chi, 1);
+        clo += __shfl_xor_sync(0xffffffffu, clo, 1);
+        chi += __shfl_xor_sync(0xffffffffu, chi, 2);
+        clo += __shfl_xor_sync(0xffffffffu, clo, 2);
+        if (act && q == 0) {
+            corr[((size_t)r * (K / 32) + g) * 2 + 0] = chi;
+            corr[((size_t)r * (K / 32) + g) * 2 + 1] = clo;
+        }
+    }
 }
 
 }  // namespace
@@ -264,12 +310,12 @@ int launch_router_topk(const float *logits, const float *bias, int T, int E, int
     return cuda_status(cudaGetLastError());
 }
 
-int launch_act_frag(const float *x, int rows, int K, uint16_t *frag, cudaStream_t s)
+int launch_act_frag(const float *x, int rows, int K, uint16_t *frag, float *row_scale, float *corr,
+                    cudaStream_t s)
 {
-    const long long n = (long long)rows * (K / 32) * 4;
-    if (n == 0)
+    if (rows <= 0)
         return MOE_OK;
-    act_frag_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(x, rows, K, frag);
+    act_frag_kernel<<<rows, kFragThreads, 0, s>>>(x, K, frag, row_scale, corr);
     return cuda_status(cudaGetLastError());
 }
 
