@@ -221,7 +221,16 @@ def run_ours(args, rank, world, local):
     outs = torch.empty((S, T, d), dtype=torch.float32, device=dev)
     ws = moe.workspace(moe.ffn_workspace_bytes(T, k, d, f, moe.MOE_MODE_DECODE), dev)
 
+    lws_step = moe.workspace(moe.layer_workspace_bytes(T, k, E, d, f, moe.MOE_MODE_DECODE), dev)
+
+    def layer_step(i):
+        """One step through the public fused entry point (the timed path)."""
+        r = i % R
+        moe.moe_layer_forward(xs[i % S], wgs[r], biases[r], layers[r], k, 1, 1.0, mode=moe.MOE_MODE_DECODE,
+                              out=outs[i % S], topk_idx=idx, topk_w=wts, hits=hits[r], ws=lws_step, err=err)
+
     def step(i, ev=None):
+        """The same step through the separate stage calls, with events between stages."""
         r = i % R
         x = xs[i % S]
         if ev:
@@ -240,7 +249,9 @@ def run_ours(args, rank, world, local):
         if ev:
             ev[4].record()
 
-    launches_per_step = 7   # logits, top-k, union, act fragments, gate/up, down, combine
+    # kernels per fused step: small batches logits(+x fragments), select+union, gate/up, down,
+    # combine; otherwise logits, top-k, union, x fragments, gate/up, down, combine
+    launches_per_step = 5 if (T <= 8 and T * k <= 64) else 7
 
     # warm the code paths once outside capture, then capture
     side = torch.cuda.Stream(device=dev)
@@ -248,6 +259,7 @@ def run_ours(args, rank, world, local):
     with torch.cuda.stream(side):
         for i in range(min(S, 2 * R)):
             step(i)
+            layer_step(i)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
 
@@ -258,10 +270,14 @@ def run_ours(args, rank, world, local):
             if with_events else None
         with torch.cuda.graph(g, capture_error_mode="thread_local"):
             for i in range(n):
-                step(i, evs[i] if evs else None)
+                if with_events:
+                    step(i, evs[i])
+                else:
+                    layer_step(i)
         return g, evs
 
-    g_main, evs = capture(S, True)
+    g_main, _ = capture(S, False)
+    g_stages, evs = capture(S, True)
     tail = args.steps % S
     g_tail = capture(tail, False)[0] if tail else None
     n_main = args.steps // S
@@ -291,7 +307,11 @@ def run_ours(args, rank, world, local):
     elapsed_ms = t0.elapsed_time(t1)
     dev_err = int(err.item())
 
-    # stage durations of the last replay of the main graph (S steps, inside the timed region)
+    # stage durations: the same S steps through the separate stage calls, replayed right after the
+    # timed region (events between stages; the fused path has no stage boundaries to time)
+    g_stages.replay()
+    g_stages.replay()
+    torch.cuda.synchronize()
     st = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)] for i in range(S)])
     stage_ms = st.mean(axis=0)
     n_uniq = int(un["n_uniq"].item())

@@ -5,6 +5,7 @@
 // Revision Ledger", "Exact Architecture and Data-Flow Reconstruction" (selected
 // experts weighted by the router; the shared branch is always used).
 #include "moe_internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -15,6 +16,8 @@ combine_kernel(const float4 *__restrict__ y_pair, const float4 *__restrict__ y_s
                const float *__restrict__ w, const int32_t *__restrict__ perm,
                const float4 *res, int T, int k, int d4, float4 *out)
 {
+    griddep_launch_dependents();
+    griddep_wait();   // y_pair / y_shared come from the previous kernel
     const long long id = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (id >= (long long)T * d4)
         return;
@@ -43,10 +46,9 @@ int launch_combine(const float *y_pair, const float *y_shared, const float *w, c
 {
     const int d4 = d / 4;
     const long long n = (long long)T * d4;
-    combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
-        reinterpret_cast<const float4 *>(y_pair), reinterpret_cast<const float4 *>(y_shared), w,
-        perm, reinterpret_cast<const float4 *>(res), T, k, d4, reinterpret_cast<float4 *>(out));
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(combine_kernel, (int)((n + 255) / 256), 256, 0, s,
+                      reinterpret_cast<const float4 *>(y_pair), reinterpret_cast<const float4 *>(y_shared), w,
+                      perm, reinterpret_cast<const float4 *>(res), T, k, d4, reinterpret_cast<float4 *>(out));
 }
 
 }  // namespace moe

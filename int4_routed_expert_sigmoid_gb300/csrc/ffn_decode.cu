@@ -49,14 +49,15 @@ constexpr int kProducerWarp = kConsumerWarps;
 
 enum { kGateUp = 0, kDown = 1 };
 
-template <int MODE, int NT, int KC>
+// TOK: tokens per pass (1, 4, 8 or 16); NT = ceil(TOK / 4) MMA n-tiles of 4 tokens (hi + lo columns).
+template <int MODE, int TOK, int KC>
 struct Cfg {
     static constexpr int kRowsPerMat = MODE == kGateUp ? 32 : 64;   // output rows per item
     static constexpr int kMats = MODE == kGateUp ? 2 : 1;
     static constexpr int kRowBytes = KC / 2;                        // packed bytes per row per stage
     static constexpr int kGps = KC / 32;                            // scale groups per stage
     static constexpr int kGph = kGps / 2;                           // groups per k-half
-    static constexpr int kTok = 4 * NT;                             // tokens per pass
+    static constexpr int kTok = TOK;                                // tokens per pass
     static constexpr int kQBytes = kRowsPerMat * kRowBytes;         // per matrix
     static constexpr int kSBytes = kRowsPerMat * kGps * 4;          // per matrix
     static constexpr int kPlaneBytes = kGps * 64;                   // one token's hi (or lo) chunk
@@ -151,11 +152,12 @@ __device__ __forceinline__ int act_row(const Params &p, const Item &it, int tt)
     return it.expert < 0 ? p.T * p.k + tt : it.pos0 + tt;
 }
 
-template <int MODE, int NT, int KC>
+template <int MODE, int TOK, int KC>
 __global__ void __launch_bounds__(kThreads, 2)
 ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
 {
-    using C = Cfg<MODE, NT, KC>;
+    using C = Cfg<MODE, TOK, KC>;
+    constexpr int NT = (TOK + 3) / 4;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t full_bar[C::kStages];
     __shared__ __align__(8) uint64_t empty_bar[C::kStages];
@@ -451,13 +453,14 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
     }
 }
 
-template <int MODE, int NT, int KC>
+template <int MODE, int TOK, int KC>
 int launch_one(const Maps &maps, const Params &prm, int max_items, cudaStream_t s)
 {
-    using C = Cfg<MODE, NT, KC>;
+    using C = Cfg<MODE, TOK, KC>;
+    constexpr int NT = (TOK + 3) / 4;
     const size_t smem = 1024 + (size_t)C::kStages * C::kStageBytes + (size_t)kConsumerWarps * NT * 32 * 16 +
                         (size_t)C::kTok * 32 * 4;
-    auto kern = ffn_decode_kernel<MODE, NT, KC>;
+    auto kern = ffn_decode_kernel<MODE, TOK, KC>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return MOE_ERR_CUDA;
@@ -483,11 +486,13 @@ int launch_one(const Maps &maps, const Params &prm, int max_items, cudaStream_t 
 template <int MODE, int KC>
 int launch_nt(const Maps &maps, const Params &prm, int max_items, int T, cudaStream_t s)
 {
-    if (T <= 4)
+    if (T == 1)
         return launch_one<MODE, 1, KC>(maps, prm, max_items, s);
+    if (T <= 4)
+        return launch_one<MODE, 4, KC>(maps, prm, max_items, s);
     if (T <= 8)
-        return launch_one<MODE, 2, KC>(maps, prm, max_items, s);
-    return launch_one<MODE, 4, KC>(maps, prm, max_items, s);
+        return launch_one<MODE, 8, KC>(maps, prm, max_items, s);
+    return launch_one<MODE, 16, KC>(maps, prm, max_items, s);
 }
 
 }  // namespace

@@ -265,17 +265,27 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
     int32_t *idx = topk_idx ? topk_idx : sc.idx;
     float *wt = topk_w ? topk_w : sc.w;
     const cudaStream_t s = as_stream(stream);
-    rc = launch_router_logits(x, w_gate, T, d, E, sc.logits, s);
-    if (rc == MOE_OK)
-        rc = launch_router_topk(sc.logits, bias, T, E, k, normalize, route_scale, idx, wt, s);
-    if (rc == MOE_OK)
-        rc = launch_union(idx, T, k, E, sc.counts, sc.offsets, sc.perm, sc.sorted_pair, sc.uniq,
-                          sc.n_uniq, hits, err, s);
-    if (rc != MOE_OK)
-        return rc;
     FfnScratch fs{};
     ffn_scratch_layout(T, k, d, f, sc.ffn, &fs);
-    rc = launch_act_frag(x, T, d, fs.x_frag, fs.x_scale, fs.x_corr, s);
+    // Small batches: logits + fragments of x in one grid, then top-k + union +
+    // hits in one block; the kernels are chained with programmatic dependent
+    // launches.  Larger batches use the separate stage kernels.
+    const bool small = T <= 8 && T * k <= 64 && (E + 1) / 2 >= T;
+    if (small) {
+        rc = launch_router_logits_frag(x, w_gate, T, d, E, sc.logits, fs.x_frag, fs.x_scale, fs.x_corr, s);
+        if (rc == MOE_OK)
+            rc = launch_select_union(sc.logits, bias, T, E, k, normalize, route_scale, idx, wt, sc.counts,
+                                     sc.offsets, sc.perm, sc.sorted_pair, sc.uniq, sc.n_uniq, hits, err, s);
+    } else {
+        rc = launch_router_logits(x, w_gate, T, d, E, sc.logits, s);
+        if (rc == MOE_OK)
+            rc = launch_router_topk(sc.logits, bias, T, E, k, normalize, route_scale, idx, wt, s);
+        if (rc == MOE_OK)
+            rc = launch_union(idx, T, k, E, sc.counts, sc.offsets, sc.perm, sc.sorted_pair, sc.uniq,
+                              sc.n_uniq, hits, err, s);
+        if (rc == MOE_OK)
+            rc = launch_act_frag(x, T, d, fs.x_frag, fs.x_scale, fs.x_corr, s);
+    }
     if (rc != MOE_OK)
         return rc;
     DecodeFfnArgs a{};

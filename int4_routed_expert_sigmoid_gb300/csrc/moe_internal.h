@@ -55,6 +55,9 @@ int launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStr
 // router.cu
 int launch_router_logits(const float *x, const float *wg, int T, int d, int E, float *logits,
                          cudaStream_t s);
+// logits plus the FFN fragments of x in one kernel (T <= 8)
+int launch_router_logits_frag(const float *x, const float *wg, int T, int d, int E, float *logits,
+                              uint16_t *frag, float *row_scale, float *corr, cudaStream_t s);
 int launch_router_topk(const float *logits, const float *bias, int T, int E, int k, int normalize,
                        float route_scale, int32_t *idx, float *w, cudaStream_t s);
 int launch_act_frag(const float *x, int rows, int K, uint16_t *frag, float *row_scale, float *corr,
@@ -65,6 +68,11 @@ int launch_union(const int32_t *idx, int T, int k, int E, int32_t *counts, int32
                  int32_t *perm, int32_t *sorted_pair, int32_t *uniq, int32_t *n_uniq,
                  uint64_t *hits, int32_t *err, cudaStream_t s);
 int launch_hits(const int32_t *counts, int E, uint64_t *hits, cudaStream_t s);
+// top-k + union + hits in one block (T <= 8, T*k <= 64)
+int launch_select_union(const float *logits, const float *bias, int T, int E, int k, int normalize,
+                        float route_scale, int32_t *idx, float *w, int32_t *counts, int32_t *offsets,
+                        int32_t *perm, int32_t *sorted_pair, int32_t *uniq, int32_t *n_uniq,
+                        uint64_t *hits, int32_t *err, cudaStream_t s);
 
 // ffn_decode.cu
 struct DecodeFfnArgs {

@@ -10,9 +10,14 @@
 #include <climits>
 
 #include "moe_internal.h"
+#include "ptx.cuh"
+#include "route_common.cuh"
 
 namespace moe {
 namespace {
+
+__device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint16_t *__restrict__ frag,
+                             float *__restrict__ row_scale, float *__restrict__ corr);
 
 // ----------------------------------------------------------------- logits ---
 // Small T: each CTA owns kEB experts x kTB tokens and splits the reduction
@@ -21,8 +26,10 @@ constexpr int kEB = 2, kTB = 8, kSkinnyThreads = 256;
 
 __global__ void __launch_bounds__(kSkinnyThreads)
 logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, int T, int d, int E,
-                     float *__restrict__ logits)
+                     float *__restrict__ logits, uint16_t *frag, float *row_scale, float *corr)
 {
+    griddep_launch_dependents();
+    griddep_wait();   // x may come from the previous kernel in the stream
     const int e0 = blockIdx.x * kEB;
     const int t0 = blockIdx.y * kTB;
     const int nt = min(kTB, T - t0);
@@ -77,6 +84,11 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
                 v += part[w][threadIdx.x];
             logits[(size_t)(t0 + b) * E + e0 + a] = v;
         }
+    }
+    // fused path: the first T blocks also build the FFN's fragments of x
+    if (frag != nullptr && blockIdx.y == 0 && blockIdx.x < T) {
+        __syncthreads();
+        act_frag_row(x, blockIdx.x, d, frag, row_scale, corr);
     }
 }
 
@@ -134,74 +146,16 @@ logits_tiled_kernel(const float *__restrict__ x, const float *__restrict__ wg, i
 }
 
 // ------------------------------------------------------------------ top-k ---
-// One warp per token.  Lane l holds experts l, l+32, ...; k rounds of a warp
-// arg-max on (key desc, id asc) pick the experts in order.
 template <int EPL>
 __global__ void __launch_bounds__(256)
 topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int k,
             int normalize, float route_scale, int32_t *__restrict__ idx, float *__restrict__ w)
 {
-    const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T)
         return;
-    float key[EPL], score[EPL];
-    uint32_t live = 0;
-#pragma unroll
-    for (int i = 0; i < EPL; i++) {
-        const int e = lane + 32 * i;
-        if (e < E) {
-            const float l = logits[(size_t)t * E + e];
-            score[i] = 1.0f / (1.0f + expf(-l));
-            key[i] = score[i] + (bias ? bias[e] : 0.0f);
-            live |= 1u << i;
-        } else {
-            score[i] = 0.f;
-            key[i] = -FLT_MAX;
-        }
-    }
-    float my_score = 0.f;   // lane j keeps the score of slot j
-    for (int j = 0; j < k; j++) {
-        float bk = -INFINITY, bs = 0.f;
-        int be = INT_MAX;
-#pragma unroll
-        for (int i = 0; i < EPL; i++) {
-            const int e = lane + 32 * i;
-            if ((live >> i) & 1u) {
-                if (key[i] > bk || (key[i] == bk && e < be)) {
-                    bk = key[i];
-                    be = e;
-                    bs = score[i];
-                }
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-            if (ok > bk || (ok == bk && oe < be)) {
-                bk = ok;
-                be = oe;
-                bs = os;
-            }
-        }
-        if ((be & 31) == lane)
-            live &= ~(1u << (be >> 5));
-        if (lane == j)
-            my_score = bs;
-        if (lane == 0)
-            idx[(size_t)t * k + j] = be;
-    }
-    float scale = 1.0f;
-    if (normalize) {
-        float sum = 0.f;
-        for (int j = 0; j < k; j++)
-            sum += __shfl_sync(0xffffffffu, my_score, j);
-        scale = route_scale / sum;
-    }
-    if (lane < k)
-        w[(size_t)t * k + lane] = normalize ? my_score * scale : my_score;
+    topk_warp<EPL>(logits + (size_t)t * E, bias, E, k, normalize, route_scale, idx + (size_t)t * k,
+                   w + (size_t)t * k);
 }
 
 // --------------------------------------------------------- act fragments ---
@@ -212,12 +166,11 @@ topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, in
 // corr[r][g][plane] = 8 * sum (16 at odd offsets, else 1) * stored value.
 constexpr int kFragThreads = 256;
 
-__global__ void __launch_bounds__(kFragThreads)
-act_frag_kernel(const float *__restrict__ x, int K, uint16_t *__restrict__ frag,
-                float *__restrict__ row_scale, float *__restrict__ corr)
+// Fragments of row r of x, computed by the whole (256-thread) block.
+__device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint16_t *__restrict__ frag,
+                             float *__restrict__ row_scale, float *__restrict__ corr)
 {
     __shared__ float wmax[kFragThreads / 32];
-    const int r = blockIdx.x;
     const float *xr = x + (size_t)r * K;
     float mx = 0.f;
     for (int i = threadIdx.x; i < K / 4; i += kFragThreads) {
@@ -234,6 +187,7 @@ act_frag_kernel(const float *__restrict__ x, int K, uint16_t *__restrict__ frag,
 #pragma unroll
     for (int w = 0; w < kFragThreads / 32; w++)
         mx = fmaxf(mx, wmax[w]);
+    __syncthreads();   // wmax may be reused by the caller
     int e = 0;
     frexpf(mx, &e);
     const float up = mx > 0.f ? ldexpf(1.0f, 14 - e) : 1.0f;
@@ -278,6 +232,18 @@ act_frag_kernel(const float *__restrict__ x, int K, uint16_t *__restrict__ frag,
     }
 }
 
+// One CTA per row: the row's max |x| picks a power of two 2^(14-e) that brings
+// every element below 2^14 (exact scaling); elements at odd offsets within
+// each 8 are further divided by 16.  Each value becomes hi = fp16(v),
+// lo = fp16(v - hi); row_scale[r] = 2^(e-14) undoes the scaling and
+// corr[r][g][plane] = 8 * sum (16 at odd offsets, else 1) * stored value.
+__global__ void __launch_bounds__(kFragThreads)
+act_frag_kernel(const float *__restrict__ x, int K, uint16_t *__restrict__ frag,
+                float *__restrict__ row_scale, float *__restrict__ corr)
+{
+    act_frag_row(x, blockIdx.x, K, frag, row_scale, corr);
+}
+
 }  // namespace
 
 int launch_router_logits(const float *x, const float *wg, int T, int d, int E, float *logits,
@@ -288,9 +254,19 @@ int launch_router_logits(const float *x, const float *wg, int T, int d, int E, f
         logits_tiled_kernel<<<grid, 256, 0, s>>>(x, wg, T, d, E, logits);
     } else {
         dim3 grid((E + kEB - 1) / kEB, (T + kTB - 1) / kTB);
-        logits_skinny_kernel<<<grid, kSkinnyThreads, 0, s>>>(x, wg, T, d, E, logits);
+        logits_skinny_kernel<<<grid, kSkinnyThreads, 0, s>>>(x, wg, T, d, E, logits, nullptr, nullptr, nullptr);
     }
     return cuda_status(cudaGetLastError());
+}
+
+int launch_router_logits_frag(const float *x, const float *wg, int T, int d, int E, float *logits,
+                              uint16_t *frag, float *row_scale, float *corr, cudaStream_t s)
+{
+    const int grid = (E + kEB - 1) / kEB;
+    if (T > kTB || grid < T)
+        return MOE_ERR_UNSUPPORTED;
+    return launch_pdl(logits_skinny_kernel, grid, kSkinnyThreads, 0, s, x, wg, T, d, E, logits, frag,
+                      row_scale, corr);
 }
 
 int launch_router_topk(const float *logits, const float *bias, int T, int E, int k, int normalize,

@@ -14,6 +14,8 @@
 // its warp (match_any) plus the counts of earlier warps and earlier chunks.
 // The result is deterministic and independent of scheduling.
 #include "moe_internal.h"
+#include "ptx.cuh"
+#include "route_common.cuh"
 
 namespace moe {
 namespace {
@@ -162,6 +164,113 @@ size_t union_smem_bytes(int E)
     return (size_t)E * 2 * sizeof(int) + (size_t)kWarps * E * sizeof(unsigned short);
 }
 
+// ------------------------------------------------- small-batch select+union
+// One block of 256 threads for batches of at most 8 tokens and 64 pairs:
+// warp t selects token t's experts (the same top-k as topk_kernel), then the
+// block forms the union as above (histogram, exclusive scans over ascending
+// expert id, stable placement by counting earlier pairs of the same expert)
+// and bumps the hit counters.
+constexpr int kSelThreads = 256;
+constexpr int kSelMaxPairs = 64;
+
+template <int EPL>
+__global__ void __launch_bounds__(kSelThreads)
+select_union_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int k,
+                    int normalize, float route_scale, int32_t *__restrict__ idx, float *__restrict__ w,
+                    int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
+                    int32_t *__restrict__ sorted_pair, int32_t *__restrict__ uniq,
+                    int32_t *__restrict__ n_uniq, uint64_t *__restrict__ hits, int32_t *__restrict__ err)
+{
+    __shared__ int cnt[kMaxE];
+    __shared__ int sidx[kSelMaxPairs];
+    __shared__ int wsum[kSelThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    griddep_launch_dependents();
+    griddep_wait();   // logits come from the previous kernel
+    if (warp < T)
+        topk_warp<EPL>(logits + (size_t)warp * E, bias, E, k, normalize, route_scale, idx + (size_t)warp * k,
+                       w + (size_t)warp * k);
+    for (int e = tid; e < E; e += kSelThreads)
+        cnt[e] = 0;
+    __syncthreads();
+    const int P = T * k;
+    if (tid < P) {
+        const int e = idx[tid];
+        sidx[tid] = e;
+        if (e >= 0 && e < E)
+            atomicAdd(&cnt[e], 1);
+        else
+            atomicOr(err, MOE_DEVERR_BAD_EXPERT);
+    }
+    __syncthreads();
+    // each thread owns 4 consecutive experts: local prefix, then a block scan
+    // of the thread totals (counts) and of the non-empty flags (uniq)
+    int c[4], fl[4], ctot = 0, ftot = 0;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int e = tid * 4 + j;
+        c[j] = e < E ? cnt[e] : 0;
+        fl[j] = c[j] > 0 ? 1 : 0;
+        ctot += c[j];
+        ftot += fl[j];
+    }
+    auto excl_scan = [&](int v, int *total) {
+        int inc = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off)
+                inc += n;
+        }
+        if (lane == 31)
+            wsum[warp] = inc;
+        __syncthreads();
+        int before = 0, all = 0;
+        for (int q = 0; q < kSelThreads / 32; q++) {
+            before += q < warp ? wsum[q] : 0;
+            all += wsum[q];
+        }
+        __syncthreads();
+        *total = all;
+        return before + inc - v;
+    };
+    int ctotal = 0, ftotal = 0;
+    int cbase = excl_scan(ctot, &ctotal);
+    int fbase = excl_scan(ftot, &ftotal);
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int e = tid * 4 + j;
+        if (e < E) {
+            offsets[e] = cbase;
+            counts[e] = c[j];
+            cnt[e] = cbase;   // start of expert e's range (read below)
+            if (fl[j])
+                uniq[fbase] = e;
+            if (hits)
+                hits[e] += (uint64_t)c[j];
+        }
+        cbase += c[j];
+        fbase += fl[j];
+    }
+    if (tid == 0) {
+        offsets[E] = ctotal;
+        *n_uniq = ftotal;
+    }
+    __syncthreads();
+    if (tid < P) {
+        const int e = sidx[tid];
+        int pos = -1;
+        if (e >= 0 && e < E) {
+            int rank = 0;
+            for (int q = 0; q < tid; q++)
+                rank += sidx[q] == e ? 1 : 0;
+            pos = cnt[e] + rank;
+            sorted_pair[pos] = tid;
+        }
+        perm[tid] = pos;
+    }
+}
+
 __global__ void hits_kernel(const int32_t *__restrict__ counts, int E, uint64_t *__restrict__ hits)
 {
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -188,6 +297,26 @@ int launch_union(const int32_t *idx, int T, int k, int E, int32_t *counts, int32
     union_kernel<<<1, kThreads, smem, s>>>(idx, T * k, E, counts, offsets, perm, sorted_pair, uniq,
                                         n_uniq, hits, err);
     return cuda_status(cudaGetLastError());
+}
+
+int launch_select_union(const float *logits, const float *bias, int T, int E, int k, int normalize,
+                        float route_scale, int32_t *idx, float *w, int32_t *counts, int32_t *offsets,
+                        int32_t *perm, int32_t *sorted_pair, int32_t *uniq, int32_t *n_uniq,
+                        uint64_t *hits, int32_t *err, cudaStream_t s)
+{
+    if (T > kSelThreads / 32 || T * k > kSelMaxPairs || E > kMaxE)
+        return MOE_ERR_UNSUPPORTED;
+    const int epl = (E + 31) / 32;
+#define MOE_SEL(N)                                                                                      \
+    return launch_pdl(select_union_kernel<N>, 1, kSelThreads, 0, s, logits, bias, T, E, k, normalize,      \
+                      route_scale, idx, w, counts, offsets, perm, sorted_pair, uniq, n_uniq, hits, err)
+    if (epl <= 1) MOE_SEL(1);
+    if (epl <= 2) MOE_SEL(2);
+    if (epl <= 4) MOE_SEL(4);
+    if (epl <= 8) MOE_SEL(8);
+    if (epl <= 16) MOE_SEL(16);
+    MOE_SEL(32);
+#undef MOE_SEL
 }
 
 int launch_hits(const int32_t *counts, int E, uint64_t *hits, cudaStream_t s)
