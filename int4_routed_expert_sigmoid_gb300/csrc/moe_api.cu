@@ -37,10 +37,14 @@ int check_layer(const moe_layer_int4 *w)
 int resolve_mode(int mode, int T)
 {
     if (mode == MOE_MODE_AUTO)
-        return MOE_MODE_DECODE;
-    (void)T;
+        return T < 1024 ? MOE_MODE_DECODE : MOE_MODE_PREFILL;
     return mode;
 }
+
+bool valid_mode(int mode) { return mode == MOE_MODE_AUTO || mode == MOE_MODE_DECODE || mode == MOE_MODE_PREFILL; }
+
+// FFN scratch of either path (the union never has more than T*k experts).
+size_t ffn_scratch_bytes_mode(int T, int k, int d, int f, int mode);
 
 // Scratch of the decode FFN: activation fragments of x and of h, their
 // factors and bias corrections.
@@ -79,7 +83,7 @@ struct LayerScratch {
     uint8_t *ffn;
 };
 
-size_t layer_scratch_layout(int T, int k, int E, int d, int f, uint8_t *base, LayerScratch *o)
+size_t layer_scratch_layout(int T, int k, int E, int d, int f, int mode, uint8_t *base, LayerScratch *o)
 {
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -100,10 +104,17 @@ size_t layer_scratch_layout(int T, int k, int E, int d, int f, uint8_t *base, La
     s.n_uniq = reinterpret_cast<int32_t *>(take(4));
     s.y_pair = reinterpret_cast<float *>(take(P * d * 4));
     s.y_shared = reinterpret_cast<float *>(take((size_t)T * d * 4));
-    s.ffn = take(ffn_scratch_layout(T, k, d, f, nullptr, nullptr));
+    s.ffn = take(ffn_scratch_bytes_mode(T, k, d, f, mode));
     if (o)
         *o = s;
     return off;
+}
+
+size_t ffn_scratch_bytes_mode(int T, int k, int d, int f, int mode)
+{
+    if (resolve_mode(mode, T) == MOE_MODE_PREFILL)
+        return prefill_scratch_bytes(T, k, d, f);
+    return ffn_scratch_layout(T, k, d, f, nullptr, nullptr);
 }
 
 }  // namespace
@@ -171,10 +182,9 @@ int moe_hits(const int32_t *counts, int E, uint64_t *hits, void *stream)
 
 size_t moe_ffn_workspace_bytes(int T, int k, int d, int f, int mode)
 {
-    (void)mode;
-    if (T < 1 || k < 1 || d < 1 || f < 1)
+    if (T < 1 || k < 1 || d < 1 || f < 1 || !valid_mode(mode))
         return 0;
-    return ffn_scratch_layout(T, k, d, f, nullptr, nullptr);
+    return ffn_scratch_bytes_mode(T, k, d, f, mode);
 }
 
 int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *offsets,
@@ -191,11 +201,27 @@ int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *
         return MOE_ERR_INVALID_ARG;
     if (T < 1 || k < 1 || k > 32 || k > w->E || (long long)T * (k + 1) > (1LL << 24))
         return MOE_ERR_INVALID_ARG;
-    mode = resolve_mode(mode, T);
-    if (mode != MOE_MODE_DECODE)
-        return MOE_ERR_UNSUPPORTED;
+    if (!valid_mode(mode))
+        return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe_ffn_workspace_bytes(T, k, w->d, w->f, mode))
         return MOE_ERR_WORKSPACE;
+    mode = resolve_mode(mode, T);
+    if (mode == MOE_MODE_PREFILL) {
+        PrefillFfnArgs pa{};
+        pa.w = w;
+        pa.x = x;
+        pa.offsets = offsets;
+        pa.sorted_pair = sorted_pair;
+        pa.uniq = uniq;
+        pa.n_uniq = n_uniq;
+        pa.T = T;
+        pa.k = k;
+        pa.scratch = workspace;
+        pa.y_pair = y_pair;
+        pa.y_shared = y_shared;
+        pa.err = err;
+        return launch_ffn_prefill(pa, as_stream(stream));
+    }
     FfnScratch sc{};
     ffn_scratch_layout(T, k, w->d, w->f, static_cast<uint8_t *>(workspace), &sc);
     const cudaStream_t s = as_stream(stream);
@@ -234,10 +260,9 @@ int moe_combine(const float *y_pair, const float *y_shared, const float *topk_w,
 
 size_t moe_layer_workspace_bytes(int T, int k, int E, int d, int f, int mode)
 {
-    (void)mode;
-    if (T < 1 || k < 1 || E < 1 || d < 1 || f < 1)
+    if (T < 1 || k < 1 || E < 1 || d < 1 || f < 1 || !valid_mode(mode))
         return 0;
-    return layer_scratch_layout(T, k, E, d, f, nullptr, nullptr);
+    return layer_scratch_layout(T, k, E, d, f, mode, nullptr, nullptr);
 }
 
 int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
@@ -255,16 +280,43 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
         return MOE_ERR_INVALID_ARG;
     if (!ok_route_shape(T, d, E, k) || (long long)T * (k + 1) > (1LL << 22))
         return MOE_ERR_INVALID_ARG;
-    mode = resolve_mode(mode, T);
-    if (mode != MOE_MODE_DECODE)
-        return MOE_ERR_UNSUPPORTED;
+    if (!valid_mode(mode))
+        return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe_layer_workspace_bytes(T, k, E, d, f, mode))
         return MOE_ERR_WORKSPACE;
     LayerScratch sc{};
-    layer_scratch_layout(T, k, E, d, f, static_cast<uint8_t *>(workspace), &sc);
+    layer_scratch_layout(T, k, E, d, f, mode, static_cast<uint8_t *>(workspace), &sc);
+    mode = resolve_mode(mode, T);
     int32_t *idx = topk_idx ? topk_idx : sc.idx;
     float *wt = topk_w ? topk_w : sc.w;
     const cudaStream_t s = as_stream(stream);
+    if (mode == MOE_MODE_PREFILL) {
+        rc = launch_router_logits(x, w_gate, T, d, E, sc.logits, s);
+        if (rc == MOE_OK)
+            rc = launch_router_topk(sc.logits, bias, T, E, k, normalize, route_scale, idx, wt, s);
+        if (rc == MOE_OK)
+            rc = launch_union(idx, T, k, E, sc.counts, sc.offsets, sc.perm, sc.sorted_pair, sc.uniq,
+                              sc.n_uniq, hits, err, s);
+        if (rc != MOE_OK)
+            return rc;
+        PrefillFfnArgs pa{};
+        pa.w = w;
+        pa.x = x;
+        pa.offsets = sc.offsets;
+        pa.sorted_pair = sc.sorted_pair;
+        pa.uniq = sc.uniq;
+        pa.n_uniq = sc.n_uniq;
+        pa.T = T;
+        pa.k = k;
+        pa.scratch = sc.ffn;
+        pa.y_pair = sc.y_pair;
+        pa.y_shared = sc.y_shared;
+        pa.err = err;
+        rc = launch_ffn_prefill(pa, s);
+        if (rc != MOE_OK)
+            return rc;
+        return launch_combine(sc.y_pair, sc.y_shared, wt, sc.perm, residual, T, k, d, out, s);
+    }
     FfnScratch fs{};
     ffn_scratch_layout(T, k, d, f, sc.ffn, &fs);
     // Small batches: logits + fragments of x in one grid, then top-k + union +

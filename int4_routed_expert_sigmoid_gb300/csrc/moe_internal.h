@@ -90,6 +90,19 @@ struct DecodeFfnArgs {
 };
 int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s);
 
+// ffn_prefill.cu
+struct PrefillFfnArgs {
+    const moe_layer_int4 *w;
+    const float *x;                      // [T][d] fp32
+    const int32_t *offsets, *sorted_pair, *uniq, *n_uniq;
+    int T, k;
+    void *scratch;                       // prefill_scratch_bytes(T, k, d, f) bytes, 256-aligned
+    float *y_pair, *y_shared;
+    int32_t *err;
+};
+size_t prefill_scratch_bytes(int T, int k, int d, int f);
+int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s);
+
 // combine.cu
 int launch_combine(const float *y_pair, const float *y_shared, const float *w, const int32_t *perm,
                    const float *res, int T, int k, int d, float *out, cudaStream_t s);
@@ -100,6 +113,9 @@ int make_tmap_3d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, in
                  uint64_t inner, uint64_t rows, uint64_t outer, uint64_t row_stride_bytes,
                  uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_rows,
                  CUtensorMapSwizzle swizzle);
+
+int make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, uint64_t inner, uint64_t rows,
+                 uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
 // device properties cached per device
 int sm_count(int device);
