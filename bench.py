@@ -46,7 +46,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode", choices=["decode", "batched_decode"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "batched_decode", "prefill"])
     ap.add_argument("--replicas", type=int, default=4, help="device copies of the layer rotated across steps")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the routed expert count (small-footprint profiling runs); 0 = workload's")
@@ -179,8 +179,10 @@ def run_ours(args, rank, world, local):
         import dataclasses
         sh = dataclasses.replace(sh, E=args.experts)
     T, E, k, d, f = sh.T, sh.E, sh.k, sh.d, sh.f
-    R = max(1, args.replicas)
-    S = max(1, min(args.graph_steps, args.steps))
+    prefill = args.workload == "prefill"
+    mode = moe.MOE_MODE_PREFILL if prefill else moe.MOE_MODE_DECODE
+    R = max(1, min(args.replicas, 2) if prefill else args.replicas)
+    S = max(1, min(args.graph_steps if not prefill else 4, args.steps))
 
     # ---- inputs: one seeded layer, R device copies (weights, router, bias)
     L = workloads.layer_inputs(sh, seed=0, threads=os.cpu_count() or 8)
@@ -219,14 +221,14 @@ def run_ours(args, rank, world, local):
     y_pair = torch.empty((T * k, d), dtype=torch.float32, device=dev)
     y_shared = torch.empty((T, d), dtype=torch.float32, device=dev)
     outs = torch.empty((S, T, d), dtype=torch.float32, device=dev)
-    ws = moe.workspace(moe.ffn_workspace_bytes(T, k, d, f, moe.MOE_MODE_DECODE), dev)
+    ws = moe.workspace(moe.ffn_workspace_bytes(T, k, d, f, mode), dev)
 
-    lws_step = moe.workspace(moe.layer_workspace_bytes(T, k, E, d, f, moe.MOE_MODE_DECODE), dev)
+    lws_step = moe.workspace(moe.layer_workspace_bytes(T, k, E, d, f, mode), dev)
 
     def layer_step(i):
         """One step through the public fused entry point (the timed path)."""
         r = i % R
-        moe.moe_layer_forward(xs[i % S], wgs[r], biases[r], layers[r], k, 1, 1.0, mode=moe.MOE_MODE_DECODE,
+        moe.moe_layer_forward(xs[i % S], wgs[r], biases[r], layers[r], k, 1, 1.0, mode=mode,
                               out=outs[i % S], topk_idx=idx, topk_w=wts, hits=hits[r], ws=lws_step, err=err)
 
     def step(i, ev=None):
@@ -241,7 +243,7 @@ def run_ours(args, rank, world, local):
         moe.moe_union(idx, E, hits=hits[r], err=err, out=un)
         if ev:
             ev[2].record()
-        moe.moe_expert_ffn_int4(x, layers[r], un, k, moe.MOE_MODE_DECODE, y_pair=y_pair, y_shared=y_shared,
+        moe.moe_expert_ffn_int4(x, layers[r], un, k, mode, y_pair=y_pair, y_shared=y_shared,
                                 ws=ws, err=err)
         if ev:
             ev[3].record()
@@ -251,7 +253,10 @@ def run_ours(args, rank, world, local):
 
     # kernels per fused step: small batches logits(+x fragments), select+union, gate/up, down,
     # combine; otherwise logits, top-k, union, x fragments, gate/up, down, combine
-    launches_per_step = 5 if (T <= 8 and T * k <= 64) else 7
+    if prefill:   # logits, top-k, union, plan, gather, gate/up, h conversion, down, combine
+        launches_per_step = 9
+    else:
+        launches_per_step = 5 if (T <= 8 and T * k <= 64) else 7
 
     # warm the code paths once outside capture, then capture
     side = torch.cuda.Stream(device=dev)
@@ -317,16 +322,16 @@ def run_ours(args, rank, world, local):
     n_uniq = int(un["n_uniq"].item())
 
     # ---- end to end through the public API with host buffers (not graph-captured)
-    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    e2e_steps = max(1, min(args.e2e_steps, args.steps, 8 if prefill else args.e2e_steps))
     x_host = torch.from_numpy(workloads.activations(e2e_steps * T, d, seed=5000 + rank)).view(e2e_steps, T, d)
     x_host = x_host.pin_memory()
     out_host = torch.empty((e2e_steps, T, d), dtype=torch.float32).pin_memory()
     x_dev = torch.empty((T, d), dtype=torch.float32, device=dev)
     out_dev = torch.empty((T, d), dtype=torch.float32, device=dev)
-    lws = moe.workspace(moe.layer_workspace_bytes(T, k, E, d, f, moe.MOE_MODE_DECODE), dev)
+    lws = moe.workspace(moe.layer_workspace_bytes(T, k, E, d, f, mode), dev)
     for i in range(min(50, e2e_steps)):   # warm-up of the host path
         r = i % R
-        moe.moe_layer_forward(x_dev, wgs[r], biases[r], layers[r], k, mode=moe.MOE_MODE_DECODE, out=out_dev,
+        moe.moe_layer_forward(x_dev, wgs[r], biases[r], layers[r], k, mode=mode, out=out_dev,
                               ws=lws, err=err)
     torch.cuda.synchronize()
     barrier(world)
@@ -334,7 +339,7 @@ def run_ours(args, rank, world, local):
     for i in range(e2e_steps):
         r = i % R
         x_dev.copy_(x_host[i], non_blocking=True)
-        moe.moe_layer_forward(x_dev, wgs[r], biases[r], layers[r], k, mode=moe.MOE_MODE_DECODE, out=out_dev,
+        moe.moe_layer_forward(x_dev, wgs[r], biases[r], layers[r], k, mode=mode, out=out_dev,
                               hits=hits[r], ws=lws, err=err)
         out_host[i].copy_(out_dev, non_blocking=True)
     torch.cuda.synchronize()
@@ -346,7 +351,21 @@ def run_ours(args, rank, world, local):
     peaks = load_peaks()
     byts = layer_bytes(sh, n_uniq)
     ffn_ms = float(stage_ms[2])
-    achieved = byts["ffn"] / (ffn_ms * 1e-3) / 1e9
+    if prefill:
+        # dense work of the grouped GEMMs: 3 matrices of d x f per (token, expert) pair, 2 flops per MAC
+        flops = 6.0 * d * f * (T * k + T)
+        achieved = flops / (ffn_ms * 1e-3) / 1e12
+        roof = {"kernel": "expert FFN stage (gather, tcgen05 gate/up, h conversion, tcgen05 down)",
+                "bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": ncu_traffic(ROOT, "ffn_prefill"),
+                "peak_source": peaks["source"] + " bf16 dense (fp16 operands run at the same tensor rate)",
+                "flops_per_launch": flops, "ms_per_launch": round(ffn_ms, 5)}
+    else:
+        achieved = byts["ffn"] / (ffn_ms * 1e-3) / 1e9
+        roof = {"kernel": "expert FFN stage (act fragments + gate/up + down kernels)", "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(ROOT, "ffn"),
+                "peak_source": peaks["source"], "bytes_per_launch": byts["ffn"], "ms_per_launch": round(ffn_ms, 5)}
     value = T * args.steps * world / (elapsed_max * 1e-3)
     ms_per_step = elapsed_max / args.steps
     line = {
@@ -360,10 +379,7 @@ def run_ours(args, rank, world, local):
                          f"({R * E * byts['expert_block'] / 1e9:.1f} GB) rotated across steps",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "cuda_graph_steps": S},
-        "roofline": {"kernel": "expert FFN stage (act fragments + gate/up + down kernels)", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(ROOT, "ffn"),
-                     "peak_source": peaks["source"], "bytes_per_launch": byts["ffn"], "ms_per_launch": round(ffn_ms, 5)},
+        "roofline": roof,
         "stages_ms": {"route": round(float(stage_ms[0]), 5), "union": round(float(stage_ms[1]), 5),
                       "ffn": round(ffn_ms, 5), "combine": round(float(stage_ms[3]), 5)},
         "layer_gbs": round(byts["layer"] / (ms_per_step * 1e-3) / 1e9, 1),
