@@ -46,10 +46,13 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode", choices=["decode", "batched_decode", "prefill"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "batched_decode", "prefill", "tiny"],
+                    help="tiny is the parity-size layer (fits in L2; for quick checks, not a bench line)")
     ap.add_argument("--replicas", type=int, default=4, help="device copies of the layer rotated across steps")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the routed expert count (small-footprint profiling runs); 0 = workload's")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the tokens per step (small-footprint profiling runs); 0 = workload's")
     ap.add_argument("--graph-steps", type=int, default=100, help="steps captured per CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -175,9 +178,9 @@ def run_ours(args, rank, world, local):
             dist.init_process_group("nccl")
     libbuild.build()
     sh = workloads.WORKLOADS[args.workload]
-    if args.experts:
+    if args.experts or args.tokens:
         import dataclasses
-        sh = dataclasses.replace(sh, E=args.experts)
+        sh = dataclasses.replace(sh, E=args.experts or sh.E, T=args.tokens or sh.T)
     T, E, k, d, f = sh.T, sh.E, sh.k, sh.d, sh.f
     prefill = args.workload == "prefill"
     mode = moe.MOE_MODE_PREFILL if prefill else moe.MOE_MODE_DECODE
@@ -366,7 +369,7 @@ def run_ours(args, rank, world, local):
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(ROOT, "ffn"),
                 "peak_source": peaks["source"], "bytes_per_launch": byts["ffn"], "ms_per_launch": round(ffn_ms, 5)}
-    value = T * args.steps * world / (elapsed_max * 1e-3)
+    value = job_throughput(T, args.steps, world, elapsed_max)
     ms_per_step = elapsed_max / args.steps
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -375,8 +378,9 @@ def run_ours(args, rank, world, local):
         "config": {"workload": f"{args.workload}: 1 MoE layer, E={E} routed + 1 shared, k={k}, d={d}, f={f}, "
                                f"int4 group-{sh.G} fp32 scales, T={T} token(s) per step",
                    "T": T, "E": E, "k": k, "d": d, "f": f, "G": sh.G, "weights": "int4",
-                   "l2": f"inputs larger than L2: {R} device copies of the layer "
-                         f"({R * E * byts['expert_block'] / 1e9:.1f} GB) rotated across steps",
+                   "l2": (f"inputs larger than L2: {R} device copies of the layer "
+                          f"({R * E * byts['expert_block'] / 1e9:.1f} GB) rotated across steps")
+                   if R * E * byts["expert_block"] > 2 * 129e6 else "parity-size layer: fits in L2 (not a bench line)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "cuda_graph_steps": S},
         "roofline": roof,
@@ -404,6 +408,11 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def job_throughput(T, steps, world, elapsed_ms):
+    """Whole-job tokens/s: every rank processes T tokens per step; the slowest rank's time counts."""
+    return T * steps * world / (elapsed_ms * 1e-3)
 
 
 def reduce_max(world, vals, dev):

@@ -17,15 +17,15 @@
  * on the thread count.
  *
  * Sources (page title, section):
- *  [L13]  "Public Colibri Observation and Revision Ledger", "Exact Architecture
+ *  [arch]  "Public Colibri Observation and Revision Ledger", "Exact Architecture
  *         and Data-Flow Reconstruction": sigmoid router with n_group=1 over the
  *         experts of a layer; each routed expert is a three-matrix MLP stored
  *         contiguously at int4; an always-on shared expert; fp32 gate
  *         parameters.
- *  [L15]  same page and section: the five per-layer stages Route, Union,
+ *  [stages] same page and section: the five per-layer stages Route, Union,
  *         Place, Overlap, Learn; routing and precision are unchanged by them.
- *  [L17]  same section: per-expert hit counters updated after each token.
- *  [L62]  same page, "Cache/Prefetch Design Comparison" figure caption: the
+ *  [hits]  same section: per-expert hit counters updated after each token.
+ *  [union] same page, "Cache/Prefetch Design Comparison" figure caption: the
  *         batch-union reads each unique expert once per batched decode.
  *  [R-idea] colibri README, "The idea": ~11 GB of routed experts change per
  *         token, which with 75 layers and ~19 MB experts means 8 experts per

@@ -1,0 +1,216 @@
+"""GPU parity at the GLM-5.2 layer shape (E = 256 routed + 1 shared, k = 8,
+d = 6144, f = 2048, G = 32), in the launch configuration the benchmark times
+(the fused moe_layer_forward entry point with an explicit mode).
+
+Every token's routing is checked against the oracle (bit-exact outside flagged
+near-ties), the union and hit counters exactly, and the outputs of a sample of
+tokens, which the oracle evaluates one by one, within the path's tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from moe_testlib import (TOL_DECODE, TOL_PREFILL, check_union_equal, compare_routing, host, moe,
+                         near_tie_tokens, rel_max_err, run_steps)
+
+pytestmark = pytest.mark.gpu
+
+FULL = workloads.WORKLOADS["decode"]
+E, K, D, F, G = FULL.E, FULL.k, FULL.d, FULL.f, FULL.G
+
+
+@pytest.fixture(scope="module")
+def full():
+    """Layer 0's weights (identical for the decode, batched-decode and prefill workloads), host + device."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from int4_routed_expert_sigmoid_gb300 import build
+    build.build()
+    m = moe()
+    L = workloads.layer_inputs(FULL, seed=0, threads=16)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    lw = m.LayerWeights(t(L.q_base.reshape(-1)), t(L.s_base.reshape(-1)), t(L.shared_q), t(L.shared_s),
+                        E=E, d=D, f=F, G=G)
+    yield L, lw, t(L.wg)
+    torch.cuda.synchronize()
+
+
+def _oracle(L, x, bias, res=None):
+    return oracle.Layer(x, L.wg, bias, L.q_base, L.s_base, L.shared_q, L.shared_s, d=D, f=F, E=E, k=K, G=G,
+                        normalize=1, route_scale=1.0, res=res)
+
+
+def _fused(lw, wg_d, x, bias, mode, res=None):
+    m = moe()
+    T = x.shape[0]
+    idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    hits = torch.zeros(E, dtype=torch.int64, device="cuda")
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out, err = m.moe_layer_forward(t(x), wg_d, t(bias), lw, K, 1, 1.0, mode=mode, residual=t(res),
+                                   topk_idx=idx, topk_w=w, hits=hits)
+    torch.cuda.synchronize()
+    return dict(out=host(out), err=int(host(err)[0]), idx=host(idx), w=host(w), hits=host(hits))
+
+
+def _sample(T, n, seed, must=()):
+    rng = np.random.default_rng(seed)
+    s = set(int(t) for t in must if 0 <= t < T)
+    s.update(int(t) for t in rng.choice(T, size=min(n, T), replace=False))
+    return np.array(sorted(s), dtype=np.int32)
+
+
+def _check_layer(L, lw, wg_d, x, bias, mode, tol, n_sample, res=None):
+    """Fused layer vs oracle: routing (all tokens), union/hits, sampled outputs."""
+    T = x.shape[0]
+    r = _fused(lw, wg_d, x, bias, mode, res)
+    assert r["err"] == 0
+    o_idx, o_w, _, keys = oracle.route(x, L.wg, bias, K)
+    same, flagged = compare_routing(r["idx"], r["w"], o_idx, o_w, keys, K)
+    # union and hit counters from the GPU's own routing; equal to the oracle's where routing agrees
+    u = oracle.union(r["idx"], E)
+    assert np.array_equal(r["hits"], u["counts"].astype(np.int64))
+    assert int(r["hits"].sum()) == T * K
+    if same.all():
+        assert np.array_equal(r["idx"], o_idx)
+    # sampled outputs: always the first and last token and a token of the hottest expert
+    hot = int(np.argmax(u["counts"]))
+    hot_tok = u["sorted_pair"][u["offsets"][hot + 1] - 1] // K
+    toks = _sample(T, n_sample, seed=T, must=(0, T - 1, hot_tok))
+    toks = toks[same[toks]]
+    _, _, o_out = _oracle(L, x, bias, res).tokens(toks)
+    err = rel_max_err(r["out"][toks], o_out)
+    print(f"[T={T} mode={mode}] n_uniq={u['n_uniq']} max/expert="
+          f"{int(u['counts'].max())} flagged={int(flagged.sum())} sampled={toks.size} rel_err={err:.3e}")
+    assert err <= tol
+    return r, u
+
+
+def test_decode_t1_full(full):
+    """T = 1 with the N(0, 0.1) selection bias: the 5-launch small-batch path."""
+    L, lw, wg_d = full
+    m = moe()
+    x = workloads.activations(1, D, seed=0)
+    bias = workloads.selection_bias(E, "normal", seed=0)
+    r, u = _check_layer(L, lw, wg_d, x, bias, m.MOE_MODE_DECODE, TOL_DECODE, 1)
+    assert u["n_uniq"] == K
+
+
+def test_decode_t1_residual_stages(full):
+    """T = 1 through the separate entry points with a residual: per-expert y rows and the union."""
+    L, lw, wg_d = full
+    x = workloads.activations(1, D, seed=3)
+    res = workloads.activations(1, D, seed=4)
+    bias = workloads.selection_bias(E, "normal", seed=0)
+    dev = dict(x=torch.from_numpy(x).cuda(), wg=wg_d, bias=torch.from_numpy(bias).cuda(), layer=lw)
+    r = run_steps(dev, K, res=torch.from_numpy(res).cuda(), mode=moe().MOE_MODE_DECODE)
+    assert r["err"] == 0
+    o_idx, o_w, _, keys = oracle.route(x, L.wg, bias, K)
+    same, _ = compare_routing(r["idx"], r["w"], o_idx, o_w, keys, K)
+    if not same.all():
+        pytest.skip("near-tie routing at this seed")
+    check_union_equal(r, oracle.union(o_idx, E), E)
+    for j in range(K):
+        e = int(r["uniq"][j])
+        p = int(r["offsets"][e])
+        y = oracle.expert_ffn(x[0], L.q_base[e], L.s_base[e], D, F, G)
+        assert rel_max_err(r["y_pair"][p:p + 1], y[None]) <= TOL_DECODE, f"expert {e}"
+    y_sh = oracle.expert_ffn(x[0], L.shared_q, L.shared_s, D, F, G)
+    assert rel_max_err(r["y_shared"], y_sh[None]) <= TOL_DECODE
+    _, _, o_out = _oracle(L, x, bias, res).tokens(np.array([0]))
+    assert rel_max_err(r["out"], o_out) <= TOL_DECODE
+
+
+def test_batched_decode_t64_zipf(full):
+    """T = 64 with the Zipf(1.1) selection bias: union well below T*k, hot experts with many tokens."""
+    L, lw, wg_d = full
+    m = moe()
+    x = workloads.activations(64, D, seed=0)
+    bias = workloads.selection_bias(E, "zipf", seed=0)
+    r, u = _check_layer(L, lw, wg_d, x, bias, m.MOE_MODE_DECODE, TOL_DECODE, 12)
+    assert u["n_uniq"] < 64 * K
+    # every row of the hottest expert, through the separate calls on the same routing
+    dev = dict(x=torch.from_numpy(x).cuda(), wg=wg_d, bias=torch.from_numpy(bias).cuda(), layer=lw)
+    s = run_steps(dev, K, mode=m.MOE_MODE_DECODE, teacher_idx=r["idx"], teacher_w=r["w"])
+    assert s["err"] == 0
+    check_union_equal(s, u, E)
+    hot = int(np.argmax(u["counts"]))
+    lo, hi = u["offsets"][hot], u["offsets"][hot + 1]
+    y = oracle.expert_ffn_tokens(x, u["sorted_pair"][lo:hi] // K, L.q_base[hot], L.s_base[hot], D, F, G)
+    assert rel_max_err(s["y_pair"][lo:hi], y) <= TOL_DECODE
+    # the fused entry point and the separate calls give the same bits
+    assert np.array_equal(s["out"], r["out"])
+
+
+def test_prefill_t4096(full):
+    """T = 4096, no bias (about 128 tokens per expert): the tcgen05 grouped-GEMM path."""
+    L, lw, wg_d = full
+    m = moe()
+    x = workloads.activations(4096, D, seed=0)
+    r, u = _check_layer(L, lw, wg_d, x, None, m.MOE_MODE_PREFILL, TOL_PREFILL, 12)
+    assert u["n_uniq"] == E
+    # sampled rows of the hottest expert's pair outputs (its last row is in the ragged tail of a tile)
+    dev = dict(x=torch.from_numpy(x).cuda(), wg=wg_d, bias=None, layer=lw)
+    s = run_steps(dev, K, mode=m.MOE_MODE_PREFILL, teacher_idx=r["idx"], teacher_w=r["w"])
+    assert s["err"] == 0
+    check_union_equal(s, u, E)
+    hot = int(np.argmax(u["counts"]))
+    lo, hi = int(u["offsets"][hot]), int(u["offsets"][hot + 1])
+    rows = np.unique(np.array([lo, lo + 1, (lo + hi) // 2, hi - 2, hi - 1]))
+    y = oracle.expert_ffn_tokens(x, u["sorted_pair"][rows] // K, L.q_base[hot], L.s_base[hot], D, F, G)
+    assert rel_max_err(s["y_pair"][rows], y) <= TOL_PREFILL
+    toks = _sample(4096, 4, seed=9, must=(4095,))
+    y_sh = oracle.expert_ffn_tokens(x, toks, L.shared_q, L.shared_s, D, F, G)
+    assert rel_max_err(s["y_shared"][toks], y_sh) <= TOL_PREFILL
+
+
+def test_stack_8_layers(full):
+    """8 resident-shape layers with the residual stream and a per-layer Zipf permutation.
+
+    T = 4 (small-batch path) and T = 16 (general decode path) run end to end: the
+    oracle carries its own x_l through all 8 layers and every token is compared at
+    every layer.  T = 256 runs teacher-forced: the oracle routes every token from
+    the GPU's x_l and evaluates a sample of tokens."""
+    del full   # weights of layer 0 are regenerated with the stack's per-layer seeds
+    m = moe()
+    sh = workloads.WORKLOADS["stack"]
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    Ts = (4, 16, 256)
+    x_gpu = {T: workloads.activations(T, D, seed=0) for T in Ts}
+    x_orc = {T: x_gpu[T].copy() for T in Ts if T <= 16}
+    diverged = []
+    for layer in range(sh.layers):
+        L = workloads.layer_inputs(sh, seed=0, layer=layer, T=1, threads=16)
+        lw = m.LayerWeights(t(L.q_base.reshape(-1)), t(L.s_base.reshape(-1)), t(L.shared_q), t(L.shared_s),
+                            E=E, d=D, f=F, G=G)
+        wg_d, bias = t(L.wg), L.bias
+        for T in Ts:
+            r = _fused(lw, wg_d, x_gpu[T], bias, m.MOE_MODE_DECODE, res=x_gpu[T])
+            assert r["err"] == 0
+            assert np.array_equal(r["hits"], oracle.union(r["idx"], E)["counts"].astype(np.int64))
+            if T <= 16:
+                o_idx, o_w, _, keys = oracle.route(x_orc[T], L.wg, bias, K)
+                if not np.array_equal(o_idx, r["idx"]):
+                    flagged = near_tie_tokens(keys, K)
+                    assert flagged[(o_idx != r["idx"]).any(axis=1)].all(), f"layer {layer} T={T}"
+                    diverged.append((layer, T))
+                _, _, o_out = _oracle(L, x_orc[T], bias, res=x_orc[T]).dense()
+                if (layer, T) not in diverged and not any(dt == T for _, dt in diverged):
+                    err = rel_max_err(r["out"], o_out)
+                    assert err <= TOL_DECODE, f"layer {layer} T={T}: {err:.3e}"
+                x_orc[T] = o_out.astype(np.float32)
+            else:
+                o_idx, o_w, _, keys = oracle.route(x_gpu[T], L.wg, bias, K)
+                same, _ = compare_routing(r["idx"], r["w"], o_idx, o_w, keys, K)
+                toks = _sample(T, 6, seed=layer, must=(T - 1,))
+                toks = toks[same[toks]]
+                _, _, o_out = _oracle(L, x_gpu[T], bias, res=x_gpu[T]).tokens(toks)
+                err = rel_max_err(r["out"][toks], o_out)
+                assert err <= TOL_DECODE, f"layer {layer} T={T} (teacher-forced): {err:.3e}"
+            x_gpu[T] = r["out"]
+        del lw, L
+        torch.cuda.empty_cache()
+    if diverged:
+        print(f"[near-tie] end-to-end routing diverged at (layer, T) = {diverged}")
