@@ -77,8 +77,10 @@ enum {
 /* FFN execution modes. */
 enum {
     MOE_MODE_AUTO = 0,     /* decode path when T < 1024, else prefill */
-    MOE_MODE_DECODE = 1,   /* fp32-accurate path (exact int4 x split-bf16 activations) */
-    MOE_MODE_PREFILL = 2   /* bf16 tensor-core grouped GEMM (tcgen05), fp32 accumulate */
+    MOE_MODE_DECODE = 1,   /* fp32-accurate grouped GEMV: exact int4 against activations split
+                              into fp16 hi + lo parts, fp32 accumulation */
+    MOE_MODE_PREFILL = 2   /* tcgen05 grouped GEMM on 16-bit operands (fp16 q*s weights, fp16
+                              activations scaled per row by a power of two), fp32 accumulate */
 };
 
 /* Human-readable name of a status code (static string). */
@@ -221,6 +223,20 @@ MOE_API int moe_expert_ffn_int4_noalloc(const float *x, const moe_layer_int4 *w,
 MOE_API int moe_combine(const float *y_pair, const float *y_shared, const float *topk_w,
                 const int32_t *perm, const float *residual, int T, int k, int d,
                 float *out, void *stream);
+
+/*
+ * RMS normalisation of each row (unit weight), the input of a stacked layer:
+ *   out[t][i] = x[t][i] / sqrt( (1/d) sum_i x[t][i]^2 + eps )
+ * x, out: [T][d] fp32 (out may alias x); d a multiple of 4; eps >= 0.
+ * fp32 sum of squares, IEEE square root and division.
+ * Source: the dense part keeps its norms in fp32 ("Public Colibri Observation
+ * and Revision Ledger", "Exact Architecture and Data-Flow Reconstruction").
+ * A stack of MoE layers with nothing between them overflows fp32 within a few
+ * layers (the SwiGLU is quadratic in x); stacked layers therefore take the
+ * normalised residual stream, out_l = x_l + MoE(norm(x_l)), the pre-norm
+ * placement of the model family (a reading: the pages do not place the norm).
+ */
+MOE_API int moe_rms_norm(const float *x, int T, int d, float eps, float *out, void *stream);
 
 /*
  * The whole layer in one call: route -> union (+ hits) -> FFN -> combine, all

@@ -53,6 +53,7 @@ _SIGNATURES = {
     "moe_expert_ffn_int4_noalloc": ([_P, ctypes.POINTER(moe_layer_int4), _P, _P, _P, _P, _I, _I, _I, _P, _P,
                                      _P, _P], _I),
     "moe_combine": ([_P, _P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "moe_rms_norm": ([_P, _I, _I, _F, _P, _P], _I),
     "moe_layer_forward": ([_P, _P, _P, ctypes.POINTER(moe_layer_int4), _P, _I, _I, _I, _F, _I, _P, _P,
                            _P, _P, _P, _SZ, _P, _P], _I),
     "moe_layer_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
@@ -243,6 +244,14 @@ def moe_combine(y_pair, y_shared, topk_w, perm, residual=None, out=None, stream=
     out = torch.empty((T, d), dtype=torch.float32, device=y_shared.device) if out is None else out
     _check(lib().moe_combine(_p(y_pair), _p(y_shared), _p(topk_w), _p(perm), _p(residual), T, k, d, _p(out),
                              _stream(stream)), "moe_combine")
+    return out
+
+
+def moe_rms_norm(x, eps: float = 1e-5, out=None, stream=None):
+    _need(x, torch.float32, "x")
+    T, d = x.shape
+    out = torch.empty_like(x) if out is None else out
+    _check(lib().moe_rms_norm(_p(x), T, d, float(eps), _p(out), _stream(stream)), "moe_rms_norm")
     return out
 
 

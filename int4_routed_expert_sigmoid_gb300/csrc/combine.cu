@@ -39,7 +39,54 @@ combine_kernel(const float4 *__restrict__ y_pair, const float4 *__restrict__ y_s
     out[id] = acc;
 }
 
+// RMS normalisation of one row per CTA: fp32 sum of squares (per-thread, then
+// warp and CTA tree), one IEEE square root and division, then x * r.  Each
+// thread reads only its own elements before and after the reduction, so out
+// may alias x.
+__global__ void __launch_bounds__(256)
+rms_norm_kernel(const float4 *x, int d4, float eps, float4 *out)
+{
+    __shared__ float part[8];
+    griddep_launch_dependents();
+    griddep_wait();   // x comes from the previous kernel
+    const float4 *xr = x + (size_t)blockIdx.x * d4;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+        const float4 v = xr[c];
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        ss = fmaf(v.z, v.z, ss);
+        ss = fmaf(v.w, v.w, ss);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((threadIdx.x & 31) == 0)
+        part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; w++)
+        tot += part[w];
+    const float r = 1.0f / sqrtf(tot / (float)(4 * d4) + eps);
+    float4 *orow = out + (size_t)blockIdx.x * d4;
+    for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+        float4 v = xr[c];
+        v.x *= r;
+        v.y *= r;
+        v.z *= r;
+        v.w *= r;
+        orow[c] = v;
+    }
+}
+
 }  // namespace
+
+int launch_rms_norm(const float *x, int T, int d, float eps, float *out, cudaStream_t s)
+{
+    return launch_pdl(rms_norm_kernel, T, 256, 0, s, reinterpret_cast<const float4 *>(x), d / 4, eps,
+                      reinterpret_cast<float4 *>(out));
+}
 
 int launch_combine(const float *y_pair, const float *y_shared, const float *w, const int32_t *perm,
                    const float *res, int T, int k, int d, float *out, cudaStream_t s)

@@ -258,6 +258,14 @@ int moe_combine(const float *y_pair, const float *y_shared, const float *topk_w,
     return launch_combine(y_pair, y_shared, topk_w, perm, residual, T, k, d, out, as_stream(stream));
 }
 
+int moe_rms_norm(const float *x, int T, int d, float eps, float *out, void *stream)
+{
+    if (!ok_ptr(x) || !ok_ptr(out) || T < 1 || T > (1 << 24) || d < 4 || d % 4 != 0 || d > (1 << 20) ||
+        !(eps >= 0.0f) || !(eps < 1e30f))
+        return MOE_ERR_INVALID_ARG;
+    return launch_rms_norm(x, T, d, eps, out, as_stream(stream));
+}
+
 size_t moe_layer_workspace_bytes(int T, int k, int E, int d, int f, int mode)
 {
     if (T < 1 || k < 1 || E < 1 || d < 1 || f < 1 || !valid_mode(mode))

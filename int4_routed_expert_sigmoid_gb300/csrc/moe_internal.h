@@ -106,6 +106,7 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s);
 // combine.cu
 int launch_combine(const float *y_pair, const float *y_shared, const float *w, const int32_t *perm,
                    const float *res, int T, int k, int d, float *out, cudaStream_t s);
+int launch_rms_norm(const float *x, int T, int d, float eps, float *out, cudaStream_t s);
 
 // tmap.cu
 // 3-D tiled tensor map over `outer` equally strided blocks of a [rows][inner] matrix.

@@ -92,6 +92,7 @@ def _declare(L: ctypes.CDLL) -> None:
                                          _P, _P, _P, _P]
     L.oracle_moe_layer_union.restype = _I
     L.oracle_threads.restype = _I
+    L.oracle_rms_norm.argtypes = [_P, _I, _I, _D, _P]
 
 
 def _c(a: np.ndarray, dtype) -> np.ndarray:
@@ -226,6 +227,17 @@ def expert_ffn_tokens(x, tokens, q_e, s_e, d: int, f: int, G: int) -> np.ndarray
     lib().oracle_expert_ffn_tokens(_ptr(x), _ptr(tokens), tokens.size, _ptr(q_e), _ptr(s_e),
                                    d, f, G, _ptr(y))
     return y
+
+
+# ----------------------------------------------------------------- stack ----
+
+def rms_norm(x: np.ndarray, eps: float = 1e-5) -> np.ndarray:
+    """Rows of x divided by their RMS (unit weight), fp64: the input of a stacked layer."""
+    x = _c(x, np.float32)
+    T, d = x.shape
+    out = np.empty((T, d), dtype=np.float64)
+    lib().oracle_rms_norm(_ptr(x), T, d, float(eps), _ptr(out))
+    return out
 
 
 # ----------------------------------------------------------------- layer ----

@@ -435,6 +435,30 @@ ORACLE_API int oracle_moe_layer_union(const oracle_layer *L, int32_t *idx, doubl
     return 0;
 }
 
+/* ------------------------------------------------------- layer stack ---- */
+
+/* RMS normalisation of each row before a stacked MoE layer:
+ *   n[t][i] = x[t][i] / sqrt( (1/d) sum_i x[t][i]^2 + eps ),  unit weight.
+ * [arch] keeps the norms of the dense part in fp32; a stack of MoE layers with
+ * nothing between them is not defined numerically (the SwiGLU is quadratic in
+ * x, so activations overflow fp32 within four layers at the stated weight
+ * distribution).  Reading: each stacked layer sees the RMS-normalised residual
+ * stream, out_l = x_l + MoE(norm(x_l)), the pre-norm placement of the model
+ * family.  Returns fp64 rows; the layer input is their fp32 rounding. */
+ORACLE_API void oracle_rms_norm(const float *x, int T, int d, double eps, double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; t++) {
+        const float *xr = x + (int64_t)t * d;
+        double ss = 0.0;
+        for (int i = 0; i < d; i++)
+            ss += (double)xr[i] * (double)xr[i];
+        const double r = 1.0 / sqrt(ss / d + eps);
+        for (int i = 0; i < d; i++)
+            out[(int64_t)t * d + i] = (double)xr[i] * r;
+    }
+}
+
 /* Thread count the OpenMP runtime will use (1 without OpenMP). */
 #ifdef _OPENMP
 #include <omp.h>

@@ -55,6 +55,12 @@ def test_host_validation_rejects_without_launching(m):
     assert L.moe_union(P, 1, 2, 8, P, P, P, P, P, P, P, P, P) == m.MOE_ERR_INVALID_ARG
     assert L.moe_hits(P, 8, P, P) == m.MOE_ERR_INVALID_ARG
     assert L.moe_combine(P, P, P, P, P, 1, 2, 256, P, P) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_rms_norm(P, 1, 256, 1e-5, P, P) == m.MOE_ERR_INVALID_ARG
+    ok = ctypes.c_void_p(0x10000)   # aligned, never dereferenced: the sizes are refused first
+    assert L.moe_rms_norm(ok, 1, 6, 1e-5, ok, P) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_rms_norm(ok, 0, 256, 1e-5, ok, P) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_rms_norm(ok, 1, 256, -1.0, ok, P) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_rms_norm(ok, 1, 256, float("nan"), ok, P) == m.MOE_ERR_INVALID_ARG
     assert L.moe_layer_forward(P, P, P, None, P, 1, 2, 1, 1.0, 0, P, P, P, P, P, 0, P, P) == m.MOE_ERR_INVALID_ARG
     # a layer with an unsupported group size is refused before its pointers are used
     fake = m._binding.moe_layer_int4(16, 16, 16, 16, 8, 256, 128, 64)

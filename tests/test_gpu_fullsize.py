@@ -17,6 +17,11 @@ from moe_testlib import (TOL_DECODE, TOL_PREFILL, check_union_equal, compare_rou
 
 pytestmark = pytest.mark.gpu
 
+# fp32 norm vs fp64: the sum of squares carries <= ~37 roundings (24 per thread,
+# 5 warp and 8 CTA levels), the square root, division and product 2 more, so
+# |error| <= ~40 * 2^-24 * max|x_n| with max|x_n| ~ 4.5 for Gaussian rows.
+TOL_NORM = 1.2e-5
+
 FULL = workloads.WORKLOADS["decode"]
 E, K, D, F, G = FULL.E, FULL.k, FULL.d, FULL.f, FULL.G
 
@@ -167,50 +172,58 @@ def test_prefill_t4096(full):
 
 
 def test_stack_8_layers(full):
-    """8 resident-shape layers with the residual stream and a per-layer Zipf permutation.
+    """8 resident-shape layers, each out_l = x_l + MoE(norm(x_l)) with a per-layer Zipf permutation.
 
-    T = 4 (small-batch path) and T = 16 (general decode path) run end to end: the
-    oracle carries its own x_l through all 8 layers and every token is compared at
-    every layer.  T = 256 runs teacher-forced: the oracle routes every token from
-    the GPU's x_l and evaluates a sample of tokens."""
-    del full   # weights of layer 0 are regenerated with the stack's per-layer seeds
+    Every layer is checked teacher-forced (the oracle takes the GPU's x_l and its
+    normalised copy) at the layer tolerance: T = 4 (small-batch path) and T = 16
+    (general decode path) on every token, T = 256 on every token's routing and a
+    sample of outputs.  T = 4 and 16 also run end to end (the oracle carries its
+    own x_l through all 8 layers); there the error of earlier layers is carried
+    forward by the residual, so layer l is held to (l + 1) times the tolerance,
+    and a layer whose routing diverged on a flagged near-tie is reported."""
+    del full   # layer 0 is regenerated with the stack's per-layer seeds
     m = moe()
     sh = workloads.WORKLOADS["stack"]
+    eps = 1e-5
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     Ts = (4, 16, 256)
     x_gpu = {T: workloads.activations(T, D, seed=0) for T in Ts}
     x_orc = {T: x_gpu[T].copy() for T in Ts if T <= 16}
-    diverged = []
+    diverged = set()
     for layer in range(sh.layers):
         L = workloads.layer_inputs(sh, seed=0, layer=layer, T=1, threads=16)
         lw = m.LayerWeights(t(L.q_base.reshape(-1)), t(L.s_base.reshape(-1)), t(L.shared_q), t(L.shared_s),
                             E=E, d=D, f=F, G=G)
         wg_d, bias = t(L.wg), L.bias
         for T in Ts:
-            r = _fused(lw, wg_d, x_gpu[T], bias, m.MOE_MODE_DECODE, res=x_gpu[T])
+            xn_gpu = host(m.moe_rms_norm(t(x_gpu[T]), eps))
+            assert rel_max_err(xn_gpu, oracle.rms_norm(x_gpu[T], eps)) <= TOL_NORM
+            r = _fused(lw, wg_d, xn_gpu, bias, m.MOE_MODE_DECODE, res=x_gpu[T])
             assert r["err"] == 0
             assert np.array_equal(r["hits"], oracle.union(r["idx"], E)["counts"].astype(np.int64))
+            # teacher-forced: the oracle on the GPU's own layer input
+            o_idx, o_w, _, keys = oracle.route(xn_gpu, L.wg, bias, K)
+            same, _ = compare_routing(r["idx"], r["w"], o_idx, o_w, keys, K)
+            toks = np.arange(T, dtype=np.int32) if T <= 16 else _sample(T, 6, seed=layer, must=(T - 1,))
+            toks = toks[same[toks]]
+            _, _, o_out = _oracle(L, xn_gpu, bias, res=x_gpu[T]).tokens(toks)
+            err = rel_max_err(r["out"][toks], o_out)
+            assert err <= TOL_DECODE, f"layer {layer} T={T} (teacher-forced): {err:.3e}"
             if T <= 16:
-                o_idx, o_w, _, keys = oracle.route(x_orc[T], L.wg, bias, K)
-                if not np.array_equal(o_idx, r["idx"]):
-                    flagged = near_tie_tokens(keys, K)
-                    assert flagged[(o_idx != r["idx"]).any(axis=1)].all(), f"layer {layer} T={T}"
-                    diverged.append((layer, T))
-                _, _, o_out = _oracle(L, x_orc[T], bias, res=x_orc[T]).dense()
-                if (layer, T) not in diverged and not any(dt == T for _, dt in diverged):
-                    err = rel_max_err(r["out"], o_out)
-                    assert err <= TOL_DECODE, f"layer {layer} T={T}: {err:.3e}"
-                x_orc[T] = o_out.astype(np.float32)
-            else:
-                o_idx, o_w, _, keys = oracle.route(x_gpu[T], L.wg, bias, K)
-                same, _ = compare_routing(r["idx"], r["w"], o_idx, o_w, keys, K)
-                toks = _sample(T, 6, seed=layer, must=(T - 1,))
-                toks = toks[same[toks]]
-                _, _, o_out = _oracle(L, x_gpu[T], bias, res=x_gpu[T]).tokens(toks)
-                err = rel_max_err(r["out"][toks], o_out)
-                assert err <= TOL_DECODE, f"layer {layer} T={T} (teacher-forced): {err:.3e}"
+                # end to end: the oracle's own stream
+                xn_o = oracle.rms_norm(x_orc[T], eps).astype(np.float32)
+                e_idx, _, _, e_keys = oracle.route(xn_o, L.wg, bias, K)
+                if not np.array_equal(e_idx, r["idx"]):
+                    flagged = near_tie_tokens(e_keys, K)
+                    assert flagged[(e_idx != r["idx"]).any(axis=1)].all(), f"layer {layer} T={T}"
+                    diverged.add(T)
+                    print(f"[near-tie] end-to-end routing diverged at layer {layer}, T={T}")
+                _, _, e_out = _oracle(L, xn_o, bias, res=x_orc[T]).dense()
+                if T not in diverged:
+                    e2e = rel_max_err(r["out"], e_out)
+                    print(f"[stack] layer {layer} T={T}: teacher-forced {err:.2e}, end to end {e2e:.2e}")
+                    assert e2e <= (layer + 1) * TOL_DECODE, f"layer {layer} T={T} end to end: {e2e:.3e}"
+                x_orc[T] = e_out.astype(np.float32)
             x_gpu[T] = r["out"]
         del lw, L
         torch.cuda.empty_cache()
-    if diverged:
-        print(f"[near-tie] end-to-end routing diverged at (layer, T) = {diverged}")

@@ -182,3 +182,18 @@ def test_prefill_ffn_parity(shape):
     r = run_steps(dev, k)
     same = (r["idx"] == o_idx).all(axis=1)
     assert rel_max_err(host(out_f)[same], o_out[same]) <= TOL_PREFILL
+
+
+@pytest.mark.parametrize("T,d,scale", [(1, 256, 1.0), (37, 1024, 1e-3), (5, 6144, 3e4)])
+def test_rms_norm_parity(T, d, scale):
+    """The stack's normalisation vs the oracle (fp32 vs fp64), in place and out of place."""
+    m = moe()
+    x = workloads.activations(T, d, seed=T) * np.float32(scale)
+    ref = oracle.rms_norm(x, 1e-5)
+    xd = torch.from_numpy(x).cuda()
+    out = host(m.moe_rms_norm(xd, 1e-5))
+    # <= ~40 roundings of 2^-24 relative on |x_n| <= ~4.5 (see the full-size test)
+    assert rel_max_err(out, ref) <= 1.2e-5
+    m.moe_rms_norm(xd, 1e-5, out=xd)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(xd), out)

@@ -420,3 +420,29 @@ def test_workload_generator_is_seeded_and_layer_independent():
     v = oracle.int4_unpack(a.q_base, a.q_base.size * 2)
     assert v.min() == -8 and v.max() == 7 and abs(v.mean() + 0.5) < 0.02
     assert abs(np.log(a.s_base).mean() + 4.0) < 0.01 and abs(np.log(a.s_base).std() - 0.3) < 0.01
+
+
+# ------------------------------------------------------------- stack norm ----
+
+def test_rms_norm_closed_forms():
+    """Rows worked by hand: a constant row maps to +-1; (3, -4, 0, 0) has RMS 2.5."""
+    x = np.array([[2, 2, 2, 2], [-0.5, -0.5, -0.5, -0.5], [3, -4, 0, 0], [0, 0, 0, 0]], np.float32)
+    n = oracle.rms_norm(x, eps=0.0)[:3]
+    assert np.array_equal(n[:2], np.array([[1, 1, 1, 1], [-1, -1, -1, -1]]))
+    assert np.allclose(n[2], [1.2, -1.6, 0, 0], rtol=0, atol=1e-15)
+    # with eps: c / sqrt(c^2 + eps); an all-zero row stays zero
+    e = oracle.rms_norm(x, eps=0.25)
+    assert np.allclose(e[0], 2 / np.sqrt(4.25), rtol=0, atol=1e-15)
+    assert np.allclose(e[2], np.array([3, -4, 0, 0]) / np.sqrt(6.25 + 0.25), rtol=0, atol=1e-15)
+    assert not e[3].any()
+
+
+def test_rms_norm_invariants():
+    """Unit mean square, scale invariance (exact for powers of two) and row independence."""
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((6, 384)) * rng.uniform(0.1, 100, (6, 1))).astype(np.float32)
+    n = oracle.rms_norm(x, eps=0.0)
+    assert np.allclose(np.mean(n * n, axis=1), 1.0, rtol=0, atol=1e-12)
+    assert np.array_equal(oracle.rms_norm(x * np.float32(64.0), eps=0.0), n)
+    assert np.array_equal(oracle.rms_norm(x[3:4], eps=0.0), n[3:4])
+    assert np.all(np.sign(n) == np.sign(x))
