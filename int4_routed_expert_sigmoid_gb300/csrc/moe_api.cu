@@ -46,11 +46,11 @@ bool valid_mode(int mode) { return mode == MOE_MODE_AUTO || mode == MOE_MODE_DEC
 // FFN scratch of either path (the union never has more than T*k experts).
 size_t ffn_scratch_bytes_mode(int T, int k, int d, int f, int mode);
 
-// Scratch of the decode FFN: activation fragments of x and of h, their
-// factors and bias corrections.
+// Scratch of the decode FFN: activation fragments of x (with a factor per
+// row) and of h (factors inside the fragment blocks).
 struct FfnScratch {
-    uint16_t *x_frag, *h_frag;
-    float *x_scale, *h_scale, *x_corr, *h_corr;
+    uint8_t *x_frag, *h_frag;
+    float *x_scale;
 };
 
 size_t ffn_scratch_layout(int T, int k, int d, int f, uint8_t *base, FfnScratch *out)
@@ -63,12 +63,9 @@ size_t ffn_scratch_layout(int T, int k, int d, int f, uint8_t *base, FfnScratch 
         return p;
     };
     FfnScratch s{};
-    s.x_frag = reinterpret_cast<uint16_t *>(take((size_t)T * 2 * d * sizeof(uint16_t)));
+    s.x_frag = take((size_t)T * frag_row_bytes(d, 8));
     s.x_scale = reinterpret_cast<float *>(take((size_t)T * sizeof(float)));
-    s.x_corr = reinterpret_cast<float *>(take((size_t)T * (d / 32) * 2 * sizeof(float)));
-    s.h_frag = reinterpret_cast<uint16_t *>(take(rows_h * 2 * f * sizeof(uint16_t)));
-    s.h_scale = reinterpret_cast<float *>(take(rows_h * (f / 32) * sizeof(float)));
-    s.h_corr = reinterpret_cast<float *>(take(rows_h * (f / 32) * 2 * sizeof(float)));
+    s.h_frag = take(rows_h * frag_row_bytes(f, frag_gpc_h(f)));
     if (out)
         *out = s;
     return off;
@@ -225,7 +222,7 @@ int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *
     FfnScratch sc{};
     ffn_scratch_layout(T, k, w->d, w->f, static_cast<uint8_t *>(workspace), &sc);
     const cudaStream_t s = as_stream(stream);
-    rc = launch_act_frag(x, T, w->d, sc.x_frag, sc.x_scale, sc.x_corr, s);
+    rc = launch_act_frag(x, T, w->d, sc.x_frag, sc.x_scale, s);
     if (rc != MOE_OK)
         return rc;
     DecodeFfnArgs a{};
@@ -238,10 +235,7 @@ int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *
     a.k = k;
     a.x_frag = sc.x_frag;
     a.x_scale = sc.x_scale;
-    a.x_corr = sc.x_corr;
     a.h_frag = sc.h_frag;
-    a.h_scale = sc.h_scale;
-    a.h_corr = sc.h_corr;
     a.y_pair = y_pair;
     a.y_shared = y_shared;
     a.err = err;
@@ -332,7 +326,7 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
     // launches.  Larger batches use the separate stage kernels.
     const bool small = T <= 8 && T * k <= 64 && (E + 1) / 2 >= T;
     if (small) {
-        rc = launch_router_logits_frag(x, w_gate, T, d, E, sc.logits, fs.x_frag, fs.x_scale, fs.x_corr, s);
+        rc = launch_router_logits_frag(x, w_gate, T, d, E, sc.logits, fs.x_frag, fs.x_scale, s);
         if (rc == MOE_OK)
             rc = launch_select_union(sc.logits, bias, T, E, k, normalize, route_scale, idx, wt, sc.counts,
                                      sc.offsets, sc.perm, sc.sorted_pair, sc.uniq, sc.n_uniq, hits, err, s);
@@ -344,7 +338,7 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
             rc = launch_union(idx, T, k, E, sc.counts, sc.offsets, sc.perm, sc.sorted_pair, sc.uniq,
                               sc.n_uniq, hits, err, s);
         if (rc == MOE_OK)
-            rc = launch_act_frag(x, T, d, fs.x_frag, fs.x_scale, fs.x_corr, s);
+            rc = launch_act_frag(x, T, d, fs.x_frag, fs.x_scale, s);
     }
     if (rc != MOE_OK)
         return rc;
@@ -358,10 +352,7 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
     a.k = k;
     a.x_frag = fs.x_frag;
     a.x_scale = fs.x_scale;
-    a.x_corr = fs.x_corr;
     a.h_frag = fs.h_frag;
-    a.h_scale = fs.h_scale;
-    a.h_corr = fs.h_corr;
     a.y_pair = sc.y_pair;
     a.y_shared = sc.y_shared;
     a.err = err;

@@ -14,20 +14,39 @@ namespace moe {
 // Activation fragment layout ("frag"): the B operand of the decode FFN's
 // m16n8k16 fp16 MMAs, precomputed once per activation row.
 //
-// A row of K fp32 values, scaled by a power of two (per row for x, per
-// 32-element group for h; the inverse is kept in a factor array) so that
-// |v| < 2^14, becomes two planes (hi = fp16(v), lo = fp16(v - hi)), each
-// [K/32 groups][4 quads][8 fp16]; row stride 2*K.  Quad t of group g holds
-// elements 32g + 8t + o at position frag_pos(o), o = 0..7, i.e. in the order
-// {0,4,1,5,2,6,3,7}: the order in which the MMA's k index meets the nibbles
-// of a packed 32-bit weight word.  Elements with odd o are stored divided by
-// 16, because their weights enter the MMA multiplied by 16.
+// A row of K fp32 values is scaled by a power of two (per row for x, per
+// 32-element group for h; the inverse is kept as a factor) so that
+// |v| < 2^14, and split into two planes, hi = fp16(v) and lo = fp16(v - hi).
+// Within a plane, quad t of group g holds elements 32g + 8t + o at position
+// frag_pos(o), o = 0..7, i.e. in the order {0,4,1,5,2,6,3,7}: the order in
+// which the MMA's k index meets the nibbles of a packed 32-bit weight word.
+// Elements with odd o are stored divided by 16, because their weights enter
+// the MMA multiplied by 16.
 //
 // The weights enter the MMA as fp16 subnormals (q + 8) * 2^-24 (times 16 at
-// odd o), so a group's MMA sum is 2^-24 * (sum q v + corr / 1), where
-// corr = 8 * sum_k w_k B_k (w_k = 16 at odd o, else 1; B the stored fp16
-// values) is kept per (row, group, plane) in fp32 and subtracted exactly.
+// odd o).  With corr = 8 * sum_k w_k B_k (w_k = 16 at odd o, else 1; B the
+// stored fp16 values) per (row, group, plane), an MMA whose accumulator
+// starts at -2^-24 * corr ends at 2^-24 * sum_k q_k v_k.  The fragments keep
+// -2^-24 * corr, so it can be the accumulator input directly.
+//
+// A row is stored as blocks of GPC groups (a "chunk" of 32 * GPC elements),
+// each block holding, at byte offsets:
+//   0                 hi plane  [GPC groups][4 quads][8 fp16]
+//   frag_lo(GPC)      lo plane  (64 bytes after hi: the two planes then fall
+//                               in different shared-memory banks)
+//   frag_corr(GPC)    [GPC][2] fp32: -2^-24 * corr of hi and lo
+//   frag_fac(GPC)     [GPC] fp32: per-group factor (h only)
+// so one stage of the pipeline copies one token's blocks with a single bulk
+// copy.  x rows use GPC = 8; h rows GPC = 8 when f is a multiple of 256, else 4.
 // ---------------------------------------------------------------------------
+__host__ __device__ constexpr int frag_lo(int gpc) { return gpc * 64 + 64; }
+__host__ __device__ constexpr int frag_corr(int gpc) { return 2 * gpc * 64 + 64; }
+__host__ __device__ constexpr int frag_fac(int gpc) { return frag_corr(gpc) + gpc * 8; }
+__host__ __device__ constexpr int frag_blk(int gpc) { return frag_fac(gpc) + gpc * 4; }
+__host__ __device__ constexpr int frag_gpc_h(int f) { return f % 256 == 0 ? 8 : 4; }
+static_assert(frag_blk(8) % 16 == 0 && frag_blk(4) % 16 == 0, "bulk copies move 16-byte multiples");
+// Bytes of one fragment row of K elements with GPC groups per block.
+__host__ __device__ constexpr size_t frag_row_bytes(int K, int gpc) { return (size_t)(K / (32 * gpc)) * frag_blk(gpc); }
 __host__ __device__ constexpr int frag_pos(int o) { return 2 * (o & 3) + (o >> 2); }
 
 // Error propagation helper for launchers.
@@ -57,11 +76,11 @@ int launch_router_logits(const float *x, const float *wg, int T, int d, int E, f
                          cudaStream_t s);
 // logits plus the FFN fragments of x in one kernel (T <= 8)
 int launch_router_logits_frag(const float *x, const float *wg, int T, int d, int E, float *logits,
-                              uint16_t *frag, float *row_scale, float *corr, cudaStream_t s);
+                              uint8_t *frag, float *row_scale, cudaStream_t s);
 int launch_router_topk(const float *logits, const float *bias, int T, int E, int k, int normalize,
                        float route_scale, int32_t *idx, float *w, cudaStream_t s);
-int launch_act_frag(const float *x, int rows, int K, uint16_t *frag, float *row_scale, float *corr,
-                    cudaStream_t s);
+// fragments (GPC = 8) of `rows` rows of x [rows][K], K a multiple of 256
+int launch_act_frag(const float *x, int rows, int K, uint8_t *frag, float *row_scale, cudaStream_t s);
 
 // union.cu
 int launch_union(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
@@ -79,12 +98,9 @@ struct DecodeFfnArgs {
     const moe_layer_int4 *w;
     const int32_t *offsets, *sorted_pair, *uniq, *n_uniq;
     int T, k;
-    const uint16_t *x_frag;   // [T][2*d] fp16 frag layout
+    const uint8_t *x_frag;    // [T] rows of frag_row_bytes(d, 8)
     const float *x_scale;     // [T] per-row factor of x_frag
-    const float *x_corr;      // [T][d/32][2] bias corrections of x_frag
-    uint16_t *h_frag;         // [T*k + T][2*f] fp16 frag layout (scratch)
-    float *h_scale;           // [T*k + T][f/32] per-group factor of h_frag (scratch)
-    float *h_corr;            // [T*k + T][f/32][2] bias corrections of h_frag (scratch)
+    uint8_t *h_frag;          // [T*k + T] rows of frag_row_bytes(f, frag_gpc_h(f)) (scratch)
     float *y_pair, *y_shared;
     int32_t *err;
 };

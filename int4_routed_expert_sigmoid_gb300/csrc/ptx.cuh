@@ -72,6 +72,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     }
 }
 
+// As mbar_wait, but also gives up as soon as *abort is set (another role of
+// the CTA already timed out, so nothing more will arrive).
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, const volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort)
+            return false;
+        if (global_timer_ns() - t0 > kWaitTimeoutNs)
+            return false;
+    }
+}
+
 // 3-D tiled TMA load global -> shared, completion signalled on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int c0, int c1, int c2,
                                             uint32_t bar)

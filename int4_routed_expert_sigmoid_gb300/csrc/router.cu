@@ -16,8 +16,8 @@
 namespace moe {
 namespace {
 
-__device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint16_t *__restrict__ frag,
-                             float *__restrict__ row_scale, float *__restrict__ corr);
+__device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint8_t *__restrict__ frag,
+                             float *__restrict__ row_scale);
 
 // ----------------------------------------------------------------- logits ---
 // Small T: each CTA owns kEB experts x kTB tokens and splits the reduction
@@ -26,7 +26,7 @@ constexpr int kEB = 2, kTB = 8, kSkinnyThreads = 256;
 
 __global__ void __launch_bounds__(kSkinnyThreads)
 logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, int T, int d, int E,
-                     float *__restrict__ logits, uint16_t *frag, float *row_scale, float *corr)
+                     float *__restrict__ logits, uint8_t *frag, float *row_scale)
 {
     griddep_launch_dependents();
     griddep_wait();   // x may come from the previous kernel in the stream
@@ -88,7 +88,7 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
     // fused path: the first T blocks also build the FFN's fragments of x
     if (frag != nullptr && blockIdx.y == 0 && blockIdx.x < T) {
         __syncthreads();
-        act_frag_row(x, blockIdx.x, d, frag, row_scale, corr);
+        act_frag_row(x, blockIdx.x, d, frag, row_scale);
     }
 }
 
@@ -162,13 +162,15 @@ topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, in
 // One CTA per row: the row's max |x| picks a power of two 2^(14-e) that brings
 // every element below 2^14 (exact scaling); elements at odd offsets within
 // each 8 are further divided by 16.  Each value becomes hi = fp16(v),
-// lo = fp16(v - hi); row_scale[r] = 2^(e-14) undoes the scaling and
-// corr[r][g][plane] = 8 * sum (16 at odd offsets, else 1) * stored value.
+// lo = fp16(v - hi); row_scale[r] = 2^(e-14) undoes the scaling.  The row is
+// written as fragment blocks of 8 groups (layout in moe_internal.h), with the
+// accumulator inputs -2^-24 * 8 * sum (16 at odd offsets, else 1) * value.
 constexpr int kFragThreads = 256;
+constexpr int kXGpc = 8;
 
 // Fragments of row r of x, computed by the whole (256-thread) block.
-__device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint16_t *__restrict__ frag,
-                             float *__restrict__ row_scale, float *__restrict__ corr)
+__device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint8_t *__restrict__ frag,
+                             float *__restrict__ row_scale)
 {
     __shared__ float wmax[kFragThreads / 32];
     const float *xr = x + (size_t)r * K;
@@ -193,12 +195,14 @@ __device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint16_t
     const float up = mx > 0.f ? ldexpf(1.0f, 14 - e) : 1.0f;
     if (threadIdx.x == 0)
         row_scale[r] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
-    uint16_t *row = frag + (size_t)r * 2 * K;
+    uint8_t *row = frag + (size_t)r * frag_row_bytes(K, kXGpc);
     const int n = (K / 32) * 4;                       // (group, quad) pairs; quads of a group are adjacent ids
     const int n_pad = (n + 31) / 32 * 32;             // whole warps take part in the shuffles
     for (int id = threadIdx.x; id < n_pad; id += kFragThreads) {
         const bool act = id < n;
         const int g = id >> 2, q = id & 3;
+        uint8_t *blk = row + (size_t)(g / kXGpc) * frag_blk(kXGpc);
+        const int gl = g % kXGpc;
         float chi = 0.f, clo = 0.f;
         if (act) {
             const float4 *src = reinterpret_cast<const float4 *>(xr + 32 * g + 8 * q);
@@ -218,30 +222,26 @@ __device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint16_t
                 chi += wgt * __half2float(h);
                 clo += wgt * __half2float(l);
             }
-            *reinterpret_cast<uint4 *>(row + (size_t)id * 8) = *reinterpret_cast<const uint4 *>(hi);
-            *reinterpret_cast<uint4 *>(row + K + (size_t)id * 8) = *reinterpret_cast<const uint4 *>(lo);
+            *reinterpret_cast<uint4 *>(blk + gl * 64 + q * 16) = *reinterpret_cast<const uint4 *>(hi);
+            *reinterpret_cast<uint4 *>(blk + frag_lo(kXGpc) + gl * 64 + q * 16) =
+                *reinterpret_cast<const uint4 *>(lo);
         }
         chi += __shfl_xor_sync(0xffffffffu, chi, 1);
         clo += __shfl_xor_sync(0xffffffffu, clo, 1);
         chi += __shfl_xor_sync(0xffffffffu, chi, 2);
         clo += __shfl_xor_sync(0xffffffffu, clo, 2);
         if (act && q == 0) {
-            corr[((size_t)r * (K / 32) + g) * 2 + 0] = chi;
-            corr[((size_t)r * (K / 32) + g) * 2 + 1] = clo;
+            float *c = reinterpret_cast<float *>(blk + frag_corr(kXGpc)) + gl * 2;
+            c[0] = -chi * 0x1p-24f;
+            c[1] = -clo * 0x1p-24f;
         }
     }
 }
 
-// One CTA per row: the row's max |x| picks a power of two 2^(14-e) that brings
-// every element below 2^14 (exact scaling); elements at odd offsets within
-// each 8 are further divided by 16.  Each value becomes hi = fp16(v),
-// lo = fp16(v - hi); row_scale[r] = 2^(e-14) undoes the scaling and
-// corr[r][g][plane] = 8 * sum (16 at odd offsets, else 1) * stored value.
 __global__ void __launch_bounds__(kFragThreads)
-act_frag_kernel(const float *__restrict__ x, int K, uint16_t *__restrict__ frag,
-                float *__restrict__ row_scale, float *__restrict__ corr)
+act_frag_kernel(const float *__restrict__ x, int K, uint8_t *__restrict__ frag, float *__restrict__ row_scale)
 {
-    act_frag_row(x, blockIdx.x, K, frag, row_scale, corr);
+    act_frag_row(x, blockIdx.x, K, frag, row_scale);
 }
 
 }  // namespace
@@ -254,19 +254,19 @@ int launch_router_logits(const float *x, const float *wg, int T, int d, int E, f
         logits_tiled_kernel<<<grid, 256, 0, s>>>(x, wg, T, d, E, logits);
     } else {
         dim3 grid((E + kEB - 1) / kEB, (T + kTB - 1) / kTB);
-        logits_skinny_kernel<<<grid, kSkinnyThreads, 0, s>>>(x, wg, T, d, E, logits, nullptr, nullptr, nullptr);
+        logits_skinny_kernel<<<grid, kSkinnyThreads, 0, s>>>(x, wg, T, d, E, logits, nullptr, nullptr);
     }
     return cuda_status(cudaGetLastError());
 }
 
 int launch_router_logits_frag(const float *x, const float *wg, int T, int d, int E, float *logits,
-                              uint16_t *frag, float *row_scale, float *corr, cudaStream_t s)
+                              uint8_t *frag, float *row_scale, cudaStream_t s)
 {
     const int grid = (E + kEB - 1) / kEB;
     if (T > kTB || grid < T)
         return MOE_ERR_UNSUPPORTED;
     return launch_pdl(logits_skinny_kernel, grid, kSkinnyThreads, 0, s, x, wg, T, d, E, logits, frag,
-                      row_scale, corr);
+                      row_scale);
 }
 
 int launch_router_topk(const float *logits, const float *bias, int T, int E, int k, int normalize,
@@ -286,12 +286,11 @@ int launch_router_topk(const float *logits, const float *bias, int T, int E, int
     return cuda_status(cudaGetLastError());
 }
 
-int launch_act_frag(const float *x, int rows, int K, uint16_t *frag, float *row_scale, float *corr,
-                    cudaStream_t s)
+int launch_act_frag(const float *x, int rows, int K, uint8_t *frag, float *row_scale, cudaStream_t s)
 {
     if (rows <= 0)
         return MOE_OK;
-    act_frag_kernel<<<rows, kFragThreads, 0, s>>>(x, K, frag, row_scale, corr);
+    act_frag_kernel<<<rows, kFragThreads, 0, s>>>(x, K, frag, row_scale);
     return cuda_status(cudaGetLastError());
 }
 
