@@ -70,7 +70,7 @@ struct Cfg {
     static constexpr int kWeightBytes = kMats * CPS * (kQSub + kSSub);
     static constexpr int kRedBytes = kConsumerWarps * kNTM * 32 * 8;
     static constexpr int kHBufBytes = TOK * 32 * 4;
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kRedBytes + kHBufBytes;
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kRedBytes + kHBufBytes;   // + unit table
     static_assert(kStages >= 3, "ring too shallow");
     static_assert(kGpw == 2 || kGpw % 4 == 0, "scale vector loads");
     static_assert(kBOff % 16 == 0 && kTokBytes % 16 == 0, "bulk copy alignment");
@@ -127,21 +127,40 @@ struct Item {
     int pos0;     // first pair position (routed) of the expert's group
 };
 
-__device__ __forceinline__ Item decode_item(const Params &p, int i)
+// Unit table: unit 0 is the shared expert (all T tokens), unit u >= 1 the
+// union's expert uniq[u - 1]; built once per CTA in shared memory so that
+// walking the items needs no dependent global loads.
+struct Unit {
+    int expert, pos0, m;
+};
+
+__device__ __forceinline__ void load_units(const Params &p, int units, Unit *tab)
+{
+    for (int u = threadIdx.x; u < units; u += blockDim.x) {
+        Unit t;
+        if (u == 0) {
+            t.expert = -1;
+            t.pos0 = 0;
+            t.m = p.T;
+        } else {
+            const int e = p.uniq[u - 1];
+            t.expert = e;
+            t.pos0 = p.offsets[e];
+            t.m = p.offsets[e + 1] - t.pos0;
+        }
+        tab[u] = t;
+    }
+}
+
+__device__ __forceinline__ Item decode_item(const Params &p, const Unit *tab, int i)
 {
     Item it;
     const int u = i / p.tiles;
     it.tile = i - u * p.tiles;
-    if (u == 0) {
-        it.expert = -1;
-        it.m = p.T;
-        it.pos0 = 0;
-    } else {
-        const int e = p.uniq[u - 1];
-        it.expert = e;
-        it.pos0 = p.offsets[e];
-        it.m = p.offsets[e + 1] - it.pos0;
-    }
+    const Unit t = tab[u];
+    it.expert = t.expert;
+    it.pos0 = t.pos0;
+    it.m = t.m;
     return it;
 }
 
@@ -200,6 +219,14 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
 #pragma unroll
     for (int n = 0; n < NT; n++)
         acc[n][0] = acc[n][1] = 0.f;
+    // gate/up: the x factor of token t4 of each n-tile, loaded now and used in the epilogue
+    float xfac[NT];
+#pragma unroll
+    for (int n = 0; n < NT; n++) {
+        const int tl = n * 4 + t4;
+        xfac[n] = (MODE == kGateUp && (warp == 2 || warp == 3) && tl < ntok)
+                      ? p.x_scale[act_row<MODE>(p, it, t0 + tl)] : 0.f;
+    }
     const NibConst nk = {0x000F000Fu, 0x00080008u, 0x00F000F0u, 0x00800080u};
     const int nstages = p.nchunks / CPS;
 
@@ -277,7 +304,7 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
                 const int tl = n * 4 + t4;
                 if (tl >= ntok)
                     continue;
-                const float xf = p.x_scale[act_row<MODE>(p, it, t0 + tl)] * kTwo24;
+                const float xf = xfac[n] * kTwo24;
                 const float2 g0 = part(warp - 2, n), g1 = part(warp + 2, n);
                 const float2 u0 = part(warp, n), u1 = part(warp + 4, n);
                 const float gva = (g0.x + g1.x) * xf, gvb = (g0.y + g1.y) * xf;
@@ -373,8 +400,12 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
     griddep_launch_dependents();
     griddep_wait();   // routing, union and activation fragments come from the previous kernels
 
-    const int n_items = (*p.n_uniq + 1) * p.tiles;
+    const int units = *p.n_uniq + 1;
+    const int n_items = units * p.tiles;
     const int nstages = p.nchunks / CPS;
+    Unit *tab = reinterpret_cast<Unit *>(base + C::kStages * C::kStageBytes + C::kRedBytes + C::kHBufBytes);
+    load_units(p, units, tab);
+    __syncthreads();
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------- producer
@@ -382,7 +413,7 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
         uint32_t phase = 0;
         uint32_t issued = 0;   // bit s: stage s was filled at least once
         for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
-            const Item it = decode_item(p, i);
+            const Item it = decode_item(p, tab, i);
             const int npass = (it.m + TOK - 1) / TOK;
             const int z = it.expert < 0 ? 0 : it.expert;
             const int mb = it.expert < 0 ? 2 * C::kMats : 0;   // the shared expert's maps follow
@@ -390,10 +421,9 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
             for (int pass = 0; pass < npass; pass++) {
                 int t0, ntok;
                 pass_range(it.m, npass, pass, t0, ntok);
-                // lane j < ntok copies the fragment blocks of token j of this pass
+                // lane j < ntok copies the fragment blocks of token j of this pass; its row is looked up
+                // after the first stage's weight loads are issued, so the lookup overlaps them
                 const uint8_t *src = p.act;
-                if (lane < ntok)
-                    src += (size_t)act_row<MODE>(p, it, t0 + lane) * p.act_row_bytes;
                 const uint32_t tx = C::kWeightBytes + ntok * C::kTokBytes;
                 for (int c = 0; c < nstages; c++) {
                     if (lane == 0 && !abort_flag) {
@@ -420,6 +450,8 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
                                 }
                             issued |= 1u << stage;
                         }
+                        if (c == 0 && lane < ntok)
+                            src += (size_t)act_row<MODE>(p, it, t0 + lane) * p.act_row_bytes;
                         __syncwarp();   // expect_tx is posted before any copy below can complete
                         if (lane < ntok)
                             bulk_load(sb + C::kBOff + lane * C::kTokBytes, src + (size_t)c * C::kTokBytes,
@@ -480,7 +512,7 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
     const uint32_t plane_off = (cs.g & 1) * frag_lo(GPC) + cs.t4 * 16;
 
     for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
-        const Item it = decode_item(p, i);
+        const Item it = decode_item(p, tab, i);
         const int npass = (it.m + TOK - 1) / TOK;
         for (int pass = 0; pass < npass; pass++) {
             int t0, ntok;
@@ -501,45 +533,54 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
 }
 
 template <int MODE, int TOK, int CPS, int GPC>
-int launch_one(const Maps &maps, const Params &prm, int max_items, cudaStream_t s)
+int launch_one(const Maps &maps, const Params &prm, int max_items, int max_units, cudaStream_t s)
 {
     using C = Cfg<MODE, TOK, CPS, GPC>;
     auto kern = ffn_decode_kernel<MODE, TOK, CPS, GPC>;
+    const size_t smem = C::kSmem + ((size_t)max_units * sizeof(Unit) + 15) / 16 * 16;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return MOE_ERR_CUDA;
-    // per device, once: opt in to the dynamic shared memory and cache the occupancy
-    static int per_sm_cache[64] = {0};
-    int per_sm = per_sm_cache[dev];
-    if (per_sm == 0) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
+    // per device: opt in to the largest dynamic shared memory once; cache the occupancy per size
+    static bool opted[64] = {false};
+    static size_t occ_smem[64] = {0};
+    static int occ_val[64] = {0};
+    if (!opted[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(C::kSmem + 1025 * sizeof(Unit) + 16)) != cudaSuccess)
             return MOE_ERR_CUDA;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, C::kSmem) != cudaSuccess ||
+        opted[dev] = true;
+    }
+    int per_sm = occ_smem[dev] == smem ? occ_val[dev] : 0;
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess ||
             per_sm < 1)
             per_sm = 1;
-        per_sm_cache[dev] = per_sm;
+        occ_smem[dev] = smem;
+        occ_val[dev] = per_sm;
     }
     int grid = per_sm * sm_count(dev);
     if (grid > max_items)
         grid = max_items;
     if (grid < 1)
         grid = 1;
-    return launch_pdl(kern, grid, kThreads, C::kSmem, s, maps, prm);
+    return launch_pdl(kern, grid, kThreads, smem, s, maps, prm);
 }
 
 // Pass width by batch size: one token per pass for T = 1 (two k-chunks per
 // stage when the chunk count is even), else up to 4, 8 or 16 tokens.
 template <int MODE, int GPC>
-int launch_tok(const Maps &maps, const Params &prm, int max_items, int T, cudaStream_t s)
+int launch_tok(const Maps &maps, const Params &prm, int max_units, int T, cudaStream_t s)
 {
+    const int mi = max_units * prm.tiles;
     if (T == 1)
-        return prm.nchunks % 2 == 0 ? launch_one<MODE, 1, 2, GPC>(maps, prm, max_items, s)
-                                    : launch_one<MODE, 1, 1, GPC>(maps, prm, max_items, s);
+        return prm.nchunks % 2 == 0 ? launch_one<MODE, 1, 2, GPC>(maps, prm, mi, max_units, s)
+                                    : launch_one<MODE, 1, 1, GPC>(maps, prm, mi, max_units, s);
     if (T <= 4)
-        return launch_one<MODE, 4, 1, GPC>(maps, prm, max_items, s);
+        return launch_one<MODE, 4, 1, GPC>(maps, prm, mi, max_units, s);
     if (T <= 8)
-        return launch_one<MODE, 8, 1, GPC>(maps, prm, max_items, s);
-    return launch_one<MODE, 16, 1, GPC>(maps, prm, max_items, s);
+        return launch_one<MODE, 8, 1, GPC>(maps, prm, mi, max_units, s);
+    return launch_one<MODE, 16, 1, GPC>(maps, prm, mi, max_units, s);
 }
 
 }  // namespace
@@ -592,7 +633,7 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
     pg.nchunks = d / 256;
     pg.tiles = f / 32;
     pg.out_rows = f;
-    rc = launch_tok<kGateUp, 8>(gu, pg, max_experts * pg.tiles, a.T, s);
+    rc = launch_tok<kGateUp, 8>(gu, pg, max_experts, a.T, s);
     if (rc != MOE_OK)
         return rc;
 
@@ -618,8 +659,8 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
     pd.tiles = d / 64;
     pd.out_rows = d;
     if (gpc_h == 8)
-        return launch_tok<kDown, 8>(dn, pd, max_experts * pd.tiles, a.T, s);
-    return launch_tok<kDown, 4>(dn, pd, max_experts * pd.tiles, a.T, s);
+        return launch_tok<kDown, 8>(dn, pd, max_experts, a.T, s);
+    return launch_tok<kDown, 4>(dn, pd, max_experts, a.T, s);
 }
 
 }  // namespace moe

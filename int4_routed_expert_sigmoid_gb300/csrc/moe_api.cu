@@ -324,7 +324,7 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
     // Small batches: logits + fragments of x in one grid, then top-k + union +
     // hits in one block; the kernels are chained with programmatic dependent
     // launches.  Larger batches use the separate stage kernels.
-    const bool small = T <= 8 && T * k <= 64 && (E + 1) / 2 >= T;
+    const bool small = T <= 8 && T * k <= 64;
     if (small) {
         rc = launch_router_logits_frag(x, w_gate, T, d, E, sc.logits, fs.x_frag, fs.x_scale, s);
         if (rc == MOE_OK)

@@ -1,5 +1,5 @@
-// route_common.cuh -- warp-level top-k of one token's router logits, shared by
-// the stand-alone top-k kernel and the fused select+union kernel.
+// route_common.cuh -- block-level top-k of up to 8 tokens' router logits,
+// shared by the stand-alone top-k kernel and the fused select+union kernel.
 //
 // Source: "Public Colibri Observation and Revision Ledger", "Exact Architecture
 // and Data-Flow Reconstruction" (sigmoid router scores every expert; the top
@@ -13,72 +13,107 @@
 
 namespace moe {
 
-// One warp: lane l holds experts l, l+32, ...; k rounds of a warp arg-max on
-// (key desc, id asc) pick the experts in order.  Writes idx[0..k) and w[0..k).
-template <int EPL>
-__device__ __forceinline__ void topk_warp(const float *__restrict__ lrow, const float *__restrict__ bias,
-                                          int E, int k, int normalize, float route_scale,
-                                          int32_t *__restrict__ idx, float *__restrict__ w)
+constexpr int kTopkThreads = 256;   // threads of a block running topk_block
+constexpr int kTopkTokens = 8;      // tokens per block
+
+// sigmoid(l) = 1 / (1 + e^-l); the reciprocal is correctly rounded, as a division would be.
+__device__ __forceinline__ float router_score(float l) { return __frcp_rn(1.0f + expf(-l)); }
+
+// (key, id) ranks before (key', id') in selection order.
+__device__ __forceinline__ bool key_before(float ka, int ea, float kb, int eb)
 {
-    const int lane = threadIdx.x & 31;
-    float key[EPL], score[EPL];
-    uint32_t live = 0;
-#pragma unroll
-    for (int i = 0; i < EPL; i++) {
-        const int e = lane + 32 * i;
-        if (e < E) {
-            const float l = lrow[e];
-            score[i] = 1.0f / (1.0f + expf(-l));
-            key[i] = score[i] + (bias ? bias[e] : 0.0f);
-            live |= 1u << i;
-        } else {
-            score[i] = 0.f;
-            key[i] = -FLT_MAX;
-        }
-    }
-    float my_score = 0.f;   // lane j keeps the score of slot j
-    for (int j = 0; j < k; j++) {
-        float bk = -INFINITY, bs = 0.f;
-        int be = INT_MAX;
-#pragma unroll
-        for (int i = 0; i < EPL; i++) {
-            const int e = lane + 32 * i;
-            if ((live >> i) & 1u) {
-                if (key[i] > bk || (key[i] == bk && e < be)) {
-                    bk = key[i];
-                    be = e;
-                    bs = score[i];
-                }
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-            if (ok > bk || (ok == bk && oe < be)) {
-                bk = ok;
-                be = oe;
-                bs = os;
-            }
-        }
-        if ((be & 31) == lane)
-            live &= ~(1u << (be >> 5));
-        if (lane == j)
-            my_score = bs;
-        if (lane == 0)
-            idx[j] = be;
-    }
-    float scale = 1.0f;
-    if (normalize) {
-        float sum = 0.f;
-        for (int j = 0; j < k; j++)
-            sum += __shfl_sync(0xffffffffu, my_score, j);
-        scale = route_scale / sum;
-    }
-    if (lane < k)
-        w[lane] = normalize ? my_score * scale : my_score;
+    return ka > kb || (ka == kb && ea < eb);
 }
 
+// Dynamic shared memory of topk_block: keys [8][E] and, per token, the
+// candidates followed by the k result slots.
+__host__ __device__ constexpr int topk_cand_cap(int E, int k) { return ((E + 31) / 32) * (k < 32 ? k : 32); }
+__host__ __device__ constexpr int topk_cand_stride(int E, int k) { return topk_cand_cap(E, k) + 32; }
+__host__ __device__ constexpr size_t topk_smem_bytes(int E, int k)
+{
+    return (size_t)kTopkTokens * E * 4 + (size_t)kTopkTokens * topk_cand_stride(E, k) * 4;
+}
+
+// Top-k of tokens t0 .. t0 + nt - 1 (nt <= 8) by the whole block (256 threads):
+//  1. every (token, expert) key into shared memory (one thread each);
+//  2. per 32-expert block, each expert's rank within the block; the block's
+//     first k (at most) become candidates -- every expert of the overall top-k
+//     is among its block's top-k;
+//  3. every candidate is ranked among its token's candidates (one thread
+//     each); rank j < k fills slot j; one warp per token forms the weights.
+// Writes idx/w rows of the tokens and, when sel is not null, the ids to
+// sel[(t - t0) * k + j].  Called by all threads of the block (it synchronises).
+__device__ __forceinline__ void topk_block(const float *__restrict__ logits, const float *__restrict__ bias,
+                                           int t0, int nt, int E, int k, int normalize, float route_scale,
+                                           int32_t *__restrict__ idx, float *__restrict__ w, int *sel,
+                                           uint8_t *smem)
+{
+    float *keys = reinterpret_cast<float *>(smem);                   // [8][E]
+    int *cand = reinterpret_cast<int *>(smem + (size_t)kTopkTokens * E * 4);
+    const int stride = topk_cand_stride(E, k);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < nt * E; i += kTopkThreads) {
+        const int t = i / E, e = i - t * E;
+        keys[t * E + e] = router_score(logits[(size_t)(t0 + t) * E + e]) + (bias ? bias[e] : 0.0f);
+    }
+    __syncthreads();
+    const int nblk = (E + 31) / 32;
+    const int kb = k < 32 ? k : 32;
+    for (int task = warp; task < nt * nblk; task += kTopkThreads / 32) {
+        const int t = task / nblk, b = task - t * nblk;
+        const int n_in = E - b * 32 < 32 ? E - b * 32 : 32;
+        const float *kr = keys + t * E + b * 32;
+        if (lane < n_in) {
+            const float kv = kr[lane];
+            int r = 0;
+            for (int j = 0; j < n_in; j++)
+                r += key_before(kr[j], j, kv, lane) ? 1 : 0;
+            if (r < kb)
+                cand[t * stride + b * kb + r] = b * 32 + lane;
+        }
+        // a block with fewer than k experts leaves its remaining slots empty
+        if (lane >= n_in && lane < kb)
+            cand[t * stride + b * kb + lane] = -1;
+    }
+    __syncthreads();
+    const int nc = nblk * kb;
+    for (int i = tid; i < nt * nc; i += kTopkThreads) {
+        const int t = i / nc, c = i - t * nc;
+        const int *cr = cand + t * stride;
+        const int e = cr[c];
+        if (e < 0)
+            continue;
+        const float *kr = keys + t * E;
+        const float kv = kr[e];
+        int r = 0;
+        for (int j = 0; j < nc; j++) {
+            const int ej = cr[j];
+            r += (ej >= 0 && key_before(kr[ej], ej, kv, e)) ? 1 : 0;
+        }
+        if (r < k)
+            cand[t * stride + nc + r] = e;
+    }
+    __syncthreads();
+    if (warp < nt) {
+        const int t = warp;
+        const int my_e = lane < k ? cand[t * stride + nc + lane] : 0;
+        const float my_s = lane < k ? router_score(logits[(size_t)(t0 + t) * E + my_e]) : 0.0f;
+        float scale = 1.0f;
+        if (normalize) {
+            float sum = my_s;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            scale = route_scale / sum;
+        }
+        if (lane < k) {
+            idx[(size_t)(t0 + t) * k + lane] = my_e;
+            w[(size_t)(t0 + t) * k + lane] = normalize ? my_s * scale : my_s;
+            if (sel)
+                sel[t * k + lane] = my_e;
+        }
+    }
+    __syncthreads();
+}
 
 }  // namespace moe

@@ -16,8 +16,8 @@
 namespace moe {
 namespace {
 
-__device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint8_t *__restrict__ frag,
-                             float *__restrict__ row_scale);
+__device__ void act_frag_row(const float *__restrict__ x, int r, int K, int id0, int id1,
+                             uint8_t *__restrict__ frag, float *__restrict__ row_scale);
 
 // ----------------------------------------------------------------- logits ---
 // Small T: each CTA owns kEB experts x kTB tokens and splits the reduction
@@ -68,6 +68,8 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
     for (int a = 0; a < kEB; a++)
 #pragma unroll
         for (int b = 0; b < kTB; b++) {
+            if (b >= nt)
+                continue;
             float v = acc[a][b];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1)
@@ -86,10 +88,14 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
         }
     }
     // fused path: the first T blocks also build the FFN's fragments of x
-    if (frag != nullptr && blockIdx.y == 0 && blockIdx.x < T) {
-        __syncthreads();
-        act_frag_row(x, blockIdx.x, d, frag, row_scale);
-    }
+    // (256-element chunks of the rows, spread over the blocks)
+    const int chunks = d / 256;
+    if (frag != nullptr && blockIdx.y == 0)
+        for (int wu = blockIdx.x; wu < T * chunks; wu += gridDim.x) {
+            __syncthreads();
+            const int r = wu / chunks, c = wu - r * chunks;
+            act_frag_row(x, r, d, c * 32, c * 32 + 32, frag, row_scale);
+        }
 }
 
 // Large T: register-tiled fp32 GEMM, C[T][E] = X[T][d] * Wg[E][d]^T.
@@ -146,16 +152,15 @@ logits_tiled_kernel(const float *__restrict__ x, const float *__restrict__ wg, i
 }
 
 // ------------------------------------------------------------------ top-k ---
-template <int EPL>
-__global__ void __launch_bounds__(256)
+// One block per 8 tokens (see topk_block).
+__global__ void __launch_bounds__(kTopkThreads)
 topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int k,
             int normalize, float route_scale, int32_t *__restrict__ idx, float *__restrict__ w)
 {
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (t >= T)
-        return;
-    topk_warp<EPL>(logits + (size_t)t * E, bias, E, k, normalize, route_scale, idx + (size_t)t * k,
-                   w + (size_t)t * k);
+    extern __shared__ __align__(16) uint8_t tk_smem[];
+    const int t0 = blockIdx.x * kTopkTokens;
+    const int nt = min(kTopkTokens, T - t0);
+    topk_block(logits, bias, t0, nt, E, k, normalize, route_scale, idx, w, nullptr, tk_smem);
 }
 
 // --------------------------------------------------------- act fragments ---
@@ -168,9 +173,11 @@ topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, in
 constexpr int kFragThreads = 256;
 constexpr int kXGpc = 8;
 
-// Fragments of row r of x, computed by the whole (256-thread) block.
-__device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint8_t *__restrict__ frag,
-                             float *__restrict__ row_scale)
+// Fragments of (group, quad) ids [id0, id1) of row r of x, computed by the
+// whole (256-thread) block; every block reads the whole row for its maximum,
+// the block holding id 0 writes the row factor.
+__device__ void act_frag_row(const float *__restrict__ x, int r, int K, int id0, int id1,
+                             uint8_t *__restrict__ frag, float *__restrict__ row_scale)
 {
     __shared__ float wmax[kFragThreads / 32];
     const float *xr = x + (size_t)r * K;
@@ -193,13 +200,13 @@ __device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint8_t 
     int e = 0;
     frexpf(mx, &e);
     const float up = mx > 0.f ? ldexpf(1.0f, 14 - e) : 1.0f;
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0 && id0 == 0)
         row_scale[r] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
     uint8_t *row = frag + (size_t)r * frag_row_bytes(K, kXGpc);
-    const int n = (K / 32) * 4;                       // (group, quad) pairs; quads of a group are adjacent ids
-    const int n_pad = (n + 31) / 32 * 32;             // whole warps take part in the shuffles
-    for (int id = threadIdx.x; id < n_pad; id += kFragThreads) {
-        const bool act = id < n;
+    // (group, quad) ids: quads of a group are adjacent; whole warps take part in the shuffles
+    const int n_pad = id0 + (id1 - id0 + 31) / 32 * 32;
+    for (int id = id0 + threadIdx.x; id < n_pad; id += kFragThreads) {
+        const bool act = id < id1;
         const int g = id >> 2, q = id & 3;
         uint8_t *blk = row + (size_t)(g / kXGpc) * frag_blk(kXGpc);
         const int gl = g % kXGpc;
@@ -241,7 +248,7 @@ __device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint8_t 
 __global__ void __launch_bounds__(kFragThreads)
 act_frag_kernel(const float *__restrict__ x, int K, uint8_t *__restrict__ frag, float *__restrict__ row_scale)
 {
-    act_frag_row(x, blockIdx.x, K, frag, row_scale);
+    act_frag_row(x, blockIdx.x, K, 0, (K / 32) * 4, frag, row_scale);
 }
 
 }  // namespace
@@ -263,7 +270,7 @@ int launch_router_logits_frag(const float *x, const float *wg, int T, int d, int
                               uint8_t *frag, float *row_scale, cudaStream_t s)
 {
     const int grid = (E + kEB - 1) / kEB;
-    if (T > kTB || grid < T)
+    if (T > kTB)
         return MOE_ERR_UNSUPPORTED;
     return launch_pdl(logits_skinny_kernel, grid, kSkinnyThreads, 0, s, x, wg, T, d, E, logits, frag,
                       row_scale);
@@ -272,17 +279,12 @@ int launch_router_logits_frag(const float *x, const float *wg, int T, int d, int
 int launch_router_topk(const float *logits, const float *bias, int T, int E, int k, int normalize,
                        float route_scale, int32_t *idx, float *w, cudaStream_t s)
 {
-    const int blocks = (T + 7) / 8;
-    const int epl = (E + 31) / 32;
-#define MOE_TOPK(N)                                                                                \
-    topk_kernel<N><<<blocks, 256, 0, s>>>(logits, bias, T, E, k, normalize, route_scale, idx, w)
-    if (epl <= 1) MOE_TOPK(1);
-    else if (epl <= 2) MOE_TOPK(2);
-    else if (epl <= 4) MOE_TOPK(4);
-    else if (epl <= 8) MOE_TOPK(8);
-    else if (epl <= 16) MOE_TOPK(16);
-    else MOE_TOPK(32);
-#undef MOE_TOPK
+    const size_t smem = topk_smem_bytes(E, k);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    topk_kernel<<<(T + kTopkTokens - 1) / kTopkTokens, kTopkThreads, smem, s>>>(logits, bias, T, E, k, normalize,
+                                                                               route_scale, idx, w);
     return cuda_status(cudaGetLastError());
 }
 

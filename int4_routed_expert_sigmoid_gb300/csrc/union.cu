@@ -171,9 +171,9 @@ size_t union_smem_bytes(int E)
 // expert id, stable placement by counting earlier pairs of the same expert)
 // and bumps the hit counters.
 constexpr int kSelThreads = 256;
+static_assert(kSelThreads == kTopkThreads, "the select kernel runs topk_block");
 constexpr int kSelMaxPairs = 64;
 
-template <int EPL>
 __global__ void __launch_bounds__(kSelThreads)
 select_union_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int k,
                     int normalize, float route_scale, int32_t *__restrict__ idx, float *__restrict__ w,
@@ -181,93 +181,64 @@ select_union_kernel(const float *__restrict__ logits, const float *__restrict__ 
                     int32_t *__restrict__ sorted_pair, int32_t *__restrict__ uniq,
                     int32_t *__restrict__ n_uniq, uint64_t *__restrict__ hits, int32_t *__restrict__ err)
 {
-    __shared__ int cnt[kMaxE];
-    __shared__ int sidx[kSelMaxPairs];
-    __shared__ int wsum[kSelThreads / 32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ int se[kSelMaxPairs];      // expert of pair p (INT_MAX when out of range)
+    __shared__ int sfirst[kSelMaxPairs];  // 1 when pair p is the first pair of its expert
+    extern __shared__ __align__(16) uint8_t tk_smem[];
+    const int tid = threadIdx.x;
     griddep_launch_dependents();
     griddep_wait();   // logits come from the previous kernel
-    if (warp < T)
-        topk_warp<EPL>(logits + (size_t)warp * E, bias, E, k, normalize, route_scale, idx + (size_t)warp * k,
-                       w + (size_t)warp * k);
-    for (int e = tid; e < E; e += kSelThreads)
-        cnt[e] = 0;
-    __syncthreads();
+    topk_block(logits, bias, 0, T, E, k, normalize, route_scale, idx, w, se, tk_smem);
     const int P = T * k;
     if (tid < P) {
-        const int e = idx[tid];
-        sidx[tid] = e;
-        if (e >= 0 && e < E)
-            atomicAdd(&cnt[e], 1);
-        else
+        const int e = se[tid];
+        if (e < 0 || e >= E) {
             atomicOr(err, MOE_DEVERR_BAD_EXPERT);
-    }
-    __syncthreads();
-    // each thread owns 4 consecutive experts: local prefix, then a block scan
-    // of the thread totals (counts) and of the non-empty flags (uniq)
-    int c[4], fl[4], ctot = 0, ftot = 0;
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        const int e = tid * 4 + j;
-        c[j] = e < E ? cnt[e] : 0;
-        fl[j] = c[j] > 0 ? 1 : 0;
-        ctot += c[j];
-        ftot += fl[j];
-    }
-    auto excl_scan = [&](int v, int *total) {
-        int inc = v;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, inc, off);
-            if (lane >= off)
-                inc += n;
+            se[tid] = INT_MAX;
         }
-        if (lane == 31)
-            wsum[warp] = inc;
-        __syncthreads();
-        int before = 0, all = 0;
-        for (int q = 0; q < kSelThreads / 32; q++) {
-            before += q < warp ? wsum[q] : 0;
-            all += wsum[q];
-        }
-        __syncthreads();
-        *total = all;
-        return before + inc - v;
-    };
-    int ctotal = 0, ftotal = 0;
-    int cbase = excl_scan(ctot, &ctotal);
-    int fbase = excl_scan(ftot, &ftotal);
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        const int e = tid * 4 + j;
-        if (e < E) {
-            offsets[e] = cbase;
-            counts[e] = c[j];
-            cnt[e] = cbase;   // start of expert e's range (read below)
-            if (fl[j])
-                uniq[fbase] = e;
-            if (hits)
-                hits[e] += (uint64_t)c[j];
-        }
-        cbase += c[j];
-        fbase += fl[j];
-    }
-    if (tid == 0) {
-        offsets[E] = ctotal;
-        *n_uniq = ftotal;
     }
     __syncthreads();
     if (tid < P) {
-        const int e = sidx[tid];
+        const int e = se[tid];
+        int first = e != INT_MAX ? 1 : 0;
+        for (int q = 0; q < tid; q++)
+            first = se[q] == e ? 0 : first;
+        sfirst[tid] = first;
+    }
+    __syncthreads();
+    // pairs: position = (#pairs of smaller experts) + (#earlier pairs of the same expert)
+    if (tid < P) {
+        const int e = se[tid];
         int pos = -1;
-        if (e >= 0 && e < E) {
-            int rank = 0;
-            for (int q = 0; q < tid; q++)
-                rank += sidx[q] == e ? 1 : 0;
-            pos = cnt[e] + rank;
+        if (e != INT_MAX) {
+            pos = 0;
+            for (int q = 0; q < P; q++) {
+                const int eq = se[q];
+                pos += (eq < e || (eq == e && q < tid)) ? 1 : 0;
+            }
             sorted_pair[pos] = tid;
         }
         perm[tid] = pos;
+    }
+    // experts: count, exclusive offset, rank among the distinct experts, hits
+    for (int e = tid; e <= E; e += kSelThreads) {
+        int cnt = 0, before = 0, ubefore = 0;
+        for (int q = 0; q < P; q++) {
+            const int eq = se[q];
+            cnt += eq == e ? 1 : 0;
+            before += eq < e ? 1 : 0;
+            ubefore += (eq < e && sfirst[q]) ? 1 : 0;
+        }
+        offsets[e] = before;
+        if (e == E) {
+            *n_uniq = ubefore;
+            continue;
+        }
+        counts[e] = cnt;
+        if (cnt > 0) {
+            uniq[ubefore] = e;
+            if (hits)
+                hits[e] += (uint64_t)cnt;
+        }
     }
 }
 
@@ -304,19 +275,14 @@ int launch_select_union(const float *logits, const float *bias, int T, int E, in
                         int32_t *perm, int32_t *sorted_pair, int32_t *uniq, int32_t *n_uniq,
                         uint64_t *hits, int32_t *err, cudaStream_t s)
 {
-    if (T > kSelThreads / 32 || T * k > kSelMaxPairs || E > kMaxE)
+    if (T > kTopkTokens || T * k > kSelMaxPairs || E > kMaxE)
         return MOE_ERR_UNSUPPORTED;
-    const int epl = (E + 31) / 32;
-#define MOE_SEL(N)                                                                                      \
-    return launch_pdl(select_union_kernel<N>, 1, kSelThreads, 0, s, logits, bias, T, E, k, normalize,      \
-                      route_scale, idx, w, counts, offsets, perm, sorted_pair, uniq, n_uniq, hits, err)
-    if (epl <= 1) MOE_SEL(1);
-    if (epl <= 2) MOE_SEL(2);
-    if (epl <= 4) MOE_SEL(4);
-    if (epl <= 8) MOE_SEL(8);
-    if (epl <= 16) MOE_SEL(16);
-    MOE_SEL(32);
-#undef MOE_SEL
+    const size_t smem = topk_smem_bytes(E, k);
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(select_union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  (int)smem) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return launch_pdl(select_union_kernel, 1, kSelThreads, smem, s, logits, bias, T, E, k, normalize, route_scale,
+                      idx, w, counts, offsets, perm, sorted_pair, uniq, n_uniq, hits, err);
 }
 
 int launch_hits(const int32_t *counts, int E, uint64_t *hits, cudaStream_t s)
