@@ -134,6 +134,8 @@ struct Unit {
     int expert, pos0, m;
 };
 
+// (L2 loads: the down kernel reads the table before its grid wait, when the
+// union is complete but this SM's L1 may hold an older launch's copy)
 __device__ __forceinline__ void load_units(const Params &p, int units, Unit *tab)
 {
     for (int u = threadIdx.x; u < units; u += blockDim.x) {
@@ -143,10 +145,10 @@ __device__ __forceinline__ void load_units(const Params &p, int units, Unit *tab
             t.pos0 = 0;
             t.m = p.T;
         } else {
-            const int e = p.uniq[u - 1];
+            const int e = __ldcg(p.uniq + u - 1);
             t.expert = e;
-            t.pos0 = p.offsets[e];
-            t.m = p.offsets[e + 1] - t.pos0;
+            t.pos0 = __ldcg(p.offsets + e);
+            t.m = __ldcg(p.offsets + e + 1) - t.pos0;
         }
         tab[u] = t;
     }
@@ -370,6 +372,25 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
     named_bar_sync(1, kConsumerWarps * 32);   // red and hbuf are reused by the next pass
 }
 
+// Weight loads (packed rows and scales) of stage `c` of an item into ring slot sb.
+template <int MODE, int TOK, int CPS, int GPC>
+__device__ __forceinline__ void issue_weights(const Maps &maps, const Item &it, int c, uint32_t sb, uint32_t fb)
+{
+    using C = Cfg<MODE, TOK, CPS, GPC>;
+    const int z = it.expert < 0 ? 0 : it.expert;
+    const int mb = it.expert < 0 ? 2 * C::kMats : 0;   // the shared expert's maps follow
+    const int row0 = it.tile * C::kRows;
+#pragma unroll
+    for (int mat = 0; mat < C::kMats; mat++)
+#pragma unroll
+        for (int ch = 0; ch < CPS; ch++) {
+            const int cg = c * CPS + ch;
+            tma_load_3d(sb + (mat * CPS + ch) * C::kQSub, &maps.m[mb + mat], cg * C::kRowB, row0, z, fb);
+            tma_load_3d(sb + C::kSOff + (mat * CPS + ch) * C::kSSub, &maps.m[mb + C::kMats + mat], cg * GPC, row0,
+                        z, fb);
+        }
+}
+
 template <int MODE, int TOK, int CPS, int GPC>
 __global__ void __launch_bounds__(kThreads, 2)
 ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
@@ -397,27 +418,65 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
         for (int i = 0; i < 8; i++)
             prefetch_tmap(&maps.m[i]);
     __syncthreads();
-    griddep_launch_dependents();
-    griddep_wait();   // routing, union and activation fragments come from the previous kernels
-
-    const int units = *p.n_uniq + 1;
-    const int n_items = units * p.tiles;
     const int nstages = p.nchunks / CPS;
     Unit *tab = reinterpret_cast<Unit *>(base + C::kStages * C::kStageBytes + C::kRedBytes + C::kHBufBytes);
-    load_units(p, units, tab);
-    __syncthreads();
+
+    // Before waiting on the previous kernel, start the weight loads of the first stages of this
+    // CTA's first item when that item is already known: every down item (the union was complete
+    // before the gate/up kernel released this one), and a gate/up item of the shared expert
+    // (items 0 .. tiles - 1, whatever the union).  Weights do not depend on the previous kernel.
+    int units = 0;
+    if (MODE == kDown) {
+        units = __ldcg(p.n_uniq) + 1;
+        load_units(p, units, tab);
+        __syncthreads();
+    }
+    int pre = 0;   // producer: stages of the first item's first pass already holding their weights
+    if (warp == kProducerWarp) {
+        const bool known = MODE == kDown ? (int)blockIdx.x < units * p.tiles : (int)blockIdx.x < p.tiles;
+        if (known) {
+            Item it0;
+            if (MODE == kDown) {
+                it0 = decode_item(p, tab, blockIdx.x);
+            } else {
+                it0.expert = -1;
+                it0.tile = blockIdx.x;
+                it0.m = p.T;
+                it0.pos0 = 0;
+            }
+            int t0, ntok;
+            pass_range(it0.m, (it0.m + TOK - 1) / TOK, 0, t0, ntok);
+            pre = nstages < C::kStages ? nstages : C::kStages;
+            if (lane == 0)
+                for (int c = 0; c < pre; c++) {
+                    const uint32_t fb = smem_addr(&full_bar[c]);
+                    mbar_arrive_expect_tx(fb, C::kWeightBytes + ntok * C::kTokBytes);
+                    issue_weights<MODE, TOK, CPS, GPC>(maps, it0, c, stage0 + c * C::kStageBytes, fb);
+                }
+        }
+    }
+    if (MODE == kGateUp) {
+        // the down kernel reads the union before its own grid wait: release it only after ours
+        griddep_wait();   // routing, union and activation fragments come from the previous kernels
+        griddep_launch_dependents();
+        units = *p.n_uniq + 1;
+        load_units(p, units, tab);
+        __syncthreads();
+    } else {
+        griddep_launch_dependents();
+        griddep_wait();   // h comes from the gate/up kernel
+    }
+    const int n_items = units * p.tiles;
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------- producer
         int stage = 0;
         uint32_t phase = 0;
-        uint32_t issued = 0;   // bit s: stage s was filled at least once
+        uint32_t issued = (1u << pre) - 1u;   // bit s: stage s was filled at least once
+        bool first = true;
         for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
             const Item it = decode_item(p, tab, i);
             const int npass = (it.m + TOK - 1) / TOK;
-            const int z = it.expert < 0 ? 0 : it.expert;
-            const int mb = it.expert < 0 ? 2 * C::kMats : 0;   // the shared expert's maps follow
-            const int row0 = it.tile * C::kRows;
             for (int pass = 0; pass < npass; pass++) {
                 int t0, ntok;
                 pass_range(it.m, npass, pass, t0, ntok);
@@ -426,7 +485,8 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
                 const uint8_t *src = p.act;
                 const uint32_t tx = C::kWeightBytes + ntok * C::kTokBytes;
                 for (int c = 0; c < nstages; c++) {
-                    if (lane == 0 && !abort_flag) {
+                    const bool pre_issued = first && pass == 0 && c < pre;
+                    if (lane == 0 && !abort_flag && !pre_issued) {
                         if (!mbar_wait_or_abort(smem_addr(&empty_bar[stage]), phase ^ 1u, &abort_flag)) {
                             atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                             abort_flag = 1;
@@ -436,18 +496,9 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
                     if (!abort_flag) {
                         const uint32_t sb = stage0 + stage * C::kStageBytes;
                         const uint32_t fb = smem_addr(&full_bar[stage]);
-                        if (lane == 0) {
+                        if (lane == 0 && !pre_issued) {
                             mbar_arrive_expect_tx(fb, tx);
-#pragma unroll
-                            for (int mat = 0; mat < C::kMats; mat++)
-#pragma unroll
-                                for (int ch = 0; ch < CPS; ch++) {
-                                    const int cg = c * CPS + ch;
-                                    tma_load_3d(sb + (mat * CPS + ch) * C::kQSub, &maps.m[mb + mat],
-                                                cg * C::kRowB, row0, z, fb);
-                                    tma_load_3d(sb + C::kSOff + (mat * CPS + ch) * C::kSSub,
-                                                &maps.m[mb + C::kMats + mat], cg * GPC, row0, z, fb);
-                                }
+                            issue_weights<MODE, TOK, CPS, GPC>(maps, it, c, sb, fb);
                             issued |= 1u << stage;
                         }
                         if (c == 0 && lane < ntok)
@@ -463,6 +514,7 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
                     }
                 }
             }
+            first = false;
         }
         // Let every copy issued here land before the CTA may exit: stages below
         // `stage` were last filled in the current round, the rest in the

@@ -23,13 +23,13 @@ __device__ void act_frag_row(const float *__restrict__ x, int r, int K, int id0,
 // Small T: each CTA owns kEB experts x kTB tokens and splits the reduction
 // over d across its 256 threads (float4 loads), then reduces in a fixed order.
 constexpr int kEB = 2, kTB = 8, kSkinnyThreads = 256;
+constexpr int kSkinnyIt = 8;   // d up to 8192: the weight slice of a thread stays in registers
 
 __global__ void __launch_bounds__(kSkinnyThreads)
 logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, int T, int d, int E,
                      float *__restrict__ logits, uint8_t *frag, float *row_scale)
 {
     griddep_launch_dependents();
-    griddep_wait();   // x may come from the previous kernel in the stream
     const int e0 = blockIdx.x * kEB;
     const int t0 = blockIdx.y * kTB;
     const int nt = min(kTB, T - t0);
@@ -43,23 +43,53 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
             acc[a][b] = 0.f;
     const float4 *w4 = reinterpret_cast<const float4 *>(wg);
     const float4 *x4 = reinterpret_cast<const float4 *>(x);
-    for (int i = threadIdx.x; i < d4; i += kSkinnyThreads) {
-        float4 wv[kEB];
+    auto fma4 = [&](const float4 &xv, const float4 &wv, float &a) {
+        a = fmaf(xv.x, wv.x, a);
+        a = fmaf(xv.y, wv.y, a);
+        a = fmaf(xv.z, wv.z, a);
+        a = fmaf(xv.w, wv.w, a);
+    };
+    if (d4 <= kSkinnyIt * kSkinnyThreads) {
+        // the router weights do not depend on the previous kernel: all of this thread's loads are
+        // issued before waiting on it
+        float4 wv[kSkinnyIt][kEB];
 #pragma unroll
-        for (int a = 0; a < kEB; a++)
-            wv[a] = a < ne ? __ldg(w4 + (size_t)(e0 + a) * d4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int it = 0; it < kSkinnyIt; it++) {
+            const int i = threadIdx.x + it * kSkinnyThreads;
 #pragma unroll
-        for (int b = 0; b < kTB; b++) {
-            if (b < nt) {
-                const float4 xv = __ldg(x4 + (size_t)(t0 + b) * d4 + i);
+            for (int a = 0; a < kEB; a++)
+                wv[it][a] = (i < d4 && a < ne) ? __ldg(w4 + (size_t)(e0 + a) * d4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        griddep_wait();   // x may come from the previous kernel in the stream
 #pragma unroll
-                for (int a = 0; a < kEB; a++) {
-                    acc[a][b] = fmaf(xv.x, wv[a].x, acc[a][b]);
-                    acc[a][b] = fmaf(xv.y, wv[a].y, acc[a][b]);
-                    acc[a][b] = fmaf(xv.z, wv[a].z, acc[a][b]);
-                    acc[a][b] = fmaf(xv.w, wv[a].w, acc[a][b]);
+        for (int it = 0; it < kSkinnyIt; it++) {
+            const int i = threadIdx.x + it * kSkinnyThreads;
+            if (i >= d4)
+                break;
+#pragma unroll
+            for (int b = 0; b < kTB; b++)
+                if (b < nt) {
+                    const float4 xv = __ldg(x4 + (size_t)(t0 + b) * d4 + i);
+#pragma unroll
+                    for (int a = 0; a < kEB; a++)
+                        fma4(xv, wv[it][a], acc[a][b]);
                 }
-            }
+        }
+    } else {
+        griddep_wait();
+        for (int i = threadIdx.x; i < d4; i += kSkinnyThreads) {
+            float4 wv[kEB];
+#pragma unroll
+            for (int a = 0; a < kEB; a++)
+                wv[a] = a < ne ? __ldg(w4 + (size_t)(e0 + a) * d4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int b = 0; b < kTB; b++)
+                if (b < nt) {
+                    const float4 xv = __ldg(x4 + (size_t)(t0 + b) * d4 + i);
+#pragma unroll
+                    for (int a = 0; a < kEB; a++)
+                        fma4(xv, wv[a], acc[a][b]);
+                }
         }
     }
     __shared__ float part[kSkinnyThreads / 32][kEB * kTB];
