@@ -76,9 +76,14 @@ struct Cfg {
     static_assert(kBOff % 16 == 0 && kTokBytes % 16 == 0, "bulk copy alignment");
 };
 
+// Tensor maps of one half of the FFN: packed rows and scales, [0] routed
+// experts, [1] the shared expert.  A stage's box lands in shared memory as
+// [chunk][matrix][row][bytes of the chunk].  With `merged`, the chunk is a
+// dimension of the map, so one load per stage moves all nibbles (and one all
+// scales); otherwise one load per chunk.
 struct Maps {
-    CUtensorMap m[8];   // gate/up: gq, uq, gs, us (routed) then the shared expert's
-                        // down:    dq, ds (routed), dq, ds (shared)
+    CUtensorMap q[2], s[2];
+    int merged;
 };
 
 struct Params {
@@ -378,17 +383,30 @@ __device__ __forceinline__ void issue_weights(const Maps &maps, const Item &it, 
 {
     using C = Cfg<MODE, TOK, CPS, GPC>;
     const int z = it.expert < 0 ? 0 : it.expert;
-    const int mb = it.expert < 0 ? 2 * C::kMats : 0;   // the shared expert's maps follow
+    const int w = it.expert < 0 ? 1 : 0;
     const int row0 = it.tile * C::kRows;
-#pragma unroll
-    for (int mat = 0; mat < C::kMats; mat++)
-#pragma unroll
-        for (int ch = 0; ch < CPS; ch++) {
-            const int cg = c * CPS + ch;
-            tma_load_3d(sb + (mat * CPS + ch) * C::kQSub, &maps.m[mb + mat], cg * C::kRowB, row0, z, fb);
-            tma_load_3d(sb + C::kSOff + (mat * CPS + ch) * C::kSSub, &maps.m[mb + C::kMats + mat], cg * GPC, row0,
-                        z, fb);
+    const void *mq = &maps.q[w], *ms = &maps.s[w];
+    if (maps.merged) {
+        if (MODE == kGateUp) {
+            tma_load_5d(sb, mq, 0, row0, 0, c * CPS, z, fb);
+            tma_load_5d(sb + C::kSOff, ms, 0, row0, 0, c * CPS, z, fb);
+        } else {
+            tma_load_4d(sb, mq, 0, row0, c * CPS, z, fb);
+            tma_load_4d(sb + C::kSOff, ms, 0, row0, c * CPS, z, fb);
         }
+        return;
+    }
+#pragma unroll
+    for (int ch = 0; ch < CPS; ch++) {
+        const int cg = c * CPS + ch;
+        if (MODE == kGateUp) {
+            tma_load_4d(sb + ch * C::kMats * C::kQSub, mq, cg * C::kRowB, row0, 0, z, fb);
+            tma_load_4d(sb + C::kSOff + ch * C::kMats * C::kSSub, ms, cg * GPC, row0, 0, z, fb);
+        } else {
+            tma_load_3d(sb + ch * C::kQSub, mq, cg * C::kRowB, row0, z, fb);
+            tma_load_3d(sb + C::kSOff + ch * C::kSSub, ms, cg * GPC, row0, z, fb);
+        }
+    }
 }
 
 template <int MODE, int TOK, int CPS, int GPC>
@@ -415,8 +433,10 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
         fence_mbar_init();
     }
     if (warp == kProducerWarp && lane == 0)
-        for (int i = 0; i < 8; i++)
-            prefetch_tmap(&maps.m[i]);
+        for (int i = 0; i < 2; i++) {
+            prefetch_tmap(&maps.q[i]);
+            prefetch_tmap(&maps.s[i]);
+        }
     __syncthreads();
     const int nstages = p.nchunks / CPS;
     Unit *tab = reinterpret_cast<Unit *>(base + C::kStages * C::kStageBytes + C::kRedBytes + C::kHBufBytes);
@@ -556,8 +576,9 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
     uint32_t qoff[C::kGpw];
 #pragma unroll
     for (int gi = 0; gi < C::kGpw; gi++)
-        qoff[gi] = (mat * CPS + ch0) * C::kQSub + ra * C::kRowB + (((gl0 + gi) ^ swz<GPC>(ra)) << 4) + 4 * cs.t4;
-    const uint32_t soff = C::kSOff + (mat * CPS + ch0) * C::kSSub + (ra * GPC + gl0) * 4;
+        qoff[gi] = (ch0 * C::kMats + mat) * C::kQSub + ra * C::kRowB + (((gl0 + gi) ^ swz<GPC>(ra)) << 4) +
+                   4 * cs.t4;
+    const uint32_t soff = C::kSOff + (ch0 * C::kMats + mat) * C::kSSub + (ra * GPC + gl0) * 4;
     const uint32_t kb = ch0 * C::kBlk + gl0 * 64;
     const uint32_t kbc = ch0 * C::kBlk + frag_corr(GPC) + gl0 * 8;
     const uint32_t kbf = ch0 * C::kBlk + frag_fac(GPC) + gl0 * 4;
@@ -648,23 +669,57 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
     const int max_experts = (E < a.T * a.k ? E : a.T * a.k) + 1;
     int rc = MOE_OK;
 
-    // ---- gate / up
-    Maps gu{};
+    // ---- tensor maps: merged (chunk as a map dimension) when the driver accepts them, else per chunk
     const uint8_t *qs[2] = {w.q_base, w.shared_q};
     const float *ss[2] = {w.s_base, w.shared_s};
     const uint64_t outer[2] = {(uint64_t)E, 1};
+    const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const int cps_gu = (a.T == 1 && (d / 256) % 2 == 0) ? 2 : 1;
+    const int cps_dn = (a.T == 1 && (f / (32 * gpc_h)) % 2 == 0) ? 2 : 1;
+    Maps gu{}, dn{};
+    gu.merged = dn.merged = 1;
     for (int i = 0; i < 2 && rc == MOE_OK; i++) {
-        const uint8_t *q = qs[i];
-        const float *sp = ss[i];
-        rc |= make_tmap_3d(&gu.m[4 * i + 0], q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d / 2, f, outer[i],
-                           d / 2, qb, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
-        rc |= make_tmap_3d(&gu.m[4 * i + 1], q + (size_t)f * d / 2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                           d / 2, f, outer[i], d / 2, qb, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
-        rc |= make_tmap_3d(&gu.m[4 * i + 2], sp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d / G, f,
-                           outer[i], (uint64_t)(d / G) * 4, sc * 4, 8, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
-        rc |= make_tmap_3d(&gu.m[4 * i + 3], sp + (size_t)f * d / G, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
-                           d / G, f, outer[i], (uint64_t)(d / G) * 4, sc * 4, 8, 32,
-                           CU_TENSOR_MAP_SWIZZLE_NONE);
+        // gate/up: (bytes of a chunk, row, matrix, chunk, expert)
+        const uint64_t gq_dim[5] = {128, (uint64_t)f, 2, (uint64_t)d / 256, outer[i]};
+        const uint64_t gq_str[4] = {(uint64_t)d / 2, (uint64_t)f * d / 2, 128, qb};
+        const uint32_t gq_box[5] = {128, 32, 2, (uint32_t)cps_gu, 1};
+        const uint64_t gs_dim[5] = {8, (uint64_t)f, 2, (uint64_t)d / 256, outer[i]};
+        const uint64_t gs_str[4] = {(uint64_t)(d / G) * 4, (uint64_t)f * (d / G) * 4, 32, sc * 4};
+        const uint32_t gs_box[5] = {8, 32, 2, (uint32_t)cps_gu, 1};
+        // down: (bytes of a chunk, row, chunk, expert)
+        const uint64_t dq_dim[4] = {(uint64_t)16 * gpc_h, (uint64_t)d, (uint64_t)f / (32 * gpc_h), outer[i]};
+        const uint64_t dq_str[3] = {(uint64_t)f / 2, (uint64_t)16 * gpc_h, qb};
+        const uint32_t dq_box[4] = {(uint32_t)16 * gpc_h, 64, (uint32_t)cps_dn, 1};
+        const uint64_t ds_dim[4] = {(uint64_t)gpc_h, (uint64_t)d, (uint64_t)f / (32 * gpc_h), outer[i]};
+        const uint64_t ds_str[3] = {(uint64_t)(f / G) * 4, (uint64_t)gpc_h * 4, sc * 4};
+        const uint32_t ds_box[4] = {(uint32_t)gpc_h, 64, (uint32_t)cps_dn, 1};
+        if (gu.merged)
+            gu.merged = make_tmap_nd(&gu.q[i], qs[i], U8, 5, gq_dim, gq_str, gq_box, CU_TENSOR_MAP_SWIZZLE_128B) ==
+                            MOE_OK &&
+                        make_tmap_nd(&gu.s[i], ss[i], F32, 5, gs_dim, gs_str, gs_box, CU_TENSOR_MAP_SWIZZLE_NONE) ==
+                            MOE_OK;
+        if (dn.merged)
+            dn.merged = make_tmap_nd(&dn.q[i], qs[i] + (size_t)f * d, U8, 4, dq_dim, dq_str, dq_box, sw_dn) ==
+                            MOE_OK &&
+                        make_tmap_nd(&dn.s[i], ss[i] + (size_t)2 * f * d / G, F32, 4, ds_dim, ds_str, ds_box,
+                                     CU_TENSOR_MAP_SWIZZLE_NONE) == MOE_OK;
+    }
+    for (int i = 0; i < 2 && !gu.merged && rc == MOE_OK; i++) {
+        // per chunk: (row bytes, row, matrix, expert)
+        const uint64_t q_dim[4] = {(uint64_t)d / 2, (uint64_t)f, 2, outer[i]};
+        const uint64_t q_str[3] = {(uint64_t)d / 2, (uint64_t)f * d / 2, qb};
+        const uint32_t q_box[4] = {128, 32, 2, 1};
+        const uint64_t s_dim[4] = {(uint64_t)d / G, (uint64_t)f, 2, outer[i]};
+        const uint64_t s_str[3] = {(uint64_t)(d / G) * 4, (uint64_t)f * (d / G) * 4, sc * 4};
+        const uint32_t s_box[4] = {8, 32, 2, 1};
+        rc |= make_tmap_nd(&gu.q[i], qs[i], U8, 4, q_dim, q_str, q_box, CU_TENSOR_MAP_SWIZZLE_128B);
+        rc |= make_tmap_nd(&gu.s[i], ss[i], F32, 4, s_dim, s_str, s_box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    for (int i = 0; i < 2 && !dn.merged && rc == MOE_OK; i++) {
+        rc |= make_tmap_3d(&dn.q[i], qs[i] + (size_t)f * d, U8, 1, f / 2, d, outer[i], f / 2, qb, 16 * gpc_h, 64,
+                           sw_dn);
+        rc |= make_tmap_3d(&dn.s[i], ss[i] + (size_t)2 * f * d / G, F32, 4, f / G, d, outer[i],
+                           (uint64_t)(f / G) * 4, sc * 4, gpc_h, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     if (rc != MOE_OK)
         return MOE_ERR_INVALID_ARG;
@@ -689,17 +744,6 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
     if (rc != MOE_OK)
         return rc;
 
-    // ---- down
-    Maps dn{};
-    for (int i = 0; i < 2 && rc == MOE_OK; i++) {
-        rc |= make_tmap_3d(&dn.m[2 * i + 0], qs[i] + (size_t)f * d, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                           f / 2, d, outer[i], f / 2, qb, 16 * gpc_h, 64, sw_dn);
-        rc |= make_tmap_3d(&dn.m[2 * i + 1], ss[i] + (size_t)2 * f * d / G,
-                           CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, f / G, d, outer[i],
-                           (uint64_t)(f / G) * 4, sc * 4, gpc_h, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
-    }
-    if (rc != MOE_OK)
-        return MOE_ERR_INVALID_ARG;
     Params pd = pg;
     pd.act = a.h_frag;
     pd.act_row_bytes = frag_row_bytes(f, gpc_h);

@@ -134,6 +134,11 @@ int make_tmap_3d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, in
 int make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, uint64_t inner, uint64_t rows,
                  uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
+// Tiled tensor map of rank 1..5: dims and box innermost first, strides_bytes[i] the
+// byte stride of dimension i + 1 (any order of strides).
+int make_tmap_nd(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, int rank, const uint64_t *dims,
+                 const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle);
+
 // device properties cached per device
 int sm_count(int device);
 

@@ -60,6 +60,29 @@ int make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, ui
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
 }
 
+int make_tmap_nd(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, int rank, const uint64_t *dims,
+                 const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle)
+{
+    std::call_once(g_encode_once, load_encode);
+    if (!g_encode)
+        return MOE_ERR_CUDA;
+    if (rank < 1 || rank > 5)
+        return MOE_ERR_INVALID_ARG;
+    cuuint64_t d[5], st[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; i++) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+    }
+    for (int i = 0; i + 1 < rank; i++)
+        st[i] = strides_bytes[i];
+    const CUresult r = g_encode(m, dtype, (cuuint32_t)rank, const_cast<void *>(base), d, st, bx, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
 int sm_count(int device)
 {
     static int cache[64] = {0};
