@@ -8,22 +8,33 @@
 // With ~128 tokens per routed expert the FFN is a real dense contraction.
 //
 // Design (GB300, sm_103a), one CTA per SM, persistent over work items:
-//  * item = (expert unit, 128-row tile of the output matrix, tile of <= 256
-//    tokens).  D[rows][tokens] = W[rows][K] * X[tokens][K]^T ("swap AB": the
-//    weights are the M = 128 operand, the tokens the N <= 256 operand).
+//  * item = (expert unit, tile of output rows, tile of <= 256 tokens).
+//    D[rows][tokens] = W[rows][K] * X[tokens][K]^T ("swap AB": the weights
+//    are the M = 128 operand, the tokens the N operand).  Gate/up stacks 64
+//    gate rows over the same 64 up rows in one A tile (an item is 64 rows of
+//    h; one MMA per k16 serves both matrices); down takes 128 rows.  Every CTA builds the unit table
+//    (expert, first sorted row, tokens, prefix of token tiles) in shared
+//    memory once, so items are decoded without global loads.
 //  * warp 0 (producer): TMA loads of the packed int4 rows + fp32 scales
 //    (raw ring, k-blocks of 128) and of the bf16 token rows (operand ring,
 //    k-blocks of 64, 128-byte swizzle).
-//  * warps 6-9 (dequant, thread = weight row): nibbles -> fp16 / bf16 (q * s)
-//    with an exact magic-exponent conversion (fp16: 0x6400|(n^8) = 1032 + q;
-//    bf16: 0x4300|(n^8) = 136 + q; then subtract) and one multiply, written into the operand stage in the 128B-swizzled K-major
-//    layout the MMA reads.  Nibble pairs come out as (k, k+4); the token rows
-//    are stored with the same within-8 permutation, so no reshuffle is needed.
+//  * warps 6-13 (dequant, thread = row of the A tile and 32-element group):
+//    nibbles -> fp16 (q * s) with an exact magic-exponent conversion
+//    (0x6400|(n^8) = 1032 + q, then subtract) and one multiply, written straight
+//    into tensor memory: the MMA reads A from there, so shared memory carries
+//    only the raw nibbles and the token rows (the operand traffic that bounded
+//    the kernel when A went through shared memory).  Nibble pairs come out as
+//    (k, k+4); the token rows are stored with the same within-8 permutation,
+//    so no reshuffle is needed.
 //  * warp 1: allocates tensor memory; one lane issues tcgen05.mma (M = 128,
-//    N = tokens rounded up to 16, K = 16 per instruction) into fp32
-//    accumulators (gate and up: two), and commits stage releases.
-//  * warps 2-5 (epilogue, one TMEM subpartition each): gate/up ->
-//    h = silu(g) * u in fp32 plus the per-token max |h|; down -> y in fp32.
+//    N = tokens rounded up to 16, K = 16 per instruction) into an fp32
+//    accumulator, and commits stage releases.  The 512 TMEM columns hold two
+//    accumulator buffers, so the MMAs of the next item run while the
+//    epilogue drains the previous one.
+//  * warps 2-5 (epilogue, one TMEM subpartition each): gate/up -> the two
+//    up warps hand their values to the two gate warps through shared memory,
+//    which form h = silu(g) * u in fp32 plus the per-token max |h|; down -> y
+//    in fp32.
 //  * precision: both GEMMs run on fp16 operands, weights fp16(q * s) and
 //    activations scaled per row by a power of two so that |v| < 2^14 (the
 //    factor is applied to the fp32 result); fp32 accumulation, round to
@@ -42,37 +53,59 @@ namespace {
 
 enum { kPGateUp = 0, kPDown = 1 };
 
-constexpr int kPThreads = 320;                 // 10 warps
+constexpr int kPThreads = 448;                 // 14 warps
 constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kDeqWarp0 = 6;
-constexpr int kTileM = 128, kTileN = 256;
+constexpr int kDeqThreads = 256;               // warps 6-13: one (A row, 32-element group) each
+constexpr int kTileM = 128;                    // rows of the MMA's A tile
+constexpr int kTileN = 192;                    // tokens per item
 constexpr int kRawK = 128, kOpK = 64;
 constexpr uint32_t kTmemCols = 512;
+// Tensor memory: two accumulator buffers of kTileN columns, then the A tiles of
+// the op stages (128 lanes x kOpK / 2 columns of packed fp16 each).
+constexpr int kAccStride = kTileN;
+constexpr int kACol0 = 2 * kTileN;
+constexpr int kACols = kOpK / 2;
 
+// Gate/up: the A tile stacks 64 rows of gate over the same 64 rows of up (one
+// MMA per k16 computes both), so an item covers 64 rows of h and the
+// accumulator needs only N columns.  Down: 128 rows of the down matrix.
 template <int MODE>
 struct PCfg {
-    static constexpr int kMats = MODE == kPGateUp ? 2 : 1;
-    static constexpr int kRawQ = kTileM * kRawK / 2;        // 8 KB of packed nibbles per matrix
-    static constexpr int kRawS = kTileM * (kRawK / 32) * 4; // 2 KB of scales per matrix
-    static constexpr int kRawStage = kMats * (kRawQ + kRawS);
-    static constexpr int kRawStages = MODE == kPGateUp ? 3 : 4;
-    static constexpr int kOpA = kTileM * kOpK * 2;          // 16 KB bf16 per matrix
-    static constexpr int kOpB = kTileN * kOpK * 2;          // 32 KB bf16 of token rows
-    static constexpr int kOpStage = kMats * kOpA + kOpB;
-    static constexpr int kOpStages = MODE == kPGateUp ? 2 : 3;
-    static constexpr int kSmem = 1024 + kRawStages * kRawStage + kOpStages * kOpStage;
+    static constexpr int kRawMats = MODE == kPGateUp ? 2 : 1;
+    static constexpr int kRowsPerMat = kTileM / kRawMats;      // weight rows of one matrix per item
+    static constexpr int kRawQ = kRowsPerMat * kRawK / 2;      // packed nibbles per matrix per raw stage
+    static constexpr int kRawS = kRowsPerMat * (kRawK / 32) * 4;
+    static constexpr int kRawStage = kRawMats * (kRawQ + kRawS);   // 10 KB either way
+    static constexpr int kRawStages = 4;
+    static constexpr int kOpB = kTileN * kOpK * 2;             // 24 KB fp16 of token rows (A is in TMEM)
+    static constexpr int kOpStage = kOpB;
+    static constexpr int kOpStages = 3;
+    static_assert(kACol0 + kOpStages * kACols <= (int)kTmemCols, "tensor memory budget");
+    static constexpr int kXchg = MODE == kPGateUp ? 2 * 2 * 32 * 16 * 4 : 0;   // up values for the gate warps (x2)
+    static constexpr int kRing = kRawStages * kRawStage + kOpStages * kOpStage + kXchg;
     static_assert(kRawStage % 1024 == 0 && kOpStage % 1024 == 0, "alignment");
 };
 
+// Unit table in shared memory: unit 0 = shared expert (T tokens), unit u >= 1
+// = uniq[u - 1]; cum = prefix of token tiles over the units.
+struct PUnit {
+    int expert, row0, m, cum;
+};
+
+__host__ __device__ constexpr size_t prefill_smem(int ring, int max_units)
+{
+    return 1024 + (size_t)ring + (size_t)(max_units + 1) * sizeof(PUnit);
+}
+
 struct PMaps {
-    CUtensorMap q[4];   // packed weights: routed mat0, routed mat1, shared mat0, shared mat1
-    CUtensorMap s[4];   // scales, same order
-    CUtensorMap b;      // bf16 token rows (X_sorted or H_sorted), [rows][K]
+    CUtensorMap q[2];   // packed weights: routed, shared; gate/up maps carry the matrix as a dimension
+    CUtensorMap s[2];   // scales, same order
+    CUtensorMap b;      // fp16 token rows (X_sorted or H_sorted), [rows][K]
 };
 
 struct PParams {
     const int32_t *offsets, *uniq, *n_uniq;
     const float *row_scale;       // power-of-two factor of each sorted activation row (x or h)
-    const int32_t *cum;           // [n_uniq + 2] prefix of token tiles per unit (unit 0 = shared)
     float *h32;                   // gate/up: h [rows][f] fp32, natural order
     unsigned int *hmax;           // gate/up: per-row max |h| (fp32 bits)
     float *y_pair, *y_shared;     // down outputs
@@ -86,37 +119,92 @@ struct PItem {
     int expert;   // -1 = shared
     int mtile;
     int tok0;     // first token of the tile within the unit
-    int ntok;     // tokens in this tile (1..256)
+    int ntok;     // tokens in this tile (1..N)
     int row0;     // first row of the unit in the sorted activation rows
     int m;
 };
 
-__device__ __forceinline__ PItem decode_pitem(const PParams &p, int i)
+// Build the unit table and the prefix of token tiles (N tokens per tile) for
+// units 0 .. units - 1; tab[units].cum = total tiles.  All threads of the block.
+template <int N>
+__device__ void build_units(const PParams &p, int units, PUnit *tab)
+{
+    constexpr int kPer = 4;   // units per thread (blockDim.x * 4 >= E + 1)
+    __shared__ int wsum[kPThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int tiles[kPer], tot = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; j++) {
+        const int u = tid * kPer + j;
+        tiles[j] = 0;
+        if (u < units) {
+            PUnit t;
+            if (u == 0) {
+                t.expert = -1;
+                t.row0 = p.T * p.k;
+                t.m = p.T;
+            } else {
+                const int e = p.uniq[u - 1];
+                t.expert = e;
+                t.row0 = p.offsets[e];
+                t.m = p.offsets[e + 1] - t.row0;
+            }
+            tiles[j] = (t.m + N - 1) / N;
+            tab[u] = t;
+        }
+        tot += tiles[j];
+    }
+    int inc = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off)
+            inc += v;
+    }
+    if (lane == 31)
+        wsum[warp] = inc;
+    __syncthreads();
+    int base = 0, all = 0;
+    for (int w = 0; w < kPThreads / 32; w++) {
+        base += w < warp ? wsum[w] : 0;
+        all += wsum[w];
+    }
+    int run = base + inc - tot;
+#pragma unroll
+    for (int j = 0; j < kPer; j++) {
+        const int u = tid * kPer + j;
+        if (u < units)
+            tab[u].cum = run;
+        run += tiles[j];
+    }
+    if (tid == 0)
+        tab[units].cum = all;
+    __syncthreads();
+}
+
+template <int N>
+__device__ __forceinline__ PItem decode_pitem(const PParams &p, const PUnit *tab, int units, int i)
 {
     PItem it;
     const int ntg = i / p.mtiles;
     it.mtile = i - ntg * p.mtiles;
     // unit u: largest u with cum[u] <= ntg
-    int lo = 0, hi = *p.n_uniq + 1;   // cum[hi] > ntg
+    int lo = 0, hi = units;   // tab[hi].cum > ntg
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (p.cum[mid] <= ntg)
+        if (tab[mid].cum <= ntg)
             lo = mid;
         else
             hi = mid;
     }
-    const int u = lo;
-    if (u == 0) {
-        it.expert = -1;
-        it.m = p.T;
-        it.row0 = p.T * p.k;
-    } else {
-        it.expert = p.uniq[u - 1];
-        it.row0 = p.offsets[it.expert];
-        it.m = p.offsets[it.expert + 1] - it.row0;
-    }
-    it.tok0 = (ntg - p.cum[u]) * kTileN;
-    it.ntok = min(kTileN, it.m - it.tok0);
+    const PUnit t = tab[lo];
+    it.expert = t.expert;
+    it.row0 = t.row0;
+    it.m = t.m;
+    // the unit's tokens in ceil(m / N) balanced tiles (each <= N)
+    const int nt = tab[lo + 1].cum - t.cum, j = ntg - t.cum;
+    it.tok0 = j * t.m / nt;
+    it.ntok = (j + 1) * t.m / nt - it.tok0;
     return it;
 }
 
@@ -163,30 +251,36 @@ __global__ void __launch_bounds__(kPThreads, 1)
 ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
 {
     using C = PCfg<MODE>;
+    constexpr int N = kTileN;
     constexpr bool kF16 = true;   // operand type of both GEMMs
     extern __shared__ uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t raw_full[C::kRawStages], raw_empty[C::kRawStages];
     __shared__ __align__(8) uint64_t op_full[C::kOpStages], op_empty[C::kOpStages];
-    __shared__ __align__(8) uint64_t acc_full, acc_empty;
+    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
 
     const uint32_t raw_base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
     const uint8_t *gen_base = dyn_smem + (raw_base - smem_addr(dyn_smem));
     const uint32_t op_base = raw_base + C::kRawStages * C::kRawStage;
+    float *xchg = reinterpret_cast<float *>(const_cast<uint8_t *>(gen_base) + C::kRawStages * C::kRawStage +
+                                            C::kOpStages * C::kOpStage);   // [2][2 warps][16][32]
+    PUnit *tab = reinterpret_cast<PUnit *>(const_cast<uint8_t *>(gen_base) + C::kRing);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kRawStages; s++) {
             mbar_init(smem_addr(&raw_full[s]), 1);
-            mbar_init(smem_addr(&raw_empty[s]), 128);
+            mbar_init(smem_addr(&raw_empty[s]), kDeqThreads);
         }
         for (int s = 0; s < C::kOpStages; s++) {
-            mbar_init(smem_addr(&op_full[s]), 128 + 1);
+            mbar_init(smem_addr(&op_full[s]), kDeqThreads + 1);
             mbar_init(smem_addr(&op_empty[s]), 1);
         }
-        mbar_init(smem_addr(&acc_full), 1);
-        mbar_init(smem_addr(&acc_empty), 128);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(smem_addr(&acc_full[b]), 1);
+            mbar_init(smem_addr(&acc_empty[b]), 128);
+        }
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -199,10 +293,11 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_sh;
     griddep_launch_dependents();
-    griddep_wait();   // union, plan and sorted activation rows come from earlier kernels
+    griddep_wait();   // union and sorted activation rows come from earlier kernels
 
-    const int n_units_tiles = p.cum[*p.n_uniq + 1];
-    const int n_items = n_units_tiles * p.mtiles;
+    const int units = *p.n_uniq + 1;
+    build_units<N>(p, units, tab);
+    const int n_items = tab[units].cum * p.mtiles;
     const int nraw = p.K / kRawK;
 
     if (warp == kProdWarp) {
@@ -211,10 +306,10 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
             int rs = 0, os = 0;
             uint32_t rph = 0, oph = 0;
             for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
-                const PItem it = decode_pitem(p, i);
+                const PItem it = decode_pitem<N>(p, tab, units, i);
                 const int z = it.expert < 0 ? 0 : it.expert;
-                const int mb = it.expert < 0 ? 2 : 0;
-                const int wrow0 = it.mtile * kTileM;
+                const int w = it.expert < 0 ? 1 : 0;
+                const int wrow0 = it.mtile * C::kRowsPerMat;
                 for (int r = 0; r < nraw; r++) {
                     if (!abort_flag && !mbar_wait(smem_addr(&raw_empty[rs]), rph ^ 1u)) {
                         atomicOr(p.err, MOE_DEVERR_TIMEOUT);
@@ -224,10 +319,12 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                         const uint32_t sb = raw_base + rs * C::kRawStage;
                         const uint32_t fb = smem_addr(&raw_full[rs]);
                         mbar_arrive_expect_tx(fb, C::kRawStage);
-                        for (int mat = 0; mat < C::kMats; mat++) {
-                            tma_load_3d(sb + mat * C::kRawQ, &maps.q[mb + mat], r * (kRawK / 2), wrow0, z, fb);
-                            tma_load_3d(sb + C::kMats * C::kRawQ + mat * C::kRawS, &maps.s[mb + mat],
-                                        r * (kRawK / 32), wrow0, z, fb);
+                        if (MODE == kPGateUp) {   // both matrices in one load each
+                            tma_load_4d(sb, &maps.q[w], r * (kRawK / 2), wrow0, 0, z, fb);
+                            tma_load_4d(sb + 2 * C::kRawQ, &maps.s[w], r * (kRawK / 32), wrow0, 0, z, fb);
+                        } else {
+                            tma_load_3d(sb, &maps.q[w], r * (kRawK / 2), wrow0, z, fb);
+                            tma_load_3d(sb + C::kRawQ, &maps.s[w], r * (kRawK / 32), wrow0, z, fb);
                         }
                     }
                     if (++rs == C::kRawStages) {
@@ -242,8 +339,8 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                         if (!abort_flag) {
                             const uint32_t fb = smem_addr(&op_full[os]);
                             mbar_arrive_expect_tx(fb, C::kOpB);
-                            tma_load_2d(op_base + os * C::kOpStage + C::kMats * C::kOpA, &maps.b,
-                                        (2 * r + h) * kOpK, it.row0 + it.tok0, fb);
+                            tma_load_2d(op_base + os * C::kOpStage, &maps.b, (2 * r + h) * kOpK, it.row0 + it.tok0,
+                                        fb);
                         }
                         if (++os == C::kOpStages) {
                             os = 0;
@@ -255,52 +352,50 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
         }
     } else if (warp >= kDeqWarp0) {
         // -------------------------------------------------- dequantisation
-        const int row = threadIdx.x - kDeqWarp0 * 32;   // 0..127
+        // a warp writes the 32 TMEM lanes of its subpartition: A rows 32 * (warp % 4) + lane
+        const int ar = ((warp & 3) << 5) | lane;        // row of the A tile
+        const int grp = (warp - kDeqWarp0) >> 2;        // which 32-element group of the op stage
+        const int mat = C::kRawMats == 2 ? (ar >> 6) : 0;
+        const int r = C::kRawMats == 2 ? (ar & 63) : ar;   // row within the matrix's raw tile
+        const uint32_t tlane = tmem_base + ((uint32_t)((warp & 3) << 5) << 16);
         int rs = 0, os = 0;
         uint32_t rph = 0, oph = 0;
         for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
-            for (int r = 0; r < nraw; r++) {
+            for (int rr = 0; rr < nraw; rr++) {
                 if (!abort_flag && !mbar_wait(smem_addr(&raw_full[rs]), rph)) {
                     atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                     abort_flag = 1;
                 }
                 const uint8_t *rsb = gen_base + rs * C::kRawStage;
+                // this row's 64 packed bytes, 64B-swizzled: 16-byte chunk c at (c ^ ((r >> 1) & 3))
+                const uint8_t *qrow = rsb + mat * C::kRawQ + r * 64;
+                const float4 sc = *reinterpret_cast<const float4 *>(rsb + C::kRawMats * C::kRawQ + mat * C::kRawS +
+                                                                   r * 16);
                 for (int h = 0; h < 2; h++) {
                     if (!abort_flag && !mbar_wait(smem_addr(&op_empty[os]), oph ^ 1u)) {
                         atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                         abort_flag = 1;
                     }
                     if (!abort_flag) {
-                        uint8_t *osb = const_cast<uint8_t *>(gen_base) + (op_base - raw_base) + os * C::kOpStage;
+                        tc_fence_after();
+                        const int c = 2 * h + grp;   // group of the raw stage
+                        const float sg = c == 0 ? sc.x : c == 1 ? sc.y : c == 2 ? sc.z : sc.w;
+                        const uint32_t sfac = pack_scale<kF16>(sg);
+                        const uint4 wv = *reinterpret_cast<const uint4 *>(qrow + ((c ^ ((r >> 1) & 3)) << 4));
+                        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+                        uint32_t out[16];
 #pragma unroll
-                        for (int mat = 0; mat < C::kMats; mat++) {
-                            // this row's 64 packed bytes, 64B-swizzled: 16-byte chunk c at (c ^ ((row >> 1) & 3))
-                            const uint8_t *qrow = rsb + mat * C::kRawQ + row * 64;
-                            const float4 sc = *reinterpret_cast<const float4 *>(rsb + C::kMats * C::kRawQ +
-                                                                               mat * C::kRawS + row * 16);
-                            const float s_lo = h ? sc.z : sc.x, s_hi = h ? sc.w : sc.y;
-                            const uint32_t sbl = pack_scale<kF16>(s_lo), sbh = pack_scale<kF16>(s_hi);
-                            uint8_t *arow = osb + mat * C::kOpA + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-                            for (int cc = 0; cc < 2; cc++) {   // two 16-byte chunks = 32 elements = one group
-                                const int c = 2 * h + cc;
-                                const uint4 wv = *reinterpret_cast<const uint4 *>(qrow + ((c ^ ((row >> 1) & 3)) << 4));
-                                const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-                                const uint32_t sfac = cc ? sbh : sbl;
-#pragma unroll
-                                for (int j = 0; j < 4; j++) {   // word j: elements 8j .. 8j+7 of the group
-                                    const uint32_t w = ws[j];
-                                    uint4 out;
-                                    out.x = mul_x2<kF16>(nib_q2<kF16>(w), sfac);          // (e0, e4)
-                                    out.y = mul_x2<kF16>(nib_q2<kF16>(w >> 4), sfac);     // (e1, e5)
-                                    out.z = mul_x2<kF16>(nib_q2<kF16>(w >> 8), sfac);     // (e2, e6)
-                                    out.w = mul_x2<kF16>(nib_q2<kF16>(w >> 12), sfac);    // (e3, e7)
-                                    const int chunk = cc * 4 + j;                   // 8-element chunk of the 64
-                                    *reinterpret_cast<uint4 *>(arow + ((chunk ^ (row & 7)) << 4)) = out;
-                                }
-                            }
+                        for (int j = 0; j < 4; j++) {   // word j: elements 8j .. 8j+7 of the group
+                            const uint32_t w = ws[j];
+                            out[4 * j + 0] = mul_x2<kF16>(nib_q2<kF16>(w), sfac);          // (e0, e4)
+                            out[4 * j + 1] = mul_x2<kF16>(nib_q2<kF16>(w >> 4), sfac);     // (e1, e5)
+                            out[4 * j + 2] = mul_x2<kF16>(nib_q2<kF16>(w >> 8), sfac);     // (e2, e6)
+                            out[4 * j + 3] = mul_x2<kF16>(nib_q2<kF16>(w >> 12), sfac);    // (e3, e7)
                         }
-                        fence_proxy_async_smem();
+                        // k pairs of this group = columns grp * 16 .. + 15 of the stage's A tile
+                        tmem_st16(tlane + kACol0 + os * kACols + grp * 16, out);
+                        tmem_wait_st();
+                        tc_fence_before();
                         mbar_arrive(smem_addr(&op_full[os]));
                     }
                     if (++os == C::kOpStages) {
@@ -319,18 +414,20 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------ MMA issue
         if (lane == 0) {
-            int os = 0;
-            uint32_t oph = 0, aph = 0;
-            for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
-                const PItem it = decode_pitem(p, i);
+            int os = 0, j = 0;
+            uint32_t oph = 0, eph[2] = {0u, 0u};
+            for (int i = blockIdx.x; i < n_items; i += gridDim.x, j++) {
+                const PItem it = decode_pitem<N>(p, tab, units, i);
+                const int b = j & 1;
                 const int n_mma = (it.ntok + 15) & ~15;
                 const uint32_t idesc = kF16 ? idesc_f16_f32(kTileM, n_mma) : idesc_bf16_f32(kTileM, n_mma);
-                if (!abort_flag && !mbar_wait(smem_addr(&acc_empty), aph ^ 1u)) {
+                if (!abort_flag && !mbar_wait(smem_addr(&acc_empty[b]), eph[b] ^ 1u)) {
                     atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                     abort_flag = 1;
                 }
-                aph ^= 1u;
+                eph[b] ^= 1u;
                 tc_fence_after();
+                const uint32_t dcol = tmem_base + b * kAccStride;
                 for (int kb = 0; kb < 2 * nraw; kb++) {
                     if (!abort_flag && !mbar_wait(smem_addr(&op_full[os]), oph)) {
                         atomicOr(p.err, MOE_DEVERR_TIMEOUT);
@@ -338,16 +435,11 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                     }
                     tc_fence_after();
                     if (!abort_flag) {
-                        const uint32_t sb = op_base + os * C::kOpStage;
+                        const uint64_t bd = smem_desc_sw128(op_base + os * C::kOpStage);
+                        const uint32_t acol = tmem_base + kACol0 + os * kACols;
 #pragma unroll
-                        for (int k16 = 0; k16 < kOpK / 16; k16++) {
-                            const uint64_t bd = smem_desc_sw128(sb + C::kMats * C::kOpA + k16 * 32);
-                            const uint32_t acc = (kb > 0 || k16 > 0) ? 1u : 0u;
-#pragma unroll
-                            for (int mat = 0; mat < C::kMats; mat++)
-                                umma_f16(tmem_base + mat * kTileN, smem_desc_sw128(sb + mat * C::kOpA + k16 * 32), bd,
-                                         idesc, acc);
-                        }
+                        for (int k16 = 0; k16 < kOpK / 16; k16++)   // B: +32 bytes = +2 in the descriptor
+                            umma_f16_ts(dcol, acol + 8 * k16, bd + 2 * k16, idesc, (kb > 0 || k16 > 0) ? 1u : 0u);
                         umma_commit(smem_addr(&op_empty[os]));
                     }
                     if (++os == C::kOpStages) {
@@ -356,60 +448,81 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                     }
                 }
                 if (!abort_flag)
-                    umma_commit(smem_addr(&acc_full));
+                    umma_commit(smem_addr(&acc_full[b]));
             }
         }
     } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------------- epilogue
-        const int sub = warp & 3;                 // TMEM lanes 32*sub .. 32*sub+31
-        const int row = sub * 32 + lane;          // output row within the tile
-        uint32_t aph = 0;
-        for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
-            const PItem it = decode_pitem(p, i);
-            if (!abort_flag && !mbar_wait(smem_addr(&acc_full), aph)) {
+        const int sub = warp & 3;                 // TMEM lanes 32*sub .. 32*sub+31 = A rows
+        uint32_t fph[2] = {0u, 0u};
+        int j = 0;
+        int xpar = 0;   // exchange buffer of the next 16-column chunk (alternates across items too)
+        for (int i = blockIdx.x; i < n_items; i += gridDim.x, j++) {
+            const PItem it = decode_pitem<N>(p, tab, units, i);
+            const int b = j & 1;
+            if (!abort_flag && !mbar_wait(smem_addr(&acc_full[b]), fph[b])) {
                 atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                 abort_flag = 1;
             }
-            aph ^= 1u;
+            fph[b] ^= 1u;
             tc_fence_after();
-            if (!abort_flag) {
-                const int orow = it.mtile * kTileM + row;
-                const uint32_t tl = tmem_base + ((uint32_t)(sub * 32) << 16);
+            // (no early exit on abort: the four warps meet at a named barrier per chunk, so they
+            // all run the same chunks; after an abort the values are discarded garbage)
+            {
+                const uint32_t tl = tmem_base + ((uint32_t)(sub * 32) << 16) + b * kAccStride;
                 for (int c0 = 0; c0 < it.ntok; c0 += 16) {
-                    uint32_t g[16], u[16];
-                    tmem_ld16(tl + c0, g);
-                    if (MODE == kPGateUp)
-                        tmem_ld16(tl + kTileN + c0, u);
-                    tmem_wait_ld();
+                    const int ch = xpar;
+                    xpar ^= 1;
+                    uint32_t v[16];
+                    tmem_ld16(tl + c0, v);
+                    // the row factors of these 16 tokens, one per lane, broadcast below
                     const int nj = min(16, it.ntok - c0);
+                    const float rfl = lane < nj ? p.row_scale[it.row0 + it.tok0 + c0 + lane] : 0.f;
+                    tmem_wait_ld();
+                    if (MODE == kPGateUp) {
+                        // up rows (subpartitions 2, 3) hand their values to the gate rows (0, 1)
+                        float *xb = xchg + ch * (2 * 16 * 32);
+                        if (sub >= 2) {
 #pragma unroll
-                    for (int j = 0; j < 16; j++) {
-                        if (j >= nj)
-                            break;
-                        const int tok = it.tok0 + c0 + j;
-                        const float rf = p.row_scale[it.row0 + tok];
-                        const float gv = __uint_as_float(g[j]) * rf;
-                        if (MODE == kPGateUp) {
-                            const float uv = __uint_as_float(u[j]) * rf;
-                            const float hv = gv / (1.0f + expf(-gv)) * uv;
-                            p.h32[(size_t)(it.row0 + tok) * p.out_rows + orow] = hv;
-                            float mx = fabsf(hv);
+                            for (int jj = 0; jj < 16; jj++)
+                                xb[((sub - 2) * 16 + jj) * 32 + lane] = __uint_as_float(v[jj]);
+                        }
+                        named_bar_sync(2, 128);
+                        if (sub < 2) {
+                            const int hr = it.mtile * 64 + sub * 32 + lane;   // row of h
 #pragma unroll
-                            for (int off = 16; off > 0; off >>= 1)
-                                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                            if (lane == 0)
-                                atomicMax(p.hmax + it.row0 + tok, __float_as_uint(mx));
-                        } else {
+                            for (int jj = 0; jj < 16; jj++) {
+                                const float rf = __shfl_sync(0xffffffffu, rfl, jj);
+                                if (jj >= nj)
+                                    break;
+                                const int tok = it.tok0 + c0 + jj;
+                                const float gv = __uint_as_float(v[jj]) * rf;
+                                const float uv = xb[(sub * 16 + jj) * 32 + lane] * rf;
+                                const float hv = gv / (1.0f + expf(-gv)) * uv;
+                                p.h32[(size_t)(it.row0 + tok) * p.out_rows + hr] = hv;
+                                const unsigned mx = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
+                                if (lane == 0)
+                                    atomicMax(p.hmax + it.row0 + tok, mx);
+                            }
+                        }
+                    } else {
+                        const int orow = it.mtile * kTileM + sub * 32 + lane;
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj++) {
+                            const float rf = __shfl_sync(0xffffffffu, rfl, jj);
+                            if (jj >= nj)
+                                break;
+                            const int tok = it.tok0 + c0 + jj;
                             float *dst = it.expert < 0 ? p.y_shared + (size_t)tok * p.out_rows
                                                        : p.y_pair + (size_t)(it.row0 + tok) * p.out_rows;
-                            dst[orow] = gv;
+                            dst[orow] = __uint_as_float(v[jj]) * rf;
                         }
                     }
                 }
             }
             tc_fence_before();
             if (!abort_flag)
-                mbar_arrive(smem_addr(&acc_empty));
+                mbar_arrive(smem_addr(&acc_empty[b]));
         }
     }
 
@@ -501,41 +614,8 @@ h_to_f16_kernel(const float *__restrict__ h32, const unsigned int *__restrict__ 
     }
 }
 
-// Prefix of 256-token tiles per unit (unit 0 = shared expert with T tokens,
-// unit u >= 1 = uniq[u-1]); cum has n_uniq + 2 entries.
-__global__ void prefill_plan_kernel(const int32_t *__restrict__ offsets, const int32_t *__restrict__ uniq,
-                                    const int32_t *__restrict__ n_uniq, int T, int32_t *__restrict__ cum)
-{
-    griddep_wait();
-    if (threadIdx.x >= 32)
-        return;
-    const int lane = threadIdx.x;
-    const int nu = *n_uniq + 1;
-    int carry = 0;
-    for (int u0 = 0; u0 < nu; u0 += 32) {
-        const int u = u0 + lane;
-        int nt = 0;
-        if (u < nu) {
-            const int m = u == 0 ? T : offsets[uniq[u - 1] + 1] - offsets[uniq[u - 1]];
-            nt = (m + kTileN - 1) / kTileN;
-        }
-        int inc = nt;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, inc, off);
-            if (lane >= off)
-                inc += v;
-        }
-        if (u < nu)
-            cum[u] = carry + inc - nt;
-        carry += __shfl_sync(0xffffffffu, inc, 31);
-    }
-    if (lane == 0)
-        cum[nu] = carry;
-}
-
 template <int MODE>
-int launch_prefill_one(const PMaps &maps, const PParams &prm, cudaStream_t s)
+int launch_prefill_one(const PMaps &maps, const PParams &prm, int max_units, cudaStream_t s)
 {
     using C = PCfg<MODE>;
     auto kern = ffn_prefill_kernel<MODE>;
@@ -544,11 +624,12 @@ int launch_prefill_one(const PMaps &maps, const PParams &prm, cudaStream_t s)
         return MOE_ERR_CUDA;
     static int configured[64] = {0};
     if (!configured[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)prefill_smem(C::kRing, 1025)) != cudaSuccess)
             return MOE_ERR_CUDA;
         configured[dev] = 1;
     }
-    return launch_pdl(kern, sm_count(dev), kPThreads, (size_t)C::kSmem, s, maps, prm);
+    return launch_pdl(kern, sm_count(dev), kPThreads, prefill_smem(C::kRing, max_units), s, maps, prm);
 }
 
 }  // namespace
@@ -559,7 +640,6 @@ struct PrefillScratch {
     uint16_t *x16, *h16;
     float *x_scale, *h_scale, *h32;
     unsigned int *hmax;
-    int32_t *cum;
 };
 
 size_t prefill_layout(int T, int k, int d, int f, uint8_t *base, PrefillScratch *o)
@@ -578,7 +658,6 @@ size_t prefill_layout(int T, int k, int d, int f, uint8_t *base, PrefillScratch 
     s.x_scale = reinterpret_cast<float *>(take(rows * 4));
     s.h_scale = reinterpret_cast<float *>(take(rows * 4));
     s.hmax = reinterpret_cast<unsigned int *>(take(rows * 4));
-    s.cum = reinterpret_cast<int32_t *>(take(((size_t)T * k + 2) * 4));
     if (o)
         *o = s;
     return off;
@@ -599,14 +678,10 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     prefill_layout(T, k, d, f, static_cast<uint8_t *>(a.scratch), &ps);
     uint16_t *x_sorted = ps.x16;
     uint16_t *h_sorted = ps.h16;
-    int32_t *cum = ps.cum;
     float *row_scale = ps.x_scale;
     int rc = MOE_OK;
 
-    // plan + gathered bf16 token rows
-    rc = launch_pdl(prefill_plan_kernel, 1, 32, 0, s, a.offsets, a.uniq, a.n_uniq, T, cum);
-    if (rc != MOE_OK)
-        return rc;
+    // gathered fp16 token rows
     rc = launch_pdl(gather_rows_kernel, (int)rows, 256, 0, s, a.x, a.sorted_pair, T, k, d, x_sorted, row_scale,
                     ps.hmax);
     if (rc != MOE_OK)
@@ -616,16 +691,20 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     const float *ss[2] = {w.s_base, w.shared_s};
     const uint64_t outer[2] = {(uint64_t)E, 1};
 
-    // ---- gate / up
+    // ---- gate / up: (row bytes, row, matrix, expert) maps, both matrices per load
     PMaps gm{};
-    for (int i = 0; i < 2 && rc == MOE_OK; i++)
-        for (int mat = 0; mat < 2; mat++) {
-            rc |= make_tmap_3d(&gm.q[2 * i + mat], qs[i] + (size_t)mat * f * d / 2, CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                               1, d / 2, f, outer[i], d / 2, qb, kRawK / 2, kTileM, CU_TENSOR_MAP_SWIZZLE_64B);
-            rc |= make_tmap_3d(&gm.s[2 * i + mat], ss[i] + (size_t)mat * f * d / G,
-                               CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d / G, f, outer[i], (uint64_t)(d / G) * 4,
-                               sc * 4, kRawK / 32, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE);
-        }
+    for (int i = 0; i < 2 && rc == MOE_OK; i++) {
+        const uint64_t q_dim[4] = {(uint64_t)d / 2, (uint64_t)f, 2, outer[i]};
+        const uint64_t q_str[3] = {(uint64_t)d / 2, (uint64_t)f * d / 2, qb};
+        const uint32_t q_box[4] = {kRawK / 2, (uint32_t)PCfg<kPGateUp>::kRowsPerMat, 2, 1};
+        const uint64_t s_dim[4] = {(uint64_t)d / G, (uint64_t)f, 2, outer[i]};
+        const uint64_t s_str[3] = {(uint64_t)(d / G) * 4, (uint64_t)f * (d / G) * 4, sc * 4};
+        const uint32_t s_box[4] = {kRawK / 32, (uint32_t)PCfg<kPGateUp>::kRowsPerMat, 2, 1};
+        rc |= make_tmap_nd(&gm.q[i], qs[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, q_dim, q_str, q_box,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
+        rc |= make_tmap_nd(&gm.s[i], ss[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s_dim, s_str, s_box,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
     rc |= make_tmap_2d(&gm.b, x_sorted, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, d, rows, (uint64_t)d * 2, kOpK, kTileN,
                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != MOE_OK)
@@ -634,7 +713,6 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pg.offsets = a.offsets;
     pg.uniq = a.uniq;
     pg.n_uniq = a.n_uniq;
-    pg.cum = cum;
     pg.row_scale = row_scale;
     pg.h32 = ps.h32;
     pg.hmax = ps.hmax;
@@ -642,9 +720,10 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pg.T = T;
     pg.k = k;
     pg.K = d;
-    pg.mtiles = f / kTileM;
+    pg.mtiles = f / PCfg<kPGateUp>::kRowsPerMat;
     pg.out_rows = f;
-    rc = launch_prefill_one<kPGateUp>(gm, pg, s);
+    const int max_units = (E < T * k ? E : T * k) + 1;
+    rc = launch_prefill_one<kPGateUp>(gm, pg, max_units, s);
     if (rc == MOE_OK)
         rc = launch_pdl(h_to_f16_kernel, (int)rows, 256, 0, s, (const float *)ps.h32,
                         (const unsigned int *)ps.hmax, f, h_sorted, ps.h_scale);
@@ -654,13 +733,10 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     // ---- down
     PMaps dm{};
     for (int i = 0; i < 2 && rc == MOE_OK; i++) {
-        rc |= make_tmap_3d(&dm.q[2 * i], qs[i] + (size_t)f * d, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, f / 2, d,
-                           outer[i], f / 2, qb, kRawK / 2, kTileM, CU_TENSOR_MAP_SWIZZLE_64B);
-        rc |= make_tmap_3d(&dm.s[2 * i], ss[i] + (size_t)2 * f * d / G, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
-                           f / G, d, outer[i], (uint64_t)(f / G) * 4, sc * 4, kRawK / 32, kTileM,
-                           CU_TENSOR_MAP_SWIZZLE_NONE);
-        dm.q[2 * i + 1] = dm.q[2 * i];
-        dm.s[2 * i + 1] = dm.s[2 * i];
+        rc |= make_tmap_3d(&dm.q[i], qs[i] + (size_t)f * d, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, f / 2, d, outer[i],
+                           f / 2, qb, kRawK / 2, kTileM, CU_TENSOR_MAP_SWIZZLE_64B);
+        rc |= make_tmap_3d(&dm.s[i], ss[i] + (size_t)2 * f * d / G, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, f / G, d,
+                           outer[i], (uint64_t)(f / G) * 4, sc * 4, kRawK / 32, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     rc |= make_tmap_2d(&dm.b, h_sorted, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, f, rows, (uint64_t)f * 2, kOpK, kTileN,
                        CU_TENSOR_MAP_SWIZZLE_128B);
@@ -675,7 +751,7 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pd.K = f;
     pd.mtiles = d / kTileM;
     pd.out_rows = d;
-    return launch_prefill_one<kPDown>(dm, pd, s);
+    return launch_prefill_one<kPDown>(dm, pd, max_units, s);
 }
 
 }  // namespace moe
