@@ -15,10 +15,12 @@
 //    h; one MMA per k16 serves both matrices); down takes 128 rows.  Every CTA builds the unit table
 //    (expert, first sorted row, tokens, prefix of token tiles) in shared
 //    memory once, so items are decoded without global loads.
-//  * warp 0 (producer): TMA loads of the packed int4 rows + fp32 scales
-//    (raw ring, k-blocks of 128) and of the bf16 token rows (operand ring,
+//  * warp 0 (weight producer): TMA loads of the packed int4 rows + fp32 scales
+//    (raw ring, k-blocks of 128), running ahead of everything else; warp 14
+//    (token producer): TMA loads of the fp16 token rows (operand ring,
 //    k-blocks of 64, 128-byte swizzle).
-//  * warps 6-13 (dequant, thread = row of the A tile and 32-element group):
+//  * warps 6-13 (dequant: two groups of four warps taking alternate op
+//    stages, thread = row of the A tile):
 //    nibbles -> fp16 (q * s) with an exact magic-exponent conversion
 //    (0x6400|(n^8) = 1032 + q, then subtract) and one multiply, written straight
 //    into tensor memory: the MMA reads A from there, so shared memory carries
@@ -53,9 +55,9 @@ namespace {
 
 enum { kPGateUp = 0, kPDown = 1 };
 
-constexpr int kPThreads = 448;                 // 14 warps
-constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kDeqWarp0 = 6;
-constexpr int kDeqThreads = 256;               // warps 6-13: one (A row, 32-element group) each
+constexpr int kPThreads = 480;                 // 15 warps
+constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kDeqWarp0 = 6, kBProdWarp = 14;
+constexpr int kDeqThreads = 256;               // warps 6-13: two groups of 128 (A row each), alternate op stages
 constexpr int kTileM = 128;                    // rows of the MMA's A tile
 constexpr int kTileN = 192;                    // tokens per item
 constexpr int kRawK = 128, kOpK = 64;
@@ -76,10 +78,10 @@ struct PCfg {
     static constexpr int kRawQ = kRowsPerMat * kRawK / 2;      // packed nibbles per matrix per raw stage
     static constexpr int kRawS = kRowsPerMat * (kRawK / 32) * 4;
     static constexpr int kRawStage = kRawMats * (kRawQ + kRawS);   // 10 KB either way
-    static constexpr int kRawStages = 4;
+    static constexpr int kRawStages = 6;
     static constexpr int kOpB = kTileN * kOpK * 2;             // 24 KB fp16 of token rows (A is in TMEM)
     static constexpr int kOpStage = kOpB;
-    static constexpr int kOpStages = 3;
+    static constexpr int kOpStages = 4;
     static_assert(kACol0 + kOpStages * kACols <= (int)kTmemCols, "tensor memory budget");
     static constexpr int kXchg = MODE == kPGateUp ? 2 * 2 * 32 * 16 * 4 : 0;   // up values for the gate warps (x2)
     static constexpr int kRing = kRawStages * kRawStage + kOpStages * kOpStage + kXchg;
@@ -274,7 +276,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
             mbar_init(smem_addr(&raw_empty[s]), kDeqThreads);
         }
         for (int s = 0; s < C::kOpStages; s++) {
-            mbar_init(smem_addr(&op_full[s]), kDeqThreads + 1);
+            mbar_init(smem_addr(&op_full[s]), kDeqThreads / 2 + 1);   // one dequant group + the token load
             mbar_init(smem_addr(&op_empty[s]), 1);
         }
         for (int b = 0; b < 2; b++) {
@@ -301,10 +303,10 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
     const int nraw = p.K / kRawK;
 
     if (warp == kProdWarp) {
-        // -------------------------------------------------------- producer
+        // ------------------------------------------------- weight producer
         if (lane == 0) {
-            int rs = 0, os = 0;
-            uint32_t rph = 0, oph = 0;
+            int rs = 0;
+            uint32_t rph = 0;
             for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
                 const PItem it = decode_pitem<N>(p, tab, units, i);
                 const int z = it.expert < 0 ? 0 : it.expert;
@@ -331,35 +333,46 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                         rs = 0;
                         rph ^= 1u;
                     }
-                    for (int h = 0; h < 2; h++) {
-                        if (!abort_flag && !mbar_wait(smem_addr(&op_empty[os]), oph ^ 1u)) {
-                            atomicOr(p.err, MOE_DEVERR_TIMEOUT);
-                            abort_flag = 1;
-                        }
-                        if (!abort_flag) {
-                            const uint32_t fb = smem_addr(&op_full[os]);
-                            mbar_arrive_expect_tx(fb, C::kOpB);
-                            tma_load_2d(op_base + os * C::kOpStage, &maps.b, (2 * r + h) * kOpK, it.row0 + it.tok0,
-                                        fb);
-                        }
-                        if (++os == C::kOpStages) {
-                            os = 0;
-                            oph ^= 1u;
-                        }
+                }
+            }
+        }
+    } else if (warp == kBProdWarp) {
+        // -------------------------------------------------- token producer
+        if (lane == 0) {
+            int os = 0;
+            uint32_t oph = 0;
+            for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+                const PItem it = decode_pitem<N>(p, tab, units, i);
+                for (int kb = 0; kb < 2 * nraw; kb++) {
+                    if (!abort_flag && !mbar_wait(smem_addr(&op_empty[os]), oph ^ 1u)) {
+                        atomicOr(p.err, MOE_DEVERR_TIMEOUT);
+                        abort_flag = 1;
+                    }
+                    if (!abort_flag) {
+                        const uint32_t fb = smem_addr(&op_full[os]);
+                        mbar_arrive_expect_tx(fb, C::kOpB);
+                        tma_load_2d(op_base + os * C::kOpStage, &maps.b, kb * kOpK, it.row0 + it.tok0, fb);
+                    }
+                    if (++os == C::kOpStages) {
+                        os = 0;
+                        oph ^= 1u;
                     }
                 }
             }
         }
     } else if (warp >= kDeqWarp0) {
         // -------------------------------------------------- dequantisation
-        // a warp writes the 32 TMEM lanes of its subpartition: A rows 32 * (warp % 4) + lane
+        // two groups of four warps take alternate op stages (group g: the second half-stage g of
+        // every raw stage), so each has two stage periods for its work; a warp writes the 32 TMEM
+        // lanes of its subpartition: A rows 32 * (warp % 4) + lane
         const int ar = ((warp & 3) << 5) | lane;        // row of the A tile
-        const int grp = (warp - kDeqWarp0) >> 2;        // which 32-element group of the op stage
+        const int g = (warp - kDeqWarp0) >> 2;          // 0 or 1
         const int mat = C::kRawMats == 2 ? (ar >> 6) : 0;
         const int r = C::kRawMats == 2 ? (ar & 63) : ar;   // row within the matrix's raw tile
         const uint32_t tlane = tmem_base + ((uint32_t)((warp & 3) << 5) << 16);
-        int rs = 0, os = 0;
-        uint32_t rph = 0, oph = 0;
+        int rs = 0;
+        uint32_t rph = 0;
+        uint32_t kop = g;   // global index of this group's next op stage
         for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
             for (int rr = 0; rr < nraw; rr++) {
                 if (!abort_flag && !mbar_wait(smem_addr(&raw_full[rs]), rph)) {
@@ -367,21 +380,33 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                     abort_flag = 1;
                 }
                 const uint8_t *rsb = gen_base + rs * C::kRawStage;
-                // this row's 64 packed bytes, 64B-swizzled: 16-byte chunk c at (c ^ ((r >> 1) & 3))
+                // this row's 64 packed bytes, 64B-swizzled: 16-byte chunk c at (c ^ ((r >> 1) & 3));
+                // the op stage takes chunks 2g and 2g + 1 (64 elements)
                 const uint8_t *qrow = rsb + mat * C::kRawQ + r * 64;
                 const float4 sc = *reinterpret_cast<const float4 *>(rsb + C::kRawMats * C::kRawQ + mat * C::kRawS +
                                                                    r * 16);
-                for (int h = 0; h < 2; h++) {
-                    if (!abort_flag && !mbar_wait(smem_addr(&op_empty[os]), oph ^ 1u)) {
-                        atomicOr(p.err, MOE_DEVERR_TIMEOUT);
-                        abort_flag = 1;
-                    }
-                    if (!abort_flag) {
-                        tc_fence_after();
-                        const int c = 2 * h + grp;   // group of the raw stage
-                        const float sg = c == 0 ? sc.x : c == 1 ? sc.y : c == 2 ? sc.z : sc.w;
+                const uint4 wv0 = *reinterpret_cast<const uint4 *>(qrow + (((2 * g) ^ ((r >> 1) & 3)) << 4));
+                const uint4 wv1 = *reinterpret_cast<const uint4 *>(qrow + (((2 * g + 1) ^ ((r >> 1) & 3)) << 4));
+                if (!abort_flag)
+                    mbar_arrive(smem_addr(&raw_empty[rs]));   // the raw stage is in registers now
+                if (++rs == C::kRawStages) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
+                const int os = (int)(kop % C::kOpStages);
+                const uint32_t oph = (kop / C::kOpStages) & 1u;
+                kop += 2;
+                if (!abort_flag && !mbar_wait(smem_addr(&op_empty[os]), oph ^ 1u)) {
+                    atomicOr(p.err, MOE_DEVERR_TIMEOUT);
+                    abort_flag = 1;
+                }
+                if (!abort_flag) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int q = 0; q < 2; q++) {
+                        const uint4 wv = q ? wv1 : wv0;
+                        const float sg = g ? (q ? sc.w : sc.z) : (q ? sc.y : sc.x);
                         const uint32_t sfac = pack_scale<kF16>(sg);
-                        const uint4 wv = *reinterpret_cast<const uint4 *>(qrow + ((c ^ ((r >> 1) & 3)) << 4));
                         const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
                         uint32_t out[16];
 #pragma unroll
@@ -392,22 +417,12 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                             out[4 * j + 2] = mul_x2<kF16>(nib_q2<kF16>(w >> 8), sfac);     // (e2, e6)
                             out[4 * j + 3] = mul_x2<kF16>(nib_q2<kF16>(w >> 12), sfac);    // (e3, e7)
                         }
-                        // k pairs of this group = columns grp * 16 .. + 15 of the stage's A tile
-                        tmem_st16(tlane + kACol0 + os * kACols + grp * 16, out);
-                        tmem_wait_st();
-                        tc_fence_before();
-                        mbar_arrive(smem_addr(&op_full[os]));
+                        // k pairs of this group = columns q * 16 .. + 15 of the stage's A tile
+                        tmem_st16(tlane + kACol0 + os * kACols + q * 16, out);
                     }
-                    if (++os == C::kOpStages) {
-                        os = 0;
-                        oph ^= 1u;
-                    }
-                }
-                if (!abort_flag)
-                    mbar_arrive(smem_addr(&raw_empty[rs]));
-                if (++rs == C::kRawStages) {
-                    rs = 0;
-                    rph ^= 1u;
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(smem_addr(&op_full[os]));
                 }
             }
         }
