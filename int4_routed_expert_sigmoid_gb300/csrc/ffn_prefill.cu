@@ -60,7 +60,7 @@ constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kDeqWarp0 = 6, kBProdW
 constexpr int kDeqThreads = 256;               // warps 6-13: two groups of 128 (A row each), alternate op stages
 constexpr int kTileM = 128;                    // rows of the MMA's A tile
 constexpr int kTileN = 192;                    // tokens per item
-constexpr int kRawK = 128, kOpK = 64;
+constexpr int kOpK = 64;
 constexpr uint32_t kTmemCols = 512;
 // Tensor memory: two accumulator buffers of kTileN columns, then the A tiles of
 // the op stages (128 lanes x kOpK / 2 columns of packed fp16 each).
@@ -71,14 +71,20 @@ constexpr int kACols = kOpK / 2;
 // Gate/up: the A tile stacks 64 rows of gate over the same 64 rows of up (one
 // MMA per k16 computes both), so an item covers 64 rows of h and the
 // accumulator needs only N columns.  Down: 128 rows of the down matrix.
-template <int MODE>
+// RAWK: elements of a row per raw stage -- 256 (128-byte row segments, 128B
+// swizzle) when the reduction length allows it, else 128 (64 bytes, 64B swizzle).
+template <int MODE, int RAWK>
 struct PCfg {
+    static constexpr int kRawK = RAWK;
+    static constexpr int kRowB = RAWK / 2;                     // packed bytes of a row per raw stage
+    static constexpr int kChunks = RAWK / 32;                  // 16-byte chunks (= groups) per row
+    static constexpr int kOpPerRaw = RAWK / kOpK;
     static constexpr int kRawMats = MODE == kPGateUp ? 2 : 1;
     static constexpr int kRowsPerMat = kTileM / kRawMats;      // weight rows of one matrix per item
     static constexpr int kRawQ = kRowsPerMat * kRawK / 2;      // packed nibbles per matrix per raw stage
     static constexpr int kRawS = kRowsPerMat * (kRawK / 32) * 4;
     static constexpr int kRawStage = kRawMats * (kRawQ + kRawS);   // 10 KB either way
-    static constexpr int kRawStages = 6;
+    static constexpr int kRawStages = RAWK == 256 ? 4 : 6;
     static constexpr int kOpB = kTileN * kOpK * 2;             // 24 KB fp16 of token rows (A is in TMEM)
     static constexpr int kOpStage = kOpB;
     static constexpr int kOpStages = 4;
@@ -248,11 +254,11 @@ __device__ __forceinline__ uint32_t pack_scale(float s)
     return *reinterpret_cast<const uint32_t *>(&b);
 }
 
-template <int MODE>
+template <int MODE, int RAWK>
 __global__ void __launch_bounds__(kPThreads, 1)
 ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
 {
-    using C = PCfg<MODE>;
+    using C = PCfg<MODE, RAWK>;
     constexpr int N = kTileN;
     constexpr bool kF16 = true;   // operand type of both GEMMs
     extern __shared__ uint8_t dyn_smem[];
@@ -300,7 +306,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
     const int units = *p.n_uniq + 1;
     build_units<N>(p, units, tab);
     const int n_items = tab[units].cum * p.mtiles;
-    const int nraw = p.K / kRawK;
+    const int nraw = p.K / RAWK;
 
     if (warp == kProdWarp) {
         // ------------------------------------------------- weight producer
@@ -322,11 +328,11 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                         const uint32_t fb = smem_addr(&raw_full[rs]);
                         mbar_arrive_expect_tx(fb, C::kRawStage);
                         if (MODE == kPGateUp) {   // both matrices in one load each
-                            tma_load_4d(sb, &maps.q[w], r * (kRawK / 2), wrow0, 0, z, fb);
-                            tma_load_4d(sb + 2 * C::kRawQ, &maps.s[w], r * (kRawK / 32), wrow0, 0, z, fb);
+                            tma_load_4d(sb, &maps.q[w], r * C::kRowB, wrow0, 0, z, fb);
+                            tma_load_4d(sb + 2 * C::kRawQ, &maps.s[w], r * C::kChunks, wrow0, 0, z, fb);
                         } else {
-                            tma_load_3d(sb, &maps.q[w], r * (kRawK / 2), wrow0, z, fb);
-                            tma_load_3d(sb + C::kRawQ, &maps.s[w], r * (kRawK / 32), wrow0, z, fb);
+                            tma_load_3d(sb, &maps.q[w], r * C::kRowB, wrow0, z, fb);
+                            tma_load_3d(sb + C::kRawQ, &maps.s[w], r * C::kChunks, wrow0, z, fb);
                         }
                     }
                     if (++rs == C::kRawStages) {
@@ -343,7 +349,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
             uint32_t oph = 0;
             for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
                 const PItem it = decode_pitem<N>(p, tab, units, i);
-                for (int kb = 0; kb < 2 * nraw; kb++) {
+                for (int kb = 0; kb < C::kOpPerRaw * nraw; kb++) {
                     if (!abort_flag && !mbar_wait(smem_addr(&op_empty[os]), oph ^ 1u)) {
                         atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                         abort_flag = 1;
@@ -362,7 +368,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
         }
     } else if (warp >= kDeqWarp0) {
         // -------------------------------------------------- dequantisation
-        // two groups of four warps take alternate op stages (group g: the second half-stage g of
+        // two groups of four warps take alternate op stages (group g: op stages g and g + 2 of
         // every raw stage), so each has two stage periods for its work; a warp writes the 32 TMEM
         // lanes of its subpartition: A rows 32 * (warp % 4) + lane
         const int ar = ((warp & 3) << 5) | lane;        // row of the A tile
@@ -380,49 +386,60 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                     abort_flag = 1;
                 }
                 const uint8_t *rsb = gen_base + rs * C::kRawStage;
-                // this row's 64 packed bytes, 64B-swizzled: 16-byte chunk c at (c ^ ((r >> 1) & 3));
-                // the op stage takes chunks 2g and 2g + 1 (64 elements)
-                const uint8_t *qrow = rsb + mat * C::kRawQ + r * 64;
-                const float4 sc = *reinterpret_cast<const float4 *>(rsb + C::kRawMats * C::kRawQ + mat * C::kRawS +
-                                                                   r * 16);
-                const uint4 wv0 = *reinterpret_cast<const uint4 *>(qrow + (((2 * g) ^ ((r >> 1) & 3)) << 4));
-                const uint4 wv1 = *reinterpret_cast<const uint4 *>(qrow + (((2 * g + 1) ^ ((r >> 1) & 3)) << 4));
+                // this row's packed bytes, swizzled (128B: 16-byte chunk c at c ^ (r & 7); 64B: at
+                // c ^ ((r >> 1) & 3)); chunk c = group c; the group's op stages h = g (+ 2) take chunks
+                // 2h, 2h + 1
+                constexpr int kQ = 2 * (C::kOpPerRaw / 2);   // chunks this thread uses per raw stage
+                const uint8_t *qrow = rsb + mat * C::kRawQ + r * C::kRowB;
+                const float *srow = reinterpret_cast<const float *>(rsb + C::kRawMats * C::kRawQ + mat * C::kRawS +
+                                                                    r * C::kChunks * 4);
+                const int sw = RAWK == 256 ? (r & 7) : ((r >> 1) & 3);
+                uint4 wv[kQ];
+                float sg[kQ];
+#pragma unroll
+                for (int q = 0; q < kQ; q++) {
+                    const int c = 2 * g + (q & 1) + 4 * (q >> 1);
+                    wv[q] = *reinterpret_cast<const uint4 *>(qrow + ((c ^ sw) << 4));
+                    sg[q] = srow[c];
+                }
                 if (!abort_flag)
                     mbar_arrive(smem_addr(&raw_empty[rs]));   // the raw stage is in registers now
                 if (++rs == C::kRawStages) {
                     rs = 0;
                     rph ^= 1u;
                 }
-                const int os = (int)(kop % C::kOpStages);
-                const uint32_t oph = (kop / C::kOpStages) & 1u;
-                kop += 2;
-                if (!abort_flag && !mbar_wait(smem_addr(&op_empty[os]), oph ^ 1u)) {
-                    atomicOr(p.err, MOE_DEVERR_TIMEOUT);
-                    abort_flag = 1;
-                }
-                if (!abort_flag) {
-                    tc_fence_after();
 #pragma unroll
-                    for (int q = 0; q < 2; q++) {
-                        const uint4 wv = q ? wv1 : wv0;
-                        const float sg = g ? (q ? sc.w : sc.z) : (q ? sc.y : sc.x);
-                        const uint32_t sfac = pack_scale<kF16>(sg);
-                        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-                        uint32_t out[16];
-#pragma unroll
-                        for (int j = 0; j < 4; j++) {   // word j: elements 8j .. 8j+7 of the group
-                            const uint32_t w = ws[j];
-                            out[4 * j + 0] = mul_x2<kF16>(nib_q2<kF16>(w), sfac);          // (e0, e4)
-                            out[4 * j + 1] = mul_x2<kF16>(nib_q2<kF16>(w >> 4), sfac);     // (e1, e5)
-                            out[4 * j + 2] = mul_x2<kF16>(nib_q2<kF16>(w >> 8), sfac);     // (e2, e6)
-                            out[4 * j + 3] = mul_x2<kF16>(nib_q2<kF16>(w >> 12), sfac);    // (e3, e7)
-                        }
-                        // k pairs of this group = columns q * 16 .. + 15 of the stage's A tile
-                        tmem_st16(tlane + kACol0 + os * kACols + q * 16, out);
+                for (int hh = 0; hh < C::kOpPerRaw / 2; hh++) {
+                    const int os = (int)(kop % C::kOpStages);
+                    const uint32_t oph = (kop / C::kOpStages) & 1u;
+                    kop += 2;
+                    if (!abort_flag && !mbar_wait(smem_addr(&op_empty[os]), oph ^ 1u)) {
+                        atomicOr(p.err, MOE_DEVERR_TIMEOUT);
+                        abort_flag = 1;
                     }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(smem_addr(&op_full[os]));
+                    if (!abort_flag) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int q = 0; q < 2; q++) {
+                            const uint4 w4 = wv[2 * hh + q];
+                            const uint32_t sfac = pack_scale<kF16>(sg[2 * hh + q]);
+                            const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+                            uint32_t out[16];
+#pragma unroll
+                            for (int j = 0; j < 4; j++) {   // word j: elements 8j .. 8j+7 of the group
+                                const uint32_t w = ws[j];
+                                out[4 * j + 0] = mul_x2<kF16>(nib_q2<kF16>(w), sfac);          // (e0, e4)
+                                out[4 * j + 1] = mul_x2<kF16>(nib_q2<kF16>(w >> 4), sfac);     // (e1, e5)
+                                out[4 * j + 2] = mul_x2<kF16>(nib_q2<kF16>(w >> 8), sfac);     // (e2, e6)
+                                out[4 * j + 3] = mul_x2<kF16>(nib_q2<kF16>(w >> 12), sfac);    // (e3, e7)
+                            }
+                            // k pairs of this group = columns q * 16 .. + 15 of the stage's A tile
+                            tmem_st16(tlane + kACol0 + os * kACols + q * 16, out);
+                        }
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(smem_addr(&op_full[os]));
+                    }
                 }
             }
         }
@@ -443,7 +460,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                 eph[b] ^= 1u;
                 tc_fence_after();
                 const uint32_t dcol = tmem_base + b * kAccStride;
-                for (int kb = 0; kb < 2 * nraw; kb++) {
+                for (int kb = 0; kb < C::kOpPerRaw * nraw; kb++) {
                     if (!abort_flag && !mbar_wait(smem_addr(&op_full[os]), oph)) {
                         atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                         abort_flag = 1;
@@ -629,11 +646,11 @@ h_to_f16_kernel(const float *__restrict__ h32, const unsigned int *__restrict__ 
     }
 }
 
-template <int MODE>
+template <int MODE, int RAWK>
 int launch_prefill_one(const PMaps &maps, const PParams &prm, int max_units, cudaStream_t s)
 {
-    using C = PCfg<MODE>;
-    auto kern = ffn_prefill_kernel<MODE>;
+    using C = PCfg<MODE, RAWK>;
+    auto kern = ffn_prefill_kernel<MODE, RAWK>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return MOE_ERR_CUDA;
@@ -711,12 +728,12 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     for (int i = 0; i < 2 && rc == MOE_OK; i++) {
         const uint64_t q_dim[4] = {(uint64_t)d / 2, (uint64_t)f, 2, outer[i]};
         const uint64_t q_str[3] = {(uint64_t)d / 2, (uint64_t)f * d / 2, qb};
-        const uint32_t q_box[4] = {kRawK / 2, (uint32_t)PCfg<kPGateUp>::kRowsPerMat, 2, 1};
+        const uint32_t q_box[4] = {128, (uint32_t)PCfg<kPGateUp, 256>::kRowsPerMat, 2, 1};
         const uint64_t s_dim[4] = {(uint64_t)d / G, (uint64_t)f, 2, outer[i]};
         const uint64_t s_str[3] = {(uint64_t)(d / G) * 4, (uint64_t)f * (d / G) * 4, sc * 4};
-        const uint32_t s_box[4] = {kRawK / 32, (uint32_t)PCfg<kPGateUp>::kRowsPerMat, 2, 1};
+        const uint32_t s_box[4] = {8, (uint32_t)PCfg<kPGateUp, 256>::kRowsPerMat, 2, 1};
         rc |= make_tmap_nd(&gm.q[i], qs[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, q_dim, q_str, q_box,
-                           CU_TENSOR_MAP_SWIZZLE_64B);
+                           CU_TENSOR_MAP_SWIZZLE_128B);
         rc |= make_tmap_nd(&gm.s[i], ss[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s_dim, s_str, s_box,
                            CU_TENSOR_MAP_SWIZZLE_NONE);
     }
@@ -735,10 +752,10 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pg.T = T;
     pg.k = k;
     pg.K = d;
-    pg.mtiles = f / PCfg<kPGateUp>::kRowsPerMat;
+    pg.mtiles = f / PCfg<kPGateUp, 256>::kRowsPerMat;
     pg.out_rows = f;
     const int max_units = (E < T * k ? E : T * k) + 1;
-    rc = launch_prefill_one<kPGateUp>(gm, pg, max_units, s);
+    rc = launch_prefill_one<kPGateUp, 256>(gm, pg, max_units, s);   // d is a multiple of 256
     if (rc == MOE_OK)
         rc = launch_pdl(h_to_f16_kernel, (int)rows, 256, 0, s, (const float *)ps.h32,
                         (const unsigned int *)ps.hmax, f, h_sorted, ps.h_scale);
@@ -746,12 +763,14 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
         return rc;
 
     // ---- down
+    const int dn_rawk = f % 256 == 0 ? 256 : 128;
     PMaps dm{};
     for (int i = 0; i < 2 && rc == MOE_OK; i++) {
         rc |= make_tmap_3d(&dm.q[i], qs[i] + (size_t)f * d, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, f / 2, d, outer[i],
-                           f / 2, qb, kRawK / 2, kTileM, CU_TENSOR_MAP_SWIZZLE_64B);
+                           f / 2, qb, dn_rawk / 2, kTileM,
+                           dn_rawk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
         rc |= make_tmap_3d(&dm.s[i], ss[i] + (size_t)2 * f * d / G, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, f / G, d,
-                           outer[i], (uint64_t)(f / G) * 4, sc * 4, kRawK / 32, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                           outer[i], (uint64_t)(f / G) * 4, sc * 4, dn_rawk / 32, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     rc |= make_tmap_2d(&dm.b, h_sorted, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, f, rows, (uint64_t)f * 2, kOpK, kTileN,
                        CU_TENSOR_MAP_SWIZZLE_128B);
@@ -766,7 +785,9 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pd.K = f;
     pd.mtiles = d / kTileM;
     pd.out_rows = d;
-    return launch_prefill_one<kPDown>(dm, pd, max_units, s);
+    if (dn_rawk == 256)
+        return launch_prefill_one<kPDown, 256>(dm, pd, max_units, s);
+    return launch_prefill_one<kPDown, 128>(dm, pd, max_units, s);
 }
 
 }  // namespace moe
