@@ -46,13 +46,18 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode", choices=["decode", "batched_decode", "prefill", "tiny"],
-                    help="tiny is the parity-size layer (fits in L2; for quick checks, not a bench line)")
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "batched_decode", "prefill", "stack", "tiny"],
+                    help="tiny is the parity-size layer (fits in L2; for quick checks, not a bench line); "
+                         "stack is 8 resident layers, the line's T from --tokens (default 64) plus a sweep "
+                         "over T in {1, 4, 16, 64, 256}")
     ap.add_argument("--replicas", type=int, default=4, help="device copies of the layer rotated across steps")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the routed expert count (small-footprint profiling runs); 0 = workload's")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the tokens per step (small-footprint profiling runs); 0 = workload's")
+    ap.add_argument("--mode", choices=["workload", "decode", "prefill"], default="workload",
+                    help="FFN path: the workload's own (prefill for prefill, decode otherwise) or forced")
     ap.add_argument("--graph-steps", type=int, default=100, help="steps captured per CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -182,7 +187,7 @@ def run_ours(args, rank, world, local):
         import dataclasses
         sh = dataclasses.replace(sh, E=args.experts or sh.E, T=args.tokens or sh.T)
     T, E, k, d, f = sh.T, sh.E, sh.k, sh.d, sh.f
-    prefill = args.workload == "prefill"
+    prefill = args.workload == "prefill" if args.mode == "workload" else args.mode == "prefill"
     mode = moe.MOE_MODE_PREFILL if prefill else moe.MOE_MODE_DECODE
     R = max(1, min(args.replicas, 2) if prefill else args.replicas)
     S = max(1, min(args.graph_steps if not prefill else 4, args.steps))
@@ -256,8 +261,8 @@ def run_ours(args, rank, world, local):
 
     # kernels per fused step: small batches logits(+x fragments), select+union, gate/up, down,
     # combine; otherwise logits, top-k, union, x fragments, gate/up, down, combine
-    if prefill:   # logits, top-k, union, plan, gather, gate/up, h conversion, down, combine
-        launches_per_step = 9
+    if prefill:   # logits, top-k, union, gather, gate/up, h conversion, down, combine
+        launches_per_step = 8
     else:
         launches_per_step = 5 if (T <= 8 and T * k <= 64) else 7
 
@@ -404,6 +409,218 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------- layer stack --
+
+def run_stack(args, rank, world, local):
+    """8 resident layers, out_l = x_l + MoE(RMSNorm(x_l)), each layer with its own
+    seeded experts, router and Zipf selection bias (its own expert permutation).
+    A step is one pass of T tokens through all 8 layers; tokens/s = T / step time.
+    The line's T is --tokens (default 64); "sweep" holds every T of the stack's
+    batch sweep, each timed the same way with its own step count."""
+    import torch
+
+    import int4_routed_expert_sigmoid_gb300 as moe
+    import workloads
+    from int4_routed_expert_sigmoid_gb300 import build as libbuild
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        try:
+            dist.init_process_group("nccl", device_id=dev)
+        except TypeError:
+            dist.init_process_group("nccl")
+    libbuild.build()
+    sh = workloads.WORKLOADS["stack"]
+    E, k, d, f, G, NL = sh.E, sh.k, sh.d, sh.f, sh.G, sh.layers
+    T_line = args.tokens or sh.T
+    mode = moe.MOE_MODE_PREFILL if args.mode == "prefill" else moe.MOE_MODE_DECODE
+    eps = 1e-5
+
+    # ---- the 8 layers, generated one at a time into one host buffer and copied to the device
+    qb, sc = workloads.expert_q_bytes(d, f), workloads.expert_s_count(d, f, G)
+    q_all = torch.empty((NL, E * qb + qb), dtype=torch.uint8, device=dev)
+    s_all = torch.empty((NL, E * sc + sc), dtype=torch.float32, device=dev)
+    q_host = np.empty((E, qb), dtype=np.uint8)
+    s_host = np.empty((E, sc), dtype=np.float32)
+    wgs, biases = [], []
+    for l in range(NL):
+        L = workloads.layer_inputs(sh, seed=0, layer=l, T=1, threads=os.cpu_count() or 8,
+                                   q_base=q_host, s_base=s_host)
+        q_all[l, :E * qb].copy_(torch.from_numpy(q_host.reshape(-1)))
+        s_all[l, :E * sc].copy_(torch.from_numpy(s_host.reshape(-1)))
+        q_all[l, E * qb:].copy_(torch.from_numpy(L.shared_q))
+        s_all[l, E * sc:].copy_(torch.from_numpy(L.shared_s))
+        wgs.append(torch.from_numpy(L.wg).to(dev))
+        biases.append(torch.from_numpy(L.bias).to(dev))
+        del L
+    torch.cuda.synchronize()
+    del q_host, s_host
+    layers = [moe.LayerWeights(q_all[l, :E * qb], s_all[l, :E * sc], q_all[l, E * qb:], s_all[l, E * sc:],
+                               E=E, d=d, f=f, G=G) for l in range(NL)]
+    hits = torch.zeros((NL, E), dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    blk = workloads.expert_q_bytes(d, f) + 4 * workloads.expert_s_count(d, f, G)
+    S = 8   # steps per captured graph (distinct inputs)
+
+    def make(T):
+        ctx = {"T": T}
+        ctx["xs"] = torch.from_numpy(workloads.activations(S * T, d, seed=1000 + rank)).to(dev).view(S, T, d)
+        ctx["acts"] = torch.empty((NL, T, d), dtype=torch.float32, device=dev)   # outputs of layers 0..6
+        ctx["outs"] = torch.empty((S, T, d), dtype=torch.float32, device=dev)
+        ctx["xn"] = torch.empty((T, d), dtype=torch.float32, device=dev)
+        ctx["idx"] = torch.empty((NL, T, k), dtype=torch.int32, device=dev)
+        ctx["wts"] = torch.empty((T, k), dtype=torch.float32, device=dev)
+        ctx["ws"] = moe.workspace(moe.layer_workspace_bytes(T, k, E, d, f, mode), dev)
+        return ctx
+
+    def stack_step(ctx, x, out):
+        for l in range(NL):
+            xin = x if l == 0 else ctx["acts"][l - 1]
+            xo = out if l == NL - 1 else ctx["acts"][l]
+            moe.moe_rms_norm(xin, eps, out=ctx["xn"])
+            moe.moe_layer_forward(ctx["xn"], wgs[l], biases[l], layers[l], k, 1, 1.0, mode=mode, residual=xin,
+                                  out=xo, topk_idx=ctx["idx"][l], topk_w=ctx["wts"], hits=hits[l],
+                                  ws=ctx["ws"], err=err)
+
+    def graph(ctx, n):
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for i in range(S):
+                stack_step(ctx, ctx["xs"][i], ctx["outs"][i])
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            for i in range(n):
+                stack_step(ctx, ctx["xs"][i % S], ctx["outs"][i % S])
+        return g
+
+    def n_uniq_layers(ctx):
+        idx = ctx["idx"].cpu().numpy()
+        return [int(np.unique(idx[l]).size) for l in range(NL)]
+
+    def timed(g, reps, tail_g=None):
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            g.replay()
+        if tail_g is not None:
+            tail_g.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        return t0.elapsed_time(t1)
+
+    peaks = load_peaks()
+
+    def bytes_of(T, nu):
+        # per layer: unique experts + shared, router weights and bias, x in, out, residual
+        return sum((n + 1) * blk + E * d * 4 + E * 4 + 3 * T * d * 4 for n in nu)
+
+    # ---- the batch sweep (each T timed for about two seconds)
+    sweep = []
+    for T in sh.batch_sweep:
+        ctx = make(T)
+        g = graph(ctx, S)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        probe = timed(g, 2) / (2 * S)
+        reps = max(3, min(500, int(2000.0 / max(probe * S, 1e-3))))
+        err.zero_()
+        el = reduce_max(world, [timed(g, reps)], dev)[0]
+        nu = n_uniq_layers(ctx)
+        ms = el / (reps * S)
+        by = bytes_of(T, nu)
+        sweep.append({"T": T, "steps": reps * S, "ms_per_step": round(ms, 5),
+                      "tokens_per_s": round(job_throughput(T, reps * S, world, el), 2),
+                      "stack_gbs": round(by / (ms * 1e-3) / 1e9, 1),
+                      "frac": round(by / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                      "n_uniq_per_layer": nu, "device_error": int(err.item())})
+        del g, ctx
+        torch.cuda.empty_cache()
+
+    # ---- the line: exactly --steps steps at T_line
+    ctx = make(T_line)
+    g_main = graph(ctx, S)
+    n_main, tail = divmod(args.steps, S)
+    g_tail = graph(ctx, tail) if tail else None
+    for _ in range(max(1, -(-args.warmup // S))):
+        g_main.replay()
+    torch.cuda.synchronize()
+    err.zero_()
+    sampler = ClockSampler(gpu_uuid(torch, local))
+    sampler.start()
+    time.sleep(0.3)
+    elapsed = timed(g_main, n_main, g_tail)
+    clocks = sampler.stop()
+    dev_err = int(err.item())
+    nu = n_uniq_layers(ctx)
+
+    # ---- end to end with host buffers (not graph-captured)
+    e2e_steps = max(1, min(args.e2e_steps, args.steps, 200))
+    x_host = torch.from_numpy(workloads.activations(e2e_steps * T_line, d, seed=5000 + rank))
+    x_host = x_host.view(e2e_steps, T_line, d).pin_memory()
+    out_host = torch.empty((e2e_steps, T_line, d), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty((T_line, d), dtype=torch.float32, device=dev)
+    out_dev = torch.empty((T_line, d), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        stack_step(ctx, x_dev, out_dev)
+    torch.cuda.synchronize()
+    barrier(world)
+    w0 = time.perf_counter()
+    for i in range(e2e_steps):
+        x_dev.copy_(x_host[i], non_blocking=True)
+        stack_step(ctx, x_dev, out_dev)
+        out_host[i].copy_(out_dev, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - w0
+    barrier(world)
+    dev_err |= int(err.item())
+
+    elapsed_max, e2e_max = reduce_max(world, [elapsed, e2e_s], dev)
+    ms_per_step = elapsed_max / args.steps
+    by = bytes_of(T_line, nu)
+    achieved = by / (ms_per_step * 1e-3) / 1e9
+    small = T_line <= 8 and T_line * k <= 64
+    per_layer = 1 + (5 if small else 7)    # RMS norm + the fused layer's kernels
+    line = {
+        "metric": METRIC, "value": round(job_throughput(T_line, args.steps, world, elapsed_max), 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"stack: {NL} resident MoE layers (out = x + MoE(RMSNorm(x))), E={E} routed + 1 "
+                               f"shared, k={k}, d={d}, f={f}, int4 group-{G} fp32 scales, Zipf(1.1) selection "
+                               f"bias with a per-layer expert permutation, T={T_line} token(s) per step",
+                   "T": T_line, "E": E, "k": k, "d": d, "f": f, "G": G, "layers": NL, "weights": "int4",
+                   "l2": f"inputs larger than L2: {NL} resident layers ({NL * (E + 1) * blk / 1e9:.1f} GB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "cuda_graph_steps": S},
+        "roofline": {"kernel": "whole 8-layer step (all kernels; bytes = sum of the layers' algorithmic bytes)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": peaks["source"], "bytes_per_step": by},
+        "n_uniq_per_layer": nu,
+        "sweep": sweep,
+        "e2e": {"value": round(T_line * e2e_steps * world / e2e_max, 2), "unit": UNIT,
+                "h2d_bytes_per_step": T_line * d * 4, "d2h_bytes_per_step": T_line * d * 4, "steps": e2e_steps},
+        "gpu_launches": NL * per_layer * args.steps,
+        "clocks": clocks,
+        "device_error": dev_err,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sh, args.cpu_seconds, layers=NL)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -481,8 +698,10 @@ def _oracle_layer(sh, f_used, seed=0):
     return oracle, L, q_base, s_base, shq, shs
 
 
-def cpu_baseline(sh, seconds: float) -> dict:
-    """The oracle, as it stands, on a bounded sample: full layers for a few tokens."""
+def cpu_baseline(sh, seconds: float, layers: int = 1) -> dict:
+    """The oracle, as it stands, on a bounded sample: full layers for a few tokens.
+    With layers > 1 (a stack of equally shaped layers) the rate of one layer is
+    divided by the layer count."""
     import workloads
     oracle, L, q_base, s_base, shq, shs = _oracle_layer(sh, sh.f)
     threads = oracle.threads()
@@ -496,9 +715,10 @@ def cpu_baseline(sh, seconds: float) -> dict:
     t = time.perf_counter()
     lay.tokens(np.arange(n, dtype=np.int32))
     el = time.perf_counter() - t
-    return {"value": round(n / el, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+    per = f"; rate / {layers} for the {layers}-layer stack" if layers > 1 else ""
+    return {"value": round(n / el / layers, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{n} tokens of the {sh.name} layer (route + shared + {sh.k} routed int4 experts, full "
-                      f"d={sh.d}, f={sh.f}), fp64 C oracle, OpenMP over tokens, {el:.1f} s"}
+                      f"d={sh.d}, f={sh.f}), fp64 C oracle, OpenMP over tokens, {el:.1f} s{per}"}
 
 
 def run_reference(args, rank, world):
@@ -537,16 +757,20 @@ def run_reference(args, rank, world):
     for i in range(args.steps):
         one(args.warmup + i)
     el = time.perf_counter() - t
-    value = args.steps * sh.T * (f_used / sh.f) / el
+    # each step carries one token of the workload's batch (tokens are independent);
+    # a stack step passes it through every layer, here one layer standing for each
+    value = args.steps * (f_used / sh.f) / el / sh.layers
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"{sh.name}: 1 MoE layer, E={sh.E} routed + 1 shared, k={sh.k}, d={sh.d}, "
+            "config": {"workload": f"{sh.name}: {sh.layers} MoE layer(s), E={sh.E} routed + 1 shared, k={sh.k}, d={sh.d}, "
                                    f"f={sh.f}, int4 group-{sh.G}, T={sh.T}"},
             "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
-                             "sample": f"each step: one token through the layer with every expert cut to its first "
-                                       f"{f_used} of {sh.f} intermediate rows; rate scaled by {sh.f}/{f_used}"},
+                             "sample": f"each step: one token of the T={sh.T} batch through the layer with every "
+                                       f"expert cut to its first {f_used} of {sh.f} intermediate rows; rate scaled "
+                                       f"by {sh.f}/{f_used}" + (f" and divided by {sh.layers} layers"
+                                                               if sh.layers > 1 else "")},
             "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -556,6 +780,9 @@ def main(argv=None):
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.workload == "stack":
+        run_stack(args, rank, world, local)
         return
     run_ours(args, rank, world, local)
 

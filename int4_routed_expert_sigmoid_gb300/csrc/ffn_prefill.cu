@@ -8,7 +8,7 @@
 // With ~128 tokens per routed expert the FFN is a real dense contraction.
 //
 // Design (GB300, sm_103a), one CTA per SM, persistent over work items:
-//  * item = (expert unit, tile of output rows, tile of <= 256 tokens).
+//  * item = (expert unit, tile of output rows, tile of <= 160 tokens).
 //    D[rows][tokens] = W[rows][K] * X[tokens][K]^T ("swap AB": the weights
 //    are the M = 128 operand, the tokens the N operand).  Gate/up stacks 64
 //    gate rows over the same 64 up rows in one A tile (an item is 64 rows of
@@ -16,11 +16,11 @@
 //    (expert, first sorted row, tokens, prefix of token tiles) in shared
 //    memory once, so items are decoded without global loads.
 //  * warp 0 (weight producer): TMA loads of the packed int4 rows + fp32 scales
-//    (raw ring, k-blocks of 128), running ahead of everything else; warp 14
-//    (token producer): TMA loads of the fp16 token rows (operand ring,
-//    k-blocks of 64, 128-byte swizzle).
-//  * warps 6-13 (dequant: two groups of four warps taking alternate op
-//    stages, thread = row of the A tile):
+//    (raw ring, 256 elements of a row per stage), running ahead of everything
+//    else; warp 14 (token producer): TMA loads of the fp16 token rows (operand
+//    ring, 128 elements per stage, 128-byte swizzle).
+//  * warps 6-13 (dequant: two groups of four warps, each taking one of the two
+//    op stages of every raw stage, thread = row of the A tile):
 //    nibbles -> fp16 (q * s) with an exact magic-exponent conversion
 //    (0x6400|(n^8) = 1032 + q, then subtract) and one multiply, written straight
 //    into tensor memory: the MMA reads A from there, so shared memory carries
@@ -31,8 +31,11 @@
 //  * warp 1: allocates tensor memory; one lane issues tcgen05.mma (M = 128,
 //    N = tokens rounded up to 16, K = 16 per instruction) into an fp32
 //    accumulator, and commits stage releases.  The 512 TMEM columns hold two
-//    accumulator buffers, so the MMAs of the next item run while the
-//    epilogue drains the previous one.
+//    accumulator buffers (so the MMAs of the next item run while the epilogue
+//    drains the previous one) and three A stages.  Issuing an MMA, waiting for
+//    a stage and committing its release each cost the single issuing thread
+//    tens of cycles whatever N is, so stages are made long (8 MMAs each) and
+//    N as large as the token tile allows.
 //  * warps 2-5 (epilogue, one TMEM subpartition each): gate/up -> the two
 //    up warps hand their values to the two gate warps through shared memory,
 //    which form h = silu(g) * u in fp32 plus the per-token max |h|; down -> y
@@ -59,35 +62,38 @@ constexpr int kPThreads = 480;                 // 15 warps
 constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kDeqWarp0 = 6, kBProdWarp = 14;
 constexpr int kDeqThreads = 256;               // warps 6-13: two groups of 128 (A row each), alternate op stages
 constexpr int kTileM = 128;                    // rows of the MMA's A tile
-constexpr int kTileN = 192;                    // tokens per item
-constexpr int kOpK = 64;
+constexpr int kTileN = 160;                    // tokens per item
 constexpr uint32_t kTmemCols = 512;
 // Tensor memory: two accumulator buffers of kTileN columns, then the A tiles of
 // the op stages (128 lanes x kOpK / 2 columns of packed fp16 each).
 constexpr int kAccStride = kTileN;
 constexpr int kACol0 = 2 * kTileN;
-constexpr int kACols = kOpK / 2;
 
 // Gate/up: the A tile stacks 64 rows of gate over the same 64 rows of up (one
 // MMA per k16 computes both), so an item covers 64 rows of h and the
 // accumulator needs only N columns.  Down: 128 rows of the down matrix.
 // RAWK: elements of a row per raw stage -- 256 (128-byte row segments, 128B
 // swizzle) when the reduction length allows it, else 128 (64 bytes, 64B swizzle).
+// A raw stage feeds two op stages of RAWK / 2 elements, one per dequant group.
 template <int MODE, int RAWK>
 struct PCfg {
     static constexpr int kRawK = RAWK;
     static constexpr int kRowB = RAWK / 2;                     // packed bytes of a row per raw stage
     static constexpr int kChunks = RAWK / 32;                  // 16-byte chunks (= groups) per row
-    static constexpr int kOpPerRaw = RAWK / kOpK;
+    static constexpr int kOpK = RAWK / 2;                      // reduction elements per op stage
+    static constexpr int kOpPerRaw = 2;
+    static constexpr int kCPO = kOpK / 32;                     // groups (16-byte chunks) per op stage
+    static constexpr int kACols = kOpK / 2;                    // TMEM columns of one A stage
+    static constexpr int kBChunks = kOpK / 64;                 // 128-byte token-row chunks per op stage
     static constexpr int kRawMats = MODE == kPGateUp ? 2 : 1;
     static constexpr int kRowsPerMat = kTileM / kRawMats;      // weight rows of one matrix per item
     static constexpr int kRawQ = kRowsPerMat * kRawK / 2;      // packed nibbles per matrix per raw stage
     static constexpr int kRawS = kRowsPerMat * (kRawK / 32) * 4;
-    static constexpr int kRawStage = kRawMats * (kRawQ + kRawS);   // 10 KB either way
+    static constexpr int kRawStage = kRawMats * (kRawQ + kRawS);   // 20 KB (RAWK 256) or 10 KB
     static constexpr int kRawStages = RAWK == 256 ? 4 : 6;
-    static constexpr int kOpB = kTileN * kOpK * 2;             // 24 KB fp16 of token rows (A is in TMEM)
+    static constexpr int kOpB = kTileN * kOpK * 2;             // fp16 token rows of a stage (A is in TMEM)
     static constexpr int kOpStage = kOpB;
-    static constexpr int kOpStages = 4;
+    static constexpr int kOpStages = 3;
     static_assert(kACol0 + kOpStages * kACols <= (int)kTmemCols, "tensor memory budget");
     static constexpr int kXchg = MODE == kPGateUp ? 2 * 2 * 32 * 16 * 4 : 0;   // up values for the gate warps (x2)
     static constexpr int kRing = kRawStages * kRawStage + kOpStages * kOpStage + kXchg;
@@ -357,7 +363,8 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                     if (!abort_flag) {
                         const uint32_t fb = smem_addr(&op_full[os]);
                         mbar_arrive_expect_tx(fb, C::kOpB);
-                        tma_load_2d(op_base + os * C::kOpStage, &maps.b, kb * kOpK, it.row0 + it.tok0, fb);
+                        tma_load_3d(op_base + os * C::kOpStage, &maps.b, 0, it.row0 + it.tok0, kb * C::kBChunks,
+                                    fb);
                     }
                     if (++os == C::kOpStages) {
                         os = 0;
@@ -368,9 +375,9 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
         }
     } else if (warp >= kDeqWarp0) {
         // -------------------------------------------------- dequantisation
-        // two groups of four warps take alternate op stages (group g: op stages g and g + 2 of
-        // every raw stage), so each has two stage periods for its work; a warp writes the 32 TMEM
-        // lanes of its subpartition: A rows 32 * (warp % 4) + lane
+        // two groups of four warps take alternate op stages (group g: op stage g of every raw
+        // stage, i.e. its chunks g * kCPO .. g * kCPO + kCPO - 1), so each has two stage periods for
+        // its work; a warp writes the 32 TMEM lanes of its subpartition: A rows 32 * (warp % 4) + lane
         const int ar = ((warp & 3) << 5) | lane;        // row of the A tile
         const int g = (warp - kDeqWarp0) >> 2;          // 0 or 1
         const int mat = C::kRawMats == 2 ? (ar >> 6) : 0;
@@ -387,18 +394,16 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                 }
                 const uint8_t *rsb = gen_base + rs * C::kRawStage;
                 // this row's packed bytes, swizzled (128B: 16-byte chunk c at c ^ (r & 7); 64B: at
-                // c ^ ((r >> 1) & 3)); chunk c = group c; the group's op stages h = g (+ 2) take chunks
-                // 2h, 2h + 1
-                constexpr int kQ = 2 * (C::kOpPerRaw / 2);   // chunks this thread uses per raw stage
+                // c ^ ((r >> 1) & 3)); chunk c = group c of the raw stage
                 const uint8_t *qrow = rsb + mat * C::kRawQ + r * C::kRowB;
                 const float *srow = reinterpret_cast<const float *>(rsb + C::kRawMats * C::kRawQ + mat * C::kRawS +
                                                                     r * C::kChunks * 4);
                 const int sw = RAWK == 256 ? (r & 7) : ((r >> 1) & 3);
-                uint4 wv[kQ];
-                float sg[kQ];
+                uint4 wv[C::kCPO];
+                float sg[C::kCPO];
 #pragma unroll
-                for (int q = 0; q < kQ; q++) {
-                    const int c = 2 * g + (q & 1) + 4 * (q >> 1);
+                for (int q = 0; q < C::kCPO; q++) {
+                    const int c = g * C::kCPO + q;
                     wv[q] = *reinterpret_cast<const uint4 *>(qrow + ((c ^ sw) << 4));
                     sg[q] = srow[c];
                 }
@@ -408,38 +413,35 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                     rs = 0;
                     rph ^= 1u;
                 }
+                const int os = (int)(kop % C::kOpStages);
+                const uint32_t oph = (kop / C::kOpStages) & 1u;
+                kop += 2;
+                if (!abort_flag && !mbar_wait(smem_addr(&op_empty[os]), oph ^ 1u)) {
+                    atomicOr(p.err, MOE_DEVERR_TIMEOUT);
+                    abort_flag = 1;
+                }
+                if (!abort_flag) {
+                    tc_fence_after();
 #pragma unroll
-                for (int hh = 0; hh < C::kOpPerRaw / 2; hh++) {
-                    const int os = (int)(kop % C::kOpStages);
-                    const uint32_t oph = (kop / C::kOpStages) & 1u;
-                    kop += 2;
-                    if (!abort_flag && !mbar_wait(smem_addr(&op_empty[os]), oph ^ 1u)) {
-                        atomicOr(p.err, MOE_DEVERR_TIMEOUT);
-                        abort_flag = 1;
-                    }
-                    if (!abort_flag) {
-                        tc_fence_after();
+                    for (int q = 0; q < C::kCPO; q++) {
+                        const uint4 w4 = wv[q];
+                        const uint32_t sfac = pack_scale<kF16>(sg[q]);
+                        const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+                        uint32_t out[16];
 #pragma unroll
-                        for (int q = 0; q < 2; q++) {
-                            const uint4 w4 = wv[2 * hh + q];
-                            const uint32_t sfac = pack_scale<kF16>(sg[2 * hh + q]);
-                            const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
-                            uint32_t out[16];
-#pragma unroll
-                            for (int j = 0; j < 4; j++) {   // word j: elements 8j .. 8j+7 of the group
-                                const uint32_t w = ws[j];
-                                out[4 * j + 0] = mul_x2<kF16>(nib_q2<kF16>(w), sfac);          // (e0, e4)
-                                out[4 * j + 1] = mul_x2<kF16>(nib_q2<kF16>(w >> 4), sfac);     // (e1, e5)
-                                out[4 * j + 2] = mul_x2<kF16>(nib_q2<kF16>(w >> 8), sfac);     // (e2, e6)
-                                out[4 * j + 3] = mul_x2<kF16>(nib_q2<kF16>(w >> 12), sfac);    // (e3, e7)
-                            }
-                            // k pairs of this group = columns q * 16 .. + 15 of the stage's A tile
-                            tmem_st16(tlane + kACol0 + os * kACols + q * 16, out);
+                        for (int j = 0; j < 4; j++) {   // word j: elements 8j .. 8j+7 of the group
+                            const uint32_t w = ws[j];
+                            out[4 * j + 0] = mul_x2<kF16>(nib_q2<kF16>(w), sfac);          // (e0, e4)
+                            out[4 * j + 1] = mul_x2<kF16>(nib_q2<kF16>(w >> 4), sfac);     // (e1, e5)
+                            out[4 * j + 2] = mul_x2<kF16>(nib_q2<kF16>(w >> 8), sfac);     // (e2, e6)
+                            out[4 * j + 3] = mul_x2<kF16>(nib_q2<kF16>(w >> 12), sfac);    // (e3, e7)
                         }
-                        tmem_wait_st();
-                        tc_fence_before();
-                        mbar_arrive(smem_addr(&op_full[os]));
+                        // k pairs of this group = columns q * 16 .. + 15 of the stage's A tile
+                        tmem_st16(tlane + kACol0 + os * C::kACols + q * 16, out);
                     }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(smem_addr(&op_full[os]));
                 }
             }
         }
@@ -468,10 +470,14 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                     tc_fence_after();
                     if (!abort_flag) {
                         const uint64_t bd = smem_desc_sw128(op_base + os * C::kOpStage);
-                        const uint32_t acol = tmem_base + kACol0 + os * kACols;
+                        const uint32_t acol = tmem_base + kACol0 + os * C::kACols;
+                        // B: 128-byte chunk c of the token rows at c * kTileN * 128 bytes; k16 step
+                        // within it +32 bytes (descriptor units of 16 bytes)
 #pragma unroll
-                        for (int k16 = 0; k16 < kOpK / 16; k16++)   // B: +32 bytes = +2 in the descriptor
-                            umma_f16_ts(dcol, acol + 8 * k16, bd + 2 * k16, idesc, (kb > 0 || k16 > 0) ? 1u : 0u);
+                        for (int k16 = 0; k16 < C::kOpK / 16; k16++)
+                            umma_f16_ts(dcol, acol + 8 * k16,
+                                        bd + (uint64_t)((k16 >> 2) * (kTileN * 128 / 16) + 2 * (k16 & 3)), idesc,
+                                        (kb > 0 || k16 > 0) ? 1u : 0u);
                         umma_commit(smem_addr(&op_empty[os]));
                     }
                     if (++os == C::kOpStages) {
@@ -646,6 +652,16 @@ h_to_f16_kernel(const float *__restrict__ h32, const unsigned int *__restrict__ 
     }
 }
 
+// fp16 token rows [rows][K] as (64 elements, row, 128-byte chunk): one load
+// brings kTileN rows x `chunks` chunks, chunk-major, 128-byte swizzled.
+int make_tmap_rows(CUtensorMap *m, const uint16_t *base, int K, size_t rows, int chunks)
+{
+    const uint64_t dim[3] = {64, (uint64_t)rows, (uint64_t)K / 64};
+    const uint64_t str[2] = {(uint64_t)K * 2, 128};
+    const uint32_t box[3] = {64, (uint32_t)kTileN, (uint32_t)chunks};
+    return make_tmap_nd(m, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, dim, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 template <int MODE, int RAWK>
 int launch_prefill_one(const PMaps &maps, const PParams &prm, int max_units, cudaStream_t s)
 {
@@ -737,8 +753,7 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
         rc |= make_tmap_nd(&gm.s[i], ss[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s_dim, s_str, s_box,
                            CU_TENSOR_MAP_SWIZZLE_NONE);
     }
-    rc |= make_tmap_2d(&gm.b, x_sorted, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, d, rows, (uint64_t)d * 2, kOpK, kTileN,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
+    rc |= make_tmap_rows(&gm.b, x_sorted, d, rows, PCfg<kPGateUp, 256>::kBChunks);
     if (rc != MOE_OK)
         return MOE_ERR_INVALID_ARG;
     PParams pg{};
@@ -772,8 +787,8 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
         rc |= make_tmap_3d(&dm.s[i], ss[i] + (size_t)2 * f * d / G, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, f / G, d,
                            outer[i], (uint64_t)(f / G) * 4, sc * 4, dn_rawk / 32, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
-    rc |= make_tmap_2d(&dm.b, h_sorted, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, f, rows, (uint64_t)f * 2, kOpK, kTileN,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
+    rc |= make_tmap_rows(&dm.b, h_sorted, f, rows, dn_rawk == 256 ? PCfg<kPDown, 256>::kBChunks
+                                                                   : PCfg<kPDown, 128>::kBChunks);
     if (rc != MOE_OK)
         return MOE_ERR_INVALID_ARG;
     PParams pd = pg;

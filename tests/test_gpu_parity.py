@@ -150,6 +150,7 @@ PREFILL_SHAPES = [
     workloads.WORKLOADS["tiny"],                                            # 1 gate/up m-tile, 2 down m-tiles
     Shape("prefill_ragged", E=16, k=4, d=1024, f=384, T=37, bias="normal"),  # 3 and 8 m-tiles
     Shape("prefill_two_ntiles", E=8, k=2, d=256, f=128, T=300),              # shared expert: 256 + 44 tokens
+    Shape("prefill_one_token", E=16, k=4, d=1024, f=384, T=1, bias="normal"),  # every unit a single token
 ]
 
 
