@@ -447,47 +447,52 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------ MMA issue
-        if (lane == 0) {
-            int os = 0, j = 0;
-            uint32_t oph = 0, eph[2] = {0u, 0u};
-            for (int i = blockIdx.x; i < n_items; i += gridDim.x, j++) {
-                const PItem it = decode_pitem<N>(p, tab, units, i);
-                const int b = j & 1;
-                const int n_mma = (it.ntok + 15) & ~15;
-                const uint32_t idesc = kF16 ? idesc_f16_f32(kTileM, n_mma) : idesc_bf16_f32(kTileM, n_mma);
-                if (!abort_flag && !mbar_wait(smem_addr(&acc_empty[b]), eph[b] ^ 1u)) {
+        // The whole warp runs the loop (lane 0 waits, the warp re-converges) and one elected
+        // lane issues each MMA and commit: the operands stay warp-uniform, which keeps the
+        // issue cost per instruction low.
+        int os = 0, j = 0;
+        uint32_t oph = 0, eph[2] = {0u, 0u};
+        for (int i = blockIdx.x; i < n_items; i += gridDim.x, j++) {
+            const PItem it = decode_pitem<N>(p, tab, units, i);
+            const int b = j & 1;
+            const int n_mma = (it.ntok + 15) & ~15;
+            const uint32_t idesc = kF16 ? idesc_f16_f32(kTileM, n_mma) : idesc_bf16_f32(kTileM, n_mma);
+            if (lane == 0 && !abort_flag && !mbar_wait(smem_addr(&acc_empty[b]), eph[b] ^ 1u)) {
+                atomicOr(p.err, MOE_DEVERR_TIMEOUT);
+                abort_flag = 1;
+            }
+            __syncwarp();
+            eph[b] ^= 1u;
+            tc_fence_after();
+            const uint32_t dcol = tmem_base + b * kAccStride;
+            for (int kb = 0; kb < C::kOpPerRaw * nraw; kb++) {
+                if (lane == 0 && !abort_flag && !mbar_wait(smem_addr(&op_full[os]), oph)) {
                     atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                     abort_flag = 1;
                 }
-                eph[b] ^= 1u;
+                __syncwarp();
                 tc_fence_after();
-                const uint32_t dcol = tmem_base + b * kAccStride;
-                for (int kb = 0; kb < C::kOpPerRaw * nraw; kb++) {
-                    if (!abort_flag && !mbar_wait(smem_addr(&op_full[os]), oph)) {
-                        atomicOr(p.err, MOE_DEVERR_TIMEOUT);
-                        abort_flag = 1;
-                    }
-                    tc_fence_after();
-                    if (!abort_flag) {
-                        const uint64_t bd = smem_desc_sw128(op_base + os * C::kOpStage);
-                        const uint32_t acol = tmem_base + kACol0 + os * C::kACols;
-                        // B: 128-byte chunk c of the token rows at c * kTileN * 128 bytes; k16 step
-                        // within it +32 bytes (descriptor units of 16 bytes)
+                if (!abort_flag) {   // one load for the warp: the same value in every lane
+                    const uint64_t bd = smem_desc_sw128(op_base + os * C::kOpStage);
+                    const uint32_t acol = tmem_base + kACol0 + os * C::kACols;
+                    // B: 128-byte chunk c of the token rows at c * kTileN * 128 bytes; k16 step
+                    // within it +32 bytes (descriptor units of 16 bytes)
 #pragma unroll
-                        for (int k16 = 0; k16 < C::kOpK / 16; k16++)
-                            umma_f16_ts(dcol, acol + 8 * k16,
-                                        bd + (uint64_t)((k16 >> 2) * (kTileN * 128 / 16) + 2 * (k16 & 3)), idesc,
-                                        (kb > 0 || k16 > 0) ? 1u : 0u);
-                        umma_commit(smem_addr(&op_empty[os]));
-                    }
-                    if (++os == C::kOpStages) {
-                        os = 0;
-                        oph ^= 1u;
-                    }
+                    for (int k16 = 0; k16 < C::kOpK / 16; k16++)
+                        umma_f16_ts_elect(dcol, acol + 8 * k16,
+                                          bd + (uint64_t)((k16 >> 2) * (kTileN * 128 / 16) + 2 * (k16 & 3)), idesc,
+                                          (kb > 0 || k16 > 0) ? 1u : 0u);
+                    umma_commit_elect(smem_addr(&op_empty[os]));
                 }
-                if (!abort_flag)
-                    umma_commit(smem_addr(&acc_full[b]));
+                __syncwarp();
+                if (++os == C::kOpStages) {
+                    os = 0;
+                    oph ^= 1u;
+                }
             }
+            if (!abort_flag)
+                umma_commit_elect(smem_addr(&acc_full[b]));
+            __syncwarp();
         }
     } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------------- epilogue
