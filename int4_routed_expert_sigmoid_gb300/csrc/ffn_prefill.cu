@@ -447,52 +447,67 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------ MMA issue
-        // The whole warp runs the loop (lane 0 waits, the warp re-converges) and one elected
-        // lane issues each MMA and commit: the operands stay warp-uniform, which keeps the
-        // issue cost per instruction low.
+        // The whole warp runs the loop and one elected lane issues each MMA and commit: the
+        // operands stay warp-uniform, which keeps the issue cost per instruction low.  The
+        // next stage's readiness is tested before this stage's MMAs are issued, so the test's
+        // latency overlaps them; only a stage found not ready is waited for (lane 0, then the
+        // result is broadcast).  After a timeout (here or in another role) the warp stops
+        // waiting and runs its loop to the end on whatever the stages hold.
         int os = 0, j = 0;
         uint32_t oph = 0, eph[2] = {0u, 0u};
+        int stop = 0, rdy = 0;   // warp-uniform
+        const int nkb = C::kOpPerRaw * nraw;
         for (int i = blockIdx.x; i < n_items; i += gridDim.x, j++) {
             const PItem it = decode_pitem<N>(p, tab, units, i);
             const int b = j & 1;
             const int n_mma = (it.ntok + 15) & ~15;
             const uint32_t idesc = kF16 ? idesc_f16_f32(kTileM, n_mma) : idesc_bf16_f32(kTileM, n_mma);
-            if (lane == 0 && !abort_flag && !mbar_wait(smem_addr(&acc_empty[b]), eph[b] ^ 1u)) {
-                atomicOr(p.err, MOE_DEVERR_TIMEOUT);
-                abort_flag = 1;
-            }
-            __syncwarp();
-            eph[b] ^= 1u;
-            tc_fence_after();
-            const uint32_t dcol = tmem_base + b * kAccStride;
-            for (int kb = 0; kb < C::kOpPerRaw * nraw; kb++) {
-                if (lane == 0 && !abort_flag && !mbar_wait(smem_addr(&op_full[os]), oph)) {
+            stop |= abort_flag;
+            int ok = 1;
+            if (lane == 0 && !stop)
+                ok = mbar_wait_or_abort(smem_addr(&acc_empty[b]), eph[b] ^ 1u, &abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
                     atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                     abort_flag = 1;
                 }
-                __syncwarp();
-                tc_fence_after();
-                if (!abort_flag) {   // one load for the warp: the same value in every lane
-                    const uint64_t bd = smem_desc_sw128(op_base + os * C::kOpStage);
-                    const uint32_t acol = tmem_base + kACol0 + os * C::kACols;
-                    // B: 128-byte chunk c of the token rows at c * kTileN * 128 bytes; k16 step
-                    // within it +32 bytes (descriptor units of 16 bytes)
-#pragma unroll
-                    for (int k16 = 0; k16 < C::kOpK / 16; k16++)
-                        umma_f16_ts_elect(dcol, acol + 8 * k16,
-                                          bd + (uint64_t)((k16 >> 2) * (kTileN * 128 / 16) + 2 * (k16 & 3)), idesc,
-                                          (kb > 0 || k16 > 0) ? 1u : 0u);
-                    umma_commit_elect(smem_addr(&op_empty[os]));
-                }
-                __syncwarp();
-                if (++os == C::kOpStages) {
-                    os = 0;
-                    oph ^= 1u;
-                }
+                stop = 1;
             }
-            if (!abort_flag)
-                umma_commit_elect(smem_addr(&acc_full[b]));
-            __syncwarp();
+            eph[b] ^= 1u;
+            tc_fence_after();
+            const uint32_t dcol = tmem_base + b * kAccStride;
+            for (int kb = 0; kb < nkb; kb++) {
+                if (!rdy && !stop) {
+                    ok = lane == 0 ? (mbar_wait_or_abort(smem_addr(&op_full[os]), oph, &abort_flag) ? 1 : 0) : 1;
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) {
+                        if (lane == 0) {
+                            atomicOr(p.err, MOE_DEVERR_TIMEOUT);
+                            abort_flag = 1;
+                        }
+                        stop = 1;
+                    }
+                }
+                tc_fence_after();
+                const int nos = os + 1 == C::kOpStages ? 0 : os + 1;
+                const uint32_t noph = nos == 0 ? oph ^ 1u : oph;
+                const int nrdy = mbar_test(smem_addr(&op_full[nos]), noph) ? 1 : 0;   // the next stage
+                const uint64_t bd = smem_desc_sw128(op_base + os * C::kOpStage);
+                const uint32_t acol = tmem_base + kACol0 + os * C::kACols;
+                // B: 128-byte chunk c of the token rows at c * kTileN * 128 bytes; k16 step
+                // within it +32 bytes (descriptor units of 16 bytes)
+#pragma unroll
+                for (int k16 = 0; k16 < C::kOpK / 16; k16++)
+                    umma_f16_ts_elect(dcol, acol + 8 * k16,
+                                      bd + (uint64_t)((k16 >> 2) * (kTileN * 128 / 16) + 2 * (k16 & 3)), idesc,
+                                      (kb > 0 || k16 > 0) ? 1u : 0u);
+                umma_commit_elect(smem_addr(&op_empty[os]));
+                os = nos;
+                oph = noph;
+                rdy = __shfl_sync(0xffffffffu, nrdy, 0);
+            }
+            umma_commit_elect(smem_addr(&acc_full[b]));
         }
     } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------------- epilogue
