@@ -12,12 +12,13 @@
 //    D[rows][tokens] = W[rows][K] * X[tokens][K]^T ("swap AB": the weights
 //    are the M = 128 operand, the tokens the N operand).  Gate/up stacks 64
 //    gate rows over the same 64 up rows in one A tile (an item is 64 rows of
-//    h; one MMA per k16 serves both matrices); down takes 128 rows.  Every CTA builds the unit table
+//    h; one MMA per k16 serves both matrices; each TMEM subpartition holds 16
+//    gate rows and the same 16 up rows); down takes 128 rows.  Every CTA builds the unit table
 //    (expert, first sorted row, tokens, prefix of token tiles) in shared
 //    memory once, so items are decoded without global loads.
 //  * warp 0 (weight producer): TMA loads of the packed int4 rows + fp32 scales
 //    (raw ring, 256 elements of a row per stage), running ahead of everything
-//    else; warp 14 (token producer): TMA loads of the fp16 token rows (operand
+//    else; warp 14 (token producer): TMA loads of the 16-bit token rows (operand
 //    ring, 128 elements per stage, 128-byte swizzle).
 //  * warps 6-13 (dequant: two groups of four warps, each taking one of the two
 //    op stages of every raw stage, thread = row of the A tile):
@@ -36,15 +37,16 @@
 //    a stage and committing its release each cost the single issuing thread
 //    tens of cycles whatever N is, so stages are made long (8 MMAs each) and
 //    N as large as the token tile allows.
-//  * warps 2-5 (epilogue, one TMEM subpartition each): gate/up -> the two
-//    up warps hand their values to the two gate warps through shared memory,
-//    which form h = silu(g) * u in fp32 plus the per-token max |h|; down -> y
-//    in fp32.
+//  * warps 2-5 (epilogue, one TMEM subpartition each): gate/up -> a gate lane
+//    and its up lane swap one value per token pair with a shuffle and form
+//    h = silu(g) * u in fp32; down -> y in fp32.
 //  * precision: both GEMMs run on fp16 operands, weights fp16(q * s) and
 //    activations scaled per row by a power of two so that |v| < 2^14 (the
 //    factor is applied to the fp32 result); fp32 accumulation, round to
-//    nearest even.  h is written in fp32 with a per-token max, then turned
-//    into scaled fp16 rows by a small kernel before the down GEMM.
+//    nearest even.  h is written in fp32, then a small kernel finds each
+//    row's max |h| and writes the scaled fp16 rows the down GEMM reads.
+//    (bf16 h and weights for the down GEMM would skip that pass, but their
+//    rounding alone uses up the prefill tolerance of 2e-2 of the output RMS.)
 //  * every wait is bounded; a timeout sets MOE_DEVERR_TIMEOUT, the roles stop
 //    working but keep their loop structure, and tensor memory is freed.
 #include <cuda_bf16.h>
@@ -95,8 +97,7 @@ struct PCfg {
     static constexpr int kOpStage = kOpB;
     static constexpr int kOpStages = 3;
     static_assert(kACol0 + kOpStages * kACols <= (int)kTmemCols, "tensor memory budget");
-    static constexpr int kXchg = MODE == kPGateUp ? 2 * 2 * 32 * 16 * 4 : 0;   // up values for the gate warps (x2)
-    static constexpr int kRing = kRawStages * kRawStage + kOpStages * kOpStage + kXchg;
+    static constexpr int kRing = kRawStages * kRawStage + kOpStages * kOpStage;
     static_assert(kRawStage % 1024 == 0 && kOpStage % 1024 == 0, "alignment");
 };
 
@@ -121,7 +122,6 @@ struct PParams {
     const int32_t *offsets, *uniq, *n_uniq;
     const float *row_scale;       // power-of-two factor of each sorted activation row (x or h)
     float *h32;                   // gate/up: h [rows][f] fp32, natural order
-    unsigned int *hmax;           // gate/up: per-row max |h| (fp32 bits)
     float *y_pair, *y_shared;     // down outputs
     int32_t *err;
     int T, k, K, mtiles, out_rows;
@@ -277,8 +277,6 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
     const uint32_t raw_base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
     const uint8_t *gen_base = dyn_smem + (raw_base - smem_addr(dyn_smem));
     const uint32_t op_base = raw_base + C::kRawStages * C::kRawStage;
-    float *xchg = reinterpret_cast<float *>(const_cast<uint8_t *>(gen_base) + C::kRawStages * C::kRawStage +
-                                            C::kOpStages * C::kOpStage);   // [2][2 warps][16][32]
     PUnit *tab = reinterpret_cast<PUnit *>(const_cast<uint8_t *>(gen_base) + C::kRing);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -378,10 +376,12 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
         // two groups of four warps take alternate op stages (group g: op stage g of every raw
         // stage, i.e. its chunks g * kCPO .. g * kCPO + kCPO - 1), so each has two stage periods for
         // its work; a warp writes the 32 TMEM lanes of its subpartition: A rows 32 * (warp % 4) + lane
+        // Gate/up: subpartition s holds gate rows 16s .. 16s + 15 in its lanes 0-15 and the same
+        // up rows in lanes 16-31, so the epilogue pairs them with a shuffle.
         const int ar = ((warp & 3) << 5) | lane;        // row of the A tile
         const int g = (warp - kDeqWarp0) >> 2;          // 0 or 1
-        const int mat = C::kRawMats == 2 ? (ar >> 6) : 0;
-        const int r = C::kRawMats == 2 ? (ar & 63) : ar;   // row within the matrix's raw tile
+        const int mat = C::kRawMats == 2 ? ((lane >> 4) & 1) : 0;
+        const int r = C::kRawMats == 2 ? (((warp & 3) << 4) | (lane & 15)) : ar;   // row within the matrix's tile
         const uint32_t tlane = tmem_base + ((uint32_t)((warp & 3) << 5) << 16);
         int rs = 0;
         uint32_t rph = 0;
@@ -514,7 +514,6 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
         const int sub = warp & 3;                 // TMEM lanes 32*sub .. 32*sub+31 = A rows
         uint32_t fph[2] = {0u, 0u};
         int j = 0;
-        int xpar = 0;   // exchange buffer of the next 16-column chunk (alternates across items too)
         for (int i = blockIdx.x; i < n_items; i += gridDim.x, j++) {
             const PItem it = decode_pitem<N>(p, tab, units, i);
             const int b = j & 1;
@@ -524,57 +523,46 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
             }
             fph[b] ^= 1u;
             tc_fence_after();
-            // (no early exit on abort: the four warps meet at a named barrier per chunk, so they
-            // all run the same chunks; after an abort the values are discarded garbage)
-            {
-                const uint32_t tl = tmem_base + ((uint32_t)(sub * 32) << 16) + b * kAccStride;
-                for (int c0 = 0; c0 < it.ntok; c0 += 16) {
-                    const int ch = xpar;
-                    xpar ^= 1;
-                    uint32_t v[16];
-                    tmem_ld16(tl + c0, v);
-                    // the row factors of these 16 tokens, one per lane, broadcast below
-                    const int nj = min(16, it.ntok - c0);
+            const uint32_t tl = tmem_base + ((uint32_t)(sub * 32) << 16) + b * kAccStride;
+            for (int c0 = 0; c0 < it.ntok; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(tl + c0, v);
+                const int nj = min(16, it.ntok - c0);
+                if (MODE == kPGateUp) {
+                    // lane l < 16: gate row 16 sub + l; lane l + 16: the same up row.  Pair q of
+                    // tokens (2q, 2q + 1): the gate lane forms h of token 2q, the up lane token 2q + 1,
+                    // each taking the other's value with one shuffle.
                     const float rfl = lane < nj ? p.row_scale[it.row0 + it.tok0 + c0 + lane] : 0.f;
                     tmem_wait_ld();
-                    if (MODE == kPGateUp) {
-                        // up rows (subpartitions 2, 3) hand their values to the gate rows (0, 1)
-                        float *xb = xchg + ch * (2 * 16 * 32);
-                        if (sub >= 2) {
+                    const int hi = lane >> 4;
+                    const int hr = it.mtile * 64 + sub * 16 + (lane & 15);   // column of h
 #pragma unroll
-                            for (int jj = 0; jj < 16; jj++)
-                                xb[((sub - 2) * 16 + jj) * 32 + lane] = __uint_as_float(v[jj]);
+                    for (int q = 0; q < 8; q++) {
+                        const float mine = __uint_as_float(hi ? v[2 * q + 1] : v[2 * q]);
+                        const float other = __shfl_xor_sync(0xffffffffu,
+                                                            __uint_as_float(hi ? v[2 * q] : v[2 * q + 1]), 16);
+                        const int jj = 2 * q + hi;
+                        const float rf = __shfl_sync(0xffffffffu, rfl, jj);
+                        if (jj < nj) {
+                            const float gv = (hi ? other : mine) * rf;
+                            const float uv = (hi ? mine : other) * rf;
+                            const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                            p.h32[(size_t)(it.row0 + it.tok0 + c0 + jj) * p.out_rows + hr] = hv;
                         }
-                        named_bar_sync(2, 128);
-                        if (sub < 2) {
-                            const int hr = it.mtile * 64 + sub * 32 + lane;   // row of h
+                    }
+                } else {
+                    const float rfl = lane < nj ? p.row_scale[it.row0 + it.tok0 + c0 + lane] : 0.f;
+                    tmem_wait_ld();
+                    const int orow = it.mtile * kTileM + sub * 32 + lane;
 #pragma unroll
-                            for (int jj = 0; jj < 16; jj++) {
-                                const float rf = __shfl_sync(0xffffffffu, rfl, jj);
-                                if (jj >= nj)
-                                    break;
-                                const int tok = it.tok0 + c0 + jj;
-                                const float gv = __uint_as_float(v[jj]) * rf;
-                                const float uv = xb[(sub * 16 + jj) * 32 + lane] * rf;
-                                const float hv = gv / (1.0f + expf(-gv)) * uv;
-                                p.h32[(size_t)(it.row0 + tok) * p.out_rows + hr] = hv;
-                                const unsigned mx = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
-                                if (lane == 0)
-                                    atomicMax(p.hmax + it.row0 + tok, mx);
-                            }
-                        }
-                    } else {
-                        const int orow = it.mtile * kTileM + sub * 32 + lane;
-#pragma unroll
-                        for (int jj = 0; jj < 16; jj++) {
-                            const float rf = __shfl_sync(0xffffffffu, rfl, jj);
-                            if (jj >= nj)
-                                break;
-                            const int tok = it.tok0 + c0 + jj;
-                            float *dst = it.expert < 0 ? p.y_shared + (size_t)tok * p.out_rows
-                                                       : p.y_pair + (size_t)(it.row0 + tok) * p.out_rows;
-                            dst[orow] = __uint_as_float(v[jj]) * rf;
-                        }
+                    for (int jj = 0; jj < 16; jj++) {
+                        const float rf = __shfl_sync(0xffffffffu, rfl, jj);
+                        if (jj >= nj)
+                            break;
+                        const int tok = it.tok0 + c0 + jj;
+                        float *dst = it.expert < 0 ? p.y_shared + (size_t)tok * p.out_rows
+                                                   : p.y_pair + (size_t)(it.row0 + tok) * p.out_rows;
+                        dst[orow] = __uint_as_float(v[jj]) * rf;
                     }
                 }
             }
@@ -602,7 +590,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
 // One block of 256 threads per row.
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ sorted_pair, int T, int k, int K,
-                   uint16_t *__restrict__ out, float *__restrict__ row_scale, unsigned int *__restrict__ hmax)
+                   uint16_t *__restrict__ out, float *__restrict__ row_scale)
 {
     __shared__ float wmax[8];
     griddep_launch_dependents();
@@ -628,10 +616,8 @@ gather_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ sort
     int e = 0;
     frexpf(mx, &e);
     const float up = mx > 0.f ? ldexpf(1.0f, 14 - e) : 1.0f;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0)
         row_scale[r] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
-        hmax[r] = 0u;
-    }
     for (int c = threadIdx.x; c < K / 8; c += 256) {
         const float4 *sp = reinterpret_cast<const float4 *>(xr + c * 8);
         const float4 a = sp[0], b = sp[1];
@@ -645,21 +631,37 @@ gather_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ sort
 }
 
 // h rows (fp32) -> fp16 rows scaled by 2^(14-e), e from the row's max |h|,
-// permuted within each 8; h_scale keeps 2^(e-14).  One block per row.
+// permuted within each 8 like the weights; h_scale keeps 2^(e-14).  One block
+// of 256 threads per row: a pass for the max, a pass to convert (the row is
+// then in L1).
 __global__ void __launch_bounds__(256)
-h_to_f16_kernel(const float *__restrict__ h32, const unsigned int *__restrict__ hmax, int K,
-                uint16_t *__restrict__ out, float *__restrict__ h_scale)
+h_to_f16_kernel(const float *__restrict__ h32, int K, uint16_t *__restrict__ out, float *__restrict__ h_scale)
 {
+    __shared__ float wmax[8];
     griddep_launch_dependents();
     griddep_wait();
     const int r = blockIdx.x;
-    const float mx = __uint_as_float(hmax[r]);
+    const float *hr = h32 + (size_t)r * K;
+    float mx = 0.f;
+    for (int i = threadIdx.x; i < K / 4; i += 256) {
+        const float4 v = reinterpret_cast<const float4 *>(hr)[i];
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if ((threadIdx.x & 31) == 0)
+        wmax[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; w++)
+        mx = fmaxf(mx, wmax[w]);
     int e = 0;
     frexpf(mx, &e);
     const float up = mx > 0.f ? ldexpf(1.0f, 14 - e) : 1.0f;
     if (threadIdx.x == 0)
         h_scale[r] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
-    const float *hr = h32 + (size_t)r * K;
     for (int c = threadIdx.x; c < K / 8; c += 256) {
         const float4 *sp = reinterpret_cast<const float4 *>(hr + c * 8);
         const float4 a = sp[0], b = sp[1];
@@ -672,7 +674,7 @@ h_to_f16_kernel(const float *__restrict__ h32, const unsigned int *__restrict__ 
     }
 }
 
-// fp16 token rows [rows][K] as (64 elements, row, 128-byte chunk): one load
+// 16-bit token rows [rows][K] as (64 elements, row, 128-byte chunk): one load
 // brings kTileN rows x `chunks` chunks, chunk-major, 128-byte swizzled.
 int make_tmap_rows(CUtensorMap *m, const uint16_t *base, int K, size_t rows, int chunks)
 {
@@ -705,9 +707,8 @@ int launch_prefill_one(const PMaps &maps, const PParams &prm, int max_units, cud
 namespace {
 
 struct PrefillScratch {
-    uint16_t *x16, *h16;
+    uint16_t *x16, *h16;   // scaled fp16 x and h rows
     float *x_scale, *h_scale, *h32;
-    unsigned int *hmax;
 };
 
 size_t prefill_layout(int T, int k, int d, int f, uint8_t *base, PrefillScratch *o)
@@ -725,7 +726,6 @@ size_t prefill_layout(int T, int k, int d, int f, uint8_t *base, PrefillScratch 
     s.h32 = reinterpret_cast<float *>(take(rows * f * 4));
     s.x_scale = reinterpret_cast<float *>(take(rows * 4));
     s.h_scale = reinterpret_cast<float *>(take(rows * 4));
-    s.hmax = reinterpret_cast<unsigned int *>(take(rows * 4));
     if (o)
         *o = s;
     return off;
@@ -750,8 +750,7 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     int rc = MOE_OK;
 
     // gathered fp16 token rows
-    rc = launch_pdl(gather_rows_kernel, (int)rows, 256, 0, s, a.x, a.sorted_pair, T, k, d, x_sorted, row_scale,
-                    ps.hmax);
+    rc = launch_pdl(gather_rows_kernel, (int)rows, 256, 0, s, a.x, a.sorted_pair, T, k, d, x_sorted, row_scale);
     if (rc != MOE_OK)
         return rc;
 
@@ -782,7 +781,6 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pg.n_uniq = a.n_uniq;
     pg.row_scale = row_scale;
     pg.h32 = ps.h32;
-    pg.hmax = ps.hmax;
     pg.err = a.err;
     pg.T = T;
     pg.k = k;
@@ -792,8 +790,7 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     const int max_units = (E < T * k ? E : T * k) + 1;
     rc = launch_prefill_one<kPGateUp, 256>(gm, pg, max_units, s);   // d is a multiple of 256
     if (rc == MOE_OK)
-        rc = launch_pdl(h_to_f16_kernel, (int)rows, 256, 0, s, (const float *)ps.h32,
-                        (const unsigned int *)ps.hmax, f, h_sorted, ps.h_scale);
+        rc = launch_pdl(h_to_f16_kernel, (int)rows, 256, 0, s, (const float *)ps.h32, f, h_sorted, ps.h_scale);
     if (rc != MOE_OK)
         return rc;
 
@@ -813,7 +810,6 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
         return MOE_ERR_INVALID_ARG;
     PParams pd = pg;
     pd.h32 = nullptr;
-    pd.hmax = nullptr;
     pd.row_scale = ps.h_scale;
     pd.y_pair = a.y_pair;
     pd.y_shared = a.y_shared;
