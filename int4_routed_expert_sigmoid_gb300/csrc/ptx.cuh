@@ -278,6 +278,20 @@ __device__ __forceinline__ void umma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tm
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::tf32 (fp32 D), called by a whole
+// converged warp: one elected lane issues.
+__device__ __forceinline__ void umma_tf32_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // As umma_commit, called by a whole converged warp (one elected lane commits).
 __device__ __forceinline__ void umma_commit_elect(uint32_t bar)
 {
@@ -343,6 +357,23 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
            | (1u << 10)                   // B format: bf16
            | ((uint32_t)(N >> 3) << 17)   // N / 8
            | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
+// Instruction descriptor of kind::tf32: tf32 A and B, fp32 D, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N)
+{
+    return (1u << 4)                      // D format: f32
+           | (2u << 7)                    // A format: tf32
+           | (2u << 10)                   // B format: tf32
+           | ((uint32_t)(N >> 3) << 17)   // N / 8
+           | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
+// Round an fp32 value to tf32 (10 fraction bits; nearest, ties away from zero):
+// add half a unit of the 11th fraction bit, clear the 13 low bits.
+__device__ __forceinline__ float to_tf32(float v)
+{
+    return __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xFFFFE000u);
 }
 
 // Instruction descriptor of kind::f16: fp16 A and B, fp32 D, both K-major, M x N.

@@ -132,6 +132,7 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
 // 64 x 64 tile per CTA, 256 threads x (4 x 4), k-slabs of 16 staged in shared
 // memory (transposed so both operands are read as float4 broadcasts).
 constexpr int kBM = 64, kBN = 64, kBK = 16;
+constexpr int kTcMinTokens = 512;   // from here on the tensor-core kernel below is used
 
 __global__ void __launch_bounds__(256)
 logits_tiled_kernel(const float *__restrict__ x, const float *__restrict__ wg, int T, int d, int E,
@@ -179,6 +180,182 @@ logits_tiled_kernel(const float *__restrict__ x, const float *__restrict__ wg, i
         for (int j = 0; j < 4; j++)
             if (m0 + tm + i < T && n0 + tn + j < E)
                 logits[(size_t)(m0 + tm + i) * E + n0 + tn + j] = acc[i][j];
+}
+
+// Large T on the tensor cores: split-tf32 GEMM.  Every fp32 operand is split
+// into hi = tf32(v) and lo = tf32(v - hi) (together within about 2^-22 of v,
+// with fp32's range, so no scaling is needed), and
+//   x . w = x_hi w_hi + x_hi w_lo + x_lo w_hi (+ x_lo w_lo, below 2^-22, dropped)
+// takes three kind::tf32 MMAs per k8 step.  The tensor cores' fp32
+// accumulation does not round to nearest, and its error grows with the number
+// of accumulation steps, so tensor memory holds only the partial sum of a
+// short run of k (kRChunk stages, 24 MMAs); drain warps add the partials in
+// fp32 registers, rounding to nearest, while the MMAs of the next run go to
+// the other accumulator.
+// CTA = 128 tokens x 64 experts; 32 reduction elements per stage (one 128-byte
+// swizzled row of fp32 per token/expert).  Warp 0: TMA producer; warp 1: MMA
+// issue (whole warp, one elected lane) and tensor-memory owner; warps 2-5:
+// split each stage in place (hi over the loaded values, lo beside them);
+// warps 6-9: drain the partials (one TMEM subpartition each) and write the
+// logits.  Waits are bounded; a CTA that timed out writes NaN logits (the
+// routing call has no error word).
+constexpr int kRM = 128, kRN = 64, kRK = 32, kRStages = 4, kRThreads = 320, kRChunk = 2;
+constexpr int kRXB = kRM * kRK * 4, kRWB = kRN * kRK * 4;   // 16 KB, 8 KB
+constexpr int kRStage = 2 * (kRXB + kRWB);                    // x hi, w hi, x lo, w lo
+constexpr size_t kRSmem = 1024 + (size_t)kRStages * kRStage;
+
+__global__ void __launch_bounds__(kRThreads, 1)
+logits_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mw, int T, int d,
+                 int E, float *__restrict__ logits)
+{
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ __align__(8) uint64_t full[kRStages], conv[kRStages], empty[kRStages], accf[2], acce[2];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_flag;
+    const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
+    uint8_t *gbase = dyn_smem + (base - smem_addr(dyn_smem));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRStages; s++) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&conv[s]), 128);
+            mbar_init(smem_addr(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(smem_addr(&accf[b]), 1);
+            mbar_init(smem_addr(&acce[b]), 128);
+        }
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&tmem_base_sh), 2 * kRN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+    const int m0 = blockIdx.y * kRM, n0 = blockIdx.x * kRN;
+    const int nk = d / kRK;
+    const int nchunk = (nk + kRChunk - 1) / kRChunk;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int kb = 0; kb < nk; kb++) {
+                const int s = kb % kRStages;
+                const uint32_t ph = (uint32_t)(kb / kRStages) & 1u;
+                if (!abort_flag && !mbar_wait(smem_addr(&empty[s]), ph ^ 1u))
+                    abort_flag = 1;
+                if (!abort_flag) {
+                    const uint32_t sb = base + s * kRStage;
+                    mbar_arrive_expect_tx(smem_addr(&full[s]), kRXB + kRWB);
+                    tma_load_2d(sb, &mx, kb * kRK, m0, smem_addr(&full[s]));
+                    tma_load_2d(sb + kRXB, &mw, kb * kRK, n0, smem_addr(&full[s]));
+                }
+            }
+        }
+    } else if (warp == 1) {
+        constexpr uint32_t idesc = idesc_tf32_f32(kRM, kRN);
+        for (int ch = 0; ch < nchunk; ch++) {
+            const int b = ch & 1;
+            int ok = 1;
+            if (lane == 0)
+                ok = (!abort_flag &&
+                      mbar_wait_or_abort(smem_addr(&acce[b]), ((uint32_t)(ch >> 1) & 1u) ^ 1u, &abort_flag)) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok && lane == 0)
+                abort_flag = 1;
+            tc_fence_after();
+            const uint32_t dcol = tmem + b * kRN;
+            const int kb1 = min(nk, (ch + 1) * kRChunk);
+            for (int kb = ch * kRChunk; kb < kb1; kb++) {
+                const int s = kb % kRStages;
+                const uint32_t ph = (uint32_t)(kb / kRStages) & 1u;
+                ok = 1;
+                if (lane == 0)
+                    ok = (!abort_flag && mbar_wait_or_abort(smem_addr(&conv[s]), ph, &abort_flag)) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok && lane == 0)
+                    abort_flag = 1;
+                tc_fence_after();
+                const uint32_t sb = base + s * kRStage;
+                const uint64_t xh = smem_desc_sw128(sb), wh = smem_desc_sw128(sb + kRXB);
+                const uint64_t xl = smem_desc_sw128(sb + kRXB + kRWB), wl = smem_desc_sw128(sb + 2 * kRXB + kRWB);
+#pragma unroll
+                for (int j = 0; j < kRK / 8; j++) {   // k8 step j: +32 bytes = +2 in the descriptors
+                    umma_tf32_elect(dcol, xh + 2 * j, wh + 2 * j, idesc, (kb > ch * kRChunk || j > 0) ? 1u : 0u);
+                    umma_tf32_elect(dcol, xh + 2 * j, wl + 2 * j, idesc, 1u);
+                    umma_tf32_elect(dcol, xl + 2 * j, wh + 2 * j, idesc, 1u);
+                }
+                umma_commit_elect(smem_addr(&empty[s]));
+            }
+            umma_commit_elect(smem_addr(&accf[b]));
+        }
+    } else if (warp < 6) {
+        // split: hi in place, lo at the same offset in the lo half of the stage
+        const int c = threadIdx.x - 64;   // 0 .. 127
+        for (int kb = 0; kb < nk; kb++) {
+            const int s = kb % kRStages;
+            const uint32_t ph = (uint32_t)(kb / kRStages) & 1u;
+            if (!abort_flag && !mbar_wait(smem_addr(&full[s]), ph))
+                abort_flag = 1;
+            float4 *hi = reinterpret_cast<float4 *>(gbase + s * kRStage);
+            float4 *lo = reinterpret_cast<float4 *>(gbase + s * kRStage + kRXB + kRWB);
+#pragma unroll 4
+            for (int i = c; i < (kRXB + kRWB) / 16; i += 128) {
+                const float4 v = hi[i];
+                float4 h, l;
+                h.x = to_tf32(v.x); l.x = to_tf32(v.x - h.x);
+                h.y = to_tf32(v.y); l.y = to_tf32(v.y - h.y);
+                h.z = to_tf32(v.z); l.z = to_tf32(v.z - h.z);
+                h.w = to_tf32(v.w); l.w = to_tf32(v.w - h.w);
+                hi[i] = h;
+                lo[i] = l;
+            }
+            fence_proxy_async_smem();   // generic-proxy writes, read next by the tensor cores
+            mbar_arrive(smem_addr(&conv[s]));
+        }
+    } else {
+        // drain: TMEM lane = token row of the tile, columns = experts
+        const int sub = warp & 3;
+        float sum[kRN];
+#pragma unroll
+        for (int q = 0; q < kRN; q++)
+            sum[q] = 0.f;
+        bool ok = true;
+        for (int ch = 0; ch < nchunk; ch++) {
+            const int b = ch & 1;
+            ok = ok && !abort_flag && mbar_wait_or_abort(smem_addr(&accf[b]), (uint32_t)(ch >> 1) & 1u, &abort_flag);
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < kRN; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem + ((uint32_t)(sub * 32) << 16) + b * kRN + c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 16; q++)
+                    sum[c0 + q] += __uint_as_float(v[q]);
+            }
+            tc_fence_before();
+            mbar_arrive(smem_addr(&acce[b]));
+        }
+        const int t = m0 + sub * 32 + lane;
+        if (t < T) {
+            float4 *dst = reinterpret_cast<float4 *>(logits + (size_t)t * E + n0);
+#pragma unroll
+            for (int q = 0; q < kRN / 4; q++)
+                dst[q] = ok ? make_float4(sum[4 * q], sum[4 * q + 1], sum[4 * q + 2], sum[4 * q + 3])
+                            : make_float4(NAN, NAN, NAN, NAN);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, 2 * kRN);
+    }
 }
 
 // ------------------------------------------------------------------ top-k ---
@@ -286,7 +463,28 @@ act_frag_kernel(const float *__restrict__ x, int K, uint8_t *__restrict__ frag, 
 int launch_router_logits(const float *x, const float *wg, int T, int d, int E, float *logits,
                          cudaStream_t s)
 {
-    if (T >= 128 && d % kBK == 0) {
+    if (T >= kTcMinTokens && d % kRK == 0 && E % kRN == 0 && ((uintptr_t)x & 15) == 0 &&
+        ((uintptr_t)wg & 15) == 0 && ((uintptr_t)logits & 15) == 0) {
+        CUtensorMap mx, mw;
+        int rc = make_tmap_2d(&mx, x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, T, (uint64_t)d * 4, kRK, kRM,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+        rc |= make_tmap_2d(&mw, wg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, E, (uint64_t)d * 4, kRK, kRN,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != MOE_OK)
+            return MOE_ERR_INVALID_ARG;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+            return MOE_ERR_CUDA;
+        static int configured[64] = {0};
+        if (!configured[dev]) {
+            if (cudaFuncSetAttribute(logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmem) !=
+                cudaSuccess)
+                return MOE_ERR_CUDA;
+            configured[dev] = 1;
+        }
+        dim3 grid(E / kRN, (T + kRM - 1) / kRM);
+        logits_tc_kernel<<<grid, kRThreads, kRSmem, s>>>(mx, mw, T, d, E, logits);
+    } else if (T >= 128 && d % kBK == 0) {
         dim3 grid((E + kBN - 1) / kBN, (T + kBM - 1) / kBM);
         logits_tiled_kernel<<<grid, 256, 0, s>>>(x, wg, T, d, E, logits);
     } else {

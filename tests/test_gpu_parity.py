@@ -198,3 +198,31 @@ def test_rms_norm_parity(T, d, scale):
     m.moe_rms_norm(xd, 1e-5, out=xd)
     torch.cuda.synchronize()
     assert np.array_equal(host(xd), out)
+
+
+ROUTE_TC = [
+    # (T, E, d, bias, x scale): token counts that take the tensor-core logits kernel, a ragged last
+    # token tile, several expert tiles, and inputs far from unit scale (the split keeps fp32's range)
+    (512, 64, 1024, "normal", 1.0),
+    (777, 128, 2048, "zipf", 1.0),
+    (640, 256, 512, "normal", 1e3),
+    (520, 64, 256, "zero", 1e-3),
+]
+
+
+@pytest.mark.parametrize("T,E,d,bias,xs", ROUTE_TC, ids=lambda v: str(v))
+def test_route_tensor_core_logits(T, E, d, bias, xs):
+    """Large-T routing (split-tf32 logits on the tensor cores) against the fp64 oracle."""
+    m = moe()
+    k = 8
+    x = workloads.activations(T, d, seed=11) * np.float32(xs)
+    wg = workloads.router_weights(E, d, seed=12)
+    b = workloads.selection_bias(E, bias, seed=13)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    idx, w, logits = m.moe_route(t(x), t(wg), None if b is None else t(b), k)
+    torch.cuda.synchronize()
+    o_idx, o_w, o_logits, keys = oracle.route(x, wg, b, k, 1, 1.0)
+    lg = host(logits)
+    assert np.isfinite(lg).all()
+    assert np.max(np.abs(lg - o_logits)) <= 1e-5 * max(1.0, float(np.abs(o_logits).max()))
+    compare_routing(host(idx), host(w), o_idx, o_w, keys, k)
