@@ -435,7 +435,8 @@ def run_stack(args, rank, world, local):
     sh = workloads.WORKLOADS["stack"]
     E, k, d, f, G, NL = sh.E, sh.k, sh.d, sh.f, sh.G, sh.layers
     T_line = args.tokens or sh.T
-    mode = moe.MOE_MODE_PREFILL if args.mode == "prefill" else moe.MOE_MODE_DECODE
+    mode = {"workload": moe.MOE_MODE_AUTO, "decode": moe.MOE_MODE_DECODE,
+            "prefill": moe.MOE_MODE_PREFILL}[args.mode]   # automatic: the library picks the path by T
     eps = 1e-5
 
     # ---- the 8 layers, generated one at a time into one host buffer and copied to the device
@@ -588,15 +589,17 @@ def run_stack(args, rank, world, local):
     ms_per_step = elapsed_max / args.steps
     by = bytes_of(T_line, nu)
     achieved = by / (ms_per_step * 1e-3) / 1e9
+    path_prefill = mode == moe.MOE_MODE_PREFILL or (mode == moe.MOE_MODE_AUTO and T_line >= 128)
     small = T_line <= 8 and T_line * k <= 64
-    per_layer = 1 + (5 if small else 7)    # RMS norm + the fused layer's kernels
+    per_layer = 1 + (8 if path_prefill else 5 if small else 7)    # RMS norm + the fused layer's kernels
     line = {
         "metric": METRIC, "value": round(job_throughput(T_line, args.steps, world, elapsed_max), 2), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"stack: {NL} resident MoE layers (out = x + MoE(RMSNorm(x))), E={E} routed + 1 "
                                f"shared, k={k}, d={d}, f={f}, int4 group-{G} fp32 scales, Zipf(1.1) selection "
-                               f"bias with a per-layer expert permutation, T={T_line} token(s) per step",
+                               f"bias with a per-layer expert permutation, T={T_line} token(s) per step, "
+                               f"FFN path {args.mode if args.mode != 'workload' else 'automatic'}",
                    "T": T_line, "E": E, "k": k, "d": d, "f": f, "G": G, "layers": NL, "weights": "int4",
                    "l2": f"inputs larger than L2: {NL} resident layers ({NL * (E + 1) * blk / 1e9:.1f} GB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "cuda_graph_steps": S},

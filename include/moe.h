@@ -76,7 +76,7 @@ enum {
 
 /* FFN execution modes. */
 enum {
-    MOE_MODE_AUTO = 0,     /* decode path when T < 1024, else prefill */
+    MOE_MODE_AUTO = 0,     /* decode path when T < 128, else prefill */
     MOE_MODE_DECODE = 1,   /* fp32-accurate grouped GEMV: exact int4 against activations split
                               into fp16 hi + lo parts, fp32 accumulation */
     MOE_MODE_PREFILL = 2   /* tcgen05 grouped GEMM on 16-bit operands (fp16 q*s weights, fp16

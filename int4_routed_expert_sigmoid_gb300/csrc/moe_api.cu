@@ -37,7 +37,7 @@ int check_layer(const moe_layer_int4 *w)
 int resolve_mode(int mode, int T)
 {
     if (mode == MOE_MODE_AUTO)
-        return T < 1024 ? MOE_MODE_DECODE : MOE_MODE_PREFILL;
+        return T < 128 ? MOE_MODE_DECODE : MOE_MODE_PREFILL;   // measured crossover of the two FFN paths
     return mode;
 }
 

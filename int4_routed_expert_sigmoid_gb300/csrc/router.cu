@@ -132,7 +132,7 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
 // 64 x 64 tile per CTA, 256 threads x (4 x 4), k-slabs of 16 staged in shared
 // memory (transposed so both operands are read as float4 broadcasts).
 constexpr int kBM = 64, kBN = 64, kBK = 16;
-constexpr int kTcMinTokens = 512;   // from here on the tensor-core kernel below is used
+constexpr int kTcMinTokens = 128;   // from here on the tensor-core kernel below is used
 
 __global__ void __launch_bounds__(256)
 logits_tiled_kernel(const float *__restrict__ x, const float *__restrict__ wg, int T, int d, int E,

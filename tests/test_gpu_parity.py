@@ -47,7 +47,8 @@ def test_layer_parity_small(shape, normalize, route_scale, with_res):
 
     # 1) the layer as the GPU routes it
     hits = torch.zeros(shape.E, dtype=torch.int64, device="cuda")
-    r = run_steps(dev, k, normalize=normalize, route_scale=route_scale, res=res_d, hits=hits)
+    dec = m.MOE_MODE_DECODE   # this test holds the decode path to its tolerance at every T
+    r = run_steps(dev, k, normalize=normalize, route_scale=route_scale, res=res_d, hits=hits, mode=dec)
     assert r["err"] == 0
     assert np.max(np.abs(r["logits"] - o_logits)) <= 1e-5 * max(1.0, float(np.abs(o_logits).max()))
     same, flagged = compare_routing(r["idx"], r["w"], o_idx, o_w, keys, k)
@@ -58,7 +59,7 @@ def test_layer_parity_small(shape, normalize, route_scale, with_res):
     assert rel_max_err(r["out"][same], o_out[same]) <= TOL_DECODE
 
     # 2) teacher-forced: downstream stages on the oracle's routing, all tokens
-    t = run_steps(dev, k, res=res_d, teacher_idx=o_idx, teacher_w=o_w)
+    t = run_steps(dev, k, res=res_d, teacher_idx=o_idx, teacher_w=o_w, mode=dec)
     assert t["err"] == 0
     check_union_equal(t, o_union, shape.E)
     assert rel_max_err(t["out"], o_out) <= TOL_DECODE
@@ -72,7 +73,7 @@ def test_layer_parity_small(shape, normalize, route_scale, with_res):
 
     # 3) the fused entry point gives the same bits as the separate calls
     out_f, err_f = m.moe_layer_forward(dev["x"], dev["wg"], dev["bias"], dev["layer"], k, normalize, route_scale,
-                                       residual=res_d)
+                                       mode=dec, residual=res_d)
     torch.cuda.synchronize()
     assert int(host(err_f)[0]) == 0
     assert np.array_equal(host(out_f), r["out"])
@@ -183,6 +184,11 @@ def test_prefill_ffn_parity(shape):
     r = run_steps(dev, k)
     same = (r["idx"] == o_idx).all(axis=1)
     assert rel_max_err(host(out_f)[same], o_out[same]) <= TOL_PREFILL
+    # the automatic mode takes the prefill path from 128 tokens on, the decode path below
+    out_a, _ = m.moe_layer_forward(dev["x"], dev["wg"], dev["bias"], dev["layer"], k)
+    want = out_f if shape.T >= 128 else m.moe_layer_forward(dev["x"], dev["wg"], dev["bias"], dev["layer"], k,
+                                                            mode=m.MOE_MODE_DECODE)[0]
+    assert np.array_equal(host(out_a), host(want))
 
 
 @pytest.mark.parametrize("T,d,scale", [(1, 256, 1.0), (37, 1024, 1e-3), (5, 6144, 3e4)])
