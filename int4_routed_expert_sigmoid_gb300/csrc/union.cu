@@ -58,13 +58,12 @@ __device__ int block_exclusive_scan(int v, int *warp_sums, int *total)
     return r;
 }
 
-__global__ void __launch_bounds__(kThreads)
-union_kernel(const int32_t *__restrict__ idx, int P, int E, int32_t *__restrict__ counts,
-             int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
-             int32_t *__restrict__ sorted_pair, int32_t *__restrict__ uniq,
-             int32_t *__restrict__ n_uniq, uint64_t *__restrict__ hits, int32_t *__restrict__ err)
+__device__ void union_chunked(const int32_t *__restrict__ idx, int P, int E, int32_t *__restrict__ counts,
+                              int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
+                              int32_t *__restrict__ sorted_pair, int32_t *__restrict__ uniq,
+                              int32_t *__restrict__ n_uniq, uint64_t *__restrict__ hits, int32_t *__restrict__ err,
+                              int *dyn)
 {
-    extern __shared__ int dyn[];
     int *cnt = dyn;                 // [E] pairs per expert
     int *base = dyn + E;            // [E] next free position per expert
     unsigned short *wcnt = reinterpret_cast<unsigned short *>(dyn + 2 * E);   // [kWarps][E]
@@ -164,6 +163,125 @@ size_t union_smem_bytes(int E)
     return (size_t)E * 2 * sizeof(int) + (size_t)kWarps * E * sizeof(unsigned short);
 }
 
+// Bitmap union for batches whose (expert x token) bitmap fits in shared memory.
+// The top-k gives every token distinct experts, so the pairs of expert e are
+// the set bits of row e of a bitmap over tokens, and a pair's rank inside its
+// expert's group is the number of set bits before its token: a per-word prefix
+// of bit counts plus one masked popcount.  Every step is one pass over the
+// pairs or the bitmap, all threads in parallel.  A token that names an expert
+// twice (not a top-k result, but a caller may pass any ids) sends the whole
+// call to the chunked algorithm above, which ranks pairs by position.
+__host__ __device__ constexpr size_t union_bitmap_smem_bytes(int E, int T)
+{
+    return (size_t)E * ((T + 31) / 32) * (4 + 2) + (size_t)E * 4 + 16;
+}
+constexpr size_t kBitmapSmemMax = 200 * 1024;
+
+__global__ void __launch_bounds__(kThreads)
+union_kernel(const int32_t *__restrict__ idx, int T, int k, int E, int use_bitmap, int32_t *__restrict__ counts,
+             int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
+             int32_t *__restrict__ sorted_pair, int32_t *__restrict__ uniq,
+             int32_t *__restrict__ n_uniq, uint64_t *__restrict__ hits, int32_t *__restrict__ err)
+{
+    extern __shared__ int dyn[];
+    __shared__ int warp_sums[32];
+    __shared__ int total;
+    const int P = T * k;
+    if (!use_bitmap) {
+        union_chunked(idx, P, E, counts, offsets, perm, sorted_pair, uniq, n_uniq, hits, err, dyn);
+        return;
+    }
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int W = (T + 31) / 32;                                      // bitmap words per expert
+    uint32_t *bits = reinterpret_cast<uint32_t *>(dyn);                 // [E][W]
+    int *base = dyn + (size_t)E * W;                                    // [E] first position of the expert
+    unsigned short *pre = reinterpret_cast<unsigned short *>(base + E); // [E][W] set bits before the word
+    for (int i = tid; i < E * W; i += kThreads)
+        bits[i] = 0u;
+    __syncthreads();
+    int bad = 0, dup = 0;
+    for (int p = tid; p < P; p += kThreads) {
+        const int e = idx[p];
+        if (e < 0 || e >= E) {
+            bad = 1;
+            continue;
+        }
+        const int t = p / k;
+        const uint32_t b = 1u << (t & 31);
+        if (atomicOr(&bits[e * W + (t >> 5)], b) & b)
+            dup = 1;
+    }
+    bad = __syncthreads_or(bad);
+    if (__syncthreads_or(dup)) {   // the same expert twice in one token: rank by position instead
+        union_chunked(idx, P, E, counts, offsets, perm, sorted_pair, uniq, n_uniq, hits, err, dyn);
+        return;
+    }
+    if (bad && tid == 0)
+        atomicOr(err, MOE_DEVERR_BAD_EXPERT);
+    // per expert (one warp each): prefix of bit counts over the words; lane l takes words
+    // l * q .. l * q + q - 1
+    const int q = (W + 31) / 32;
+    for (int e = warp; e < E; e += kWarps) {
+        const uint32_t *row = bits + (size_t)e * W;
+        int mine = 0;
+        for (int w = lane * q; w < min(W, lane * q + q); w++)
+            mine += __popc(row[w]);
+        int inc = mine;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off)
+                inc += v;
+        }
+        int run = inc - mine;
+        for (int w = lane * q; w < min(W, lane * q + q); w++) {
+            pre[(size_t)e * W + w] = (unsigned short)run;
+            run += __popc(row[w]);
+        }
+        if (lane == 31)
+            base[e] = inc;   // the expert's count, turned into its first position below
+    }
+    __syncthreads();
+    // offsets (exclusive scan over ascending expert id), counts, hits, uniq
+    int carry = 0, ucarry = 0;
+    for (int e0 = 0; e0 < E; e0 += kThreads) {
+        const int e = e0 + tid;
+        const int c = e < E ? base[e] : 0;
+        const int ex = block_exclusive_scan(c, warp_sums, &total) + carry;
+        const int add = total;
+        const int flag = c > 0 ? 1 : 0;
+        const int ux = block_exclusive_scan(flag, warp_sums, &total) + ucarry;
+        if (e < E) {
+            base[e] = ex;
+            offsets[e] = ex;
+            counts[e] = c;
+            if (hits)
+                hits[e] += (uint64_t)c;
+            if (flag)
+                uniq[ux] = e;
+        }
+        carry += add;
+        ucarry += total;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        offsets[E] = carry;
+        *n_uniq = ucarry;
+    }
+    // placement: rank = set bits of the expert's row before the token
+    for (int p = tid; p < P; p += kThreads) {
+        const int e = idx[p];
+        int pos = -1;
+        if (e >= 0 && e < E) {
+            const int t = p / k, w = t >> 5;
+            const uint32_t below = bits[(size_t)e * W + w] & ((1u << (t & 31)) - 1u);
+            pos = base[e] + pre[(size_t)e * W + w] + __popc(below);
+            sorted_pair[pos] = p;
+        }
+        perm[p] = pos;
+    }
+}
+
 // ------------------------------------------------- small-batch select+union
 // One block of 256 threads for batches of at most 8 tokens and 64 pairs:
 // warp t selects token t's experts (the same top-k as topk_kernel), then the
@@ -255,17 +373,22 @@ int launch_union(const int32_t *idx, int T, int k, int E, int32_t *counts, int32
                  int32_t *perm, int32_t *sorted_pair, int32_t *uniq, int32_t *n_uniq,
                  uint64_t *hits, int32_t *err, cudaStream_t s)
 {
-    const size_t smem = union_smem_bytes(E);
+    const size_t bm = union_bitmap_smem_bytes(E, T);
+    // one chunk of the chunked path is cheaper than the bitmap's passes; beyond that the bitmap wins
+    const int use_bitmap = (bm <= kBitmapSmemMax && T * k > kThreads) ? 1 : 0;
+    const size_t chunked = union_smem_bytes(E);
+    const size_t smem = use_bitmap && bm > chunked ? bm : chunked;   // the bitmap path may fall back
     static thread_local int configured_for = -1;   // per host thread, per device attribute set once
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {
-        if (cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)union_smem_bytes(kMaxE)) != cudaSuccess)
+        const size_t most = kBitmapSmemMax > union_smem_bytes(kMaxE) ? kBitmapSmemMax : union_smem_bytes(kMaxE);
+        if (cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most) !=
+            cudaSuccess)
             return MOE_ERR_CUDA;
         configured_for = dev;
     }
-    union_kernel<<<1, kThreads, smem, s>>>(idx, T * k, E, counts, offsets, perm, sorted_pair, uniq,
+    union_kernel<<<1, kThreads, smem, s>>>(idx, T, k, E, use_bitmap, counts, offsets, perm, sorted_pair, uniq,
                                         n_uniq, hits, err);
     return cuda_status(cudaGetLastError());
 }

@@ -232,3 +232,34 @@ def test_route_tensor_core_logits(T, E, d, bias, xs):
     assert np.isfinite(lg).all()
     assert np.max(np.abs(lg - o_logits)) <= 1e-5 * max(1.0, float(np.abs(o_logits).max()))
     compare_routing(host(idx), host(w), o_idx, o_w, keys, k)
+
+
+UNION_CASES = [
+    # (T, k, E, duplicates): more than 1024 pairs with distinct experts per token take the bitmap
+    # path (sizes up to the prefill batch), fewer the chunked path; an expert named twice by one
+    # token sends a bitmap call to the chunked path; a bitmap too large for shared memory
+    # (E = 1024, T = 2048) takes the chunked path directly
+    (1, 8, 256, False), (37, 4, 16, False), (4096, 8, 256, False), (300, 8, 1024, False),
+    (2048, 8, 1024, False), (64, 8, 256, True), (5000, 2, 8, True), (700, 8, 64, True),
+]
+
+
+@pytest.mark.parametrize("T,k,E,dups", UNION_CASES, ids=lambda v: str(v))
+def test_union_paths_bit_exact(T, k, E, dups):
+    """The union kernel's paths against the oracle's stable counting sort, bit for bit."""
+    m = moe()
+    rng = np.random.default_rng(T * 7 + E)
+    if dups:
+        idx = rng.integers(0, E, size=(T, k)).astype(np.int32)
+        idx[:, 1] = idx[:, 0]   # every token names its first expert twice
+    else:
+        idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    hits = torch.zeros(E, dtype=torch.int64, device="cuda")
+    un = m.moe_union(torch.from_numpy(idx).cuda(), E, hits=hits)
+    torch.cuda.synchronize()
+    r = {key: host(v) for key, v in un.items()}
+    r["n_uniq"] = int(r["n_uniq"][0])
+    assert int(r["err"][0]) == 0
+    o = oracle.union(idx, E)
+    check_union_equal(r, o, E)
+    assert np.array_equal(host(hits), o["counts"].astype(np.int64))
