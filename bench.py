@@ -261,8 +261,8 @@ def run_ours(args, rank, world, local):
 
     # kernels per fused step: small batches logits(+x fragments), select+union, gate/up, down,
     # combine; otherwise logits, top-k, union, x fragments, gate/up, down, combine
-    if prefill:   # logits, top-k, union, gather, gate/up, h conversion, down, combine
-        launches_per_step = 8
+    if prefill:   # logits, top-k, union, token rows, row copies, gate/up, h conversion, down, combine
+        launches_per_step = 9
     else:
         launches_per_step = 5 if (T <= 8 and T * k <= 64) else 7
 
@@ -363,7 +363,7 @@ def run_ours(args, rank, world, local):
         # dense work of the grouped GEMMs: 3 matrices of d x f per (token, expert) pair, 2 flops per MAC
         flops = 6.0 * d * f * (T * k + T)
         achieved = flops / (ffn_ms * 1e-3) / 1e12
-        roof = {"kernel": "expert FFN stage (gather, tcgen05 gate/up, h conversion, tcgen05 down)",
+        roof = {"kernel": "expert FFN stage (token rows + row copies, tcgen05 gate/up, h conversion, tcgen05 down)",
                 "bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": ncu_traffic(ROOT, "ffn_prefill"),
                 "peak_source": peaks["source"] + " bf16 dense (fp16 operands run at the same tensor rate)",
@@ -591,7 +591,7 @@ def run_stack(args, rank, world, local):
     achieved = by / (ms_per_step * 1e-3) / 1e9
     path_prefill = mode == moe.MOE_MODE_PREFILL or (mode == moe.MOE_MODE_AUTO and T_line >= 128)
     small = T_line <= 8 and T_line * k <= 64
-    per_layer = 1 + (8 if path_prefill else 5 if small else 7)    # RMS norm + the fused layer's kernels
+    per_layer = 1 + (9 if path_prefill else 5 if small else 7)    # RMS norm + the fused layer's kernels
     line = {
         "metric": METRIC, "value": round(job_throughput(T_line, args.steps, world, elapsed_max), 2), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),

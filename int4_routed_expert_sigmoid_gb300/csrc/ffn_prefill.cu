@@ -587,16 +587,18 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
 // Token rows in expert order as fp16, permuted within each 8 like the weights
 // and scaled per row by a power of two 2^(14-e) (|value| < 2^14; row_scale
 // keeps 2^(e-14)): row p < T*k is x[sorted_pair[p] / k], row T*k + t is x[t].
-// One block of 256 threads per row.
+// Two kernels: token_rows_kernel converts each token once into row T*k + t
+// (one block of 256 threads per token), copy_rows_kernel then copies those
+// rows into the pair rows (the converted rows are L2-resident).
 __global__ void __launch_bounds__(256)
-gather_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ sorted_pair, int T, int k, int K,
-                   uint16_t *__restrict__ out, float *__restrict__ row_scale)
+token_rows_kernel(const float *__restrict__ x, int T, int k, int K, uint16_t *__restrict__ out,
+                  float *__restrict__ row_scale)
 {
     __shared__ float wmax[8];
     griddep_launch_dependents();
     griddep_wait();
-    const int r = blockIdx.x;
-    const int src = r < T * k ? sorted_pair[r] / k : r - T * k;
+    const int src = blockIdx.x;
+    const int r = T * k + src;
     const float *xr = x + (size_t)src * K;
     float mx = 0.f;
     for (int i = threadIdx.x; i < K / 4; i += 256) {
@@ -627,6 +629,31 @@ gather_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ sort
         for (int el = 0; el < 8; el++)
             o[frag_pos8(el)] = __half_as_ushort(__float2half_rn(v[el] * up));
         *reinterpret_cast<uint4 *>(out + (size_t)r * K + c * 8) = *reinterpret_cast<const uint4 *>(o);
+    }
+}
+
+// Pair row p < T*k <- token row T*k + sorted_pair[p] / k, with its factor.  Each
+// block copies kCopyRows rows, 16 bytes per thread and step.
+constexpr int kCopyRows = 4;
+__global__ void __launch_bounds__(256)
+copy_rows_kernel(const int32_t *__restrict__ sorted_pair, int T, int k, int K, uint16_t *__restrict__ out,
+                 float *__restrict__ row_scale)
+{
+    griddep_launch_dependents();
+    griddep_wait();
+    const int P = T * k;
+    const int n16 = K / 8;   // 16-byte units per row
+    for (int j = 0; j < kCopyRows; j++) {
+        const int r = blockIdx.x * kCopyRows + j;
+        if (r >= P)
+            break;
+        const int src = P + sorted_pair[r] / k;
+        const uint4 *from = reinterpret_cast<const uint4 *>(out + (size_t)src * K);
+        uint4 *to = reinterpret_cast<uint4 *>(out + (size_t)r * K);
+        for (int i = threadIdx.x; i < n16; i += 256)
+            to[i] = from[i];
+        if (threadIdx.x == 0)
+            row_scale[r] = row_scale[src];
     }
 }
 
@@ -749,8 +776,11 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     float *row_scale = ps.x_scale;
     int rc = MOE_OK;
 
-    // gathered fp16 token rows
-    rc = launch_pdl(gather_rows_kernel, (int)rows, 256, 0, s, a.x, a.sorted_pair, T, k, d, x_sorted, row_scale);
+    // fp16 token rows: each token once, then copied into the pair rows
+    rc = launch_pdl(token_rows_kernel, T, 256, 0, s, a.x, T, k, d, x_sorted, row_scale);
+    if (rc == MOE_OK)
+        rc = launch_pdl(copy_rows_kernel, (T * k + kCopyRows - 1) / kCopyRows, 256, 0, s,
+                        (const int32_t *)a.sorted_pair, T, k, d, x_sorted, row_scale);
     if (rc != MOE_OK)
         return rc;
 
