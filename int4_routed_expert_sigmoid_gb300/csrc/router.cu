@@ -193,31 +193,39 @@ logits_tiled_kernel(const float *__restrict__ x, const float *__restrict__ wg, i
 // fp32 registers, rounding to nearest, while the MMAs of the next run go to
 // the other accumulator.
 // CTA = 128 tokens x 64 experts; 32 reduction elements per stage (one 128-byte
-// swizzled row of fp32 per token/expert).  Warp 0: TMA producer; warp 1: MMA
-// issue (whole warp, one elected lane) and tensor-memory owner; warps 2-5:
-// split each stage in place (hi over the loaded values, lo beside them);
-// warps 6-9: drain the partials (one TMEM subpartition each) and write the
-// logits.  Waits are bounded; a CTA that timed out writes NaN logits (the
-// routing call has no error word).
-constexpr int kRM = 128, kRN = 64, kRK = 32, kRStages = 4, kRThreads = 320, kRChunk = 2;
+// swizzled row of fp32 per token/expert).  Two rings: the raw ring takes the
+// TMA loads (fp32 x and w), the operand ring the split values (x hi, w hi,
+// x lo, w lo in the same swizzled layout); a raw stage is free again as soon
+// as the split warps hold it in registers, so the loads run ahead of the MMAs
+// by the whole raw ring.  Warp 0: TMA producer; warp 1: MMA issue (whole
+// warp, one elected lane) and tensor-memory owner; warps 2-5: split; warps
+// 6-9: drain the partials (one TMEM subpartition each) and write the logits.
+// Waits are bounded; a CTA that timed out writes NaN logits (the routing call
+// has no error word).
+constexpr int kRM = 128, kRN = 64, kRK = 32, kRThreads = 320, kRChunk = 2;
+constexpr int kRRaw = 4, kROps = 2;                           // raw and operand stages
 constexpr int kRXB = kRM * kRK * 4, kRWB = kRN * kRK * 4;   // 16 KB, 8 KB
-constexpr int kRStage = 2 * (kRXB + kRWB);                    // x hi, w hi, x lo, w lo
-constexpr size_t kRSmem = 1024 + (size_t)kRStages * kRStage;
+constexpr int kRRawStage = kRXB + kRWB;                       // x, w
+constexpr int kROpStage = 2 * (kRXB + kRWB);                  // x hi, w hi, x lo, w lo
+constexpr size_t kRSmem = 1024 + (size_t)kRRaw * kRRawStage + (size_t)kROps * kROpStage;
 
 __global__ void __launch_bounds__(kRThreads, 1)
 logits_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mw, int T, int d,
                  int E, float *__restrict__ logits)
 {
     extern __shared__ uint8_t dyn_smem[];
-    __shared__ __align__(8) uint64_t full[kRStages], conv[kRStages], empty[kRStages], accf[2], acce[2];
+    __shared__ __align__(8) uint64_t full[kRRaw], rfree[kRRaw], conv[kROps], empty[kROps], accf[2], acce[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
     const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
     uint8_t *gbase = dyn_smem + (base - smem_addr(dyn_smem));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kRStages; s++) {
+        for (int s = 0; s < kRRaw; s++) {
             mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&rfree[s]), 128);
+        }
+        for (int s = 0; s < kROps; s++) {
             mbar_init(smem_addr(&conv[s]), 128);
             mbar_init(smem_addr(&empty[s]), 1);
         }
@@ -239,16 +247,17 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     const int m0 = blockIdx.y * kRM, n0 = blockIdx.x * kRN;
     const int nk = d / kRK;
     const int nchunk = (nk + kRChunk - 1) / kRChunk;
+    const uint32_t opbase = base + kRRaw * kRRawStage;
 
     if (warp == 0) {
         if (lane == 0) {
             for (int kb = 0; kb < nk; kb++) {
-                const int s = kb % kRStages;
-                const uint32_t ph = (uint32_t)(kb / kRStages) & 1u;
-                if (!abort_flag && !mbar_wait(smem_addr(&empty[s]), ph ^ 1u))
+                const int s = kb % kRRaw;
+                const uint32_t ph = (uint32_t)(kb / kRRaw) & 1u;
+                if (!abort_flag && !mbar_wait(smem_addr(&rfree[s]), ph ^ 1u))
                     abort_flag = 1;
                 if (!abort_flag) {
-                    const uint32_t sb = base + s * kRStage;
+                    const uint32_t sb = base + s * kRRawStage;
                     mbar_arrive_expect_tx(smem_addr(&full[s]), kRXB + kRWB);
                     tma_load_2d(sb, &mx, kb * kRK, m0, smem_addr(&full[s]));
                     tma_load_2d(sb + kRXB, &mw, kb * kRK, n0, smem_addr(&full[s]));
@@ -270,8 +279,8 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
             const uint32_t dcol = tmem + b * kRN;
             const int kb1 = min(nk, (ch + 1) * kRChunk);
             for (int kb = ch * kRChunk; kb < kb1; kb++) {
-                const int s = kb % kRStages;
-                const uint32_t ph = (uint32_t)(kb / kRStages) & 1u;
+                const int s = kb % kROps;
+                const uint32_t ph = (uint32_t)(kb / kROps) & 1u;
                 ok = 1;
                 if (lane == 0)
                     ok = (!abort_flag && mbar_wait_or_abort(smem_addr(&conv[s]), ph, &abort_flag)) ? 1 : 0;
@@ -279,7 +288,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                 if (!ok && lane == 0)
                     abort_flag = 1;
                 tc_fence_after();
-                const uint32_t sb = base + s * kRStage;
+                const uint32_t sb = opbase + s * kROpStage;
                 const uint64_t xh = smem_desc_sw128(sb), wh = smem_desc_sw128(sb + kRXB);
                 const uint64_t xl = smem_desc_sw128(sb + kRXB + kRWB), wl = smem_desc_sw128(sb + 2 * kRXB + kRWB);
 #pragma unroll
@@ -293,28 +302,39 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
             umma_commit_elect(smem_addr(&accf[b]));
         }
     } else if (warp < 6) {
-        // split: hi in place, lo at the same offset in the lo half of the stage
+        // split: the raw stage into registers (then free for the next load), hi and lo into the
+        // operand stage at the same offsets (the swizzle is a property of the offset)
+        constexpr int kV = kRRawStage / 16 / 128;   // float4 per thread per stage
         const int c = threadIdx.x - 64;   // 0 .. 127
         for (int kb = 0; kb < nk; kb++) {
-            const int s = kb % kRStages;
-            const uint32_t ph = (uint32_t)(kb / kRStages) & 1u;
+            const int s = kb % kRRaw;
+            const uint32_t ph = (uint32_t)(kb / kRRaw) & 1u;
             if (!abort_flag && !mbar_wait(smem_addr(&full[s]), ph))
                 abort_flag = 1;
-            float4 *hi = reinterpret_cast<float4 *>(gbase + s * kRStage);
-            float4 *lo = reinterpret_cast<float4 *>(gbase + s * kRStage + kRXB + kRWB);
-#pragma unroll 4
-            for (int i = c; i < (kRXB + kRWB) / 16; i += 128) {
-                const float4 v = hi[i];
+            const float4 *raw = reinterpret_cast<const float4 *>(gbase + s * kRRawStage);
+            float4 v[kV];
+#pragma unroll
+            for (int q = 0; q < kV; q++)
+                v[q] = raw[c + 128 * q];
+            mbar_arrive(smem_addr(&rfree[s]));
+            const int os = kb % kROps;
+            const uint32_t oph = (uint32_t)(kb / kROps) & 1u;
+            if (!abort_flag && !mbar_wait(smem_addr(&empty[os]), oph ^ 1u))
+                abort_flag = 1;
+            float4 *hi = reinterpret_cast<float4 *>(gbase + kRRaw * kRRawStage + os * kROpStage);
+            float4 *lo = hi + kRRawStage / 16;
+#pragma unroll
+            for (int q = 0; q < kV; q++) {
                 float4 h, l;
-                h.x = to_tf32(v.x); l.x = to_tf32(v.x - h.x);
-                h.y = to_tf32(v.y); l.y = to_tf32(v.y - h.y);
-                h.z = to_tf32(v.z); l.z = to_tf32(v.z - h.z);
-                h.w = to_tf32(v.w); l.w = to_tf32(v.w - h.w);
-                hi[i] = h;
-                lo[i] = l;
+                h.x = to_tf32(v[q].x); l.x = to_tf32(v[q].x - h.x);
+                h.y = to_tf32(v[q].y); l.y = to_tf32(v[q].y - h.y);
+                h.z = to_tf32(v[q].z); l.z = to_tf32(v[q].z - h.z);
+                h.w = to_tf32(v[q].w); l.w = to_tf32(v[q].w - h.w);
+                hi[c + 128 * q] = h;
+                lo[c + 128 * q] = l;
             }
             fence_proxy_async_smem();   // generic-proxy writes, read next by the tensor cores
-            mbar_arrive(smem_addr(&conv[s]));
+            mbar_arrive(smem_addr(&conv[os]));
         }
     } else {
         // drain: TMEM lane = token row of the tile, columns = experts
