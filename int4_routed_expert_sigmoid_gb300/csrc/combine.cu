@@ -10,9 +10,19 @@
 namespace moe {
 namespace {
 
-// One thread per 4 consecutive columns of one token.
+__device__ __forceinline__ float4 load4(const float4 *p, size_t i) { return p[i]; }
+__device__ __forceinline__ float4 load4(const uint2 *p, size_t i)   // 4 bf16
+{
+    const uint2 u = p[i];
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xFFFF0000u));
+}
+
+// One thread per 4 consecutive columns of one token.  Y: float4 (fp32 y_pair)
+// or uint2 (four bf16).
+template <typename Y>
 __global__ void __launch_bounds__(256)
-combine_kernel(const float4 *__restrict__ y_pair, const float4 *__restrict__ y_shared,
+combine_kernel(const Y *__restrict__ y_pair, const float4 *__restrict__ y_shared,
                const float *__restrict__ w, const int32_t *__restrict__ perm,
                const float4 *res, int T, int k, int d4, float4 *out)
 {
@@ -30,7 +40,7 @@ combine_kernel(const float4 *__restrict__ y_pair, const float4 *__restrict__ y_s
         if (q < 0)
             continue;
         const float wj = w[(size_t)t * k + j];
-        const float4 y = y_pair[(size_t)q * d4 + c];
+        const float4 y = load4(y_pair, (size_t)q * d4 + c);
         acc.x = fmaf(wj, y.x, acc.x);
         acc.y = fmaf(wj, y.y, acc.y);
         acc.z = fmaf(wj, y.z, acc.z);
@@ -93,8 +103,18 @@ int launch_combine(const float *y_pair, const float *y_shared, const float *w, c
 {
     const int d4 = d / 4;
     const long long n = (long long)T * d4;
-    return launch_pdl(combine_kernel, (int)((n + 255) / 256), 256, 0, s,
+    return launch_pdl(combine_kernel<float4>, (int)((n + 255) / 256), 256, 0, s,
                       reinterpret_cast<const float4 *>(y_pair), reinterpret_cast<const float4 *>(y_shared), w,
+                      perm, reinterpret_cast<const float4 *>(res), T, k, d4, reinterpret_cast<float4 *>(out));
+}
+
+int launch_combine_bf16(const uint16_t *y_pair, const float *y_shared, const float *w, const int32_t *perm,
+                        const float *res, int T, int k, int d, float *out, cudaStream_t s)
+{
+    const int d4 = d / 4;
+    const long long n = (long long)T * d4;
+    return launch_pdl(combine_kernel<uint2>, (int)((n + 255) / 256), 256, 0, s,
+                      reinterpret_cast<const uint2 *>(y_pair), reinterpret_cast<const float4 *>(y_shared), w,
                       perm, reinterpret_cast<const float4 *>(res), T, k, d4, reinterpret_cast<float4 *>(out));
 }
 

@@ -123,6 +123,7 @@ struct PParams {
     const float *row_scale;       // power-of-two factor of each sorted activation row (x or h)
     float *h32;                   // gate/up: h [rows][f] fp32, natural order
     float *y_pair, *y_shared;     // down outputs
+    uint16_t *y_pair16;           // down: routed outputs as bf16 instead of y_pair, when set
     int32_t *err;
     int T, k, K, mtiles, out_rows;
 };
@@ -560,9 +561,14 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                         if (jj >= nj)
                             break;
                         const int tok = it.tok0 + c0 + jj;
-                        float *dst = it.expert < 0 ? p.y_shared + (size_t)tok * p.out_rows
-                                                   : p.y_pair + (size_t)(it.row0 + tok) * p.out_rows;
-                        dst[orow] = __uint_as_float(v[jj]) * rf;
+                        const float yv = __uint_as_float(v[jj]) * rf;
+                        if (it.expert < 0)
+                            p.y_shared[(size_t)tok * p.out_rows + orow] = yv;
+                        else if (p.y_pair16)
+                            p.y_pair16[(size_t)(it.row0 + tok) * p.out_rows + orow] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(yv));
+                        else
+                            p.y_pair[(size_t)(it.row0 + tok) * p.out_rows + orow] = yv;
                     }
                 }
             }
@@ -842,6 +848,7 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pd.h32 = nullptr;
     pd.row_scale = ps.h_scale;
     pd.y_pair = a.y_pair;
+    pd.y_pair16 = a.y_pair16;
     pd.y_shared = a.y_shared;
     pd.K = f;
     pd.mtiles = d / kTileM;

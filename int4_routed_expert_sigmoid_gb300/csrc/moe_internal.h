@@ -114,6 +114,7 @@ struct PrefillFfnArgs {
     int T, k;
     void *scratch;                       // prefill_scratch_bytes(T, k, d, f) bytes, 256-aligned
     float *y_pair, *y_shared;
+    uint16_t *y_pair16;                  // when set: routed outputs as bf16 here instead of y_pair (fp32)
     int32_t *err;
 };
 size_t prefill_scratch_bytes(int T, int k, int d, int f);
@@ -122,6 +123,9 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s);
 // combine.cu
 int launch_combine(const float *y_pair, const float *y_shared, const float *w, const int32_t *perm,
                    const float *res, int T, int k, int d, float *out, cudaStream_t s);
+// the same with the routed outputs in bf16
+int launch_combine_bf16(const uint16_t *y_pair, const float *y_shared, const float *w, const int32_t *perm,
+                        const float *res, int T, int k, int d, float *out, cudaStream_t s);
 int launch_rms_norm(const float *x, int T, int d, float eps, float *out, cudaStream_t s);
 
 // tmap.cu
