@@ -261,7 +261,7 @@ def run_ours(args, rank, world, local):
 
     # kernels per fused step: small batches logits(+x fragments), select+union, gate/up, down,
     # combine; otherwise logits, top-k, union, x fragments, gate/up, down, combine
-    if prefill:   # logits, top-k, union, token rows, row copies, gate/up, h conversion, down, combine
+    if prefill:   # logits, top-k, union, pair positions, token rows, gate/up, h conversion, down, combine
         launches_per_step = 9
     else:
         launches_per_step = 5 if (T <= 8 and T * k <= 64) else 7
@@ -363,7 +363,7 @@ def run_ours(args, rank, world, local):
         # dense work of the grouped GEMMs: 3 matrices of d x f per (token, expert) pair, 2 flops per MAC
         flops = 6.0 * d * f * (T * k + T)
         achieved = flops / (ffn_ms * 1e-3) / 1e12
-        roof = {"kernel": "expert FFN stage (token rows + row copies, tcgen05 gate/up, h conversion, tcgen05 down)",
+        roof = {"kernel": "expert FFN stage (pair positions + token rows, tcgen05 gate/up, h conversion, tcgen05 down)",
                 "bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": ncu_traffic(ROOT, "ffn_prefill"),
                 "peak_source": peaks["source"] + " bf16 dense (fp16 operands run at the same tensor rate)",

@@ -593,19 +593,31 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
 // Token rows in expert order as fp16, permuted within each 8 like the weights
 // and scaled per row by a power of two 2^(14-e) (|value| < 2^14; row_scale
 // keeps 2^(e-14)): row p < T*k is x[sorted_pair[p] / k], row T*k + t is x[t].
-// Two kernels: token_rows_kernel converts each token once into row T*k + t
-// (one block of 256 threads per token), copy_rows_kernel then copies those
-// rows into the pair rows (the converted rows are L2-resident).
+// pair_pos_kernel inverts sorted_pair (pos[q] = p for q = sorted_pair[p]);
+// token_rows_kernel then converts each token once (one block of 256 threads)
+// and writes the result to the token's k pair rows and its shared-expert row.
 __global__ void __launch_bounds__(256)
-token_rows_kernel(const float *__restrict__ x, int T, int k, int K, uint16_t *__restrict__ out,
-                  float *__restrict__ row_scale)
+pair_pos_kernel(const int32_t *__restrict__ sorted_pair, int P, int32_t *__restrict__ pos)
 {
-    __shared__ float wmax[8];
     griddep_launch_dependents();
     griddep_wait();
-    const int src = blockIdx.x;
-    const int r = T * k + src;
-    const float *xr = x + (size_t)src * K;
+    const int p = blockIdx.x * 256 + threadIdx.x;
+    if (p < P)
+        pos[sorted_pair[p]] = p;
+}
+
+__global__ void __launch_bounds__(256)
+token_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ pos, int T, int k, int K,
+                  uint16_t *__restrict__ out, float *__restrict__ row_scale)
+{
+    __shared__ float wmax[8];
+    __shared__ int dst[33];
+    griddep_launch_dependents();
+    griddep_wait();
+    const int t = blockIdx.x;
+    if (threadIdx.x <= k)
+        dst[threadIdx.x] = threadIdx.x < k ? pos[(size_t)t * k + threadIdx.x] : T * k + t;
+    const float *xr = x + (size_t)t * K;
     float mx = 0.f;
     for (int i = threadIdx.x; i < K / 4; i += 256) {
         const float4 v = reinterpret_cast<const float4 *>(xr)[i];
@@ -624,8 +636,8 @@ token_rows_kernel(const float *__restrict__ x, int T, int k, int K, uint16_t *__
     int e = 0;
     frexpf(mx, &e);
     const float up = mx > 0.f ? ldexpf(1.0f, 14 - e) : 1.0f;
-    if (threadIdx.x == 0)
-        row_scale[r] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
+    if (threadIdx.x <= k)
+        row_scale[dst[threadIdx.x]] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
     for (int c = threadIdx.x; c < K / 8; c += 256) {
         const float4 *sp = reinterpret_cast<const float4 *>(xr + c * 8);
         const float4 a = sp[0], b = sp[1];
@@ -634,32 +646,9 @@ token_rows_kernel(const float *__restrict__ x, int T, int k, int K, uint16_t *__
 #pragma unroll
         for (int el = 0; el < 8; el++)
             o[frag_pos8(el)] = __half_as_ushort(__float2half_rn(v[el] * up));
-        *reinterpret_cast<uint4 *>(out + (size_t)r * K + c * 8) = *reinterpret_cast<const uint4 *>(o);
-    }
-}
-
-// Pair row p < T*k <- token row T*k + sorted_pair[p] / k, with its factor.  Each
-// block copies kCopyRows rows, 16 bytes per thread and step.
-constexpr int kCopyRows = 4;
-__global__ void __launch_bounds__(256)
-copy_rows_kernel(const int32_t *__restrict__ sorted_pair, int T, int k, int K, uint16_t *__restrict__ out,
-                 float *__restrict__ row_scale)
-{
-    griddep_launch_dependents();
-    griddep_wait();
-    const int P = T * k;
-    const int n16 = K / 8;   // 16-byte units per row
-    for (int j = 0; j < kCopyRows; j++) {
-        const int r = blockIdx.x * kCopyRows + j;
-        if (r >= P)
-            break;
-        const int src = P + sorted_pair[r] / k;
-        const uint4 *from = reinterpret_cast<const uint4 *>(out + (size_t)src * K);
-        uint4 *to = reinterpret_cast<uint4 *>(out + (size_t)r * K);
-        for (int i = threadIdx.x; i < n16; i += 256)
-            to[i] = from[i];
-        if (threadIdx.x == 0)
-            row_scale[r] = row_scale[src];
+        const uint4 ov = *reinterpret_cast<const uint4 *>(o);
+        for (int j = 0; j <= k; j++)
+            *reinterpret_cast<uint4 *>(out + (size_t)dst[j] * K + c * 8) = ov;
     }
 }
 
@@ -742,6 +731,7 @@ namespace {
 struct PrefillScratch {
     uint16_t *x16, *h16;   // scaled fp16 x and h rows
     float *x_scale, *h_scale, *h32;
+    int32_t *pos;          // pair position of each (token, slot)
 };
 
 size_t prefill_layout(int T, int k, int d, int f, uint8_t *base, PrefillScratch *o)
@@ -759,6 +749,7 @@ size_t prefill_layout(int T, int k, int d, int f, uint8_t *base, PrefillScratch 
     s.h32 = reinterpret_cast<float *>(take(rows * f * 4));
     s.x_scale = reinterpret_cast<float *>(take(rows * 4));
     s.h_scale = reinterpret_cast<float *>(take(rows * 4));
+    s.pos = reinterpret_cast<int32_t *>(take((size_t)T * k * 4));
     if (o)
         *o = s;
     return off;
@@ -782,11 +773,11 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     float *row_scale = ps.x_scale;
     int rc = MOE_OK;
 
-    // fp16 token rows: each token once, then copied into the pair rows
-    rc = launch_pdl(token_rows_kernel, T, 256, 0, s, a.x, T, k, d, x_sorted, row_scale);
+    // fp16 token rows: each token converted once and written to its pair rows and shared row
+    rc = launch_pdl(pair_pos_kernel, (T * k + 255) / 256, 256, 0, s, a.sorted_pair, T * k, ps.pos);
     if (rc == MOE_OK)
-        rc = launch_pdl(copy_rows_kernel, (T * k + kCopyRows - 1) / kCopyRows, 256, 0, s,
-                        (const int32_t *)a.sorted_pair, T, k, d, x_sorted, row_scale);
+        rc = launch_pdl(token_rows_kernel, T, 256, 0, s, a.x, (const int32_t *)ps.pos, T, k, d, x_sorted,
+                        row_scale);
     if (rc != MOE_OK)
         return rc;
 
