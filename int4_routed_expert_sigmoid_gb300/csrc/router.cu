@@ -192,7 +192,10 @@ logits_tiled_kernel(const float *__restrict__ x, const float *__restrict__ wg, i
 // short run of k (kRChunk stages, 24 MMAs); drain warps add the partials in
 // fp32 registers, rounding to nearest, while the MMAs of the next run go to
 // the other accumulator.
-// CTA = 128 tokens x 64 experts; 32 reduction elements per stage (one 128-byte
+// A cluster of two CTAs covers 128 tokens x 128 experts: each CTA one half of
+// the reduction, the second CTA's sums added to the first's through distributed
+// shared memory (in a fixed order: the result does not depend on timing).
+// 32 reduction elements per stage (one 128-byte
 // swizzled row of fp32 per token/expert).  Two rings: the raw ring takes the
 // TMA loads (fp32 x and w), the operand ring the split values (x hi, w hi,
 // x lo, w lo in the same swizzled layout); a raw stage is free again as soon
@@ -202,9 +205,9 @@ logits_tiled_kernel(const float *__restrict__ x, const float *__restrict__ wg, i
 // 6-9: drain the partials (one TMEM subpartition each) and write the logits.
 // Waits are bounded; a CTA that timed out writes NaN logits (the routing call
 // has no error word).
-constexpr int kRM = 128, kRN = 64, kRK = 32, kRThreads = 320, kRChunk = 2;
-constexpr int kRRaw = 4, kROps = 2;                           // raw and operand stages
-constexpr int kRXB = kRM * kRK * 4, kRWB = kRN * kRK * 4;   // 16 KB, 8 KB
+constexpr int kRM = 128, kRN = 128, kRK = 32, kRThreads = 320, kRChunk = 2, kRSplit = 2;
+constexpr int kRRaw = 3, kROps = 2;                           // raw and operand stages
+constexpr int kRXB = kRM * kRK * 4, kRWB = kRN * kRK * 4;   // 16 KB, 16 KB
 constexpr int kRRawStage = kRXB + kRWB;                       // x, w
 constexpr int kROpStage = 2 * (kRXB + kRWB);                  // x hi, w hi, x lo, w lo
 constexpr size_t kRSmem = 1024 + (size_t)kRRaw * kRRawStage + (size_t)kROps * kROpStage;
@@ -244,8 +247,10 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
-    const int m0 = blockIdx.y * kRM, n0 = blockIdx.x * kRN;
-    const int nk = d / kRK;
+    const uint32_t rank = cluster_rank();           // which half of the reduction
+    const int m0 = blockIdx.y * kRM, n0 = (blockIdx.x / kRSplit) * kRN;
+    const int nk = d / kRK / kRSplit;               // stages of this CTA
+    const int k0 = (int)rank * nk * kRK;            // first reduction element
     const int nchunk = (nk + kRChunk - 1) / kRChunk;
     const uint32_t opbase = base + kRRaw * kRRawStage;
 
@@ -259,8 +264,8 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                 if (!abort_flag) {
                     const uint32_t sb = base + s * kRRawStage;
                     mbar_arrive_expect_tx(smem_addr(&full[s]), kRXB + kRWB);
-                    tma_load_2d(sb, &mx, kb * kRK, m0, smem_addr(&full[s]));
-                    tma_load_2d(sb + kRXB, &mw, kb * kRK, n0, smem_addr(&full[s]));
+                    tma_load_2d(sb, &mx, k0 + kb * kRK, m0, smem_addr(&full[s]));
+                    tma_load_2d(sb + kRXB, &mw, k0 + kb * kRK, n0, smem_addr(&full[s]));
                 }
             }
         }
@@ -360,15 +365,35 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
             tc_fence_before();
             mbar_arrive(smem_addr(&acce[b]));
         }
-        const int t = m0 + sub * 32 + lane;
-        if (t < T) {
-            float4 *dst = reinterpret_cast<float4 *>(logits + (size_t)t * E + n0);
+        // the second CTA leaves its sums (row = TMEM lane) in its raw ring, which is idle now
+        const int row = sub * 32 + lane;
+        if (rank != 0) {
+            float4 *xs = reinterpret_cast<float4 *>(gbase) + (size_t)row * (kRN / 4);
 #pragma unroll
             for (int q = 0; q < kRN / 4; q++)
-                dst[q] = ok ? make_float4(sum[4 * q], sum[4 * q + 1], sum[4 * q + 2], sum[4 * q + 3])
-                            : make_float4(NAN, NAN, NAN, NAN);
+                xs[q] = make_float4(sum[4 * q], sum[4 * q + 1], sum[4 * q + 2], sum[4 * q + 3]);
+            reinterpret_cast<int *>(gbase + (size_t)kRM * kRN * 4)[row] = ok ? 1 : 0;
         }
+        cluster_sync();
+        if (rank == 0) {
+            const uint32_t peer = map_to_rank(base, 1);
+            const uint32_t prow = peer + (uint32_t)row * kRN * 4;
+            const bool pok = ld_cluster_s32(peer + (uint32_t)kRM * kRN * 4 + row * 4) != 0;
+            const int t = m0 + row;
+            float4 *dst = reinterpret_cast<float4 *>(logits + (size_t)t * E + n0);
+#pragma unroll
+            for (int q = 0; q < kRN / 4; q++) {
+                const float4 o = ld_cluster_f4(prow + q * 16);
+                const float4 v = make_float4(sum[4 * q] + o.x, sum[4 * q + 1] + o.y, sum[4 * q + 2] + o.z,
+                                             sum[4 * q + 3] + o.w);
+                if (t < T)
+                    dst[q] = (ok && pok) ? v : make_float4(NAN, NAN, NAN, NAN);
+            }
+        }
+        cluster_sync();   // the peer's shared memory stays until it has been read
     }
+    if (warp < 6)
+        cluster_sync(), cluster_sync();   // the other roles take part in both cluster barriers
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -483,7 +508,7 @@ act_frag_kernel(const float *__restrict__ x, int K, uint8_t *__restrict__ frag, 
 int launch_router_logits(const float *x, const float *wg, int T, int d, int E, float *logits,
                          cudaStream_t s)
 {
-    if (T >= kTcMinTokens && d % kRK == 0 && E % kRN == 0 && ((uintptr_t)x & 15) == 0 &&
+    if (T >= kTcMinTokens && d % (kRK * kRSplit) == 0 && E % kRN == 0 && ((uintptr_t)x & 15) == 0 &&
         ((uintptr_t)wg & 15) == 0 && ((uintptr_t)logits & 15) == 0) {
         CUtensorMap mx, mw;
         int rc = make_tmap_2d(&mx, x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, T, (uint64_t)d * 4, kRK, kRM,
@@ -502,8 +527,19 @@ int launch_router_logits(const float *x, const float *wg, int T, int d, int E, f
                 return MOE_ERR_CUDA;
             configured[dev] = 1;
         }
-        dim3 grid(E / kRN, (T + kRM - 1) / kRM);
-        logits_tc_kernel<<<grid, kRThreads, kRSmem, s>>>(mx, mw, T, d, E, logits);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(E / kRN * kRSplit), (unsigned)((T + kRM - 1) / kRM));
+        cfg.blockDim = dim3(kRThreads);
+        cfg.dynamicSmemBytes = kRSmem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kRSplit;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cuda_status(cudaLaunchKernelEx(&cfg, logits_tc_kernel, mx, mw, T, d, E, logits));
     } else if (T >= 128 && d % kBK == 0) {
         dim3 grid((E + kBN - 1) / kBN, (T + kBM - 1) / kBM);
         logits_tiled_kernel<<<grid, 256, 0, s>>>(x, wg, T, d, E, logits);

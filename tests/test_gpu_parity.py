@@ -213,6 +213,7 @@ ROUTE_TC = [
     (777, 128, 2048, "zipf", 1.0),
     (640, 256, 512, "normal", 1e3),
     (520, 64, 256, "zero", 1e-3),
+    (130, 256, 6144, "normal", 1.0),   # the GLM-5.2 router width, a ragged second token tile
 ]
 
 
