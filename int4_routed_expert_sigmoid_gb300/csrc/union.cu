@@ -193,9 +193,11 @@ union_kernel(const int32_t *__restrict__ idx, int T, int k, int E, int use_bitma
     }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int W = (T + 31) / 32;                                      // bitmap words per expert
-    uint32_t *bits = reinterpret_cast<uint32_t *>(dyn);                 // [E][W]
+    // word-major layouts (word w of expert e at w * E + e): the lanes of a warp touch different
+    // experts of the same word, i.e. different banks
+    uint32_t *bits = reinterpret_cast<uint32_t *>(dyn);                 // [W][E]
     int *base = dyn + (size_t)E * W;                                    // [E] first position of the expert
-    unsigned short *pre = reinterpret_cast<unsigned short *>(base + E); // [E][W] set bits before the word
+    unsigned short *pre = reinterpret_cast<unsigned short *>(base + E); // [W][E] set bits before the word
     for (int i = tid; i < E * W; i += kThreads)
         bits[i] = 0u;
     __syncthreads();
@@ -208,7 +210,7 @@ union_kernel(const int32_t *__restrict__ idx, int T, int k, int E, int use_bitma
         }
         const int t = p / k;
         const uint32_t b = 1u << (t & 31);
-        if (atomicOr(&bits[e * W + (t >> 5)], b) & b)
+        if (atomicOr(&bits[(t >> 5) * E + e], b) & b)
             dup = 1;
     }
     bad = __syncthreads_or(bad);
@@ -218,28 +220,14 @@ union_kernel(const int32_t *__restrict__ idx, int T, int k, int E, int use_bitma
     }
     if (bad && tid == 0)
         atomicOr(err, MOE_DEVERR_BAD_EXPERT);
-    // per expert (one warp each): prefix of bit counts over the words; lane l takes words
-    // l * q .. l * q + q - 1
-    const int q = (W + 31) / 32;
-    for (int e = warp; e < E; e += kWarps) {
-        const uint32_t *row = bits + (size_t)e * W;
-        int mine = 0;
-        for (int w = lane * q; w < min(W, lane * q + q); w++)
-            mine += __popc(row[w]);
-        int inc = mine;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, inc, off);
-            if (lane >= off)
-                inc += v;
+    // per expert (one thread each): prefix of bit counts over the words
+    for (int e = tid; e < E; e += kThreads) {
+        int run = 0;
+        for (int w = 0; w < W; w++) {
+            pre[(size_t)w * E + e] = (unsigned short)run;
+            run += __popc(bits[(size_t)w * E + e]);
         }
-        int run = inc - mine;
-        for (int w = lane * q; w < min(W, lane * q + q); w++) {
-            pre[(size_t)e * W + w] = (unsigned short)run;
-            run += __popc(row[w]);
-        }
-        if (lane == 31)
-            base[e] = inc;   // the expert's count, turned into its first position below
+        base[e] = run;   // the expert's count, turned into its first position below
     }
     __syncthreads();
     // offsets (exclusive scan over ascending expert id), counts, hits, uniq
@@ -274,8 +262,8 @@ union_kernel(const int32_t *__restrict__ idx, int T, int k, int E, int use_bitma
         int pos = -1;
         if (e >= 0 && e < E) {
             const int t = p / k, w = t >> 5;
-            const uint32_t below = bits[(size_t)e * W + w] & ((1u << (t & 31)) - 1u);
-            pos = base[e] + pre[(size_t)e * W + w] + __popc(below);
+            const uint32_t below = bits[(size_t)w * E + e] & ((1u << (t & 31)) - 1u);
+            pos = base[e] + pre[(size_t)w * E + e] + __popc(below);
             sorted_pair[pos] = p;
         }
         perm[p] = pos;
