@@ -513,11 +513,19 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
     } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------------- epilogue
         const int sub = warp & 3;                 // TMEM lanes 32*sub .. 32*sub+31 = A rows
+        // the row factors of an item's tokens, loaded into this warp's slice before the item's
+        // accumulator is waited for (one global round trip per item instead of one per chunk)
+        __shared__ float epi_scale[4][kTileN];
+        float *rsc = epi_scale[warp - kEpiWarp0];
         uint32_t fph[2] = {0u, 0u};
         int j = 0;
         for (int i = blockIdx.x; i < n_items; i += gridDim.x, j++) {
             const PItem it = decode_pitem<N>(p, tab, units, i);
             const int b = j & 1;
+            __syncwarp();
+            for (int q = lane; q < it.ntok; q += 32)
+                rsc[q] = p.row_scale[it.row0 + it.tok0 + q];
+            __syncwarp();
             if (!abort_flag && !mbar_wait(smem_addr(&acc_full[b]), fph[b])) {
                 atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                 abort_flag = 1;
@@ -533,7 +541,6 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                     // lane l < 16: gate row 16 sub + l; lane l + 16: the same up row.  Pair q of
                     // tokens (2q, 2q + 1): the gate lane forms h of token 2q, the up lane token 2q + 1,
                     // each taking the other's value with one shuffle.
-                    const float rfl = lane < nj ? p.row_scale[it.row0 + it.tok0 + c0 + lane] : 0.f;
                     tmem_wait_ld();
                     const int hi = lane >> 4;
                     const int hr = it.mtile * 64 + sub * 16 + (lane & 15);   // column of h
@@ -543,8 +550,8 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                         const float other = __shfl_xor_sync(0xffffffffu,
                                                             __uint_as_float(hi ? v[2 * q] : v[2 * q + 1]), 16);
                         const int jj = 2 * q + hi;
-                        const float rf = __shfl_sync(0xffffffffu, rfl, jj);
                         if (jj < nj) {
+                            const float rf = rsc[c0 + jj];
                             const float gv = (hi ? other : mine) * rf;
                             const float uv = (hi ? mine : other) * rf;
                             const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
@@ -552,14 +559,13 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                         }
                     }
                 } else {
-                    const float rfl = lane < nj ? p.row_scale[it.row0 + it.tok0 + c0 + lane] : 0.f;
                     tmem_wait_ld();
                     const int orow = it.mtile * kTileM + sub * 32 + lane;
 #pragma unroll
                     for (int jj = 0; jj < 16; jj++) {
-                        const float rf = __shfl_sync(0xffffffffu, rfl, jj);
                         if (jj >= nj)
                             break;
+                        const float rf = rsc[c0 + jj];
                         const int tok = it.tok0 + c0 + jj;
                         const float yv = __uint_as_float(v[jj]) * rf;
                         if (it.expert < 0)
