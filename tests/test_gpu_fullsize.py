@@ -171,6 +171,18 @@ def test_prefill_t4096(full):
     assert rel_max_err(s["y_shared"][toks], y_sh) <= TOL_PREFILL
 
 
+@pytest.mark.parametrize("T", [32, 128, 256])
+def test_automatic_mode_mid_batches(full, T):
+    """The automatic mode at the batch sizes between decode and prefill, Zipf-biased: T = 32 takes the
+    decode path (8-token passes), T = 128 and 256 the prefill path with the tensor-core router."""
+    L, lw, wg_d = full
+    m = moe()
+    x = workloads.activations(T, D, seed=T)
+    bias = workloads.selection_bias(E, "zipf", seed=0)
+    tol = TOL_DECODE if T < 128 else TOL_PREFILL
+    _check_layer(L, lw, wg_d, x, bias, m.MOE_MODE_AUTO, tol, 8)
+
+
 def test_stack_8_layers(full):
     """8 resident-shape layers, each out_l = x_l + MoE(norm(x_l)) with a per-layer Zipf permutation.
 
