@@ -84,3 +84,35 @@ def test_reference_arm_under_torchrun():
     assert j["impl"] == "reference" and j["n_gpus"] == 2 and j["steps"] == 3
     assert j["value"] > 0 and j["e2e"]["h2d_bytes_per_step"] == 0
     assert j["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_bench_arguments_and_bytes():
+    """Argument forms the benchmark accepts, and the algorithmic bytes of a layer step against the
+    per-expert figure (3 d f int4 weights + 3 d f / 32 fp32 scales) and the router's weights."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    a = bench.parse_args([])
+    assert (a.workload, a.mode, a.gpus, a.impl) == ("decode", "workload", 1, "ours")
+    for wl in ("decode", "batched_decode", "prefill", "stack", "tiny"):
+        assert bench.parse_args(["--workload", wl]).workload == wl
+    assert bench.parse_args(["--mode", "prefill"]).mode == "prefill"
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--workload", "nope"])
+    sh = workloads.WORKLOADS["decode"]
+    b = bench.layer_bytes(sh, n_uniq=8)
+    assert b["expert_block"] == 23_592_960
+    assert b["ffn"] == 9 * 23_592_960 and b["nibbles"] == 9 * 18_874_368
+    assert b["layer"] == b["ffn"] + 256 * 6144 * 4 + 256 * 4 + 2 * 1 * 6144 * 4
+
+
+def test_kernel_source_hash_and_traffic_record():
+    """The traffic record is used only while its hash matches the kernel sources."""
+    sys.path.insert(0, ROOT)
+    import bench
+    h = bench.kernel_source_hash(ROOT)
+    assert len(h) == 16 and h == bench.kernel_source_hash(ROOT)
+    rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+    for key in ("ffn", "ffn_prefill"):
+        got = bench.ncu_traffic(ROOT, key)
+        assert got == (rec[key]["dram_bytes_per_launch"] if rec[key]["source_hash"] == h else None)
