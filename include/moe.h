@@ -37,9 +37,9 @@
  *    of the three matrices in that order (moe_expert_q_bytes bytes), then their
  *    scales in the same order (moe_expert_s_count floats).  Expert e of a layer
  *    starts at q_base + e * moe_expert_q_bytes(d, f) and
- *    s_base + e * moe_expert_s_count(d, f, G).  ("each activated expert is a
- *    three-matrix MLP (size ~19 MB at int4) stored contiguously": same page and
- *    section as above.)
+ *    s_base + e * moe_expert_s_count(d, f, G).  (Same page and section: an
+ *    expert's three weight matrices lie next to one another, about 19 MB per
+ *    expert at int4.)
  *  - FFN_e(x) = down_e( silu(gate_e x) * (up_e x) ), silu(g) = g * sigmoid(g).
  *
  * Supported shapes: G = 32; d a multiple of 256; f a multiple of 128;
@@ -76,7 +76,12 @@ enum {
 
 /* FFN execution modes. */
 enum {
-    MOE_MODE_AUTO = 0,     /* decode path when T < 128, else prefill */
+    MOE_MODE_AUTO = 0,     /* decode path when T < 128, else prefill.  The two paths differ in
+                              precision (decode within 1e-4 of the output RMS of the exact
+                              result, prefill within 2e-2), so under this mode the same token's
+                              output can move by up to 2e-2 * RMS when the batch around it
+                              crosses 128 tokens.  Pass MOE_MODE_DECODE to keep the decode
+                              path's precision at every batch size. */
     MOE_MODE_DECODE = 1,   /* fp32-accurate grouped GEMV: exact int4 against activations split
                               into fp16 hi + lo parts, fp32 accumulation */
     MOE_MODE_PREFILL = 2   /* tcgen05 grouped GEMM on 16-bit operands (fp16 q*s weights, fp16
@@ -131,9 +136,10 @@ MOE_API int moe_route(const float *x, const float *w_gate, const float *bias, in
 /*
  * Union: merge the routed (token, slot) pairs of the batch so each unique
  * expert is read once, and group the pairs by expert.
- * Source: same page and section ("Union -- merge requests across the batch");
- * same page, "Cache/Prefetch Design Comparison" figure caption ("each unique
- * expert is read only once" under batch-union).
+ * Source: same page and section (the Union stage combines the expert requests
+ * of all tokens in the batch); same page, "Cache/Prefetch Design Comparison"
+ * figure caption (with the batch union, a unique expert's weights are fetched
+ * a single time per batch).
  *
  * Pair p = t*k + j.  Outputs (all int32, caller-owned):
  *   counts [E]        number of pairs routed to each expert
@@ -156,17 +162,17 @@ MOE_API int moe_union(const int32_t *topk_idx, int T, int k, int E, int32_t *cou
  * Learn: per-expert hit counters, hits[e] += counts[e] (uint64, cumulative
  * across calls; one count per routed (token, slot) pair).
  * Source: "Public Colibri Observation and Revision Ledger", "Exact
- * Architecture and Data-Flow Reconstruction" ("after each token the engine
- * updates per-expert hit counters (the Learn step)").
+ * Architecture and Data-Flow Reconstruction", Learn stage (the engine counts,
+ * per expert, how often the router picked it).
  */
 MOE_API int moe_hits(const int32_t *counts, int E, uint64_t *hits, void *stream);
 
 /*
  * Expert FFN over the batch union: each expert in uniq (and the shared expert)
  * is streamed once and applied to all of its grouped tokens.
- * Source: same section ("Each activated expert is a three-matrix MLP ...
- * stored contiguously"; "a small shared expert branch ... is always used");
- * the SwiGLU form is a reading (see the design notes).
+ * Source: same section (a routed expert is an MLP of three int4 matrices
+ * kept side by side; a small shared expert runs for every token); the SwiGLU
+ * form is a reading of the pages.
  *
  * x [T][d] fp32; w: the layer's experts; offsets/sorted_pair/uniq/n_uniq from
  * moe_union (device).  Outputs:

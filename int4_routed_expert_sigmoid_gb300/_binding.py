@@ -215,7 +215,16 @@ def moe_expert_ffn_int4(x, layer: LayerWeights, un: dict, k: int, mode: int = MO
     return y_pair, y_shared, err
 
 
-NOALLOC_SCRATCH_BYTES = 8 << 20
+def _header_scratch_bytes() -> int:
+    """MOE_NOALLOC_SCRATCH_BYTES as include/moe.h defines it (one source for the limit)."""
+    import re
+    m = re.search(r"#define\s+MOE_NOALLOC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", open(HEADER).read())
+    if not m:
+        raise RuntimeError("MOE_NOALLOC_SCRATCH_BYTES not found in include/moe.h")
+    return int(m.group(1)) << int(m.group(2))
+
+
+NOALLOC_SCRATCH_BYTES = _header_scratch_bytes()
 
 
 def moe_expert_ffn_int4_noalloc(x, layer: LayerWeights, un: dict, k: int, mode: int = MOE_MODE_AUTO,

@@ -3,10 +3,10 @@
 // HBM once per pass through a TMA-fed shared-memory ring.
 //
 // Sources: "Public Colibri Observation and Revision Ledger", "Exact
-// Architecture and Data-Flow Reconstruction" (each selected expert is a
-// three-matrix MLP stored contiguously at int4; a shared expert is always
-// used) and the batch-union of "Cache/Prefetch Design Comparison" (each unique
-// expert read once per batch).  SwiGLU (h = silu(gate x) * up x, y = down h)
+// Architecture and Data-Flow Reconstruction" (a routed expert is an MLP of
+// three int4 matrices kept side by side; the shared expert runs for every
+// token) and the batch union of "Cache/Prefetch Design Comparison" (one fetch
+// of a selected expert serves the whole batch).  SwiGLU (h = silu(gate x) * up x, y = down h)
 // and the group-32 fp32 scales are readings of the pages.
 //
 // Design (GB300, sm_103a)
@@ -614,23 +614,26 @@ int launch_one(const Maps &maps, const Params &prm, int max_items, int max_units
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return MOE_ERR_CUDA;
-    // per device: opt in to the largest dynamic shared memory once; cache the occupancy per size
-    static bool opted[64] = {false};
-    static size_t occ_smem[64] = {0};
-    static int occ_val[64] = {0};
-    if (!opted[dev]) {
+    // per device: opt in to the largest dynamic shared memory once; cache the occupancy of the last
+    // shared-memory size as one atomic word (smem << 8 | blocks per SM), so host threads calling
+    // together at worst repeat the query
+    static std::atomic<int> opted[64];
+    static std::atomic<uint64_t> occ[64];
+    if (!opted[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)(C::kSmem + 1025 * sizeof(Unit) + 16)) != cudaSuccess)
             return MOE_ERR_CUDA;
-        opted[dev] = true;
+        opted[dev].store(1, std::memory_order_release);
     }
-    int per_sm = occ_smem[dev] == smem ? occ_val[dev] : 0;
+    const uint64_t oc = occ[dev].load(std::memory_order_relaxed);
+    int per_sm = (oc >> 8) == (uint64_t)smem ? (int)(oc & 0xff) : 0;
     if (per_sm == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess ||
             per_sm < 1)
             per_sm = 1;
-        occ_smem[dev] = smem;
-        occ_val[dev] = per_sm;
+        if (per_sm > 255)
+            per_sm = 255;
+        occ[dev].store(((uint64_t)smem << 8) | (uint64_t)per_sm, std::memory_order_relaxed);
     }
     int grid = per_sm * sm_count(dev);
     if (grid > max_items)

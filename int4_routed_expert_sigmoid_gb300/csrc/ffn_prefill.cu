@@ -720,12 +720,14 @@ int launch_prefill_one(const PMaps &maps, const PParams &prm, int max_units, cud
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return MOE_ERR_CUDA;
-    static int configured[64] = {0};
-    if (!configured[dev]) {
+    // per device and instantiation, once (several host threads may get here together: a second
+    // attribute call is harmless, and the flag is atomic)
+    static std::atomic<int> configured[64];
+    if (!configured[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)prefill_smem(C::kRing, 1025)) != cudaSuccess)
             return MOE_ERR_CUDA;
-        configured[dev] = 1;
+        configured[dev].store(1, std::memory_order_release);
     }
     return launch_pdl(kern, sm_count(dev), kPThreads, prefill_smem(C::kRing, max_units), s, maps, prm);
 }

@@ -1,6 +1,7 @@
 // moe_internal.h -- launchers shared between the translation units of libmoe.
 // Internal: not part of the C ABI.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>

@@ -520,12 +520,14 @@ int launch_router_logits(const float *x, const float *wg, int T, int d, int E, f
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
             return MOE_ERR_CUDA;
-        static int configured[64] = {0};
-        if (!configured[dev]) {
+        // per device, once (several host threads may get here together: a second attribute call is
+        // harmless, and the flag is atomic)
+        static std::atomic<int> configured[64];
+        if (!configured[dev].load(std::memory_order_acquire)) {
             if (cudaFuncSetAttribute(logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmem) !=
                 cudaSuccess)
                 return MOE_ERR_CUDA;
-            configured[dev] = 1;
+            configured[dev].store(1, std::memory_order_release);
         }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(E / kRN * kRSplit), (unsigned)((T + kRM - 1) / kRM));

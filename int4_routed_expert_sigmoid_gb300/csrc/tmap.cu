@@ -85,16 +85,16 @@ int make_tmap_nd(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, in
 
 int sm_count(int device)
 {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];   // 0 = not yet queried
     if (device < 0 || device >= 64)
         return 0;
-    if (cache[device] == 0) {
-        int n = 0;
+    int n = cache[device].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
             return 0;
-        cache[device] = n;
+        cache[device].store(n, std::memory_order_relaxed);
     }
-    return cache[device];
+    return n;
 }
 
 }  // namespace moe

@@ -3,10 +3,10 @@
 // counters.
 //
 // Sources: "Public Colibri Observation and Revision Ledger", "Exact
-// Architecture and Data-Flow Reconstruction" (Union merges requests across the
-// batch; Learn records which experts were used, per-expert hit counters), and
-// the figure caption of "Cache/Prefetch Design Comparison" (with batch-union
-// each unique expert is read only once).
+// Architecture and Data-Flow Reconstruction" (the Union stage combines the
+// batch's expert requests; the Learn stage counts per expert how often it was
+// picked), and the figure caption of "Cache/Prefetch Design Comparison" (with
+// the batch union, a selected expert's weights are fetched a single time).
 //
 // One thread block: a shared-memory histogram (atomics only count), a block
 // scan for the offsets, then a stable placement pass over the pairs in chunks
