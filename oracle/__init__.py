@@ -67,7 +67,7 @@ class _Layer(ctypes.Structure):
     _fields_ = [("x", _P), ("wg", _P), ("bias", _P), ("q_base", _P), ("s_base", _P),
                 ("shared_q", _P), ("shared_s", _P), ("res", _P),
                 ("T", _I), ("d", _I), ("f", _I), ("E", _I), ("k", _I), ("G", _I),
-                ("normalize", _I), ("route_scale", _D)]
+                ("normalize", _I), ("route_scale", _D), ("top_p", _D)]
 
 
 def _declare(L: ctypes.CDLL) -> None:
@@ -81,7 +81,8 @@ def _declare(L: ctypes.CDLL) -> None:
     L.oracle_expert_s_count.restype = _I64
     L.oracle_router_logits.argtypes = [_P, _P, _I, _I, _I, _P]
     L.oracle_route.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _D, _P, _P, _P, _P]
-    L.oracle_route_from_logits.argtypes = [_P, _P, _I, _I, _I, _I, _D, _P, _P, _P]
+    L.oracle_route_topp.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _D, _D, _P, _P, _P, _P]
+    L.oracle_route_from_logits.argtypes = [_P, _P, _I, _I, _I, _I, _D, _D, _P, _P, _P]
     L.oracle_union.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
     L.oracle_union.restype = _I
     L.oracle_hits.argtypes = [_P, _I, _P]
@@ -92,6 +93,7 @@ def _declare(L: ctypes.CDLL) -> None:
                                          _P, _P, _P, _P]
     L.oracle_moe_layer_union.restype = _I
     L.oracle_threads.restype = _I
+    L.oracle_set_threads.argtypes = [_I]
     L.oracle_rms_norm.argtypes = [_P, _I, _I, _D, _P]
 
 
@@ -106,6 +108,11 @@ def _ptr(a: np.ndarray | None):
 
 def threads() -> int:
     return int(lib().oracle_threads())
+
+
+def set_threads(n: int) -> None:
+    """OpenMP thread count of later oracle calls (results do not depend on it)."""
+    lib().oracle_set_threads(int(n))
 
 
 # ------------------------------------------------------------------ int4 ----
@@ -154,8 +161,9 @@ def router_logits(x: np.ndarray, wg: np.ndarray) -> np.ndarray:
     return out
 
 
-def route(x, wg, bias, k: int, normalize: int = 1, route_scale: float = 1.0):
-    """Returns (idx [T,k] int32, w [T,k] f64, logits [T,E] f64, keys [T,E] f64)."""
+def route(x, wg, bias, k: int, normalize: int = 1, route_scale: float = 1.0, top_p: float = 1.0):
+    """Returns (idx [T,k] int32, w [T,k] f64, logits [T,E] f64, keys [T,E] f64).
+    top_p < 1 empties the pruned slots (id -1, weight 0)."""
     x = _c(x, np.float32)
     wg = _c(wg, np.float32)
     bias = None if bias is None else _c(bias, np.float32)
@@ -165,12 +173,15 @@ def route(x, wg, bias, k: int, normalize: int = 1, route_scale: float = 1.0):
     w = np.empty((T, k), dtype=np.float64)
     logits = np.empty((T, E), dtype=np.float64)
     keys = np.empty((T, E), dtype=np.float64)
-    lib().oracle_route(_ptr(x), _ptr(wg), _ptr(bias), T, d, E, k, int(normalize),
-                       float(route_scale), _ptr(idx), _ptr(w), _ptr(logits), _ptr(keys))
+    lib().oracle_route_topp(_ptr(x), _ptr(wg), _ptr(bias), T, d, E, k, int(normalize),
+                            float(route_scale), float(top_p), _ptr(idx), _ptr(w), _ptr(logits),
+                            _ptr(keys))
     return idx, w, logits, keys
 
 
-def route_from_logits(logits, bias, k: int, normalize: int = 1, route_scale: float = 1.0):
+def route_from_logits(logits, bias, k: int, normalize: int = 1, route_scale: float = 1.0,
+                      top_p: float = 1.0):
+    """Routing of given fp64 logits [T,E]: (idx, w, keys) as in route()."""
     logits = _c(logits, np.float64)
     bias = None if bias is None else _c(bias, np.float32)
     T, E = logits.shape
@@ -178,7 +189,7 @@ def route_from_logits(logits, bias, k: int, normalize: int = 1, route_scale: flo
     w = np.empty((T, k), dtype=np.float64)
     keys = np.empty((T, E), dtype=np.float64)
     lib().oracle_route_from_logits(_ptr(logits), _ptr(bias), T, E, k, int(normalize),
-                                   float(route_scale), _ptr(idx), _ptr(w), _ptr(keys))
+                                   float(route_scale), float(top_p), _ptr(idx), _ptr(w), _ptr(keys))
     return idx, w, keys
 
 
@@ -246,7 +257,7 @@ class Layer:
     """One MoE layer's inputs (numpy, host).  Arrays are kept alive here."""
 
     def __init__(self, x, wg, bias, q_base, s_base, shared_q, shared_s, *, d, f, E, k,
-                 G=32, normalize=1, route_scale=1.0, res=None):
+                 G=32, normalize=1, route_scale=1.0, res=None, top_p=1.0):
         self.x = _c(x, np.float32)
         self.wg = _c(wg, np.float32)
         self.bias = None if bias is None else _c(bias, np.float32)
@@ -257,7 +268,7 @@ class Layer:
         self.res = None if res is None else _c(res, np.float32)
         self.T = self.x.shape[0]
         self.d, self.f, self.E, self.k, self.G = d, f, E, k, G
-        self.normalize, self.route_scale = int(normalize), float(route_scale)
+        self.normalize, self.route_scale, self.top_p = int(normalize), float(route_scale), float(top_p)
         assert self.x.shape == (self.T, d) and self.wg.shape == (E, d)
         assert self.q_base.size >= E * expert_q_bytes(d, f)
         assert self.s_base.size >= E * expert_s_count(d, f, G)
@@ -266,7 +277,7 @@ class Layer:
         return _Layer(_ptr(self.x), _ptr(self.wg), _ptr(self.bias), _ptr(self.q_base),
                       _ptr(self.s_base), _ptr(self.shared_q), _ptr(self.shared_s),
                       _ptr(self.res), self.T, self.d, self.f, self.E, self.k, self.G,
-                      self.normalize, self.route_scale)
+                      self.normalize, self.route_scale, self.top_p)
 
     def tokens(self, tokens) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
         """Dense masked evaluation of the listed tokens: (idx, w, out fp64)."""

@@ -54,6 +54,10 @@
  *    pair p in that order, sorted_pair[position] = p, uniq = experts with a
  *    non-zero count in ascending order.
  *  - hits[e] += counts[e] (one count per routed (token, slot) pair).
+ *  - top-p pruning (lossy, off at top_p = 1): of the k chosen experts in
+ *    selection order, the shortest prefix whose scores reach top_p times the
+ *    scores of all k is kept; the other slots hold id -1 and weight 0, join no
+ *    union group and add nothing to the output or the hit counters.
  *
  * Pins: every function here is pinned by the CPU test suite (closed forms,
  * invariants, brute force, exhaustive enumeration).  Nothing printed on the
@@ -136,11 +140,12 @@ static double sigmoid(double v)
     return 1.0 / (1.0 + exp(-v));
 }
 
-/* l[t, e] = sum_i x[t, i] * Wg[e, i]   (fp64, i ascending). */
+/* l[t, e] = sum_i x[t, i] * Wg[e, i]   (fp64, i ascending; the (t, e) sums
+ * are independent and may run on any thread). */
 ORACLE_API void oracle_router_logits(const float *x, const float *wg, int T,
                                      int d, int E, double *logits)
 {
-#pragma omp parallel for schedule(static)
+#pragma omp parallel for collapse(2) schedule(static)
     for (int t = 0; t < T; t++)
         for (int e = 0; e < E; e++) {
             double acc = 0.0;
@@ -162,10 +167,20 @@ static int key_before(double ka, int a, double kb, int b)
  * Route one token: scores s_e = sigmoid(l_e), keys s_e + bias_e, top-k by key
  * (descending, ties -> lower id), then weights.  Selection is done by k passes
  * that each pick the best expert not yet chosen.
+ *
+ * top_p < 1 prunes the selection (the lossy "top-p gating" of "Public Colibri
+ * Observation and Revision Ledger", "Exact-Versus-Lossy Mode Table"; the
+ * `--topp` setting of the summary page "Colibri is an open-source, lightweight
+ * Mixture-of-Experts", "Configuration"): the k chosen experts, in selection
+ * order, keep their shortest prefix of m >= 1 slots whose scores add up to at
+ * least top_p times the scores of all k,
+ *     m = min { m : s_1 + ... + s_m >= top_p * (s_1 + ... + s_k) },
+ * and the other k - m slots become empty (id -1, weight 0).  Normalised
+ * weights are then taken over the m kept slots.  top_p >= 1 keeps all k.
  */
 static void route_token(const double *l, const float *bias, int E, int k,
-                        int normalize, double route_scale, int32_t *idx,
-                        double *w, double *keys)
+                        int normalize, double route_scale, double top_p,
+                        int32_t *idx, double *w, double *keys)
 {
     double *key = keys;
     char *taken = calloc((size_t)E, 1);
@@ -183,11 +198,29 @@ static void route_token(const double *l, const float *bias, int E, int k,
         idx[j] = best;
         w[j] = sigmoid(l[best]);
     }
+    int m = k;
+    if (top_p < 1.0) {
+        double total = 0.0;
+        for (int j = 0; j < k; j++)
+            total += w[j];
+        double cum = 0.0;
+        for (m = 1; m <= k; m++) {
+            cum += w[m - 1];
+            if (cum >= top_p * total)
+                break;
+        }
+        if (m > k)
+            m = k;
+        for (int j = m; j < k; j++) {
+            idx[j] = -1;
+            w[j] = 0.0;
+        }
+    }
     if (normalize) {
         double sum = 0.0;
-        for (int j = 0; j < k; j++)
+        for (int j = 0; j < m; j++)
             sum += w[j];
-        for (int j = 0; j < k; j++)
+        for (int j = 0; j < m; j++)
             w[j] = route_scale * w[j] / sum;
     }
     free(taken);
@@ -195,19 +228,20 @@ static void route_token(const double *l, const float *bias, int E, int k,
 
 /*
  * Route T tokens.  Outputs: idx [T][k] int32, w [T][k] fp64, and optionally
- * logits [T][E] and keys [T][E] (fp64; either may be NULL).
+ * logits [T][E] and keys [T][E] (fp64; either may be NULL).  top_p as in
+ * route_token (1 = plain top-k).
  */
-ORACLE_API void oracle_route(const float *x, const float *wg, const float *bias,
-                             int T, int d, int E, int k, int normalize,
-                             double route_scale, int32_t *idx, double *w,
-                             double *logits_out, double *keys_out)
+ORACLE_API void oracle_route_topp(const float *x, const float *wg, const float *bias,
+                                  int T, int d, int E, int k, int normalize,
+                                  double route_scale, double top_p, int32_t *idx,
+                                  double *w, double *logits_out, double *keys_out)
 {
     double *logits = logits_out ? logits_out : malloc(sizeof(double) * (size_t)T * E);
     oracle_router_logits(x, wg, T, d, E, logits);
 #pragma omp parallel for schedule(static)
     for (int t = 0; t < T; t++) {
         double *keys = keys_out ? keys_out + (int64_t)t * E : malloc(sizeof(double) * (size_t)E);
-        route_token(logits + (int64_t)t * E, bias, E, k, normalize, route_scale,
+        route_token(logits + (int64_t)t * E, bias, E, k, normalize, route_scale, top_p,
                     idx + (int64_t)t * k, w + (int64_t)t * k, keys);
         if (!keys_out)
             free(keys);
@@ -216,15 +250,24 @@ ORACLE_API void oracle_route(const float *x, const float *wg, const float *bias,
         free(logits);
 }
 
-/* Same as oracle_route, but from precomputed fp64 logits [T][E]. */
+ORACLE_API void oracle_route(const float *x, const float *wg, const float *bias,
+                             int T, int d, int E, int k, int normalize,
+                             double route_scale, int32_t *idx, double *w,
+                             double *logits_out, double *keys_out)
+{
+    oracle_route_topp(x, wg, bias, T, d, E, k, normalize, route_scale, 1.0, idx, w,
+                      logits_out, keys_out);
+}
+
+/* Same as oracle_route_topp, but from precomputed fp64 logits [T][E]. */
 ORACLE_API void oracle_route_from_logits(const double *logits, const float *bias,
                                          int T, int E, int k, int normalize,
-                                         double route_scale, int32_t *idx,
+                                         double route_scale, double top_p, int32_t *idx,
                                          double *w, double *keys_out)
 {
     for (int t = 0; t < T; t++) {
         double *keys = keys_out ? keys_out + (int64_t)t * E : malloc(sizeof(double) * (size_t)E);
-        route_token(logits + (int64_t)t * E, bias, E, k, normalize, route_scale,
+        route_token(logits + (int64_t)t * E, bias, E, k, normalize, route_scale, top_p,
                     idx + (int64_t)t * k, w + (int64_t)t * k, keys);
         if (!keys_out)
             free(keys);
@@ -234,8 +277,9 @@ ORACLE_API void oracle_route_from_logits(const double *logits, const float *bias
 /* ---------------------------------------------------------------- union --- */
 
 /*
- * Batch union of the routed (token, slot) pairs p = t*k + j.
- * Returns 0, or -1 when an expert id is outside [0, E).
+ * Batch union of the routed (token, slot) pairs p = t*k + j.  A slot holding
+ * -1 is empty (pruned by top-p): it joins no group and gets perm[p] = -1.
+ * Returns 0, or -1 when any other expert id is outside [0, E).
  */
 ORACLE_API int oracle_union(const int32_t *idx, int T, int k, int E,
                             int32_t *counts, int32_t *offsets, int32_t *perm,
@@ -245,6 +289,8 @@ ORACLE_API int oracle_union(const int32_t *idx, int T, int k, int E,
     for (int e = 0; e < E; e++)
         counts[e] = 0;
     for (int64_t p = 0; p < P; p++) {
+        if (idx[p] == -1)
+            continue;
         if (idx[p] < 0 || idx[p] >= E)
             return -1;
         counts[idx[p]]++;
@@ -258,6 +304,10 @@ ORACLE_API int oracle_union(const int32_t *idx, int T, int k, int E,
     for (int e = 0; e < E; e++)
         next[e] = offsets[e];
     for (int64_t p = 0; p < P; p++) {
+        if (idx[p] == -1) {
+            perm[p] = -1;
+            continue;
+        }
         int32_t pos = next[idx[p]]++;
         perm[p] = pos;
         sorted_pair[pos] = (int32_t)p;
@@ -297,6 +347,10 @@ ORACLE_API void oracle_expert_ffn(const float *x, const uint8_t *q, const float 
     const float *s_up = s + (int64_t)f * d / G;
     const float *s_down = s + 2 * (int64_t)f * d / G;
     double *h = malloc(sizeof(double) * (size_t)f);
+    /* Output rows are independent: they are split over the OpenMP threads when
+     * this runs outside another parallel region (one token, as in decode).
+     * Every row's sum keeps its order, so the bits do not depend on it. */
+#pragma omp parallel for schedule(static)
     for (int r = 0; r < f; r++) {
         double g = 0.0, u = 0.0;
         for (int i = 0; i < d; i++) {
@@ -305,6 +359,7 @@ ORACLE_API void oracle_expert_ffn(const float *x, const uint8_t *q, const float 
         }
         h[r] = g * sigmoid(g) * u;
     }
+#pragma omp parallel for schedule(static)
     for (int c = 0; c < d; c++) {
         double acc = 0.0;
         for (int r = 0; r < f; r++)
@@ -314,12 +369,17 @@ ORACLE_API void oracle_expert_ffn(const float *x, const uint8_t *q, const float 
     free(h);
 }
 
-/* The same FFN for a list of tokens (independent, OpenMP over tokens). */
+/* Threads of the OpenMP runtime (1 without OpenMP). */
+static int max_threads(void);
+
+/* The same FFN for a list of tokens (independent).  With at least as many
+ * tokens as threads, OpenMP splits the tokens; with fewer, the rows inside
+ * each token's FFN are split instead. */
 ORACLE_API void oracle_expert_ffn_tokens(const float *x, const int32_t *tokens,
                                          int n, const uint8_t *q, const float *s,
                                          int d, int f, int G, double *y)
 {
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for schedule(dynamic, 1) if (n >= max_threads())
     for (int i = 0; i < n; i++)
         oracle_expert_ffn(x + (int64_t)tokens[i] * d, q, s, d, f, G,
                           y + (int64_t)i * d);
@@ -338,6 +398,7 @@ typedef struct {
     const float *res;      /* [T][d] or NULL */
     int T, d, f, E, k, G, normalize;
     double route_scale;
+    double top_p;          /* 1 = plain top-k; < 1 prunes as in route_token */
 } oracle_layer;
 
 /*
@@ -354,7 +415,7 @@ ORACLE_API void oracle_moe_layer_tokens(const oracle_layer *L, const int32_t *to
     const int d = L->d, E = L->E, k = L->k;
     const int64_t qb = oracle_expert_q_bytes(d, L->f);
     const int64_t sc = oracle_expert_s_count(d, L->f, L->G);
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for schedule(dynamic, 1) if (n >= max_threads())
     for (int i = 0; i < n; i++) {
         int t = tokens[i];
         const float *xt = L->x + (int64_t)t * d;
@@ -363,7 +424,7 @@ ORACLE_API void oracle_moe_layer_tokens(const oracle_layer *L, const int32_t *to
         double *y = malloc(sizeof(double) * (size_t)d);
         double *o = out + (int64_t)i * d;
         oracle_router_logits(xt, L->wg, 1, d, E, l);
-        route_token(l, L->bias, E, k, L->normalize, L->route_scale,
+        route_token(l, L->bias, E, k, L->normalize, L->route_scale, L->top_p,
                     idx + (int64_t)i * k, w + (int64_t)i * k, keys);
         oracle_expert_ffn(xt, L->shared_q, L->shared_s, d, L->f, L->G, y);
         for (int c = 0; c < d; c++)
@@ -371,6 +432,8 @@ ORACLE_API void oracle_moe_layer_tokens(const oracle_layer *L, const int32_t *to
         for (int j = 0; j < k; j++) {
             int e = idx[(int64_t)i * k + j];
             double wj = w[(int64_t)i * k + j];
+            if (e < 0)
+                continue;   /* slot emptied by top-p */
             oracle_expert_ffn(xt, L->q_base + e * qb, L->s_base + e * sc, d, L->f,
                               L->G, y);
             for (int c = 0; c < d; c++)
@@ -398,8 +461,8 @@ ORACLE_API int oracle_moe_layer_union(const oracle_layer *L, int32_t *idx, doubl
     const int T = L->T, d = L->d, E = L->E, k = L->k;
     const int64_t qb = oracle_expert_q_bytes(d, L->f);
     const int64_t sc = oracle_expert_s_count(d, L->f, L->G);
-    oracle_route(L->x, L->wg, L->bias, T, d, E, k, L->normalize, L->route_scale,
-                 idx, w, NULL, NULL);
+    oracle_route_topp(L->x, L->wg, L->bias, T, d, E, k, L->normalize, L->route_scale,
+                      L->top_p, idx, w, NULL, NULL);
     if (oracle_union(idx, T, k, E, counts, offsets, perm, sorted_pair, uniq, n_uniq))
         return -1;
     int64_t P = (int64_t)T * k;
@@ -425,9 +488,12 @@ ORACLE_API int oracle_moe_layer_union(const oracle_layer *L, int32_t *idx, doubl
         for (int c = 0; c < d; c++) {
             double o = (L->res ? (double)L->res[(int64_t)t * d + c] : 0.0) +
                        y_shared[(int64_t)t * d + c];
-            for (int j = 0; j < k; j++)
-                o += w[(int64_t)t * k + j] *
-                     y_pair[(int64_t)perm[(int64_t)t * k + j] * d + c];
+            for (int j = 0; j < k; j++) {
+                int32_t pos = perm[(int64_t)t * k + j];
+                if (pos < 0)
+                    continue;   /* slot emptied by top-p */
+                o += w[(int64_t)t * k + j] * y_pair[(int64_t)pos * d + c];
+            }
             out[(int64_t)t * d + c] = o;
         }
     free(y_pair);
@@ -459,10 +525,14 @@ ORACLE_API void oracle_rms_norm(const float *x, int T, int d, double eps, double
     }
 }
 
-/* Thread count the OpenMP runtime will use (1 without OpenMP). */
+/* Thread count the OpenMP runtime will use (1 without OpenMP), and a setter
+ * for it (tests check that results do not depend on it). */
 #ifdef _OPENMP
 #include <omp.h>
-ORACLE_API int oracle_threads(void) { return omp_get_max_threads(); }
+static int max_threads(void) { return omp_get_max_threads(); }
+ORACLE_API void oracle_set_threads(int n) { if (n > 0) omp_set_num_threads(n); }
 #else
-ORACLE_API int oracle_threads(void) { return 1; }
+static int max_threads(void) { return 1; }
+ORACLE_API void oracle_set_threads(int n) { (void)n; }
 #endif
+ORACLE_API int oracle_threads(void) { return max_threads(); }

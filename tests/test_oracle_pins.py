@@ -446,3 +446,147 @@ def test_rms_norm_invariants():
     assert np.array_equal(oracle.rms_norm(x * np.float32(64.0), eps=0.0), n)
     assert np.array_equal(oracle.rms_norm(x[3:4], eps=0.0), n[3:4])
     assert np.all(np.sign(n) == np.sign(x))
+
+
+# ---------------------------------------------------- routing from logits ----
+
+def test_route_from_logits_matches_route_and_brute_force():
+    """Routing given the logits equals routing from x (bit for bit) and a full sort of the keys."""
+    rng = np.random.default_rng(21)
+    T, d, E, k = 30, 40, 24, 5
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    wg = (rng.standard_normal((E, d)) * 0.4).astype(np.float32)
+    bias = workloads.selection_bias(E, "normal", seed=5)
+    i1, w1, logits, keys = oracle.route(x, wg, bias, k, normalize=1, route_scale=1.5)
+    i2, w2, keys2 = oracle.route_from_logits(logits, bias, k, normalize=1, route_scale=1.5)
+    assert np.array_equal(i1, i2) and np.array_equal(w1, w2) and np.array_equal(keys, keys2)
+    for t in range(T):
+        assert list(i2[t]) == brute_force_topk(list(keys2[t]), k)
+
+
+def test_route_from_logits_hand_worked():
+    # sigmoid is monotone: without bias the order is the logits' order, ties to the lower id
+    logits = np.array([[0.0, 3.0, -3.0, 1.0, 1.0]])
+    idx, w, _ = oracle.route_from_logits(logits, None, 3, normalize=0)
+    assert list(idx[0]) == [1, 3, 4]
+    # a zero bias array and no bias agree; a bias of +1 on expert 2 lifts it to the top
+    idx0, _, _ = oracle.route_from_logits(logits, np.zeros(5, np.float32), 3, normalize=0)
+    assert list(idx0[0]) == [1, 3, 4]
+    idxb, wb, _ = oracle.route_from_logits(logits, np.array([0, 0, 1, 0, 0], np.float32), 3, normalize=0)
+    assert list(idxb[0]) == [2, 1, 3]
+    assert wb[0, 0] == pytest.approx(1.0 / (1.0 + math.exp(3.0)), rel=1e-15)   # unbiased score
+
+
+# ------------------------------------------------------------ top-p cut ----
+# Scores sigmoid(ln 3) = 3/4, sigmoid(0) = 1/2, sigmoid(-ln 3) = 1/4 (sum 3/2) give
+# hand-worked cut points: p = 0.3 -> 0.45 of mass, reached by the first score;
+# p = 0.6 -> 0.9, reached by 3/4 + 1/2 = 5/4; p = 0.9 -> 1.35, only by all three.
+
+HAND_LOGITS = np.array([[math.log(3.0), 0.0, -math.log(3.0), -5.0]])
+
+
+@pytest.mark.parametrize("p,kept,w_norm", [
+    (0.3, [0], [1.0, 0.0, 0.0]),
+    (0.6, [0, 1], [0.6, 0.4, 0.0]),
+    (0.9, [0, 1, 2], [0.5, 1.0 / 3.0, 1.0 / 6.0]),
+    (1.0, [0, 1, 2], [0.5, 1.0 / 3.0, 1.0 / 6.0]),
+])
+def test_topp_hand_worked(p, kept, w_norm):
+    idx, w, _ = oracle.route_from_logits(HAND_LOGITS, None, 3, normalize=1, top_p=p)
+    expect_idx = [e if j < len(kept) else -1 for j, e in enumerate([0, 1, 2])]
+    assert list(idx[0]) == expect_idx
+    assert np.allclose(w[0], w_norm, rtol=1e-14, atol=0)
+    idx0, w0, _ = oracle.route_from_logits(HAND_LOGITS, None, 3, normalize=0, top_p=p)
+    raw = [0.75, 0.5, 0.25]
+    assert np.allclose(w0[0], [raw[j] if j < len(kept) else 0.0 for j in range(3)], rtol=1e-14, atol=0)
+
+
+def test_topp_one_is_plain_topk_and_tiny_p_keeps_one():
+    rng = np.random.default_rng(31)
+    T, d, E, k = 25, 32, 40, 8
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    wg = (rng.standard_normal((E, d)) * 0.5).astype(np.float32)
+    bias = workloads.selection_bias(E, "normal", seed=2)
+    i1, w1, _, _ = oracle.route(x, wg, bias, k, normalize=1, route_scale=2.5)
+    ip, wp, _, _ = oracle.route(x, wg, bias, k, normalize=1, route_scale=2.5, top_p=1.0)
+    assert np.array_equal(i1, ip) and np.array_equal(w1, wp)
+    it, wt, _, _ = oracle.route(x, wg, bias, k, normalize=1, route_scale=2.5, top_p=1e-9)
+    assert np.array_equal(it[:, 0], i1[:, 0]) and np.all(it[:, 1:] == -1)
+    assert np.all(np.abs(wt[:, 0] - 2.5) <= np.spacing(2.5)) and np.all(wt[:, 1:] == 0.0)   # within 1 ulp
+
+
+def test_topp_keeps_a_prefix_growing_with_p():
+    """The kept experts are always a prefix of the top-k list, never fewer as p grows,
+    and their normalised weights add up to route_scale."""
+    rng = np.random.default_rng(41)
+    T, d, E, k = 40, 24, 32, 8
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    wg = rng.standard_normal((E, d)).astype(np.float32)
+    full, _, _, _ = oracle.route(x, wg, None, k)
+    prev = np.ones(T, np.int64)
+    for p in (0.05, 0.2, 0.4, 0.55, 0.7, 0.85, 0.95, 0.999):
+        idx, w, _, _ = oracle.route(x, wg, None, k, normalize=1, route_scale=1.0, top_p=p)
+        m = (idx >= 0).sum(axis=1)
+        assert np.all(m >= 1) and np.all(m >= prev)
+        for t in range(T):
+            assert list(idx[t, :m[t]]) == list(full[t, :m[t]]) and np.all(idx[t, m[t]:] == -1)
+        assert np.allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-15)
+        prev = m
+
+
+def test_union_skips_empty_slots():
+    idx = np.array([[3, -1, -1], [0, 3, -1], [2, 0, 1]], np.int32)
+    u = oracle.union(idx, 4)
+    assert u["counts"].tolist() == [2, 1, 1, 2] and u["offsets"][4] == 6
+    perm = u["perm"]
+    assert perm[1] == -1 and perm[2] == -1 and perm[5] == -1
+    valid = [p for p in range(9) if idx.reshape(-1)[p] != -1]
+    assert sorted(perm[valid].tolist()) == list(range(6))
+    assert np.array_equal(u["sorted_pair"][perm[valid]], np.array(valid))
+    with pytest.raises(ValueError):
+        oracle.union(np.array([[0, -2]], np.int32), 4)   # only -1 marks an empty slot
+
+
+@pytest.mark.parametrize("p", [0.3, 0.5])
+def test_topp_layer_closed_forms(p):
+    """With identical routed experts and normalised weights, the pruned layer is still
+    res + shared + route_scale * FFN(x); the dense and union-path evaluations agree bit for bit."""
+    lay, L = tiny_layer(res=True)
+    sh = workloads.WORKLOADS["tiny"]
+    q_same = np.tile(L.q_base[5], (sh.E, 1))
+    s_same = np.tile(L.s_base[5], (sh.E, 1))
+    lay2 = oracle.Layer(L.x, L.wg, L.bias, q_same, s_same, L.shared_q, L.shared_s, d=sh.d, f=sh.f,
+                        E=sh.E, k=sh.k, G=sh.G, normalize=1, route_scale=1.5, res=lay.res, top_p=p)
+    idx, _, out = lay2.dense()
+    assert (idx == -1).any()          # the cut removes some slots at this p
+    for t in range(sh.T):
+        y = oracle.expert_ffn(L.x[t], L.q_base[5], L.s_base[5], sh.d, sh.f, sh.G)
+        ys = oracle.expert_ffn(L.x[t], L.shared_q, L.shared_s, sh.d, sh.f, sh.G)
+        assert np.allclose(out[t], lay.res[t] + ys + 1.5 * y, rtol=1e-13, atol=1e-13)
+    lay3 = oracle.Layer(L.x, L.wg, L.bias, L.q_base, L.s_base, L.shared_q, L.shared_s, d=sh.d, f=sh.f,
+                        E=sh.E, k=sh.k, G=sh.G, normalize=1, res=lay.res, top_p=p)
+    i3, w3, o3 = lay3.dense()
+    u = lay3.union_path()
+    assert np.array_equal(i3, u["idx"]) and np.array_equal(w3, u["w"]) and np.array_equal(o3, u["out"])
+    assert int(u["counts"].sum()) == int((i3 >= 0).sum())
+
+
+# --------------------------------------------------------- thread count ----
+
+def test_results_do_not_depend_on_thread_count():
+    lay, L = tiny_layer(res=True)
+    sh = workloads.WORKLOADS["tiny"]
+    n0 = oracle.threads()
+    try:
+        oracle.set_threads(1)
+        a = lay.dense()
+        ya = oracle.expert_ffn(L.x[3], L.q_base[2], L.s_base[2], sh.d, sh.f, sh.G)
+        oracle.set_threads(max(2, n0))
+        b = lay.dense()
+        yb = oracle.expert_ffn(L.x[3], L.q_base[2], L.s_base[2], sh.d, sh.f, sh.G)
+        c = lay.tokens(np.array([4], np.int32))   # one token: rows split over the threads
+    finally:
+        oracle.set_threads(n0)
+    assert all(np.array_equal(u, v) for u, v in zip(a, b))
+    assert np.array_equal(ya, yb)
+    assert np.array_equal(c[2][0], a[2][4])
