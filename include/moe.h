@@ -73,6 +73,10 @@ enum {
 /* Bits of the device error word `err`. */
 #define MOE_DEVERR_BAD_EXPERT 0x1   /* an expert id in topk_idx was outside [0, E) */
 #define MOE_DEVERR_TIMEOUT 0x2      /* a bounded pipeline wait gave up; outputs are incomplete */
+#define MOE_DEVERR_SCALE_RANGE 0x4  /* prefill path: a group scale lies more than 2^13 above or 2^14
+                                       below the first group scale of its weight row, beyond what
+                                       the path's fp16 weights hold; that row's outputs lose
+                                       precision (the decode path has no such limit) */
 
 /* FFN execution modes. */
 enum {
@@ -84,15 +88,20 @@ enum {
                               path's precision at every batch size. */
     MOE_MODE_DECODE = 1,   /* fp32-accurate grouped GEMV: exact int4 against activations split
                               into fp16 hi + lo parts, fp32 accumulation */
-    MOE_MODE_PREFILL = 2   /* tcgen05 grouped GEMM on 16-bit operands (fp16 q*s weights, fp16
-                              activations scaled per row by a power of two), fp32 accumulate */
+    MOE_MODE_PREFILL = 2   /* tcgen05 grouped GEMM on 16-bit operands (fp16 q*s weights scaled
+                              per weight row by a power of two, fp16 activations scaled per
+                              row by a power of two), fp32 accumulate.  Scale magnitudes are
+                              free; within one weight row, group scales must stay within
+                              2^-14 .. 2^13 of the row's first group scale (else
+                              MOE_DEVERR_SCALE_RANGE) */
 };
 
 /* Human-readable name of a status code (static string). */
 MOE_API const char *moe_status_str(int status);
 
 /* Decode a device error word copied to the host: MOE_OK when zero, else
- * MOE_ERR_INVALID_ARG for a bad expert id or MOE_ERR_CUDA for a timeout. */
+ * MOE_ERR_CUDA for a timeout, MOE_ERR_INVALID_ARG for a bad expert id,
+ * MOE_ERR_UNSUPPORTED for scales outside the prefill path's range. */
 MOE_API int moe_device_error(int32_t err_word_host);
 
 /* Packed bytes / fp32 scale count of one expert block (layout above). */
@@ -134,6 +143,27 @@ MOE_API int moe_route(const float *x, const float *w_gate, const float *bias, in
               float *topk_w, float *logits, void *stream);
 
 /*
+ * moe_route with top-p pruning of the selection (a lossy mode).
+ * Source: "Public Colibri Observation and Revision Ledger", "Exact-Versus-Lossy
+ * Mode Table" (top-p gating restricts a layer to fewer experts and changes
+ * the output); "Colibri is an open-source, lightweight Mixture-of-Experts",
+ * "Configuration" (the --topp setting reads fewer experts).  The pages give no
+ * formula; the cut taken here:
+ *   s_1 .. s_k  the scores of the k chosen experts in selection order
+ *   m = min { m >= 1 : s_1 + ... + s_m >= top_p * (s_1 + ... + s_k) }
+ *   slots 1..m keep their expert; slots m+1..k get topk_idx = -1, topk_w = 0
+ *   normalize != 0: topk_w = route_scale * s_j / (s_1 + ... + s_m) over kept slots
+ * The sums are fp32 (a warp scan, not left to right), so a token whose cut
+ * falls within rounding of top_p * total may keep one expert more or fewer
+ * than an exact evaluation.  top_p >= 1 gives exactly moe_route's result.
+ * An id of -1 in topk_idx is an empty slot for moe_union and moe_combine.
+ * Errors: as moe_route; MOE_ERR_INVALID_ARG when top_p <= 0 or not finite.
+ */
+MOE_API int moe_route_topp(const float *x, const float *w_gate, const float *bias, int T, int d,
+                           int E, int k, int normalize, float route_scale, float top_p,
+                           int32_t *topk_idx, float *topk_w, float *logits, void *stream);
+
+/*
  * Union: merge the routed (token, slot) pairs of the batch so each unique
  * expert is read once, and group the pairs by expert.
  * Source: same page and section (the Union stage combines the expert requests
@@ -145,13 +175,17 @@ MOE_API int moe_route(const float *x, const float *w_gate, const float *bias, in
  *   counts [E]        number of pairs routed to each expert
  *   offsets [E+1]     exclusive scan of counts over ascending expert id
  *   sorted_pair [T*k] pairs ordered by (expert, p): expert e's pairs occupy
- *                     positions offsets[e] .. offsets[e+1]-1, tokens ascending
+ *                     positions offsets[e] .. offsets[e+1]-1, tokens ascending;
+ *                     positions from offsets[E] on (left when slots are empty
+ *                     or bad) are unspecified
  *   perm [T*k]        perm[p] = position of pair p in sorted_pair
  *   uniq [E]          experts with counts > 0, ascending; entries >= n_uniq unspecified
  *   n_uniq [1]        number of such experts
  * hits [E] uint64 or NULL: when given, hits[e] += counts[e] (the Learn stage,
- * fused; see moe_hits).  A pair whose id is outside [0, E) sets
- * MOE_DEVERR_BAD_EXPERT in *err, gets perm[p] = -1 and is left out.
+ * fused; see moe_hits).  An id of -1 is an empty slot (pruned by
+ * moe_route_topp): perm[p] = -1, no group, no hit, no error.  Any other id
+ * outside [0, E) sets MOE_DEVERR_BAD_EXPERT in *err, gets perm[p] = -1 and is
+ * left out.
  * Runs in one thread block; T*k <= 1<<22.
  */
 MOE_API int moe_union(const int32_t *topk_idx, int T, int k, int E, int32_t *counts,
@@ -257,6 +291,14 @@ MOE_API int moe_layer_forward(const float *x, const float *w_gate, const float *
                       int normalize, float route_scale, int mode, float *out,
                       int32_t *topk_idx, float *topk_w, uint64_t *hits, void *workspace,
                       size_t ws_bytes, int32_t *err, void *stream);
+
+/* moe_layer_forward with moe_route_topp's pruning (top_p >= 1: identical to
+ * moe_layer_forward).  Empty slots add nothing to the output or the hits. */
+MOE_API int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bias,
+                                   const moe_layer_int4 *w, const float *residual, int T, int k,
+                                   int normalize, float route_scale, float top_p, int mode,
+                                   float *out, int32_t *topk_idx, float *topk_w, uint64_t *hits,
+                                   void *workspace, size_t ws_bytes, int32_t *err, void *stream);
 
 MOE_API size_t moe_layer_workspace_bytes(int T, int k, int E, int d, int f, int mode);
 

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libmoe.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = 0, -1, -2, -3, -4
-MOE_DEVERR_BAD_EXPERT, MOE_DEVERR_TIMEOUT = 0x1, 0x2
+MOE_DEVERR_BAD_EXPERT, MOE_DEVERR_TIMEOUT, MOE_DEVERR_SCALE_RANGE = 0x1, 0x2, 0x4
 MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL = 0, 1, 2
 
 _HITS_DTYPES = tuple(getattr(torch, n) for n in ("int64", "uint64") if hasattr(torch, n))
@@ -45,6 +45,7 @@ _SIGNATURES = {
     "moe_expert_q_bytes": ([_I, _I], _SZ),
     "moe_expert_s_count": ([_I, _I, _I], _SZ),
     "moe_route": ([_P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P], _I),
+    "moe_route_topp": ([_P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _P, _P, _P, _P], _I),
     "moe_union": ([_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_hits": ([_P, _I, _P, _P], _I),
     "moe_expert_ffn_int4": ([_P, ctypes.POINTER(moe_layer_int4), _P, _P, _P, _P, _I, _I, _I, _P, _P,
@@ -56,6 +57,8 @@ _SIGNATURES = {
     "moe_rms_norm": ([_P, _I, _I, _F, _P, _P], _I),
     "moe_layer_forward": ([_P, _P, _P, ctypes.POINTER(moe_layer_int4), _P, _I, _I, _I, _F, _I, _P, _P,
                            _P, _P, _P, _SZ, _P, _P], _I),
+    "moe_layer_forward_topp": ([_P, _P, _P, ctypes.POINTER(moe_layer_int4), _P, _I, _I, _I, _F, _F, _I, _P,
+                                _P, _P, _P, _P, _SZ, _P, _P], _I),
     "moe_layer_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
 }
 
@@ -132,7 +135,8 @@ class LayerWeights:
 
 
 def moe_route(x, w_gate, bias, k: int, normalize: int = 1, route_scale: float = 1.0,
-              topk_idx=None, topk_w=None, logits=None, stream=None):
+              topk_idx=None, topk_w=None, logits=None, stream=None, top_p: float | None = None):
+    """moe_route, or moe_route_topp when top_p is given."""
     _need(x, torch.float32, "x")
     _need(w_gate, torch.float32, "w_gate")
     T, d = x.shape
@@ -143,8 +147,13 @@ def moe_route(x, w_gate, bias, k: int, normalize: int = 1, route_scale: float = 
     topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
     topk_w = torch.empty((T, k), dtype=torch.float32, device=dev) if topk_w is None else topk_w
     logits = torch.empty((T, E), dtype=torch.float32, device=dev) if logits is None else logits
-    _check(lib().moe_route(_p(x), _p(w_gate), _p(bias), T, d, E, k, int(normalize), float(route_scale),
-                           _p(topk_idx), _p(topk_w), _p(logits), _stream(stream)), "moe_route")
+    if top_p is None:
+        _check(lib().moe_route(_p(x), _p(w_gate), _p(bias), T, d, E, k, int(normalize), float(route_scale),
+                               _p(topk_idx), _p(topk_w), _p(logits), _stream(stream)), "moe_route")
+    else:
+        _check(lib().moe_route_topp(_p(x), _p(w_gate), _p(bias), T, d, E, k, int(normalize), float(route_scale),
+                                    float(top_p), _p(topk_idx), _p(topk_w), _p(logits), _stream(stream)),
+               "moe_route_topp")
     return topk_idx, topk_w, logits
 
 
@@ -266,7 +275,9 @@ def moe_rms_norm(x, eps: float = 1e-5, out=None, stream=None):
 
 def moe_layer_forward(x, w_gate, bias, layer: LayerWeights, k: int, normalize: int = 1,
                       route_scale: float = 1.0, mode: int = MOE_MODE_AUTO, residual=None, out=None,
-                      topk_idx=None, topk_w=None, hits=None, ws=None, err=None, stream=None):
+                      topk_idx=None, topk_w=None, hits=None, ws=None, err=None, stream=None,
+                      top_p: float | None = None):
+    """moe_layer_forward, or moe_layer_forward_topp when top_p is given."""
     _need(x, torch.float32, "x")
     T, d = x.shape
     dev = x.device
@@ -276,9 +287,15 @@ def moe_layer_forward(x, w_gate, bias, layer: LayerWeights, k: int, normalize: i
     if err is None:
         err = torch.zeros(1, dtype=torch.int32, device=dev)
     wp, wn = _ws_ptr(ws)
-    _check(lib().moe_layer_forward(_p(x), _p(w_gate), _p(bias), ctypes.byref(layer.c), _p(residual), T, k,
-                                   int(normalize), float(route_scale), mode, _p(out), _p(topk_idx), _p(topk_w),
-                                   _p(hits), wp, wn, _p(err), _stream(stream)), "moe_layer_forward")
+    if top_p is None:
+        _check(lib().moe_layer_forward(_p(x), _p(w_gate), _p(bias), ctypes.byref(layer.c), _p(residual), T, k,
+                                       int(normalize), float(route_scale), mode, _p(out), _p(topk_idx),
+                                       _p(topk_w), _p(hits), wp, wn, _p(err), _stream(stream)), "moe_layer_forward")
+    else:
+        _check(lib().moe_layer_forward_topp(_p(x), _p(w_gate), _p(bias), ctypes.byref(layer.c), _p(residual), T,
+                                            k, int(normalize), float(route_scale), float(top_p), mode, _p(out),
+                                            _p(topk_idx), _p(topk_w), _p(hits), wp, wn, _p(err),
+                                            _stream(stream)), "moe_layer_forward_topp")
     return out, err
 
 

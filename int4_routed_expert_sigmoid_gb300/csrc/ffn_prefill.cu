@@ -40,10 +40,14 @@
 //  * warps 2-5 (epilogue, one TMEM subpartition each): gate/up -> a gate lane
 //    and its up lane swap one value per token pair with a shuffle and form
 //    h = silu(g) * u in fp32; down -> y in fp32.
-//  * precision: both GEMMs run on fp16 operands, weights fp16(q * s) and
-//    activations scaled per row by a power of two so that |v| < 2^14 (the
-//    factor is applied to the fp32 result); fp32 accumulation, round to
-//    nearest even.  h is written in fp32, then a small kernel finds each
+//  * precision: both GEMMs run on fp16 operands, weights fp16(q * s * 2^-e_r)
+//    with e_r the binary exponent of the first group scale of weight row r (so
+//    the row's first group has |s * 2^-e_r| in [1, 2) whatever the absolute
+//    size of the scales), and activations scaled per row by a power of two so
+//    that |v| < 2^14; both factors are applied to the fp32 result.  A group
+//    scale more than 2^13 above or 2^14 below its row's first scale would
+//    overflow or lose bits in fp16: it sets MOE_DEVERR_SCALE_RANGE.  fp32
+//    accumulation, round to nearest even.  h is written in fp32, then a small kernel finds each
 //    row's max |h| and writes the scaled fp16 rows the down GEMM reads.
 //    (bf16 h and weights for the down GEMM would skip that pass, but their
 //    rounding alone uses up the prefill tolerance of 2e-2 of the output RMS.)
@@ -120,6 +124,11 @@ struct PMaps {
 
 struct PParams {
     const int32_t *offsets, *uniq, *n_uniq;
+    // first-group scale of each weight row, read by the epilogue for the row's power-of-two
+    // factor: expert block base + s_off0 + matrix * s_mat + row * s_row
+    const float *s_routed, *s_shared;
+    uint64_t s_expert, s_off0, s_mat;
+    int s_row;
     const float *row_scale;       // power-of-two factor of each sorted activation row (x or h)
     float *h32;                   // gate/up: h [rows][f] fp32, natural order
     float *y_pair, *y_shared;     // down outputs
@@ -249,6 +258,21 @@ __device__ __forceinline__ uint32_t mul_x2(uint32_t a, uint32_t b)
         asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
+
+// Power-of-two shift of a weight row: s0 * 2^shift in [1, 2) for the row's first group scale s0,
+// read from its fp32 exponent field (0 when s0 is 0 or not finite; clamped to [-126, 126] so that
+// 2^shift and 2^-shift are normal fp32; subnormal s0 take 126).
+__device__ __forceinline__ int row_shift(float s0)
+{
+    const uint32_t bits = __float_as_uint(s0) & 0x7fffffffu;
+    const int biased = (int)(bits >> 23);
+    if (bits == 0u || biased == 255)
+        return 0;
+    return min(max(127 - biased, -126), 126);
+}
+
+// 2^n for n in [-126, 127], exactly.
+__device__ __forceinline__ float pow2i(int n) { return __uint_as_float((uint32_t)(127 + n) << 23); }
 
 template <bool F16>
 __device__ __forceinline__ uint32_t pack_scale(float s)
@@ -387,6 +411,8 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
         int rs = 0;
         uint32_t rph = 0;
         uint32_t kop = g;   // global index of this group's next op stage
+        float rowfac = 1.0f;   // 2^shift of this thread's weight row (set from the item's first raw stage)
+        bool range_bad = false;
         for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
             for (int rr = 0; rr < nraw; rr++) {
                 if (!abort_flag && !mbar_wait(smem_addr(&raw_full[rs]), rph)) {
@@ -402,11 +428,15 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                 const int sw = RAWK == 256 ? (r & 7) : ((r >> 1) & 3);
                 uint4 wv[C::kCPO];
                 float sg[C::kCPO];
+                if (rr == 0)
+                    rowfac = pow2i(row_shift(srow[0]));
 #pragma unroll
                 for (int q = 0; q < C::kCPO; q++) {
                     const int c = g * C::kCPO + q;
                     wv[q] = *reinterpret_cast<const uint4 *>(qrow + ((c ^ sw) << 4));
-                    sg[q] = srow[c];
+                    sg[q] = srow[c] * rowfac;   // exact: a power of two
+                    const float a = fabsf(sg[q]);
+                    range_bad |= a > 0.f && (a < 0x1p-14f || a > 8192.0f);
                 }
                 if (!abort_flag)
                     mbar_arrive(smem_addr(&raw_empty[rs]));   // the raw stage is in registers now
@@ -446,6 +476,8 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                 }
             }
         }
+        if (range_bad)
+            atomicOr(p.err, MOE_DEVERR_SCALE_RANGE);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------ MMA issue
         // The whole warp runs the loop and one elected lane issues each MMA and commit: the
@@ -526,6 +558,12 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
             for (int q = lane; q < it.ntok; q += 32)
                 rsc[q] = p.row_scale[it.row0 + it.tok0 + q];
             __syncwarp();
+            // this lane's weight row and the power of two its dequantised weights were scaled by
+            const int wrow = MODE == kPGateUp ? it.mtile * 64 + sub * 16 + (lane & 15) : it.mtile * kTileM + sub * 32 + lane;
+            const int wmat = MODE == kPGateUp ? (lane >> 4) : 0;
+            const float *sbase = it.expert < 0 ? p.s_shared : p.s_routed + (size_t)it.expert * p.s_expert;
+            const float ef = pow2i(-row_shift(__ldg(sbase + p.s_off0 + (size_t)wmat * p.s_mat +
+                                                    (size_t)wrow * p.s_row)));
             if (!abort_flag && !mbar_wait(smem_addr(&acc_full[b]), fph[b])) {
                 atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                 abort_flag = 1;
@@ -546,9 +584,9 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                     const int hr = it.mtile * 64 + sub * 16 + (lane & 15);   // column of h
 #pragma unroll
                     for (int q = 0; q < 8; q++) {
-                        const float mine = __uint_as_float(hi ? v[2 * q + 1] : v[2 * q]);
+                        const float mine = __uint_as_float(hi ? v[2 * q + 1] : v[2 * q]) * ef;
                         const float other = __shfl_xor_sync(0xffffffffu,
-                                                            __uint_as_float(hi ? v[2 * q] : v[2 * q + 1]), 16);
+                                                            __uint_as_float(hi ? v[2 * q] : v[2 * q + 1]) * ef, 16);
                         const int jj = 2 * q + hi;
                         if (jj < nj) {
                             const float rf = rsc[c0 + jj];
@@ -567,7 +605,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                             break;
                         const float rf = rsc[c0 + jj];
                         const int tok = it.tok0 + c0 + jj;
-                        const float yv = __uint_as_float(v[jj]) * rf;
+                        const float yv = __uint_as_float(v[jj]) * ef * rf;
                         if (it.expert < 0)
                             p.y_shared[(size_t)tok * p.out_rows + orow] = yv;
                         else if (p.y_pair16)
@@ -599,30 +637,41 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
 // Token rows in expert order as fp16, permuted within each 8 like the weights
 // and scaled per row by a power of two 2^(14-e) (|value| < 2^14; row_scale
 // keeps 2^(e-14)): row p < T*k is x[sorted_pair[p] / k], row T*k + t is x[t].
-// pair_pos_kernel inverts sorted_pair (pos[q] = p for q = sorted_pair[p]);
-// token_rows_kernel then converts each token once (one block of 256 threads)
-// and writes the result to the token's k pair rows and its shared-expert row.
+// pair_pos_kernel inverts sorted_pair over its n_valid = offsets[E] valid
+// positions (pos[q] = p for q = sorted_pair[p]); token_rows_kernel then
+// converts each token once (one block of 256 threads) and writes the result to
+// the token's pair rows and its shared-expert row.  A slot that joined no
+// group (an empty slot, id -1, or a bad id) has no valid position: pos[q] is
+// then whatever an earlier call left there, so a slot counts as placed only
+// when pos[q] is a valid position whose sorted_pair entry is q itself.
 __global__ void __launch_bounds__(256)
-pair_pos_kernel(const int32_t *__restrict__ sorted_pair, int P, int32_t *__restrict__ pos)
+pair_pos_kernel(const int32_t *__restrict__ sorted_pair, const int32_t *__restrict__ offsets, int E,
+                int32_t *__restrict__ pos)
 {
     griddep_launch_dependents();
     griddep_wait();
     const int p = blockIdx.x * 256 + threadIdx.x;
-    if (p < P)
+    if (p < offsets[E])
         pos[sorted_pair[p]] = p;
 }
 
 __global__ void __launch_bounds__(256)
-token_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ pos, int T, int k, int K,
-                  uint16_t *__restrict__ out, float *__restrict__ row_scale)
+token_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ pos,
+                  const int32_t *__restrict__ sorted_pair, const int32_t *__restrict__ offsets, int E, int T,
+                  int k, int K, uint16_t *__restrict__ out, float *__restrict__ row_scale)
 {
     __shared__ float wmax[8];
     __shared__ int dst[33];
     griddep_launch_dependents();
     griddep_wait();
     const int t = blockIdx.x;
-    if (threadIdx.x <= k)
-        dst[threadIdx.x] = threadIdx.x < k ? pos[(size_t)t * k + threadIdx.x] : T * k + t;
+    if (threadIdx.x < k) {
+        const int q = t * k + threadIdx.x;
+        const int v = pos[q];
+        dst[threadIdx.x] = (v >= 0 && v < offsets[E] && sorted_pair[v] == q) ? v : -1;
+    } else if (threadIdx.x == k) {
+        dst[k] = T * k + t;
+    }
     const float *xr = x + (size_t)t * K;
     float mx = 0.f;
     for (int i = threadIdx.x; i < K / 4; i += 256) {
@@ -642,7 +691,7 @@ token_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ pos, 
     int e = 0;
     frexpf(mx, &e);
     const float up = mx > 0.f ? ldexpf(1.0f, 14 - e) : 1.0f;
-    if (threadIdx.x <= k)
+    if (threadIdx.x <= k && dst[threadIdx.x] >= 0)
         row_scale[dst[threadIdx.x]] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
     for (int c = threadIdx.x; c < K / 8; c += 256) {
         const float4 *sp = reinterpret_cast<const float4 *>(xr + c * 8);
@@ -654,7 +703,8 @@ token_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ pos, 
             o[frag_pos8(el)] = __half_as_ushort(__float2half_rn(v[el] * up));
         const uint4 ov = *reinterpret_cast<const uint4 *>(o);
         for (int j = 0; j <= k; j++)
-            *reinterpret_cast<uint4 *>(out + (size_t)dst[j] * K + c * 8) = ov;
+            if (dst[j] >= 0)
+                *reinterpret_cast<uint4 *>(out + (size_t)dst[j] * K + c * 8) = ov;
     }
 }
 
@@ -782,10 +832,10 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     int rc = MOE_OK;
 
     // fp16 token rows: each token converted once and written to its pair rows and shared row
-    rc = launch_pdl(pair_pos_kernel, (T * k + 255) / 256, 256, 0, s, a.sorted_pair, T * k, ps.pos);
+    rc = launch_pdl(pair_pos_kernel, (T * k + 255) / 256, 256, 0, s, a.sorted_pair, a.offsets, E, ps.pos);
     if (rc == MOE_OK)
-        rc = launch_pdl(token_rows_kernel, T, 256, 0, s, a.x, (const int32_t *)ps.pos, T, k, d, x_sorted,
-                        row_scale);
+        rc = launch_pdl(token_rows_kernel, T, 256, 0, s, a.x, (const int32_t *)ps.pos, a.sorted_pair, a.offsets, E,
+                        T, k, d, x_sorted, row_scale);
     if (rc != MOE_OK)
         return rc;
 
@@ -814,6 +864,12 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pg.offsets = a.offsets;
     pg.uniq = a.uniq;
     pg.n_uniq = a.n_uniq;
+    pg.s_routed = w.s_base;
+    pg.s_shared = w.shared_s;
+    pg.s_expert = sc;
+    pg.s_off0 = 0;
+    pg.s_mat = (uint64_t)f * (d / G);
+    pg.s_row = d / G;
     pg.row_scale = row_scale;
     pg.h32 = ps.h32;
     pg.err = a.err;
@@ -844,6 +900,9 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     if (rc != MOE_OK)
         return MOE_ERR_INVALID_ARG;
     PParams pd = pg;
+    pd.s_off0 = (uint64_t)2 * f * (d / G);
+    pd.s_mat = 0;
+    pd.s_row = f / G;
     pd.h32 = nullptr;
     pd.row_scale = ps.h_scale;
     pd.y_pair = a.y_pair;

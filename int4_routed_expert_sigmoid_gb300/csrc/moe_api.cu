@@ -17,6 +17,9 @@ inline bool ok_ptr(const void *p) { return p != nullptr && aligned16(p); }
 inline bool ok_opt(const void *p) { return p == nullptr || aligned16(p); }
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// top_p in (0, 1]; 1 (or more) keeps all k experts
+bool ok_top_p(float top_p) { return top_p > 0.0f && top_p < 3.0e38f; }
+
 bool ok_route_shape(int T, int d, int E, int k)
 {
     return T >= 1 && d >= 4 && d % 4 == 0 && E >= 1 && E <= 1024 && k >= 1 && k <= 32 && k <= E;
@@ -136,25 +139,35 @@ int moe_device_error(int32_t err)
         return MOE_OK;
     if (err & MOE_DEVERR_TIMEOUT)
         return MOE_ERR_CUDA;
-    return MOE_ERR_INVALID_ARG;
+    if (err & MOE_DEVERR_BAD_EXPERT)
+        return MOE_ERR_INVALID_ARG;
+    return MOE_ERR_UNSUPPORTED;
 }
 
 size_t moe_expert_q_bytes(int d, int f) { return (size_t)3 * d * f / 2; }
 
 size_t moe_expert_s_count(int d, int f, int G) { return G > 0 ? (size_t)3 * d * f / G : 0; }
 
-int moe_route(const float *x, const float *w_gate, const float *bias, int T, int d, int E, int k,
-              int normalize, float route_scale, int32_t *topk_idx, float *topk_w, float *logits,
-              void *stream)
+int moe_route_topp(const float *x, const float *w_gate, const float *bias, int T, int d, int E, int k,
+                   int normalize, float route_scale, float top_p, int32_t *topk_idx, float *topk_w,
+                   float *logits, void *stream)
 {
     if (!ok_ptr(x) || !ok_ptr(w_gate) || !ok_opt(bias) || !ok_ptr(topk_idx) || !ok_ptr(topk_w) ||
-        !ok_ptr(logits) || !ok_route_shape(T, d, E, k))
+        !ok_ptr(logits) || !ok_route_shape(T, d, E, k) || !ok_top_p(top_p))
         return MOE_ERR_INVALID_ARG;
     const cudaStream_t s = as_stream(stream);
     int rc = launch_router_logits(x, w_gate, T, d, E, logits, s);
     if (rc == MOE_OK)
-        rc = launch_router_topk(logits, bias, T, E, k, normalize, route_scale, topk_idx, topk_w, s);
+        rc = launch_router_topk(logits, bias, T, E, k, normalize, route_scale, top_p, topk_idx, topk_w, s);
     return rc;
+}
+
+int moe_route(const float *x, const float *w_gate, const float *bias, int T, int d, int E, int k,
+              int normalize, float route_scale, int32_t *topk_idx, float *topk_w, float *logits,
+              void *stream)
+{
+    return moe_route_topp(x, w_gate, bias, T, d, E, k, normalize, route_scale, 1.0f, topk_idx, topk_w, logits,
+                          stream);
 }
 
 int moe_union(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
@@ -272,6 +285,16 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
                       float route_scale, int mode, float *out, int32_t *topk_idx, float *topk_w,
                       uint64_t *hits, void *workspace, size_t ws_bytes, int32_t *err, void *stream)
 {
+    return moe_layer_forward_topp(x, w_gate, bias, w, residual, T, k, normalize, route_scale, 1.0f, mode, out,
+                                  topk_idx, topk_w, hits, workspace, ws_bytes, err, stream);
+}
+
+int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bias,
+                           const moe_layer_int4 *w, const float *residual, int T, int k, int normalize,
+                           float route_scale, float top_p, int mode, float *out, int32_t *topk_idx,
+                           float *topk_w, uint64_t *hits, void *workspace, size_t ws_bytes, int32_t *err,
+                           void *stream)
+{
     int rc = check_layer(w);
     if (rc != MOE_OK)
         return rc;
@@ -280,7 +303,7 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
         !ok_opt(topk_idx) || !ok_opt(topk_w) || !ok_opt(hits) || !ok_ptr(err) ||
         workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
         return MOE_ERR_INVALID_ARG;
-    if (!ok_route_shape(T, d, E, k) || (long long)T * (k + 1) > (1LL << 22))
+    if (!ok_route_shape(T, d, E, k) || (long long)T * (k + 1) > (1LL << 22) || !ok_top_p(top_p))
         return MOE_ERR_INVALID_ARG;
     if (!valid_mode(mode))
         return MOE_ERR_INVALID_ARG;
@@ -295,7 +318,7 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
     if (mode == MOE_MODE_PREFILL) {
         rc = launch_router_logits(x, w_gate, T, d, E, sc.logits, s);
         if (rc == MOE_OK)
-            rc = launch_router_topk(sc.logits, bias, T, E, k, normalize, route_scale, idx, wt, s);
+            rc = launch_router_topk(sc.logits, bias, T, E, k, normalize, route_scale, top_p, idx, wt, s);
         if (rc == MOE_OK)
             rc = launch_union(idx, T, k, E, sc.counts, sc.offsets, sc.perm, sc.sorted_pair, sc.uniq,
                               sc.n_uniq, hits, err, s);
@@ -332,12 +355,12 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
     if (small) {
         rc = launch_router_logits_frag(x, w_gate, T, d, E, sc.logits, fs.x_frag, fs.x_scale, s);
         if (rc == MOE_OK)
-            rc = launch_select_union(sc.logits, bias, T, E, k, normalize, route_scale, idx, wt, sc.counts,
+            rc = launch_select_union(sc.logits, bias, T, E, k, normalize, route_scale, top_p, idx, wt, sc.counts,
                                      sc.offsets, sc.perm, sc.sorted_pair, sc.uniq, sc.n_uniq, hits, err, s);
     } else {
         rc = launch_router_logits(x, w_gate, T, d, E, sc.logits, s);
         if (rc == MOE_OK)
-            rc = launch_router_topk(sc.logits, bias, T, E, k, normalize, route_scale, idx, wt, s);
+            rc = launch_router_topk(sc.logits, bias, T, E, k, normalize, route_scale, top_p, idx, wt, s);
         if (rc == MOE_OK)
             rc = launch_union(idx, T, k, E, sc.counts, sc.offsets, sc.perm, sc.sorted_pair, sc.uniq,
                               sc.n_uniq, hits, err, s);

@@ -78,19 +78,20 @@ int launch_router_logits(const float *x, const float *wg, int T, int d, int E, f
 // logits plus the FFN fragments of x in one kernel (T <= 8)
 int launch_router_logits_frag(const float *x, const float *wg, int T, int d, int E, float *logits,
                               uint8_t *frag, float *row_scale, cudaStream_t s);
+// top_p >= 1: plain top-k; below, the pruned slots get id -1 and weight 0
 int launch_router_topk(const float *logits, const float *bias, int T, int E, int k, int normalize,
-                       float route_scale, int32_t *idx, float *w, cudaStream_t s);
+                       float route_scale, float top_p, int32_t *idx, float *w, cudaStream_t s);
 // fragments (GPC = 8) of `rows` rows of x [rows][K], K a multiple of 256
 int launch_act_frag(const float *x, int rows, int K, uint8_t *frag, float *row_scale, cudaStream_t s);
 
-// union.cu
+// union.cu (an id of -1 is an empty slot: no group, perm -1, no hit, no error)
 int launch_union(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
                  int32_t *perm, int32_t *sorted_pair, int32_t *uniq, int32_t *n_uniq,
                  uint64_t *hits, int32_t *err, cudaStream_t s);
 int launch_hits(const int32_t *counts, int E, uint64_t *hits, cudaStream_t s);
 // top-k + union + hits in one block (T <= 8, T*k <= 64)
 int launch_select_union(const float *logits, const float *bias, int T, int E, int k, int normalize,
-                        float route_scale, int32_t *idx, float *w, int32_t *counts, int32_t *offsets,
+                        float route_scale, float top_p, int32_t *idx, float *w, int32_t *counts, int32_t *offsets,
                         int32_t *perm, int32_t *sorted_pair, int32_t *uniq, int32_t *n_uniq,
                         uint64_t *hits, int32_t *err, cudaStream_t s);
 

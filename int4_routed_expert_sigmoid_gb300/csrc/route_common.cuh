@@ -5,7 +5,11 @@
 // and Data-Flow Reconstruction" (sigmoid router scores every expert; the top
 // experts are selected).  Key = sigmoid(l) + bias (bias selects only), order
 // key descending with ties to the lower expert id; weights are the sigmoid
-// scores, optionally renormalised to route_scale.
+// scores, optionally renormalised to route_scale.  top_p < 1 keeps only the
+// shortest prefix of the k chosen slots whose scores reach top_p times the
+// scores of all k (the lossy top-p gating of the Ledger's "Exact-Versus-Lossy
+// Mode Table", the `--topp` setting of the summary page's "Configuration");
+// the other slots are emptied (id -1, weight 0).
 #pragma once
 #include <cfloat>
 #include <climits>
@@ -40,13 +44,15 @@ __host__ __device__ constexpr size_t topk_smem_bytes(int E, int k)
 //     first k (at most) become candidates -- every expert of the overall top-k
 //     is among its block's top-k;
 //  3. every candidate is ranked among its token's candidates (one thread
-//     each); rank j < k fills slot j; one warp per token forms the weights.
+//     each); rank j < k fills slot j; one warp per token forms the weights
+//     (and, with top_p < 1, cuts the slots: slot j stays when the scores of
+//     slots 0 .. j-1 add up to less than top_p times the scores of all k).
 // Writes idx/w rows of the tokens and, when sel is not null, the ids to
 // sel[(t - t0) * k + j].  Called by all threads of the block (it synchronises).
 __device__ __forceinline__ void topk_block(const float *__restrict__ logits, const float *__restrict__ bias,
                                            int t0, int nt, int E, int k, int normalize, float route_scale,
-                                           int32_t *__restrict__ idx, float *__restrict__ w, int *sel,
-                                           uint8_t *smem)
+                                           float top_p, int32_t *__restrict__ idx, float *__restrict__ w,
+                                           int *sel, uint8_t *smem)
 {
     float *keys = reinterpret_cast<float *>(smem);                   // [8][E]
     int *cand = reinterpret_cast<int *>(smem + (size_t)kTopkTokens * E * 4);
@@ -96,8 +102,25 @@ __device__ __forceinline__ void topk_block(const float *__restrict__ logits, con
     __syncthreads();
     if (warp < nt) {
         const int t = warp;
-        const int my_e = lane < k ? cand[t * stride + nc + lane] : 0;
-        const float my_s = lane < k ? router_score(logits[(size_t)(t0 + t) * E + my_e]) : 0.0f;
+        int my_e = lane < k ? cand[t * stride + nc + lane] : 0;
+        float my_s = lane < k ? router_score(logits[(size_t)(t0 + t) * E + my_e]) : 0.0f;
+        if (top_p < 1.0f) {
+            // exclusive prefix of the scores in slot order, and their total
+            float inc = my_s;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float v = __shfl_up_sync(0xffffffffu, inc, off);
+                if (lane >= off)
+                    inc += v;
+            }
+            const float total = __shfl_sync(0xffffffffu, inc, 31);
+            float excl = __shfl_up_sync(0xffffffffu, inc, 1);
+            excl = lane == 0 ? 0.0f : excl;
+            if (!(excl < top_p * total)) {   // slots from the first one past the cut
+                my_e = -1;
+                my_s = 0.0f;
+            }
+        }
         float scale = 1.0f;
         if (normalize) {
             float sum = my_s;

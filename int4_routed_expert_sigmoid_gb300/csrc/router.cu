@@ -407,12 +407,12 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
 // One block per 8 tokens (see topk_block).
 __global__ void __launch_bounds__(kTopkThreads)
 topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int k,
-            int normalize, float route_scale, int32_t *__restrict__ idx, float *__restrict__ w)
+            int normalize, float route_scale, float top_p, int32_t *__restrict__ idx, float *__restrict__ w)
 {
     extern __shared__ __align__(16) uint8_t tk_smem[];
     const int t0 = blockIdx.x * kTopkTokens;
     const int nt = min(kTopkTokens, T - t0);
-    topk_block(logits, bias, t0, nt, E, k, normalize, route_scale, idx, w, nullptr, tk_smem);
+    topk_block(logits, bias, t0, nt, E, k, normalize, route_scale, top_p, idx, w, nullptr, tk_smem);
 }
 
 // --------------------------------------------------------- act fragments ---
@@ -563,14 +563,14 @@ int launch_router_logits_frag(const float *x, const float *wg, int T, int d, int
 }
 
 int launch_router_topk(const float *logits, const float *bias, int T, int E, int k, int normalize,
-                       float route_scale, int32_t *idx, float *w, cudaStream_t s)
+                       float route_scale, float top_p, int32_t *idx, float *w, cudaStream_t s)
 {
     const size_t smem = topk_smem_bytes(E, k);
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MOE_ERR_CUDA;
     topk_kernel<<<(T + kTopkTokens - 1) / kTopkTokens, kTopkThreads, smem, s>>>(logits, bias, T, E, k, normalize,
-                                                                               route_scale, idx, w);
+                                                                               route_scale, top_p, idx, w);
     return cuda_status(cudaGetLastError());
 }
 

@@ -77,10 +77,10 @@ __device__ void union_chunked(const int32_t *__restrict__ idx, int P, int E, int
     int bad = 0;
     for (int p = tid; p < P; p += kThreads) {
         const int e = idx[p];
-        if (e < 0 || e >= E)
-            bad = 1;
-        else
+        if (e >= 0 && e < E)
             atomicAdd(&cnt[e], 1);
+        else if (e != -1)   // -1: an empty slot
+            bad = 1;
     }
     if (__syncthreads_or(bad) && tid == 0)
         atomicOr(err, MOE_DEVERR_BAD_EXPERT);
@@ -205,7 +205,7 @@ union_kernel(const int32_t *__restrict__ idx, int T, int k, int E, int use_bitma
     for (int p = tid; p < P; p += kThreads) {
         const int e = idx[p];
         if (e < 0 || e >= E) {
-            bad = 1;
+            bad |= e != -1 ? 1 : 0;   // -1: an empty slot
             continue;
         }
         const int t = p / k;
@@ -282,7 +282,8 @@ constexpr int kSelMaxPairs = 64;
 
 __global__ void __launch_bounds__(kSelThreads)
 select_union_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int k,
-                    int normalize, float route_scale, int32_t *__restrict__ idx, float *__restrict__ w,
+                    int normalize, float route_scale, float top_p, int32_t *__restrict__ idx,
+                    float *__restrict__ w,
                     int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
                     int32_t *__restrict__ sorted_pair, int32_t *__restrict__ uniq,
                     int32_t *__restrict__ n_uniq, uint64_t *__restrict__ hits, int32_t *__restrict__ err)
@@ -293,12 +294,13 @@ select_union_kernel(const float *__restrict__ logits, const float *__restrict__ 
     const int tid = threadIdx.x;
     griddep_launch_dependents();
     griddep_wait();   // logits come from the previous kernel
-    topk_block(logits, bias, 0, T, E, k, normalize, route_scale, idx, w, se, tk_smem);
+    topk_block(logits, bias, 0, T, E, k, normalize, route_scale, top_p, idx, w, se, tk_smem);
     const int P = T * k;
     if (tid < P) {
         const int e = se[tid];
         if (e < 0 || e >= E) {
-            atomicOr(err, MOE_DEVERR_BAD_EXPERT);
+            if (e != -1)   // -1: a slot emptied by top-p
+                atomicOr(err, MOE_DEVERR_BAD_EXPERT);
             se[tid] = INT_MAX;
         }
     }
@@ -382,7 +384,7 @@ int launch_union(const int32_t *idx, int T, int k, int E, int32_t *counts, int32
 }
 
 int launch_select_union(const float *logits, const float *bias, int T, int E, int k, int normalize,
-                        float route_scale, int32_t *idx, float *w, int32_t *counts, int32_t *offsets,
+                        float route_scale, float top_p, int32_t *idx, float *w, int32_t *counts, int32_t *offsets,
                         int32_t *perm, int32_t *sorted_pair, int32_t *uniq, int32_t *n_uniq,
                         uint64_t *hits, int32_t *err, cudaStream_t s)
 {
@@ -393,7 +395,7 @@ int launch_select_union(const float *logits, const float *bias, int T, int E, in
                                                   (int)smem) != cudaSuccess)
         return MOE_ERR_CUDA;
     return launch_pdl(select_union_kernel, 1, kSelThreads, smem, s, logits, bias, T, E, k, normalize, route_scale,
-                      idx, w, counts, offsets, perm, sorted_pair, uniq, n_uniq, hits, err);
+                      top_p, idx, w, counts, offsets, perm, sorted_pair, uniq, n_uniq, hits, err);
 }
 
 int launch_hits(const int32_t *counts, int E, uint64_t *hits, cudaStream_t s)

@@ -39,11 +39,12 @@ def device_layer(L: workloads.LayerInputs, device="cuda"):
     return dict(x=t(L.x), wg=t(L.wg), bias=None if L.bias is None else t(L.bias), layer=lw)
 
 
-def oracle_layer(L: workloads.LayerInputs, *, k=None, normalize=1, route_scale=1.0, res=None, x=None):
+def oracle_layer(L: workloads.LayerInputs, *, k=None, normalize=1, route_scale=1.0, res=None, x=None,
+                 top_p=1.0):
     sh = L.shape
     return oracle.Layer(L.x if x is None else x, L.wg, L.bias, L.q_base, L.s_base, L.shared_q, L.shared_s,
                         d=sh.d, f=sh.f, E=sh.E, k=sh.k if k is None else k, G=sh.G, normalize=normalize,
-                        route_scale=route_scale, res=res)
+                        route_scale=route_scale, res=res, top_p=top_p)
 
 
 def near_tie_tokens(keys: np.ndarray, k: int, tol: float = NEAR_TIE) -> np.ndarray:
@@ -53,9 +54,22 @@ def near_tie_tokens(keys: np.ndarray, k: int, tol: float = NEAR_TIE) -> np.ndarr
     return (gaps <= tol).any(axis=1) if gaps.shape[1] else np.zeros(keys.shape[0], bool)
 
 
-def compare_routing(gpu_idx, gpu_w, o_idx, o_w, keys, k):
+def topp_cut_ties(raw_w: np.ndarray, top_p: float, tol: float = NEAR_TIE) -> np.ndarray:
+    """Tokens whose top-p cut is decided by <= tol: raw_w holds the oracle's unnormalised
+    scores of the k chosen experts in selection order (top_p = 1), and a token is
+    flagged when some prefix sum of them lies within tol * total of top_p * total."""
+    if top_p >= 1.0:
+        return np.zeros(raw_w.shape[0], bool)
+    cum = np.cumsum(raw_w, axis=1)
+    total = cum[:, -1:]
+    return (np.abs(cum[:, :-1] - top_p * total) <= tol * total).any(axis=1)
+
+
+def compare_routing(gpu_idx, gpu_w, o_idx, o_w, keys, k, extra_flags=None):
     """Asserts exact indices outside near-ties; returns (matched mask, flagged mask)."""
     flagged = near_tie_tokens(keys, k)
+    if extra_flags is not None:
+        flagged = flagged | extra_flags
     same = (gpu_idx == o_idx).all(axis=1)
     bad = ~same & ~flagged
     assert not bad.any(), f"routing differs on tokens {np.nonzero(bad)[0][:10]} (not near-ties)"
@@ -103,7 +117,11 @@ def run_steps(dev: dict, k: int, *, normalize=1, route_scale=1.0, res=None, hits
 
 
 def check_union_equal(r: dict, u: dict, E: int):
+    """Union arrays equal; sorted_pair only over its offsets[E] placed pairs (the rest is unspecified
+    when slots are empty)."""
     assert r["n_uniq"] == u["n_uniq"]
-    for key in ("counts", "offsets", "perm", "sorted_pair"):
+    for key in ("counts", "offsets", "perm"):
         assert np.array_equal(r[key], u[key]), key
+    n = int(u["offsets"][E])
+    assert np.array_equal(r["sorted_pair"][:n], u["sorted_pair"][:n]), "sorted_pair"
     assert np.array_equal(r["uniq"][:u["n_uniq"]], u["uniq"][:u["n_uniq"]])

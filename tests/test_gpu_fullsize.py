@@ -136,15 +136,16 @@ def test_batched_decode_t64_zipf(full):
     bias = workloads.selection_bias(E, "zipf", seed=0)
     r, u = _check_layer(L, lw, wg_d, x, bias, m.MOE_MODE_DECODE, TOL_DECODE, 12)
     assert u["n_uniq"] < 64 * K
-    # every row of the hottest expert, through the separate calls on the same routing
+    # the separate calls on the same routing
     dev = dict(x=torch.from_numpy(x).cuda(), wg=wg_d, bias=torch.from_numpy(bias).cuda(), layer=lw)
     s = run_steps(dev, K, mode=m.MOE_MODE_DECODE, teacher_idx=r["idx"], teacher_w=r["w"])
     assert s["err"] == 0
     check_union_equal(s, u, E)
-    hot = int(np.argmax(u["counts"]))
-    lo, hi = u["offsets"][hot], u["offsets"][hot + 1]
-    y = oracle.expert_ffn_tokens(x, u["sorted_pair"][lo:hi] // K, L.q_base[hot], L.s_base[hot], D, F, G)
-    assert rel_max_err(s["y_pair"][lo:hi], y) <= TOL_DECODE
+    # every row of the three hottest experts (the most 16-token passes)
+    for hot in np.argsort(-u["counts"], kind="stable")[:3]:
+        lo, hi = u["offsets"][hot], u["offsets"][hot + 1]
+        y = oracle.expert_ffn_tokens(x, u["sorted_pair"][lo:hi] // K, L.q_base[hot], L.s_base[hot], D, F, G)
+        assert rel_max_err(s["y_pair"][lo:hi], y) <= TOL_DECODE, f"expert {hot} ({hi - lo} tokens)"
     # the fused entry point and the separate calls give the same bits
     assert np.array_equal(s["out"], r["out"])
 
@@ -156,19 +157,30 @@ def test_prefill_t4096(full):
     x = workloads.activations(4096, D, seed=0)
     r, u = _check_layer(L, lw, wg_d, x, None, m.MOE_MODE_PREFILL, TOL_PREFILL, 12)
     assert u["n_uniq"] == E
-    # sampled rows of the hottest expert's pair outputs (its last row is in the ragged tail of a tile)
+    # the pair outputs through the separate calls on the GPU's own routing
     dev = dict(x=torch.from_numpy(x).cuda(), wg=wg_d, bias=None, layer=lw)
     s = run_steps(dev, K, mode=m.MOE_MODE_PREFILL, teacher_idx=r["idx"], teacher_w=r["w"])
     assert s["err"] == 0
     check_union_equal(s, u, E)
-    hot = int(np.argmax(u["counts"]))
-    lo, hi = int(u["offsets"][hot]), int(u["offsets"][hot + 1])
-    rows = np.unique(np.array([lo, lo + 1, (lo + hi) // 2, hi - 2, hi - 1]))
-    y = oracle.expert_ffn_tokens(x, u["sorted_pair"][rows] // K, L.q_base[hot], L.s_base[hot], D, F, G)
-    assert rel_max_err(s["y_pair"][rows], y) <= TOL_PREFILL
-    toks = _sample(4096, 4, seed=9, must=(4095,))
+    # the first and the last pair row of every expert group (a group's last row closes the ragged
+    # tail of its last token tile), checked against the oracle expert by expert
+    worst = 0.0
+    for e in u["uniq"][:u["n_uniq"]]:
+        lo, hi = int(u["offsets"][e]), int(u["offsets"][e + 1])
+        rows = np.unique(np.array([lo, hi - 1]))
+        y = oracle.expert_ffn_tokens(x, u["sorted_pair"][rows] // K, L.q_base[e], L.s_base[e], D, F, G)
+        err = rel_max_err(s["y_pair"][rows], y)
+        worst = max(worst, err)
+        assert err <= TOL_PREFILL, f"expert {e}: {err:.3e}"
+    # the shared expert's first and last token of every 160-token tile (the kernel's balanced split)
+    ntile = -(-4096 // 160)
+    toks = np.unique(np.array([j * 4096 // ntile for j in range(ntile)] +
+                              [(j + 1) * 4096 // ntile - 1 for j in range(ntile)], np.int32))
     y_sh = oracle.expert_ffn_tokens(x, toks, L.shared_q, L.shared_s, D, F, G)
-    assert rel_max_err(s["y_shared"][toks], y_sh) <= TOL_PREFILL
+    err_sh = rel_max_err(s["y_shared"][toks], y_sh)
+    print(f"[prefill T=4096] pair rows checked {2 * int(u['n_uniq'])}, worst {worst:.3e}; "
+          f"shared rows {toks.size}, {err_sh:.3e}")
+    assert err_sh <= TOL_PREFILL
 
 
 @pytest.mark.parametrize("T", [32, 128, 256])

@@ -7,8 +7,8 @@ import torch
 
 import oracle
 import workloads
-from moe_testlib import (TOL_DECODE, check_union_equal, compare_routing, device_layer, host, moe,
-                         oracle_layer, rel_max_err, run_steps)
+from moe_testlib import (TOL_DECODE, TOL_PREFILL, check_union_equal, compare_routing, device_layer, host, moe,
+                         near_tie_tokens, oracle_layer, rel_max_err, run_steps, topp_cut_ties)
 
 pytestmark = pytest.mark.gpu
 
@@ -95,7 +95,7 @@ def test_fused_layer_is_deterministic():
 def test_union_flags_bad_expert_ids():
     m = moe()
     E, k = 8, 2
-    idx = torch.tensor([[0, 3], [8, 3], [3, -1], [7, 0]], dtype=torch.int32, device="cuda")
+    idx = torch.tensor([[0, 3], [8, 3], [3, -2], [7, 0]], dtype=torch.int32, device="cuda")
     un = m.moe_union(idx, E)
     torch.cuda.synchronize()
     assert int(host(un["err"])[0]) & m.MOE_DEVERR_BAD_EXPERT
@@ -264,3 +264,184 @@ def test_union_paths_bit_exact(T, k, E, dups):
     o = oracle.union(idx, E)
     check_union_equal(r, o, E)
     assert np.array_equal(host(hits), o["counts"].astype(np.int64))
+
+
+# ------------------------------------------------------------ wide routing ----
+# Selection widths and expert counts the ABI accepts beyond the GLM-5.2 shape: k up to 32
+# (every candidate slot of a 32-expert block is used), E up to 1024 (32 blocks of 32).
+WIDE = [(64, 16), (256, 16), (64, 32), (256, 32), (512, 8), (1024, 8)]
+
+
+@pytest.mark.parametrize("E,k", WIDE, ids=lambda v: str(v))
+def test_route_wide_selection_block_topk(E, k):
+    """The stand-alone top-k kernel (T > 8) against the oracle's brute-force order."""
+    m = moe()
+    T, d = 37, 256
+    x = workloads.activations(T, d, seed=E + k)
+    wg = workloads.router_weights(E, d, seed=E * k) * np.float32(20.0)   # logits ~ N(0, 0.8)
+    b = workloads.selection_bias(E, "normal", seed=k)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    idx, w, logits = m.moe_route(t(x), t(wg), t(b), k)
+    torch.cuda.synchronize()
+    o_idx, o_w, o_logits, keys = oracle.route(x, wg, b, k)
+    assert np.max(np.abs(host(logits) - o_logits)) <= 1e-5 * max(1.0, float(np.abs(o_logits).max()))
+    same, _ = compare_routing(host(idx), host(w), o_idx, o_w, keys, k)
+    assert same.sum() >= T - 2
+
+
+@pytest.mark.parametrize("E,k", WIDE, ids=lambda v: str(v))
+def test_layer_wide_selection_small_batch(E, k):
+    """The fused small-batch path (select + union in one block, T <= 8 and T*k <= 64) and the
+    general decode path at the same widths: routing, union, hits and outputs against the oracle."""
+    m = moe()
+    T_small = min(8, 64 // k)
+    for T in (T_small, 11):
+        sh = Shape(f"wide_{E}_{k}_{T}", E=E, k=k, d=256, f=128, T=T, bias="normal")
+        L = workloads.layer_inputs(sh, seed=E + T, threads=8)
+        dev = device_layer(L)
+        hits = torch.zeros(E, dtype=torch.int64, device="cuda")
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        out, err = m.moe_layer_forward(dev["x"], dev["wg"], dev["bias"], dev["layer"], k, mode=m.MOE_MODE_DECODE,
+                                       topk_idx=idx, hits=hits)
+        torch.cuda.synchronize()
+        assert int(host(err)[0]) == 0
+        o_idx, o_w, _, keys = oracle.route(L.x, L.wg, L.bias, k)
+        gi = host(idx)
+        flagged = near_tie_tokens(keys, k)
+        assert np.array_equal(gi[~flagged], o_idx[~flagged]), f"T={T}"
+        assert np.array_equal(host(hits), oracle.union(gi, E)["counts"].astype(np.int64))
+        same = (gi == o_idx).all(axis=1)
+        _, _, o_out = oracle_layer(L).dense()
+        assert rel_max_err(host(out)[same], o_out[same]) <= TOL_DECODE, f"T={T}"
+
+
+# ------------------------------------------------------------------ top-p ----
+
+def _topp_flags(L_or_x, wg, bias, k, top_p):
+    x = L_or_x
+    _, raw, _, keys = oracle.route(x, wg, bias, k, normalize=0, top_p=1.0)
+    return near_tie_tokens(keys, k) | topp_cut_ties(raw, top_p)
+
+
+@pytest.mark.parametrize("top_p", [0.3, 0.6, 0.85, 0.999])
+def test_route_topp_parity(top_p):
+    """moe_route_topp against the oracle's cut (bit-exact outside flagged ties), on the
+    stand-alone top-k kernel; top_p = 1 gives moe_route's bits."""
+    m = moe()
+    T, d, E, k = 300, 512, 256, 8
+    x = workloads.activations(T, d, seed=7)
+    wg = workloads.router_weights(E, d, seed=8) * np.float32(30.0)
+    b = workloads.selection_bias(E, "normal", seed=9)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    idx, w, _ = m.moe_route(t(x), t(wg), t(b), k, top_p=top_p)
+    torch.cuda.synchronize()
+    o_idx, o_w, _, keys = oracle.route(x, wg, b, k, top_p=top_p)
+    flags = _topp_flags(x, wg, b, k, top_p)
+    same, _ = compare_routing(host(idx), host(w), o_idx, o_w, keys, k, extra_flags=flags)
+    gi = host(idx)
+    assert same.sum() >= T - 5
+    assert np.all(gi[:, 0] >= 0) and ((gi == -1).any() or top_p > 0.99)
+    # the kept slots are a prefix of plain top-k's slots
+    i1, w1, _ = m.moe_route(t(x), t(wg), t(b), k, top_p=1.0)
+    i0, w0, _ = m.moe_route(t(x), t(wg), t(b), k)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(i1), host(i0)) and np.array_equal(host(w1), host(w0))
+    kept = gi >= 0
+    assert np.array_equal(gi[kept], host(i0)[kept])
+
+
+@pytest.mark.parametrize("T,mode_name", [(5, "MOE_MODE_DECODE"), (37, "MOE_MODE_DECODE"), (37, "MOE_MODE_PREFILL")])
+def test_layer_topp_parity(T, mode_name):
+    """The fused layer with top-p pruning (small-batch select+union path at T = 5, stage kernels at
+    T = 37, both FFN paths): routing, union with empty slots, hits and outputs against the oracle."""
+    m = moe()
+    mode = getattr(m, mode_name)
+    tol = TOL_DECODE if mode == m.MOE_MODE_DECODE else TOL_PREFILL
+    top_p = 0.7
+    sh = Shape(f"topp_{T}", E=32, k=8, d=512, f=256, T=T, bias="normal")
+    L = workloads.layer_inputs(sh, seed=T, threads=8)
+    dev = device_layer(L)
+    res = workloads.activations(T, sh.d, seed=5)
+    hits = torch.zeros(sh.E, dtype=torch.int64, device="cuda")
+    idx = torch.empty((T, sh.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, sh.k), dtype=torch.float32, device="cuda")
+    out, err = m.moe_layer_forward(dev["x"], dev["wg"], dev["bias"], dev["layer"], sh.k, 1, 1.0, mode=mode,
+                                   residual=torch.from_numpy(res).cuda(), topk_idx=idx, topk_w=w, hits=hits,
+                                   top_p=top_p)
+    torch.cuda.synchronize()
+    assert int(host(err)[0]) == 0
+    o_idx, o_w, _, keys = oracle.route(L.x, L.wg, L.bias, sh.k, top_p=top_p)
+    same, _ = compare_routing(host(idx), host(w), o_idx, o_w, keys, sh.k,
+                              extra_flags=_topp_flags(L.x, L.wg, L.bias, sh.k, top_p))
+    gi = host(idx)
+    assert (gi == -1).any()
+    assert np.array_equal(host(hits), oracle.union(gi, sh.E)["counts"].astype(np.int64))
+    assert int(host(hits).sum()) == int((gi >= 0).sum())
+    _, _, o_out = oracle_layer(L, res=res, top_p=top_p).dense()
+    assert rel_max_err(host(out)[same], o_out[same]) <= tol
+
+
+def test_union_empty_slots():
+    """-1 marks an empty slot: no group, perm -1, no hit, no error (bitmap and chunked paths)."""
+    m = moe()
+    rng = np.random.default_rng(3)
+    for T, k, E in ((5, 4, 16), (600, 8, 64)):
+        idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+        cut = rng.integers(1, k + 1, size=T)
+        for t in range(T):
+            idx[t, cut[t]:] = -1
+        hits = torch.zeros(E, dtype=torch.int64, device="cuda")
+        un = m.moe_union(torch.from_numpy(idx).cuda(), E, hits=hits)
+        torch.cuda.synchronize()
+        r = {key: host(v) for key, v in un.items()}
+        r["n_uniq"] = int(r["n_uniq"][0])
+        assert int(r["err"][0]) == 0
+        o = oracle.union(idx, E)
+        check_union_equal(r, o, E)
+        assert np.all(r["perm"][idx.reshape(-1) == -1] == -1)
+        assert np.array_equal(host(hits), o["counts"].astype(np.int64))
+
+
+# -------------------------------------------------- prefill scale range ----
+
+@pytest.mark.parametrize("mu", [-12.0, 5.0, -25.0, 12.0])
+def test_prefill_weight_scale_range(mu):
+    """Group scales lognormal(mu, 0.3) far from the workloads' mu = -4: the prefill path scales each
+    weight row by a power of two, so its fp16 weights keep their precision at any magnitude
+    (2e-2 of the RMS); the decode path applies fp32 scales after the MMA (1e-4)."""
+    from moe_testlib import TOL_PREFILL
+    m = moe()
+    sh = Shape("scale_range", E=16, k=4, d=1024, f=384, T=37, bias="normal")
+    L = workloads.layer_inputs(sh, seed=4, threads=8)
+    fac = np.float32(np.exp(mu + 4.0))
+    L.s_base[:] *= fac
+    L.shared_s[:] *= fac
+    dev = device_layer(L)
+    o_idx, o_w, _, _ = oracle.route(L.x, L.wg, L.bias, sh.k)
+    o_union = oracle.union(o_idx, sh.E)
+    for mode, tol in ((m.MOE_MODE_PREFILL, TOL_PREFILL), (m.MOE_MODE_DECODE, TOL_DECODE)):
+        t = run_steps(dev, sh.k, teacher_idx=o_idx, teacher_w=o_w, mode=mode)
+        assert t["err"] == 0, f"mode {mode}: device error {t['err']}"
+        assert np.isfinite(t["y_pair"]).all() and np.isfinite(t["y_shared"]).all()
+        y_sh = oracle.expert_ffn_tokens(L.x, np.arange(sh.T), L.shared_q, L.shared_s, sh.d, sh.f, sh.G)
+        assert rel_max_err(t["y_shared"], y_sh) <= tol, f"mode {mode} shared"
+        for e in o_union["uniq"][:o_union["n_uniq"]]:
+            lo, hi = o_union["offsets"][e], o_union["offsets"][e + 1]
+            toks = o_union["sorted_pair"][lo:hi] // sh.k
+            y = oracle.expert_ffn_tokens(L.x, toks, L.q_base[e], L.s_base[e], sh.d, sh.f, sh.G)
+            assert rel_max_err(t["y_pair"][lo:hi], y) <= tol, f"mode {mode} expert {e}"
+
+
+def test_prefill_flags_scales_beyond_its_row_range():
+    """A group scale 2^20 times its row's first group scale is beyond the prefill path's fp16
+    weights: the device error word says so (MOE_DEVERR_SCALE_RANGE)."""
+    m = moe()
+    sh = Shape("scale_spread", E=8, k=2, d=256, f=128, T=16)
+    L = workloads.layer_inputs(sh, seed=6, threads=4)
+    G, d = sh.G, sh.d
+    L.s_base[3, 5 * (d // G) + 2] *= np.float32(2.0 ** 20)   # gate row 5 of expert 3, group 2
+    dev = device_layer(L)
+    idx = np.tile(np.array([[3, 0]], np.int32), (sh.T, 1))
+    t = run_steps(dev, sh.k, teacher_idx=idx, teacher_w=np.full((sh.T, 2), 0.5), mode=m.MOE_MODE_PREFILL)
+    assert t["err"] & m.MOE_DEVERR_SCALE_RANGE
+    assert m.device_error(m.MOE_DEVERR_SCALE_RANGE) == m.MOE_ERR_UNSUPPORTED
