@@ -61,6 +61,9 @@ def parse_args(argv=None):
     ap.add_argument("--graph-steps", type=int, default=100, help="steps captured per CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="decode line only (by default it also carries the batched-decode, prefill and stack "
+                         "workloads under \"workloads\")")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU-baseline sample")
     return ap.parse_args(argv)
 
@@ -166,13 +169,8 @@ def layer_bytes(sh, n_uniq: int) -> dict:
 
 # ------------------------------------------------------------------ our arm --
 
-def run_ours(args, rank, world, local):
+def init_device(local, world):
     import torch
-
-    import int4_routed_expert_sigmoid_gb300 as moe
-    import workloads
-    from int4_routed_expert_sigmoid_gb300 import build as libbuild
-
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
@@ -181,36 +179,58 @@ def run_ours(args, rank, world, local):
             dist.init_process_group("nccl", device_id=dev)
         except TypeError:
             dist.init_process_group("nccl")
+    from int4_routed_expert_sigmoid_gb300 import build as libbuild
     libbuild.build()
-    sh = workloads.WORKLOADS[args.workload]
-    if args.experts or args.tokens:
-        import dataclasses
-        sh = dataclasses.replace(sh, E=args.experts or sh.E, T=args.tokens or sh.T)
-    T, E, k, d, f = sh.T, sh.E, sh.k, sh.d, sh.f
-    prefill = args.workload == "prefill" if args.mode == "workload" else args.mode == "prefill"
-    mode = moe.MOE_MODE_PREFILL if prefill else moe.MOE_MODE_DECODE
-    R = max(1, min(args.replicas, 2) if prefill else args.replicas)
-    S = max(1, min(args.graph_steps if not prefill else 4, args.steps))
+    return dev
 
-    # ---- inputs: one seeded layer, R device copies (weights, router, bias)
-    L = workloads.layer_inputs(sh, seed=0, threads=os.cpu_count() or 8)
-    qb, sc = workloads.expert_q_bytes(d, f), workloads.expert_s_count(d, f, sh.G)
-    q_all = torch.empty((R, E * qb + qb), dtype=torch.uint8, device=dev)     # routed experts + shared
-    s_all = torch.empty((R, E * sc + sc), dtype=torch.float32, device=dev)
-    q_all[0, :E * qb].copy_(torch.from_numpy(L.q_base.reshape(-1)))
-    q_all[0, E * qb:].copy_(torch.from_numpy(L.shared_q))
-    s_all[0, :E * sc].copy_(torch.from_numpy(L.s_base.reshape(-1)))
-    s_all[0, E * sc:].copy_(torch.from_numpy(L.shared_s))
-    wg0 = torch.from_numpy(L.wg).to(dev)
-    bias0 = None if L.bias is None else torch.from_numpy(L.bias).to(dev)
-    for r in range(1, R):
-        q_all[r].copy_(q_all[0])
-        s_all[r].copy_(s_all[0])
-    wgs = [wg0] + [wg0.clone() for _ in range(R - 1)]
-    biases = [bias0] + [None if bias0 is None else bias0.clone() for _ in range(R - 1)]
-    layers = [moe.LayerWeights(q_all[r, :E * qb], s_all[r, :E * sc], q_all[r, E * qb:], s_all[r, E * sc:],
-                               E=E, d=d, f=f, G=sh.G) for r in range(R)]
-    del L
+
+class LayerCopies:
+    """R device copies of one seeded GLM-5.2-shaped layer (routed experts + shared expert, router
+    weights), rotated across steps so that consecutive steps never find their weights in L2.  The
+    decode, batched-decode and prefill workloads share layer 0's weights; only the selection bias
+    (per workload) differs."""
+
+    def __init__(self, sh, R, dev):
+        import torch
+
+        import int4_routed_expert_sigmoid_gb300 as moe
+        import workloads
+        E, d, f, G = sh.E, sh.d, sh.f, sh.G
+        L = workloads.layer_inputs(sh, seed=0, threads=os.cpu_count() or 8)
+        qb, sc = workloads.expert_q_bytes(d, f), workloads.expert_s_count(d, f, G)
+        self.q_all = torch.empty((R, E * qb + qb), dtype=torch.uint8, device=dev)
+        self.s_all = torch.empty((R, E * sc + sc), dtype=torch.float32, device=dev)
+        self.q_all[0, :E * qb].copy_(torch.from_numpy(L.q_base.reshape(-1)))
+        self.q_all[0, E * qb:].copy_(torch.from_numpy(L.shared_q))
+        self.s_all[0, :E * sc].copy_(torch.from_numpy(L.s_base.reshape(-1)))
+        self.s_all[0, E * sc:].copy_(torch.from_numpy(L.shared_s))
+        wg0 = torch.from_numpy(L.wg).to(dev)
+        for r in range(1, R):
+            self.q_all[r].copy_(self.q_all[0])
+            self.s_all[r].copy_(self.s_all[0])
+        self.wgs = [wg0] + [wg0.clone() for _ in range(R - 1)]
+        self.layers = [moe.LayerWeights(self.q_all[r, :E * qb], self.s_all[r, :E * sc], self.q_all[r, E * qb:],
+                                        self.s_all[r, E * sc:], E=E, d=d, f=f, G=G) for r in range(R)]
+        self.R, self.E, self.d, self.f, self.G = R, E, d, f, G
+        self.block_bytes = qb + 4 * sc
+        del L
+
+
+def measure_layer(copies, sh, prefill, steps, warmup, graph_steps, e2e_steps, rank, world, dev):
+    """One workload of the single-layer benchmark: `steps` timed steps of moe_layer_forward over T
+    tokens (CUDA graphs of S steps), stage durations from a second graph with events between the
+    stage calls, and an end-to-end run with host buffers.  Returns the workload's measurements."""
+    import torch
+
+    import int4_routed_expert_sigmoid_gb300 as moe
+    import workloads
+    T, E, k, d, f = sh.T, sh.E, sh.k, sh.d, sh.f
+    mode = moe.MOE_MODE_PREFILL if prefill else moe.MOE_MODE_DECODE
+    R = copies.R
+    S = max(1, min(graph_steps, steps))
+    bias0 = workloads.selection_bias(E, sh.bias, seed=0)
+    biases = [None if bias0 is None else torch.from_numpy(bias0).to(dev) for _ in range(R)]
+    wgs, layers = copies.wgs, copies.layers
     # distinct tokens per captured step position, seeded per rank
     xs = torch.from_numpy(workloads.activations(S * T, d, seed=1000 + rank)).to(dev).view(S, T, d)
 
@@ -230,7 +250,6 @@ def run_ours(args, rank, world, local):
     y_shared = torch.empty((T, d), dtype=torch.float32, device=dev)
     outs = torch.empty((S, T, d), dtype=torch.float32, device=dev)
     ws = moe.workspace(moe.ffn_workspace_bytes(T, k, d, f, mode), dev)
-
     lws_step = moe.workspace(moe.layer_workspace_bytes(T, k, E, d, f, mode), dev)
 
     def layer_step(i):
@@ -291,17 +310,17 @@ def run_ours(args, rank, world, local):
 
     g_main, _ = capture(S, False)
     g_stages, evs = capture(S, True)
-    tail = args.steps % S
+    tail = steps % S
     g_tail = capture(tail, False)[0] if tail else None
-    n_main = args.steps // S
+    n_main = steps // S
 
     # ---- warm-up (untimed)
-    for _ in range(max(1, -(-args.warmup // S))):
+    for _ in range(max(1, -(-warmup // S))):
         g_main.replay()
     torch.cuda.synchronize()
     err.zero_()
 
-    sampler = ClockSampler(gpu_uuid(torch, local))
+    sampler = ClockSampler(gpu_uuid(torch, dev.index))
     sampler.start()
     time.sleep(0.3)
     barrier(world)
@@ -330,7 +349,7 @@ def run_ours(args, rank, world, local):
     n_uniq = int(un["n_uniq"].item())
 
     # ---- end to end through the public API with host buffers (not graph-captured)
-    e2e_steps = max(1, min(args.e2e_steps, args.steps, 8 if prefill else args.e2e_steps))
+    e2e_steps = max(1, min(e2e_steps, steps))
     x_host = torch.from_numpy(workloads.activations(e2e_steps * T, d, seed=5000 + rank)).view(e2e_steps, T, d)
     x_host = x_host.pin_memory()
     out_host = torch.empty((e2e_steps, T, d), dtype=torch.float32).pin_memory()
@@ -363,25 +382,27 @@ def run_ours(args, rank, world, local):
         # dense work of the grouped GEMMs: 3 matrices of d x f per (token, expert) pair, 2 flops per MAC
         flops = 6.0 * d * f * (T * k + T)
         achieved = flops / (ffn_ms * 1e-3) / 1e12
-        roof = {"kernel": "expert FFN stage (pair positions + token rows, tcgen05 gate/up, h conversion, tcgen05 down)",
+        roof = {"kernel": "expert FFN stage (pair positions + token rows, tcgen05 gate/up, h conversion, "
+                          "tcgen05 down)",
                 "bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": ncu_traffic(ROOT, "ffn_prefill"),
-                "peak_source": peaks["source"] + " bf16 dense (fp16 operands run at the same tensor rate)",
+                "peak_source": peaks["source"] + " bf16 dense burst (fp16 operands run at the same tensor rate)",
+                "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
                 "flops_per_launch": flops, "ms_per_launch": round(ffn_ms, 5)}
     else:
         achieved = byts["ffn"] / (ffn_ms * 1e-3) / 1e9
         roof = {"kernel": "expert FFN stage (act fragments + gate/up + down kernels)", "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic(ROOT, "ffn"),
+                "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": ncu_traffic(ROOT, "ffn" if T == 1 else f"ffn_T{T}"),
                 "peak_source": peaks["source"], "bytes_per_launch": byts["ffn"], "ms_per_launch": round(ffn_ms, 5)}
-    value = job_throughput(T, args.steps, world, elapsed_max)
-    ms_per_step = elapsed_max / args.steps
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: 1 MoE layer, E={E} routed + 1 shared, k={k}, d={d}, f={f}, "
-                               f"int4 group-{sh.G} fp32 scales, T={T} token(s) per step",
+    ms_per_step = elapsed_max / steps
+    return {
+        "value": round(job_throughput(T, steps, world, elapsed_max), 2), "unit": UNIT, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(ms_per_step, 6),
+        "config": {"workload": f"{sh.name}: 1 MoE layer, E={E} routed + 1 shared, k={k}, d={d}, f={f}, "
+                               f"int4 group-{sh.G} fp32 scales, T={T} token(s) per step, selection bias "
+                               f"{sh.bias}, FFN path {'prefill' if prefill else 'decode'}",
                    "T": T, "E": E, "k": k, "d": d, "f": f, "G": sh.G, "weights": "int4",
                    "l2": (f"inputs larger than L2: {R} device copies of the layer "
                           f"({R * E * byts['expert_block'] / 1e9:.1f} GB) rotated across steps")
@@ -396,10 +417,64 @@ def run_ours(args, rank, world, local):
         "n_uniq": n_uniq,
         "e2e": {"value": round(T * e2e_steps * world / e2e_max, 2), "unit": UNIT,
                 "h2d_bytes_per_step": T * d * 4, "d2h_bytes_per_step": T * d * 4, "steps": e2e_steps},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step * steps,
         "clocks": clocks,
         "device_error": dev_err,
     }
+
+
+def workload_shape(args, name):
+    import dataclasses
+
+    import workloads
+    sh = workloads.WORKLOADS[name]
+    if args.experts or args.tokens:
+        sh = dataclasses.replace(sh, E=args.experts or sh.E, T=args.tokens or sh.T)
+    return sh
+
+
+def is_prefill(args, name):
+    return name == "prefill" if args.mode == "workload" else args.mode == "prefill"
+
+
+# steps of the secondary workloads carried in the default line (their own counts, a few seconds each)
+EXTRA_STEPS = {"prefill": 40, "batched_decode": 200}
+
+
+def run_ours(args, rank, world, local):
+    """The single-layer workloads.  The default (decode T = 1) line also carries, under "workloads",
+    the prefill T = 4096 and batched-decode T = 64 layers on the same weights and the 8-layer stack
+    sweep, each with its own steps, roofline, stage times, union size and clocks."""
+    import torch
+    dev = init_device(local, world)
+    sh = workload_shape(args, args.workload)
+    prefill = is_prefill(args, args.workload)
+    R = max(1, min(args.replicas, 2) if prefill else args.replicas)
+    copies = LayerCopies(sh, R, dev)
+    res = measure_layer(copies, sh, prefill, args.steps, args.warmup,
+                        args.graph_steps if not prefill else 4, 8 if prefill else args.e2e_steps, rank, world, dev)
+    line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic"}
+    for key in ("config", "roofline", "stages_ms", "layer_gbs", "nibble_gbs", "n_uniq", "e2e", "gpu_launches",
+                "clocks", "device_error"):
+        line[key] = res[key]
+    extras = {}
+    if args.workload == "decode" and not args.no_workloads and not (args.experts or args.tokens):
+        # the other single-layer workloads on the same weights, then the stack on its own 8 layers
+        for name in ("batched_decode", "prefill"):
+            sh_x = workload_shape(args, name)
+            pf = is_prefill(args, name)
+            extras[name] = measure_layer(copies, sh_x, pf, EXTRA_STEPS[name], max(3, args.warmup),
+                                         4 if pf else args.graph_steps, 8 if pf else 200, rank, world, dev)
+            line["gpu_launches"] += extras[name]["gpu_launches"]
+        del copies
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        extras["stack"] = measure_stack(args, rank, world, dev, T_line=64, steps=48, warmup=max(3, args.warmup),
+                                        sweep_seconds=1.0)
+        line["gpu_launches"] += extras["stack"]["gpu_launches"]
+        line["workloads"] = extras
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sh, args.cpu_seconds)
     if world > 1:
@@ -411,30 +486,17 @@ def run_ours(args, rank, world, local):
 
 # ------------------------------------------------------------- layer stack --
 
-def run_stack(args, rank, world, local):
-    """8 resident layers, out_l = x_l + MoE(RMSNorm(x_l)), each layer with its own
-    seeded experts, router and Zipf selection bias (its own expert permutation).
-    A step is one pass of T tokens through all 8 layers; tokens/s = T / step time.
-    The line's T is --tokens (default 64); "sweep" holds every T of the stack's
-    batch sweep, each timed the same way with its own step count."""
+def measure_stack(args, rank, world, dev, T_line, steps, warmup, sweep_seconds=2.0):
+    """8 resident layers, out_l = x_l + MoE(RMSNorm(x_l)), each layer with its own seeded experts,
+    router and Zipf selection bias (its own expert permutation).  A step is one pass of T tokens
+    through all 8 layers; tokens/s = T / step time.  Times exactly `steps` steps at T_line and, under
+    "sweep", every T of the stack's batch sweep, each for about `sweep_seconds`."""
     import torch
 
     import int4_routed_expert_sigmoid_gb300 as moe
     import workloads
-    from int4_routed_expert_sigmoid_gb300 import build as libbuild
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        try:
-            dist.init_process_group("nccl", device_id=dev)
-        except TypeError:
-            dist.init_process_group("nccl")
-    libbuild.build()
     sh = workloads.WORKLOADS["stack"]
     E, k, d, f, G, NL = sh.E, sh.k, sh.d, sh.f, sh.G, sh.layers
-    T_line = args.tokens or sh.T
     mode = {"workload": moe.MOE_MODE_AUTO, "decode": moe.MOE_MODE_DECODE,
             "prefill": moe.MOE_MODE_PREFILL}[args.mode]   # automatic: the library picks the path by T
     eps = 1e-5
@@ -524,8 +586,13 @@ def run_stack(args, rank, world, local):
         # per layer: unique experts + shared, router weights and bias, x in, out, residual
         return sum((n + 1) * blk + E * d * 4 + E * 4 + 3 * T * d * 4 for n in nu)
 
-    # ---- the batch sweep (each T timed for about two seconds)
+    def path_of(T):
+        pf = mode == moe.MOE_MODE_PREFILL or (mode == moe.MOE_MODE_AUTO and T >= 128)
+        return pf, 1 + (9 if pf else 5 if (T <= 8 and T * k <= 64) else 7)   # RMS norm + the layer's kernels
+
+    # ---- the batch sweep (each T timed for about sweep_seconds)
     sweep = []
+    launches = 0
     for T in sh.batch_sweep:
         ctx = make(T)
         g = graph(ctx, S)
@@ -533,30 +600,35 @@ def run_stack(args, rank, world, local):
             g.replay()
         torch.cuda.synchronize()
         probe = timed(g, 2) / (2 * S)
-        reps = max(3, min(500, int(2000.0 / max(probe * S, 1e-3))))
+        reps = max(3, min(500, int(sweep_seconds * 1000.0 / max(probe * S, 1e-3))))
         err.zero_()
+        smp = ClockSampler(gpu_uuid(torch, dev.index))
+        smp.start()
         el = reduce_max(world, [timed(g, reps)], dev)[0]
+        ck = smp.stop()
         nu = n_uniq_layers(ctx)
         ms = el / (reps * S)
         by = bytes_of(T, nu)
+        launches += NL * path_of(T)[1] * reps * S
         sweep.append({"T": T, "steps": reps * S, "ms_per_step": round(ms, 5),
                       "tokens_per_s": round(job_throughput(T, reps * S, world, el), 2),
                       "stack_gbs": round(by / (ms * 1e-3) / 1e9, 1),
                       "frac": round(by / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                      "n_uniq_per_layer": nu, "device_error": int(err.item())})
+                      "ffn_path": "prefill" if path_of(T)[0] else "decode",
+                      "n_uniq_per_layer": nu, "clocks": ck, "device_error": int(err.item())})
         del g, ctx
         torch.cuda.empty_cache()
 
-    # ---- the line: exactly --steps steps at T_line
+    # ---- the line: exactly `steps` steps at T_line
     ctx = make(T_line)
     g_main = graph(ctx, S)
-    n_main, tail = divmod(args.steps, S)
+    n_main, tail = divmod(steps, S)
     g_tail = graph(ctx, tail) if tail else None
-    for _ in range(max(1, -(-args.warmup // S))):
+    for _ in range(max(1, -(-warmup // S))):
         g_main.replay()
     torch.cuda.synchronize()
     err.zero_()
-    sampler = ClockSampler(gpu_uuid(torch, local))
+    sampler = ClockSampler(gpu_uuid(torch, dev.index))
     sampler.start()
     time.sleep(0.3)
     elapsed = timed(g_main, n_main, g_tail)
@@ -565,7 +637,7 @@ def run_stack(args, rank, world, local):
     nu = n_uniq_layers(ctx)
 
     # ---- end to end with host buffers (not graph-captured)
-    e2e_steps = max(1, min(args.e2e_steps, args.steps, 200))
+    e2e_steps = max(1, min(args.e2e_steps, steps, 200))
     x_host = torch.from_numpy(workloads.activations(e2e_steps * T_line, d, seed=5000 + rank))
     x_host = x_host.view(e2e_steps, T_line, d).pin_memory()
     out_host = torch.empty((e2e_steps, T_line, d), dtype=torch.float32).pin_memory()
@@ -586,16 +658,16 @@ def run_stack(args, rank, world, local):
     dev_err |= int(err.item())
 
     elapsed_max, e2e_max = reduce_max(world, [elapsed, e2e_s], dev)
-    ms_per_step = elapsed_max / args.steps
+    ms_per_step = elapsed_max / steps
     by = bytes_of(T_line, nu)
     achieved = by / (ms_per_step * 1e-3) / 1e9
-    path_prefill = mode == moe.MOE_MODE_PREFILL or (mode == moe.MOE_MODE_AUTO and T_line >= 128)
-    small = T_line <= 8 and T_line * k <= 64
-    per_layer = 1 + (9 if path_prefill else 5 if small else 7)    # RMS norm + the fused layer's kernels
-    line = {
-        "metric": METRIC, "value": round(job_throughput(T_line, args.steps, world, elapsed_max), 2), "unit": UNIT,
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+    launches += NL * path_of(T_line)[1] * steps
+    del layers, q_all, s_all, ctx, g_main, g_tail
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return {
+        "value": round(job_throughput(T_line, steps, world, elapsed_max), 2), "unit": UNIT, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(ms_per_step, 6),
         "config": {"workload": f"stack: {NL} resident MoE layers (out = x + MoE(RMSNorm(x))), E={E} routed + 1 "
                                f"shared, k={k}, d={d}, f={f}, int4 group-{G} fp32 scales, Zipf(1.1) selection "
                                f"bias with a per-layer expert permutation, T={T_line} token(s) per step, "
@@ -611,12 +683,26 @@ def run_stack(args, rank, world, local):
         "sweep": sweep,
         "e2e": {"value": round(T_line * e2e_steps * world / e2e_max, 2), "unit": UNIT,
                 "h2d_bytes_per_step": T_line * d * 4, "d2h_bytes_per_step": T_line * d * 4, "steps": e2e_steps},
-        "gpu_launches": NL * per_layer * args.steps,
+        "gpu_launches": launches,
         "clocks": clocks,
         "device_error": dev_err,
     }
+
+
+def run_stack(args, rank, world, local):
+    """The stack workload as its own line (T from --tokens, default 64)."""
+    import workloads
+    dev = init_device(local, world)
+    sh = workloads.WORKLOADS["stack"]
+    res = measure_stack(args, rank, world, dev, args.tokens or sh.T, args.steps, args.warmup)
+    line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic"}
+    for key in ("config", "roofline", "n_uniq_per_layer", "sweep", "e2e", "gpu_launches", "clocks",
+                "device_error"):
+        line[key] = res[key]
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(sh, args.cpu_seconds, layers=NL)
+        line["cpu_baseline"] = cpu_baseline(sh, args.cpu_seconds, layers=sh.layers)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -701,6 +787,29 @@ def _oracle_layer(sh, f_used, seed=0):
     return oracle, L, q_base, s_base, shq, shs
 
 
+def host_cpu() -> dict:
+    """The host's logical CPU count and model name (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            key, _, val = ln.partition(":")
+            if key.strip() in ("Model name", "Vendor ID") and val.strip():
+                model = val.strip() if model is None or key.strip() == "Model name" else model
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as fh:
+                for ln in fh:
+                    if ln.lower().startswith(("model name", "cpu part", "hardware")):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"nproc": os.cpu_count(), "cpu_model": model or "unknown"}
+
+
 def cpu_baseline(sh, seconds: float, layers: int = 1) -> dict:
     """The oracle, as it stands, on a bounded sample: full layers for a few tokens.
     With layers > 1 (a stack of equally shaped layers) the rate of one layer is
@@ -721,7 +830,7 @@ def cpu_baseline(sh, seconds: float, layers: int = 1) -> dict:
     per = f"; rate / {layers} for the {layers}-layer stack" if layers > 1 else ""
     return {"value": round(n / el / layers, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{n} tokens of the {sh.name} layer (route + shared + {sh.k} routed int4 experts, full "
-                      f"d={sh.d}, f={sh.f}), fp64 C oracle, OpenMP over tokens, {el:.1f} s{per}"}
+                      f"d={sh.d}, f={sh.f}), fp64 C oracle, OpenMP over tokens, {el:.1f} s{per}", **host_cpu()}
 
 
 def run_reference(args, rank, world):
@@ -770,7 +879,9 @@ def run_reference(args, rank, world):
             "config": {"workload": f"{sh.name}: {sh.layers} MoE layer(s), E={sh.E} routed + 1 shared, k={sh.k}, d={sh.d}, "
                                    f"f={sh.f}, int4 group-{sh.G}, T={sh.T}"},
             "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
-                             "sample": f"each step: one token of the T={sh.T} batch through the layer with every "
+                             **host_cpu(),
+                             "sample": f"each step: one token of the T={sh.T} batch through the layer (OpenMP over "
+                                       f"the output rows of every expert matrix) with every "
                                        f"expert cut to its first {f_used} of {sh.f} intermediate rows; rate scaled "
                                        f"by {sh.f}/{f_used}" + (f" and divided by {sh.layers} layers"
                                                                if sh.layers > 1 else "")},
