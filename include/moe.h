@@ -31,8 +31,9 @@
  *  - int4 weights: symmetric two's complement in [-8, 7], no zero point; in a
  *    row of `cols` elements, element 2i is the low nibble of byte i and element
  *    2i+1 its high nibble; a matrix is [rows][cols/2] bytes.
- *  - scales: fp32, one per G = 32 consecutive elements of a row along the
- *    input (reduction) axis: [rows][cols/G].  deq(W)[r][i] = q[r][i] * s[r][i/G].
+ *  - scales: fp32, one per G consecutive elements of a row along the input
+ *    (reduction) axis, G = 32 or 64: [rows][cols/G].
+ *    deq(W)[r][i] = q[r][i] * s[r][i/G].
  *  - expert block: gate [f][d], up [f][d], down [d][f]: first the packed bytes
  *    of the three matrices in that order (moe_expert_q_bytes bytes), then their
  *    scales in the same order (moe_expert_s_count floats).  Expert e of a layer
@@ -42,8 +43,10 @@
  *    expert at int4.)
  *  - FFN_e(x) = down_e( silu(gate_e x) * (up_e x) ), silu(g) = g * sigmoid(g).
  *
- * Supported shapes: G = 32; d a multiple of 256; f a multiple of 128;
- * 1 <= k <= min(E, 32); 1 <= E <= 1024; 1 <= T.
+ * Supported shapes: G = 32 or 64 (the colibri README, "2. Get the model":
+ * group-scaled int4 containers, gs64 among them); d a multiple of 256; f a
+ * multiple of 128 (of 256 when G = 64); 1 <= k <= min(E, 32); 1 <= E <= 1024;
+ * 1 <= T.  Other shapes return MOE_ERR_UNSUPPORTED.
  */
 #ifndef MOE_H
 #define MOE_H

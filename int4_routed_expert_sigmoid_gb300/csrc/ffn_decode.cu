@@ -12,9 +12,16 @@
 // Design (GB300, sm_103a)
 //  * Work item = (expert of the union or the shared expert, tile of output
 //    rows: 32 rows of gate and of up, or 64 rows of down).  A persistent grid
-//    walks the items; an item's tokens are taken in passes of at most TOK
-//    tokens (balanced), each pass streaming the item's weights once (a second
-//    pass finds them in L2).
+//    walks the items; CTA c starts with item c.  For batches of more than one
+//    token each CTA's producer then takes the next unclaimed item from a
+//    global counter (zeroed by the kernel that precedes the FFN): units of
+//    very different token counts make items of very different lengths, and
+//    CTAs that finish early take more of them (at 64 tokens this shortened the
+//    FFN by 6 %).  At T = 1 all items are equal and CTA c takes c, c + G, ...
+//    (claiming was 2 us slower there).  The producer tags every ring stage
+//    with its item, so the consumers follow without knowing the schedule.  An
+//    item's tokens are taken in passes of at most TOK tokens (balanced), each
+//    pass streaming the item's weights once (a second pass finds them in L2).
 //  * Warp 8 of every CTA is the producer: per stage (one or two k-chunks of
 //    32 * GPC elements) it TMA-loads the item's packed rows (swizzled) and
 //    scales and, with one bulk copy per token, that token's activation
@@ -51,14 +58,15 @@ constexpr int kRingBytes = 96 * 1024;   // two CTAs per SM
 enum { kGateUp = 0, kDown = 1 };
 
 // TOK: tokens per pass (1, 4, 8 or 16); CPS: k-chunks per stage; GPC: groups per chunk (8 or 4).
-template <int MODE, int TOK, int CPS, int GPC>
+template <int MODE, int TOK, int CPS, int GPC, int GS>
 struct Cfg {
     static constexpr int kRows = MODE == kGateUp ? 32 : 64;   // output rows per matrix per item
     static constexpr int kMats = MODE == kGateUp ? 2 : 1;
     static constexpr int kNTM = (TOK + 3) / 4;                 // n-tiles (4 tokens each) at most
     static constexpr int kRowB = 16 * GPC;                     // packed bytes of a row per chunk
     static constexpr int kQSub = kRows * kRowB;                // one (matrix, chunk) tile of nibbles
-    static constexpr int kSSub = kRows * GPC * 4;              // one (matrix, chunk) tile of scales
+    static constexpr int kSpr = GPC * 32 / GS;                 // scales of a row per chunk (group size GS)
+    static constexpr int kSSub = kRows * kSpr * 4;             // one (matrix, chunk) tile of scales
     static constexpr int kBlk = frag_blk(GPC);
     static constexpr int kGpw = CPS * GPC / 2;                 // groups per warp per stage
     static constexpr int kSOff = kMats * CPS * kQSub;
@@ -72,7 +80,10 @@ struct Cfg {
     static constexpr int kHBufBytes = TOK * 32 * 4;
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kRedBytes + kHBufBytes;   // + unit table
     static_assert(kStages >= 3, "ring too shallow");
-    static_assert(kGpw == 2 || kGpw % 4 == 0, "scale vector loads");
+    static constexpr int kSpw = kGpw * 32 / GS;                // scales per warp per stage
+    static_assert(GS == 32 || GS == 64, "group sizes");
+    static_assert(kSpr * 4 % 16 == 0, "a scale box row is a multiple of 16 bytes");
+    static_assert(kSpw == 1 || kSpw == 2 || kSpw % 4 == 0, "scale vector loads");
     static_assert(kBOff % 16 == 0 && kTokBytes % 16 == 0, "bulk copy alignment");
 };
 
@@ -95,8 +106,10 @@ struct Params {
     size_t h_row_bytes;
     int gpc_h;                  // groups per block of the h fragments
     float *y_pair, *y_shared;
+    int32_t *work;              // items claimed beyond the first one per CTA; zero on entry
     int32_t *err;
     int T, k, nchunks, tiles, out_rows;   // nchunks: k-chunks of the reduction; out_rows: d (down)
+    int dynamic;                // 1: items after the first from the counter; 0: CTA c takes c, c + G, ...
 };
 
 // Packed nibbles -> fp16 subnormal pairs: lo takes the nibbles at bits 0-3 and
@@ -200,12 +213,12 @@ struct Consumer {
 };
 
 // One pass over an item's tokens [t0, t0 + ntok), NT = ceil(ntok / 4) n-tiles.
-template <int MODE, int TOK, int CPS, int GPC, int NT>
+template <int MODE, int TOK, int CPS, int GPC, int GS, int NT>
 __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0, int ntok, Consumer &cs,
-                                         const uint32_t (&qoff)[Cfg<MODE, TOK, CPS, GPC>::kGpw], uint32_t soff,
+                                         const uint32_t (&qoff)[Cfg<MODE, TOK, CPS, GPC, GS>::kGpw], uint32_t soff,
                                          uint32_t kb, uint32_t kbc, uint32_t kbf, uint32_t plane_off)
 {
-    using C = Cfg<MODE, TOK, CPS, GPC>;
+    using C = Cfg<MODE, TOK, CPS, GPC, GS>;
     constexpr int kGpw = C::kGpw;
     const int g = cs.g, t4 = cs.t4, lane = cs.lane, warp = cs.warp;
     // stage offsets of this lane's B chunk (token g/2 of each n-tile, plane g&1) and of the
@@ -226,14 +239,12 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
 #pragma unroll
     for (int n = 0; n < NT; n++)
         acc[n][0] = acc[n][1] = 0.f;
-    // gate/up: the x factor of token t4 of each n-tile, loaded now and used in the epilogue
+    // gate/up: the x factor of token t4 of each n-tile (every group's factor slot of an x fragment
+    // block holds it), read from the first stage and used in the epilogue
     float xfac[NT];
 #pragma unroll
-    for (int n = 0; n < NT; n++) {
-        const int tl = n * 4 + t4;
-        xfac[n] = (MODE == kGateUp && (warp == 2 || warp == 3) && tl < ntok)
-                      ? p.x_scale[act_row<MODE>(p, it, t0 + tl)] : 0.f;
-    }
+    for (int n = 0; n < NT; n++)
+        xfac[n] = 0.f;
     const NibConst nk = {0x000F000Fu, 0x00080008u, 0x00F000F0u, 0x00800080u};
     const int nstages = p.nchunks / CPS;
 
@@ -245,20 +256,31 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
             *cs.abort = 1;
         }
         const uint8_t *sb = cs.base + cs.stage * C::kStageBytes;
-        // group scales of rows ra and ra + 8 for this warp's groups
-        float sa[kGpw], sc[kGpw];
-        if (kGpw == 2) {
+        if (MODE == kGateUp && c == 0) {
+#pragma unroll
+            for (int n = 0; n < NT; n++)
+                xfac[n] = *reinterpret_cast<const float *>(sb + foff[n]);
+        }
+        // group scales of rows ra and ra + 8 for this warp's groups (one per GS elements)
+        constexpr int kSpw = C::kSpw;
+        float sa[kSpw], sc[kSpw];
+        if (kSpw == 1) {
+            sa[0] = *reinterpret_cast<const float *>(sb + soff);
+            sc[0] = *reinterpret_cast<const float *>(sb + soff + 8 * C::kSpr * 4);
+        } else if (kSpw == 2) {
             const float2 va = *reinterpret_cast<const float2 *>(sb + soff);
-            const float2 vb = *reinterpret_cast<const float2 *>(sb + soff + 8 * GPC * 4);
-            sa[0] = va.x; sa[1 % kGpw] = va.y;
-            sc[0] = vb.x; sc[1 % kGpw] = vb.y;
+            const float2 vb = *reinterpret_cast<const float2 *>(sb + soff + 8 * C::kSpr * 4);
+            sa[0] = va.x; sa[1 % kSpw] = va.y;
+            sc[0] = vb.x; sc[1 % kSpw] = vb.y;
         } else {
 #pragma unroll
-            for (int v = 0; v < kGpw / 4; v++) {
+            for (int v = 0; v < kSpw / 4; v++) {
                 const float4 va = *reinterpret_cast<const float4 *>(sb + soff + 16 * v);
-                const float4 vb = *reinterpret_cast<const float4 *>(sb + soff + 8 * GPC * 4 + 16 * v);
-                sa[4 * v + 0] = va.x; sa[4 * v + 1] = va.y; sa[4 * v + 2] = va.z; sa[4 * v + 3] = va.w;
-                sc[4 * v + 0] = vb.x; sc[4 * v + 1] = vb.y; sc[4 * v + 2] = vb.z; sc[4 * v + 3] = vb.w;
+                const float4 vb = *reinterpret_cast<const float4 *>(sb + soff + 8 * C::kSpr * 4 + 16 * v);
+                sa[4 * v + 0] = va.x; sa[(4 * v + 1) % kSpw] = va.y;
+                sa[(4 * v + 2) % kSpw] = va.z; sa[(4 * v + 3) % kSpw] = va.w;
+                sc[4 * v + 0] = vb.x; sc[(4 * v + 1) % kSpw] = vb.y;
+                sc[(4 * v + 2) % kSpw] = vb.z; sc[(4 * v + 3) % kSpw] = vb.w;
             }
         }
 #pragma unroll
@@ -276,7 +298,7 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
                 float d[4];
                 mma_f16_16816(d, a0, bv.x, bv.y, cin);
                 mma_f16_16816(d, a1, bv.z, bv.w, d);
-                float fa = sa[gi], fb = sc[gi];
+                float fa = sa[gi * 32 / GS], fb = sc[gi * 32 / GS];
                 if (MODE == kDown) {
                     const float hf = *reinterpret_cast<const float *>(sb + foff[n] + gi * 4);
                     fa *= hf;
@@ -304,8 +326,10 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
     named_bar_sync(1, kConsumerWarps * 32);
     auto part = [&](int w, int n) { return cs.red[(w * C::kNTM + n) * 32 + lane]; };
     if (MODE == kGateUp) {
-        if (warp == 2 || warp == 3) {
-            // up warps of k-half 0: h for rows 16 * mtile + g (+ 8), token t4 of each n-tile
+        const bool hw = warp == 2 || warp == 3;   // up warps of k-half 0: rows 16 * mtile + g (+ 8)
+        const int rg = cs.mtile * 16 + g;
+        if (hw) {
+            // h for rows rg (+ 8), token t4 of each n-tile
 #pragma unroll
             for (int n = 0; n < NT; n++) {
                 const int tl = n * 4 + t4;
@@ -316,8 +340,8 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
                 const float2 u0 = part(warp, n), u1 = part(warp + 4, n);
                 const float gva = (g0.x + g1.x) * xf, gvb = (g0.y + g1.y) * xf;
                 const float uva = (u0.x + u1.x) * xf, uvb = (u0.y + u1.y) * xf;
-                cs.hbuf[tl * 32 + cs.mtile * 16 + g] = gva / (1.0f + expf(-gva)) * uva;
-                cs.hbuf[tl * 32 + cs.mtile * 16 + g + 8] = gvb / (1.0f + expf(-gvb)) * uvb;
+                cs.hbuf[tl * 32 + rg] = gva / (1.0f + expf(-gva)) * uva;
+                cs.hbuf[tl * 32 + rg + 8] = gvb / (1.0f + expf(-gvb)) * uvb;
             }
         }
         named_bar_sync(1, kConsumerWarps * 32);
@@ -378,10 +402,10 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
 }
 
 // Weight loads (packed rows and scales) of stage `c` of an item into ring slot sb.
-template <int MODE, int TOK, int CPS, int GPC>
+template <int MODE, int TOK, int CPS, int GPC, int GS>
 __device__ __forceinline__ void issue_weights(const Maps &maps, const Item &it, int c, uint32_t sb, uint32_t fb)
 {
-    using C = Cfg<MODE, TOK, CPS, GPC>;
+    using C = Cfg<MODE, TOK, CPS, GPC, GS>;
     const int z = it.expert < 0 ? 0 : it.expert;
     const int w = it.expert < 0 ? 1 : 0;
     const int row0 = it.tile * C::kRows;
@@ -401,22 +425,23 @@ __device__ __forceinline__ void issue_weights(const Maps &maps, const Item &it, 
         const int cg = c * CPS + ch;
         if (MODE == kGateUp) {
             tma_load_4d(sb + ch * C::kMats * C::kQSub, mq, cg * C::kRowB, row0, 0, z, fb);
-            tma_load_4d(sb + C::kSOff + ch * C::kMats * C::kSSub, ms, cg * GPC, row0, 0, z, fb);
+            tma_load_4d(sb + C::kSOff + ch * C::kMats * C::kSSub, ms, cg * C::kSpr, row0, 0, z, fb);
         } else {
             tma_load_3d(sb + ch * C::kQSub, mq, cg * C::kRowB, row0, z, fb);
-            tma_load_3d(sb + C::kSOff + ch * C::kSSub, ms, cg * GPC, row0, z, fb);
+            tma_load_3d(sb + C::kSOff + ch * C::kSSub, ms, cg * C::kSpr, row0, z, fb);
         }
     }
 }
 
-template <int MODE, int TOK, int CPS, int GPC>
+template <int MODE, int TOK, int CPS, int GPC, int GS>
 __global__ void __launch_bounds__(kThreads, 2)
 ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
 {
-    using C = Cfg<MODE, TOK, CPS, GPC>;
+    using C = Cfg<MODE, TOK, CPS, GPC, GS>;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t full_bar[C::kStages];
     __shared__ __align__(8) uint64_t empty_bar[C::kStages];
+    __shared__ int stage_item[C::kStages];   // item of the stage in each slot (-1: no more items)
     __shared__ volatile int abort_flag;
 
     const uint32_t raw = smem_addr(dyn_smem);
@@ -470,8 +495,9 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
             if (lane == 0)
                 for (int c = 0; c < pre; c++) {
                     const uint32_t fb = smem_addr(&full_bar[c]);
+                    stage_item[c] = blockIdx.x;
                     mbar_arrive_expect_tx(fb, C::kWeightBytes + ntok * C::kTokBytes);
-                    issue_weights<MODE, TOK, CPS, GPC>(maps, it0, c, stage0 + c * C::kStageBytes, fb);
+                    issue_weights<MODE, TOK, CPS, GPC, GS>(maps, it0, c, stage0 + c * C::kStageBytes, fb);
                 }
         }
     }
@@ -494,7 +520,12 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
         uint32_t phase = 0;
         uint32_t issued = (1u << pre) - 1u;   // bit s: stage s was filled at least once
         bool first = true;
-        for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+        int i = blockIdx.x;
+        while (i < n_items) {
+            // claim the next item now: the atomic's round trip overlaps this item's loads
+            int next = i + (int)gridDim.x;
+            if (lane == 0 && p.dynamic)
+                next = (int)gridDim.x + atomicAdd(p.work, 1);
             const Item it = decode_item(p, tab, i);
             const int npass = (it.m + TOK - 1) / TOK;
             for (int pass = 0; pass < npass; pass++) {
@@ -517,8 +548,9 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
                         const uint32_t sb = stage0 + stage * C::kStageBytes;
                         const uint32_t fb = smem_addr(&full_bar[stage]);
                         if (lane == 0 && !pre_issued) {
+                            stage_item[stage] = i;   // published to the consumers by the arrive below
                             mbar_arrive_expect_tx(fb, tx);
-                            issue_weights<MODE, TOK, CPS, GPC>(maps, it, c, sb, fb);
+                            issue_weights<MODE, TOK, CPS, GPC, GS>(maps, it, c, sb, fb);
                             issued |= 1u << stage;
                         }
                         if (c == 0 && lane < ntok)
@@ -535,6 +567,24 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
                 }
             }
             first = false;
+            i = __shfl_sync(0xffffffffu, next, 0);
+        }
+        // no more items: one more slot, tagged -1 and completed without data, stops the consumers
+        // (only when they follow the tags; in the fixed order they know where to stop)
+        if (p.dynamic && lane == 0 && !abort_flag) {
+            if (!mbar_wait_or_abort(smem_addr(&empty_bar[stage]), phase ^ 1u, &abort_flag)) {
+                atomicOr(p.err, MOE_DEVERR_TIMEOUT);
+                abort_flag = 1;
+            } else {
+                stage_item[stage] = -1;
+                mbar_arrive(smem_addr(&full_bar[stage]));
+                issued |= 1u << stage;
+            }
+        }
+        __syncwarp();
+        if (p.dynamic && ++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
         }
         // Let every copy issued here land before the CTA may exit: stages below
         // `stage` were last filled in the current round, the rest in the
@@ -578,13 +628,29 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
     for (int gi = 0; gi < C::kGpw; gi++)
         qoff[gi] = (ch0 * C::kMats + mat) * C::kQSub + ra * C::kRowB + (((gl0 + gi) ^ swz<GPC>(ra)) << 4) +
                    4 * cs.t4;
-    const uint32_t soff = C::kSOff + (ch0 * C::kMats + mat) * C::kSSub + (ra * GPC + gl0) * 4;
+    const uint32_t soff = C::kSOff + (ch0 * C::kMats + mat) * C::kSSub + (ra * C::kSpr + gl0 * 32 / GS) * 4;
     const uint32_t kb = ch0 * C::kBlk + gl0 * 64;
     const uint32_t kbc = ch0 * C::kBlk + frag_corr(GPC) + gl0 * 8;
     const uint32_t kbf = ch0 * C::kBlk + frag_fac(GPC) + gl0 * 4;
     const uint32_t plane_off = (cs.g & 1) * frag_lo(GPC) + cs.t4 * 16;
 
-    for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+    for (int ii = blockIdx.x;; ii += gridDim.x) {
+        int i = ii;
+        if (p.dynamic) {
+            // the next slot's tag names its item (the first stage of that item: the passes below then
+            // wait on this slot again, which returns at once)
+            if (!mbar_wait_or_abort(smem_addr(&full_bar[cs.stage]), cs.phase, &abort_flag)) {
+                if (lane == 0)
+                    atomicOr(p.err, MOE_DEVERR_TIMEOUT);
+                abort_flag = 1;
+                break;
+            }
+            i = stage_item[cs.stage];
+            if (i < 0)
+                break;
+        } else if (i >= n_items) {
+            break;   // fixed order: CTA c takes c, c + G, ...
+        }
         const Item it = decode_item(p, tab, i);
         const int npass = (it.m + TOK - 1) / TOK;
         for (int pass = 0; pass < npass; pass++) {
@@ -592,24 +658,24 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
             pass_range(it.m, npass, pass, t0, ntok);
             const int nt = (ntok + 3) >> 2;
             if (nt <= 1)
-                run_pass<MODE, TOK, CPS, GPC, 1>(p, it, t0, ntok, cs, qoff, soff, kb, kbc, kbf, plane_off);
+                run_pass<MODE, TOK, CPS, GPC, GS, 1>(p, it, t0, ntok, cs, qoff, soff, kb, kbc, kbf, plane_off);
             else if (C::kNTM >= 2 && nt == 2)
-                run_pass<MODE, TOK, CPS, GPC, (C::kNTM >= 2 ? 2 : 1)>(p, it, t0, ntok, cs, qoff, soff, kb, kbc,
+                run_pass<MODE, TOK, CPS, GPC, GS, (C::kNTM >= 2 ? 2 : 1)>(p, it, t0, ntok, cs, qoff, soff, kb, kbc,
                                                                       kbf, plane_off);
             else if (C::kNTM >= 3 && nt == 3)
-                run_pass<MODE, TOK, CPS, GPC, (C::kNTM >= 3 ? 3 : 1)>(p, it, t0, ntok, cs, qoff, soff, kb, kbc,
+                run_pass<MODE, TOK, CPS, GPC, GS, (C::kNTM >= 3 ? 3 : 1)>(p, it, t0, ntok, cs, qoff, soff, kb, kbc,
                                                                       kbf, plane_off);
             else
-                run_pass<MODE, TOK, CPS, GPC, C::kNTM>(p, it, t0, ntok, cs, qoff, soff, kb, kbc, kbf, plane_off);
+                run_pass<MODE, TOK, CPS, GPC, GS, C::kNTM>(p, it, t0, ntok, cs, qoff, soff, kb, kbc, kbf, plane_off);
         }
     }
 }
 
-template <int MODE, int TOK, int CPS, int GPC>
+template <int MODE, int TOK, int CPS, int GPC, int GS>
 int launch_one(const Maps &maps, const Params &prm, int max_items, int max_units, cudaStream_t s)
 {
-    using C = Cfg<MODE, TOK, CPS, GPC>;
-    auto kern = ffn_decode_kernel<MODE, TOK, CPS, GPC>;
+    using C = Cfg<MODE, TOK, CPS, GPC, GS>;
+    auto kern = ffn_decode_kernel<MODE, TOK, CPS, GPC, GS>;
     const size_t smem = C::kSmem + ((size_t)max_units * sizeof(Unit) + 15) / 16 * 16;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
@@ -645,20 +711,20 @@ int launch_one(const Maps &maps, const Params &prm, int max_items, int max_units
 
 // Pass width by batch size: one token per pass for T = 1 (two k-chunks per
 // stage when the chunk count is even), else up to 4, 8 or 16 tokens.
-template <int MODE, int GPC>
+template <int MODE, int GPC, int GS>
 int launch_tok(const Maps &maps, const Params &prm, int max_units, int T, cudaStream_t s)
 {
     const int mi = max_units * prm.tiles;
     if (T == 1)
-        return prm.nchunks % 2 == 0 ? launch_one<MODE, 1, 2, GPC>(maps, prm, mi, max_units, s)
-                                    : launch_one<MODE, 1, 1, GPC>(maps, prm, mi, max_units, s);
+        return prm.nchunks % 2 == 0 ? launch_one<MODE, 1, 2, GPC, GS>(maps, prm, mi, max_units, s)
+                                    : launch_one<MODE, 1, 1, GPC, GS>(maps, prm, mi, max_units, s);
     if (T <= 4)
-        return launch_one<MODE, 4, 1, GPC>(maps, prm, mi, max_units, s);
+        return launch_one<MODE, 4, 1, GPC, GS>(maps, prm, mi, max_units, s);
     // 8 tokens per pass up to T = 32 (measured faster than 16 at T = 16 and 32: fewer registers,
     // no spills); above, 16, so that an expert taken by many tokens is streamed fewer times
     if (T <= 32)
-        return launch_one<MODE, 8, 1, GPC>(maps, prm, mi, max_units, s);
-    return launch_one<MODE, 16, 1, GPC>(maps, prm, mi, max_units, s);
+        return launch_one<MODE, 8, 1, GPC, GS>(maps, prm, mi, max_units, s);
+    return launch_one<MODE, 16, 1, GPC, GS>(maps, prm, mi, max_units, s);
 }
 
 }  // namespace
@@ -681,6 +747,10 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
     const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const int cps_gu = (a.T == 1 && (d / 256) % 2 == 0) ? 2 : 1;
     const int cps_dn = (a.T == 1 && (f / (32 * gpc_h)) % 2 == 0) ? 2 : 1;
+    // scales per row of a chunk: a gate/up chunk is 256 elements, a down chunk 32 * gpc_h
+    const uint32_t spr_gu = 256 / G, spr_dn = 32 * gpc_h / G;
+    if (spr_dn * 4 % 16 != 0)
+        return MOE_ERR_UNSUPPORTED;   // a scale box row must be a multiple of 16 bytes
     Maps gu{}, dn{};
     gu.merged = dn.merged = 1;
     for (int i = 0; i < 2 && rc == MOE_OK; i++) {
@@ -688,16 +758,16 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
         const uint64_t gq_dim[5] = {128, (uint64_t)f, 2, (uint64_t)d / 256, outer[i]};
         const uint64_t gq_str[4] = {(uint64_t)d / 2, (uint64_t)f * d / 2, 128, qb};
         const uint32_t gq_box[5] = {128, 32, 2, (uint32_t)cps_gu, 1};
-        const uint64_t gs_dim[5] = {8, (uint64_t)f, 2, (uint64_t)d / 256, outer[i]};
-        const uint64_t gs_str[4] = {(uint64_t)(d / G) * 4, (uint64_t)f * (d / G) * 4, 32, sc * 4};
-        const uint32_t gs_box[5] = {8, 32, 2, (uint32_t)cps_gu, 1};
+        const uint64_t gs_dim[5] = {spr_gu, (uint64_t)f, 2, (uint64_t)d / 256, outer[i]};
+        const uint64_t gs_str[4] = {(uint64_t)(d / G) * 4, (uint64_t)f * (d / G) * 4, spr_gu * 4, sc * 4};
+        const uint32_t gs_box[5] = {spr_gu, 32, 2, (uint32_t)cps_gu, 1};
         // down: (bytes of a chunk, row, chunk, expert)
         const uint64_t dq_dim[4] = {(uint64_t)16 * gpc_h, (uint64_t)d, (uint64_t)f / (32 * gpc_h), outer[i]};
         const uint64_t dq_str[3] = {(uint64_t)f / 2, (uint64_t)16 * gpc_h, qb};
         const uint32_t dq_box[4] = {(uint32_t)16 * gpc_h, 64, (uint32_t)cps_dn, 1};
-        const uint64_t ds_dim[4] = {(uint64_t)gpc_h, (uint64_t)d, (uint64_t)f / (32 * gpc_h), outer[i]};
-        const uint64_t ds_str[3] = {(uint64_t)(f / G) * 4, (uint64_t)gpc_h * 4, sc * 4};
-        const uint32_t ds_box[4] = {(uint32_t)gpc_h, 64, (uint32_t)cps_dn, 1};
+        const uint64_t ds_dim[4] = {spr_dn, (uint64_t)d, (uint64_t)f / (32 * gpc_h), outer[i]};
+        const uint64_t ds_str[3] = {(uint64_t)(f / G) * 4, (uint64_t)spr_dn * 4, sc * 4};
+        const uint32_t ds_box[4] = {spr_dn, 64, (uint32_t)cps_dn, 1};
         if (gu.merged)
             gu.merged = make_tmap_nd(&gu.q[i], qs[i], U8, 5, gq_dim, gq_str, gq_box, CU_TENSOR_MAP_SWIZZLE_128B) ==
                             MOE_OK &&
@@ -716,7 +786,7 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
         const uint32_t q_box[4] = {128, 32, 2, 1};
         const uint64_t s_dim[4] = {(uint64_t)d / G, (uint64_t)f, 2, outer[i]};
         const uint64_t s_str[3] = {(uint64_t)(d / G) * 4, (uint64_t)f * (d / G) * 4, sc * 4};
-        const uint32_t s_box[4] = {8, 32, 2, 1};
+        const uint32_t s_box[4] = {spr_gu, 32, 2, 1};
         rc |= make_tmap_nd(&gu.q[i], qs[i], U8, 4, q_dim, q_str, q_box, CU_TENSOR_MAP_SWIZZLE_128B);
         rc |= make_tmap_nd(&gu.s[i], ss[i], F32, 4, s_dim, s_str, s_box, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
@@ -724,7 +794,7 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
         rc |= make_tmap_3d(&dn.q[i], qs[i] + (size_t)f * d, U8, 1, f / 2, d, outer[i], f / 2, qb, 16 * gpc_h, 64,
                            sw_dn);
         rc |= make_tmap_3d(&dn.s[i], ss[i] + (size_t)2 * f * d / G, F32, 4, f / G, d, outer[i],
-                           (uint64_t)(f / G) * 4, sc * 4, gpc_h, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+                           (uint64_t)(f / G) * 4, sc * 4, spr_dn, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     if (rc != MOE_OK)
         return MOE_ERR_INVALID_ARG;
@@ -739,13 +809,19 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
     pg.h_out = a.h_frag;
     pg.h_row_bytes = frag_row_bytes(f, gpc_h);
     pg.gpc_h = gpc_h;
+    pg.work = a.work;
+    // T = 1: every unit has one token and the items are equal, so the fixed order c, c + G, ...
+    // balances them as well as claiming would (and saves the atomics, measured 2 us faster per
+    // layer); larger batches give units of very different lengths: claim dynamically
+    pg.dynamic = a.T > 1 ? 1 : 0;
     pg.err = a.err;
     pg.T = a.T;
     pg.k = a.k;
     pg.nchunks = d / 256;
     pg.tiles = f / 32;
     pg.out_rows = f;
-    rc = launch_tok<kGateUp, 8>(gu, pg, max_experts, a.T, s);
+    rc = G == 64 ? launch_tok<kGateUp, 8, 64>(gu, pg, max_experts, a.T, s)
+                 : launch_tok<kGateUp, 8, 32>(gu, pg, max_experts, a.T, s);
     if (rc != MOE_OK)
         return rc;
 
@@ -756,12 +832,15 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
     pd.h_out = nullptr;
     pd.y_pair = a.y_pair;
     pd.y_shared = a.y_shared;
+    pd.work = a.work + 1;
+
     pd.nchunks = f / (32 * gpc_h);
     pd.tiles = d / 64;
     pd.out_rows = d;
     if (gpc_h == 8)
-        return launch_tok<kDown, 8>(dn, pd, max_experts, a.T, s);
-    return launch_tok<kDown, 4>(dn, pd, max_experts, a.T, s);
+        return G == 64 ? launch_tok<kDown, 8, 64>(dn, pd, max_experts, a.T, s)
+                       : launch_tok<kDown, 8, 32>(dn, pd, max_experts, a.T, s);
+    return launch_tok<kDown, 4, 32>(dn, pd, max_experts, a.T, s);   // G = 64 needs gpc_h = 8 (checked above)
 }
 
 }  // namespace moe

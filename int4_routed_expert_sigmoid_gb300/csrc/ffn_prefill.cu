@@ -81,7 +81,7 @@ constexpr int kACol0 = 2 * kTileN;
 // RAWK: elements of a row per raw stage -- 256 (128-byte row segments, 128B
 // swizzle) when the reduction length allows it, else 128 (64 bytes, 64B swizzle).
 // A raw stage feeds two op stages of RAWK / 2 elements, one per dequant group.
-template <int MODE, int RAWK>
+template <int MODE, int RAWK, int GS>
 struct PCfg {
     static constexpr int kRawK = RAWK;
     static constexpr int kRowB = RAWK / 2;                     // packed bytes of a row per raw stage
@@ -94,7 +94,9 @@ struct PCfg {
     static constexpr int kRawMats = MODE == kPGateUp ? 2 : 1;
     static constexpr int kRowsPerMat = kTileM / kRawMats;      // weight rows of one matrix per item
     static constexpr int kRawQ = kRowsPerMat * kRawK / 2;      // packed nibbles per matrix per raw stage
-    static constexpr int kRawS = kRowsPerMat * (kRawK / 32) * 4;
+    static constexpr int kSpr = kRawK / GS;                     // scales of a row per raw stage
+    static constexpr int kRawS = kRowsPerMat * kSpr * 4;
+    static_assert(kSpr * 4 % 16 == 0, "a scale box row is a multiple of 16 bytes");
     static constexpr int kRawStage = kRawMats * (kRawQ + kRawS);   // 20 KB (RAWK 256) or 10 KB
     static constexpr int kRawStages = RAWK == 256 ? 4 : 6;
     static constexpr int kOpB = kTileN * kOpK * 2;             // fp16 token rows of a stage (A is in TMEM)
@@ -285,11 +287,11 @@ __device__ __forceinline__ uint32_t pack_scale(float s)
     return *reinterpret_cast<const uint32_t *>(&b);
 }
 
-template <int MODE, int RAWK>
+template <int MODE, int RAWK, int GS>
 __global__ void __launch_bounds__(kPThreads, 1)
 ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
 {
-    using C = PCfg<MODE, RAWK>;
+    using C = PCfg<MODE, RAWK, GS>;
     constexpr int N = kTileN;
     constexpr bool kF16 = true;   // operand type of both GEMMs
     extern __shared__ uint8_t dyn_smem[];
@@ -358,10 +360,10 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                         mbar_arrive_expect_tx(fb, C::kRawStage);
                         if (MODE == kPGateUp) {   // both matrices in one load each
                             tma_load_4d(sb, &maps.q[w], r * C::kRowB, wrow0, 0, z, fb);
-                            tma_load_4d(sb + 2 * C::kRawQ, &maps.s[w], r * C::kChunks, wrow0, 0, z, fb);
+                            tma_load_4d(sb + 2 * C::kRawQ, &maps.s[w], r * C::kSpr, wrow0, 0, z, fb);
                         } else {
                             tma_load_3d(sb, &maps.q[w], r * C::kRowB, wrow0, z, fb);
-                            tma_load_3d(sb + C::kRawQ, &maps.s[w], r * C::kChunks, wrow0, z, fb);
+                            tma_load_3d(sb + C::kRawQ, &maps.s[w], r * C::kSpr, wrow0, z, fb);
                         }
                     }
                     if (++rs == C::kRawStages) {
@@ -424,7 +426,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                 // c ^ ((r >> 1) & 3)); chunk c = group c of the raw stage
                 const uint8_t *qrow = rsb + mat * C::kRawQ + r * C::kRowB;
                 const float *srow = reinterpret_cast<const float *>(rsb + C::kRawMats * C::kRawQ + mat * C::kRawS +
-                                                                    r * C::kChunks * 4);
+                                                                    r * C::kSpr * 4);
                 const int sw = RAWK == 256 ? (r & 7) : ((r >> 1) & 3);
                 uint4 wv[C::kCPO];
                 float sg[C::kCPO];
@@ -434,7 +436,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
                 for (int q = 0; q < C::kCPO; q++) {
                     const int c = g * C::kCPO + q;
                     wv[q] = *reinterpret_cast<const uint4 *>(qrow + ((c ^ sw) << 4));
-                    sg[q] = srow[c] * rowfac;   // exact: a power of two
+                    sg[q] = srow[c * 32 / GS] * rowfac;   // exact: a power of two
                     const float a = fabsf(sg[q]);
                     range_bad |= a > 0.f && (a < 0x1p-14f || a > 8192.0f);
                 }
@@ -762,11 +764,11 @@ int make_tmap_rows(CUtensorMap *m, const uint16_t *base, int K, size_t rows, int
     return make_tmap_nd(m, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, dim, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int MODE, int RAWK>
+template <int MODE, int RAWK, int GS>
 int launch_prefill_one(const PMaps &maps, const PParams &prm, int max_units, cudaStream_t s)
 {
-    using C = PCfg<MODE, RAWK>;
-    auto kern = ffn_prefill_kernel<MODE, RAWK>;
+    using C = PCfg<MODE, RAWK, GS>;
+    auto kern = ffn_prefill_kernel<MODE, RAWK, GS>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return MOE_ERR_CUDA;
@@ -848,16 +850,16 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     for (int i = 0; i < 2 && rc == MOE_OK; i++) {
         const uint64_t q_dim[4] = {(uint64_t)d / 2, (uint64_t)f, 2, outer[i]};
         const uint64_t q_str[3] = {(uint64_t)d / 2, (uint64_t)f * d / 2, qb};
-        const uint32_t q_box[4] = {128, (uint32_t)PCfg<kPGateUp, 256>::kRowsPerMat, 2, 1};
+        const uint32_t q_box[4] = {128, (uint32_t)PCfg<kPGateUp, 256, 32>::kRowsPerMat, 2, 1};
         const uint64_t s_dim[4] = {(uint64_t)d / G, (uint64_t)f, 2, outer[i]};
         const uint64_t s_str[3] = {(uint64_t)(d / G) * 4, (uint64_t)f * (d / G) * 4, sc * 4};
-        const uint32_t s_box[4] = {8, (uint32_t)PCfg<kPGateUp, 256>::kRowsPerMat, 2, 1};
+        const uint32_t s_box[4] = {(uint32_t)(256 / G), (uint32_t)PCfg<kPGateUp, 256, 32>::kRowsPerMat, 2, 1};
         rc |= make_tmap_nd(&gm.q[i], qs[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, q_dim, q_str, q_box,
                            CU_TENSOR_MAP_SWIZZLE_128B);
         rc |= make_tmap_nd(&gm.s[i], ss[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s_dim, s_str, s_box,
                            CU_TENSOR_MAP_SWIZZLE_NONE);
     }
-    rc |= make_tmap_rows(&gm.b, x_sorted, d, rows, PCfg<kPGateUp, 256>::kBChunks);
+    rc |= make_tmap_rows(&gm.b, x_sorted, d, rows, PCfg<kPGateUp, 256, 32>::kBChunks);
     if (rc != MOE_OK)
         return MOE_ERR_INVALID_ARG;
     PParams pg{};
@@ -876,10 +878,12 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pg.T = T;
     pg.k = k;
     pg.K = d;
-    pg.mtiles = f / PCfg<kPGateUp, 256>::kRowsPerMat;
+    pg.mtiles = f / PCfg<kPGateUp, 256, 32>::kRowsPerMat;
     pg.out_rows = f;
     const int max_units = (E < T * k ? E : T * k) + 1;
-    rc = launch_prefill_one<kPGateUp, 256>(gm, pg, max_units, s);   // d is a multiple of 256
+    // d is a multiple of 256
+    rc = G == 64 ? launch_prefill_one<kPGateUp, 256, 64>(gm, pg, max_units, s)
+                 : launch_prefill_one<kPGateUp, 256, 32>(gm, pg, max_units, s);
     if (rc == MOE_OK)
         rc = launch_pdl(h_to_f16_kernel, (int)rows, 256, 0, s, (const float *)ps.h32, f, h_sorted, ps.h_scale);
     if (rc != MOE_OK)
@@ -887,16 +891,18 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
 
     // ---- down
     const int dn_rawk = f % 256 == 0 ? 256 : 128;
+    if (dn_rawk / G * 4 % 16 != 0)
+        return MOE_ERR_UNSUPPORTED;   // G = 64 needs f a multiple of 256 (a scale box row of 16 bytes)
     PMaps dm{};
     for (int i = 0; i < 2 && rc == MOE_OK; i++) {
         rc |= make_tmap_3d(&dm.q[i], qs[i] + (size_t)f * d, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, f / 2, d, outer[i],
                            f / 2, qb, dn_rawk / 2, kTileM,
                            dn_rawk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
         rc |= make_tmap_3d(&dm.s[i], ss[i] + (size_t)2 * f * d / G, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, f / G, d,
-                           outer[i], (uint64_t)(f / G) * 4, sc * 4, dn_rawk / 32, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                           outer[i], (uint64_t)(f / G) * 4, sc * 4, dn_rawk / G, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
-    rc |= make_tmap_rows(&dm.b, h_sorted, f, rows, dn_rawk == 256 ? PCfg<kPDown, 256>::kBChunks
-                                                                   : PCfg<kPDown, 128>::kBChunks);
+    rc |= make_tmap_rows(&dm.b, h_sorted, f, rows, dn_rawk == 256 ? PCfg<kPDown, 256, 32>::kBChunks
+                                                                   : PCfg<kPDown, 128, 32>::kBChunks);
     if (rc != MOE_OK)
         return MOE_ERR_INVALID_ARG;
     PParams pd = pg;
@@ -912,8 +918,9 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pd.mtiles = d / kTileM;
     pd.out_rows = d;
     if (dn_rawk == 256)
-        return launch_prefill_one<kPDown, 256>(dm, pd, max_units, s);
-    return launch_prefill_one<kPDown, 128>(dm, pd, max_units, s);
+        return G == 64 ? launch_prefill_one<kPDown, 256, 64>(dm, pd, max_units, s)
+                       : launch_prefill_one<kPDown, 256, 32>(dm, pd, max_units, s);
+    return launch_prefill_one<kPDown, 128, 32>(dm, pd, max_units, s);
 }
 
 }  // namespace moe

@@ -32,7 +32,9 @@ int check_layer(const moe_layer_int4 *w)
         return MOE_ERR_INVALID_ARG;
     if (w->E < 1 || w->E > 1024 || w->d < 1 || w->f < 1)
         return MOE_ERR_INVALID_ARG;
-    if (w->G != 32 || w->d % 256 != 0 || w->f % 128 != 0)
+    // group sizes 32 and 64 (the README's group-scaled container); with 64, f must be a multiple of
+    // 256 so that every scale tile row the kernels load is a whole 16 bytes
+    if ((w->G != 32 && w->G != 64) || w->d % 256 != 0 || w->f % 128 != 0 || (w->G == 64 && w->f % 256 != 0))
         return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
@@ -54,6 +56,7 @@ size_t ffn_scratch_bytes_mode(int T, int k, int d, int f, int mode);
 struct FfnScratch {
     uint8_t *x_frag, *h_frag;
     float *x_scale;
+    int32_t *work;   // the decode FFN's item counters
 };
 
 size_t ffn_scratch_layout(int T, int k, int d, int f, uint8_t *base, FfnScratch *out)
@@ -69,6 +72,7 @@ size_t ffn_scratch_layout(int T, int k, int d, int f, uint8_t *base, FfnScratch 
     s.x_frag = take((size_t)T * frag_row_bytes(d, 8));
     s.x_scale = reinterpret_cast<float *>(take((size_t)T * sizeof(float)));
     s.h_frag = take(rows_h * frag_row_bytes(f, frag_gpc_h(f)));
+    s.work = reinterpret_cast<int32_t *>(take(kDecodeCounters * sizeof(int32_t)));
     if (out)
         *out = s;
     return off;
@@ -235,7 +239,7 @@ int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *
     FfnScratch sc{};
     ffn_scratch_layout(T, k, w->d, w->f, static_cast<uint8_t *>(workspace), &sc);
     const cudaStream_t s = as_stream(stream);
-    rc = launch_act_frag(x, T, w->d, sc.x_frag, sc.x_scale, s);
+    rc = launch_act_frag(x, T, w->d, sc.x_frag, sc.x_scale, sc.work, kDecodeCounters, s);
     if (rc != MOE_OK)
         return rc;
     DecodeFfnArgs a{};
@@ -251,6 +255,7 @@ int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *
     a.h_frag = sc.h_frag;
     a.y_pair = y_pair;
     a.y_shared = y_shared;
+    a.work = sc.work;
     a.err = err;
     return launch_ffn_decode(a, s);
 }
@@ -353,7 +358,8 @@ int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bia
     // launches.  Larger batches use the separate stage kernels.
     const bool small = T <= 8 && T * k <= 64;
     if (small) {
-        rc = launch_router_logits_frag(x, w_gate, T, d, E, sc.logits, fs.x_frag, fs.x_scale, s);
+        rc = launch_router_logits_frag(x, w_gate, T, d, E, sc.logits, fs.x_frag, fs.x_scale, fs.work,
+                                       kDecodeCounters, s);
         if (rc == MOE_OK)
             rc = launch_select_union(sc.logits, bias, T, E, k, normalize, route_scale, top_p, idx, wt, sc.counts,
                                      sc.offsets, sc.perm, sc.sorted_pair, sc.uniq, sc.n_uniq, hits, err, s);
@@ -365,7 +371,7 @@ int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bia
             rc = launch_union(idx, T, k, E, sc.counts, sc.offsets, sc.perm, sc.sorted_pair, sc.uniq,
                               sc.n_uniq, hits, err, s);
         if (rc == MOE_OK)
-            rc = launch_act_frag(x, T, d, fs.x_frag, fs.x_scale, s);
+            rc = launch_act_frag(x, T, d, fs.x_frag, fs.x_scale, fs.work, kDecodeCounters, s);
     }
     if (rc != MOE_OK)
         return rc;
@@ -382,6 +388,7 @@ int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bia
     a.h_frag = fs.h_frag;
     a.y_pair = sc.y_pair;
     a.y_shared = sc.y_shared;
+    a.work = fs.work;
     a.err = err;
     rc = launch_ffn_decode(a, s);
     if (rc != MOE_OK)

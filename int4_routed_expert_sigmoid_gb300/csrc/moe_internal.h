@@ -36,7 +36,8 @@ namespace moe {
 //   frag_lo(GPC)      lo plane  (64 bytes after hi: the two planes then fall
 //                               in different shared-memory banks)
 //   frag_corr(GPC)    [GPC][2] fp32: -2^-24 * corr of hi and lo
-//   frag_fac(GPC)     [GPC] fp32: per-group factor (h only)
+//   frag_fac(GPC)     [GPC] fp32: per-group factor (h), or the row factor in every
+//                     slot (x), so the factor travels with the stage's data
 // so one stage of the pipeline copies one token's blocks with a single bulk
 // copy.  x rows use GPC = 8; h rows GPC = 8 when f is a multiple of 256, else 4.
 // ---------------------------------------------------------------------------
@@ -75,14 +76,17 @@ int launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStr
 // router.cu
 int launch_router_logits(const float *x, const float *wg, int T, int d, int E, float *logits,
                          cudaStream_t s);
-// logits plus the FFN fragments of x in one kernel (T <= 8)
+// logits plus the FFN fragments of x in one kernel (T <= 8); also zeroes the nzero counters of the
+// decode FFN (after its grid wait, so no earlier kernel still uses them)
 int launch_router_logits_frag(const float *x, const float *wg, int T, int d, int E, float *logits,
-                              uint8_t *frag, float *row_scale, cudaStream_t s);
+                              uint8_t *frag, float *row_scale, int32_t *zero, int nzero, cudaStream_t s);
 // top_p >= 1: plain top-k; below, the pruned slots get id -1 and weight 0
 int launch_router_topk(const float *logits, const float *bias, int T, int E, int k, int normalize,
                        float route_scale, float top_p, int32_t *idx, float *w, cudaStream_t s);
-// fragments (GPC = 8) of `rows` rows of x [rows][K], K a multiple of 256
-int launch_act_frag(const float *x, int rows, int K, uint8_t *frag, float *row_scale, cudaStream_t s);
+// fragments (GPC = 8) of `rows` rows of x [rows][K], K a multiple of 256; also zeroes the nzero
+// counters of the decode FFN
+int launch_act_frag(const float *x, int rows, int K, uint8_t *frag, float *row_scale, int32_t *zero, int nzero,
+                    cudaStream_t s);
 
 // union.cu (an id of -1 is an empty slot: no group, perm -1, no hit, no error)
 int launch_union(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
@@ -104,8 +108,10 @@ struct DecodeFfnArgs {
     const float *x_scale;     // [T] per-row factor of x_frag
     uint8_t *h_frag;          // [T*k + T] rows of frag_row_bytes(f, frag_gpc_h(f)) (scratch)
     float *y_pair, *y_shared;
+    int32_t *work;            // kDecodeCounters item counters, zeroed by the kernel before (scratch)
     int32_t *err;
 };
+constexpr int kDecodeCounters = 2;   // items claimed by the gate/up and the down kernel
 int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s);
 
 // ffn_prefill.cu

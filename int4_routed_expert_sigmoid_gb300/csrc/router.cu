@@ -27,7 +27,7 @@ constexpr int kSkinnyIt = 8;   // d up to 8192: the weight slice of a thread sta
 
 __global__ void __launch_bounds__(kSkinnyThreads)
 logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, int T, int d, int E,
-                     float *__restrict__ logits, uint8_t *frag, float *row_scale)
+                     float *__restrict__ logits, uint8_t *frag, float *row_scale, int32_t *zero, int nzero)
 {
     griddep_launch_dependents();
     const int e0 = blockIdx.x * kEB;
@@ -117,8 +117,12 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
             logits[(size_t)(t0 + b) * E + e0 + a] = v;
         }
     }
-    // fused path: the first T blocks also build the FFN's fragments of x
+    // fused path: block (0, 0) zeroes the FFN's counters (this is after the grid wait: the previous
+    // layer's FFN, which used them, has finished), and the blocks build the FFN's fragments of x
     // (256-element chunks of the rows, spread over the blocks)
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < nzero; i += blockDim.x)
+            zero[i] = 0;
     const int chunks = d / 256;
     if (frag != nullptr && blockIdx.y == 0)
         for (int wu = blockIdx.x; wu < T * chunks; wu += gridDim.x) {
@@ -421,7 +425,8 @@ topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, in
 // each 8 are further divided by 16.  Each value becomes hi = fp16(v),
 // lo = fp16(v - hi); row_scale[r] = 2^(e-14) undoes the scaling.  The row is
 // written as fragment blocks of 8 groups (layout in moe_internal.h), with the
-// accumulator inputs -2^-24 * 8 * sum (16 at odd offsets, else 1) * value.
+// accumulator inputs -2^-24 * 8 * sum (16 at odd offsets, else 1) * value and,
+// in every group's factor slot, the row factor 2^(e-14).
 constexpr int kFragThreads = 256;
 constexpr int kXGpc = 8;
 
@@ -493,13 +498,19 @@ __device__ void act_frag_row(const float *__restrict__ x, int r, int K, int id0,
             float *c = reinterpret_cast<float *>(blk + frag_corr(kXGpc)) + gl * 2;
             c[0] = -chi * 0x1p-24f;
             c[1] = -clo * 0x1p-24f;
+            // every group's factor slot holds the row factor, so it reaches the FFN with each stage
+            reinterpret_cast<float *>(blk + frag_fac(kXGpc))[gl] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
         }
     }
 }
 
 __global__ void __launch_bounds__(kFragThreads)
-act_frag_kernel(const float *__restrict__ x, int K, uint8_t *__restrict__ frag, float *__restrict__ row_scale)
+act_frag_kernel(const float *__restrict__ x, int K, uint8_t *__restrict__ frag, float *__restrict__ row_scale,
+                int32_t *__restrict__ zero, int nzero)
 {
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < nzero; i += blockDim.x)
+            zero[i] = 0;
     act_frag_row(x, blockIdx.x, K, 0, (K / 32) * 4, frag, row_scale);
 }
 
@@ -547,19 +558,19 @@ int launch_router_logits(const float *x, const float *wg, int T, int d, int E, f
         logits_tiled_kernel<<<grid, 256, 0, s>>>(x, wg, T, d, E, logits);
     } else {
         dim3 grid((E + kEB - 1) / kEB, (T + kTB - 1) / kTB);
-        logits_skinny_kernel<<<grid, kSkinnyThreads, 0, s>>>(x, wg, T, d, E, logits, nullptr, nullptr);
+        logits_skinny_kernel<<<grid, kSkinnyThreads, 0, s>>>(x, wg, T, d, E, logits, nullptr, nullptr, nullptr, 0);
     }
     return cuda_status(cudaGetLastError());
 }
 
 int launch_router_logits_frag(const float *x, const float *wg, int T, int d, int E, float *logits,
-                              uint8_t *frag, float *row_scale, cudaStream_t s)
+                              uint8_t *frag, float *row_scale, int32_t *zero, int nzero, cudaStream_t s)
 {
     const int grid = (E + kEB - 1) / kEB;
     if (T > kTB)
         return MOE_ERR_UNSUPPORTED;
     return launch_pdl(logits_skinny_kernel, grid, kSkinnyThreads, 0, s, x, wg, T, d, E, logits, frag,
-                      row_scale);
+                      row_scale, zero, nzero);
 }
 
 int launch_router_topk(const float *logits, const float *bias, int T, int E, int k, int normalize,
@@ -574,11 +585,12 @@ int launch_router_topk(const float *logits, const float *bias, int T, int E, int
     return cuda_status(cudaGetLastError());
 }
 
-int launch_act_frag(const float *x, int rows, int K, uint8_t *frag, float *row_scale, cudaStream_t s)
+int launch_act_frag(const float *x, int rows, int K, uint8_t *frag, float *row_scale, int32_t *zero, int nzero,
+                    cudaStream_t s)
 {
     if (rows <= 0)
         return MOE_OK;
-    act_frag_kernel<<<rows, kFragThreads, 0, s>>>(x, K, frag, row_scale);
+    act_frag_kernel<<<rows, kFragThreads, 0, s>>>(x, K, frag, row_scale, zero, nzero);
     return cuda_status(cudaGetLastError());
 }
 

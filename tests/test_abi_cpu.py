@@ -62,10 +62,12 @@ def test_host_validation_rejects_without_launching(m):
     assert L.moe_rms_norm(ok, 1, 256, -1.0, ok, P) == m.MOE_ERR_INVALID_ARG
     assert L.moe_rms_norm(ok, 1, 256, float("nan"), ok, P) == m.MOE_ERR_INVALID_ARG
     assert L.moe_layer_forward(P, P, P, None, P, 1, 2, 1, 1.0, 0, P, P, P, P, P, 0, P, P) == m.MOE_ERR_INVALID_ARG
-    # a layer with an unsupported group size is refused before its pointers are used
-    fake = m._binding.moe_layer_int4(16, 16, 16, 16, 8, 256, 128, 64)
-    assert L.moe_expert_ffn_int4(P, ctypes.byref(fake), P, P, P, P, 1, 2, 0, P, P, P, 0, P, P) == \
-        m.MOE_ERR_UNSUPPORTED
+    # a layer with an unsupported group size is refused before its pointers are used: G = 48, and
+    # G = 64 with f not a multiple of 256
+    for G, f in ((48, 256), (64, 128)):
+        fake = m._binding.moe_layer_int4(16, 16, 16, 16, 8, 256, f, G)
+        assert L.moe_expert_ffn_int4(P, ctypes.byref(fake), P, P, P, P, 1, 2, 0, P, P, P, 0, P, P) == \
+            m.MOE_ERR_UNSUPPORTED
     # misaligned pointers are refused
     bad = ctypes.c_void_p(0x1004)
     assert L.moe_hits(bad, 8, bad, P) == m.MOE_ERR_INVALID_ARG

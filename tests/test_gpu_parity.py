@@ -20,6 +20,8 @@ SMALL = [
     Shape("single_token", E=33, k=3, d=256, f=256, T=1, bias="normal"),
     Shape("multi_pass", E=8, k=2, d=256, f=128, T=300),                     # > 16 tokens per expert
     Shape("k1", E=4, k=1, d=256, f=128, T=9, bias="normal"),
+    Shape("split4_t1", E=16, k=4, d=2048, f=256, T=1, bias="normal"),      # gate/up reduction in 4 parts
+    Shape("split2_t1", E=12, k=2, d=1024, f=128, T=1, bias="normal"),      # ... in 2 parts
 ]
 
 
@@ -445,3 +447,58 @@ def test_prefill_flags_scales_beyond_its_row_range():
     t = run_steps(dev, sh.k, teacher_idx=idx, teacher_w=np.full((sh.T, 2), 0.5), mode=m.MOE_MODE_PREFILL)
     assert t["err"] & m.MOE_DEVERR_SCALE_RANGE
     assert m.device_error(m.MOE_DEVERR_SCALE_RANGE) == m.MOE_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------- group size 64 ----
+G64 = [
+    Shape("g64_ragged", E=16, k=4, d=1024, f=512, T=37, G=64, bias="normal"),
+    Shape("g64_t1", E=12, k=3, d=2048, f=256, T=1, G=64, bias="normal"),
+    Shape("g64_multi_pass", E=8, k=2, d=256, f=256, T=300, G=64),
+]
+
+
+@pytest.mark.parametrize("shape", G64, ids=lambda s: s.name)
+def test_group_size_64_parity(shape):
+    """One scale per 64 elements (the gs64 container) on both FFN paths, against the oracle on its
+    routing; and bit for bit equal to the same layer stated with G = 32 and paired scales."""
+    from moe_testlib import TOL_PREFILL
+    m = moe()
+    L = workloads.layer_inputs(shape, seed=5, threads=4)
+    dev = device_layer(L)
+    k = shape.k
+    o_idx, o_w, _, _ = oracle.route(L.x, L.wg, L.bias, k)
+    o_union = oracle.union(o_idx, shape.E)
+    _, _, o_out = oracle_layer(L).dense()
+    # the same layer with G = 32: each scale repeated for both halves of its group
+    n32 = workloads.expert_s_count(shape.d, shape.f, 32)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    s32 = np.repeat(L.s_base.reshape(shape.E, -1), 2, axis=1).reshape(-1)
+    lw32 = m.LayerWeights(dev["layer"].q_base, t(s32), dev["layer"].shared_q, t(np.repeat(L.shared_s, 2)),
+                          E=shape.E, d=shape.d, f=shape.f, G=32)
+    assert s32.size == shape.E * n32
+    for mode, tol in ((m.MOE_MODE_DECODE, TOL_DECODE), (m.MOE_MODE_PREFILL, TOL_PREFILL)):
+        r = run_steps(dev, k, teacher_idx=o_idx, teacher_w=o_w, mode=mode)
+        assert r["err"] == 0
+        check_union_equal(r, o_union, shape.E)
+        assert rel_max_err(r["out"], o_out) <= tol, f"mode {mode}"
+        y_sh = oracle.expert_ffn_tokens(L.x, np.arange(shape.T), L.shared_q, L.shared_s, shape.d, shape.f, 64)
+        assert rel_max_err(r["y_shared"], y_sh) <= tol
+        for e in o_union["uniq"][:o_union["n_uniq"]]:
+            lo, hi = o_union["offsets"][e], o_union["offsets"][e + 1]
+            y = oracle.expert_ffn_tokens(L.x, o_union["sorted_pair"][lo:hi] // k, L.q_base[e], L.s_base[e],
+                                         shape.d, shape.f, 64)
+            assert rel_max_err(r["y_pair"][lo:hi], y) <= tol, f"mode {mode} expert {e}"
+        r32 = run_steps(dict(dev, layer=lw32), k, teacher_idx=o_idx, teacher_w=o_w, mode=mode)
+        assert r32["err"] == 0
+        assert np.array_equal(r["y_pair"][:o_union["offsets"][shape.E]], r32["y_pair"][:o_union["offsets"][shape.E]])
+        assert np.array_equal(r["y_shared"], r32["y_shared"]) and np.array_equal(r["out"], r32["out"])
+
+
+def test_group_size_64_needs_f_multiple_of_256():
+    m = moe()
+    sh = Shape("g64_bad", E=4, k=2, d=256, f=384, T=3, G=64)
+    L = workloads.layer_inputs(sh, seed=1, threads=2)
+    dev = device_layer(L)
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_layer_forward(dev["x"], dev["wg"], None, dev["layer"], sh.k)
+    assert ei.value.status == m.MOE_ERR_UNSUPPORTED

@@ -590,3 +590,38 @@ def test_results_do_not_depend_on_thread_count():
     assert all(np.array_equal(u, v) for u, v in zip(a, b))
     assert np.array_equal(ya, yb)
     assert np.array_equal(c[2][0], a[2][4])
+
+
+# ---------------------------------------------------------- group size 64 ----
+
+def test_dequant_group_size_64_boundaries():
+    """With G = 64, elements 63 and 64 of a row use different scales, 31 and 32 the same."""
+    rows, cols, G = 2, 256, 64
+    q, _ = oracle.int4_pack(np.ones(rows * cols, np.int8))
+    s = (np.arange(rows * cols // G, dtype=np.float32) + 1.0) * np.float32(0.25)
+    w = oracle.dequant(q, s, rows, cols, G)
+    for r in range(rows):
+        assert w[r, 31] == w[r, 32] == s[r * (cols // G)]
+        assert w[r, 63] == s[r * (cols // G)] and w[r, 64] == s[r * (cols // G) + 1]
+        assert w[r, 255] == s[r * (cols // G) + 3]
+
+
+def test_group_64_layer_equals_group_32_with_paired_scales():
+    """A layer with one scale per 64 elements is the layer with one scale per 32 elements whose
+    two halves of each 64-group share that scale: the same fp64 bits, expert by expert."""
+    sh64 = workloads.Shape("g64", E=6, k=2, d=256, f=256, T=5, G=64, bias="normal")
+    L = workloads.layer_inputs(sh64, seed=3, threads=2)
+    d, f = sh64.d, sh64.f
+    n32 = workloads.expert_s_count(d, f, 32)
+    s32 = np.repeat(L.s_base.reshape(sh64.E, -1), 2, axis=1).reshape(sh64.E, n32)
+    sh32 = np.repeat(L.shared_s, 2)
+    a = oracle.Layer(L.x, L.wg, L.bias, L.q_base, L.s_base, L.shared_q, L.shared_s, d=d, f=f, E=sh64.E,
+                     k=sh64.k, G=64).dense()
+    b = oracle.Layer(L.x, L.wg, L.bias, L.q_base, s32, L.shared_q, sh32, d=d, f=f, E=sh64.E, k=sh64.k,
+                     G=32).dense()
+    assert all(np.array_equal(u, v) for u, v in zip(a, b))
+    # the group size is read: the G = 64 scales taken as G = 32 scales (half of the expert's scale
+    # array, each used for 32 elements) give another result
+    e = oracle.expert_ffn(L.x[0], L.q_base[1], L.s_base[1], d, f, 64)
+    wrong = oracle.expert_ffn(L.x[0], L.q_base[1], np.concatenate([L.s_base[1], L.s_base[1]]), d, f, 32)
+    assert not np.array_equal(wrong, e)
