@@ -12,8 +12,9 @@
  * Conventions shared by every entry point
  *  - Pointers are CUDA device pointers owned by the caller, unless a comment
  *    says "host".  Arrays are dense, row-major, with no padding; every pointer
- *    must be 16-byte aligned.  The library allocates no memory: scratch comes
- *    from a caller workspace whose size the *_workspace_bytes queries return.
+ *    must be 16-byte aligned.  The library allocates no device memory: scratch
+ *    comes from a caller workspace whose size the *_workspace_bytes queries
+ *    return (an expert tier keeps its own small host-side tables).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Every call only enqueues work on that stream and returns; nothing is
  *    synchronised and nothing is read back to the host.  The calls keep no
@@ -70,7 +71,8 @@ enum {
     MOE_ERR_INVALID_ARG = -1,   /* NULL pointer, misaligned pointer, size out of range */
     MOE_ERR_UNSUPPORTED = -2,   /* a shape or mode this build does not implement */
     MOE_ERR_WORKSPACE = -3,     /* workspace smaller than the matching *_workspace_bytes */
-    MOE_ERR_CUDA = -4           /* a CUDA runtime call or kernel launch failed */
+    MOE_ERR_CUDA = -4,          /* a CUDA runtime call or kernel launch failed */
+    MOE_ERR_STALE = -5          /* a usage file written for another model or shape (not used) */
 };
 
 /* Bits of the device error word `err`. */
@@ -304,6 +306,98 @@ MOE_API int moe_layer_forward_topp(const float *x, const float *w_gate, const fl
                                    void *workspace, size_t ws_bytes, int32_t *err, void *stream);
 
 MOE_API size_t moe_layer_workspace_bytes(int T, int k, int E, int d, int f, int mode);
+
+/* --------------------------------------------- usage file (Learn, kept) ---- */
+/*
+ * The per-expert hit counters of `layers` layers (hits [layers][E], host)
+ * saved to a file and loaded back, and the most used experts of a layer.
+ * Source: "Public Colibri Observation and Revision Ledger", "Exact Architecture
+ * and Data-Flow Reconstruction" (a learning cache of the most used experts,
+ * persisted between runs) and "Failure, Corruption, and Restart Behavior" (the
+ * usage file decides what is pinned on restart and is not checked against the
+ * model).  The file holds a caller-chosen model id (e.g. a hash of the
+ * weights), the shape, the counts and a checksum; it is written to
+ * "<path>.tmp" and renamed over path.
+ *   moe_usage_save: MOE_OK, or MOE_ERR_INVALID_ARG when it cannot be written.
+ *   moe_usage_load: MOE_OK (hits filled); MOE_ERR_STALE when the file is sound
+ *     but for another model id, layer count or E (hits untouched);
+ *     MOE_ERR_INVALID_ARG when missing, of another version, cut short or
+ *     corrupted (hits untouched).
+ *   moe_usage_top: the n most used experts of one layer's hits [E], count
+ *     descending, equal counts by ascending id (experts: host [n]).
+ */
+MOE_API int moe_usage_save(const char *path, const uint64_t *hits, int layers, int E, uint64_t model_id);
+MOE_API int moe_usage_load(const char *path, uint64_t *hits, int layers, int E, uint64_t model_id);
+MOE_API int moe_usage_top(const uint64_t *hits, int E, int n, int32_t *experts);
+
+/* ------------------------------------------------- expert tier (Place) ---- */
+/*
+ * Place and Overlap: a layer whose routed experts live in host memory, with a
+ * cache of n_slots expert blocks in device memory.
+ * Source: "Public Colibri Observation and Revision Ledger", "Exact Architecture
+ * and Data-Flow Reconstruction" (Place loads the experts a batch needs into
+ * fast memory; Overlap computes on the experts already there while the loads
+ * run); colibri README, "How it works" (placement decides speed only: the
+ * router's choices and the weights' precision are the same).
+ *
+ * A tier belongs to one layer and one device (the current device at
+ * creation).  It keeps host-side tables, two events and a small page-locked
+ * staging buffer, all freed by moe_tier_destroy; device memory is the
+ * caller's: slot_q [n_slots][moe_expert_q_bytes(d, f)] and slot_s
+ * [n_slots][moe_expert_s_count(d, f, G)].  host_q/host_s hold all E expert
+ * blocks in the layout of moe_layer_int4 and must be page-locked
+ * (cudaHostAlloc or cudaHostRegister) and stay valid for the tier's life.
+ * A tier is used by one host thread and one stream at a time (calls on it are
+ * serialised by a lock).  Errors: MOE_ERR_INVALID_ARG for bad sizes or
+ * pointers, MOE_ERR_UNSUPPORTED for shapes the FFN does not support,
+ * MOE_ERR_CUDA when a runtime call fails.
+ */
+typedef struct moe_tier_s *moe_tier;
+
+MOE_API int moe_tier_create(int E, int d, int f, int G, const uint8_t *host_q, const float *host_s,
+                            uint8_t *slot_q, float *slot_s, int n_slots, moe_tier *out);
+MOE_API void moe_tier_destroy(moe_tier tier);
+
+/*
+ * Pin experts (host array of n ids) in slots: they are loaded now (copies on
+ * copy_stream, which this call waits for) and never evicted until
+ * moe_tier_unpin_all.  At least one slot always stays unpinned.  This is how
+ * a learned hot set (moe_usage_top) is kept resident.  Call it when no layer
+ * call on this tier is still running on the device (its slots may be
+ * rewritten).
+ */
+MOE_API int moe_tier_pin(moe_tier tier, const int32_t *experts, int n, void *copy_stream);
+MOE_API int moe_tier_unpin_all(moe_tier tier);
+
+/* stats (host [4]): resident hits, misses (experts copied), bytes copied, layer calls. */
+MOE_API int moe_tier_stats(moe_tier tier, uint64_t *stats);
+/* The expert in each slot (-1: empty) and its pin flag (host [n_slots] each; either may be NULL). */
+MOE_API int moe_tier_slots(moe_tier tier, int32_t *expert_in_slot, uint8_t *pinned);
+
+MOE_API size_t moe_tier_workspace_bytes(int T, int k, int E, int d, int f, int mode);
+
+/*
+ * moe_layer_forward_topp over a tier (top_p = 1: plain top-k).  Steps:
+ *   route and union on `stream`; the union's expert list is copied to the
+ *   host and this call WAITS for it (the only call of this library that
+ *   synchronises with the device, so it cannot be captured in a CUDA graph);
+ *   experts already in a slot are hits, each missing one takes the least
+ *   recently used unpinned slot not needed by this batch and is copied there
+ *   (one cudaMemcpyAsync per block, on copy_stream); the FFN runs over the
+ *   hits and the shared expert while the copies proceed, then, after the
+ *   copies (an event), over the copied experts; then the combine.
+ * The output is bit-identical to moe_layer_forward_topp on the same weights
+ * resident in device memory, at any residency.  A batch whose union has more
+ * experts than unpinned slots returns MOE_ERR_INVALID_ARG (nothing is copied).
+ * The shared expert (shared_q, shared_s) is in device memory.  workspace:
+ * moe_tier_workspace_bytes(T, k, E, d, f, mode) bytes, 256-byte aligned.
+ */
+MOE_API int moe_layer_forward_tier(const float *x, const float *w_gate, const float *bias, moe_tier tier,
+                                   const uint8_t *shared_q, const float *shared_s, const float *residual,
+                                   int T, int k, int normalize, float route_scale, float top_p, int mode,
+                                   float *out, int32_t *topk_idx, float *topk_w, uint64_t *hits,
+                                   void *workspace, size_t ws_bytes, int32_t *err, void *stream,
+                                   void *copy_stream);
 
 #ifdef __cplusplus
 }

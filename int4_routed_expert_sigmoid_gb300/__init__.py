@@ -11,5 +11,6 @@ from ._binding import (  # noqa: F401
     MOE_ERR_WORKSPACE, MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL, MOE_OK, LayerWeights, MoeError,
     device_error, expert_q_bytes, expert_s_count, ffn_workspace_bytes, header_functions, layer_workspace_bytes,
     lib, moe_combine, moe_expert_ffn_int4, moe_expert_ffn_int4_noalloc, moe_hits, moe_layer_forward, moe_rms_norm,
-    moe_route, moe_union, status_str, workspace,
+    moe_route, moe_union, status_str, workspace, ExpertTier, tier_workspace_bytes, moe_layer_forward_tier,
+    MOE_ERR_STALE, usage_save, usage_load, usage_top,
 )

@@ -17,7 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libmoe.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
 
-MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = 0, -1, -2, -3, -4
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_STALE = 0, -1, -2, -3, -4, -5
 MOE_DEVERR_BAD_EXPERT, MOE_DEVERR_TIMEOUT, MOE_DEVERR_SCALE_RANGE = 0x1, 0x2, 0x4
 MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL = 0, 1, 2
 
@@ -60,6 +60,18 @@ _SIGNATURES = {
     "moe_layer_forward_topp": ([_P, _P, _P, ctypes.POINTER(moe_layer_int4), _P, _I, _I, _I, _F, _F, _I, _P,
                                 _P, _P, _P, _P, _SZ, _P, _P], _I),
     "moe_layer_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
+    "moe_usage_save": ([ctypes.c_char_p, _P, _I, _I, ctypes.c_uint64], _I),
+    "moe_usage_load": ([ctypes.c_char_p, _P, _I, _I, ctypes.c_uint64], _I),
+    "moe_usage_top": ([_P, _I, _I, _P], _I),
+    "moe_tier_create": ([_I, _I, _I, _I, _P, _P, _P, _P, _I, ctypes.POINTER(ctypes.c_void_p)], _I),
+    "moe_tier_destroy": ([_P], None),
+    "moe_tier_pin": ([_P, _P, _I, _P], _I),
+    "moe_tier_unpin_all": ([_P], _I),
+    "moe_tier_stats": ([_P, _P], _I),
+    "moe_tier_slots": ([_P, _P, _P], _I),
+    "moe_tier_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
+    "moe_layer_forward_tier": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _F, _I, _P, _P, _P, _P, _P, _SZ, _P,
+                                _P, _P], _I),
 }
 
 
@@ -305,3 +317,122 @@ def header_functions() -> list[str]:
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"^\s*MOE_API\s+(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+class ExpertTier:
+    """A layer's routed experts in page-locked host memory with n_slots of them cached in device
+    memory (moe_tier_*).  host_q/host_s: pinned CPU tensors [E * q_bytes] uint8 / [E * s_count]
+    float32; the slot arrays are allocated here as torch device tensors (the library allocates no
+    device memory)."""
+
+    def __init__(self, host_q: torch.Tensor, host_s: torch.Tensor, E: int, d: int, f: int, n_slots: int,
+                 G: int = 32, device=None):
+        if host_q.is_cuda or host_s.is_cuda or not (host_q.is_pinned() and host_s.is_pinned()):
+            raise ValueError("host_q and host_s must be page-locked CPU tensors")
+        if host_q.dtype != torch.uint8 or host_s.dtype != torch.float32:
+            raise ValueError("host_q must be uint8 and host_s float32")
+        device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        qb, sc = expert_q_bytes(d, f), expert_s_count(d, f, G)
+        self.host_q, self.host_s = host_q, host_s
+        self.slot_q = torch.empty(n_slots * qb, dtype=torch.uint8, device=device)
+        self.slot_s = torch.empty(n_slots * sc, dtype=torch.float32, device=device)
+        self.E, self.d, self.f, self.G, self.n_slots = E, d, f, G, n_slots
+        h = ctypes.c_void_p()
+        _check(lib().moe_tier_create(E, d, f, G, ctypes.c_void_p(host_q.data_ptr()),
+                                     ctypes.c_void_p(host_s.data_ptr()), _p(self.slot_q), _p(self.slot_s), n_slots,
+                                     ctypes.byref(h)), "moe_tier_create")
+        self.h = h
+
+    def close(self):
+        if getattr(self, "h", None) is not None and self.h.value:
+            lib().moe_tier_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def pin(self, experts, copy_stream=None):
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(experts, dtype=np.int32))
+        _check(lib().moe_tier_pin(self.h, ids.ctypes.data_as(ctypes.c_void_p), ids.size, _stream(copy_stream)),
+               "moe_tier_pin")
+
+    def unpin_all(self):
+        _check(lib().moe_tier_unpin_all(self.h), "moe_tier_unpin_all")
+
+    def stats(self) -> dict:
+        import numpy as np
+        st = np.zeros(4, np.uint64)
+        _check(lib().moe_tier_stats(self.h, st.ctypes.data_as(ctypes.c_void_p)), "moe_tier_stats")
+        return {"hits": int(st[0]), "misses": int(st[1]), "bytes_copied": int(st[2]), "calls": int(st[3])}
+
+    def slots(self):
+        import numpy as np
+        ex = np.zeros(self.n_slots, np.int32)
+        pn = np.zeros(self.n_slots, np.uint8)
+        _check(lib().moe_tier_slots(self.h, ex.ctypes.data_as(ctypes.c_void_p), pn.ctypes.data_as(ctypes.c_void_p)),
+               "moe_tier_slots")
+        return ex, pn.astype(bool)
+
+
+def tier_workspace_bytes(T: int, k: int, E: int, d: int, f: int, mode: int = MOE_MODE_AUTO) -> int:
+    return int(lib().moe_tier_workspace_bytes(T, k, E, d, f, mode))
+
+
+def moe_layer_forward_tier(x, w_gate, bias, tier: ExpertTier, shared_q, shared_s, k: int, normalize: int = 1,
+                           route_scale: float = 1.0, top_p: float = 1.0, mode: int = MOE_MODE_AUTO, residual=None,
+                           out=None, topk_idx=None, topk_w=None, hits=None, ws=None, err=None, stream=None,
+                           copy_stream=None):
+    """moe_layer_forward over an expert tier: waits on the host for the routing, copies the missing
+    experts on copy_stream (a separate torch.cuda.Stream) while the resident ones are computed."""
+    _need(x, torch.float32, "x")
+    _need(shared_q, torch.uint8, "shared_q")
+    _need(shared_s, torch.float32, "shared_s")
+    if copy_stream is None:
+        raise ValueError("copy_stream: a CUDA stream other than the compute stream")
+    T, d = x.shape
+    dev = x.device
+    out = torch.empty((T, d), dtype=torch.float32, device=dev) if out is None else out
+    if ws is None:
+        ws = workspace(tier_workspace_bytes(T, k, tier.E, d, tier.f, mode), dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    wp, wn = _ws_ptr(ws)
+    _check(lib().moe_layer_forward_tier(_p(x), _p(w_gate), _p(bias), tier.h, _p(shared_q), _p(shared_s),
+                                        _p(residual), T, k, int(normalize), float(route_scale), float(top_p), mode,
+                                        _p(out), _p(topk_idx), _p(topk_w), _p(hits), wp, wn, _p(err),
+                                        _stream(stream), _stream(copy_stream)), "moe_layer_forward_tier")
+    return out, err
+
+
+def usage_save(path: str, hits, model_id: int) -> None:
+    """Save hit counters [layers][E] (numpy uint64 or int64, host) for model_id."""
+    import numpy as np
+    h = np.ascontiguousarray(np.asarray(hits).astype(np.uint64))
+    if h.ndim != 2:
+        raise ValueError("hits must be [layers][E]")
+    _check(lib().moe_usage_save(os.fsencode(path), h.ctypes.data_as(ctypes.c_void_p), h.shape[0], h.shape[1],
+                                int(model_id) & (2 ** 64 - 1)), "moe_usage_save")
+
+
+def usage_load(path: str, layers: int, E: int, model_id: int):
+    """Hit counters [layers][E] from a usage file written for model_id; raises MoeError (status
+    MOE_ERR_STALE for another model or shape, MOE_ERR_INVALID_ARG for a missing or damaged file)."""
+    import numpy as np
+    h = np.zeros((layers, E), np.uint64)
+    _check(lib().moe_usage_load(os.fsencode(path), h.ctypes.data_as(ctypes.c_void_p), layers, E,
+                                int(model_id) & (2 ** 64 - 1)), "moe_usage_load")
+    return h
+
+
+def usage_top(hits_layer, n: int):
+    """The n most used experts of one layer (count descending, ties by ascending id)."""
+    import numpy as np
+    h = np.ascontiguousarray(np.asarray(hits_layer).astype(np.uint64)).reshape(-1)
+    out = np.zeros(n, np.int32)
+    _check(lib().moe_usage_top(h.ctypes.data_as(ctypes.c_void_p), h.size, n, out.ctypes.data_as(ctypes.c_void_p)),
+           "moe_usage_top")
+    return out

@@ -107,6 +107,8 @@ struct Params {
     int gpc_h;                  // groups per block of the h fragments
     float *y_pair, *y_shared;
     int32_t *work;              // items claimed beyond the first one per CTA; zero on entry
+    const int32_t *slot_of;     // when set: routed expert e's weights are block slot_of[e] of the layer view
+    int with_shared;            // 1: unit 0 is the shared expert; 0: the units are the uniq list only
     int32_t *err;
     int T, k, nchunks, tiles, out_rows;   // nchunks: k-chunks of the reduction; out_rows: d (down)
     int dynamic;                // 1: items after the first from the counter; 0: CTA c takes c, c + G, ...
@@ -140,6 +142,7 @@ __device__ __forceinline__ int swz(int r)
 
 struct Item {
     int expert;   // routed expert id, or -1 for the shared expert
+    int zq;       // block of the layer view holding its weights (routed)
     int tile;     // row tile
     int m;        // tokens of this expert
     int pos0;     // first pair position (routed) of the expert's group
@@ -149,7 +152,7 @@ struct Item {
 // union's expert uniq[u - 1]; built once per CTA in shared memory so that
 // walking the items needs no dependent global loads.
 struct Unit {
-    int expert, pos0, m;
+    int expert, pos0, m, zq;
 };
 
 // (L2 loads: the down kernel reads the table before its grid wait, when the
@@ -158,15 +161,17 @@ __device__ __forceinline__ void load_units(const Params &p, int units, Unit *tab
 {
     for (int u = threadIdx.x; u < units; u += blockDim.x) {
         Unit t;
-        if (u == 0) {
+        if (u < p.with_shared) {
             t.expert = -1;
             t.pos0 = 0;
             t.m = p.T;
+            t.zq = 0;
         } else {
-            const int e = __ldcg(p.uniq + u - 1);
+            const int e = __ldcg(p.uniq + u - p.with_shared);
             t.expert = e;
             t.pos0 = __ldcg(p.offsets + e);
             t.m = __ldcg(p.offsets + e + 1) - t.pos0;
+            t.zq = p.slot_of ? __ldcg(p.slot_of + e) : e;
         }
         tab[u] = t;
     }
@@ -179,6 +184,7 @@ __device__ __forceinline__ Item decode_item(const Params &p, const Unit *tab, in
     it.tile = i - u * p.tiles;
     const Unit t = tab[u];
     it.expert = t.expert;
+    it.zq = t.zq;
     it.pos0 = t.pos0;
     it.m = t.m;
     return it;
@@ -406,7 +412,7 @@ template <int MODE, int TOK, int CPS, int GPC, int GS>
 __device__ __forceinline__ void issue_weights(const Maps &maps, const Item &it, int c, uint32_t sb, uint32_t fb)
 {
     using C = Cfg<MODE, TOK, CPS, GPC, GS>;
-    const int z = it.expert < 0 ? 0 : it.expert;
+    const int z = it.expert < 0 ? 0 : it.zq;
     const int w = it.expert < 0 ? 1 : 0;
     const int row0 = it.tile * C::kRows;
     const void *mq = &maps.q[w], *ms = &maps.s[w];
@@ -472,19 +478,21 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
     // (items 0 .. tiles - 1, whatever the union).  Weights do not depend on the previous kernel.
     int units = 0;
     if (MODE == kDown) {
-        units = __ldcg(p.n_uniq) + 1;
+        units = __ldcg(p.n_uniq) + p.with_shared;
         load_units(p, units, tab);
         __syncthreads();
     }
     int pre = 0;   // producer: stages of the first item's first pass already holding their weights
     if (warp == kProducerWarp) {
-        const bool known = MODE == kDown ? (int)blockIdx.x < units * p.tiles : (int)blockIdx.x < p.tiles;
+        const bool known = MODE == kDown ? (int)blockIdx.x < units * p.tiles
+                                         : (p.with_shared && (int)blockIdx.x < p.tiles);
         if (known) {
             Item it0;
             if (MODE == kDown) {
                 it0 = decode_item(p, tab, blockIdx.x);
             } else {
                 it0.expert = -1;
+                it0.zq = 0;
                 it0.tile = blockIdx.x;
                 it0.m = p.T;
                 it0.pos0 = 0;
@@ -505,7 +513,7 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
         // the down kernel reads the union before its own grid wait: release it only after ours
         griddep_wait();   // routing, union and activation fragments come from the previous kernels
         griddep_launch_dependents();
-        units = *p.n_uniq + 1;
+        units = *p.n_uniq + p.with_shared;
         load_units(p, units, tab);
         __syncthreads();
     } else {
@@ -810,6 +818,8 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
     pg.h_row_bytes = frag_row_bytes(f, gpc_h);
     pg.gpc_h = gpc_h;
     pg.work = a.work;
+    pg.slot_of = a.slot_of;
+    pg.with_shared = a.with_shared;
     // T = 1: every unit has one token and the items are equal, so the fixed order c, c + G, ...
     // balances them as well as claiming would (and saves the atomics, measured 2 us faster per
     // layer); larger batches give units of very different lengths: claim dynamically

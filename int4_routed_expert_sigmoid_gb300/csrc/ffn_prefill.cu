@@ -107,10 +107,11 @@ struct PCfg {
     static_assert(kRawStage % 1024 == 0 && kOpStage % 1024 == 0, "alignment");
 };
 
-// Unit table in shared memory: unit 0 = shared expert (T tokens), unit u >= 1
-// = uniq[u - 1]; cum = prefix of token tiles over the units.
+// Unit table in shared memory: unit 0 = shared expert (T tokens) when the
+// launch includes it, then the uniq list; cum = prefix of token tiles over the
+// units; zq = block of the layer view holding a routed expert's weights.
 struct PUnit {
-    int expert, row0, m, cum;
+    int expert, row0, m, cum, zq;
 };
 
 __host__ __device__ constexpr size_t prefill_smem(int ring, int max_units)
@@ -135,6 +136,8 @@ struct PParams {
     float *h32;                   // gate/up: h [rows][f] fp32, natural order
     float *y_pair, *y_shared;     // down outputs
     uint16_t *y_pair16;           // down: routed outputs as bf16 instead of y_pair, when set
+    const int32_t *slot_of;       // when set: routed expert e's weights are block slot_of[e] of the layer view
+    int with_shared;              // 1: unit 0 is the shared expert; 0: the units are the uniq list only
     int32_t *err;
     int T, k, K, mtiles, out_rows;
 };
@@ -143,6 +146,7 @@ __device__ __forceinline__ int frag_pos8(int o) { return 2 * (o & 3) + (o >> 2);
 
 struct PItem {
     int expert;   // -1 = shared
+    int zq;       // block of the layer view holding its weights (routed)
     int mtile;
     int tok0;     // first token of the tile within the unit
     int ntok;     // tokens in this tile (1..N)
@@ -165,15 +169,17 @@ __device__ void build_units(const PParams &p, int units, PUnit *tab)
         tiles[j] = 0;
         if (u < units) {
             PUnit t;
-            if (u == 0) {
+            if (u < p.with_shared) {
                 t.expert = -1;
                 t.row0 = p.T * p.k;
                 t.m = p.T;
+                t.zq = 0;
             } else {
-                const int e = p.uniq[u - 1];
+                const int e = p.uniq[u - p.with_shared];
                 t.expert = e;
                 t.row0 = p.offsets[e];
                 t.m = p.offsets[e + 1] - t.row0;
+                t.zq = p.slot_of ? p.slot_of[e] : e;
             }
             tiles[j] = (t.m + N - 1) / N;
             tab[u] = t;
@@ -225,6 +231,7 @@ __device__ __forceinline__ PItem decode_pitem(const PParams &p, const PUnit *tab
     }
     const PUnit t = tab[lo];
     it.expert = t.expert;
+    it.zq = t.zq;
     it.row0 = t.row0;
     it.m = t.m;
     // the unit's tokens in ceil(m / N) balanced tiles (each <= N)
@@ -334,7 +341,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
     griddep_launch_dependents();
     griddep_wait();   // union and sorted activation rows come from earlier kernels
 
-    const int units = *p.n_uniq + 1;
+    const int units = *p.n_uniq + p.with_shared;
     build_units<N>(p, units, tab);
     const int n_items = tab[units].cum * p.mtiles;
     const int nraw = p.K / RAWK;
@@ -346,7 +353,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
             uint32_t rph = 0;
             for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
                 const PItem it = decode_pitem<N>(p, tab, units, i);
-                const int z = it.expert < 0 ? 0 : it.expert;
+                const int z = it.expert < 0 ? 0 : it.zq;
                 const int w = it.expert < 0 ? 1 : 0;
                 const int wrow0 = it.mtile * C::kRowsPerMat;
                 for (int r = 0; r < nraw; r++) {
@@ -563,7 +570,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
             // this lane's weight row and the power of two its dequantised weights were scaled by
             const int wrow = MODE == kPGateUp ? it.mtile * 64 + sub * 16 + (lane & 15) : it.mtile * kTileM + sub * 32 + lane;
             const int wmat = MODE == kPGateUp ? (lane >> 4) : 0;
-            const float *sbase = it.expert < 0 ? p.s_shared : p.s_routed + (size_t)it.expert * p.s_expert;
+            const float *sbase = it.expert < 0 ? p.s_shared : p.s_routed + (size_t)it.zq * p.s_expert;
             const float ef = pow2i(-row_shift(__ldg(sbase + p.s_off0 + (size_t)wmat * p.s_mat +
                                                     (size_t)wrow * p.s_row)));
             if (!abort_flag && !mbar_wait(smem_addr(&acc_full[b]), fph[b])) {
@@ -834,10 +841,11 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     int rc = MOE_OK;
 
     // fp16 token rows: each token converted once and written to its pair rows and shared row
-    rc = launch_pdl(pair_pos_kernel, (T * k + 255) / 256, 256, 0, s, a.sorted_pair, a.offsets, E, ps.pos);
+    const int E_off = a.n_experts > 0 ? a.n_experts : E;   // offsets[E_off] = the placed pairs
+    rc = launch_pdl(pair_pos_kernel, (T * k + 255) / 256, 256, 0, s, a.sorted_pair, a.offsets, E_off, ps.pos);
     if (rc == MOE_OK)
-        rc = launch_pdl(token_rows_kernel, T, 256, 0, s, a.x, (const int32_t *)ps.pos, a.sorted_pair, a.offsets, E,
-                        T, k, d, x_sorted, row_scale);
+        rc = launch_pdl(token_rows_kernel, T, 256, 0, s, a.x, (const int32_t *)ps.pos, a.sorted_pair, a.offsets,
+                        E_off, T, k, d, x_sorted, row_scale);
     if (rc != MOE_OK)
         return rc;
 
@@ -874,6 +882,8 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pg.s_row = d / G;
     pg.row_scale = row_scale;
     pg.h32 = ps.h32;
+    pg.slot_of = a.slot_of;
+    pg.with_shared = a.with_shared;
     pg.err = a.err;
     pg.T = T;
     pg.k = k;

@@ -39,6 +39,10 @@ int check_layer(const moe_layer_int4 *w)
     return MOE_OK;
 }
 
+}  // namespace
+
+namespace moe {
+
 int resolve_mode(int mode, int T)
 {
     if (mode == MOE_MODE_AUTO)
@@ -47,17 +51,6 @@ int resolve_mode(int mode, int T)
 }
 
 bool valid_mode(int mode) { return mode == MOE_MODE_AUTO || mode == MOE_MODE_DECODE || mode == MOE_MODE_PREFILL; }
-
-// FFN scratch of either path (the union never has more than T*k experts).
-size_t ffn_scratch_bytes_mode(int T, int k, int d, int f, int mode);
-
-// Scratch of the decode FFN: activation fragments of x (with a factor per
-// row) and of h (factors inside the fragment blocks).
-struct FfnScratch {
-    uint8_t *x_frag, *h_frag;
-    float *x_scale;
-    int32_t *work;   // the decode FFN's item counters
-};
 
 size_t ffn_scratch_layout(int T, int k, int d, int f, uint8_t *base, FfnScratch *out)
 {
@@ -77,15 +70,6 @@ size_t ffn_scratch_layout(int T, int k, int d, int f, uint8_t *base, FfnScratch 
         *out = s;
     return off;
 }
-
-struct LayerScratch {
-    float *logits;
-    int32_t *idx;
-    float *w;
-    int32_t *counts, *offsets, *perm, *sorted_pair, *uniq, *n_uniq;
-    float *y_pair, *y_shared;
-    uint8_t *ffn;
-};
 
 size_t layer_scratch_layout(int T, int k, int E, int d, int f, int mode, uint8_t *base, LayerScratch *o)
 {
@@ -121,7 +105,7 @@ size_t ffn_scratch_bytes_mode(int T, int k, int d, int f, int mode)
     return ffn_scratch_layout(T, k, d, f, nullptr, nullptr);
 }
 
-}  // namespace
+}  // namespace moe
 
 extern "C" {
 
@@ -133,6 +117,7 @@ const char *moe_status_str(int status)
     case MOE_ERR_UNSUPPORTED: return "unsupported shape or mode";
     case MOE_ERR_WORKSPACE: return "workspace too small";
     case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_STALE: return "usage file of another model or shape";
     default: return "unknown status";
     }
 }

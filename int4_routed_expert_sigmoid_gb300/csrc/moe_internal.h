@@ -109,6 +109,8 @@ struct DecodeFfnArgs {
     uint8_t *h_frag;          // [T*k + T] rows of frag_row_bytes(f, frag_gpc_h(f)) (scratch)
     float *y_pair, *y_shared;
     int32_t *work;            // kDecodeCounters item counters, zeroed by the kernel before (scratch)
+    const int32_t *slot_of = nullptr;   // [E] block of w holding expert e (expert tier), or null: block e
+    int with_shared = 1;                // 0: only the uniq list's experts (a second launch of the tier)
     int32_t *err;
 };
 constexpr int kDecodeCounters = 2;   // items claimed by the gate/up and the down kernel
@@ -123,6 +125,9 @@ struct PrefillFfnArgs {
     void *scratch;                       // prefill_scratch_bytes(T, k, d, f) bytes, 256-aligned
     float *y_pair, *y_shared;
     uint16_t *y_pair16;                  // when set: routed outputs as bf16 here instead of y_pair (fp32)
+    const int32_t *slot_of = nullptr;    // as in DecodeFfnArgs
+    int n_experts = 0;                   // experts the union's offsets cover (0: w->E)
+    int with_shared = 1;
     int32_t *err;
 };
 size_t prefill_scratch_bytes(int T, int k, int d, int f);
@@ -153,5 +158,29 @@ int make_tmap_nd(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, in
 
 // device properties cached per device
 int sm_count(int device);
+
+// moe_api.cu: the FFN path a mode resolves to at T tokens, and the workspace layouts of the FFN
+// and of the whole layer (base may be null to size them).
+int resolve_mode(int mode, int T);
+size_t ffn_scratch_bytes_mode(int T, int k, int d, int f, int mode);
+
+// Scratch of the decode FFN: activation fragments of x (with a factor per row) and of h (factors
+// inside the fragment blocks), and the item counters.
+struct FfnScratch {
+    uint8_t *x_frag, *h_frag;
+    float *x_scale;
+    int32_t *work;
+};
+size_t ffn_scratch_layout(int T, int k, int d, int f, uint8_t *base, FfnScratch *out);
+
+struct LayerScratch {
+    float *logits;
+    int32_t *idx;
+    float *w;
+    int32_t *counts, *offsets, *perm, *sorted_pair, *uniq, *n_uniq;
+    float *y_pair, *y_shared;
+    uint8_t *ffn;
+};
+size_t layer_scratch_layout(int T, int k, int E, int d, int f, int mode, uint8_t *base, LayerScratch *o);
 
 }  // namespace moe
