@@ -47,10 +47,11 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "batched_decode", "prefill", "stack", "tiny"],
+                    choices=["decode", "batched_decode", "prefill", "stack", "tier", "tiny"],
                     help="tiny is the parity-size layer (fits in L2; for quick checks, not a bench line); "
                          "stack is 8 resident layers, the line's T from --tokens (default 64) plus a sweep "
-                         "over T in {1, 4, 16, 64, 256}")
+                         "over T in {1, 4, 16, 64, 256}; tier is the decode layer with its experts in host "
+                         "memory and a sweep over the fraction cached in HBM")
     ap.add_argument("--replicas", type=int, default=4, help="device copies of the layer rotated across steps")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the routed expert count (small-footprint profiling runs); 0 = workload's")
@@ -423,6 +424,77 @@ def measure_layer(copies, sh, prefill, steps, warmup, graph_steps, e2e_steps, ra
     }
 
 
+def measure_tier(args, rank, world, dev, fractions=(1.0, 0.5, 0.25, 0.125), steps=200, warmup=200):
+    """The decode T = 1 layer with its routed experts in page-locked host memory (Grace memory behind
+    NVLink-C2C) and an HBM cache of a fraction of them (moe_layer_forward_tier: Place and Overlap).
+    Per fraction: tokens/s, the share of union experts found resident, and the host -> device
+    bytes copied per second.  Each call waits on the host for its routing, so the loop is host
+    driven (no CUDA graph); the timed region is bracketed by synchronisations."""
+    import torch
+
+    import int4_routed_expert_sigmoid_gb300 as moe
+    import workloads
+    sh = workloads.WORKLOADS["decode"]
+    E, k, d, f, G, T = sh.E, sh.k, sh.d, sh.f, sh.G, sh.T
+    qb, sc = workloads.expert_q_bytes(d, f), workloads.expert_s_count(d, f, G)
+    hq = torch.empty(E * qb, dtype=torch.uint8).pin_memory()
+    hs = torch.empty(E * sc, dtype=torch.float32).pin_memory()
+    L = workloads.layer_inputs(sh, seed=0, threads=os.cpu_count() or 8, q_base=hq.numpy(), s_base=hs.numpy())
+    wg = torch.from_numpy(L.wg).to(dev)
+    bias = torch.from_numpy(L.bias).to(dev)
+    shq = torch.from_numpy(L.shared_q).to(dev)
+    shs = torch.from_numpy(L.shared_s).to(dev)
+    del L
+    n_x = steps + warmup   # every call a new token: a repeated token would find its experts resident
+    xs = torch.from_numpy(workloads.activations(n_x * T, d, seed=3000 + rank)).to(dev).view(n_x, T, d)
+    out = torch.empty((T, d), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = moe.workspace(moe.tier_workspace_bytes(T, k, E, d, f, moe.MOE_MODE_DECODE), dev)
+    copy = torch.cuda.Stream(device=dev)
+    blk = qb + 4 * sc
+    rows = []
+    for frac in fractions:
+        n_slots = max(k, int(round(frac * E)))
+        tier = moe.ExpertTier(hq, hs, E=E, d=d, f=f, n_slots=n_slots, G=G, device=dev)
+        if n_slots == E:
+            tier.prefetch(np.arange(E), copy_stream=copy)   # every expert in HBM: the device-only path
+
+        def call(i):
+            moe.moe_layer_forward_tier(xs[i % n_x], wg, bias, tier, shq, shs, k, mode=moe.MOE_MODE_DECODE,
+                                       out=out, ws=ws, err=err, copy_stream=copy)
+
+        for i in range(warmup):
+            call(i)
+        torch.cuda.synchronize()
+        err.zero_()
+        st0 = tier.stats()
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(steps):
+            call(warmup + i)
+        torch.cuda.synchronize()
+        el = time.perf_counter() - t0
+        el = reduce_max(world, [el], dev)[0]
+        st1 = tier.stats()
+        hits, miss = st1["hits"] - st0["hits"], st1["misses"] - st0["misses"]
+        copied = st1["bytes_copied"] - st0["bytes_copied"]
+        rows.append({"fraction_resident": frac, "n_slots": n_slots, "steps": steps,
+                     "tokens_per_s": round(T * steps * world / el, 2), "ms_per_step": round(el / steps * 1e3, 4),
+                     # every expert in HBM: the calls take the device-only path and count no hits
+                     "hit_rate": round(hits / (hits + miss), 4) if hits + miss else None,
+                     "path": "device-only (all experts resident)" if n_slots == E else "host-planned",
+                     "c2c_gbs": round(copied / el / 1e9, 2), "copied_bytes_per_step": int(copied / steps),
+                     "expert_block_bytes": blk, "device_error": int(err.item())})
+        tier.close()
+        del tier
+        torch.cuda.synchronize()
+    return {"config": {"workload": f"decode T={T} with routed experts in page-locked host memory (Grace, "
+                                   f"NVLink-C2C) and an HBM cache of a fraction of them; E={E} + 1 shared, k={k}, "
+                                   f"d={d}, f={f}, int4 group-{G}, N(0, 0.1) selection bias, LRU slots, no pins",
+                       "T": T, "E": E, "k": k, "d": d, "f": f, "G": G},
+            "fractions": rows}
+
+
 def workload_shape(args, name):
     import dataclasses
 
@@ -474,6 +546,7 @@ def run_ours(args, rank, world, local):
         extras["stack"] = measure_stack(args, rank, world, dev, T_line=64, steps=48, warmup=max(3, args.warmup),
                                         sweep_seconds=1.0)
         line["gpu_launches"] += extras["stack"]["gpu_launches"]
+        extras["tier"] = measure_tier(args, rank, world, dev)
         line["workloads"] = extras
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sh, args.cpu_seconds)
@@ -897,6 +970,15 @@ def main(argv=None):
         return
     if args.workload == "stack":
         run_stack(args, rank, world, local)
+        return
+    if args.workload == "tier":
+        dev = init_device(local, world)
+        res = measure_tier(args, rank, world, dev, steps=args.steps, warmup=args.warmup)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "unit": UNIT, "n_gpus": world, **res}), flush=True)
         return
     run_ours(args, rank, world, local)
 

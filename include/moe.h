@@ -367,6 +367,11 @@ MOE_API void moe_tier_destroy(moe_tier tier);
  * rewritten).
  */
 MOE_API int moe_tier_pin(moe_tier tier, const int32_t *experts, int n, void *copy_stream);
+/* Load experts (host array of n ids) into slots without pinning them (a warm start, e.g. from
+ * moe_usage_top): empty slots first, then the least recently used unpinned ones; once every
+ * unpinned slot holds an expert of the list, the rest of the list is left out.  The copies go on
+ * copy_stream, which this call waits for; the same rule as moe_tier_pin applies. */
+MOE_API int moe_tier_prefetch(moe_tier tier, const int32_t *experts, int n, void *copy_stream);
 MOE_API int moe_tier_unpin_all(moe_tier tier);
 
 /* stats (host [4]): resident hits, misses (experts copied), bytes copied, layer calls. */
@@ -386,6 +391,9 @@ MOE_API size_t moe_tier_workspace_bytes(int T, int k, int E, int d, int f, int m
  *   (one cudaMemcpyAsync per block, on copy_stream); the FFN runs over the
  *   hits and the shared expert while the copies proceed, then, after the
  *   copies (an event), over the copied experts; then the combine.
+ * Once every expert has a slot (n_slots = E, each used once) no call can
+ * miss: calls then skip the host round trip and run one FFN over the union
+ * (they count as calls in the stats, not as hits).
  * The output is bit-identical to moe_layer_forward_topp on the same weights
  * resident in device memory, at any residency.  A batch whose union has more
  * experts than unpinned slots returns MOE_ERR_INVALID_ARG (nothing is copied).

@@ -66,6 +66,7 @@ _SIGNATURES = {
     "moe_tier_create": ([_I, _I, _I, _I, _P, _P, _P, _P, _I, ctypes.POINTER(ctypes.c_void_p)], _I),
     "moe_tier_destroy": ([_P], None),
     "moe_tier_pin": ([_P, _P, _I, _P], _I),
+    "moe_tier_prefetch": ([_P, _P, _I, _P], _I),
     "moe_tier_unpin_all": ([_P], _I),
     "moe_tier_stats": ([_P, _P], _I),
     "moe_tier_slots": ([_P, _P, _P], _I),
@@ -359,6 +360,12 @@ class ExpertTier:
         ids = np.ascontiguousarray(np.asarray(experts, dtype=np.int32))
         _check(lib().moe_tier_pin(self.h, ids.ctypes.data_as(ctypes.c_void_p), ids.size, _stream(copy_stream)),
                "moe_tier_pin")
+
+    def prefetch(self, experts, copy_stream=None):
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(experts, dtype=np.int32))
+        _check(lib().moe_tier_prefetch(self.h, ids.ctypes.data_as(ctypes.c_void_p), ids.size, _stream(copy_stream)),
+               "moe_tier_prefetch")
 
     def unpin_all(self):
         _check(lib().moe_tier_unpin_all(self.h), "moe_tier_unpin_all")

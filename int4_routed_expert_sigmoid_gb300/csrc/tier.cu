@@ -23,6 +23,13 @@
 // The FFN kernels read routed expert e from slot slot_of[e] of the slot array;
 // each output row is computed exactly as in the all-resident layer, so the
 // results are the same bits whatever is resident.
+//
+// One stream of copies is used: on the GB300 machines measured, host-to-device
+// copies from page-locked Grace memory reached about 190 GB/s on one stream
+// and no more on 2 to 8 streams (a kernel reading host memory directly: 210
+// GB/s).  Once every expert has a slot (n_slots = E, after each has been used
+// once) nothing can miss: a call then skips the host round trip and runs the
+// FFN once over the union with the full slot map, like a resident layer.
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -49,6 +56,9 @@ struct moe_tier_s {
     int32_t *stage_out = nullptr;       // page-locked: the upload image (host -> device)
     cudaEvent_t ev_route = nullptr, ev_copy = nullptr;
     int device = -1;
+    int n_loaded = 0;                   // experts with a slot
+    int32_t *stage_map = nullptr;       // page-locked: the full slot map, once every expert has a slot
+    bool map_uploaded = false;          // stage_map is filled (every expert has a slot, none can miss)
     std::mutex mu;
 };
 
@@ -103,6 +113,8 @@ int tier_plan(moe_tier_s &t, const int32_t *uniq, int n, std::vector<int32_t> &r
         }
         if (t.expert_in[v] >= 0)
             t.slot_of[t.expert_in[v]] = -1;
+        else
+            t.n_loaded++;
         t.expert_in[v] = e;
         t.slot_of[e] = v;
         t.last_use[v] = now;
@@ -111,15 +123,18 @@ int tier_plan(moe_tier_s &t, const int32_t *uniq, int n, std::vector<int32_t> &r
     return MOE_OK;
 }
 
-// Copy expert e's block from host memory to slot v on stream s.
-int tier_copy(const moe_tier_s &t, int e, int v, cudaStream_t s)
+// Copy the blocks of experts src[i] (host) to slots dst[i] on stream s: one copy per block of
+// packed bytes and one per block of scales.
+int tier_copy(moe_tier_s &t, const std::vector<int32_t> &src, const std::vector<int32_t> &dst, cudaStream_t s)
 {
-    if (cudaMemcpyAsync(t.slot_q + (size_t)v * t.qb, t.host_q + (size_t)e * t.qb, t.qb, cudaMemcpyHostToDevice, s) !=
-        cudaSuccess)
-        return MOE_ERR_CUDA;
-    if (cudaMemcpyAsync(t.slot_s + (size_t)v * t.sc, t.host_s + (size_t)e * t.sc, t.sc * sizeof(float),
-                        cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    for (size_t i = 0; i < src.size(); i++) {
+        const int e = src[i], v = dst[i];
+        if (cudaMemcpyAsync(t.slot_q + (size_t)v * t.qb, t.host_q + (size_t)e * t.qb, t.qb, cudaMemcpyHostToDevice,
+                            s) != cudaSuccess ||
+            cudaMemcpyAsync(t.slot_s + (size_t)v * t.sc, t.host_s + (size_t)e * t.sc, t.sc * sizeof(float),
+                            cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     return MOE_OK;
 }
 
@@ -131,6 +146,8 @@ void tier_free(moe_tier_s *t)
         cudaFreeHost(t->stage_in);
     if (t->stage_out)
         cudaFreeHost(t->stage_out);
+    if (t->stage_map)
+        cudaFreeHost(t->stage_map);
     if (t->ev_route)
         cudaEventDestroy(t->ev_route);
     if (t->ev_copy)
@@ -176,6 +193,8 @@ int moe_tier_create(int E, int d, int f, int G, const uint8_t *host_q, const flo
             cudaSuccess ||
         cudaHostAlloc(reinterpret_cast<void **>(&t->stage_out), tier_image_ints(E) * sizeof(int32_t),
                       cudaHostAllocDefault) != cudaSuccess ||
+        cudaHostAlloc(reinterpret_cast<void **>(&t->stage_map), E * sizeof(int32_t), cudaHostAllocDefault) !=
+            cudaSuccess ||
         cudaEventCreateWithFlags(&t->ev_route, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&t->ev_copy, cudaEventDisableTiming) != cudaSuccess) {
         tier_free(t);
@@ -187,46 +206,89 @@ int moe_tier_create(int E, int d, int f, int G, const uint8_t *host_q, const flo
 
 void moe_tier_destroy(moe_tier t) { tier_free(t); }
 
+}  // extern "C"
+
+namespace {
+
+// Load experts into slots (least recently used unpinned slots first), optionally pinning them;
+// the copies go on copy_stream, which is waited for.
+int tier_load(moe_tier_s &t, const int32_t *experts, int n, bool pin, cudaStream_t cs)
+{
+    int npin = 0;
+    for (int sl = 0; sl < t.n_slots; sl++)
+        npin += t.pinned[sl];
+    std::vector<int32_t> src, dst;
+    std::vector<uint8_t> taken(t.n_slots, 0);   // slots filled by this call: not evicted by it
+    for (int i = 0; i < n; i++) {
+        const int e = experts[i];
+        if (e < 0 || e >= t.E)
+            return MOE_ERR_INVALID_ARG;
+        int sl = t.slot_of[e];
+        if (sl >= 0 && (t.pinned[sl] || !pin))
+            continue;
+        if (pin && npin + 1 >= t.n_slots)
+            return MOE_ERR_INVALID_ARG;   // at least one slot stays free for the experts of a call
+        if (sl < 0) {
+            // an empty slot if there is one, else the least recently used one (neither pinned nor
+            // filled by this call)
+            for (int c = 0; c < t.n_slots && sl < 0; c++)
+                if (t.expert_in[c] < 0 && !t.pinned[c] && !taken[c])
+                    sl = c;
+            if (sl < 0)
+                for (int c = 0; c < t.n_slots; c++) {
+                    if (t.pinned[c] || taken[c])
+                        continue;
+                    if (sl < 0 || t.last_use[c] < t.last_use[sl])
+                        sl = c;
+                }
+            if (sl < 0)
+                break;   // every slot is pinned or filled by this call: the rest of the list stays out
+            if (t.expert_in[sl] >= 0)
+                t.slot_of[t.expert_in[sl]] = -1;
+            else
+                t.n_loaded++;
+            t.expert_in[sl] = e;
+            t.slot_of[e] = sl;
+            t.last_use[sl] = t.clock;   // as recent as the last call
+            taken[sl] = 1;
+            src.push_back(e);
+            dst.push_back(sl);
+            t.stats[2] += t.qb + t.sc * sizeof(float);
+        }
+        if (pin) {
+            t.pinned[sl] = 1;
+            npin++;
+        }
+    }
+    int rc = tier_copy(t, src, dst, cs);
+    if (rc != MOE_OK)
+        return rc;
+    if (t.n_loaded == t.E && !t.map_uploaded) {
+        std::memcpy(t.stage_map, t.slot_of.data(), (size_t)t.E * sizeof(int32_t));
+        t.map_uploaded = true;
+    }
+    // the next layer call treats these experts as resident: their copies must be complete
+    return cudaStreamSynchronize(cs) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
 int moe_tier_pin(moe_tier t, const int32_t *experts, int n, void *copy_stream)
 {
     if (t == nullptr || n < 0 || (n > 0 && experts == nullptr))
         return MOE_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(t->mu);
-    int npin = 0;
-    for (int sl = 0; sl < t->n_slots; sl++)
-        npin += t->pinned[sl];
-    for (int i = 0; i < n; i++) {
-        const int e = experts[i];
-        if (e < 0 || e >= t->E)
-            return MOE_ERR_INVALID_ARG;
-        if (t->slot_of[e] >= 0 && t->pinned[t->slot_of[e]])
-            continue;
-        if (npin + 1 >= t->n_slots)
-            return MOE_ERR_INVALID_ARG;   // at least one slot stays free for the experts of a call
-        int sl = t->slot_of[e];
-        if (sl < 0) {
-            // load it into the least recently used unpinned slot
-            for (int c = 0; c < t->n_slots; c++) {
-                if (t->pinned[c])
-                    continue;
-                if (sl < 0 || t->last_use[c] < t->last_use[sl])
-                    sl = c;
-            }
-            if (t->expert_in[sl] >= 0)
-                t->slot_of[t->expert_in[sl]] = -1;
-            t->expert_in[sl] = e;
-            t->slot_of[e] = sl;
-            const int rc = tier_copy(*t, e, sl, reinterpret_cast<cudaStream_t>(copy_stream));
-            if (rc != MOE_OK)
-                return rc;
-            t->stats[2] += t->qb + t->sc * sizeof(float);
-        }
-        t->pinned[sl] = 1;
-        npin++;
-    }
-    // the next layer call treats pinned experts as resident: their copies must be complete
-    return cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(copy_stream)) == cudaSuccess ? MOE_OK
-                                                                                              : MOE_ERR_CUDA;
+    return tier_load(*t, experts, n, true, reinterpret_cast<cudaStream_t>(copy_stream));
+}
+
+int moe_tier_prefetch(moe_tier t, const int32_t *experts, int n, void *copy_stream)
+{
+    if (t == nullptr || n < 0 || (n > 0 && experts == nullptr))
+        return MOE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(t->mu);
+    return tier_load(*t, experts, n, false, reinterpret_cast<cudaStream_t>(copy_stream));
 }
 
 int moe_tier_unpin_all(moe_tier t)
@@ -317,6 +379,60 @@ int moe_layer_forward_tier(const float *x, const float *w_gate, const float *bia
                           err, s);
     if (rc != MOE_OK)
         return rc;
+    moe_layer_int4 view{t.slot_q, t.slot_s, shared_q, shared_s, t.n_slots, d, f, t.G};
+    if (t.map_uploaded) {
+        // every expert has a slot: no host round trip, one FFN launch over the union
+        if (cudaMemcpyAsync(map, t.stage_map, (size_t)E * sizeof(int32_t), cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        t.stats[3] += 1;
+        if (mode == MOE_MODE_PREFILL) {
+            PrefillFfnArgs pa{};
+            pa.w = &view;
+            pa.x = x;
+            pa.offsets = sc.offsets;
+            pa.sorted_pair = sc.sorted_pair;
+            pa.uniq = sc.uniq;
+            pa.n_uniq = sc.n_uniq;
+            pa.T = T;
+            pa.k = k;
+            pa.scratch = sc.ffn;
+            pa.y_pair = nullptr;
+            pa.y_pair16 = reinterpret_cast<uint16_t *>(sc.y_pair);
+            pa.y_shared = sc.y_shared;
+            pa.slot_of = map;
+            pa.n_experts = E;
+            pa.err = err;
+            rc = launch_ffn_prefill(pa, s);
+            if (rc != MOE_OK)
+                return rc;
+            return launch_combine_bf16(reinterpret_cast<const uint16_t *>(sc.y_pair), sc.y_shared, wt, sc.perm,
+                                       residual, T, k, d, out, s);
+        }
+        FfnScratch fs{};
+        ffn_scratch_layout(T, k, d, f, sc.ffn, &fs);
+        rc = launch_act_frag(x, T, d, fs.x_frag, fs.x_scale, fs.work, kDecodeCounters, s);
+        DecodeFfnArgs a{};
+        a.w = &view;
+        a.offsets = sc.offsets;
+        a.sorted_pair = sc.sorted_pair;
+        a.uniq = sc.uniq;
+        a.n_uniq = sc.n_uniq;
+        a.T = T;
+        a.k = k;
+        a.x_frag = fs.x_frag;
+        a.x_scale = fs.x_scale;
+        a.h_frag = fs.h_frag;
+        a.y_pair = sc.y_pair;
+        a.y_shared = sc.y_shared;
+        a.work = fs.work;
+        a.slot_of = map;
+        a.err = err;
+        if (rc == MOE_OK)
+            rc = launch_ffn_decode(a, s);
+        if (rc != MOE_OK)
+            return rc;
+        return launch_combine(sc.y_pair, sc.y_shared, wt, sc.perm, residual, T, k, d, out, s);
+    }
     if (cudaMemcpyAsync(t.stage_in, sc.n_uniq, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaMemcpyAsync(t.stage_in + 1, sc.uniq, (size_t)E * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
             cudaSuccess ||
@@ -331,8 +447,7 @@ int moe_layer_forward_tier(const float *x, const float *w_gate, const float *bia
     rc = tier_plan(t, t.stage_in + 1, n, resident, missing, dst);
     if (rc != MOE_OK)
         return rc;
-    for (size_t i = 0; i < missing.size() && rc == MOE_OK; i++)
-        rc = tier_copy(t, missing[i], dst[i], cs);
+    rc = tier_copy(t, missing, dst, cs);
     if (rc != MOE_OK) {
         for (size_t i = 0; i < missing.size(); i++) {   // their slots hold nothing usable now
             t.slot_of[missing[i]] = -1;
@@ -342,6 +457,10 @@ int moe_layer_forward_tier(const float *x, const float *w_gate, const float *bia
     }
     if (!missing.empty() && cudaEventRecord(t.ev_copy, cs) != cudaSuccess)
         return MOE_ERR_CUDA;
+    if (t.n_loaded == E && !t.map_uploaded) {   // from the next call on, nothing can miss
+        std::memcpy(t.stage_map, t.slot_of.data(), (size_t)E * sizeof(int32_t));
+        t.map_uploaded = true;
+    }
     t.stats[0] += resident.size();
     t.stats[1] += missing.size();
     t.stats[2] += missing.size() * (t.qb + t.sc * sizeof(float));
@@ -360,7 +479,6 @@ int moe_layer_forward_tier(const float *x, const float *w_gate, const float *bia
 
     // ---- Overlap: the FFN over the resident experts (and the shared expert) now, over the copied
     // ones once their copies are done
-    moe_layer_int4 view{t.slot_q, t.slot_s, shared_q, shared_s, t.n_slots, d, f, t.G};
     if (mode == MOE_MODE_PREFILL) {
         PrefillFfnArgs pa{};
         pa.w = &view;

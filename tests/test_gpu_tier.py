@@ -66,10 +66,13 @@ def test_tier_matches_resident_layer(mode_name, T, n_slots):
     assert np.array_equal(host(hits_t), host(hits_r))
     st = tier.stats()
     blk = m.expert_q_bytes(sh.d, sh.f) + 4 * m.expert_s_count(sh.d, sh.f)
-    assert st["calls"] == 6 and st["hits"] + st["misses"] == uniq_total
-    assert st["bytes_copied"] == st["misses"] * blk
-    if n_slots >= sh.E:
-        assert st["misses"] <= sh.E            # every expert copied at most once
+    assert st["calls"] == 6 and st["bytes_copied"] == st["misses"] * blk
+    if n_slots < sh.E:
+        assert st["hits"] + st["misses"] == uniq_total
+    else:
+        # every expert copied at most once; once all have slots, calls skip the host round trip and
+        # count no hits
+        assert st["misses"] <= sh.E and st["hits"] + st["misses"] <= uniq_total
     tier.close()
 
 
@@ -112,4 +115,32 @@ def test_tier_pins_the_learned_hot_set_and_refuses_overfull_batches():
     tier.unpin_all()
     _, pn = tier.slots()
     assert not pn.any()
+    tier.close()
+
+
+def test_tier_prefetch_all_takes_the_device_only_path():
+    """With every expert prefetched into the slots no call can miss: calls skip the host round trip
+    (no hits counted, nothing copied) and still give the resident layer's bits."""
+    m = moe()
+    sh = Shape("tier_all", E=16, k=4, d=1024, f=256, T=5, bias="normal")
+    L = workloads.layer_inputs(sh, seed=8, threads=4)
+    dev = device_layer(L)
+    tier = _tier(m, L, sh.E)
+    copy = torch.cuda.Stream()
+    tier.prefetch(np.arange(sh.E)[::-1], copy_stream=copy)
+    ex, pn = tier.slots()
+    assert sorted(ex.tolist()) == list(range(sh.E)) and not pn.any()
+    before = tier.stats()
+    for i in range(4):
+        x = torch.from_numpy(workloads.activations(sh.T, sh.d, seed=300 + i)).cuda()
+        for mode in (m.MOE_MODE_DECODE, m.MOE_MODE_PREFILL):
+            out_t, err = m.moe_layer_forward_tier(x, dev["wg"], dev["bias"], tier, dev["layer"].shared_q,
+                                                  dev["layer"].shared_s, sh.k, mode=mode, copy_stream=copy)
+            out_r, _ = m.moe_layer_forward(x, dev["wg"], dev["bias"], dev["layer"], sh.k, mode=mode)
+            torch.cuda.synchronize()
+            assert int(host(err)[0]) == 0 and np.array_equal(host(out_t), host(out_r))
+    after = tier.stats()
+    assert after["calls"] - before["calls"] == 8
+    assert after["hits"] == before["hits"] and after["misses"] == before["misses"]
+    assert after["bytes_copied"] == before["bytes_copied"]
     tier.close()
