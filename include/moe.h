@@ -19,6 +19,11 @@
  *    Every call only enqueues work on that stream and returns; nothing is
  *    synchronised and nothing is read back to the host.  The calls keep no
  *    global state and are safe to issue from several host threads.
+ *  - The kernels are programmatic dependent launches: each may start while
+ *    the kernel before it in the stream finishes, and waits for it before it
+ *    reads activations, routing or scratch.  Weights (router, bias, experts)
+ *    are read before that wait, to start their streaming early: they must
+ *    not be written by work still running in the stream when a call starts.
  *  - Return value: MOE_OK, or a negative MOE_ERR_* code when an argument is
  *    invalid or unsupported (nothing is enqueued then) or a launch failed.
  *    The library never exits, traps or prints.

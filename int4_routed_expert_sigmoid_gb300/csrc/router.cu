@@ -508,6 +508,11 @@ __global__ void __launch_bounds__(kFragThreads)
 act_frag_kernel(const float *__restrict__ x, int K, uint8_t *__restrict__ frag, float *__restrict__ row_scale,
                 int32_t *__restrict__ zero, int nzero)
 {
+    // launched as a programmatic dependent: resident while the previous kernel finishes, but x may
+    // come from that kernel and the fragments and counters are still read by the previous FFN, so
+    // everything waits for it
+    griddep_launch_dependents();
+    griddep_wait();
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < nzero; i += blockDim.x)
             zero[i] = 0;
@@ -590,8 +595,7 @@ int launch_act_frag(const float *x, int rows, int K, uint8_t *frag, float *row_s
 {
     if (rows <= 0)
         return MOE_OK;
-    act_frag_kernel<<<rows, kFragThreads, 0, s>>>(x, K, frag, row_scale, zero, nzero);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(act_frag_kernel, rows, kFragThreads, 0, s, x, K, frag, row_scale, zero, nzero);
 }
 
 }  // namespace moe
