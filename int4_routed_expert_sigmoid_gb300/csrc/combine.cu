@@ -35,16 +35,31 @@ combine_kernel(const Y *__restrict__ y_pair, const float4 *__restrict__ y_shared
     float4 acc = res ? res[id] : make_float4(0.f, 0.f, 0.f, 0.f);
     const float4 ys = y_shared[id];
     acc.x += ys.x; acc.y += ys.y; acc.z += ys.z; acc.w += ys.w;
-    for (int j = 0; j < k; j++) {
-        const int q = perm[(size_t)t * k + j];
-        if (q < 0)
-            continue;
-        const float wj = w[(size_t)t * k + j];
-        const float4 y = load4(y_pair, (size_t)q * d4 + c);
-        acc.x = fmaf(wj, y.x, acc.x);
-        acc.y = fmaf(wj, y.y, acc.y);
-        acc.z = fmaf(wj, y.z, acc.z);
-        acc.w = fmaf(wj, y.w, acc.w);
+    // slots in groups of 8: the group's positions and weights, then all of its rows, are loaded
+    // before the first is added (two round trips per group instead of two per slot); the sum
+    // still runs in slot order
+    constexpr int kG = 8;
+    for (int j0 = 0; j0 < k; j0 += kG) {
+        int q[kG];
+        float wj[kG];
+#pragma unroll
+        for (int u = 0; u < kG; u++) {
+            const int j = j0 + u;
+            q[u] = j < k ? perm[(size_t)t * k + j] : -1;
+            wj[u] = j < k ? w[(size_t)t * k + j] : 0.f;
+        }
+        float4 y[kG];
+#pragma unroll
+        for (int u = 0; u < kG; u++)
+            y[u] = q[u] >= 0 ? load4(y_pair, (size_t)q[u] * d4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < kG; u++)
+            if (q[u] >= 0) {
+                acc.x = fmaf(wj[u], y[u].x, acc.x);
+                acc.y = fmaf(wj[u], y[u].y, acc.y);
+                acc.z = fmaf(wj[u], y[u].z, acc.z);
+                acc.w = fmaf(wj[u], y[u].w, acc.w);
+            }
     }
     out[id] = acc;
 }

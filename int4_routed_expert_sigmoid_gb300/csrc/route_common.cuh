@@ -29,24 +29,25 @@ __device__ __forceinline__ bool key_before(float ka, int ea, float kb, int eb)
     return ka > kb || (ka == kb && ea < eb);
 }
 
-// Dynamic shared memory of topk_block: keys [8][E] and, per token, the
-// candidates followed by the k result slots.
+// Dynamic shared memory of topk_block: keys and scores [8][E]; per token, the
+// candidates followed by the k result slots, and the candidates' keys.
 __host__ __device__ constexpr int topk_cand_cap(int E, int k) { return ((E + 31) / 32) * (k < 32 ? k : 32); }
 __host__ __device__ constexpr int topk_cand_stride(int E, int k) { return topk_cand_cap(E, k) + 32; }
 __host__ __device__ constexpr size_t topk_smem_bytes(int E, int k)
 {
-    return (size_t)kTopkTokens * E * 4 + (size_t)kTopkTokens * topk_cand_stride(E, k) * 4;
+    return (size_t)kTopkTokens * E * 4 * 2 + (size_t)kTopkTokens * topk_cand_stride(E, k) * 4 * 2;
 }
 
 // Top-k of tokens t0 .. t0 + nt - 1 (nt <= 8) by the whole block (256 threads):
-//  1. every (token, expert) key into shared memory (one thread each);
+//  1. every (token, expert) score and key into shared memory (one thread each);
 //  2. per 32-expert block, each expert's rank within the block; the block's
-//     first k (at most) become candidates -- every expert of the overall top-k
-//     is among its block's top-k;
+//     first k (at most) become candidates, stored with their keys -- every
+//     expert of the overall top-k is among its block's top-k;
 //  3. every candidate is ranked among its token's candidates (one thread
-//     each); rank j < k fills slot j; one warp per token forms the weights
-//     (and, with top_p < 1, cuts the slots: slot j stays when the scores of
-//     slots 0 .. j-1 add up to less than top_p times the scores of all k).
+//     each, reading the candidates' ids and keys side by side); rank j < k
+//     fills slot j; one warp per token forms the weights (and, with top_p < 1,
+//     cuts the slots: slot j stays when the scores of slots 0 .. j-1 add up to
+//     less than top_p times the scores of all k).
 // Writes idx/w rows of the tokens and, when sel is not null, the ids to
 // sel[(t - t0) * k + j].  Called by all threads of the block (it synchronises).
 __device__ __forceinline__ void topk_block(const float *__restrict__ logits, const float *__restrict__ bias,
@@ -54,13 +55,31 @@ __device__ __forceinline__ void topk_block(const float *__restrict__ logits, con
                                            float top_p, int32_t *__restrict__ idx, float *__restrict__ w,
                                            int *sel, uint8_t *smem)
 {
-    float *keys = reinterpret_cast<float *>(smem);                   // [8][E]
-    int *cand = reinterpret_cast<int *>(smem + (size_t)kTopkTokens * E * 4);
     const int stride = topk_cand_stride(E, k);
+    float *keys = reinterpret_cast<float *>(smem);                                   // [8][E]
+    float *scores = keys + kTopkTokens * E;                                          // [8][E]
+    int *cand = reinterpret_cast<int *>(scores + kTopkTokens * E);                   // [8][stride]
+    float *ckey = reinterpret_cast<float *>(cand + kTopkTokens * stride);            // [8][stride]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < nt * E; i += kTopkThreads) {
-        const int t = i / E, e = i - t * E;
-        keys[t * E + e] = router_score(logits[(size_t)(t0 + t) * E + e]) + (bias ? bias[e] : 0.0f);
+    constexpr int kU = 8;   // logits (and biases) of kU elements per thread loaded before any is used
+    for (int i0 = 0; i0 < nt * E; i0 += kU * kTopkThreads) {
+        float l[kU], bb[kU];
+#pragma unroll
+        for (int u = 0; u < kU; u++) {
+            const int i = i0 + u * kTopkThreads + tid;
+            const int t = i / E, e = i - t * E;
+            l[u] = i < nt * E ? logits[(size_t)(t0 + t) * E + e] : 0.0f;
+            bb[u] = (i < nt * E && bias) ? bias[e] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; u++) {
+            const int i = i0 + u * kTopkThreads + tid;
+            if (i < nt * E) {
+                const float sc = router_score(l[u]);
+                scores[i] = sc;
+                keys[i] = sc + bb[u];
+            }
+        }
     }
     __syncthreads();
     const int nblk = (E + 31) / 32;
@@ -74,27 +93,33 @@ __device__ __forceinline__ void topk_block(const float *__restrict__ logits, con
             int r = 0;
             for (int j = 0; j < n_in; j++)
                 r += key_before(kr[j], j, kv, lane) ? 1 : 0;
-            if (r < kb)
+            if (r < kb) {
                 cand[t * stride + b * kb + r] = b * 32 + lane;
+                ckey[t * stride + b * kb + r] = kv;
+            }
         }
         // a block with fewer than k experts leaves its remaining slots empty
-        if (lane >= n_in && lane < kb)
+        if (lane >= n_in && lane < kb) {
             cand[t * stride + b * kb + lane] = -1;
+            ckey[t * stride + b * kb + lane] = 0.0f;
+        }
     }
     __syncthreads();
     const int nc = nblk * kb;
     for (int i = tid; i < nt * nc; i += kTopkThreads) {
         const int t = i / nc, c = i - t * nc;
         const int *cr = cand + t * stride;
+        const float *kc = ckey + t * stride;
         const int e = cr[c];
         if (e < 0)
             continue;
-        const float *kr = keys + t * E;
-        const float kv = kr[e];
+        const float kv = kc[c];
         int r = 0;
+#pragma unroll 8
         for (int j = 0; j < nc; j++) {
             const int ej = cr[j];
-            r += (ej >= 0 && key_before(kr[ej], ej, kv, e)) ? 1 : 0;
+            const float kj = kc[j];
+            r += (ej >= 0 && key_before(kj, ej, kv, e)) ? 1 : 0;
         }
         if (r < k)
             cand[t * stride + nc + r] = e;
@@ -103,7 +128,7 @@ __device__ __forceinline__ void topk_block(const float *__restrict__ logits, con
     if (warp < nt) {
         const int t = warp;
         int my_e = lane < k ? cand[t * stride + nc + lane] : 0;
-        float my_s = lane < k ? router_score(logits[(size_t)(t0 + t) * E + my_e]) : 0.0f;
+        float my_s = lane < k ? scores[t * E + my_e] : 0.0f;
         if (top_p < 1.0f) {
             // exclusive prefix of the scores in slot order, and their total
             float inc = my_s;

@@ -16,8 +16,15 @@
 namespace moe {
 namespace {
 
-__device__ void act_frag_row(const float *__restrict__ x, int r, int K, int id0, int id1,
-                             uint8_t *__restrict__ frag, float *__restrict__ row_scale);
+constexpr int kFragThreads = 256;   // threads of act_frag_kernel
+constexpr int kXGpc = 8;            // scale groups per fragment block of x
+
+__device__ __forceinline__ void frag_quad(const float *__restrict__ xr, float mx, int id, bool act,
+                                          uint8_t *__restrict__ row);
+__device__ __forceinline__ float absmax4(float4 v)
+{
+    return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+}
 
 // ----------------------------------------------------------------- logits ---
 // Small T: each CTA owns kEB experts x kTB tokens and splits the reduction
@@ -49,6 +56,11 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
         a = fmaf(xv.z, wv.z, a);
         a = fmaf(xv.w, wv.w, a);
     };
+    // per-thread max |x| of each token (the fused path's fragments need the row maxima)
+    float xmax[kTB];
+#pragma unroll
+    for (int b = 0; b < kTB; b++)
+        xmax[b] = 0.f;
     if (d4 <= kSkinnyIt * kSkinnyThreads) {
         // the router weights do not depend on the previous kernel: all of this thread's loads are
         // issued before waiting on it
@@ -61,19 +73,27 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
                 wv[it][a] = (i < d4 && a < ne) ? __ldg(w4 + (size_t)(e0 + a) * d4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         griddep_wait();   // x may come from the previous kernel in the stream
+        // a token's whole slice of x is loaded before any of it is used: one round trip per token
 #pragma unroll
-        for (int it = 0; it < kSkinnyIt; it++) {
-            const int i = threadIdx.x + it * kSkinnyThreads;
-            if (i >= d4)
-                break;
+        for (int b = 0; b < kTB; b++) {
+            if (b >= nt)
+                continue;
+            float4 xv[kSkinnyIt];
 #pragma unroll
-            for (int b = 0; b < kTB; b++)
-                if (b < nt) {
-                    const float4 xv = __ldg(x4 + (size_t)(t0 + b) * d4 + i);
+            for (int it = 0; it < kSkinnyIt; it++) {
+                const int i = threadIdx.x + it * kSkinnyThreads;
+                xv[it] = i < d4 ? __ldg(x4 + (size_t)(t0 + b) * d4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int it = 0; it < kSkinnyIt; it++) {
+                const int i = threadIdx.x + it * kSkinnyThreads;
+                if (i < d4) {
 #pragma unroll
                     for (int a = 0; a < kEB; a++)
-                        fma4(xv, wv[it][a], acc[a][b]);
+                        fma4(xv[it], wv[it][a], acc[a][b]);
+                    xmax[b] = fmaxf(xmax[b], absmax4(xv[it]));
                 }
+            }
         }
     } else {
         griddep_wait();
@@ -89,17 +109,19 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
 #pragma unroll
                     for (int a = 0; a < kEB; a++)
                         fma4(xv, wv[a], acc[a][b]);
+                    xmax[b] = fmaxf(xmax[b], absmax4(xv));
                 }
         }
     }
     __shared__ float part[kSkinnyThreads / 32][kEB * kTB];
+    __shared__ float pmax[kSkinnyThreads / 32][kTB];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-    for (int a = 0; a < kEB; a++)
+    for (int b = 0; b < kTB; b++) {
+        if (b >= nt)
+            continue;
 #pragma unroll
-        for (int b = 0; b < kTB; b++) {
-            if (b >= nt)
-                continue;
+        for (int a = 0; a < kEB; a++) {
             float v = acc[a][b];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1)
@@ -107,6 +129,15 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
             if (lane == 0)
                 part[warp][a * kTB + b] = v;
         }
+        if (frag != nullptr) {
+            float m = xmax[b];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (lane == 0)
+                pmax[warp][b] = m;
+        }
+    }
     __syncthreads();
     if (threadIdx.x < kEB * kTB) {
         const int a = threadIdx.x / kTB, b = threadIdx.x % kTB;
@@ -118,18 +149,36 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
         }
     }
     // fused path: block (0, 0) zeroes the FFN's counters (this is after the grid wait: the previous
-    // layer's FFN, which used them, has finished), and the blocks build the FFN's fragments of x
-    // (256-element chunks of the rows, spread over the blocks)
+    // layer's FFN, which used them, has finished), and the blocks build the FFN's fragments of x:
+    // every block has the row maxima, and each converts an equal share of the (token, group) units,
+    // four threads (one per quad of 8 elements) per unit
     if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int i = threadIdx.x; i < nzero; i += blockDim.x)
             zero[i] = 0;
-    const int chunks = d / 256;
-    if (frag != nullptr && blockIdx.y == 0)
-        for (int wu = blockIdx.x; wu < T * chunks; wu += gridDim.x) {
-            __syncthreads();
-            const int r = wu / chunks, c = wu - r * chunks;
-            act_frag_row(x, r, d, c * 32, c * 32 + 32, frag, row_scale);
+    if (frag != nullptr && blockIdx.y == 0) {
+        const int G = d / 32;
+        const int nu = nt * G;
+        const int per = (nu + gridDim.x - 1) / gridDim.x;
+        const int u0 = min(nu, (int)blockIdx.x * per), u1 = min(nu, u0 + per);
+        if (blockIdx.x == 0 && threadIdx.x < nt) {
+            float mx = 0.f;
+            for (int w = 0; w < kSkinnyThreads / 32; w++)
+                mx = fmaxf(mx, pmax[w][threadIdx.x]);
+            int e = 0;
+            frexpf(mx, &e);
+            row_scale[t0 + threadIdx.x] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
         }
+        for (int base = u0; base < u1; base += kSkinnyThreads / 4) {   // uniform over the block
+            const int u = base + (int)(threadIdx.x >> 2);
+            const bool act = u < u1;
+            const int b = act ? u / G : 0, g = act ? u - b * G : 0;
+            float mx = 0.f;
+            for (int w = 0; w < kSkinnyThreads / 32; w++)
+                mx = fmaxf(mx, pmax[w][b]);
+            frag_quad(x + (size_t)(t0 + b) * d, mx, g * 4 + (int)(threadIdx.x & 3), act,
+                      frag + (size_t)(t0 + b) * frag_row_bytes(d, kXGpc));
+        }
+    }
 }
 
 // Large T: register-tiled fp32 GEMM, C[T][E] = X[T][d] * Wg[E][d]^T.
@@ -427,21 +476,79 @@ topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, in
 // written as fragment blocks of 8 groups (layout in moe_internal.h), with the
 // accumulator inputs -2^-24 * 8 * sum (16 at odd offsets, else 1) * value and,
 // in every group's factor slot, the row factor 2^(e-14).
-constexpr int kFragThreads = 256;
-constexpr int kXGpc = 8;
 
-// Fragments of (group, quad) ids [id0, id1) of row r of x, computed by the
-// whole (256-thread) block; every block reads the whole row for its maximum,
-// the block holding id 0 writes the row factor.
-__device__ void act_frag_row(const float *__restrict__ x, int r, int K, int id0, int id1,
-                             uint8_t *__restrict__ frag, float *__restrict__ row_scale)
+// Fragments of one (group, quad) id of a row xr of x whose max |x| is mx: the
+// 8 elements 32 * group + 8 * quad .. + 7 become hi/lo fp16 values in the
+// fragment block, and the quad's share of the group's accumulator inputs is
+// summed over the group's four quads with two shuffles, so the four quads of
+// a group must sit in lanes 4j .. 4j + 3 of one warp and the whole warp calls
+// this (act = false for lanes without an id).  The group's first quad writes
+// the corrections and, in the group's factor slot, the row factor.
+__device__ __forceinline__ void frag_quad(const float *__restrict__ xr, float mx, int id, bool act,
+                                          uint8_t *__restrict__ row)
+{
+    int e = 0;
+    frexpf(mx, &e);
+    const float up = mx > 0.f ? ldexpf(1.0f, 14 - e) : 1.0f;
+    const int g = id >> 2, q = id & 3;
+    uint8_t *blk = row + (size_t)(g / kXGpc) * frag_blk(kXGpc);
+    const int gl = g % kXGpc;
+    float chi = 0.f, clo = 0.f;
+    if (act) {
+        const float4 *src = reinterpret_cast<const float4 *>(xr + 32 * g + 8 * q);
+        const float4 v0 = src[0], v1 = src[1];
+        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        __align__(16) uint16_t hi[8], lo[8];
+#pragma unroll
+        for (int o = 0; o < 8; o++) {
+            float sv = v[o] * up;
+            if (o & 1)
+                sv *= 0.0625f;
+            const __half h = __float2half_rn(sv);
+            const __half l = __float2half_rn(sv - __half2float(h));
+            hi[frag_pos(o)] = __half_as_ushort(h);
+            lo[frag_pos(o)] = __half_as_ushort(l);
+            const float wgt = (o & 1) ? 128.0f : 8.0f;
+            chi += wgt * __half2float(h);
+            clo += wgt * __half2float(l);
+        }
+        *reinterpret_cast<uint4 *>(blk + gl * 64 + q * 16) = *reinterpret_cast<const uint4 *>(hi);
+        *reinterpret_cast<uint4 *>(blk + frag_lo(kXGpc) + gl * 64 + q * 16) = *reinterpret_cast<const uint4 *>(lo);
+    }
+    chi += __shfl_xor_sync(0xffffffffu, chi, 1);
+    clo += __shfl_xor_sync(0xffffffffu, clo, 1);
+    chi += __shfl_xor_sync(0xffffffffu, chi, 2);
+    clo += __shfl_xor_sync(0xffffffffu, clo, 2);
+    if (act && q == 0) {
+        float *c = reinterpret_cast<float *>(blk + frag_corr(kXGpc)) + gl * 2;
+        c[0] = -chi * 0x1p-24f;
+        c[1] = -clo * 0x1p-24f;
+        // every group's factor slot holds the row factor, so it reaches the FFN with each stage
+        reinterpret_cast<float *>(blk + frag_fac(kXGpc))[gl] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
+    }
+}
+
+// Fragments of the whole row r of x by one 256-thread block: the row's max |x|
+// (all of the row's loads issued before the reduction), then every (group,
+// quad) id; the row factor goes to row_scale[r].
+__device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint8_t *__restrict__ frag,
+                             float *__restrict__ row_scale)
 {
     __shared__ float wmax[kFragThreads / 32];
     const float *xr = x + (size_t)r * K;
+    const float4 *x4 = reinterpret_cast<const float4 *>(xr);
     float mx = 0.f;
-    for (int i = threadIdx.x; i < K / 4; i += kFragThreads) {
-        const float4 v = reinterpret_cast<const float4 *>(xr)[i];
-        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    constexpr int kU = 8;
+    for (int i0 = 0; i0 < K / 4; i0 += kU * kFragThreads) {
+        float4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; u++) {
+            const int i = i0 + u * kFragThreads + threadIdx.x;
+            v[u] = i < K / 4 ? x4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; u++)
+            mx = fmaxf(mx, absmax4(v[u]));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
@@ -453,55 +560,16 @@ __device__ void act_frag_row(const float *__restrict__ x, int r, int K, int id0,
 #pragma unroll
     for (int w = 0; w < kFragThreads / 32; w++)
         mx = fmaxf(mx, wmax[w]);
-    __syncthreads();   // wmax may be reused by the caller
-    int e = 0;
-    frexpf(mx, &e);
-    const float up = mx > 0.f ? ldexpf(1.0f, 14 - e) : 1.0f;
-    if (threadIdx.x == 0 && id0 == 0)
+    if (threadIdx.x == 0) {
+        int e = 0;
+        frexpf(mx, &e);
         row_scale[r] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
-    uint8_t *row = frag + (size_t)r * frag_row_bytes(K, kXGpc);
-    // (group, quad) ids: quads of a group are adjacent; whole warps take part in the shuffles
-    const int n_pad = id0 + (id1 - id0 + 31) / 32 * 32;
-    for (int id = id0 + threadIdx.x; id < n_pad; id += kFragThreads) {
-        const bool act = id < id1;
-        const int g = id >> 2, q = id & 3;
-        uint8_t *blk = row + (size_t)(g / kXGpc) * frag_blk(kXGpc);
-        const int gl = g % kXGpc;
-        float chi = 0.f, clo = 0.f;
-        if (act) {
-            const float4 *src = reinterpret_cast<const float4 *>(xr + 32 * g + 8 * q);
-            const float4 v0 = src[0], v1 = src[1];
-            const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-            __align__(16) uint16_t hi[8], lo[8];
-#pragma unroll
-            for (int o = 0; o < 8; o++) {
-                float sv = v[o] * up;
-                if (o & 1)
-                    sv *= 0.0625f;
-                const __half h = __float2half_rn(sv);
-                const __half l = __float2half_rn(sv - __half2float(h));
-                hi[frag_pos(o)] = __half_as_ushort(h);
-                lo[frag_pos(o)] = __half_as_ushort(l);
-                const float wgt = (o & 1) ? 128.0f : 8.0f;
-                chi += wgt * __half2float(h);
-                clo += wgt * __half2float(l);
-            }
-            *reinterpret_cast<uint4 *>(blk + gl * 64 + q * 16) = *reinterpret_cast<const uint4 *>(hi);
-            *reinterpret_cast<uint4 *>(blk + frag_lo(kXGpc) + gl * 64 + q * 16) =
-                *reinterpret_cast<const uint4 *>(lo);
-        }
-        chi += __shfl_xor_sync(0xffffffffu, chi, 1);
-        clo += __shfl_xor_sync(0xffffffffu, clo, 1);
-        chi += __shfl_xor_sync(0xffffffffu, chi, 2);
-        clo += __shfl_xor_sync(0xffffffffu, clo, 2);
-        if (act && q == 0) {
-            float *c = reinterpret_cast<float *>(blk + frag_corr(kXGpc)) + gl * 2;
-            c[0] = -chi * 0x1p-24f;
-            c[1] = -clo * 0x1p-24f;
-            // every group's factor slot holds the row factor, so it reaches the FFN with each stage
-            reinterpret_cast<float *>(blk + frag_fac(kXGpc))[gl] = mx > 0.f ? ldexpf(1.0f, e - 14) : 1.0f;
-        }
     }
+    uint8_t *row = frag + (size_t)r * frag_row_bytes(K, kXGpc);
+    const int n_id = (K / 32) * 4;
+    const int n_pad = (n_id + 31) / 32 * 32;   // whole warps take part in the shuffles
+    for (int id = threadIdx.x; id < n_pad; id += kFragThreads)
+        frag_quad(xr, mx, id, id < n_id, row);
 }
 
 __global__ void __launch_bounds__(kFragThreads)
@@ -516,7 +584,7 @@ act_frag_kernel(const float *__restrict__ x, int K, uint8_t *__restrict__ frag, 
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < nzero; i += blockDim.x)
             zero[i] = 0;
-    act_frag_row(x, blockIdx.x, K, 0, (K / 32) * 4, frag, row_scale);
+    act_frag_row(x, blockIdx.x, K, frag, row_scale);
 }
 
 }  // namespace

@@ -95,8 +95,8 @@ __device__ void union_chunked(const int32_t *__restrict__ idx, int P, int E, int
             base[e] = ex;
             offsets[e] = ex;
             counts[e] = c;
-            if (hits)
-                hits[e] += (uint64_t)c;
+            if (hits && c > 0)
+                atomicAdd(reinterpret_cast<unsigned long long *>(hits + e), (unsigned long long)c);   // no read back
         }
         __syncthreads();
     }
@@ -243,8 +243,8 @@ union_kernel(const int32_t *__restrict__ idx, int T, int k, int E, int use_bitma
             base[e] = ex;
             offsets[e] = ex;
             counts[e] = c;
-            if (hits)
-                hits[e] += (uint64_t)c;
+            if (hits && c > 0)
+                atomicAdd(reinterpret_cast<unsigned long long *>(hits + e), (unsigned long long)c);   // no read back
             if (flag)
                 uniq[ux] = e;
         }
@@ -345,7 +345,7 @@ select_union_kernel(const float *__restrict__ logits, const float *__restrict__ 
         if (cnt > 0) {
             uniq[ubefore] = e;
             if (hits)
-                hits[e] += (uint64_t)cnt;
+                atomicAdd(reinterpret_cast<unsigned long long *>(hits + e), (unsigned long long)cnt);   // no read back
         }
     }
 }
