@@ -409,7 +409,8 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
 
 // Weight loads (packed rows and scales) of stage `c` of an item into ring slot sb.
 template <int MODE, int TOK, int CPS, int GPC, int GS>
-__device__ __forceinline__ void issue_weights(const Maps &maps, const Item &it, int c, uint32_t sb, uint32_t fb)
+__device__ __forceinline__ void issue_weights(const Maps &maps, const Item &it, int c, uint32_t sb, uint32_t fb,
+                                              uint64_t pol)
 {
     using C = Cfg<MODE, TOK, CPS, GPC, GS>;
     const int z = it.expert < 0 ? 0 : it.zq;
@@ -418,11 +419,11 @@ __device__ __forceinline__ void issue_weights(const Maps &maps, const Item &it, 
     const void *mq = &maps.q[w], *ms = &maps.s[w];
     if (maps.merged) {
         if (MODE == kGateUp) {
-            tma_load_5d(sb, mq, 0, row0, 0, c * CPS, z, fb);
-            tma_load_5d(sb + C::kSOff, ms, 0, row0, 0, c * CPS, z, fb);
+            tma_load_5d_hint(sb, mq, 0, row0, 0, c * CPS, z, fb, pol);
+            tma_load_5d_hint(sb + C::kSOff, ms, 0, row0, 0, c * CPS, z, fb, pol);
         } else {
-            tma_load_4d(sb, mq, 0, row0, c * CPS, z, fb);
-            tma_load_4d(sb + C::kSOff, ms, 0, row0, c * CPS, z, fb);
+            tma_load_4d_hint(sb, mq, 0, row0, c * CPS, z, fb, pol);
+            tma_load_4d_hint(sb + C::kSOff, ms, 0, row0, c * CPS, z, fb, pol);
         }
         return;
     }
@@ -430,13 +431,21 @@ __device__ __forceinline__ void issue_weights(const Maps &maps, const Item &it, 
     for (int ch = 0; ch < CPS; ch++) {
         const int cg = c * CPS + ch;
         if (MODE == kGateUp) {
-            tma_load_4d(sb + ch * C::kMats * C::kQSub, mq, cg * C::kRowB, row0, 0, z, fb);
-            tma_load_4d(sb + C::kSOff + ch * C::kMats * C::kSSub, ms, cg * C::kSpr, row0, 0, z, fb);
+            tma_load_4d_hint(sb + ch * C::kMats * C::kQSub, mq, cg * C::kRowB, row0, 0, z, fb, pol);
+            tma_load_4d_hint(sb + C::kSOff + ch * C::kMats * C::kSSub, ms, cg * C::kSpr, row0, 0, z, fb, pol);
         } else {
-            tma_load_3d(sb + ch * C::kQSub, mq, cg * C::kRowB, row0, z, fb);
-            tma_load_3d(sb + C::kSOff + ch * C::kSSub, ms, cg * C::kSpr, row0, z, fb);
+            tma_load_3d_hint(sb + ch * C::kQSub, mq, cg * C::kRowB, row0, z, fb, pol);
+            tma_load_3d_hint(sb + C::kSOff + ch * C::kSSub, ms, cg * C::kSpr, row0, z, fb, pol);
         }
     }
+}
+
+// L2 policy of an item's weights: evict_first when one pass over its tokens reads them once;
+// an item taken in several passes reads them again from L2, so they are cached normally.
+template <int TOK>
+__device__ __forceinline__ uint64_t weight_policy(int m)
+{
+    return m <= TOK ? l2_policy_evict_first() : l2_policy_evict_normal();
 }
 
 template <int MODE, int TOK, int CPS, int GPC, int GS>
@@ -500,13 +509,15 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
             int t0, ntok;
             pass_range(it0.m, (it0.m + TOK - 1) / TOK, 0, t0, ntok);
             pre = nstages < C::kStages ? nstages : C::kStages;
-            if (lane == 0)
+            if (lane == 0) {
+                const uint64_t pol = weight_policy<TOK>(it0.m);
                 for (int c = 0; c < pre; c++) {
                     const uint32_t fb = smem_addr(&full_bar[c]);
                     stage_item[c] = blockIdx.x;
                     mbar_arrive_expect_tx(fb, C::kWeightBytes + ntok * C::kTokBytes);
-                    issue_weights<MODE, TOK, CPS, GPC, GS>(maps, it0, c, stage0 + c * C::kStageBytes, fb);
+                    issue_weights<MODE, TOK, CPS, GPC, GS>(maps, it0, c, stage0 + c * C::kStageBytes, fb, pol);
                 }
+            }
         }
     }
     if (MODE == kGateUp) {
@@ -536,6 +547,7 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
                 next = (int)gridDim.x + atomicAdd(p.work, 1);
             const Item it = decode_item(p, tab, i);
             const int npass = (it.m + TOK - 1) / TOK;
+            const uint64_t pol = weight_policy<TOK>(it.m);
             for (int pass = 0; pass < npass; pass++) {
                 int t0, ntok;
                 pass_range(it.m, npass, pass, t0, ntok);
@@ -558,7 +570,7 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
                         if (lane == 0 && !pre_issued) {
                             stage_item[stage] = i;   // published to the consumers by the arrive below
                             mbar_arrive_expect_tx(fb, tx);
-                            issue_weights<MODE, TOK, CPS, GPC, GS>(maps, it, c, sb, fb);
+                            issue_weights<MODE, TOK, CPS, GPC, GS>(maps, it, c, sb, fb, pol);
                             issued |= 1u << stage;
                         }
                         if (c == 0 && lane < ntok)

@@ -64,13 +64,16 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
     if (d4 <= kSkinnyIt * kSkinnyThreads) {
         // the router weights do not depend on the previous kernel: all of this thread's loads are
         // issued before waiting on it
+        // (read once per call: evict_first, see l2_policy_evict_first)
+        const uint64_t pol = l2_policy_evict_first();
         float4 wv[kSkinnyIt][kEB];
 #pragma unroll
         for (int it = 0; it < kSkinnyIt; it++) {
             const int i = threadIdx.x + it * kSkinnyThreads;
 #pragma unroll
             for (int a = 0; a < kEB; a++)
-                wv[it][a] = (i < d4 && a < ne) ? __ldg(w4 + (size_t)(e0 + a) * d4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                wv[it][a] = (i < d4 && a < ne) ? ldg_hint(w4 + (size_t)(e0 + a) * d4 + i, pol)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         griddep_wait();   // x may come from the previous kernel in the stream
         // a token's whole slice of x is loaded before any of it is used: one round trip per token
