@@ -1,4 +1,5 @@
-// route_common.cuh -- block-level top-k of up to 8 tokens' router logits,
+// route_common.cuh -- top-k of up to 8 tokens' router logits by one block
+// (a warp per token in registers for E <= 256, a rank-based block form above),
 // shared by the stand-alone top-k kernel and the fused select+union kernel.
 //
 // Source: "Public Colibri Observation and Revision Ledger", "Exact Architecture
@@ -36,6 +37,49 @@ __host__ __device__ constexpr int topk_cand_stride(int E, int k) { return topk_c
 __host__ __device__ constexpr size_t topk_smem_bytes(int E, int k)
 {
     return (size_t)kTopkTokens * E * 4 * 2 + (size_t)kTopkTokens * topk_cand_stride(E, k) * 4 * 2;
+}
+
+// The last step of both top-k forms, by the token's warp: lane j < k holds
+// slot j (expert my_e, score my_s); lanes from k on hold (0, 0).  With
+// top_p < 1 the slots are cut: slot j stays when the scores of slots 0 .. j-1
+// add up to less than top_p times the scores of all k.  Then the weights
+// (renormalised to route_scale when normalize) and the idx / w rows; the ids
+// also go to sel[t * k + j] when sel is not null.
+__device__ __forceinline__ void topk_finish(int t0, int t, int lane, int k, int my_e, float my_s, int normalize,
+                                            float route_scale, float top_p, int32_t *__restrict__ idx,
+                                            float *__restrict__ w, int *sel)
+{
+    if (top_p < 1.0f) {
+        // exclusive prefix of the scores in slot order, and their total
+        float inc = my_s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float v = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off)
+                inc += v;
+        }
+        const float total = __shfl_sync(0xffffffffu, inc, 31);
+        float excl = __shfl_up_sync(0xffffffffu, inc, 1);
+        excl = lane == 0 ? 0.0f : excl;
+        if (!(excl < top_p * total)) {   // slots from the first one past the cut
+            my_e = -1;
+            my_s = 0.0f;
+        }
+    }
+    float scale = 1.0f;
+    if (normalize) {
+        float sum = my_s;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        scale = route_scale / sum;
+    }
+    if (lane < k) {
+        idx[(size_t)(t0 + t) * k + lane] = my_e;
+        w[(size_t)(t0 + t) * k + lane] = normalize ? my_s * scale : my_s;
+        if (sel)
+            sel[t * k + lane] = my_e;
+    }
 }
 
 // Top-k of tokens t0 .. t0 + nt - 1 (nt <= 8) by the whole block (256 threads):
@@ -127,39 +171,75 @@ __device__ __forceinline__ void topk_block(const float *__restrict__ logits, con
     __syncthreads();
     if (warp < nt) {
         const int t = warp;
-        int my_e = lane < k ? cand[t * stride + nc + lane] : 0;
-        float my_s = lane < k ? scores[t * E + my_e] : 0.0f;
-        if (top_p < 1.0f) {
-            // exclusive prefix of the scores in slot order, and their total
-            float inc = my_s;
+        const int my_e = lane < k ? cand[t * stride + nc + lane] : 0;
+        const float my_s = lane < k ? scores[t * E + my_e] : 0.0f;
+        topk_finish(t0, t, lane, k, my_e, my_s, normalize, route_scale, top_p, idx, w, sel);
+    }
+    __syncthreads();
+}
+
+// Top-k of tokens t0 .. t0 + nt - 1 (nt <= 8) for E <= 32 * kWarpTopkPer, one
+// warp per token, all in registers: lane l holds the keys of experts l, l + 32,
+// ..., and the k slots are filled one per round by a warp maximum of the key
+// (keys mapped to unsigned integers in the same order, -0 as +0) followed by a
+// warp minimum of the id among the lanes holding that key -- key descending,
+// equal keys by ascending id, as topk_block.  Same outputs as topk_block.
+// Called by all threads of a 256-thread block (it synchronises at the end).
+constexpr int kWarpTopkPer = 8;
+__device__ __forceinline__ void topk_warp(const float *__restrict__ logits, const float *__restrict__ bias, int t0,
+                                          int nt, int E, int k, int normalize, float route_scale, float top_p,
+                                          int32_t *__restrict__ idx, float *__restrict__ w, int *sel)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (warp < nt) {
+        const int t = warp;
+        float l[kWarpTopkPer], bb[kWarpTopkPer];
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float v = __shfl_up_sync(0xffffffffu, inc, off);
-                if (lane >= off)
-                    inc += v;
-            }
-            const float total = __shfl_sync(0xffffffffu, inc, 31);
-            float excl = __shfl_up_sync(0xffffffffu, inc, 1);
-            excl = lane == 0 ? 0.0f : excl;
-            if (!(excl < top_p * total)) {   // slots from the first one past the cut
-                my_e = -1;
-                my_s = 0.0f;
-            }
+        for (int i = 0; i < kWarpTopkPer; i++) {
+            const int e = lane + 32 * i;
+            l[i] = e < E ? logits[(size_t)(t0 + t) * E + e] : 0.0f;
+            bb[i] = (e < E && bias) ? bias[e] : 0.0f;
         }
-        float scale = 1.0f;
-        if (normalize) {
-            float sum = my_s;
+        float sc[kWarpTopkPer];
+        uint32_t ku[kWarpTopkPer];
+        uint32_t taken = 0;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            scale = route_scale / sum;
+        for (int i = 0; i < kWarpTopkPer; i++) {
+            sc[i] = router_score(l[i]);
+            const float key = sc[i] + bb[i];
+            const uint32_t b = __float_as_uint(key);
+            ku[i] = key == 0.0f ? 0x80000000u : ((b & 0x80000000u) ? ~b : (b | 0x80000000u));
+            if (key != key)
+                ku[i] = 0u;   // NaN keys come last
+            if (lane + 32 * i >= E)
+                taken |= 1u << i;
         }
-        if (lane < k) {
-            idx[(size_t)(t0 + t) * k + lane] = my_e;
-            w[(size_t)(t0 + t) * k + lane] = normalize ? my_s * scale : my_s;
-            if (sel)
-                sel[t * k + lane] = my_e;
+        int my_e = 0;
+        float my_s = 0.0f;
+        for (int j = 0; j < k; j++) {
+            uint32_t bu = 0u;
+            int bi = -1;
+            float bs = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kWarpTopkPer; i++)
+                if (!((taken >> i) & 1u) && (bi < 0 || ku[i] > bu)) {
+                    bu = ku[i];
+                    bi = i;
+                    bs = sc[i];
+                }
+            const uint32_t m = __reduce_max_sync(0xffffffffu, bi >= 0 ? bu : 0u);
+            const uint32_t cid = (bi >= 0 && bu == m) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+            const uint32_t win = __reduce_min_sync(0xffffffffu, cid);
+            const int wl = (int)(win & 31u);
+            if (lane == wl)
+                taken |= 1u << (win >> 5);
+            const float ws = __shfl_sync(0xffffffffu, bs, wl);
+            if (lane == j) {
+                my_e = (int)win;
+                my_s = ws;
+            }
         }
+        topk_finish(t0, t, lane, k, my_e, my_s, normalize, route_scale, top_p, idx, w, sel);
     }
     __syncthreads();
 }

@@ -460,7 +460,7 @@ logits_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
 }
 
 // ------------------------------------------------------------------ top-k ---
-// One block per 8 tokens (see topk_block).
+// One block per 8 tokens (topk_warp for E <= 256, else topk_block).
 __global__ void __launch_bounds__(kTopkThreads)
 topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int k,
             int normalize, float route_scale, float top_p, int32_t *__restrict__ idx, float *__restrict__ w)
@@ -468,7 +468,10 @@ topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, in
     extern __shared__ __align__(16) uint8_t tk_smem[];
     const int t0 = blockIdx.x * kTopkTokens;
     const int nt = min(kTopkTokens, T - t0);
-    topk_block(logits, bias, t0, nt, E, k, normalize, route_scale, top_p, idx, w, nullptr, tk_smem);
+    if (E <= 32 * kWarpTopkPer)
+        topk_warp(logits, bias, t0, nt, E, k, normalize, route_scale, top_p, idx, w, nullptr);
+    else
+        topk_block(logits, bias, t0, nt, E, k, normalize, route_scale, top_p, idx, w, nullptr, tk_smem);
 }
 
 // --------------------------------------------------------- act fragments ---

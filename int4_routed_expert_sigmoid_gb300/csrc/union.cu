@@ -294,7 +294,10 @@ select_union_kernel(const float *__restrict__ logits, const float *__restrict__ 
     const int tid = threadIdx.x;
     griddep_launch_dependents();
     griddep_wait();   // logits come from the previous kernel
-    topk_block(logits, bias, 0, T, E, k, normalize, route_scale, top_p, idx, w, se, tk_smem);
+    if (E <= 32 * kWarpTopkPer)
+        topk_warp(logits, bias, 0, T, E, k, normalize, route_scale, top_p, idx, w, se);
+    else
+        topk_block(logits, bias, 0, T, E, k, normalize, route_scale, top_p, idx, w, se, tk_smem);
     const int P = T * k;
     if (tid < P) {
         const int e = se[tid];
