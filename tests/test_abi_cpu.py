@@ -71,3 +71,14 @@ def test_host_validation_rejects_without_launching(m):
     # misaligned pointers are refused
     bad = ctypes.c_void_p(0x1004)
     assert L.moe_hits(bad, 8, bad, P) == m.MOE_ERR_INVALID_ARG
+
+
+def test_binding_error_bits_match_the_header(m):
+    """The binding's device error bits are the header's values."""
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe.h")).read()
+    bits = dict(re.findall(r"#define (MOE_DEVERR_\w+) (0x[0-9a-fA-F]+)", hdr))
+    assert len(bits) == 3
+    for name, val in bits.items():
+        assert getattr(m, name) == int(val, 16), name
