@@ -64,8 +64,9 @@ logits_skinny_kernel(const float *__restrict__ x, const float *__restrict__ wg, 
     if (d4 <= kSkinnyIt * kSkinnyThreads) {
         // the router weights do not depend on the previous kernel: all of this thread's loads are
         // issued before waiting on it
-        // (read once per call: evict_first, see l2_policy_evict_first)
-        const uint64_t pol = l2_policy_evict_first();
+        // read once per call when one block of tokens covers the batch: evict_first (see
+        // l2_policy_evict_first); several token blocks read the same slice, so it stays cached
+        const uint64_t pol = gridDim.y == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
         float4 wv[kSkinnyIt][kEB];
 #pragma unroll
         for (int it = 0; it < kSkinnyIt; it++) {
