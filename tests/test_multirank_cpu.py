@@ -113,6 +113,8 @@ def test_kernel_source_hash_and_traffic_record():
     h = bench.kernel_source_hash(ROOT)
     assert len(h) == 16 and h == bench.kernel_source_hash(ROOT)
     rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
-    for key in ("ffn", "ffn_prefill"):
+    assert "ffn" in rec
+    for key in rec:
         got = bench.ncu_traffic(ROOT, key)
         assert got == (rec[key]["dram_bytes_per_launch"] if rec[key]["source_hash"] == h else None)
+    assert bench.ncu_traffic(ROOT, "no_such_workload") is None
