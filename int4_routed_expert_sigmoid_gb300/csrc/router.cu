@@ -656,7 +656,8 @@ int launch_router_logits_frag(const float *x, const float *wg, int T, int d, int
 int launch_router_topk(const float *logits, const float *bias, int T, int E, int k, int normalize,
                        float route_scale, float top_p, int32_t *idx, float *w, cudaStream_t s)
 {
-    const size_t smem = topk_smem_bytes(E, k);
+    // the warp form (E <= 256) keeps everything in registers: no shared memory to reserve
+    const size_t smem = E <= 32 * kWarpTopkPer ? 0 : topk_smem_bytes(E, k);
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MOE_ERR_CUDA;

@@ -393,7 +393,8 @@ int launch_select_union(const float *logits, const float *bias, int T, int E, in
 {
     if (T > kTopkTokens || T * k > kSelMaxPairs || E > kMaxE)
         return MOE_ERR_UNSUPPORTED;
-    const size_t smem = topk_smem_bytes(E, k);
+    // the warp form (E <= 256) keeps everything in registers: no shared memory to reserve
+    const size_t smem = E <= 32 * kWarpTopkPer ? 0 : topk_smem_bytes(E, k);
     if (smem > 48 * 1024 && cudaFuncSetAttribute(select_union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                   (int)smem) != cudaSuccess)
         return MOE_ERR_CUDA;
