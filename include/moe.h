@@ -87,6 +87,9 @@ enum {
                                        below the first group scale of its weight row, beyond what
                                        the path's fp16 weights hold; that row's outputs lose
                                        precision (the decode path has no such limit) */
+#define MOE_DEVERR_BOUNDS 0x8       /* only in a library built with MOE_DEBUG_BOUNDS: an index (expert
+                                       id, pair position, token or row) was outside its range; the
+                                       access was skipped */
 
 /* FFN execution modes. */
 enum {
@@ -110,8 +113,9 @@ enum {
 MOE_API const char *moe_status_str(int status);
 
 /* Decode a device error word copied to the host: MOE_OK when zero, else
- * MOE_ERR_CUDA for a timeout, MOE_ERR_INVALID_ARG for a bad expert id,
- * MOE_ERR_UNSUPPORTED for scales outside the prefill path's range. */
+ * MOE_ERR_CUDA for a timeout, MOE_ERR_INVALID_ARG for a bad expert id or (in a
+ * MOE_DEBUG_BOUNDS build) an index out of range, MOE_ERR_UNSUPPORTED for scales
+ * outside the prefill path's range. */
 MOE_API int moe_device_error(int32_t err_word_host);
 
 /* Packed bytes / fp32 scale count of one expert block (layout above). */

@@ -24,7 +24,7 @@ template <typename Y>
 __global__ void __launch_bounds__(256)
 combine_kernel(const Y *__restrict__ y_pair, const float4 *__restrict__ y_shared,
                const float *__restrict__ w, const int32_t *__restrict__ perm,
-               const float4 *res, int T, int k, int d4, float4 *out)
+               const float4 *res, int T, int k, int d4, float4 *out, int32_t *err)
 {
     griddep_launch_dependents();
     griddep_wait();   // y_pair / y_shared come from the previous kernel
@@ -46,6 +46,8 @@ combine_kernel(const Y *__restrict__ y_pair, const float4 *__restrict__ y_shared
         for (int u = 0; u < kG; u++) {
             const int j = j0 + u;
             q[u] = j < k ? perm[(size_t)t * k + j] : -1;
+            if (!MOE_IN_BOUNDS(q[u] < T * k, err))
+                q[u] = -1;
             wj[u] = j < k ? w[(size_t)t * k + j] : 0.f;
         }
         float4 y[kG];
@@ -114,23 +116,23 @@ int launch_rms_norm(const float *x, int T, int d, float eps, float *out, cudaStr
 }
 
 int launch_combine(const float *y_pair, const float *y_shared, const float *w, const int32_t *perm,
-                   const float *res, int T, int k, int d, float *out, cudaStream_t s)
+                   const float *res, int T, int k, int d, float *out, cudaStream_t s, int32_t *err)
 {
     const int d4 = d / 4;
     const long long n = (long long)T * d4;
     return launch_pdl(combine_kernel<float4>, (int)((n + 255) / 256), 256, 0, s,
                       reinterpret_cast<const float4 *>(y_pair), reinterpret_cast<const float4 *>(y_shared), w,
-                      perm, reinterpret_cast<const float4 *>(res), T, k, d4, reinterpret_cast<float4 *>(out));
+                      perm, reinterpret_cast<const float4 *>(res), T, k, d4, reinterpret_cast<float4 *>(out), err);
 }
 
 int launch_combine_bf16(const uint16_t *y_pair, const float *y_shared, const float *w, const int32_t *perm,
-                        const float *res, int T, int k, int d, float *out, cudaStream_t s)
+                        const float *res, int T, int k, int d, float *out, cudaStream_t s, int32_t *err)
 {
     const int d4 = d / 4;
     const long long n = (long long)T * d4;
     return launch_pdl(combine_kernel<uint2>, (int)((n + 255) / 256), 256, 0, s,
                       reinterpret_cast<const uint2 *>(y_pair), reinterpret_cast<const float4 *>(y_shared), w,
-                      perm, reinterpret_cast<const float4 *>(res), T, k, d4, reinterpret_cast<float4 *>(out));
+                      perm, reinterpret_cast<const float4 *>(res), T, k, d4, reinterpret_cast<float4 *>(out), err);
 }
 
 }  // namespace moe

@@ -112,6 +112,7 @@ struct Params {
     int32_t *err;
     int T, k, nchunks, tiles, out_rows;   // nchunks: k-chunks of the reduction; out_rows: d (down)
     int dynamic;                // 1: items after the first from the counter; 0: CTA c takes c, c + G, ...
+    int n_experts, n_view;      // routed experts of the routing; expert blocks of the weight view
 };
 
 // Packed nibbles -> fp16 subnormal pairs: lo takes the nibbles at bits 0-3 and
@@ -169,9 +170,19 @@ __device__ __forceinline__ void load_units(const Params &p, int units, Unit *tab
         } else {
             const int e = __ldcg(p.uniq + u - p.with_shared);
             t.expert = e;
-            t.pos0 = __ldcg(p.offsets + e);
-            t.m = __ldcg(p.offsets + e + 1) - t.pos0;
-            t.zq = p.slot_of ? __ldcg(p.slot_of + e) : e;
+            if (MOE_IN_BOUNDS(e >= 0 && e < p.n_experts, p.err)) {
+                t.pos0 = __ldcg(p.offsets + e);
+                t.m = __ldcg(p.offsets + e + 1) - t.pos0;
+                t.zq = p.slot_of ? __ldcg(p.slot_of + e) : e;
+                // a unit outside the pairs or the weight view gets no tokens (its items do nothing)
+                if (!MOE_IN_BOUNDS(t.pos0 >= 0 && t.m >= 0 && t.pos0 + t.m <= p.T * p.k && t.zq >= 0 &&
+                                       t.zq < p.n_view,
+                                   p.err))
+                    t.m = 0;
+            } else {
+                t.expert = 0;
+                t.pos0 = t.m = t.zq = 0;
+            }
         }
         tab[u] = t;
     }
@@ -194,8 +205,12 @@ __device__ __forceinline__ Item decode_item(const Params &p, const Unit *tab, in
 template <int MODE>
 __device__ __forceinline__ int act_row(const Params &p, const Item &it, int tt)
 {
-    if (MODE == kGateUp)
-        return it.expert < 0 ? tt : p.sorted_pair[it.pos0 + tt] / p.k;
+    if (MODE == kGateUp) {
+        if (it.expert < 0)
+            return tt;
+        const int sp = p.sorted_pair[it.pos0 + tt];
+        return MOE_IN_BOUNDS(sp >= 0 && sp < p.T * p.k, p.err) ? sp / p.k : 0;
+    }
     return it.expert < 0 ? p.T * p.k + tt : it.pos0 + tt;
 }
 
@@ -844,6 +859,8 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
     pg.nchunks = d / 256;
     pg.tiles = f / 32;
     pg.out_rows = f;
+    pg.n_experts = a.n_experts > 0 ? a.n_experts : E;
+    pg.n_view = E;
     rc = G == 64 ? launch_tok<kGateUp, 8, 64>(gu, pg, max_experts, a.T, s)
                  : launch_tok<kGateUp, 8, 32>(gu, pg, max_experts, a.T, s);
     if (rc != MOE_OK)

@@ -140,6 +140,7 @@ struct PParams {
     int with_shared;              // 1: unit 0 is the shared expert; 0: the units are the uniq list only
     int32_t *err;
     int T, k, K, mtiles, out_rows;
+    int n_experts, n_view;        // routed experts of the routing; expert blocks of the weight view
 };
 
 __device__ __forceinline__ int frag_pos8(int o) { return 2 * (o & 3) + (o >> 2); }
@@ -177,9 +178,19 @@ __device__ void build_units(const PParams &p, int units, PUnit *tab)
             } else {
                 const int e = p.uniq[u - p.with_shared];
                 t.expert = e;
-                t.row0 = p.offsets[e];
-                t.m = p.offsets[e + 1] - t.row0;
-                t.zq = p.slot_of ? p.slot_of[e] : e;
+                if (MOE_IN_BOUNDS(e >= 0 && e < p.n_experts, p.err)) {
+                    t.row0 = p.offsets[e];
+                    t.m = p.offsets[e + 1] - t.row0;
+                    t.zq = p.slot_of ? p.slot_of[e] : e;
+                    // a unit outside the pairs or the weight view gets no tokens
+                    if (!MOE_IN_BOUNDS(t.row0 >= 0 && t.m >= 0 && t.row0 + t.m <= p.T * p.k && t.zq >= 0 &&
+                                           t.zq < p.n_view,
+                                       p.err))
+                        t.m = 0;
+                } else {
+                    t.expert = 0;
+                    t.row0 = t.m = t.zq = 0;
+                }
             }
             tiles[j] = (t.m + N - 1) / N;
             tab[u] = t;
@@ -655,13 +666,18 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
 // when pos[q] is a valid position whose sorted_pair entry is q itself.
 __global__ void __launch_bounds__(256)
 pair_pos_kernel(const int32_t *__restrict__ sorted_pair, const int32_t *__restrict__ offsets, int E,
-                int32_t *__restrict__ pos)
+                int32_t *__restrict__ pos, int n_pairs, int32_t *err)
 {
     griddep_launch_dependents();
     griddep_wait();
     const int p = blockIdx.x * 256 + threadIdx.x;
-    if (p < offsets[E])
-        pos[sorted_pair[p]] = p;
+    if (p < offsets[E]) {
+        const int q = sorted_pair[p];
+        if (MOE_IN_BOUNDS(q >= 0 && q < n_pairs && p < n_pairs, err))
+            pos[q] = p;
+    }
+    (void)n_pairs;
+    (void)err;
 }
 
 __global__ void __launch_bounds__(256)
@@ -842,7 +858,8 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
 
     // fp16 token rows: each token converted once and written to its pair rows and shared row
     const int E_off = a.n_experts > 0 ? a.n_experts : E;   // offsets[E_off] = the placed pairs
-    rc = launch_pdl(pair_pos_kernel, (T * k + 255) / 256, 256, 0, s, a.sorted_pair, a.offsets, E_off, ps.pos);
+    rc = launch_pdl(pair_pos_kernel, (T * k + 255) / 256, 256, 0, s, a.sorted_pair, a.offsets, E_off, ps.pos, T * k,
+                    a.err);
     if (rc == MOE_OK)
         rc = launch_pdl(token_rows_kernel, T, 256, 0, s, a.x, (const int32_t *)ps.pos, a.sorted_pair, a.offsets,
                         E_off, T, k, d, x_sorted, row_scale);
@@ -890,6 +907,8 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pg.K = d;
     pg.mtiles = f / PCfg<kPGateUp, 256, 32>::kRowsPerMat;
     pg.out_rows = f;
+    pg.n_experts = E_off;
+    pg.n_view = E;
     const int max_units = (E < T * k ? E : T * k) + 1;
     // d is a multiple of 256
     rc = G == 64 ? launch_prefill_one<kPGateUp, 256, 64>(gm, pg, max_units, s)

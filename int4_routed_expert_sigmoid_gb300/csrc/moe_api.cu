@@ -128,7 +128,7 @@ int moe_device_error(int32_t err)
         return MOE_OK;
     if (err & MOE_DEVERR_TIMEOUT)
         return MOE_ERR_CUDA;
-    if (err & MOE_DEVERR_BAD_EXPERT)
+    if (err & (MOE_DEVERR_BAD_EXPERT | MOE_DEVERR_BOUNDS))
         return MOE_ERR_INVALID_ARG;
     return MOE_ERR_UNSUPPORTED;
 }
@@ -141,6 +141,7 @@ int moe_route_topp(const float *x, const float *w_gate, const float *bias, int T
                    int normalize, float route_scale, float top_p, int32_t *topk_idx, float *topk_w,
                    float *logits, void *stream)
 {
+    NvtxRange nvtx("moe.route");
     if (!ok_ptr(x) || !ok_ptr(w_gate) || !ok_opt(bias) || !ok_ptr(topk_idx) || !ok_ptr(topk_w) ||
         !ok_ptr(logits) || !ok_route_shape(T, d, E, k) || !ok_top_p(top_p))
         return MOE_ERR_INVALID_ARG;
@@ -163,6 +164,7 @@ int moe_union(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, int
               int32_t *perm, int32_t *sorted_pair, int32_t *uniq, int32_t *n_uniq, uint64_t *hits,
               int32_t *err, void *stream)
 {
+    NvtxRange nvtx("moe.union");
     if (!ok_ptr(topk_idx) || !ok_ptr(counts) || !ok_ptr(offsets) || !ok_ptr(perm) ||
         !ok_ptr(sorted_pair) || !ok_ptr(uniq) || !ok_ptr(n_uniq) || !ok_opt(hits) || !ok_ptr(err))
         return MOE_ERR_INVALID_ARG;
@@ -174,6 +176,7 @@ int moe_union(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, int
 
 int moe_hits(const int32_t *counts, int E, uint64_t *hits, void *stream)
 {
+    NvtxRange nvtx("moe.hits");
     if (!ok_ptr(counts) || !ok_ptr(hits) || E < 1 || E > (1 << 20))
         return MOE_ERR_INVALID_ARG;
     return launch_hits(counts, E, hits, as_stream(stream));
@@ -191,6 +194,7 @@ int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *
                         int T, int k, int mode, float *y_pair, float *y_shared, void *workspace,
                         size_t ws_bytes, int32_t *err, void *stream)
 {
+    NvtxRange nvtx("moe.expert_ffn");
     int rc = check_layer(w);
     if (rc != MOE_OK)
         return rc;
@@ -249,6 +253,7 @@ int moe_combine(const float *y_pair, const float *y_shared, const float *topk_w,
                 const int32_t *perm, const float *residual, int T, int k, int d, float *out,
                 void *stream)
 {
+    NvtxRange nvtx("moe.combine");
     if (!ok_ptr(y_pair) || !ok_ptr(y_shared) || !ok_ptr(topk_w) || !ok_ptr(perm) ||
         !ok_opt(residual) || !ok_ptr(out) || T < 1 || k < 1 || k > 32 || d < 4 || d % 4 != 0)
         return MOE_ERR_INVALID_ARG;
@@ -257,6 +262,7 @@ int moe_combine(const float *y_pair, const float *y_shared, const float *topk_w,
 
 int moe_rms_norm(const float *x, int T, int d, float eps, float *out, void *stream)
 {
+    NvtxRange nvtx("moe.rms_norm");
     if (!ok_ptr(x) || !ok_ptr(out) || T < 1 || T > (1 << 24) || d < 4 || d % 4 != 0 || d > (1 << 20) ||
         !(eps >= 0.0f) || !(eps < 1e30f))
         return MOE_ERR_INVALID_ARG;
@@ -285,6 +291,7 @@ int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bia
                            float *topk_w, uint64_t *hits, void *workspace, size_t ws_bytes, int32_t *err,
                            void *stream)
 {
+    NvtxRange nvtx("moe.layer_forward");
     int rc = check_layer(w);
     if (rc != MOE_OK)
         return rc;
@@ -334,7 +341,7 @@ int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bia
         if (rc != MOE_OK)
             return rc;
         return launch_combine_bf16(reinterpret_cast<const uint16_t *>(sc.y_pair), sc.y_shared, wt, sc.perm,
-                                   residual, T, k, d, out, s);
+                                   residual, T, k, d, out, s, err);
     }
     FfnScratch fs{};
     ffn_scratch_layout(T, k, d, f, sc.ffn, &fs);
@@ -378,7 +385,7 @@ int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bia
     rc = launch_ffn_decode(a, s);
     if (rc != MOE_OK)
         return rc;
-    return launch_combine(sc.y_pair, sc.y_shared, wt, sc.perm, residual, T, k, d, out, s);
+    return launch_combine(sc.y_pair, sc.y_shared, wt, sc.perm, residual, T, k, d, out, s, err);
 }
 
 }  // extern "C"

@@ -9,7 +9,42 @@
 
 #include "../../include/moe.h"
 
+#ifndef MOE_NO_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 namespace moe {
+
+// Bounds checks of a MOE_DEBUG_BOUNDS build: MOE_IN_BOUNDS(ok, err) is true when ok, else sets
+// MOE_DEVERR_BOUNDS in the error word (when there is one) and is false, so the caller skips the
+// access; in a normal build it is the constant true and costs nothing.
+#ifdef MOE_DEBUG_BOUNDS
+#ifdef __CUDACC__
+__device__ __forceinline__ bool in_bounds_check(bool ok, int32_t *err)
+{
+    if (!ok && err != nullptr)
+        atomicOr(err, MOE_DEVERR_BOUNDS);
+    return ok;
+}
+#endif
+#define MOE_IN_BOUNDS(ok, err) ::moe::in_bounds_check((ok), (err))
+#else
+#define MOE_IN_BOUNDS(ok, err) true
+#endif
+
+// Host-side NVTX range over one entry point's launches (a profiler's timeline shows where each
+// stage's kernels were enqueued); compiled out with MOE_NO_NVTX.  Costs a few nanoseconds when
+// no tool is attached.
+struct NvtxRange {
+#ifndef MOE_NO_NVTX
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+#else
+    explicit NvtxRange(const char *) {}
+#endif
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 // ---------------------------------------------------------------------------
 // Activation fragment layout ("frag"): the B operand of the decode FFN's
@@ -112,6 +147,7 @@ struct DecodeFfnArgs {
     const int32_t *slot_of = nullptr;   // [E] block of w holding expert e (expert tier), or null: block e
     int with_shared = 1;                // 0: only the uniq list's experts (a second launch of the tier)
     int32_t *err;
+    int n_experts = 0;                  // routed experts of the routing (offsets has n_experts + 1); 0: w->E
 };
 constexpr int kDecodeCounters = 2;   // items claimed by the gate/up and the down kernel
 int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s);
@@ -135,10 +171,10 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s);
 
 // combine.cu
 int launch_combine(const float *y_pair, const float *y_shared, const float *w, const int32_t *perm,
-                   const float *res, int T, int k, int d, float *out, cudaStream_t s);
+                   const float *res, int T, int k, int d, float *out, cudaStream_t s, int32_t *err = nullptr);
 // the same with the routed outputs in bf16
 int launch_combine_bf16(const uint16_t *y_pair, const float *y_shared, const float *w, const int32_t *perm,
-                        const float *res, int T, int k, int d, float *out, cudaStream_t s);
+                        const float *res, int T, int k, int d, float *out, cudaStream_t s, int32_t *err = nullptr);
 int launch_rms_norm(const float *x, int T, int d, float eps, float *out, cudaStream_t s);
 
 // tmap.cu

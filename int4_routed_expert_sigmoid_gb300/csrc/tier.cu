@@ -277,6 +277,7 @@ extern "C" {
 
 int moe_tier_pin(moe_tier t, const int32_t *experts, int n, void *copy_stream)
 {
+    NvtxRange nvtx("moe.tier_pin");
     if (t == nullptr || n < 0 || (n > 0 && experts == nullptr))
         return MOE_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(t->mu);
@@ -285,6 +286,7 @@ int moe_tier_pin(moe_tier t, const int32_t *experts, int n, void *copy_stream)
 
 int moe_tier_prefetch(moe_tier t, const int32_t *experts, int n, void *copy_stream)
 {
+    NvtxRange nvtx("moe.tier_prefetch");
     if (t == nullptr || n < 0 || (n > 0 && experts == nullptr))
         return MOE_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(t->mu);
@@ -338,6 +340,7 @@ int moe_layer_forward_tier(const float *x, const float *w_gate, const float *bia
                            float *topk_w, uint64_t *hits, void *workspace, size_t ws_bytes, int32_t *err,
                            void *stream, void *copy_stream)
 {
+    NvtxRange nvtx("moe.layer_forward_tier");
     if (tier == nullptr)
         return MOE_ERR_INVALID_ARG;
     moe_tier_s &t = *tier;
@@ -406,7 +409,7 @@ int moe_layer_forward_tier(const float *x, const float *w_gate, const float *bia
             if (rc != MOE_OK)
                 return rc;
             return launch_combine_bf16(reinterpret_cast<const uint16_t *>(sc.y_pair), sc.y_shared, wt, sc.perm,
-                                       residual, T, k, d, out, s);
+                                       residual, T, k, d, out, s, err);
         }
         FfnScratch fs{};
         ffn_scratch_layout(T, k, d, f, sc.ffn, &fs);
@@ -426,12 +429,13 @@ int moe_layer_forward_tier(const float *x, const float *w_gate, const float *bia
         a.y_shared = sc.y_shared;
         a.work = fs.work;
         a.slot_of = map;
+        a.n_experts = E;
         a.err = err;
         if (rc == MOE_OK)
             rc = launch_ffn_decode(a, s);
         if (rc != MOE_OK)
             return rc;
-        return launch_combine(sc.y_pair, sc.y_shared, wt, sc.perm, residual, T, k, d, out, s);
+        return launch_combine(sc.y_pair, sc.y_shared, wt, sc.perm, residual, T, k, d, out, s, err);
     }
     if (cudaMemcpyAsync(t.stage_in, sc.n_uniq, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaMemcpyAsync(t.stage_in + 1, sc.uniq, (size_t)E * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
@@ -526,6 +530,7 @@ int moe_layer_forward_tier(const float *x, const float *w_gate, const float *bia
         a.y_shared = sc.y_shared;
         a.work = fs.work;
         a.slot_of = map;
+        a.n_experts = E;
         a.with_shared = 1;
         a.err = err;
         if (rc == MOE_OK)
@@ -544,8 +549,8 @@ int moe_layer_forward_tier(const float *x, const float *w_gate, const float *bia
         return rc;
     if (mode == MOE_MODE_PREFILL)
         return launch_combine_bf16(reinterpret_cast<const uint16_t *>(sc.y_pair), sc.y_shared, wt, sc.perm, residual,
-                                   T, k, d, out, s);
-    return launch_combine(sc.y_pair, sc.y_shared, wt, sc.perm, residual, T, k, d, out, s);
+                                   T, k, d, out, s, err);
+    return launch_combine(sc.y_pair, sc.y_shared, wt, sc.perm, residual, T, k, d, out, s, err);
 }
 
 }  // extern "C"

@@ -1,0 +1,40 @@
+"""Child process of tests/test_gpu_debug_bounds.py: runs the layer through one
+libmoe build (argv[1]) on the small parity shapes and saves the outputs and
+error words to argv[2] (npz).  A separate process, so that the normal and the
+bounds-checked library are never loaded together."""
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+from int4_routed_expert_sigmoid_gb300 import _binding  # noqa: E402
+
+_binding.LIB_PATH = os.path.abspath(sys.argv[1])
+import torch  # noqa: E402
+
+import int4_routed_expert_sigmoid_gb300 as moe  # noqa: E402
+import workloads  # noqa: E402
+from moe_testlib import device_layer  # noqa: E402
+
+Shape = workloads.Shape
+SHAPES = [Shape("dbg_t1", E=16, k=4, d=1024, f=256, T=1, bias="normal"),
+          Shape("dbg_t5", E=64, k=8, d=512, f=512, T=5, bias="zipf"),
+          Shape("dbg_t37", E=16, k=4, d=1024, f=384, T=37, bias="normal")]
+out = {}
+for sh in SHAPES:
+    L = workloads.layer_inputs(sh, seed=5, threads=4)
+    dev = device_layer(L)
+    x = torch.from_numpy(workloads.activations(sh.T, sh.d, seed=6)).cuda()
+    res = torch.from_numpy(workloads.activations(sh.T, sh.d, seed=7)).cuda()
+    for mode_name in ("MOE_MODE_DECODE", "MOE_MODE_PREFILL"):
+        hits = torch.zeros(sh.E, dtype=torch.int64, device="cuda")
+        y, err = moe.moe_layer_forward(x, dev["wg"], dev["bias"], dev["layer"], sh.k, mode=getattr(moe, mode_name),
+                                       residual=res, hits=hits)
+        torch.cuda.synchronize()
+        out[f"{sh.name}_{mode_name}_y"] = y.cpu().numpy()
+        out[f"{sh.name}_{mode_name}_err"] = err.cpu().numpy()
+        out[f"{sh.name}_{mode_name}_hits"] = hits.cpu().numpy()
+np.savez(sys.argv[2], **out)

@@ -31,6 +31,7 @@ def test_status_strings_and_device_error_decoding(m):
     assert m.device_error(0) == m.MOE_OK
     assert m.device_error(m.MOE_DEVERR_BAD_EXPERT) == m.MOE_ERR_INVALID_ARG
     assert m.device_error(m.MOE_DEVERR_TIMEOUT) == m.MOE_ERR_CUDA
+    assert m.device_error(m.MOE_DEVERR_BOUNDS) == m.MOE_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("d,f", [(256, 128), (6144, 2048), (1024, 384)])
@@ -79,6 +80,16 @@ def test_binding_error_bits_match_the_header(m):
     import re
     hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe.h")).read()
     bits = dict(re.findall(r"#define (MOE_DEVERR_\w+) (0x[0-9a-fA-F]+)", hdr))
-    assert len(bits) == 3
+    assert len(bits) == 4
     for name, val in bits.items():
         assert getattr(m, name) == int(val, 16), name
+
+
+def test_debug_bounds_build_exports_every_header_symbol(m):
+    """The bounds-checked build (MOE_DEBUG_BOUNDS) compiles and exports the same symbols."""
+    from int4_routed_expert_sigmoid_gb300 import build
+    path = build.build(debug_bounds=True)
+    assert path != build.LIB
+    L = ctypes.CDLL(path)
+    missing = [n for n in m.header_functions() if not hasattr(L, n)]
+    assert not missing, missing
