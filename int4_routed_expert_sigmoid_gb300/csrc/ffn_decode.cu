@@ -304,6 +304,35 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
                 sc[(4 * v + 2) % kSpw] = vb.z; sc[(4 * v + 3) % kSpw] = vb.w;
             }
         }
+        // one-token passes: the stage's group corrections (and, down, the h factors) of each
+        // n-tile's tokens are read with 16-byte loads before the group loop, not one per group
+        constexpr bool kHoist = TOK == 1 && kGpw % 2 == 0;
+        float2 ccv[kHoist ? NT : 1][kHoist ? kGpw : 1];
+        float hfv[kHoist ? NT : 1][kHoist ? kGpw : 1];
+        if (kHoist) {
+#pragma unroll
+            for (int n = 0; n < NT; n++) {
+#pragma unroll
+                for (int v = 0; v < kGpw / 2; v++) {
+                    const float4 c4 = *reinterpret_cast<const float4 *>(sb + coff[n] + 16 * v);
+                    ccv[n][2 * v] = make_float2(c4.x, c4.y);
+                    ccv[n][2 * v + 1] = make_float2(c4.z, c4.w);
+                }
+                if (MODE == kDown) {
+#pragma unroll
+                    for (int v = 0; v < kGpw; v += 4) {
+                        if (kGpw - v >= 4) {
+                            const float4 h4 = *reinterpret_cast<const float4 *>(sb + foff[n] + 4 * v);
+                            hfv[n][v] = h4.x; hfv[n][(v + 1) % kGpw] = h4.y;
+                            hfv[n][(v + 2) % kGpw] = h4.z; hfv[n][(v + 3) % kGpw] = h4.w;
+                        } else {
+                            for (int u = v; u < kGpw; u++)
+                                hfv[n][u] = *reinterpret_cast<const float *>(sb + foff[n] + 4 * u);
+                        }
+                    }
+                }
+            }
+        }
 #pragma unroll
         for (int gi = 0; gi < kGpw; gi++) {
             const uint32_t wa = *reinterpret_cast<const uint32_t *>(sb + qoff[gi]);
@@ -314,14 +343,14 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
 #pragma unroll
             for (int n = 0; n < NT; n++) {
                 const uint4 bv = *reinterpret_cast<const uint4 *>(sb + boff[n] + gi * 64);
-                const float2 cc = *reinterpret_cast<const float2 *>(sb + coff[n] + gi * 8);
+                const float2 cc = kHoist ? ccv[n][gi] : *reinterpret_cast<const float2 *>(sb + coff[n] + gi * 8);
                 const float cin[4] = {cc.x, cc.y, cc.x, cc.y};
                 float d[4];
                 mma_f16_16816(d, a0, bv.x, bv.y, cin);
                 mma_f16_16816(d, a1, bv.z, bv.w, d);
                 float fa = sa[gi * 32 / GS], fb = sc[gi * 32 / GS];
                 if (MODE == kDown) {
-                    const float hf = *reinterpret_cast<const float *>(sb + foff[n] + gi * 4);
+                    const float hf = kHoist ? hfv[n][gi] : *reinterpret_cast<const float *>(sb + foff[n] + gi * 4);
                     fa *= hf;
                     fb *= hf;
                 }
@@ -759,9 +788,13 @@ int launch_tok(const Maps &maps, const Params &prm, int max_units, int T, cudaSt
     // no spills); above, 16 for gate/up, so that an expert taken by many tokens is streamed fewer
     // times, and still 8 for down, whose items are a third as long (a 64-token Zipf batch: 4.2 %
     // faster than 16 for both, 3 % faster than 8 for both)
-    if (T <= 32 || MODE == kDown)
+    if constexpr (MODE == kDown) {
         return launch_one<MODE, 8, 1, GPC, GS>(maps, prm, mi, max_units, s);
-    return launch_one<MODE, 16, 1, GPC, GS>(maps, prm, mi, max_units, s);
+    } else {
+        if (T <= 32)
+            return launch_one<MODE, 8, 1, GPC, GS>(maps, prm, mi, max_units, s);
+        return launch_one<MODE, 16, 1, GPC, GS>(maps, prm, mi, max_units, s);
+    }
 }
 
 }  // namespace
