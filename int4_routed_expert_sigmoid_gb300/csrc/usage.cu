@@ -3,9 +3,9 @@
 // set an expert tier pins in device memory).
 //
 // Source: "Public Colibri Observation and Revision Ledger", "Exact Architecture
-// and Data-Flow Reconstruction" (Learn updates per-expert hit counters; a
-// global learning cache keeps the most used experts, persisted in a usage
-// file) and "Failure, Corruption, and Restart Behavior" (on restart the usage
+// and Data-Flow Reconstruction" (the Learn stage counts, per expert, how
+// often the router chose it; the experts chosen most are kept in a cache
+// whose contents are saved to a usage file between runs) and "Failure, Corruption, and Restart Behavior" (on restart the usage
 // file decides which experts are pinned; the engine does not check that the
 // file belongs to the model it runs, so a changed model can be given a wrong
 // hot set).  Here the file carries a model id, its shape and a checksum, and a

@@ -19,9 +19,9 @@
  * Sources (page title, section):
  *  [arch]  "Public Colibri Observation and Revision Ledger", "Exact Architecture
  *         and Data-Flow Reconstruction": sigmoid router with n_group=1 over the
- *         experts of a layer; each routed expert is a three-matrix MLP stored
- *         contiguously at int4; an always-on shared expert; fp32 gate
- *         parameters.
+ *         experts of a layer; a routed expert's three weight matrices sit
+ *         next to each other in one int4 block; a shared expert that every
+ *         token uses; router parameters in fp32.
  *  [stages] same page and section: the five per-layer stages Route, Union,
  *         Place, Overlap, Learn; routing and precision are unchanged by them.
  *  [hits]  same section: per-expert hit counters updated after each token.
