@@ -346,8 +346,9 @@ MOE_API int moe_usage_top(const uint64_t *hits, int E, int n, int32_t *experts);
  * Source: "Public Colibri Observation and Revision Ledger", "Exact Architecture
  * and Data-Flow Reconstruction" (Place loads the experts a batch needs into
  * fast memory; Overlap computes on the experts already there while the loads
- * run); colibri README, "How it works" (placement decides speed only: the
- * router's choices and the weights' precision are the same).
+ * run); colibri README, "How it works" (where an expert is placed changes
+ * only the speed: which experts are chosen and how precisely they are
+ * computed do not depend on it).
  *
  * A tier belongs to one layer and one device (the current device at
  * creation).  It keeps host-side tables, two events and a small page-locked

@@ -4,9 +4,10 @@
 // Source: "Public Colibri Observation and Revision Ledger", "Exact Architecture
 // and Data-Flow Reconstruction" (per layer: Route, Union, Place -- bring the
 // missing experts to fast memory --, Overlap -- compute on the experts already
-// there while the transfers run --, Learn); colibri README, "How it works" (one
-// memory hierarchy instead of one memory requirement; placement decides speed,
-// never the result).
+// there while the transfers run --, Learn); colibri README, "How it works"
+// (the weights are spread over the levels of the memory hierarchy instead of
+// all having to fit in one; where an expert sits changes how fast a token
+// goes, never what it computes).
 //
 // On a GB300 the hierarchy is HBM3e and the Grace CPU's memory behind
 // NVLink-C2C.  A tier holds, for one layer, n_slots expert blocks in device
