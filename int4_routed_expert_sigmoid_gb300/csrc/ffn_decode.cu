@@ -243,19 +243,27 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
     constexpr int kGpw = C::kGpw;
     const int g = cs.g, t4 = cs.t4, lane = cs.lane, warp = cs.warp;
     // stage offsets of this lane's B chunk (token g/2 of each n-tile, plane g&1) and of the
-    // accumulator inputs / factors of the token whose D columns it holds (token t4); tokens past
-    // ntok read token 0's data (finite, discarded)
-    uint32_t boff[NT], coff[NT], foff[NT];
+    // accumulator inputs / factors of the token whose D columns it holds (token t4).  Columns of
+    // tokens past ntok are computed and discarded; when the stage has room for all 4 * NT token
+    // blocks they read whatever the stage holds there, so the offsets are a base plus a fixed
+    // stride per n-tile (no per-tile registers); a stage with fewer token blocks (TOK < 4 NT) has
+    // those columns read token 0 instead.
+    constexpr bool kClamp = TOK < 4 * NT;
+    constexpr uint32_t kNStride = 4 * C::kTokBytes;
+    uint32_t boff[kClamp ? NT : 1], coff[kClamp ? NT : 1], foff[kClamp ? NT : 1];
 #pragma unroll
-    for (int n = 0; n < NT; n++) {
+    for (int n = 0; n < (kClamp ? NT : 1); n++) {
         int jb = n * 4 + (g >> 1);
-        jb = jb < ntok ? jb : 0;
+        jb = (!kClamp || jb < ntok) ? jb : 0;
         boff[n] = C::kBOff + jb * C::kTokBytes + kb + plane_off;
         int jd = n * 4 + t4;
-        jd = jd < ntok ? jd : 0;
+        jd = (!kClamp || jd < ntok) ? jd : 0;
         coff[n] = C::kBOff + jd * C::kTokBytes + kbc;
         foff[n] = C::kBOff + jd * C::kTokBytes + kbf;
     }
+    auto bo = [&](int n) { return kClamp ? boff[n] : boff[0] + n * kNStride; };
+    auto co = [&](int n) { return kClamp ? coff[n] : coff[0] + n * kNStride; };
+    auto fo = [&](int n) { return kClamp ? foff[n] : foff[0] + n * kNStride; };
     float acc[NT][2];
 #pragma unroll
     for (int n = 0; n < NT; n++)
@@ -280,7 +288,7 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
         if (MODE == kGateUp && c == 0) {
 #pragma unroll
             for (int n = 0; n < NT; n++)
-                xfac[n] = *reinterpret_cast<const float *>(sb + foff[n]);
+                xfac[n] = *reinterpret_cast<const float *>(sb + fo(n));
         }
         // group scales of rows ra and ra + 8 for this warp's groups (one per GS elements)
         constexpr int kSpw = C::kSpw;
@@ -314,7 +322,7 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
             for (int n = 0; n < NT; n++) {
 #pragma unroll
                 for (int v = 0; v < kGpw / 2; v++) {
-                    const float4 c4 = *reinterpret_cast<const float4 *>(sb + coff[n] + 16 * v);
+                    const float4 c4 = *reinterpret_cast<const float4 *>(sb + co(n) + 16 * v);
                     ccv[n][2 * v] = make_float2(c4.x, c4.y);
                     ccv[n][2 * v + 1] = make_float2(c4.z, c4.w);
                 }
@@ -322,12 +330,12 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
 #pragma unroll
                     for (int v = 0; v < kGpw; v += 4) {
                         if (kGpw - v >= 4) {
-                            const float4 h4 = *reinterpret_cast<const float4 *>(sb + foff[n] + 4 * v);
+                            const float4 h4 = *reinterpret_cast<const float4 *>(sb + fo(n) + 4 * v);
                             hfv[n][v] = h4.x; hfv[n][(v + 1) % kGpw] = h4.y;
                             hfv[n][(v + 2) % kGpw] = h4.z; hfv[n][(v + 3) % kGpw] = h4.w;
                         } else {
                             for (int u = v; u < kGpw; u++)
-                                hfv[n][u] = *reinterpret_cast<const float *>(sb + foff[n] + 4 * u);
+                                hfv[n][u] = *reinterpret_cast<const float *>(sb + fo(n) + 4 * u);
                         }
                     }
                 }
@@ -342,15 +350,15 @@ __device__ __forceinline__ void run_pass(const Params &p, const Item &it, int t0
             const uint32_t a1[4] = {nib_lo(wa8, nk), nib_lo(wb8, nk), nib_hi(wa8, nk), nib_hi(wb8, nk)};
 #pragma unroll
             for (int n = 0; n < NT; n++) {
-                const uint4 bv = *reinterpret_cast<const uint4 *>(sb + boff[n] + gi * 64);
-                const float2 cc = kHoist ? ccv[n][gi] : *reinterpret_cast<const float2 *>(sb + coff[n] + gi * 8);
+                const uint4 bv = *reinterpret_cast<const uint4 *>(sb + bo(n) + gi * 64);
+                const float2 cc = kHoist ? ccv[n][gi] : *reinterpret_cast<const float2 *>(sb + co(n) + gi * 8);
                 const float cin[4] = {cc.x, cc.y, cc.x, cc.y};
                 float d[4];
                 mma_f16_16816(d, a0, bv.x, bv.y, cin);
                 mma_f16_16816(d, a1, bv.z, bv.w, d);
                 float fa = sa[gi * 32 / GS], fb = sc[gi * 32 / GS];
                 if (MODE == kDown) {
-                    const float hf = kHoist ? hfv[n][gi] : *reinterpret_cast<const float *>(sb + foff[n] + gi * 4);
+                    const float hf = kHoist ? hfv[n][gi] : *reinterpret_cast<const float *>(sb + fo(n) + gi * 4);
                     fa *= hf;
                     fb *= hf;
                 }
