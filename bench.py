@@ -370,27 +370,25 @@ def measure_layer(copies, sh, prefill, steps, warmup, graph_steps, e2e_steps, ra
     torch.cuda.synchronize()
     ffn_call_ms = f0.elapsed_time(f1) / (3 * S)
 
-    # ---- end to end through the public API with host buffers (not graph-captured)
+    # ---- end to end through the C-ABI call with host buffers (moe_layer_forward_host: the step's
+    # token rows copied in from page-locked memory, the layer, the result copied back; not
+    # graph-captured, one call per step from the host)
     e2e_steps = max(1, min(e2e_steps, steps))
     x_host = torch.from_numpy(workloads.activations(e2e_steps * T, d, seed=5000 + rank)).view(e2e_steps, T, d)
     x_host = x_host.pin_memory()
     out_host = torch.empty((e2e_steps, T, d), dtype=torch.float32).pin_memory()
-    x_dev = torch.empty((T, d), dtype=torch.float32, device=dev)
-    out_dev = torch.empty((T, d), dtype=torch.float32, device=dev)
-    lws = moe.workspace(moe.layer_workspace_bytes(T, k, E, d, f, mode), dev)
+    hws = moe.workspace(moe.layer_host_workspace_bytes(T, k, E, d, f, mode), dev)
     for i in range(min(50, e2e_steps)):   # warm-up of the host path
         r = i % R
-        moe.moe_layer_forward(x_dev, wgs[r], biases[r], layers[r], k, mode=mode, out=out_dev,
-                              ws=lws, err=err)
+        moe.moe_layer_forward_host(x_host[i], wgs[r], biases[r], layers[r], k, mode=mode, out_host=out_host[i],
+                                   ws=hws, err=err)
     torch.cuda.synchronize()
     barrier(world)
     w0 = time.perf_counter()
     for i in range(e2e_steps):
         r = i % R
-        x_dev.copy_(x_host[i], non_blocking=True)
-        moe.moe_layer_forward(x_dev, wgs[r], biases[r], layers[r], k, mode=mode, out=out_dev,
-                              hits=hits[r], ws=lws, err=err)
-        out_host[i].copy_(out_dev, non_blocking=True)
+        moe.moe_layer_forward_host(x_host[i], wgs[r], biases[r], layers[r], k, mode=mode, out_host=out_host[i],
+                                   hits=hits[r], ws=hws, err=err)
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - w0
     barrier(world)
@@ -440,7 +438,8 @@ def measure_layer(copies, sh, prefill, steps, warmup, graph_steps, e2e_steps, ra
         "nibble_gbs": round(byts["nibbles"] / (ms_per_step * 1e-3) / 1e9, 1),
         "n_uniq": n_uniq,
         "e2e": {"value": round(T * e2e_steps * world / e2e_max, 2), "unit": UNIT,
-                "h2d_bytes_per_step": T * d * 4, "d2h_bytes_per_step": T * d * 4, "steps": e2e_steps},
+                "h2d_bytes_per_step": T * d * 4, "d2h_bytes_per_step": T * d * 4, "steps": e2e_steps,
+                "call": "moe_layer_forward_host (page-locked host rows in and out, one call per step)"},
         "gpu_launches": launches_per_step * steps,
         "clocks": clocks,
         "device_error": dev_err,

@@ -316,6 +316,27 @@ MOE_API int moe_layer_forward_topp(const float *x, const float *w_gate, const fl
 
 MOE_API size_t moe_layer_workspace_bytes(int T, int k, int E, int d, int f, int mode);
 
+/*
+ * The layer with its token rows and its result in HOST memory: x_host [T][d]
+ * is copied to the device, moe_layer_forward_topp runs on the copy, and its
+ * out [T][d] is copied back to out_host -- all enqueued on `stream`, one
+ * cudaMemcpyAsync each way.  With page-locked host buffers the call returns
+ * before the copies finish: the caller synchronises the stream before reading
+ * out_host or rewriting x_host (pageable buffers make the copies synchronous).
+ * The device copies of the rows sit in the workspace after the layer's
+ * scratch: moe_layer_host_workspace_bytes(T, k, E, d, f, mode) bytes.
+ * residual, topk_idx, topk_w, hits and err are device pointers as in
+ * moe_layer_forward (residual may be NULL).
+ * Errors: as moe_layer_forward; MOE_ERR_INVALID_ARG for a NULL host pointer;
+ * MOE_ERR_CUDA when a copy cannot be enqueued.
+ */
+MOE_API int moe_layer_forward_host(const float *x_host, const float *w_gate, const float *bias,
+                                   const moe_layer_int4 *w, const float *residual, int T, int k,
+                                   int normalize, float route_scale, float top_p, int mode,
+                                   float *out_host, int32_t *topk_idx, float *topk_w, uint64_t *hits,
+                                   void *workspace, size_t ws_bytes, int32_t *err, void *stream);
+MOE_API size_t moe_layer_host_workspace_bytes(int T, int k, int E, int d, int f, int mode);
+
 /* --------------------------------------------- usage file (Learn, kept) ---- */
 /*
  * The per-expert hit counters of `layers` layers (hits [layers][E], host)

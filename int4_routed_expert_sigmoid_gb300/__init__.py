@@ -12,5 +12,5 @@ from ._binding import (  # noqa: F401
     device_error, expert_q_bytes, expert_s_count, ffn_workspace_bytes, header_functions, layer_workspace_bytes,
     lib, moe_combine, moe_expert_ffn_int4, moe_expert_ffn_int4_noalloc, moe_hits, moe_layer_forward, moe_rms_norm,
     moe_route, moe_union, status_str, workspace, ExpertTier, tier_workspace_bytes, moe_layer_forward_tier,
-    MOE_ERR_STALE, usage_save, usage_load, usage_top,
+    MOE_ERR_STALE, usage_save, usage_load, usage_top, moe_layer_forward_host, layer_host_workspace_bytes,
 )

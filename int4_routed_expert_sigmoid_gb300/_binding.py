@@ -60,6 +60,9 @@ _SIGNATURES = {
     "moe_layer_forward_topp": ([_P, _P, _P, ctypes.POINTER(moe_layer_int4), _P, _I, _I, _I, _F, _F, _I, _P,
                                 _P, _P, _P, _P, _SZ, _P, _P], _I),
     "moe_layer_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
+    "moe_layer_forward_host": ([_P, _P, _P, ctypes.POINTER(moe_layer_int4), _P, _I, _I, _I, _F, _F, _I, _P,
+                                _P, _P, _P, _P, _SZ, _P, _P], _I),
+    "moe_layer_host_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
     "moe_usage_save": ([ctypes.c_char_p, _P, _I, _I, ctypes.c_uint64], _I),
     "moe_usage_load": ([ctypes.c_char_p, _P, _I, _I, ctypes.c_uint64], _I),
     "moe_usage_top": ([_P, _I, _I, _P], _I),
@@ -310,6 +313,36 @@ def moe_layer_forward(x, w_gate, bias, layer: LayerWeights, k: int, normalize: i
                                             _p(topk_idx), _p(topk_w), _p(hits), wp, wn, _p(err),
                                             _stream(stream)), "moe_layer_forward_topp")
     return out, err
+
+
+def layer_host_workspace_bytes(T: int, k: int, E: int, d: int, f: int, mode: int = MOE_MODE_AUTO) -> int:
+    return int(lib().moe_layer_host_workspace_bytes(T, k, E, d, f, mode))
+
+
+def moe_layer_forward_host(x_host, w_gate, bias, layer: LayerWeights, k: int, normalize: int = 1,
+                           route_scale: float = 1.0, mode: int = MOE_MODE_AUTO, residual=None, out_host=None,
+                           topk_idx=None, topk_w=None, hits=None, ws=None, err=None, stream=None,
+                           top_p: float = 1.0):
+    """moe_layer_forward_host: x_host and out_host are CPU float32 tensors [T][d] (page-locked for
+    asynchronous copies); the device tensors as in moe_layer_forward."""
+    if x_host.device.type != "cpu" or x_host.dtype != torch.float32 or not x_host.is_contiguous():
+        raise TypeError("x_host must be a contiguous float32 CPU tensor")
+    T, d = x_host.shape
+    dev = w_gate.device
+    out_host = torch.empty((T, d), dtype=torch.float32).pin_memory() if out_host is None else out_host
+    if out_host.device.type != "cpu" or out_host.dtype != torch.float32 or not out_host.is_contiguous():
+        raise TypeError("out_host must be a contiguous float32 CPU tensor")
+    if ws is None:
+        ws = workspace(layer_host_workspace_bytes(T, k, layer.E, d, layer.f, mode), dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    wp, wn = _ws_ptr(ws)
+    _check(lib().moe_layer_forward_host(ctypes.c_void_p(x_host.data_ptr()), _p(w_gate), _p(bias),
+                                        ctypes.byref(layer.c), _p(residual), T, k, int(normalize),
+                                        float(route_scale), float(top_p), mode,
+                                        ctypes.c_void_p(out_host.data_ptr()), _p(topk_idx), _p(topk_w), _p(hits),
+                                        wp, wn, _p(err), _stream(stream)), "moe_layer_forward_host")
+    return out_host, err
 
 
 def header_functions() -> list[str]:

@@ -388,4 +388,42 @@ int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bia
     return launch_combine(sc.y_pair, sc.y_shared, wt, sc.perm, residual, T, k, d, out, s, err);
 }
 
+size_t moe_layer_host_workspace_bytes(int T, int k, int E, int d, int f, int mode)
+{
+    const size_t layer = moe_layer_workspace_bytes(T, k, E, d, f, mode);
+    if (layer == 0)
+        return 0;
+    return align_up(layer) + 2 * align_up((size_t)T * d * sizeof(float));
+}
+
+int moe_layer_forward_host(const float *x_host, const float *w_gate, const float *bias,
+                           const moe_layer_int4 *w, const float *residual, int T, int k, int normalize,
+                           float route_scale, float top_p, int mode, float *out_host, int32_t *topk_idx,
+                           float *topk_w, uint64_t *hits, void *workspace, size_t ws_bytes, int32_t *err,
+                           void *stream)
+{
+    NvtxRange nvtx("moe.layer_forward_host");
+    if (x_host == nullptr || out_host == nullptr || w == nullptr || workspace == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    const size_t layer = moe_layer_workspace_bytes(T, k, w->E, w->d, w->f, mode);
+    if (layer == 0)
+        return MOE_ERR_INVALID_ARG;
+    const size_t rows = (size_t)T * w->d * sizeof(float);
+    if (ws_bytes < moe_layer_host_workspace_bytes(T, k, w->E, w->d, w->f, mode))
+        return MOE_ERR_WORKSPACE;
+    uint8_t *base = static_cast<uint8_t *>(workspace);
+    float *x_dev = reinterpret_cast<float *>(base + align_up(layer));
+    float *out_dev = reinterpret_cast<float *>(base + align_up(layer) + align_up(rows));
+    const cudaStream_t s = as_stream(stream);
+    if (cudaMemcpyAsync(x_dev, x_host, rows, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const int rc = moe_layer_forward_topp(x_dev, w_gate, bias, w, residual, T, k, normalize, route_scale, top_p,
+                                          mode, out_dev, topk_idx, topk_w, hits, workspace, layer, err, stream);
+    if (rc != MOE_OK)
+        return rc;
+    if (cudaMemcpyAsync(out_host, out_dev, rows, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
 }  // extern "C"
