@@ -627,20 +627,28 @@ def measure_stack(args, rank, world, dev, T_line, steps, warmup, sweep_seconds=2
         ctx["xs"] = torch.from_numpy(workloads.activations(S * T, d, seed=1000 + rank)).to(dev).view(S, T, d)
         ctx["acts"] = torch.empty((NL, T, d), dtype=torch.float32, device=dev)   # outputs of layers 0..6
         ctx["outs"] = torch.empty((S, T, d), dtype=torch.float32, device=dev)
-        ctx["xn"] = torch.empty((T, d), dtype=torch.float32, device=dev)
+        ctx["xn"] = torch.empty((2, T, d), dtype=torch.float32, device=dev)   # a layer's input, the next one's
         ctx["idx"] = torch.empty((NL, T, k), dtype=torch.int32, device=dev)
         ctx["wts"] = torch.empty((T, k), dtype=torch.float32, device=dev)
         ctx["ws"] = moe.workspace(moe.layer_workspace_bytes(T, k, E, d, f, mode), dev)
         return ctx
 
     def stack_step(ctx, x, out):
+        # x_{l+1} = x_l + MoE(RMSNorm(x_l)): the first layer's input is normalised on its own; every
+        # other layer's comes from the previous layer's combine (moe_layer_forward_norm)
+        moe.moe_rms_norm(x, eps, out=ctx["xn"][0])
         for l in range(NL):
             xin = x if l == 0 else ctx["acts"][l - 1]
             xo = out if l == NL - 1 else ctx["acts"][l]
-            moe.moe_rms_norm(xin, eps, out=ctx["xn"])
-            moe.moe_layer_forward(ctx["xn"], wgs[l], biases[l], layers[l], k, 1, 1.0, mode=mode, residual=xin,
-                                  out=xo, topk_idx=ctx["idx"][l], topk_w=ctx["wts"], hits=hits[l],
-                                  ws=ctx["ws"], err=err)
+            cur, nxt = ctx["xn"][l % 2], ctx["xn"][(l + 1) % 2]
+            if l < NL - 1:
+                moe.moe_layer_forward_norm(cur, wgs[l], biases[l], layers[l], k, eps=eps, mode=mode, residual=xin,
+                                           out=xo, out_normed=nxt, topk_idx=ctx["idx"][l], topk_w=ctx["wts"],
+                                           hits=hits[l], ws=ctx["ws"], err=err)
+            else:
+                moe.moe_layer_forward(cur, wgs[l], biases[l], layers[l], k, 1, 1.0, mode=mode, residual=xin,
+                                      out=xo, topk_idx=ctx["idx"][l], topk_w=ctx["wts"], hits=hits[l],
+                                      ws=ctx["ws"], err=err)
 
     def graph(ctx, n):
         side = torch.cuda.Stream(device=dev)
@@ -683,7 +691,7 @@ def measure_stack(args, rank, world, dev, T_line, steps, warmup, sweep_seconds=2
 
     def path_of(T):
         pf = mode == moe.MOE_MODE_PREFILL or (mode == moe.MOE_MODE_AUTO and T >= 128)
-        return pf, 1 + (9 if pf else 5 if (T <= 8 and T * k <= 64) else 7)   # RMS norm + the layer's kernels
+        return pf, (9 if pf else 5 if (T <= 8 and T * k <= 64) else 7)   # the layer's kernels (the norm is fused)
 
     # ---- the batch sweep (each T timed for about sweep_seconds)
     sweep = []
@@ -704,7 +712,7 @@ def measure_stack(args, rank, world, dev, T_line, steps, warmup, sweep_seconds=2
         nu = n_uniq_layers(ctx)
         ms = el / (reps * S)
         by = bytes_of(T, nu)
-        launches += NL * path_of(T)[1] * reps * S
+        launches += (1 + NL * path_of(T)[1]) * reps * S   # + the first layer's RMS norm
         sweep.append({"T": T, "steps": reps * S, "ms_per_step": round(ms, 5),
                       "tokens_per_s": round(job_throughput(T, reps * S, world, el), 2),
                       "stack_gbs": round(by / (ms * 1e-3) / 1e9, 1),
@@ -756,7 +764,7 @@ def measure_stack(args, rank, world, dev, T_line, steps, warmup, sweep_seconds=2
     ms_per_step = elapsed_max / steps
     by = bytes_of(T_line, nu)
     achieved = by / (ms_per_step * 1e-3) / 1e9
-    launches += NL * path_of(T_line)[1] * steps
+    launches += (1 + NL * path_of(T_line)[1]) * steps
     del layers, q_all, s_all, ctx, g_main, g_tail
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

@@ -317,6 +317,22 @@ MOE_API int moe_layer_forward_topp(const float *x, const float *w_gate, const fl
 MOE_API size_t moe_layer_workspace_bytes(int T, int k, int E, int d, int f, int mode);
 
 /*
+ * moe_layer_forward_topp, and the next layer's input of a pre-norm stack from
+ * the same pass over the output: out_normed [T][d] = moe_rms_norm(out, eps)
+ * (unit weight), bitwise equal to calling moe_rms_norm on out afterwards.  The
+ * combine forms each output row in one block, so the separate normalisation
+ * kernel and its launch are saved.  out_normed may not alias out or x.
+ * Workspace: moe_layer_workspace_bytes.  Errors: as moe_layer_forward_topp;
+ * MOE_ERR_INVALID_ARG for a bad out_normed or eps (negative or not finite).
+ */
+MOE_API int moe_layer_forward_norm(const float *x, const float *w_gate, const float *bias,
+                                   const moe_layer_int4 *w, const float *residual, int T, int k,
+                                   int normalize, float route_scale, float top_p, int mode,
+                                   float *out, float *out_normed, float eps, int32_t *topk_idx,
+                                   float *topk_w, uint64_t *hits, void *workspace, size_t ws_bytes,
+                                   int32_t *err, void *stream);
+
+/*
  * The layer with its token rows and its result in HOST memory: x_host [T][d]
  * is copied to the device, moe_layer_forward_topp runs on the copy, and its
  * out [T][d] is copied back to out_host -- all enqueued on `stream`, one

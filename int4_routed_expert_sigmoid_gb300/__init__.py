@@ -13,4 +13,5 @@ from ._binding import (  # noqa: F401
     lib, moe_combine, moe_expert_ffn_int4, moe_expert_ffn_int4_noalloc, moe_hits, moe_layer_forward, moe_rms_norm,
     moe_route, moe_union, status_str, workspace, ExpertTier, tier_workspace_bytes, moe_layer_forward_tier,
     MOE_ERR_STALE, usage_save, usage_load, usage_top, moe_layer_forward_host, layer_host_workspace_bytes,
+    moe_layer_forward_norm,
 )

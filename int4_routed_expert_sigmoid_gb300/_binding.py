@@ -60,6 +60,8 @@ _SIGNATURES = {
     "moe_layer_forward_topp": ([_P, _P, _P, ctypes.POINTER(moe_layer_int4), _P, _I, _I, _I, _F, _F, _I, _P,
                                 _P, _P, _P, _P, _SZ, _P, _P], _I),
     "moe_layer_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
+    "moe_layer_forward_norm": ([_P, _P, _P, ctypes.POINTER(moe_layer_int4), _P, _I, _I, _I, _F, _F, _I, _P, _P, _F,
+                                _P, _P, _P, _P, _SZ, _P, _P], _I),
     "moe_layer_forward_host": ([_P, _P, _P, ctypes.POINTER(moe_layer_int4), _P, _I, _I, _I, _F, _F, _I, _P,
                                 _P, _P, _P, _P, _SZ, _P, _P], _I),
     "moe_layer_host_workspace_bytes": ([_I, _I, _I, _I, _I, _I], _SZ),
@@ -313,6 +315,28 @@ def moe_layer_forward(x, w_gate, bias, layer: LayerWeights, k: int, normalize: i
                                             _p(topk_idx), _p(topk_w), _p(hits), wp, wn, _p(err),
                                             _stream(stream)), "moe_layer_forward_topp")
     return out, err
+
+
+def moe_layer_forward_norm(x, w_gate, bias, layer: LayerWeights, k: int, eps: float = 1e-5, normalize: int = 1,
+                           route_scale: float = 1.0, mode: int = MOE_MODE_AUTO, residual=None, out=None,
+                           out_normed=None, topk_idx=None, topk_w=None, hits=None, ws=None, err=None, stream=None,
+                           top_p: float = 1.0):
+    """moe_layer_forward_norm: the layer's out and RMSNorm(out) (the next layer's input)."""
+    _need(x, torch.float32, "x")
+    T, d = x.shape
+    dev = x.device
+    out = torch.empty((T, d), dtype=torch.float32, device=dev) if out is None else out
+    out_normed = torch.empty((T, d), dtype=torch.float32, device=dev) if out_normed is None else out_normed
+    if ws is None:
+        ws = workspace(layer_workspace_bytes(T, k, layer.E, d, layer.f, mode), dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    wp, wn = _ws_ptr(ws)
+    _check(lib().moe_layer_forward_norm(_p(x), _p(w_gate), _p(bias), ctypes.byref(layer.c), _p(residual), T, k,
+                                        int(normalize), float(route_scale), float(top_p), mode, _p(out),
+                                        _p(out_normed), float(eps), _p(topk_idx), _p(topk_w), _p(hits), wp, wn,
+                                        _p(err), _stream(stream)), "moe_layer_forward_norm")
+    return out, out_normed, err
 
 
 def layer_host_workspace_bytes(T: int, k: int, E: int, d: int, f: int, mode: int = MOE_MODE_AUTO) -> int:

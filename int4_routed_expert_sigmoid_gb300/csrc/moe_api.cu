@@ -3,6 +3,8 @@
 // of each call.
 #include <cstdint>
 
+#include <cmath>
+
 #include "moe_internal.h"
 
 using namespace moe;
@@ -285,13 +287,17 @@ int moe_layer_forward(const float *x, const float *w_gate, const float *bias,
                                   topk_idx, topk_w, hits, workspace, ws_bytes, err, stream);
 }
 
-int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bias,
-                           const moe_layer_int4 *w, const float *residual, int T, int k, int normalize,
-                           float route_scale, float top_p, int mode, float *out, int32_t *topk_idx,
-                           float *topk_w, uint64_t *hits, void *workspace, size_t ws_bytes, int32_t *err,
-                           void *stream)
+}  // extern "C"
+
+namespace {
+
+// The layer (moe_layer_forward_topp); with out_normed set, the combine also writes RMSNorm(out)
+// there (moe_layer_forward_norm).
+int layer_forward(const float *x, const float *w_gate, const float *bias, const moe_layer_int4 *w,
+                  const float *residual, int T, int k, int normalize, float route_scale, float top_p, int mode,
+                  float *out, float *out_normed, float eps, int32_t *topk_idx, float *topk_w, uint64_t *hits,
+                  void *workspace, size_t ws_bytes, int32_t *err, void *stream)
 {
-    NvtxRange nvtx("moe.layer_forward");
     int rc = check_layer(w);
     if (rc != MOE_OK)
         return rc;
@@ -340,6 +346,9 @@ int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bia
         rc = launch_ffn_prefill(pa, s);
         if (rc != MOE_OK)
             return rc;
+        if (out_normed != nullptr)
+            return launch_combine_norm(nullptr, reinterpret_cast<const uint16_t *>(sc.y_pair), sc.y_shared, wt,
+                                       sc.perm, residual, T, k, d, out, out_normed, eps, s, err);
         return launch_combine_bf16(reinterpret_cast<const uint16_t *>(sc.y_pair), sc.y_shared, wt, sc.perm,
                                    residual, T, k, d, out, s, err);
     }
@@ -385,7 +394,38 @@ int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bia
     rc = launch_ffn_decode(a, s);
     if (rc != MOE_OK)
         return rc;
+    if (out_normed != nullptr)
+        return launch_combine_norm(sc.y_pair, nullptr, sc.y_shared, wt, sc.perm, residual, T, k, d, out, out_normed,
+                                   eps, s, err);
     return launch_combine(sc.y_pair, sc.y_shared, wt, sc.perm, residual, T, k, d, out, s, err);
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_layer_forward_topp(const float *x, const float *w_gate, const float *bias,
+                           const moe_layer_int4 *w, const float *residual, int T, int k, int normalize,
+                           float route_scale, float top_p, int mode, float *out, int32_t *topk_idx,
+                           float *topk_w, uint64_t *hits, void *workspace, size_t ws_bytes, int32_t *err,
+                           void *stream)
+{
+    NvtxRange nvtx("moe.layer_forward");
+    return layer_forward(x, w_gate, bias, w, residual, T, k, normalize, route_scale, top_p, mode, out, nullptr,
+                         0.0f, topk_idx, topk_w, hits, workspace, ws_bytes, err, stream);
+}
+
+int moe_layer_forward_norm(const float *x, const float *w_gate, const float *bias,
+                           const moe_layer_int4 *w, const float *residual, int T, int k, int normalize,
+                           float route_scale, float top_p, int mode, float *out, float *out_normed, float eps,
+                           int32_t *topk_idx, float *topk_w, uint64_t *hits, void *workspace, size_t ws_bytes,
+                           int32_t *err, void *stream)
+{
+    NvtxRange nvtx("moe.layer_forward_norm");
+    if (!ok_ptr(out_normed) || out_normed == out || out_normed == x || !(eps >= 0.0f) || !std::isfinite(eps))
+        return MOE_ERR_INVALID_ARG;
+    return layer_forward(x, w_gate, bias, w, residual, T, k, normalize, route_scale, top_p, mode, out, out_normed,
+                         eps, topk_idx, topk_w, hits, workspace, ws_bytes, err, stream);
 }
 
 size_t moe_layer_host_workspace_bytes(int T, int k, int E, int d, int f, int mode)
