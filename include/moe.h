@@ -5,9 +5,12 @@
  *
  * The five per-layer stages come from "Public Colibri Observation and Revision
  * Ledger", section "Exact Architecture and Data-Flow Reconstruction" (Route,
- * Union, Place, Overlap, Learn).  All experts are resident in device memory,
- * so Place and Overlap have no work here; the remaining stages are the calls
- * below.
+ * Union, Place, Overlap, Learn).  The layer calls take every expert resident
+ * in device memory, where Place and Overlap have no work; the expert tier
+ * (moe_tier_*, moe_layer_forward_tier, at the end of this file) keeps the
+ * routed experts in host memory with a device cache of some of them, placing
+ * the missing ones on demand and overlapping those copies with the FFN of the
+ * cached ones.  The usage file (moe_usage_*) persists the Learn stage's counts.
  *
  * Conventions shared by every entry point
  *  - Pointers are CUDA device pointers owned by the caller, unless a comment
