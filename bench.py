@@ -57,7 +57,7 @@ def parse_args(argv=None):
                     help="override the routed expert count (small-footprint profiling runs); 0 = workload's")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the tokens per step (small-footprint profiling runs); 0 = workload's")
-    ap.add_argument("--mode", choices=["workload", "decode", "prefill"], default="workload",
+    ap.add_argument("--mode", choices=["workload", "decode", "prefill", "hybrid"], default="workload",
                     help="FFN path: the workload's own (prefill for prefill, decode otherwise) or forced")
     ap.add_argument("--graph-steps", type=int, default=100, help="steps captured per CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=2000)
@@ -217,7 +217,7 @@ class LayerCopies:
         del L
 
 
-def measure_layer(copies, sh, prefill, steps, warmup, graph_steps, e2e_steps, rank, world, dev):
+def measure_layer(copies, sh, path, steps, warmup, graph_steps, e2e_steps, rank, world, dev):
     """One workload of the single-layer benchmark: `steps` timed steps of moe_layer_forward over T
     tokens (CUDA graphs of S steps), stage durations from a second graph with events between the
     stage calls, and an end-to-end run with host buffers.  Returns the workload's measurements."""
@@ -226,7 +226,8 @@ def measure_layer(copies, sh, prefill, steps, warmup, graph_steps, e2e_steps, ra
     import int4_routed_expert_sigmoid_gb300 as moe
     import workloads
     T, E, k, d, f = sh.T, sh.E, sh.k, sh.d, sh.f
-    mode = moe.MOE_MODE_PREFILL if prefill else moe.MOE_MODE_DECODE
+    mode = {"decode": moe.MOE_MODE_DECODE, "prefill": moe.MOE_MODE_PREFILL, "hybrid": moe.MOE_MODE_HYBRID}[path]
+    prefill = path == "prefill"
     R = copies.R
     S = max(1, min(graph_steps, steps))
     bias0 = workloads.selection_bias(E, sh.bias, seed=0)
@@ -283,6 +284,8 @@ def measure_layer(copies, sh, prefill, steps, warmup, graph_steps, e2e_steps, ra
     # combine; otherwise logits, top-k, union, x fragments, gate/up, down, combine
     if prefill:   # logits, top-k, union, pair positions, token rows, gate/up, h conversion, down, combine
         launches_per_step = 9
+    elif path == "hybrid":   # logits, top-k, union, split, x fragments, decode gate/up + down, the prefill
+        launches_per_step = 13   # path's pair positions, token rows, gate/up, h conversion, down; combine
     else:
         launches_per_step = 5 if (T <= 8 and T * k <= 64) else 7
 
@@ -411,11 +414,14 @@ def measure_layer(copies, sh, prefill, steps, warmup, graph_steps, e2e_steps, ra
                 "flops_per_launch": flops, "ms_per_launch": round(ffn_ms, 5)}
     else:
         achieved = byts["ffn"] / (ffn_ms * 1e-3) / 1e9
-        roof = {"kernel": "expert FFN call (act fragments + gate/up + down kernels), timed over back-to-back calls",
+        roof = {"kernel": ("expert FFN call (act fragments + gate/up + down kernels), timed over back-to-back calls"
+                           if path == "decode" else
+                           "hybrid expert FFN call (split, decode half, prefill half with the shared expert), timed "
+                           "over back-to-back calls; bytes = the union's expert blocks"),
                 "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": ncu_traffic(ROOT, "ffn" if T == 1 else f"ffn_T{T}"),
+                "traffic": ncu_traffic(ROOT, "ffn" if T == 1 else f"ffn_T{T}") if path == "decode" else None,
                 "peak_source": peaks["source"], "bytes_per_launch": byts["ffn"], "ms_per_launch": round(ffn_ms, 5)}
     ms_per_step = elapsed_max / steps
     return {
@@ -423,7 +429,7 @@ def measure_layer(copies, sh, prefill, steps, warmup, graph_steps, e2e_steps, ra
         "warmup": warmup, "ms_per_step": round(ms_per_step, 6),
         "config": {"workload": f"{sh.name}: 1 MoE layer, E={E} routed + 1 shared, k={k}, d={d}, f={f}, "
                                f"int4 group-{sh.G} fp32 scales, T={T} token(s) per step, selection bias "
-                               f"{sh.bias}, FFN path {'prefill' if prefill else 'decode'}",
+                               f"{sh.bias}, FFN path {path}",
                    "T": T, "E": E, "k": k, "d": d, "f": f, "G": sh.G, "weights": "int4",
                    "l2": (f"inputs larger than L2: {R} device copies of the layer "
                           f"({R * E * byts['expert_block'] / 1e9:.1f} GB) rotated across steps")
@@ -527,8 +533,11 @@ def workload_shape(args, name):
     return sh
 
 
-def is_prefill(args, name):
-    return name == "prefill" if args.mode == "workload" else args.mode == "prefill"
+def path_for(args, name):
+    """FFN path of a single-layer workload: its own (prefill for prefill, decode otherwise) or forced."""
+    if args.mode == "workload":
+        return "prefill" if name == "prefill" else "decode"
+    return args.mode
 
 
 # steps of the secondary workloads carried in the default line (their own counts, a few seconds each)
@@ -542,10 +551,11 @@ def run_ours(args, rank, world, local):
     import torch
     dev = init_device(local, world)
     sh = workload_shape(args, args.workload)
-    prefill = is_prefill(args, args.workload)
+    path = path_for(args, args.workload)
+    prefill = path == "prefill"
     R = max(1, min(args.replicas, 2) if prefill else args.replicas)
     copies = LayerCopies(sh, R, dev)
-    res = measure_layer(copies, sh, prefill, args.steps, args.warmup,
+    res = measure_layer(copies, sh, path, args.steps, args.warmup,
                         args.graph_steps if not prefill else 4, 8 if prefill else args.e2e_steps, rank, world, dev)
     line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
@@ -556,10 +566,14 @@ def run_ours(args, rank, world, local):
     extras = {}
     if args.workload == "decode" and not args.no_workloads and not (args.experts or args.tokens):
         # the other single-layer workloads on the same weights, then the stack on its own 8 layers
-        for name in ("batched_decode", "prefill"):
-            sh_x = workload_shape(args, name)
-            pf = is_prefill(args, name)
-            extras[name] = measure_layer(copies, sh_x, pf, EXTRA_STEPS[name], max(3, args.warmup),
+        # (batched_decode_hybrid: the same batch on the opt-in hybrid path, MOE_MODE_HYBRID, which gives
+        # the tensor-core path's precision to the experts with more than 8 of its tokens)
+        for name, wl, path_x in (("batched_decode", "batched_decode", path_for(args, "batched_decode")),
+                                 ("batched_decode_hybrid", "batched_decode", "hybrid"),
+                                 ("prefill", "prefill", path_for(args, "prefill"))):
+            sh_x = workload_shape(args, wl)
+            pf = path_x == "prefill"
+            extras[name] = measure_layer(copies, sh_x, path_x, EXTRA_STEPS[wl], max(3, args.warmup),
                                          4 if pf else args.graph_steps, 8 if pf else 200, rank, world, dev)
             line["gpu_launches"] += extras[name]["gpu_launches"]
         del copies
@@ -592,8 +606,8 @@ def measure_stack(args, rank, world, dev, T_line, steps, warmup, sweep_seconds=2
     import workloads
     sh = workloads.WORKLOADS["stack"]
     E, k, d, f, G, NL = sh.E, sh.k, sh.d, sh.f, sh.G, sh.layers
-    mode = {"workload": moe.MOE_MODE_AUTO, "decode": moe.MOE_MODE_DECODE,
-            "prefill": moe.MOE_MODE_PREFILL}[args.mode]   # automatic: the library picks the path by T
+    mode = {"workload": moe.MOE_MODE_AUTO, "decode": moe.MOE_MODE_DECODE, "prefill": moe.MOE_MODE_PREFILL,
+            "hybrid": moe.MOE_MODE_HYBRID}[args.mode]   # automatic: the library picks the path by T
     eps = 1e-5
 
     # ---- the 8 layers, generated one at a time into one host buffer and copied to the device
@@ -690,8 +704,16 @@ def measure_stack(args, rank, world, dev, T_line, steps, warmup, sweep_seconds=2
         return sum((n + 1) * blk + E * d * 4 + E * 4 + 3 * T * d * 4 for n in nu)
 
     def path_of(T):
-        pf = mode == moe.MOE_MODE_PREFILL or (mode == moe.MOE_MODE_AUTO and T >= 128)
-        return pf, (9 if pf else 5 if (T <= 8 and T * k <= 64) else 7)   # the layer's kernels (the norm is fused)
+        # the FFN path and the layer's kernels (as counted in measure_layer); every layer but the last
+        # also forms the next layer's normalised input, in its combine up to 64 tokens, else in one
+        # more kernel
+        if mode == moe.MOE_MODE_PREFILL:
+            name, n = "prefill", 9
+        elif mode == moe.MOE_MODE_HYBRID or (mode == moe.MOE_MODE_AUTO and T >= 128):
+            name, n = "hybrid", 13
+        else:
+            name, n = "decode", 5 if (T <= 8 and T * k <= 64) else 7
+        return name, n, (NL - 1) * (1 if T > 64 else 0)
 
     # ---- the batch sweep (each T timed for about sweep_seconds)
     sweep = []
@@ -712,12 +734,12 @@ def measure_stack(args, rank, world, dev, T_line, steps, warmup, sweep_seconds=2
         nu = n_uniq_layers(ctx)
         ms = el / (reps * S)
         by = bytes_of(T, nu)
-        launches += (1 + NL * path_of(T)[1]) * reps * S   # + the first layer's RMS norm
+        launches += (1 + NL * path_of(T)[1] + path_of(T)[2]) * reps * S   # + the first layer's RMS norm
         sweep.append({"T": T, "steps": reps * S, "ms_per_step": round(ms, 5),
                       "tokens_per_s": round(job_throughput(T, reps * S, world, el), 2),
                       "stack_gbs": round(by / (ms * 1e-3) / 1e9, 1),
                       "frac": round(by / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                      "ffn_path": "prefill" if path_of(T)[0] else "decode",
+                      "ffn_path": path_of(T)[0],
                       "n_uniq_per_layer": nu, "clocks": ck, "device_error": int(err.item())})
         del g, ctx
         torch.cuda.empty_cache()
@@ -764,7 +786,7 @@ def measure_stack(args, rank, world, dev, T_line, steps, warmup, sweep_seconds=2
     ms_per_step = elapsed_max / steps
     by = bytes_of(T_line, nu)
     achieved = by / (ms_per_step * 1e-3) / 1e9
-    launches += (1 + NL * path_of(T_line)[1]) * steps
+    launches += (1 + NL * path_of(T_line)[1] + path_of(T_line)[2]) * steps
     del layers, q_all, s_all, ctx, g_main, g_tail
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

@@ -96,20 +96,28 @@ enum {
 
 /* FFN execution modes. */
 enum {
-    MOE_MODE_AUTO = 0,     /* decode path when T < 128, else prefill.  The two paths differ in
+    MOE_MODE_AUTO = 0,     /* decode path when T < 128, else hybrid.  The paths differ in
                               precision (decode within 1e-4 of the output RMS of the exact
-                              result, prefill within 2e-2), so under this mode the same token's
-                              output can move by up to 2e-2 * RMS when the batch around it
-                              crosses 128 tokens.  Pass MOE_MODE_DECODE to keep the decode
-                              path's precision at every batch size. */
+                              result, prefill and hybrid within 2e-2), so under this mode the
+                              same token's output can move by up to 2e-2 * RMS when the batch
+                              around it crosses 128 tokens.  Pass MOE_MODE_DECODE to keep the
+                              decode path's precision at every batch size.  (The expert tier
+                              has no hybrid: there AUTO takes prefill from 128 tokens.) */
     MOE_MODE_DECODE = 1,   /* fp32-accurate grouped GEMV: exact int4 against activations split
                               into fp16 hi + lo parts, fp32 accumulation */
-    MOE_MODE_PREFILL = 2   /* tcgen05 grouped GEMM on 16-bit operands (fp16 q*s weights scaled
+    MOE_MODE_PREFILL = 2,  /* tcgen05 grouped GEMM on 16-bit operands (fp16 q*s weights scaled
                               per weight row by a power of two, fp16 activations scaled per
                               row by a power of two), fp32 accumulate.  Scale magnitudes are
                               free; within one weight row, group scales must stay within
                               2^-14 .. 2^13 of the row's first group scale (else
                               MOE_DEVERR_SCALE_RANGE) */
+    MOE_MODE_HYBRID = 3    /* per expert of the union: one with at most 8 tokens of the batch
+                              takes the decode path, one with more (and the shared expert) the
+                              prefill path, so the tensor cores run only where an expert's
+                              tokens make a dense contraction (a choice of this library: the
+                              pages name no GPU paths).  Each expert's outputs are bitwise those
+                              of its path; routed outputs in fp32.  Precision: the prefill
+                              path's bound. */
 };
 
 /* Human-readable name of a status code (static string). */
@@ -449,6 +457,9 @@ MOE_API size_t moe_tier_workspace_bytes(int T, int k, int E, int d, int f, int m
  * experts than unpinned slots returns MOE_ERR_INVALID_ARG (nothing is copied).
  * The shared expert (shared_q, shared_s) is in device memory.  workspace:
  * moe_tier_workspace_bytes(T, k, E, d, f, mode) bytes, 256-byte aligned.
+ * mode: MOE_MODE_AUTO (decode below 128 tokens, prefill from 128), _DECODE or
+ * _PREFILL; MOE_MODE_HYBRID returns MOE_ERR_INVALID_ARG.  The bit-identity
+ * above holds against moe_layer_forward_topp with the mode AUTO resolves to.
  */
 MOE_API int moe_layer_forward_tier(const float *x, const float *w_gate, const float *bias, moe_tier tier,
                                    const uint8_t *shared_q, const float *shared_s, const float *residual,

@@ -19,7 +19,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_STALE = 0, -1, -2, -3, -4, -5
 MOE_DEVERR_BAD_EXPERT, MOE_DEVERR_TIMEOUT, MOE_DEVERR_SCALE_RANGE, MOE_DEVERR_BOUNDS = 0x1, 0x2, 0x4, 0x8
-MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL = 0, 1, 2
+MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL, MOE_MODE_HYBRID = 0, 1, 2, 3
 
 _HITS_DTYPES = tuple(getattr(torch, n) for n in ("int64", "uint64") if hasattr(torch, n))
 _lock = threading.Lock()

@@ -113,6 +113,7 @@ struct Params {
     int T, k, nchunks, tiles, out_rows;   // nchunks: k-chunks of the reduction; out_rows: d (down)
     int dynamic;                // 1: items after the first from the counter; 0: CTA c takes c, c + G, ...
     int n_experts, n_view;      // routed experts of the routing; expert blocks of the weight view
+    int max_uniq;               // capacity of the unit table beyond the shared expert: n_uniq is clamped to it
 };
 
 // Packed nibbles -> fp16 subnormal pairs: lo takes the nibbles at bits 0-3 and
@@ -539,7 +540,7 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
     // (items 0 .. tiles - 1, whatever the union).  Weights do not depend on the previous kernel.
     int units = 0;
     if (MODE == kDown) {
-        units = __ldcg(p.n_uniq) + p.with_shared;
+        units = min(max(__ldcg(p.n_uniq), 0), p.max_uniq) + p.with_shared;
         load_units(p, units, tab);
         __syncthreads();
     }
@@ -576,7 +577,7 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
         // the down kernel reads the union before its own grid wait: release it only after ours
         griddep_wait();   // routing, union and activation fragments come from the previous kernels
         griddep_launch_dependents();
-        units = *p.n_uniq + p.with_shared;
+        units = min(max(*p.n_uniq, 0), p.max_uniq) + p.with_shared;
         load_units(p, units, tab);
         __syncthreads();
     } else {
@@ -902,8 +903,11 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
     pg.out_rows = f;
     pg.n_experts = a.n_experts > 0 ? a.n_experts : E;
     pg.n_view = E;
-    rc = G == 64 ? launch_tok<kGateUp, 8, 64>(gu, pg, max_experts, a.T, s)
-                 : launch_tok<kGateUp, 8, 32>(gu, pg, max_experts, a.T, s);
+    pg.max_uniq = max_experts - 1;
+    // pass width from the most tokens a listed expert can have (the hybrid's decode half: at most 8)
+    const int tsel = a.max_tokens > 0 && a.max_tokens < a.T ? a.max_tokens : a.T;
+    rc = G == 64 ? launch_tok<kGateUp, 8, 64>(gu, pg, max_experts, tsel, s)
+                 : launch_tok<kGateUp, 8, 32>(gu, pg, max_experts, tsel, s);
     if (rc != MOE_OK)
         return rc;
 
@@ -920,9 +924,9 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
     pd.tiles = d / 64;
     pd.out_rows = d;
     if (gpc_h == 8)
-        return G == 64 ? launch_tok<kDown, 8, 64>(dn, pd, max_experts, a.T, s)
-                       : launch_tok<kDown, 8, 32>(dn, pd, max_experts, a.T, s);
-    return launch_tok<kDown, 4, 32>(dn, pd, max_experts, a.T, s);   // G = 64 needs gpc_h = 8 (checked above)
+        return G == 64 ? launch_tok<kDown, 8, 64>(dn, pd, max_experts, tsel, s)
+                       : launch_tok<kDown, 8, 32>(dn, pd, max_experts, tsel, s);
+    return launch_tok<kDown, 4, 32>(dn, pd, max_experts, tsel, s);   // G = 64 needs gpc_h = 8 (checked above)
 }
 
 }  // namespace moe

@@ -141,6 +141,7 @@ struct PParams {
     int32_t *err;
     int T, k, K, mtiles, out_rows;
     int n_experts, n_view;        // routed experts of the routing; expert blocks of the weight view
+    int max_uniq;                 // capacity of the unit table beyond the shared expert: n_uniq is clamped to it
 };
 
 __device__ __forceinline__ int frag_pos8(int o) { return 2 * (o & 3) + (o >> 2); }
@@ -352,7 +353,7 @@ ffn_prefill_kernel(const __grid_constant__ PMaps maps, const PParams p)
     griddep_launch_dependents();
     griddep_wait();   // union and sorted activation rows come from earlier kernels
 
-    const int units = *p.n_uniq + p.with_shared;
+    const int units = min(max(*p.n_uniq, 0), p.max_uniq) + p.with_shared;
     build_units<N>(p, units, tab);
     const int n_items = tab[units].cum * p.mtiles;
     const int nraw = p.K / RAWK;
@@ -910,6 +911,7 @@ int launch_ffn_prefill(const PrefillFfnArgs &a, cudaStream_t s)
     pg.n_experts = E_off;
     pg.n_view = E;
     const int max_units = (E < T * k ? E : T * k) + 1;
+    pg.max_uniq = max_units - 1;
     // d is a multiple of 256
     rc = G == 64 ? launch_prefill_one<kPGateUp, 256, 64>(gm, pg, max_units, s)
                  : launch_prefill_one<kPGateUp, 256, 32>(gm, pg, max_units, s);

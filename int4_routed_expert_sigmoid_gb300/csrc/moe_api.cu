@@ -45,14 +45,27 @@ int check_layer(const moe_layer_int4 *w)
 
 namespace moe {
 
+// From 128 tokens the hybrid path is faster than either plain path on the measured batches (a
+// Zipf-routed 256-expert layer at 128-512 tokens; at 4096 tokens with ~128 per expert it is the
+// prefill path); below, the decode path keeps its 1e-4 precision.
 int resolve_mode(int mode, int T)
 {
     if (mode == MOE_MODE_AUTO)
-        return T < 128 ? MOE_MODE_DECODE : MOE_MODE_PREFILL;   // measured crossover of the two FFN paths
+        return T < 128 ? MOE_MODE_DECODE : MOE_MODE_HYBRID;
     return mode;
 }
 
-bool valid_mode(int mode) { return mode == MOE_MODE_AUTO || mode == MOE_MODE_DECODE || mode == MOE_MODE_PREFILL; }
+int resolve_mode_plain(int mode, int T)
+{
+    if (mode == MOE_MODE_AUTO)
+        return T < 128 ? MOE_MODE_DECODE : MOE_MODE_PREFILL;   // measured crossover of the two plain paths
+    return mode;
+}
+
+bool valid_mode(int mode)
+{
+    return mode == MOE_MODE_AUTO || mode == MOE_MODE_DECODE || mode == MOE_MODE_PREFILL || mode == MOE_MODE_HYBRID;
+}
 
 size_t ffn_scratch_layout(int T, int k, int d, int f, uint8_t *base, FfnScratch *out)
 {
@@ -100,11 +113,89 @@ size_t layer_scratch_layout(int T, int k, int E, int d, int f, int mode, uint8_t
     return off;
 }
 
+size_t hybrid_scratch_layout(int T, int k, int d, int f, uint8_t *base, HybridScratch *o)
+{
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t *p = base ? base + off : nullptr;
+        off = align_up(off + bytes);
+        return p;
+    };
+    HybridScratch h{};
+    uint8_t *dec = take(ffn_scratch_layout(T, k, d, f, nullptr, nullptr));
+    if (base)
+        ffn_scratch_layout(T, k, d, f, dec, &h.dec);
+    h.pre = take(prefill_scratch_bytes(T, k, d, f));
+    const size_t list = (size_t)T * k * sizeof(int32_t);   // the union has at most T * k experts
+    h.uniq_cold = reinterpret_cast<int32_t *>(take(list));
+    h.uniq_hot = reinterpret_cast<int32_t *>(take(list));
+    h.n_cold = reinterpret_cast<int32_t *>(take(sizeof(int32_t)));
+    h.n_hot = reinterpret_cast<int32_t *>(take(sizeof(int32_t)));
+    if (o)
+        *o = h;
+    return off;
+}
+
 size_t ffn_scratch_bytes_mode(int T, int k, int d, int f, int mode)
 {
-    if (resolve_mode(mode, T) == MOE_MODE_PREFILL)
-        return prefill_scratch_bytes(T, k, d, f);
-    return ffn_scratch_layout(T, k, d, f, nullptr, nullptr);
+    switch (resolve_mode(mode, T)) {
+    case MOE_MODE_PREFILL: return prefill_scratch_bytes(T, k, d, f);
+    case MOE_MODE_HYBRID: return hybrid_scratch_layout(T, k, d, f, nullptr, nullptr);
+    default: return ffn_scratch_layout(T, k, d, f, nullptr, nullptr);
+    }
+}
+
+// The two FFN paths one after the other over their halves of the union: the decode grouped GEMV
+// over the experts with at most kHybridColdMax pairs, then the tcgen05 grouped GEMM over the rest
+// and the shared expert.  They write disjoint rows of y_pair (each expert's pair rows) and the
+// prefill path writes y_shared.
+int run_ffn_hybrid(const moe_layer_int4 *w, const float *x, const int32_t *offsets, const int32_t *sorted_pair,
+                   const int32_t *uniq, const int32_t *n_uniq, int T, int k, void *scratch, float *y_pair,
+                   float *y_shared, int32_t *err, cudaStream_t s)
+{
+    HybridScratch h{};
+    hybrid_scratch_layout(T, k, w->d, w->f, static_cast<uint8_t *>(scratch), &h);
+    int rc = launch_split_units(offsets, uniq, n_uniq, w->E, T * k, kHybridColdMax, h.uniq_cold, h.n_cold,
+                                h.uniq_hot, h.n_hot, err, s);
+    if (rc == MOE_OK)
+        rc = launch_act_frag(x, T, w->d, h.dec.x_frag, h.dec.x_scale, h.dec.work, kDecodeCounters, s);
+    if (rc != MOE_OK)
+        return rc;
+    DecodeFfnArgs a{};
+    a.w = w;
+    a.offsets = offsets;
+    a.sorted_pair = sorted_pair;
+    a.uniq = h.uniq_cold;
+    a.n_uniq = h.n_cold;
+    a.T = T;
+    a.k = k;
+    a.x_frag = h.dec.x_frag;
+    a.x_scale = h.dec.x_scale;
+    a.h_frag = h.dec.h_frag;
+    a.y_pair = y_pair;
+    a.y_shared = y_shared;   // not written: the shared expert is the prefill half's
+    a.work = h.dec.work;
+    a.with_shared = 0;
+    a.max_tokens = kHybridColdMax;
+    a.err = err;
+    rc = launch_ffn_decode(a, s);
+    if (rc != MOE_OK)
+        return rc;
+    PrefillFfnArgs pa{};
+    pa.w = w;
+    pa.x = x;
+    pa.offsets = offsets;
+    pa.sorted_pair = sorted_pair;
+    pa.uniq = h.uniq_hot;
+    pa.n_uniq = h.n_hot;
+    pa.T = T;
+    pa.k = k;
+    pa.scratch = h.pre;
+    pa.y_pair = y_pair;
+    pa.y_shared = y_shared;
+    pa.with_shared = 1;
+    pa.err = err;
+    return launch_ffn_prefill(pa, s);
 }
 
 }  // namespace moe
@@ -211,6 +302,9 @@ int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *
     if (ws_bytes < moe_ffn_workspace_bytes(T, k, w->d, w->f, mode))
         return MOE_ERR_WORKSPACE;
     mode = resolve_mode(mode, T);
+    if (mode == MOE_MODE_HYBRID)
+        return run_ffn_hybrid(w, x, offsets, sorted_pair, uniq, n_uniq, T, k, workspace, y_pair, y_shared, err,
+                              as_stream(stream));
     if (mode == MOE_MODE_PREFILL) {
         PrefillFfnArgs pa{};
         pa.w = w;
@@ -318,6 +412,23 @@ int layer_forward(const float *x, const float *w_gate, const float *bias, const 
     int32_t *idx = topk_idx ? topk_idx : sc.idx;
     float *wt = topk_w ? topk_w : sc.w;
     const cudaStream_t s = as_stream(stream);
+    if (mode == MOE_MODE_HYBRID) {
+        rc = launch_router_logits(x, w_gate, T, d, E, sc.logits, s);
+        if (rc == MOE_OK)
+            rc = launch_router_topk(sc.logits, bias, T, E, k, normalize, route_scale, top_p, idx, wt, s);
+        if (rc == MOE_OK)
+            rc = launch_union(idx, T, k, E, sc.counts, sc.offsets, sc.perm, sc.sorted_pair, sc.uniq,
+                              sc.n_uniq, hits, err, s);
+        if (rc == MOE_OK)
+            rc = run_ffn_hybrid(w, x, sc.offsets, sc.sorted_pair, sc.uniq, sc.n_uniq, T, k, sc.ffn, sc.y_pair,
+                                sc.y_shared, err, s);
+        if (rc != MOE_OK)
+            return rc;
+        if (out_normed != nullptr)
+            return launch_combine_norm(sc.y_pair, nullptr, sc.y_shared, wt, sc.perm, residual, T, k, d, out,
+                                       out_normed, eps, s, err);
+        return launch_combine(sc.y_pair, sc.y_shared, wt, sc.perm, residual, T, k, d, out, s, err);
+    }
     if (mode == MOE_MODE_PREFILL) {
         rc = launch_router_logits(x, w_gate, T, d, E, sc.logits, s);
         if (rc == MOE_OK)

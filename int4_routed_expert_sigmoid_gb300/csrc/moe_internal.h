@@ -128,6 +128,14 @@ int launch_union(const int32_t *idx, int T, int k, int E, int32_t *counts, int32
                  int32_t *perm, int32_t *sorted_pair, int32_t *uniq, int32_t *n_uniq,
                  uint64_t *hits, int32_t *err, cudaStream_t s);
 int launch_hits(const int32_t *counts, int E, uint64_t *hits, cudaStream_t s);
+// Hybrid FFN: the union's expert list split, in its order, into the experts with at most max_cold
+// pairs (uniq_cold, *n_cold) and the rest (uniq_hot, *n_hot); an id outside [0, E) goes to neither
+// list and sets MOE_DEVERR_BAD_EXPERT.  *n_uniq is clamped to min(E, pairs), the length of each
+// list.  One block; E <= 1024.
+int launch_split_units(const int32_t *offsets, const int32_t *uniq, const int32_t *n_uniq, int E, int pairs,
+                       int max_cold, int32_t *uniq_cold, int32_t *n_cold, int32_t *uniq_hot, int32_t *n_hot,
+                       int32_t *err, cudaStream_t s);
+constexpr int kHybridColdMax = 8;   // pairs of an expert up to which the hybrid FFN takes the decode path
 // top-k + union + hits in one block (T <= 8, T*k <= 64)
 int launch_select_union(const float *logits, const float *bias, int T, int E, int k, int normalize,
                         float route_scale, float top_p, int32_t *idx, float *w, int32_t *counts, int32_t *offsets,
@@ -148,6 +156,7 @@ struct DecodeFfnArgs {
     int with_shared = 1;                // 0: only the uniq list's experts (a second launch of the tier)
     int32_t *err;
     int n_experts = 0;                  // routed experts of the routing (offsets has n_experts + 1); 0: w->E
+    int max_tokens = 0;                 // most tokens any listed expert has, when known (0: T); sets the pass width
 };
 constexpr int kDecodeCounters = 2;   // items claimed by the gate/up and the down kernel
 int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s);
@@ -200,9 +209,11 @@ int make_tmap_nd(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, in
 // device properties cached per device
 int sm_count(int device);
 
-// moe_api.cu: the FFN path a mode resolves to at T tokens, and the workspace layouts of the FFN
-// and of the whole layer (base may be null to size them).
+// moe_api.cu: the FFN path a mode resolves to at T tokens (MOE_MODE_DECODE, _PREFILL or _HYBRID;
+// resolve_mode_plain never gives _HYBRID: AUTO takes prefill from 128 tokens), and the workspace
+// layouts of the FFN and of the whole layer (base may be null to size them).
 int resolve_mode(int mode, int T);
+int resolve_mode_plain(int mode, int T);
 size_t ffn_scratch_bytes_mode(int T, int k, int d, int f, int mode);
 
 // Scratch of the decode FFN: activation fragments of x (with a factor per row) and of h (factors
@@ -213,6 +224,18 @@ struct FfnScratch {
     int32_t *work;
 };
 size_t ffn_scratch_layout(int T, int k, int d, int f, uint8_t *base, FfnScratch *out);
+
+// Scratch of the hybrid FFN: the decode path's, the prefill path's, and the two expert lists.
+struct HybridScratch {
+    FfnScratch dec;
+    void *pre;
+    int32_t *uniq_cold, *uniq_hot, *n_cold, *n_hot;
+};
+size_t hybrid_scratch_layout(int T, int k, int d, int f, uint8_t *base, HybridScratch *out);
+// The hybrid FFN over a union (both paths, fp32 routed outputs), on stream s.
+int run_ffn_hybrid(const moe_layer_int4 *w, const float *x, const int32_t *offsets, const int32_t *sorted_pair,
+                   const int32_t *uniq, const int32_t *n_uniq, int T, int k, void *scratch, float *y_pair,
+                   float *y_shared, int32_t *err, cudaStream_t s);
 
 struct LayerScratch {
     float *logits;

@@ -368,7 +368,7 @@ int moe_layer_forward_tier(const float *x, const float *w_gate, const float *bia
     int32_t *img = reinterpret_cast<int32_t *>(base + align_up(layer_bytes));
     int32_t *n1 = img, *n2 = img + 1, *work2 = img + 2, *list1 = img + kTierHead, *list2 = list1 + E,
             *map = list2 + E;
-    mode = resolve_mode(mode, T);
+    mode = resolve_mode_plain(mode, T);   // the tier has no hybrid path
     int32_t *idx = topk_idx ? topk_idx : sc.idx;
     float *wt = topk_w ? topk_w : sc.w;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

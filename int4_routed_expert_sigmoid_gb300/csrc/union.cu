@@ -353,6 +353,65 @@ select_union_kernel(const float *__restrict__ logits, const float *__restrict__ 
     }
 }
 
+// Split of the union's expert list for the hybrid FFN: a stable compaction of the flags
+// "at most max_cold pairs" and "more", one block of up to 1024 threads (warp ballots, then a scan
+// of the 32 warp counts), looping when the list is longer than the block.
+constexpr int kSplitThreads = 1024;
+
+__global__ void __launch_bounds__(kSplitThreads)
+split_units_kernel(const int32_t *__restrict__ offsets, const int32_t *__restrict__ uniq,
+                   const int32_t *__restrict__ n_uniq, int E, int cap, int max_cold, int32_t *__restrict__ uniq_cold,
+                   int32_t *__restrict__ n_cold, int32_t *__restrict__ uniq_hot, int32_t *__restrict__ n_hot,
+                   int32_t *__restrict__ err)
+{
+    __shared__ int wcold[kSplitThreads / 32], whot[kSplitThreads / 32];
+    griddep_launch_dependents();
+    griddep_wait();   // the union comes from the previous kernel
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n = max(0, min(*n_uniq, cap));   // cap: min(E, pairs), the lists' length
+    int cold_base = 0, hot_base = 0;
+    for (int base = 0; base < n; base += kSplitThreads) {
+        const int i = base + (int)threadIdx.x;
+        int e = -1;
+        bool cold = false, hot = false;
+        if (i < n) {
+            e = uniq[i];
+            if (e >= 0 && e < E) {
+                const int m = offsets[e + 1] - offsets[e];
+                cold = m <= max_cold;
+                hot = !cold;
+            } else {
+                atomicOr(err, MOE_DEVERR_BAD_EXPERT);
+            }
+        }
+        const unsigned bc = __ballot_sync(0xffffffffu, cold), bh = __ballot_sync(0xffffffffu, hot);
+        if (lane == 0) {
+            wcold[warp] = __popc(bc);
+            whot[warp] = __popc(bh);
+        }
+        __syncthreads();
+        int pc = cold_base, ph = hot_base, tc = 0, th = 0;
+        for (int w = 0; w < kSplitThreads / 32; w++) {
+            pc += w < warp ? wcold[w] : 0;
+            ph += w < warp ? whot[w] : 0;
+            tc += wcold[w];
+            th += whot[w];
+        }
+        const unsigned below = (1u << lane) - 1u;
+        if (cold)
+            uniq_cold[pc + __popc(bc & below)] = e;
+        if (hot)
+            uniq_hot[ph + __popc(bh & below)] = e;
+        cold_base += tc;
+        hot_base += th;
+        __syncthreads();   // the warp counts are rewritten by the next round
+    }
+    if (threadIdx.x == 0) {
+        *n_cold = cold_base;
+        *n_hot = hot_base;
+    }
+}
+
 __global__ void hits_kernel(const int32_t *__restrict__ counts, int E, uint64_t *__restrict__ hits)
 {
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -384,6 +443,17 @@ int launch_union(const int32_t *idx, int T, int k, int E, int32_t *counts, int32
     union_kernel<<<1, kThreads, smem, s>>>(idx, T, k, E, use_bitmap, counts, offsets, perm, sorted_pair, uniq,
                                         n_uniq, hits, err);
     return cuda_status(cudaGetLastError());
+}
+
+int launch_split_units(const int32_t *offsets, const int32_t *uniq, const int32_t *n_uniq, int E, int pairs,
+                       int max_cold, int32_t *uniq_cold, int32_t *n_cold, int32_t *uniq_hot, int32_t *n_hot,
+                       int32_t *err, cudaStream_t s)
+{
+    if (E < 1 || E > kMaxE || pairs < 1)
+        return MOE_ERR_UNSUPPORTED;
+    const int cap = E < pairs ? E : pairs;
+    return launch_pdl(split_units_kernel, 1, kSplitThreads, 0, s, offsets, uniq, n_uniq, E, cap, max_cold,
+                      uniq_cold, n_cold, uniq_hot, n_hot, err);
 }
 
 int launch_select_union(const float *logits, const float *bias, int T, int E, int k, int normalize,

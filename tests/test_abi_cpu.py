@@ -49,6 +49,26 @@ def test_workspace_queries(m):
     assert b >= 64 * 8 * 6144 * 4
 
 
+def test_mode_constants_and_workspace_by_path(m):
+    """The binding's FFN modes are the header's enum; the workspace follows the path a mode resolves to:
+    AUTO is the decode path below 128 tokens and the hybrid from 128 (decode + prefill scratch + lists)."""
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe.h")).read()
+    modes = dict(re.findall(r"(MOE_MODE_\w+) = (\d+)", hdr))
+    assert set(modes) == {"MOE_MODE_AUTO", "MOE_MODE_DECODE", "MOE_MODE_PREFILL", "MOE_MODE_HYBRID"}
+    for name, val in modes.items():
+        assert getattr(m, name) == int(val), name
+    d, f, k = 6144, 2048, 8
+    for T in (1, 127, 128, 256):
+        dec = m.ffn_workspace_bytes(T, k, d, f, m.MOE_MODE_DECODE)
+        pre = m.ffn_workspace_bytes(T, k, d, f, m.MOE_MODE_PREFILL)
+        hyb = m.ffn_workspace_bytes(T, k, d, f, m.MOE_MODE_HYBRID)
+        assert hyb >= dec + pre and hyb % 256 == 0
+        assert m.ffn_workspace_bytes(T, k, d, f, m.MOE_MODE_AUTO) == (dec if T < 128 else hyb)
+    assert m.ffn_workspace_bytes(4, k, d, f, 4) == 0   # not a mode
+
+
 def test_host_validation_rejects_without_launching(m):
     L = m.lib()
     P = None

@@ -186,7 +186,8 @@ def test_prefill_t4096(full):
 @pytest.mark.parametrize("T", [32, 128, 256])
 def test_automatic_mode_mid_batches(full, T):
     """The automatic mode at the batch sizes between decode and prefill, Zipf-biased: T = 32 takes the
-    decode path (8-token passes), T = 128 and 256 the prefill path with the tensor-core router."""
+    decode path (8-token passes), T = 128 and 256 the hybrid path (experts with more than 8 tokens and the
+    shared expert on the tensor cores, the rest on the decode path) with the tensor-core router."""
     L, lw, wg_d = full
     m = moe()
     x = workloads.activations(T, D, seed=T)

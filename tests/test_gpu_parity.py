@@ -186,10 +186,10 @@ def test_prefill_ffn_parity(shape):
     r = run_steps(dev, k)
     same = (r["idx"] == o_idx).all(axis=1)
     assert rel_max_err(host(out_f)[same], o_out[same]) <= TOL_PREFILL
-    # the automatic mode takes the prefill path from 128 tokens on, the decode path below
+    # the automatic mode takes the hybrid path from 128 tokens on, the decode path below
     out_a, _ = m.moe_layer_forward(dev["x"], dev["wg"], dev["bias"], dev["layer"], k)
-    want = out_f if shape.T >= 128 else m.moe_layer_forward(dev["x"], dev["wg"], dev["bias"], dev["layer"], k,
-                                                            mode=m.MOE_MODE_DECODE)[0]
+    want = m.moe_layer_forward(dev["x"], dev["wg"], dev["bias"], dev["layer"], k,
+                               mode=m.MOE_MODE_HYBRID if shape.T >= 128 else m.MOE_MODE_DECODE)[0]
     assert np.array_equal(host(out_a), host(want))
 
 
