@@ -158,7 +158,7 @@ int run_ffn_hybrid(const moe_layer_int4 *w, const float *x, const int32_t *offse
     int rc = launch_split_units(offsets, uniq, n_uniq, w->E, T * k, kHybridColdMax, h.uniq_cold, h.n_cold,
                                 h.uniq_hot, h.n_hot, err, s);
     if (rc == MOE_OK)
-        rc = launch_act_frag(x, T, w->d, h.dec.x_frag, h.dec.x_scale, h.dec.work, kDecodeCounters, s);
+        rc = launch_act_frag(x, T, w->d, h.dec.x_frag, h.dec.x_scale, h.dec.work, kDecodeCounters, s, h.n_cold);
     if (rc != MOE_OK)
         return rc;
     DecodeFfnArgs a{};

@@ -119,9 +119,10 @@ int launch_router_logits_frag(const float *x, const float *wg, int T, int d, int
 int launch_router_topk(const float *logits, const float *bias, int T, int E, int k, int normalize,
                        float route_scale, float top_p, int32_t *idx, float *w, cudaStream_t s);
 // fragments (GPC = 8) of `rows` rows of x [rows][K], K a multiple of 256; also zeroes the nzero
-// counters of the decode FFN
+// counters of the decode FFN.  With `gate` set, the fragments are skipped when *gate is 0 (a device
+// count of the experts that would read them).
 int launch_act_frag(const float *x, int rows, int K, uint8_t *frag, float *row_scale, int32_t *zero, int nzero,
-                    cudaStream_t s);
+                    cudaStream_t s, const int32_t *gate = nullptr);
 
 // union.cu (an id of -1 is an empty slot: no group, perm -1, no hit, no error)
 int launch_union(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offsets,

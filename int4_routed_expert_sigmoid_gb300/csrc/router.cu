@@ -581,7 +581,7 @@ __device__ void act_frag_row(const float *__restrict__ x, int r, int K, uint8_t 
 
 __global__ void __launch_bounds__(kFragThreads)
 act_frag_kernel(const float *__restrict__ x, int K, uint8_t *__restrict__ frag, float *__restrict__ row_scale,
-                int32_t *__restrict__ zero, int nzero)
+                int32_t *__restrict__ zero, int nzero, const int32_t *__restrict__ gate)
 {
     // launched as a programmatic dependent: resident while the previous kernel finishes, but x may
     // come from that kernel and the fragments and counters are still read by the previous FFN, so
@@ -591,6 +591,8 @@ act_frag_kernel(const float *__restrict__ x, int K, uint8_t *__restrict__ frag, 
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < nzero; i += blockDim.x)
             zero[i] = 0;
+    if (gate != nullptr && *gate == 0)
+        return;   // no expert will read the fragments (the hybrid's decode half is empty)
     act_frag_row(x, blockIdx.x, K, frag, row_scale);
 }
 
@@ -667,11 +669,11 @@ int launch_router_topk(const float *logits, const float *bias, int T, int E, int
 }
 
 int launch_act_frag(const float *x, int rows, int K, uint8_t *frag, float *row_scale, int32_t *zero, int nzero,
-                    cudaStream_t s)
+                    cudaStream_t s, const int32_t *gate)
 {
     if (rows <= 0)
         return MOE_OK;
-    return launch_pdl(act_frag_kernel, rows, kFragThreads, 0, s, x, K, frag, row_scale, zero, nzero);
+    return launch_pdl(act_frag_kernel, rows, kFragThreads, 0, s, x, K, frag, row_scale, zero, nzero, gate);
 }
 
 }  // namespace moe

@@ -22,7 +22,7 @@ def built():
     build.build()
 
 
-@pytest.mark.parametrize("mode_name", ["MOE_MODE_DECODE", "MOE_MODE_PREFILL"])
+@pytest.mark.parametrize("mode_name", ["MOE_MODE_DECODE", "MOE_MODE_PREFILL", "MOE_MODE_HYBRID"])
 @pytest.mark.parametrize("T", [1, 9])
 def test_host_entry_matches_device_entry(mode_name, T):
     m = moe()

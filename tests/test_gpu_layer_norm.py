@@ -22,7 +22,7 @@ def built():
     build.build()
 
 
-@pytest.mark.parametrize("mode_name", ["MOE_MODE_DECODE", "MOE_MODE_PREFILL"])
+@pytest.mark.parametrize("mode_name", ["MOE_MODE_DECODE", "MOE_MODE_PREFILL", "MOE_MODE_HYBRID"])
 @pytest.mark.parametrize("T,d", [(1, 1024), (5, 512), (37, 1024), (64, 768), (65, 768), (3, 8448)])
 def test_layer_norm_matches_layer_then_rms_norm(mode_name, T, d):
     m = moe()

@@ -352,10 +352,12 @@ def test_route_topp_parity(top_p):
     assert np.array_equal(gi[kept], host(i0)[kept])
 
 
-@pytest.mark.parametrize("T,mode_name", [(5, "MOE_MODE_DECODE"), (37, "MOE_MODE_DECODE"), (37, "MOE_MODE_PREFILL")])
+@pytest.mark.parametrize("T,mode_name", [(5, "MOE_MODE_DECODE"), (37, "MOE_MODE_DECODE"), (37, "MOE_MODE_PREFILL"),
+                                         (37, "MOE_MODE_HYBRID"), (130, "MOE_MODE_HYBRID")])
 def test_layer_topp_parity(T, mode_name):
     """The fused layer with top-p pruning (small-batch select+union path at T = 5, stage kernels at
-    T = 37, both FFN paths): routing, union with empty slots, hits and outputs against the oracle."""
+    T = 37, both FFN paths and the hybrid): routing, union with empty slots, hits and outputs against the
+    oracle."""
     m = moe()
     mode = getattr(m, mode_name)
     tol = TOL_DECODE if mode == m.MOE_MODE_DECODE else TOL_PREFILL
@@ -459,7 +461,7 @@ G64 = [
 
 @pytest.mark.parametrize("shape", G64, ids=lambda s: s.name)
 def test_group_size_64_parity(shape):
-    """One scale per 64 elements (the gs64 container) on both FFN paths, against the oracle on its
+    """One scale per 64 elements (the gs64 container) on both FFN paths and the hybrid, against the oracle on its
     routing; and bit for bit equal to the same layer stated with G = 32 and paired scales."""
     from moe_testlib import TOL_PREFILL
     m = moe()
@@ -476,7 +478,8 @@ def test_group_size_64_parity(shape):
     lw32 = m.LayerWeights(dev["layer"].q_base, t(s32), dev["layer"].shared_q, t(np.repeat(L.shared_s, 2)),
                           E=shape.E, d=shape.d, f=shape.f, G=32)
     assert s32.size == shape.E * n32
-    for mode, tol in ((m.MOE_MODE_DECODE, TOL_DECODE), (m.MOE_MODE_PREFILL, TOL_PREFILL)):
+    for mode, tol in ((m.MOE_MODE_DECODE, TOL_DECODE), (m.MOE_MODE_PREFILL, TOL_PREFILL),
+                      (m.MOE_MODE_HYBRID, TOL_PREFILL)):
         r = run_steps(dev, k, teacher_idx=o_idx, teacher_w=o_w, mode=mode)
         assert r["err"] == 0
         check_union_equal(r, o_union, shape.E)
