@@ -445,7 +445,8 @@ def measure_layer(copies, sh, path, steps, warmup, graph_steps, e2e_steps, rank,
         "n_uniq": n_uniq,
         "e2e": {"value": round(T * e2e_steps * world / e2e_max, 2), "unit": UNIT,
                 "h2d_bytes_per_step": T * d * 4, "d2h_bytes_per_step": T * d * 4, "steps": e2e_steps,
-                "call": "moe_layer_forward_host (page-locked host rows in and out, one call per step)"},
+                "call": "moe_layer_forward_host (page-locked host rows in and out, read and written by the "
+                        "kernels over the host link; one call per step)"},
         "gpu_launches": launches_per_step * steps,
         "clocks": clocks,
         "device_error": dev_err,

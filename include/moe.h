@@ -345,13 +345,17 @@ MOE_API int moe_layer_forward_norm(const float *x, const float *w_gate, const fl
 
 /*
  * The layer with its token rows and its result in HOST memory: x_host [T][d]
- * is copied to the device, moe_layer_forward_topp runs on the copy, and its
- * out [T][d] is copied back to out_host -- all enqueued on `stream`, one
- * cudaMemcpyAsync each way.  With page-locked host buffers the call returns
- * before the copies finish: the caller synchronises the stream before reading
- * out_host or rewriting x_host (pageable buffers make the copies synchronous).
- * The device copies of the rows sit in the workspace after the layer's
- * scratch: moe_layer_host_workspace_bytes(T, k, E, d, f, mode) bytes.
+ * is brought to the device, moe_layer_forward_topp runs on that copy, and its
+ * out [T][d] lands in out_host -- all enqueued on `stream`.  When both buffers
+ * are page-locked and mapped (cudaHostAlloc or cudaHostRegister on a system
+ * with unified addressing) and 16-byte aligned, a kernel reads x_host over the
+ * host link and the combine writes out_host directly, so the call is kernels
+ * only and overlaps the previous one in the stream; otherwise one
+ * cudaMemcpyAsync each way (pageable buffers make those synchronous).  Either
+ * way the call returns before the work finishes: the caller synchronises the
+ * stream before reading out_host or rewriting x_host.  The device copy of the
+ * rows (and, on the copy route, of the result) sits in the workspace after the
+ * layer's scratch: moe_layer_host_workspace_bytes(T, k, E, d, f, mode) bytes.
  * residual, topk_idx, topk_w, hits and err are device pointers as in
  * moe_layer_forward (residual may be NULL).
  * Errors: as moe_layer_forward; MOE_ERR_INVALID_ARG for a NULL host pointer;

@@ -221,7 +221,33 @@ rms_norm_kernel(const float4 *x, int d4, float eps, float4 *out)
     }
 }
 
+// n4 float4 from memory the GPU reaches over the host link (page-locked host rows, mapped) into device
+// memory, one per thread.  The source does not depend on earlier work in the stream and is read before
+// the grid wait, fetched again rather than from a line an earlier call left in this SM's L1 (ld.cv);
+// the destination may still be read by the previous kernel, so the stores wait for it.
+__global__ void __launch_bounds__(256)
+copy_rows_kernel(const float4 *src, float4 *__restrict__ dst, long long n4)
+{
+    griddep_launch_dependents();
+    const long long i = (long long)blockIdx.x * 256 + threadIdx.x;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < n4)
+        v = __ldcv(src + i);
+    griddep_wait();
+    if (i < n4)
+        dst[i] = v;
+}
+
 }  // namespace
+
+int launch_copy_rows(const float *src, float *dst, long long n, cudaStream_t s)
+{
+    const long long n4 = n / 4;
+    if (n4 <= 0)
+        return MOE_OK;
+    return launch_pdl(copy_rows_kernel, (int)((n4 + 255) / 256), 256, 0, s, reinterpret_cast<const float4 *>(src),
+                      reinterpret_cast<float4 *>(dst), n4);
+}
 
 int launch_combine_norm(const float *y_pair, const uint16_t *y_pair16, const float *y_shared, const float *w,
                         const int32_t *perm, const float *res, int T, int k, int d, float *out, float *out_normed,

@@ -539,6 +539,26 @@ int moe_layer_forward_norm(const float *x, const float *w_gate, const float *bia
                          eps, topk_idx, topk_w, hits, workspace, ws_bytes, err, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The device address of a host buffer that kernels can read and write directly (page-locked and
+// mapped: cudaHostAlloc, cudaHostRegister, on a system with unified addressing), else null.
+void *mapped_host(const void *p)
+{
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();   // a pointer the runtime does not know: not an error of the call
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
 size_t moe_layer_host_workspace_bytes(int T, int k, int E, int d, int f, int mode)
 {
     const size_t layer = moe_layer_workspace_bytes(T, k, E, d, f, mode);
@@ -566,6 +586,18 @@ int moe_layer_forward_host(const float *x_host, const float *w_gate, const float
     float *x_dev = reinterpret_cast<float *>(base + align_up(layer));
     float *out_dev = reinterpret_cast<float *>(base + align_up(layer) + align_up(rows));
     const cudaStream_t s = as_stream(stream);
+    // Page-locked, mapped host buffers (the GPU addresses them over the host link): a kernel pulls the
+    // rows and the combine writes the result straight into out_host, so the call is kernels only and
+    // each launch still overlaps the end of the previous one.  Other host memory: one copy each way.
+    const float *x_map = static_cast<const float *>(mapped_host(x_host));
+    float *out_map = static_cast<float *>(mapped_host(out_host));
+    if (x_map != nullptr && out_map != nullptr && aligned16(x_map) && aligned16(out_map)) {
+        int rc = launch_copy_rows(x_map, x_dev, (long long)T * w->d, s);
+        if (rc == MOE_OK)
+            rc = moe_layer_forward_topp(x_dev, w_gate, bias, w, residual, T, k, normalize, route_scale, top_p, mode,
+                                        out_map, topk_idx, topk_w, hits, workspace, layer, err, stream);
+        return rc;
+    }
     if (cudaMemcpyAsync(x_dev, x_host, rows, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     const int rc = moe_layer_forward_topp(x_dev, w_gate, bias, w, residual, T, k, normalize, route_scale, top_p,

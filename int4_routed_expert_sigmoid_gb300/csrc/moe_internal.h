@@ -186,6 +186,9 @@ int launch_combine(const float *y_pair, const float *y_shared, const float *w, c
 int launch_combine_bf16(const uint16_t *y_pair, const float *y_shared, const float *w, const int32_t *perm,
                         const float *res, int T, int k, int d, float *out, cudaStream_t s, int32_t *err = nullptr);
 int launch_rms_norm(const float *x, int T, int d, float eps, float *out, cudaStream_t s);
+// n floats (a multiple of 4, 16-byte aligned) from host rows the GPU addresses directly into device
+// memory, as a programmatic dependent launch (the host-buffer entry point's input)
+int launch_copy_rows(const float *src, float *dst, long long n, cudaStream_t s);
 // the combine (fp32 y_pair, or bf16 y_pair16 when set) and RMSNorm(out) into out_normed, as the two
 // separate kernels would compute them
 int launch_combine_norm(const float *y_pair, const uint16_t *y_pair16, const float *y_shared, const float *w,

@@ -45,6 +45,30 @@ def test_host_entry_matches_device_entry(mode_name, T):
     assert np.array_equal(host(hits_h), host(hits_d))
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_entry_pageable_and_pinned_buffers(pinned):
+    """Page-locked buffers take the direct route (a kernel reads the rows, the combine writes the
+    result into host memory), pageable ones the copy route; both give the device entry's bits, and
+    a direct-route call that follows another in the stream sees its own rows."""
+    m = moe()
+    sh = Shape("host_entry_route", E=16, k=4, d=512, f=256, T=5, bias="normal")
+    L = workloads.layer_inputs(sh, seed=8, threads=4)
+    dev = device_layer(L)
+    ws = m.workspace(m.layer_host_workspace_bytes(sh.T, sh.k, sh.E, sh.d, sh.f), "cuda")
+    outs, refs = [], []
+    for call in range(3):   # back to back on one stream, one synchronisation at the end
+        x = torch.from_numpy(workloads.activations(sh.T, sh.d, seed=60 + call))
+        out_host = torch.empty((sh.T, sh.d), dtype=torch.float32)
+        if pinned:
+            x, out_host = x.pin_memory(), out_host.pin_memory()
+        m.moe_layer_forward_host(x, dev["wg"], dev["bias"], dev["layer"], sh.k, out_host=out_host, ws=ws)
+        outs.append(out_host)
+        refs.append(m.moe_layer_forward(x.cuda(), dev["wg"], dev["bias"], dev["layer"], sh.k)[0])
+    torch.cuda.synchronize()
+    for call in range(3):
+        assert np.array_equal(outs[call].numpy(), host(refs[call])), f"call {call}"
+
+
 def test_host_entry_workspace_and_pointers():
     m = moe()
     sh = Shape("host_entry_ws", E=8, k=2, d=256, f=128, T=3, bias="normal")
