@@ -873,14 +873,17 @@ def ncu_traffic(root, key):
         return None
 
 
+# the sources the captured FFN kernels (and their tensor maps) are built from
+FFN_SOURCES = ("ffn_decode.cu", "ffn_prefill.cu", "moe_internal.h", "ptx.cuh", "tmap.cu")
+
+
 def kernel_source_hash(root):
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(root, "int4_routed_expert_sigmoid_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
-        if n.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, n), "rb") as fh:
-                h.update(n.encode() + fh.read())
+    for n in FFN_SOURCES:
+        with open(os.path.join(csrc, n), "rb") as fh:
+            h.update(n.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
