@@ -17,12 +17,13 @@ Shape = workloads.Shape
 COLD_MAX = 8   # pairs of an expert up to which the hybrid takes the decode path
 
 # mixed (Zipf: a few hot experts), T >= 128 (AUTO resolves to the hybrid), all cold (m <= T <= 8),
-# all hot (two experts, ~20 tokens each), f = 384 (an f that is not a multiple of 256)
+# all hot (two experts, ~20 tokens each), f = 384 (an f that is not a multiple of 256), one token
 SHAPES = [
     Shape("hyb_mixed", E=16, k=4, d=512, f=256, T=24, bias="zipf"),
     Shape("hyb_t130", E=32, k=4, d=512, f=384, T=130, bias="zipf"),
     Shape("hyb_cold", E=64, k=2, d=256, f=128, T=8, bias="normal"),
     Shape("hyb_hot", E=2, k=1, d=256, f=128, T=40, bias="zero"),
+    Shape("hyb_t1", E=16, k=4, d=512, f=256, T=1, bias="normal"),   # the decode half's one-token, fixed-order form
 ]
 
 
