@@ -143,4 +143,10 @@ def test_tier_prefetch_all_takes_the_device_only_path():
     assert after["calls"] - before["calls"] == 8
     assert after["hits"] == before["hits"] and after["misses"] == before["misses"]
     assert after["bytes_copied"] == before["bytes_copied"]
+    # the tier has no hybrid path: the mode is refused before anything is enqueued
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_layer_forward_tier(x, dev["wg"], dev["bias"], tier, dev["layer"].shared_q, dev["layer"].shared_s,
+                                 sh.k, mode=m.MOE_MODE_HYBRID, copy_stream=copy)
+    assert ei.value.status == m.MOE_ERR_INVALID_ARG
+    assert tier.stats()["calls"] == after["calls"]
     tier.close()
