@@ -99,6 +99,11 @@ def test_bench_arguments_and_bytes():
     assert bench.parse_args(["--mode", "prefill"]).mode == "prefill"
     with pytest.raises(SystemExit):
         bench.parse_args(["--workload", "nope"])
+    # the FFN path of a single-layer workload: its own unless forced
+    for wl, own in (("decode", "decode"), ("batched_decode", "decode"), ("prefill", "prefill")):
+        assert bench.path_for(bench.parse_args([]), wl) == own
+        for forced in ("decode", "prefill", "hybrid"):
+            assert bench.path_for(bench.parse_args(["--mode", forced]), wl) == forced
     sh = workloads.WORKLOADS["decode"]
     b = bench.layer_bytes(sh, n_uniq=8)
     assert b["expert_block"] == 23_592_960
@@ -118,3 +123,14 @@ def test_kernel_source_hash_and_traffic_record():
         got = bench.ncu_traffic(ROOT, key)
         assert got == (rec[key]["dram_bytes_per_launch"] if rec[key]["source_hash"] == h else None)
     assert bench.ncu_traffic(ROOT, "no_such_workload") is None
+    # keyed to the FFN kernels' own sources: every listed file exists, and a change to one of them
+    # (simulated on a copy of the tree) changes the hash
+    import shutil
+    import tempfile
+    with tempfile.TemporaryDirectory() as tmp:
+        csrc = os.path.join(tmp, "int4_routed_expert_sigmoid_gb300", "csrc")
+        shutil.copytree(os.path.join(ROOT, "int4_routed_expert_sigmoid_gb300", "csrc"), csrc)
+        assert bench.kernel_source_hash(tmp) == h
+        with open(os.path.join(csrc, bench.FFN_SOURCES[0]), "a") as fh:
+            fh.write("\n")
+        assert bench.kernel_source_hash(tmp) != h
