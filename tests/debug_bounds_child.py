@@ -22,14 +22,15 @@ from moe_testlib import device_layer  # noqa: E402
 Shape = workloads.Shape
 SHAPES = [Shape("dbg_t1", E=16, k=4, d=1024, f=256, T=1, bias="normal"),
           Shape("dbg_t5", E=64, k=8, d=512, f=512, T=5, bias="zipf"),
-          Shape("dbg_t37", E=16, k=4, d=1024, f=384, T=37, bias="normal")]
+          Shape("dbg_t37", E=16, k=4, d=1024, f=384, T=37, bias="normal"),
+          Shape("dbg_t130", E=32, k=4, d=512, f=256, T=130, bias="zipf")]
 out = {}
 for sh in SHAPES:
     L = workloads.layer_inputs(sh, seed=5, threads=4)
     dev = device_layer(L)
     x = torch.from_numpy(workloads.activations(sh.T, sh.d, seed=6)).cuda()
     res = torch.from_numpy(workloads.activations(sh.T, sh.d, seed=7)).cuda()
-    for mode_name in ("MOE_MODE_DECODE", "MOE_MODE_PREFILL"):
+    for mode_name in ("MOE_MODE_DECODE", "MOE_MODE_PREFILL", "MOE_MODE_HYBRID"):
         hits = torch.zeros(sh.E, dtype=torch.int64, device="cuda")
         y, err = moe.moe_layer_forward(x, dev["wg"], dev["bias"], dev["layer"], sh.k, mode=getattr(moe, mode_name),
                                        residual=res, hits=hits)
@@ -37,4 +38,10 @@ for sh in SHAPES:
         out[f"{sh.name}_{mode_name}_y"] = y.cpu().numpy()
         out[f"{sh.name}_{mode_name}_err"] = err.cpu().numpy()
         out[f"{sh.name}_{mode_name}_hits"] = hits.cpu().numpy()
+    # the host-buffer entry on page-locked rows (the copy kernel, the combine writing into host memory)
+    y_h, err_h = moe.moe_layer_forward_host(x.cpu().pin_memory(), dev["wg"], dev["bias"], dev["layer"], sh.k,
+                                            residual=res)
+    torch.cuda.synchronize()
+    out[f"{sh.name}_host_y"] = y_h.numpy()
+    out[f"{sh.name}_host_err"] = err_h.cpu().numpy()
 np.savez(sys.argv[2], **out)

@@ -1,6 +1,7 @@
 """The bounds-checked build (MOE_DEBUG_BOUNDS) on valid inputs: no index is
-flagged and every output is bit-identical to the normal build's, on both FFN
-paths.  Each library runs in its own child process (tests/debug_bounds_child.py)."""
+flagged and every output is bit-identical to the normal build's, on every FFN path
+and through the host-buffer entry.  Each library runs in its own child process
+(tests/debug_bounds_child.py)."""
 import os
 import subprocess
 import sys
@@ -32,7 +33,7 @@ def _run(lib, path):
 def test_debug_bounds_build_matches_and_flags_nothing(libs, tmp_path):
     normal = _run(libs[0], str(tmp_path / "normal.npz"))
     checked = _run(libs[1], str(tmp_path / "checked.npz"))
-    assert sorted(normal.files) == sorted(checked.files) and len(normal.files) == 18
+    assert sorted(normal.files) == sorted(checked.files) and len(normal.files) == 4 * (3 * 3 + 2)
     for key in normal.files:
         if key.endswith("_err"):
             assert int(checked[key][0]) == 0 and int(normal[key][0]) == 0, key
