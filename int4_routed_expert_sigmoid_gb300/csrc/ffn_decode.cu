@@ -95,6 +95,7 @@ struct Cfg {
 struct Maps {
     CUtensorMap q[2], s[2];
     int merged;
+    int cps;   // k-chunks one merged box spans: the kernel's stage layout must hold exactly that many
 };
 
 struct Params {
@@ -747,6 +748,10 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
 template <int MODE, int TOK, int CPS, int GPC, int GS>
 int launch_one(const Maps &maps, const Params &prm, int max_items, int max_units, cudaStream_t s)
 {
+    // a merged box spans maps.cps chunks and lands in one stage: a kernel laid out for another count
+    // would take more bytes into a stage than it holds
+    if (maps.merged && maps.cps != CPS)
+        return MOE_ERR_INVALID_ARG;
     using C = Cfg<MODE, TOK, CPS, GPC, GS>;
     auto kern = ffn_decode_kernel<MODE, TOK, CPS, GPC, GS>;
     const size_t smem = C::kSmem + ((size_t)max_units * sizeof(Unit) + 15) / 16 * 16;
@@ -832,6 +837,8 @@ int launch_ffn_decode(const DecodeFfnArgs &a, cudaStream_t s)
         return MOE_ERR_UNSUPPORTED;   // a scale box row must be a multiple of 16 bytes
     Maps gu{}, dn{};
     gu.merged = dn.merged = 1;
+    gu.cps = cps_gu;
+    dn.cps = cps_dn;
     for (int i = 0; i < 2 && rc == MOE_OK; i++) {
         // gate/up: (bytes of a chunk, row, matrix, chunk, expert)
         const uint64_t gq_dim[5] = {128, (uint64_t)f, 2, (uint64_t)d / 256, outer[i]};
