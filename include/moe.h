@@ -240,7 +240,9 @@ MOE_API int moe_hits(const int32_t *counts, int E, uint64_t *hits, void *stream)
  *   y_shared [T][d] fp32: FFN_shared(x_t)
  * mode: MOE_MODE_*.  workspace: at least moe_ffn_workspace_bytes(T, k, d, f,
  * mode) bytes of device memory, 256-byte aligned; its contents on entry do not
- * matter.  Calls that share a workspace must not overlap in time.
+ * matter.  Calls that share a workspace must not overlap in time.  The union
+ * arrays must be moe_union's: *n_uniq is only clamped to min(E, T*k) (the
+ * kernels' unit tables hold no more), not otherwise checked.
  */
 MOE_API int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *offsets,
                         const int32_t *sorted_pair, const int32_t *uniq,
