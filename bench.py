@@ -58,13 +58,15 @@ def parse_args(argv=None):
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the tokens per step (small-footprint profiling runs); 0 = workload's")
     ap.add_argument("--mode", choices=["workload", "decode", "prefill", "hybrid"], default="workload",
-                    help="FFN path: the workload's own (prefill for prefill, decode otherwise) or forced")
+                    help="FFN path: the workload's own (prefill for prefill, the library's automatic choice "
+                         "for the stack, decode otherwise) or forced")
     ap.add_argument("--graph-steps", type=int, default=100, help="steps captured per CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
-                    help="decode line only (by default it also carries the batched-decode, prefill and stack "
-                         "workloads under \"workloads\")")
+                    help="decode line only (by default it also carries the batched-decode layer on the decode "
+                         "and on the hybrid path, the prefill layer, the stack and the expert tier under "
+                         "\"workloads\")")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU-baseline sample")
     return ap.parse_args(argv)
 
