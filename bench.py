@@ -549,8 +549,9 @@ EXTRA_STEPS = {"prefill": 40, "batched_decode": 200}
 
 def run_ours(args, rank, world, local):
     """The single-layer workloads.  The default (decode T = 1) line also carries, under "workloads",
-    the prefill T = 4096 and batched-decode T = 64 layers on the same weights and the 8-layer stack
-    sweep, each with its own steps, roofline, stage times, union size and clocks."""
+    the batched-decode T = 64 layer (on the decode path and on the opt-in hybrid path) and the prefill
+    T = 4096 layer on the same weights, the 8-layer stack sweep and the expert tier, each with its own
+    steps, roofline, stage times, union size and clocks."""
     import torch
     dev = init_device(local, world)
     sh = workload_shape(args, args.workload)
