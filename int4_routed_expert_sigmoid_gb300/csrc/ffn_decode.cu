@@ -172,14 +172,14 @@ __device__ __forceinline__ void load_units(const Params &p, int units, Unit *tab
         } else {
             const int e = __ldcg(p.uniq + u - p.with_shared);
             t.expert = e;
-            if (MOE_IN_BOUNDS(e >= 0 && e < p.n_experts, p.err)) {
+            // checked in every build: the union arrays may come from the caller (the FFN call)
+            if (checked(e >= 0 && e < p.n_experts, p.err, MOE_DEVERR_BAD_EXPERT)) {
                 t.pos0 = __ldcg(p.offsets + e);
                 t.m = __ldcg(p.offsets + e + 1) - t.pos0;
                 t.zq = p.slot_of ? __ldcg(p.slot_of + e) : e;
                 // a unit outside the pairs or the weight view gets no tokens (its items do nothing)
-                if (!MOE_IN_BOUNDS(t.pos0 >= 0 && t.m >= 0 && t.pos0 + t.m <= p.T * p.k && t.zq >= 0 &&
-                                       t.zq < p.n_view,
-                                   p.err))
+                if (!checked(t.pos0 >= 0 && t.m >= 0 && t.pos0 + t.m <= p.T * p.k && t.zq >= 0 && t.zq < p.n_view,
+                             p.err, MOE_DEVERR_BAD_EXPERT))
                     t.m = 0;
             } else {
                 t.expert = 0;
@@ -560,16 +560,20 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
                 it0.m = p.T;
                 it0.pos0 = 0;
             }
-            int t0, ntok;
-            pass_range(it0.m, (it0.m + TOK - 1) / TOK, 0, t0, ntok);
-            pre = nstages < C::kStages ? nstages : C::kStages;
-            if (lane == 0) {
-                const uint64_t pol = weight_policy<TOK>(it0.m);
-                for (int c = 0; c < pre; c++) {
-                    const uint32_t fb = smem_addr(&full_bar[c]);
-                    stage_item[c] = blockIdx.x;
-                    mbar_arrive_expect_tx(fb, C::kWeightBytes + ntok * C::kTokBytes);
-                    issue_weights<MODE, TOK, CPS, GPC, GS>(maps, it0, c, stage0 + c * C::kStageBytes, fb, pol);
+            // an item without tokens (a unit the table check emptied) has no pass: nothing to pre-issue,
+            // and the main loop below skips it the same way
+            if (it0.m > 0) {
+                int t0, ntok;
+                pass_range(it0.m, (it0.m + TOK - 1) / TOK, 0, t0, ntok);
+                pre = nstages < C::kStages ? nstages : C::kStages;
+                if (lane == 0) {
+                    const uint64_t pol = weight_policy<TOK>(it0.m);
+                    for (int c = 0; c < pre; c++) {
+                        const uint32_t fb = smem_addr(&full_bar[c]);
+                        stage_item[c] = blockIdx.x;
+                        mbar_arrive_expect_tx(fb, C::kWeightBytes + ntok * C::kTokBytes);
+                        issue_weights<MODE, TOK, CPS, GPC, GS>(maps, it0, c, stage0 + c * C::kStageBytes, fb, pol);
+                    }
                 }
             }
         }
