@@ -84,9 +84,7 @@ enum {
 };
 
 /* Bits of the device error word `err`. */
-#define MOE_DEVERR_BAD_EXPERT 0x1   /* an expert id in topk_idx was outside [0, E), or union arrays passed
-                                       to the FFN call named an expert or a pair range outside the layer
-                                       (that expert is skipped) */
+#define MOE_DEVERR_BAD_EXPERT 0x1   /* an expert id in topk_idx was outside [0, E) */
 #define MOE_DEVERR_TIMEOUT 0x2      /* a bounded pipeline wait gave up; outputs are incomplete */
 #define MOE_DEVERR_SCALE_RANGE 0x4  /* prefill path: a group scale lies more than 2^13 above or 2^14
                                        below the first group scale of its weight row, beyond what
@@ -243,10 +241,9 @@ MOE_API int moe_hits(const int32_t *counts, int E, uint64_t *hits, void *stream)
  * mode: MOE_MODE_*.  workspace: at least moe_ffn_workspace_bytes(T, k, d, f,
  * mode) bytes of device memory, 256-byte aligned; its contents on entry do not
  * matter.  Calls that share a workspace must not overlap in time.  The union
- * arrays should be moe_union's: *n_uniq is clamped to min(E, T*k) (the
- * kernels' unit tables hold no more), and an expert id or pair range of the
- * list outside the layer sets MOE_DEVERR_BAD_EXPERT and is skipped; the
- * sorted_pair entries themselves are trusted.
+ * arrays must be moe_union's: *n_uniq is clamped to min(E, T*k) (the kernels'
+ * unit tables hold no more), the rest is trusted (a MOE_DEBUG_BOUNDS build
+ * checks every index and skips what is out of range).
  */
 MOE_API int moe_expert_ffn_int4(const float *x, const moe_layer_int4 *w, const int32_t *offsets,
                         const int32_t *sorted_pair, const int32_t *uniq,

@@ -172,14 +172,14 @@ __device__ __forceinline__ void load_units(const Params &p, int units, Unit *tab
         } else {
             const int e = __ldcg(p.uniq + u - p.with_shared);
             t.expert = e;
-            // checked in every build: the union arrays may come from the caller (the FFN call)
-            if (checked(e >= 0 && e < p.n_experts, p.err, MOE_DEVERR_BAD_EXPERT)) {
+            if (MOE_IN_BOUNDS(e >= 0 && e < p.n_experts, p.err)) {
                 t.pos0 = __ldcg(p.offsets + e);
                 t.m = __ldcg(p.offsets + e + 1) - t.pos0;
                 t.zq = p.slot_of ? __ldcg(p.slot_of + e) : e;
                 // a unit outside the pairs or the weight view gets no tokens (its items do nothing)
-                if (!checked(t.pos0 >= 0 && t.m >= 0 && t.pos0 + t.m <= p.T * p.k && t.zq >= 0 && t.zq < p.n_view,
-                             p.err, MOE_DEVERR_BAD_EXPERT))
+                if (!MOE_IN_BOUNDS(t.pos0 >= 0 && t.m >= 0 && t.pos0 + t.m <= p.T * p.k && t.zq >= 0 &&
+                                       t.zq < p.n_view,
+                                   p.err))
                     t.m = 0;
             } else {
                 t.expert = 0;
@@ -560,8 +560,8 @@ ffn_decode_kernel(const __grid_constant__ Maps maps, const Params p)
                 it0.m = p.T;
                 it0.pos0 = 0;
             }
-            // an item without tokens (a unit the table check emptied) has no pass: nothing to pre-issue,
-            // and the main loop below skips it the same way
+            // an item without tokens (a unit the bounds checks of a MOE_DEBUG_BOUNDS build emptied) has
+            // no pass: nothing to pre-issue, and the main loop below skips it the same way
             if (it0.m > 0) {
                 int t0, ntok;
                 pass_range(it0.m, (it0.m + TOK - 1) / TOK, 0, t0, ntok);

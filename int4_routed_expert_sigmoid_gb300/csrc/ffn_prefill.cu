@@ -179,15 +179,14 @@ __device__ void build_units(const PParams &p, int units, PUnit *tab)
             } else {
                 const int e = p.uniq[u - p.with_shared];
                 t.expert = e;
-                // checked in every build: the union arrays may come from the caller (the FFN call)
-                if (checked(e >= 0 && e < p.n_experts, p.err, MOE_DEVERR_BAD_EXPERT)) {
+                if (MOE_IN_BOUNDS(e >= 0 && e < p.n_experts, p.err)) {
                     t.row0 = p.offsets[e];
                     t.m = p.offsets[e + 1] - t.row0;
                     t.zq = p.slot_of ? p.slot_of[e] : e;
                     // a unit outside the pairs or the weight view gets no tokens
-                    if (!checked(t.row0 >= 0 && t.m >= 0 && t.row0 + t.m <= p.T * p.k && t.zq >= 0 &&
-                                     t.zq < p.n_view,
-                                 p.err, MOE_DEVERR_BAD_EXPERT))
+                    if (!MOE_IN_BOUNDS(t.row0 >= 0 && t.m >= 0 && t.row0 + t.m <= p.T * p.k && t.zq >= 0 &&
+                                           t.zq < p.n_view,
+                                       p.err))
                         t.m = 0;
                 } else {
                     t.expert = 0;

@@ -32,17 +32,6 @@ __device__ __forceinline__ bool in_bounds_check(bool ok, int32_t *err)
 #define MOE_IN_BOUNDS(ok, err) true
 #endif
 
-#ifdef __CUDACC__
-// A check kept in every build, for once-per-unit-of-work indices (an expert id, a pair range): false when
-// !ok, with `bit` OR-ed into the error word, so the caller skips the unit instead of reading out of range.
-__device__ __forceinline__ bool checked(bool ok, int32_t *err, int32_t bit)
-{
-    if (!ok && err != nullptr)
-        atomicOr(err, bit);
-    return ok;
-}
-#endif
-
 // Host-side NVTX range over one entry point's launches (a profiler's timeline shows where each
 // stage's kernels were enqueued); compiled out with MOE_NO_NVTX.  Costs a few nanoseconds when
 // no tool is attached.

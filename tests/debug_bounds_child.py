@@ -25,6 +25,31 @@ SHAPES = [Shape("dbg_t1", E=16, k=4, d=1024, f=256, T=1, bias="normal"),
           Shape("dbg_t37", E=16, k=4, d=1024, f=384, T=37, bias="normal"),
           Shape("dbg_t130", E=32, k=4, d=512, f=256, T=130, bias="zipf")]
 out = {}
+if len(sys.argv) > 3 and sys.argv[3] == "bad":
+    # union arrays naming an expert outside the layer, handed to the FFN call: only ever run with the
+    # bounds-checked library, whose checks turn the bad entry into an error bit and skip it
+    for T in (4, 130):
+        sh = Shape(f"dbg_bad_t{T}", E=8, k=2, d=256, f=128, T=T, bias="normal")
+        L = workloads.layer_inputs(sh, seed=4, threads=2)
+        dev = device_layer(L)
+        idx, _, _ = moe.moe_route(dev["x"], dev["wg"], dev["bias"], sh.k)
+        un = moe.moe_union(idx, sh.E)
+        bad = dict(un)
+        bad["uniq"] = un["uniq"].clone()
+        bad["uniq"][0] = sh.E + 3
+        torch.cuda.synchronize()
+        out[f"{sh.name}_n_uniq"] = un["n_uniq"].cpu().numpy()
+        out[f"{sh.name}_uniq"] = un["uniq"].cpu().numpy()
+        out[f"{sh.name}_offsets"] = un["offsets"].cpu().numpy()
+        for mode_name in ("MOE_MODE_DECODE", "MOE_MODE_PREFILL", "MOE_MODE_HYBRID"):
+            for tag, u in (("ok", un), ("bad", bad)):
+                y, ys, err = moe.moe_expert_ffn_int4(dev["x"], dev["layer"], u, sh.k, getattr(moe, mode_name))
+                torch.cuda.synchronize()
+                out[f"{sh.name}_{mode_name}_{tag}_y"] = y.cpu().numpy()
+                out[f"{sh.name}_{mode_name}_{tag}_ys"] = ys.cpu().numpy()
+                out[f"{sh.name}_{mode_name}_{tag}_err"] = err.cpu().numpy()
+    np.savez(sys.argv[2], **out)
+    sys.exit(0)
 for sh in SHAPES:
     L = workloads.layer_inputs(sh, seed=5, threads=4)
     dev = device_layer(L)

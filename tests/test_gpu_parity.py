@@ -110,36 +110,6 @@ def test_union_flags_bad_expert_ids():
     assert host(un["counts"]).tolist() == [2, 0, 0, 3, 0, 0, 0, 1]
 
 
-@pytest.mark.parametrize("T", [4, 130])
-def test_ffn_skips_and_flags_a_bad_expert_in_the_union(T):
-    """Union arrays handed to the FFN call that name an expert outside the layer: every path (decode,
-    prefill, hybrid) flags MOE_DEVERR_BAD_EXPERT, skips that entry (the kernels check the unit table in
-    every build) and gives the other experts' rows bit for bit as with the intact list."""
-    m = moe()
-    sh = Shape("bad_uniq", E=8, k=2, d=256, f=128, T=T, bias="normal")
-    L = workloads.layer_inputs(sh, seed=4, threads=2)
-    dev = device_layer(L)
-    idx, _, _ = m.moe_route(dev["x"], dev["wg"], dev["bias"], sh.k)
-    un = m.moe_union(idx, sh.E)
-    torch.cuda.synchronize()
-    n = int(host(un["n_uniq"])[0])
-    assert n >= 2
-    uniq, off = host(un["uniq"])[:n], host(un["offsets"])
-    bad = dict(un)
-    bad["uniq"] = un["uniq"].clone()
-    bad["uniq"][0] = sh.E + 3
-    for mode in (m.MOE_MODE_DECODE, m.MOE_MODE_PREFILL, m.MOE_MODE_HYBRID):
-        y_ok, s_ok, e_ok = m.moe_expert_ffn_int4(dev["x"], dev["layer"], un, sh.k, mode)
-        y_bad, s_bad, e_bad = m.moe_expert_ffn_int4(dev["x"], dev["layer"], bad, sh.k, mode)
-        torch.cuda.synchronize()
-        assert int(host(e_ok)[0]) == 0, mode
-        assert int(host(e_bad)[0]) & m.MOE_DEVERR_BAD_EXPERT, mode
-        yo, yb = host(y_ok), host(y_bad)
-        for e in uniq[1:]:
-            assert np.array_equal(yb[off[e]:off[e + 1]], yo[off[e]:off[e + 1]]), (mode, e)
-        assert np.array_equal(host(s_bad), host(s_ok)), mode
-
-
 def test_hits_accumulate_across_calls():
     m = moe()
     rng = np.random.default_rng(0)
