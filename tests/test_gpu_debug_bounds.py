@@ -1,7 +1,8 @@
-"""The bounds-checked build (MOE_DEBUG_BOUNDS) on valid inputs: no index is
+"""The bounds-checked build (MOE_DEBUG_BOUNDS).  On valid inputs no index is
 flagged and every output is bit-identical to the normal build's, on every FFN path
-and through the host-buffer entry.  Each library runs in its own child process
-(tests/debug_bounds_child.py)."""
+and through the host-buffer entry; given a union list with an expert id outside
+the layer, it flags and skips that entry and leaves the other experts' rows as
+they were.  Each library runs in its own child process (tests/debug_bounds_child.py)."""
 import os
 import subprocess
 import sys
