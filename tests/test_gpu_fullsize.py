@@ -205,7 +205,13 @@ def test_stack_8_layers(full):
     sample of outputs.  T = 4 and 16 also run end to end (the oracle carries its
     own x_l through all 8 layers); there the error of earlier layers is carried
     forward by the residual, so layer l is held to (l + 1) times the tolerance,
-    and a layer whose routing diverged on a flagged near-tie is reported."""
+    and a layer whose routing diverged on a flagged near-tie is reported.
+
+    The same layers also run in the benchmark's own launch configuration: the
+    automatic mode (decode path at T = 1 and 64, hybrid at T = 256) with every
+    layer but the last forming the next layer's normalised input in its combine
+    (moe_layer_forward_norm), checked teacher-forced on a sample of tokens, the
+    fused normalised rows against the oracle's RMSNorm of the layer's output."""
     del full   # layer 0 is regenerated with the stack's per-layer seeds
     m = moe()
     sh = workloads.WORKLOADS["stack"]
@@ -215,6 +221,9 @@ def test_stack_8_layers(full):
     x_gpu = {T: workloads.activations(T, D, seed=0) for T in Ts}
     x_orc = {T: x_gpu[T].copy() for T in Ts if T <= 16}
     diverged = set()
+    T_timed = (1, 64, 256)
+    xt = {T: t(workloads.activations(T, D, seed=7 + T)) for T in T_timed}
+    xnt = {T: m.moe_rms_norm(xt[T], eps) for T in T_timed}
     for layer in range(sh.layers):
         L = workloads.layer_inputs(sh, seed=0, layer=layer, T=1, threads=16)
         lw = m.LayerWeights(t(L.q_base.reshape(-1)), t(L.s_base.reshape(-1)), t(L.shared_q), t(L.shared_s),
@@ -250,5 +259,33 @@ def test_stack_8_layers(full):
                     assert e2e <= (layer + 1) * TOL_DECODE, f"layer {layer} T={T} end to end: {e2e:.3e}"
                 x_orc[T] = e_out.astype(np.float32)
             x_gpu[T] = r["out"]
+        last = layer == sh.layers - 1
+        for T in T_timed:
+            idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+            w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+            hits = torch.zeros(E, dtype=torch.int64, device="cuda")
+            kw = dict(mode=m.MOE_MODE_AUTO, residual=xt[T], topk_idx=idx, topk_w=w, hits=hits)
+            if last:
+                out, err = m.moe_layer_forward(xnt[T], wg_d, t(bias), lw, K, 1, 1.0, **kw)
+            else:
+                out, xn_next, err = m.moe_layer_forward_norm(xnt[T], wg_d, t(bias), lw, K, eps=eps, **kw)
+            torch.cuda.synchronize()
+            assert int(host(err)[0]) == 0, f"layer {layer} T={T} (automatic, as timed)"
+            xn_h, x_h, out_h, idx_h = host(xnt[T]), host(xt[T]), host(out), host(idx)
+            assert np.array_equal(host(hits), oracle.union(idx_h, E)["counts"].astype(np.int64))
+            o_idx, o_w, _, keys = oracle.route(xn_h, L.wg, bias, K)
+            same, _ = compare_routing(idx_h, host(w), o_idx, o_w, keys, K)
+            toks = _sample(T, 3, seed=100 + layer, must=(T - 1,))
+            toks = toks[same[toks]]
+            if toks.size:
+                _, _, o_out = _oracle(L, xn_h, bias, res=x_h).tokens(toks)
+                tol = TOL_PREFILL if T >= 128 else TOL_DECODE
+                err_t = rel_max_err(out_h[toks], o_out)
+                print(f"[stack as timed] layer {layer} T={T}: {err_t:.2e} on {toks.size} tokens")
+                assert err_t <= tol, f"layer {layer} T={T} (automatic, as timed): {err_t:.3e}"
+            if not last:
+                assert rel_max_err(host(xn_next), oracle.rms_norm(out_h, eps)) <= TOL_NORM, f"layer {layer} T={T}"
+                xnt[T] = xn_next
+            xt[T] = out
         del lw, L
         torch.cuda.empty_cache()
