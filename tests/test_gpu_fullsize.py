@@ -150,6 +150,37 @@ def test_batched_decode_t64_zipf(full):
     assert np.array_equal(s["out"], r["out"])
 
 
+def test_batched_decode_t64_zipf_hybrid(full):
+    """The batched-decode layer on the opt-in hybrid path (experts with at most 8 of the batch's tokens on
+    the decode GEMV, the others and the shared expert on the tensor-core GEMM)."""
+    L, lw, wg_d = full
+    m = moe()
+    x = workloads.activations(64, D, seed=0)
+    bias = workloads.selection_bias(E, "zipf", seed=0)
+    _check_layer(L, lw, wg_d, x, bias, m.MOE_MODE_HYBRID, TOL_PREFILL, 12)
+
+
+@pytest.mark.parametrize("T,bias_kind,mode_name", [(1, "normal", "MOE_MODE_DECODE"), (64, "zipf", "MOE_MODE_DECODE"),
+                                                   (64, "zipf", "MOE_MODE_HYBRID"), (4096, None, "MOE_MODE_PREFILL")])
+def test_host_entry_full(full, T, bias_kind, mode_name):
+    """The end-to-end call at the full layer shape (moe_layer_forward_host on page-locked token rows and
+    result, calls back to back on one workspace): bitwise the device entry's output on the same rows."""
+    L, lw, wg_d = full
+    m = moe()
+    mode = getattr(m, mode_name)
+    bias = None if bias_kind is None else torch.from_numpy(workloads.selection_bias(E, bias_kind, seed=0)).cuda()
+    ws = m.workspace(m.layer_host_workspace_bytes(T, K, E, D, F, mode), "cuda")
+    xs = [torch.from_numpy(workloads.activations(T, D, seed=90 + i)).pin_memory() for i in range(2)]
+    outs = [torch.empty((T, D), dtype=torch.float32).pin_memory() for _ in range(2)]
+    errs = [m.moe_layer_forward_host(xs[i], wg_d, bias, lw, K, mode=mode, out_host=outs[i], ws=ws)[1]
+            for i in range(2)]
+    refs = [m.moe_layer_forward(xs[i].cuda(), wg_d, bias, lw, K, mode=mode) for i in range(2)]
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert int(host(errs[i])[0]) == 0 and int(host(refs[i][1])[0]) == 0
+        assert np.array_equal(outs[i].numpy(), host(refs[i][0])), f"call {i}"
+
+
 def test_prefill_t4096(full):
     """T = 4096, no bias (about 128 tokens per expert): the tcgen05 grouped-GEMM path."""
     L, lw, wg_d = full
