@@ -181,6 +181,41 @@ def test_host_entry_full(full, T, bias_kind, mode_name):
         assert np.array_equal(outs[i].numpy(), host(refs[i][0])), f"call {i}"
 
 
+@pytest.mark.parametrize("n_slots", [32, 256])
+def test_tier_full(full, n_slots):
+    """The expert tier at the full layer shape, as the benchmark times it (decode T = 1, N(0, 0.1) bias):
+    32 slots (12.5 % resident, missing experts copied in on the copy stream) and 256 (every expert
+    prefetched: the device-only path) give, call after call, the bits of the layer with every expert
+    resident."""
+    L, lw, wg_d = full
+    m = moe()
+    hq = torch.from_numpy(np.ascontiguousarray(L.q_base.reshape(-1))).pin_memory()
+    hs = torch.from_numpy(np.ascontiguousarray(L.s_base.reshape(-1))).pin_memory()
+    tier = m.ExpertTier(hq, hs, E=E, d=D, f=F, n_slots=n_slots, G=G)
+    copy = torch.cuda.Stream()
+    if n_slots == E:
+        tier.prefetch(np.arange(E), copy_stream=copy)
+    bias = torch.from_numpy(workloads.selection_bias(E, "normal", seed=0)).cuda()
+    st0 = tier.stats()
+    for call in range(6):
+        x = torch.from_numpy(workloads.activations(1, D, seed=200 + call)).cuda()
+        out_t, err_t = m.moe_layer_forward_tier(x, wg_d, bias, tier, lw.shared_q, lw.shared_s, K,
+                                                mode=m.MOE_MODE_DECODE, copy_stream=copy)
+        out_r, err_r = m.moe_layer_forward(x, wg_d, bias, lw, K, mode=m.MOE_MODE_DECODE)
+        torch.cuda.synchronize()
+        assert int(host(err_t)[0]) == 0 and int(host(err_r)[0]) == 0
+        assert np.array_equal(host(out_t), host(out_r)), f"call {call}"
+    st1 = tier.stats()
+    assert st1["calls"] - st0["calls"] == 6
+    if n_slots < E:   # host-planned: every call looks up its 8 experts, some of them missing
+        assert st1["hits"] + st1["misses"] - st0["hits"] - st0["misses"] == 6 * K
+        assert st1["misses"] > st0["misses"]
+    else:             # every expert has a slot: no lookups, nothing copied
+        assert st1["misses"] == st0["misses"] and st1["bytes_copied"] == st0["bytes_copied"]
+    tier.close()
+    del hq, hs
+
+
 def test_prefill_t4096(full):
     """T = 4096, no bias (about 128 tokens per expert): the tcgen05 grouped-GEMM path."""
     L, lw, wg_d = full
