@@ -216,6 +216,48 @@ def test_tier_full(full, n_slots):
     del hq, hs
 
 
+@pytest.mark.parametrize("T,bias_kind,mode_name", [(1, "normal", "MOE_MODE_DECODE"), (64, "zipf", "MOE_MODE_DECODE"),
+                                                   (256, "zipf", "MOE_MODE_AUTO"), (4096, None, "MOE_MODE_PREFILL")])
+def test_graph_replay_matches_eager(full, T, bias_kind, mode_name):
+    """The form the layer is timed in: several layer calls back to back on one workspace, captured in one
+    CUDA graph (the programmatic-dependent launches become graph edges) and replayed twice, every call's
+    output bitwise the eager call's on the same rows."""
+    L, lw, wg_d = full
+    m = moe()
+    mode = getattr(m, mode_name)
+    bias = None if bias_kind is None else torch.from_numpy(workloads.selection_bias(E, bias_kind, seed=0)).cuda()
+    S = 3
+    xs = [torch.from_numpy(workloads.activations(T, D, seed=300 + i)).cuda() for i in range(S)]
+    outs = [torch.empty((T, D), dtype=torch.float32, device="cuda") for _ in range(S)]
+    ws = m.workspace(m.layer_workspace_bytes(T, K, E, D, F, mode), "cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def calls():
+        for i in range(S):
+            m.moe_layer_forward(xs[i], wg_d, bias, lw, K, 1, 1.0, mode=mode, out=outs[i], ws=ws, err=err)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        calls()   # every path once outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        calls()
+    refs = [m.moe_layer_forward(xs[i], wg_d, bias, lw, K, 1, 1.0, mode=mode) for i in range(S)]
+    torch.cuda.synchronize()
+    for rep in range(2):
+        for o in outs:
+            o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(host(err)[0]) == 0
+        for i in range(S):
+            assert int(host(refs[i][1])[0]) == 0
+            assert np.array_equal(host(outs[i]), host(refs[i][0])), f"replay {rep}, call {i}"
+
+
 def test_prefill_t4096(full):
     """T = 4096, no bias (about 128 tokens per expert): the tcgen05 grouped-GEMM path."""
     L, lw, wg_d = full
