@@ -258,6 +258,36 @@ def test_graph_replay_matches_eager(full, T, bias_kind, mode_name):
             assert np.array_equal(host(outs[i]), host(refs[i][0])), f"replay {rep}, call {i}"
 
 
+@pytest.mark.parametrize("mode_name", ["MOE_MODE_PREFILL", "MOE_MODE_AUTO"])
+def test_large_batch_64bit_offsets(full, mode_name):
+    """T = 45,056 tokens (k = 8: 360,448 pairs): the pair rows' element offsets (pair * d) pass 2^31 from pair
+    349,526 on, so the last experts' routed outputs and every shared-expert token row sit beyond 32-bit
+    indexing.  Sampled tokens, among them the owners of the last pair rows, against the oracle; the hit
+    counters against the union of the GPU's routing."""
+    L, lw, wg_d = full
+    m = moe()
+    T = 45056
+    x = workloads.activations(T, D, seed=11)
+    r = _fused(lw, wg_d, x, None, getattr(m, mode_name))
+    assert r["err"] == 0
+    u = oracle.union(r["idx"], E)
+    assert np.array_equal(r["hits"], u["counts"].astype(np.int64))
+    P = T * K
+    first_high = -(-(1 << 31) // D)   # the first pair row whose element offset passes 2^31
+    assert u["offsets"][E] == P and P > first_high
+    must = (0, T - 1, u["sorted_pair"][P - 1] // K, u["sorted_pair"][first_high] // K,
+            u["sorted_pair"][(first_high + P) // 2] // K)
+    toks = _sample(T, 3, seed=T, must=must)
+    o_idx, o_w, _, keys = oracle.route(x[toks], L.wg, None, K)
+    same, _ = compare_routing(r["idx"][toks], r["w"][toks], o_idx, o_w, keys, K)
+    toks = toks[same]
+    assert toks.size >= 4
+    _, _, o_out = _oracle(L, x, None).tokens(toks)
+    err = rel_max_err(r["out"][toks], o_out)
+    print(f"[T={T} mode={mode_name}] n_uniq={int(u['n_uniq'])} checked {toks.size} tokens, rel_err={err:.3e}")
+    assert err <= TOL_PREFILL
+
+
 def test_prefill_t4096(full):
     """T = 4096, no bias (about 128 tokens per expert): the tcgen05 grouped-GEMM path."""
     L, lw, wg_d = full
