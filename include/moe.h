@@ -55,7 +55,9 @@
  * Supported shapes: G = 32 or 64 (the colibri README, "2. Get the model":
  * group-scaled int4 containers, gs64 among them); d a multiple of 256; f a
  * multiple of 128 (of 256 when G = 64); 1 <= k <= min(E, 32); 1 <= E <= 1024;
- * 1 <= T.  Other shapes return MOE_ERR_UNSUPPORTED.
+ * 1 <= T.  A G, d or f outside these returns MOE_ERR_UNSUPPORTED; a T, k or E
+ * outside them (an empty batch, T = 0, included) MOE_ERR_INVALID_ARG, before
+ * anything is launched.
  */
 #ifndef MOE_H
 #define MOE_H

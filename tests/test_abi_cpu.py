@@ -113,3 +113,28 @@ def test_debug_bounds_build_exports_every_header_symbol(m):
     L = ctypes.CDLL(path)
     missing = [n for n in m.header_functions() if not hasattr(L, n)]
     assert not missing, missing
+
+
+def test_empty_batch_is_refused_before_launching(m):
+    """T = 0 (an empty batch) is an argument error on every entry point, found before anything is
+    launched (there is no GPU here: a launch would come back as MOE_ERR_CUDA), and the workspace size
+    queries give 0 for it."""
+    L = m.lib()
+    ok = ctypes.c_void_p(0x10000)   # aligned and never dereferenced: the batch size is refused first
+    lay = ctypes.byref(m._binding.moe_layer_int4(0x10000, 0x10000, 0x10000, 0x10000, 16, 256, 128, 32))
+    big = 1 << 40
+    inv = m.MOE_ERR_INVALID_ARG
+    assert L.moe_route(ok, ok, None, 0, 256, 16, 2, 1, 1.0, ok, ok, ok, None) == inv
+    assert L.moe_route_topp(ok, ok, None, 0, 256, 16, 2, 1, 1.0, 0.7, ok, ok, ok, None) == inv
+    assert L.moe_union(ok, 0, 2, 16, ok, ok, ok, ok, ok, ok, None, ok, None) == inv
+    for mode in (0, 1, 2, 3):
+        assert L.moe_expert_ffn_int4(ok, lay, ok, ok, ok, ok, 0, 2, mode, ok, ok, ok, big, ok, None) == inv
+        assert L.moe_layer_forward(ok, ok, None, lay, None, 0, 2, 1, 1.0, mode, ok, None, None, None, ok, big, ok,
+                                   None) == inv
+        assert L.moe_layer_forward_topp(ok, ok, None, lay, None, 0, 2, 1, 1.0, 0.7, mode, ok, None, None, None, ok,
+                                        big, ok, None) == inv
+        assert L.moe_layer_forward_norm(ok, ok, None, lay, None, 0, 2, 1, 1.0, 1.0, mode, ok, ok, 1e-5, None, None,
+                                        None, ok, big, ok, None) == inv
+        assert m.layer_workspace_bytes(0, 2, 16, 256, 128, mode) == 0
+        assert m.ffn_workspace_bytes(0, 2, 256, 128, mode) == 0
+    assert L.moe_combine(ok, ok, ok, ok, None, 0, 2, 256, ok, None) == inv
