@@ -22,6 +22,8 @@ SMALL = [
     Shape("k1", E=4, k=1, d=256, f=128, T=9, bias="normal"),
     Shape("split4_t1", E=16, k=4, d=2048, f=256, T=1, bias="normal"),      # gate/up reduction in 4 parts
     Shape("split2_t1", E=12, k=2, d=1024, f=128, T=1, bias="normal"),      # ... in 2 parts
+    Shape("k_eq_E", E=8, k=8, d=256, f=128, T=20, bias="normal"),         # every token takes every expert
+    Shape("one_expert", E=1, k=1, d=256, f=128, T=7),                      # a single routed expert
 ]
 
 
@@ -154,6 +156,8 @@ PREFILL_SHAPES = [
     Shape("prefill_ragged", E=16, k=4, d=1024, f=384, T=37, bias="normal"),  # 3 and 8 m-tiles
     Shape("prefill_two_ntiles", E=8, k=2, d=256, f=128, T=300),              # shared expert: 256 + 44 tokens
     Shape("prefill_one_token", E=16, k=4, d=1024, f=384, T=1, bias="normal"),  # every unit a single token
+    Shape("prefill_k_eq_E", E=8, k=8, d=256, f=128, T=130, bias="normal"),     # every expert takes every token
+    Shape("prefill_one_expert", E=1, k=1, d=256, f=128, T=130),                # a single routed expert
 ]
 
 
