@@ -273,9 +273,9 @@ def test_union_paths_bit_exact(T, k, E, dups):
 
 
 # ------------------------------------------------------------ wide routing ----
-# Selection widths and expert counts the ABI accepts beyond the GLM-5.2 shape: k up to 32
+# Selection widths and expert counts the ABI accepts beyond the GLM-5.2 shape, up to both maxima: k up to 32
 # (every candidate slot of a 32-expert block is used), E up to 1024 (32 blocks of 32).
-WIDE = [(64, 16), (256, 16), (64, 32), (256, 32), (512, 8), (1024, 8)]
+WIDE = [(64, 16), (256, 16), (64, 32), (256, 32), (512, 8), (1024, 8), (1024, 32)]
 
 
 @pytest.mark.parametrize("E,k", WIDE, ids=lambda v: str(v))
